@@ -1,0 +1,182 @@
+/*
+ * pkv.h -- C ABI of libpkv.so, the GB300 (sm_103a) paged KV cache hot path.
+ *
+ * The library implements the two device operations that a paged-KV decode
+ * step needs, plus the slot computation that feeds the first one:
+ *
+ *   pkv_decode_slot_mapping  slot_mapping of the token each sequence appends
+ *   pkv_kv_store             store_kvcache: scatter new K/V rows into the cache
+ *   pkv_paged_decode         q_len = 1 GQA PagedAttention over the block tables
+ *
+ * Conventions shared by every entry point
+ *   - All array pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates no memory, keeps no per-call state and never synchronises the
+ *     stream.  Work is enqueued asynchronously on `stream` (NULL = the legacy
+ *     default stream); the return code covers only host-side argument checks
+ *     and the launch itself.
+ *   - bf16 arrays hold IEEE bfloat16 values (uint16 bit patterns); index arrays
+ *     are int32.  Every multi-dimensional array is dense, row-major
+ *     (C-contiguous) with the shape given below, and must start on a 16-byte
+ *     boundary.
+ *   - Problems that only the device can see (a slot or block id outside the
+ *     cache, a context length outside its table) never trap: the kernel skips
+ *     the offending access and ORs a PKV_ERR_* bit into *err_word (a device
+ *     int32, may be NULL).  Read it after synchronising; clear it yourself.
+ *     Output values are unspecified for a call that set a bit.
+ *   - Out-of-place only: outputs may not alias inputs.
+ *   - Entry points may be called from several host threads on different
+ *     streams; calls are independent.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (struct CUstream_st *). */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_EINVAL = -1,       /* bad pointer, size, shape or alignment            */
+    PKV_EUNSUPPORTED = -2, /* valid request outside the compiled variants      */
+    PKV_ECUDA = -3,        /* a CUDA runtime/driver call or launch failed      */
+    PKV_EWORKSPACE = -4,   /* workspace missing or smaller than required       */
+    PKV_EBOUNDS = -5       /* reserved for host-visible range errors           */
+} pkv_status;
+
+/* Bits ORed into *err_word by the kernels. */
+#define PKV_ERR_SLOT_RANGE 0x1    /* slot_mapping entry not -1 and outside [0, num_blocks*block_size) */
+#define PKV_ERR_BLOCK_RANGE 0x2   /* block table entry that must be read lies outside [0, num_blocks) */
+#define PKV_ERR_CONTEXT_RANGE 0x4 /* context_len < 0 or above min(max_context_len, max_blocks*block_size) */
+#define PKV_ERR_WAIT_TIMEOUT 0x8  /* a bounded wait on an asynchronous copy gave up                    */
+
+/* Version of this ABI (bumped on any incompatible change). */
+int pkv_abi_version(void);
+
+/* Static text for a pkv_status value (never NULL). */
+const char *pkv_status_string(int status);
+
+/*
+ * pkv_decode_slot_mapping -- the cache slot of the token each sequence
+ * appends in this decode step.
+ *
+ * Defined by the nano-vLLM lab manual (§5.2.3 and appendix B.2.3) and the
+ * nano-vllm KV-cache post (§3.1, §3.5, §4.4): the physical row of logical
+ * position pos is block_tables[b][pos / block_size] * block_size +
+ * pos % block_size; in a decode step the appended token sits at
+ * pos = context_lens[b] - 1 because context_lens already count it
+ * (lab manual §5.2.1; post §4.4: context_lens [431, 434] give slots
+ * [430, 689] with block_size 256).
+ *
+ *   block_tables  [num_seqs, max_blocks_per_seq] int32, unused entries -1
+ *   context_lens  [num_seqs] int32
+ *   slot_mapping  [num_tokens] int32 output; num_tokens >= num_seqs.
+ *                 Row t < num_seqs gets the slot of sequence t (or -1 when
+ *                 context_lens[t] == 0); rows t >= num_seqs are padding and
+ *                 get -1 (lab manual appendix B.4: padding rows must not
+ *                 write the cache).
+ *   num_blocks    physical blocks in the cache (for the range check)
+ * A context length that does not fit its table row, or a table entry outside
+ * [0, num_blocks), yields -1 for that row and sets the matching err bit.
+ */
+pkv_status pkv_decode_slot_mapping(const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *context_lens, int32_t num_seqs,
+                                   int32_t block_size, int32_t num_blocks,
+                                   int32_t *slot_mapping, int32_t num_tokens,
+                                   int32_t *err_word, pkv_stream_t stream);
+
+/*
+ * pkv_kv_store -- store_kvcache: write each new token's K and V rows into
+ * the paged cache through slot_mapping.
+ *
+ * Defined by the MinivLLM review (section "注意力内核的三个分支": the store
+ * kernel writes k[t], v[t] into the cache row slot_mapping[t] of a cache laid
+ * out [num_blocks, block_size, num_kv_heads, head_dim], and returns at once
+ * for slot -1) and the nano-vllm KV-cache post (§3.1: the per-layer k_cache /
+ * v_cache views of the single preallocated pool).
+ *
+ *   k, v          [num_tokens, num_kv_heads, head_dim] bf16
+ *   slot_mapping  [num_tokens] int32; -1 = padding row, nothing written
+ *   k_cache,
+ *   v_cache       [num_blocks, block_size, num_kv_heads, head_dim] bf16
+ * The result is a bit copy.  Two rows with the same slot (other than -1) in
+ * one call are not allowed; which one lands is unspecified.
+ * A slot outside [-1, num_blocks*block_size) is skipped and sets
+ * PKV_ERR_SLOT_RANGE.  head_dim * num_kv_heads * 2 bytes must be a multiple
+ * of 16.  num_tokens == 0 is a no-op.
+ */
+pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, const int32_t *slot_mapping,
+                        int32_t num_tokens, uint16_t *k_cache, uint16_t *v_cache,
+                        int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t *err_word, pkv_stream_t stream);
+
+/*
+ * Bytes of device workspace that pkv_paged_decode needs for these sizes
+ * (split-K partial states plus a small header).  Depends only on the
+ * arguments; 0 means the sizes are invalid.  The workspace needs no
+ * initialisation and holds nothing between calls; calls that may run at the
+ * same time need separate workspaces.
+ */
+size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim);
+
+/* Upper limits of pkv_paged_decode. */
+#define PKV_MAX_SEQS 16384
+#define PKV_MAX_WORKERS 4096
+
+/*
+ * pkv_paged_decode -- decode-phase PagedAttention (one query token per
+ * sequence, grouped-query attention).
+ *
+ * Defined by the mini-vLLM README (§5 "Triton PagedAttention Decode Kernel":
+ * the kernel walks each sequence's physical blocks through its block table,
+ * kv_head = q_head / (num_q_heads / num_kv_heads), bf16 storage with fp32
+ * accumulation, online softmax with running max m, sum l and weighted sum
+ * acc) and the MinivLLM review (section "注意力内核的三个分支": the block
+ * table is looked up per token, block_tables[b, t / block_size], slot
+ * t % block_size).  For sequence b, query head h and L = context_lens[b]:
+ *     out[b, h] = sum_{j<L} softmax_j(scale * q[b, h] . K_j) * V_j
+ * where K_j, V_j are row j % block_size of physical block
+ * block_tables[b][j / block_size], kv head h / (num_q_heads / num_kv_heads).
+ * L == 0 gives out[b, h] = 0.  scale is the final multiplier (pass
+ * 1/sqrt(head_dim) for standard attention).
+ *
+ *   q             [num_seqs, num_q_heads, head_dim] bf16
+ *   k_cache,
+ *   v_cache       [num_blocks, block_size, num_kv_heads, head_dim] bf16
+ *   block_tables  [num_seqs, max_blocks_per_seq] int32 (-1 padded; only the
+ *                 first ceil(L / block_size) entries of a row are read)
+ *   context_lens  [num_seqs] int32
+ *   max_context_len  host-side upper bound of context_lens (no device->host
+ *                 read is made); lengths above it are a device error
+ *   out           [num_seqs, num_q_heads, head_dim] bf16, rounded to nearest
+ *   workspace     device buffer of at least
+ *                 pkv_paged_decode_workspace_size(...) bytes, 16-byte aligned
+ *   num_workers   0 = one worker per resident warp of the device (the
+ *                 default); otherwise the number of warps the tokens are
+ *                 split over, 1..PKV_MAX_WORKERS (testing and tuning).
+ * Supported: head_dim in {64, 128}; num_q_heads / num_kv_heads in 1..8;
+ * block_size a power of two in [8, 1024]; num_seqs <= PKV_MAX_SEQS;
+ * num_blocks * block_size < 2^31.
+ * Work is split evenly over the workers by 16-token tiles, so one sequence
+ * may be spread over several workers; their partial softmax states are
+ * merged by a second kernel (split-K / flash-decoding).
+ */
+pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                            const int32_t *block_tables, int32_t max_blocks_per_seq,
+                            const int32_t *context_lens, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+                            float scale, uint16_t *out, void *workspace, size_t workspace_bytes,
+                            int32_t num_workers, int32_t *err_word, pkv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

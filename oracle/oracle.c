@@ -1,0 +1,310 @@
+/*
+ * Oracle for the paged KV cache hot path -- TEST INFRASTRUCTURE ONLY.
+ *
+ * This file is a plain, slow, obviously correct CPU restatement of what the
+ * paged KV cache computes, in fp64.  It exists to check the CUDA library
+ * against.  Only the test suite, the package smoke check and the CPU-baseline
+ * leg of the benchmark may load it; the library itself never does, and it
+ * shares no code, header or table with the CUDA sources.
+ *
+ * Sources (all restated, nothing copied):
+ *  [P1] nano-vLLM inference lab manual ("5. 动手改造：从跑通到可测量的推理服务"),
+ *       §5.2.1 (context_lens include the position about to be written),
+ *       §5.2.3 and appendix B.2.3 (slot = block_table[pos // B] * B + pos % B),
+ *       appendix B.1.2 (softmax attention worked example),
+ *       appendix B.4 (padding rows carry slot -1 and context_len 0 and must
+ *       not write the real cache).
+ *  [P2] "mini-vLLM v0.4 -- From-Scratch LLM Inference Serving Runtime",
+ *       §5 "Triton PagedAttention Decode Kernel" (q_len = 1 decode, GQA map
+ *       kv_head = q_head // (Hq / Hkv), fp16/bf16 storage, fp32 accumulation,
+ *       online softmax state m / l / acc).
+ *  [P3] "MinivLLM：六步搭出一个 Qwen3 推理引擎", section "注意力内核的三个分支"
+ *       (store_kvcache: cache layout [num_blocks, block_size, Hkv, D],
+ *       slot -1 skips the row; decode kernel looks up block_tables[b, t // bs]
+ *       for every token t, slot t % bs).
+ *  [P4] "大模型推理引擎学习入门-2：带你理解 nano-vllm 的 KV Cache 以及 Paged
+ *       Attention", §3.1 (slot = block_table[i] * block_size + offset, per-layer
+ *       k_cache/v_cache views), §3.5 (slot_mapping), §4.4 (decode example:
+ *       context_lens [431, 434] -> slot_mapping [430, 689]).
+ *
+ * Numbers: K/V/q are bf16 bit patterns (uint16), widened exactly to double.
+ * Every sum, exp and division is done in double.  The attention uses the
+ * plain two-pass softmax (max, then exponentials, then one division); the
+ * partial-state functions at the end restate the split-and-merge identity
+ * that the online softmax of [P2] §5 relies on.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL (-1)
+#define ORACLE_EBOUNDS (-5)
+
+/* bf16 -> double: a bf16 value is the top 16 bits of an IEEE binary32. */
+static double bf16_bits_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int oracle_version(void) { return 1; }
+
+/* ---------------------------------------------------------------------------
+ * Slot of logical position `pos` of the sequence whose block table is `row`
+ * ([P1] §5.2.3 / B.2.3; [P4] §3.1): the logical block is pos // block_size,
+ * the offset inside it is pos % block_size, and the physical row number is
+ * physical_block * block_size + offset.
+ * Returns -1 through *slot_out when the logical block lies beyond the table.
+ * ------------------------------------------------------------------------- */
+int oracle_slot_of(const int32_t *row, int32_t max_blocks, int32_t block_size,
+                   int64_t pos, int64_t *slot_out)
+{
+    if (!row || !slot_out || block_size <= 0 || pos < 0) return ORACLE_EINVAL;
+    int64_t logical_block = pos / block_size;
+    int64_t offset = pos % block_size;
+    if (logical_block >= max_blocks) { *slot_out = -1; return ORACLE_EBOUNDS; }
+    *slot_out = (int64_t)row[logical_block] * block_size + offset;
+    return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * Decode-step slot_mapping ([P1] §5.2.1, [P4] §4.4, [P1] B.4): one new token
+ * per sequence; sequence t's context_len already counts that token, so its
+ * position is context_lens[t] - 1.  Rows t >= num_seqs (padding up to
+ * num_tokens) and rows with context_len 0 get -1.
+ * ------------------------------------------------------------------------- */
+int oracle_decode_slot_mapping(const int32_t *block_tables, int32_t max_blocks,
+                               const int32_t *context_lens, int32_t num_seqs,
+                               int32_t block_size, int32_t num_tokens,
+                               int32_t *slot_mapping)
+{
+    if (!block_tables || !context_lens || !slot_mapping) return ORACLE_EINVAL;
+    if (num_seqs < 0 || num_tokens < 0 || max_blocks <= 0 || block_size <= 0)
+        return ORACLE_EINVAL;
+    int rc = ORACLE_OK;
+    for (int32_t t = 0; t < num_tokens; ++t) {
+        slot_mapping[t] = -1;
+        if (t >= num_seqs) continue;
+        int32_t len = context_lens[t];
+        if (len <= 0) continue;
+        int64_t slot;
+        if (oracle_slot_of(block_tables + (int64_t)t * max_blocks, max_blocks,
+                           block_size, (int64_t)len - 1, &slot) != ORACLE_OK) {
+            rc = ORACLE_EBOUNDS;
+            continue;
+        }
+        slot_mapping[t] = (int32_t)slot;
+    }
+    return rc;
+}
+
+/* ---------------------------------------------------------------------------
+ * store_kvcache ([P3] "注意力内核的三个分支", [P4] §3.1): for every token t
+ * whose slot s is not -1, row s of the cache (all Hkv heads x D values) becomes
+ * a bit copy of k[t] (and likewise v[t]).  Nothing else changes.
+ * row_elems = Hkv * D; num_slots = num_blocks * block_size.
+ * ------------------------------------------------------------------------- */
+int oracle_kv_store(const uint16_t *k, const uint16_t *v, const int32_t *slot_mapping,
+                    int32_t num_tokens, uint16_t *k_cache, uint16_t *v_cache,
+                    int64_t num_slots, int32_t row_elems)
+{
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return ORACLE_EINVAL;
+    if (num_tokens < 0 || num_slots < 0 || row_elems <= 0) return ORACLE_EINVAL;
+    int rc = ORACLE_OK;
+    for (int32_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s == -1) continue;
+        if (s < 0 || s >= num_slots) { rc = ORACLE_EBOUNDS; continue; }
+        memcpy(k_cache + s * row_elems, k + (int64_t)t * row_elems, sizeof(uint16_t) * (size_t)row_elems);
+        memcpy(v_cache + s * row_elems, v + (int64_t)t * row_elems, sizeof(uint16_t) * (size_t)row_elems);
+    }
+    return rc;
+}
+
+/* ---------------------------------------------------------------------------
+ * Paged decode attention ([P2] §5, [P3] "注意力内核的三个分支", [P1] B.1.2).
+ * For sequence b with L = context_lens[b] and query head h:
+ *   g     = h / (Hq / Hkv)                                  (GQA map)
+ *   K_j   = k_cache[block_tables[b][j / bs]][j % bs][g][:]   for j < L
+ *   s_j   = scale * sum_d q[b][h][d] * K_j[d]
+ *   w_j   = exp(s_j - max_j s_j)
+ *   out   = sum_j w_j V_j / sum_j w_j ;  L == 0 gives out = 0.
+ * Layouts: q [B, Hq, D]; caches [num_blocks, bs, Hkv, D]; block_tables
+ * [B, max_blocks]; out [B, Hq, D] (double).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    const uint16_t *q, *k_cache, *v_cache;
+    const int32_t *block_tables, *context_lens;
+    int32_t num_seqs, hq, hkv, d, block_size, num_blocks, max_blocks;
+    double scale;
+    double *out;
+    int32_t nthreads, tid;
+    int status;
+} decode_job;
+
+/* One (sequence, query head) item.  Returns 0 or ORACLE_EBOUNDS. */
+static int decode_one(const decode_job *J, int32_t b, int32_t h, double *scores)
+{
+    const int32_t d_all = J->d;
+    const int32_t group = J->hq / J->hkv;
+    const int32_t g = h / group;
+    const int32_t len = J->context_lens[b];
+    double *o = J->out + ((int64_t)b * J->hq + h) * d_all;
+    for (int32_t d = 0; d < d_all; ++d) o[d] = 0.0;
+    if (len == 0) return ORACLE_OK;
+    if (len < 0 || (int64_t)len > (int64_t)J->max_blocks * J->block_size) return ORACLE_EBOUNDS;
+
+    const uint16_t *qv = J->q + ((int64_t)b * J->hq + h) * d_all;
+    const int32_t *row = J->block_tables + (int64_t)b * J->max_blocks;
+
+    /* pass 1: scores and their maximum */
+    double m = -INFINITY;
+    for (int32_t j = 0; j < len; ++j) {
+        int32_t phys = row[j / J->block_size];
+        if (phys < 0 || phys >= J->num_blocks) return ORACLE_EBOUNDS;
+        int64_t base = (((int64_t)phys * J->block_size + j % J->block_size) * J->hkv + g) * d_all;
+        double dot = 0.0;
+        for (int32_t d = 0; d < d_all; ++d)
+            dot += bf16_bits_to_double(qv[d]) * bf16_bits_to_double(J->k_cache[base + d]);
+        scores[j] = J->scale * dot;
+        if (scores[j] > m) m = scores[j];
+    }
+    /* pass 2: weights, their sum and the weighted sum of V rows */
+    double denom = 0.0;
+    for (int32_t j = 0; j < len; ++j) {
+        int32_t phys = row[j / J->block_size];
+        int64_t base = (((int64_t)phys * J->block_size + j % J->block_size) * J->hkv + g) * d_all;
+        double w = exp(scores[j] - m);
+        denom += w;
+        for (int32_t d = 0; d < d_all; ++d)
+            o[d] += w * bf16_bits_to_double(J->v_cache[base + d]);
+    }
+    for (int32_t d = 0; d < d_all; ++d) o[d] /= denom;
+    return ORACLE_OK;
+}
+
+static void *decode_worker(void *arg)
+{
+    decode_job *J = (decode_job *)arg;
+    int32_t max_len = J->max_blocks * J->block_size;
+    double *scores = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+    if (!scores) { J->status = ORACLE_EINVAL; return NULL; }
+    int64_t items = (int64_t)J->num_seqs * J->hq;
+    for (int64_t it = J->tid; it < items; it += J->nthreads) {
+        int rc = decode_one(J, (int32_t)(it / J->hq), (int32_t)(it % J->hq), scores);
+        if (rc != ORACLE_OK) J->status = rc;
+    }
+    free(scores);
+    return NULL;
+}
+
+int oracle_paged_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                        const int32_t *block_tables, int32_t max_blocks,
+                        const int32_t *context_lens, int32_t num_seqs, int32_t hq,
+                        int32_t hkv, int32_t d, int32_t block_size, int32_t num_blocks,
+                        double scale, double *out, int32_t nthreads)
+{
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return ORACLE_EINVAL;
+    if (num_seqs < 0 || hq <= 0 || hkv <= 0 || d <= 0 || block_size <= 0 || max_blocks <= 0)
+        return ORACLE_EINVAL;
+    if (hq % hkv != 0) return ORACLE_EINVAL; /* [P2] §5: the group size must divide */
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+
+    decode_job jobs[256];
+    pthread_t threads[256];
+    for (int32_t t = 0; t < nthreads; ++t) {
+        decode_job J = {q, k_cache, v_cache, block_tables, context_lens,
+                        num_seqs, hq, hkv, d, block_size, num_blocks, max_blocks,
+                        scale, out, nthreads, t, ORACLE_OK};
+        jobs[t] = J;
+    }
+    if (nthreads == 1) {
+        decode_worker(&jobs[0]);
+    } else {
+        for (int32_t t = 0; t < nthreads; ++t) pthread_create(&threads[t], NULL, decode_worker, &jobs[t]);
+        for (int32_t t = 0; t < nthreads; ++t) pthread_join(threads[t], NULL);
+    }
+    int rc = ORACLE_OK;
+    for (int32_t t = 0; t < nthreads; ++t)
+        if (jobs[t].status != ORACLE_OK) rc = jobs[t].status;
+    return rc;
+}
+
+/* ---------------------------------------------------------------------------
+ * Split-K partial state and merge (the online-softmax state of [P2] §5,
+ * applied to disjoint token ranges).  For the tokens j in [j0, j1) of
+ * (b, h):
+ *   m   = max s_j,   l = sum exp(s_j - m),   acc = sum exp(s_j - m) V_j.
+ * An empty range gives m = -inf, l = 0, acc = 0.
+ * Merging n states: M = max m_i; l = sum exp(m_i - M) l_i;
+ * out = sum exp(m_i - M) acc_i / l  (states with m_i = -inf contribute 0;
+ * if every state is empty, out = 0).
+ * ------------------------------------------------------------------------- */
+int oracle_partial_state(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                         const int32_t *block_tables, int32_t max_blocks, int32_t b,
+                         int32_t h, int32_t hq, int32_t hkv, int32_t d, int32_t block_size,
+                         int32_t num_blocks, double scale, int32_t j0, int32_t j1,
+                         double *m_out, double *l_out, double *acc_out)
+{
+    if (!q || !k_cache || !v_cache || !block_tables || !m_out || !l_out || !acc_out) return ORACLE_EINVAL;
+    if (hq % hkv != 0 || j0 < 0 || j1 < j0) return ORACLE_EINVAL;
+    const int32_t g = h / (hq / hkv);
+    const uint16_t *qv = q + ((int64_t)b * hq + h) * d;
+    const int32_t *row = block_tables + (int64_t)b * max_blocks;
+    for (int32_t e = 0; e < d; ++e) acc_out[e] = 0.0;
+    *m_out = -INFINITY;
+    *l_out = 0.0;
+    if (j1 == j0) return ORACLE_OK;
+    if ((int64_t)j1 > (int64_t)max_blocks * block_size) return ORACLE_EBOUNDS;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(j1 - j0));
+    if (!s) return ORACLE_EINVAL;
+    double m = -INFINITY;
+    for (int32_t j = j0; j < j1; ++j) {
+        int32_t phys = row[j / block_size];
+        if (phys < 0 || phys >= num_blocks) { free(s); return ORACLE_EBOUNDS; }
+        int64_t base = (((int64_t)phys * block_size + j % block_size) * hkv + g) * d;
+        double dot = 0.0;
+        for (int32_t e = 0; e < d; ++e)
+            dot += bf16_bits_to_double(qv[e]) * bf16_bits_to_double(k_cache[base + e]);
+        s[j - j0] = scale * dot;
+        if (s[j - j0] > m) m = s[j - j0];
+    }
+    double l = 0.0;
+    for (int32_t j = j0; j < j1; ++j) {
+        int32_t phys = row[j / block_size];
+        int64_t base = (((int64_t)phys * block_size + j % block_size) * hkv + g) * d;
+        double w = exp(s[j - j0] - m);
+        l += w;
+        for (int32_t e = 0; e < d; ++e) acc_out[e] += w * bf16_bits_to_double(v_cache[base + e]);
+    }
+    free(s);
+    *m_out = m;
+    *l_out = l;
+    return ORACLE_OK;
+}
+
+int oracle_merge_states(const double *m, const double *l, const double *acc, int32_t n,
+                        int32_t d, double *out)
+{
+    if (!m || !l || !acc || !out || n < 0 || d <= 0) return ORACLE_EINVAL;
+    double big = -INFINITY;
+    for (int32_t i = 0; i < n; ++i)
+        if (m[i] > big) big = m[i];
+    for (int32_t e = 0; e < d; ++e) out[e] = 0.0;
+    if (big == -INFINITY) return ORACLE_OK;
+    double denom = 0.0;
+    for (int32_t i = 0; i < n; ++i) {
+        if (m[i] == -INFINITY) continue;
+        double f = exp(m[i] - big);
+        denom += f * l[i];
+        for (int32_t e = 0; e < d; ++e) out[e] += f * acc[(int64_t)i * d + e];
+    }
+    for (int32_t e = 0; e < d; ++e) out[e] /= denom;
+    return ORACLE_OK;
+}
