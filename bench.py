@@ -1,0 +1,443 @@
+"""Benchmark of the paged KV cache decode step on GB300.
+
+A step is one pass of the whole hot path over one batch: the decode-step slot
+mapping, kv_store of the appended tokens, and paged_decode -- per layer for
+multi-layer workloads.  Default workload: the Qwen3-0.6B-shaped layer (batch
+64, 16 q / 8 kv heads, head_dim 128, block_size 256, context_lens U[512,4096]).
+
+Prints ONE JSON line (rank 0).  `value` is the achieved HBM bandwidth of the
+step in GB/s (algorithmic bytes / step time, whole job); the line also carries
+seq-steps/s, the roofline of the dominant kernel (paged_decode) and the CPU
+oracle baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference] [--workload NAME]
+
+Under torchrun (N > 1) every rank runs its own batch (seed + rank) on its own
+GPU with no collective on the data path (weak scaling); the time is the max
+over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of peak) and seq-steps/sec"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 126 * 1024 * 1024
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "paged_decode_qwen3_0p6b.txt")
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def step_bytes(wl) -> dict:
+    """Algorithmic bytes of one step (see the per-kernel formulas in the design doc)."""
+    s = wl.spec
+    lens = wl.lens_host().astype(np.int64)
+    B, Hq, Hkv, D = s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim
+    row = Hkv * D * 2
+    decode = int(lens.sum()) * row * 2 + B * Hq * D * 2 * 2          # K+V rows read, q read, out written
+    decode_index = B * 4 + int(sum(-(-int(L) // s.block_size) for L in lens)) * 4
+    t_valid = B - len(wl.skip_tokens)
+    store = t_valid * row * 2 * 2 + wl.num_tokens * 4                 # k,v read + cache rows written + slots
+    slots = B * 4 * 2 + wl.num_tokens * 4
+    L = s.layers
+    return {"decode": decode + decode_index, "store": store, "slots": slots,
+            "step": L * (decode + decode_index + store) + slots, "decode_kv_only": int(lens.sum()) * row * 2}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.proc = None
+        self.gpu = gpu_index
+        self.out = b""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", self.gpu], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = list(csv.reader(io.StringIO(self.out.decode(errors="replace"))))
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi unavailable"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_from_profile():
+    """DRAM bytes per paged_decode launch from the committed ncu summary, if it matches the current source."""
+    try:
+        kv = {}
+        with open(PROFILE_TRAFFIC) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, _, v = line.partition(":")
+                    kv[k.strip()] = v.strip()
+        src = os.path.join(ROOT, "paged_kv_cache_62_gb300", "csrc", "pkv_decode.cu")
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if kv.get("src_sha256") != sha:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_pkv(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_cache_62_gb300 import pkv, workloads
+
+    wl = workloads.make(args.workload, dev, seed=workloads.SEED_BASE + workloads.ORDER.index(args.workload)
+                        + 1000 * rank)
+    s = wl.spec
+    B, Hq, Hkv, D = s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim
+    max_ctx = int(wl.lens_host().max())
+    slots = torch.empty(wl.num_tokens, dtype=torch.int32, device=dev)
+    outs = [torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev) for _ in wl.layers]
+    wsbuf = pkv.alloc_workspace(B, Hq, Hkv, D, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 1 + 3 * len(wl.layers)
+
+    def step(dec_events=None):
+        pkv.decode_slot_mapping(wl.block_tables, wl.context_lens, s.block_size, wl.num_blocks, slots, err, stream)
+        for li, lay in enumerate(wl.layers):
+            pkv.kv_store(lay.k_new, lay.v_new, slots, lay.k_cache, lay.v_cache, err, stream)
+            if dec_events is not None:
+                dec_events[li][0].record(stream)
+            pkv.paged_decode(lay.q, lay.k_cache, lay.v_cache, wl.block_tables, wl.context_lens, wl.scale,
+                             outs[li], wsbuf, max_context_len=max_ctx, err_word=err, stream=stream)
+            if dec_events is not None:
+                dec_events[li][1].record(stream)
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert err.item() == 0, f"device error word {err.item():#x}"
+    if args.steps is None:
+        tw = time.perf_counter()
+        for _ in range(10):
+            step()
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - tw) / 10
+        args.steps = int(min(50000, max(50, 2.0 / per)))
+        if ws > 1:
+            t = torch.tensor([args.steps], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MIN)
+            args.steps = int(t.item())
+
+    nlay = len(wl.layers)
+    dec_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nlay)]
+              for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else str(local)
+    with ClockSampler(gpu_index) as clocks:
+        time.sleep(0.3)
+        barrier()
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for i in range(args.steps):
+            step(dec_ev[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        time.sleep(0.3)
+    ms = t0.elapsed_time(t1) / args.steps
+    dec_ms = [a.elapsed_time(b) for row in dec_ev for (a, b) in row]
+    dec_mean_ms = float(np.mean(dec_ms))
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end: host buffers in, host result out, through the same public calls
+    host = {
+        "q": [lay.q.cpu().pin_memory() for lay in wl.layers],
+        "k": [lay.k_new.cpu().pin_memory() for lay in wl.layers],
+        "v": [lay.v_new.cpu().pin_memory() for lay in wl.layers],
+        "bt": wl.block_tables.cpu().pin_memory(),
+        "lens": wl.context_lens.cpu().pin_memory(),
+        "out": [torch.empty(B, Hq, D, dtype=torch.bfloat16).pin_memory() for _ in wl.layers],
+    }
+    d_q = [torch.empty_like(lay.q) for lay in wl.layers]
+    d_k = [torch.empty_like(lay.k_new) for lay in wl.layers]
+    d_v = [torch.empty_like(lay.v_new) for lay in wl.layers]
+    d_bt = torch.empty_like(wl.block_tables)
+    d_lens = torch.empty_like(wl.context_lens)
+    h2d = sum(t.numel() * t.element_size() for k in ("q", "k", "v") for t in host[k]) + \
+        host["bt"].numel() * 4 + host["lens"].numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in host["out"])
+
+    def e2e_step():
+        d_bt.copy_(host["bt"], non_blocking=True)
+        d_lens.copy_(host["lens"], non_blocking=True)
+        pkv.decode_slot_mapping(d_bt, d_lens, s.block_size, wl.num_blocks, slots, err, stream)
+        for li, lay in enumerate(wl.layers):
+            d_q[li].copy_(host["q"][li], non_blocking=True)
+            d_k[li].copy_(host["k"][li], non_blocking=True)
+            d_v[li].copy_(host["v"][li], non_blocking=True)
+            pkv.kv_store(d_k[li], d_v[li], slots, lay.k_cache, lay.v_cache, err, stream)
+            pkv.paged_decode(d_q[li], lay.k_cache, lay.v_cache, d_bt, d_lens, wl.scale, outs[li], wsbuf,
+                             max_context_len=max_ctx, err_word=err, stream=stream)
+            host["out"][li].copy_(outs[li], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    e2e_steps = max(10, min(args.steps, 200))
+    barrier()
+    te = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_ms = (time.perf_counter() - te) * 1e3 / e2e_steps
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    torch.cuda.synchronize()
+    assert err.item() == 0, f"device error word {err.item():#x}"
+
+    nb = step_bytes(wl)
+    peak, peak_kind = hbm_peak()
+    gbs = nb["step"] * ws / (ms * 1e-3) / 1e9
+    dec_gbs = nb["decode"] / (dec_mean_ms * 1e-3) / 1e9
+    traffic = traffic_from_profile() if args.workload == "qwen3_0p6b" else None
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 1),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/q, shuffled block pool, NaN canaries in unowned rows)",
+        "config": {"workload": f"{args.workload}: {s.description}", "layers": s.layers, "batch_per_gpu": B,
+                   "q_heads": Hq, "kv_heads": Hkv, "head_dim": D, "block_size": s.block_size,
+                   "mean_context_len": float(wl.lens_host().mean()), "parallelism": f"replicas x{ws}",
+                   "l2": f"inputs larger than L2 (KV pool {2 * wl.layers[0].k_cache.numel() * 2 / 2**20:.0f} MiB"
+                         f" per layer > {L2_BYTES / 2**20:.0f} MiB)"},
+        "seq_steps_per_sec": round(B * ws / (ms * 1e-3), 1),
+        "pct_of_peak": {"measured_copy": round(100 * gbs / ws / peak, 2) if peak_kind == "measured" else None,
+                        "nominal_8TBps": round(100 * gbs / ws / NOMINAL_HBM_GBS, 2)},
+        "algorithmic_bytes_per_step": nb["step"],
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"kernel": "pkv_paged_decode (paged_decode_kernel + merge)", "bound": "hbm",
+                     "achieved": round(dec_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(dec_gbs / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": nb["decode"], "mean_launch_us": round(dec_mean_ms * 1e3, 2),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s"},
+        "e2e": {"value": round(nb["step"] * ws / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "note": "pinned host q/k/v/block_tables/context_lens in, bf16 out back, stream sync every step"},
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+def host_copy(wl):
+    from paged_kv_cache_62_gb300 import workloads
+    lays = [{k: workloads.bits(getattr(layer, k)) for k in ("q", "k_new", "v_new", "k_cache", "v_cache")}
+            for layer in wl.layers]
+    return lays, wl.block_tables.cpu().numpy(), wl.context_lens.cpu().numpy()
+
+
+def oracle_step(wl, lays, bt, lens, seqs, nthreads):
+    """Slot mapping + kv_store + paged decode of `seqs` (a prefix of the batch) in the fp64 oracle."""
+    import oracle
+    s = wl.spec
+    sub_bt, sub_lens = bt[:seqs], lens[:seqs]
+    slot = oracle.decode_slot_mapping(sub_bt, sub_lens, s.block_size, seqs)
+    for t in wl.skip_tokens:
+        if t < seqs:
+            slot[t] = -1
+    out = None
+    for L in lays:
+        oracle.kv_store(L["k_new"][:seqs], L["v_new"][:seqs], slot, L["k_cache"], L["v_cache"])
+        out = oracle.paged_decode(L["q"][:seqs], L["k_cache"], L["v_cache"], sub_bt, sub_lens, wl.scale,
+                                  nthreads=nthreads)
+    return out
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    """The oracle as it stands, on the host cores, over a bounded sample of the same workload.
+
+    The sample is a prefix of the batch on the first layer; for multi-layer
+    workloads the per-step figures are scaled by the layer count.
+    """
+    from paged_kv_cache_62_gb300 import workloads
+    first = wl.layers[0]
+    lays = [{k: workloads.bits(getattr(first, k)) for k in ("q", "k_new", "v_new", "k_cache", "v_cache")}]
+    bt, lens = wl.block_tables.cpu().numpy(), wl.context_lens.cpu().numpy()
+    cores = os.cpu_count() or 1
+    s = wl.spec
+    seqs = min(s.num_seqs, 4)
+    t = time.perf_counter()
+    oracle_step(wl, lays, bt, lens, seqs, cores)
+    dt = max(time.perf_counter() - t, 1e-6)
+    seqs = int(max(1, min(s.num_seqs, seqs * (budget_s / 3) / dt)))
+    reps, elapsed = 0, 0.0
+    t = time.perf_counter()
+    while elapsed < budget_s * 0.6 or reps == 0:
+        oracle_step(wl, lays, bt, lens, seqs, cores)
+        reps += 1
+        elapsed = time.perf_counter() - t
+    per_layer = elapsed / reps
+    lens_s = lens[:seqs].astype(np.int64)
+    row = s.num_kv_heads * s.head_dim * 2
+    nbytes = int(lens_s.sum()) * row * 2 + seqs * s.num_q_heads * s.head_dim * 4 + seqs * row * 4
+    per_step = per_layer * s.layers
+    return {"value": round(nbytes / per_layer / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "seq_steps_per_sec": round(seqs / per_step, 3), "seconds_per_step": round(per_step, 4),
+            "sample": f"first {seqs} of {s.num_seqs} sequences of the {s.name} batch"
+                      + (f", layer 0 of {s.layers} (time x{s.layers} per step)" if s.layers > 1 else "")
+                      + f"; slot mapping + kv_store + fp64 paged decode; {reps} repetition(s) in {elapsed:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    from paged_kv_cache_62_gb300 import workloads
+    wl = workloads.make(args.workload, "cpu", layers=1 if args.workload == "full_depth" else None)
+    s = wl.spec
+    lays, bt, lens = host_copy(wl)
+    cores = os.cpu_count() or 1
+    # size one step to ~1 s so that --steps K --warmup W stays within minutes
+    t = time.perf_counter()
+    oracle_step(wl, lays, bt, lens, min(4, s.num_seqs), cores)
+    dt = max(time.perf_counter() - t, 1e-6)
+    seqs = int(max(1, min(s.num_seqs, min(4, s.num_seqs) * 1.0 / dt)))
+    if args.steps is None:
+        args.steps = 10
+    for _ in range(args.warmup):
+        oracle_step(wl, lays, bt, lens, seqs, cores)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(wl, lays, bt, lens, seqs, cores)
+    per_step = (time.perf_counter() - t) / args.steps
+    lens_s = lens[:seqs].astype(np.int64)
+    row = s.num_kv_heads * s.head_dim * 2
+    nbytes = int(lens_s.sum()) * row * 2 + seqs * s.num_q_heads * s.head_dim * 4 + seqs * row * 4
+    value = nbytes / per_step / 1e9
+    sample = (f"first {seqs} of {s.num_seqs} sequences of the {s.name} batch"
+              + (", one of 28 layers" if s.name == "full_depth" else "")
+              + ", slot mapping + kv_store + fp64 paged decode per step")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16 inputs, CPU generator)",
+            "config": {"workload": f"{args.workload}: {s.description}", "parallelism": "host cores"},
+            "seq_steps_per_sec": round(seqs / per_step, 3),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: about 2 s of GPU work)")
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--workload", default="qwen3_0p6b")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_pkv(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,65 @@
+// Library-wide entry points (version, status strings) and host helpers.
+#include <mutex>
+
+#include "pkv_host.h"
+
+namespace pkv {
+
+bool current_device_info(DeviceInfo *info)
+{
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    DeviceInfo &c = cache[dev];
+    if (c.device != dev) {
+        int sms = 0, smem = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        c.sm_count = sms;
+        c.max_smem_optin = smem;
+        c.device = dev;
+    }
+    *info = c;
+    return true;
+}
+
+EncodeTiledFn encode_tiled_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+}  // namespace pkv
+
+extern "C" int pkv_abi_version(void) { return 1; }
+
+extern "C" const char *pkv_status_string(int status)
+{
+    switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_EINVAL: return "invalid argument (pointer, size, shape or alignment)";
+    case PKV_EUNSUPPORTED: return "unsupported configuration";
+    case PKV_ECUDA: return "CUDA call or kernel launch failed";
+    case PKV_EWORKSPACE: return "workspace missing or too small";
+    case PKV_EBOUNDS: return "index out of range";
+    default: return "unknown pkv status";
+    }
+}

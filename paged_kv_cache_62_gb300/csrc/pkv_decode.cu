@@ -1,0 +1,657 @@
+// Decode-phase PagedAttention for sm_103a (q_len = 1, grouped-query attention).
+//
+// What it computes (mini-vLLM README §5 "Triton PagedAttention Decode Kernel";
+// MinivLLM review, section "注意力内核的三个分支"): for sequence b, query head
+// h and L = context_lens[b],
+//     out[b, h] = softmax_j(scale * q[b, h] . K_j) V_j,   j < L,
+// with K_j / V_j read from row j % bs of physical block block_tables[b][j / bs]
+// at kv head h / G (G = Hq / Hkv), accumulated in fp32 with the online softmax
+// state (m, l, acc) of the README.
+//
+// How (GB300 design):
+//  * The work is the list of 16-token tiles of every (sequence, kv head) pair,
+//    in (b, g, tile) order.  Every CTA rebuilds the per-sequence tile prefix
+//    sum in shared memory, and worker warp w takes tiles
+//    [w*T/P, (w+1)*T/P) -- an even split of the whole batch over all resident
+//    warps, so long and short sequences balance without a host round trip.
+//  * Each warp is its own pipeline: lane 0 issues TMA tensor copies (one K and
+//    one V box of 16 tokens x head_dim for the warp's kv head) into a 3-stage
+//    ring of shared-memory tiles, completion tracked by mbarrier transaction
+//    counts.  Block-table entries for tile k+32 are fetched while tile k is
+//    issued (one register per lane), so table lookups never stall the ring.
+//  * One K/V read serves all G query heads of the group.  A token row is
+//    split over D/8 lanes (16 bytes each); the per-lane partial dot products
+//    of a tile are finished by a shuffle reduce-scatter, the softmax max is a
+//    warp max, exponentials are ex2 on log2e-prescaled scores, and P.V uses
+//    the same lane split with fp32 accumulators.
+//  * A warp whose tile range covers a whole (b, g) writes bf16 output
+//    directly; otherwise it leaves its (m, l, acc) in the workspace and the
+//    merge kernel combines the pieces (split-K / flash-decoding).
+#include <algorithm>
+#include <cmath>
+
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+
+constexpr int kTile = 16;      // tokens per tile
+constexpr int kMaxWarps = 8;   // warps per CTA (one CTA per SM)
+constexpr int kStages = 3;     // ring depth per warp
+
+struct DecodeParams {
+    const uint16_t *q;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    uint16_t *out;
+    int32_t *ws_prefix;  // [B + 1] tile prefix (written by CTA 0, read by the merge)
+    float *ws_ml;        // [slots][G][2] (m, l) per partial
+    float *ws_acc;       // [slots][G][D] unnormalised accumulators
+    int32_t *err;
+    int32_t B, Hq, Hkv, bs, log2_bs, NB, max_blocks, len_limit, num_workers;
+    float scale_log2;    // scale * log2(e)
+};
+
+struct alignas(16) StageMeta {
+    int32_t b, g, t, n, L, seg_start, pad0, pad1;
+};
+
+template <int D, int G>
+struct Shape {
+    static constexpr int LPT = D / 8;          // lanes per token row (16 bytes each)
+    static constexpr int TPI = 32 / LPT;       // tokens per warp step
+    static constexpr int NIT = kTile / TPI;    // steps per tile
+    static constexpr int DUP = LPT / NIT;      // lanes that end up holding each score
+    static constexpr int KV_BYTES = kTile * D * 2;
+    static constexpr int Q_BYTES = G * D * 2;
+    static constexpr int STAGE_BYTES = (2 * KV_BYTES + Q_BYTES + 127) / 128 * 128;
+    static_assert(LPT >= NIT && DUP >= 1, "tile too large for the lane split");
+};
+
+struct WsLayout {
+    size_t prefix_off, ml_off, acc_off, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(int32_t B, int32_t G, int32_t Hkv, int32_t D)
+{
+    const size_t slots = size_t(PKV_MAX_WORKERS) + size_t(B) * size_t(Hkv);
+    WsLayout w;
+    w.prefix_off = 0;
+    w.ml_off = align256(size_t(B + 1) * 4);
+    w.acc_off = w.ml_off + align256(slots * size_t(G) * 2 * 4);
+    w.total = w.acc_off + slots * size_t(G) * size_t(D) * 4;
+    return w;
+}
+
+// ------------------------------------------------------------------ work list walking
+struct Walker {
+    int32_t b, g, t, n;
+};
+
+__device__ __forceinline__ void walker_advance(Walker &w, const int32_t *scan, int32_t Hkv, int32_t B)
+{
+    if (++w.t < w.n) return;
+    w.t = 0;
+    if (++w.g < Hkv) return;
+    w.g = 0;
+    do {
+        ++w.b;
+        w.n = (w.b < B) ? scan[w.b + 1] - scan[w.b] : 1;
+    } while (w.n == 0);
+}
+
+// Position of global tile x (0 <= x < Hkv * scan[B]).
+__device__ __forceinline__ Walker walker_locate(const int32_t *scan, int32_t B, int32_t Hkv, int64_t x)
+{
+    int lo = 0, hi = B;  // Hkv*scan[lo] <= x < Hkv*scan[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (int64_t(Hkv) * scan[mid] <= x)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    Walker w;
+    w.b = lo;
+    w.n = scan[lo + 1] - scan[lo];
+    const int64_t rem = x - int64_t(Hkv) * scan[lo];
+    w.g = int32_t(rem / w.n);
+    w.t = int32_t(rem - int64_t(w.g) * w.n);
+    return w;
+}
+
+__device__ __forceinline__ void table_lookup(const DecodeParams &p, const Walker &w, int nsub, int32_t &e0,
+                                             int32_t &e1, int32_t &len)
+{
+    const int32_t *row = p.block_tables + int64_t(w.b) * p.max_blocks;
+    const int32_t pos0 = w.t * kTile;
+    e0 = __ldg(row + (pos0 >> p.log2_bs));
+    if (nsub == 2) {
+        const int32_t lb1 = (pos0 + kTile / 2) >> p.log2_bs;
+        e1 = lb1 < p.max_blocks ? __ldg(row + lb1) : -1;
+    }
+    len = __ldg(p.context_lens + w.b);
+}
+
+// Tiles per sequence -> exclusive prefix in scan[0..B]; CTA 0 also publishes it.
+// `tmp` needs 32 ints of shared memory that is free during the call.
+__device__ void tile_prefix_scan(const DecodeParams &p, int32_t *scan, int32_t *tmp)
+{
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
+    const int per = (p.B + nt - 1) / nt;
+    const int lo = min(p.B, tid * per), hi = min(p.B, lo + per);
+    int32_t sum = 0;
+    for (int i = lo; i < hi; ++i) {
+        const int32_t len = __ldg(p.context_lens + i);
+        int32_t n = 0;
+        if (len < 0 || len > p.len_limit) {
+            if (blockIdx.x == 0) flag_error(p.err, PKV_ERR_CONTEXT_RANGE);
+        } else {
+            n = (len + kTile - 1) / kTile;
+        }
+        scan[i] = n;
+        sum += n;
+    }
+    int32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) tmp[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        const int32_t v = lane < nw ? tmp[lane] : 0;
+        int32_t inc = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t u = __shfl_up_sync(kFull, inc, o);
+            if (lane >= o) inc += u;
+        }
+        if (lane < nw) tmp[lane] = inc - v;
+    }
+    __syncthreads();
+    int32_t run = tmp[wid] + incl - sum;
+    for (int i = lo; i < hi; ++i) {
+        const int32_t n = scan[i];
+        scan[i] = run;
+        run += n;
+    }
+    if (lo < hi && hi == p.B) scan[p.B] = run;
+    __syncthreads();
+    if (blockIdx.x == 0)
+        for (int i = tid; i <= p.B; i += nt) p.ws_prefix[i] = scan[i];
+}
+
+// ------------------------------------------------------------------ one tile
+template <int D, int G>
+__device__ __forceinline__ void attend_tile(const uint8_t *st, int valid, const float (&qf)[G][8], float (&m)[G],
+                                            float (&l)[G], float (&acc)[G][8], int c, int grp)
+{
+    using S = Shape<D, G>;
+    constexpr int LPT = S::LPT, TPI = S::TPI, NIT = S::NIT, DUP = S::DUP;
+    const uint16_t *Ks = reinterpret_cast<const uint16_t *>(st);
+    const uint16_t *Vs = reinterpret_cast<const uint16_t *>(st + S::KV_BYTES);
+
+    // scores: lane (grp, c) forms the 8-element partial dot products of tokens i*TPI + grp
+    float part[G][NIT];
+#pragma unroll
+    for (int i = 0; i < NIT; ++i) {
+        const int tok = i * TPI + grp;
+        const uint4 kw = *reinterpret_cast<const uint4 *>(Ks + tok * D + c * 8);
+        float kf[8];
+        unpack8(kw, kf);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float s = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s = fmaf(qf[h][e], kf[e], s);
+            part[h][i] = s;
+        }
+    }
+    // reduce-scatter over the LPT lanes of a token: afterwards lane c holds the
+    // full score of step c / DUP
+#pragma unroll
+    for (int cnt = NIT, mask = LPT / 2; cnt > 1; cnt >>= 1, mask >>= 1) {
+        const bool upper = (c & mask) != 0;
+#pragma unroll
+        for (int j = 0; j < cnt / 2; ++j) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float send = upper ? part[h][j] : part[h][j + cnt / 2];
+                const float keep = upper ? part[h][j + cnt / 2] : part[h][j];
+                part[h][j] = keep + __shfl_xor_sync(kFull, send, mask);
+            }
+        }
+    }
+#pragma unroll
+    for (int mask = DUP / 2; mask > 0; mask >>= 1)
+#pragma unroll
+        for (int h = 0; h < G; ++h) part[h][0] += __shfl_xor_sync(kFull, part[h][0], mask);
+
+    const int tok_s = (c / DUP) * TPI + grp;
+    const bool ok = tok_s < valid;
+    float pr[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const float s = ok ? part[h][0] : -INFINITY;
+        const float mn = fmaxf(m[h], warp_max(s));  // finite: every tile holds a valid token
+        const float alpha = ex2(m[h] - mn);         // 0 on the first tile (m = -inf)
+        pr[h] = ok ? ex2(s - mn) : 0.f;
+        l[h] = l[h] * alpha + pr[h];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[h][e] *= alpha;
+        m[h] = mn;
+    }
+    // P.V: the weight of token i*TPI + grp sits in lane grp*LPT + i*DUP
+#pragma unroll
+    for (int i = 0; i < NIT; ++i) {
+        const int tok = i * TPI + grp;
+        float ph[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) ph[h] = __shfl_sync(kFull, pr[h], grp * LPT + i * DUP);
+        if (tok < valid) {  // rows past L may hold anything, even NaN: never touch them
+            const uint4 vw = *reinterpret_cast<const uint4 *>(Vs + tok * D + c * 8);
+            float vf[8];
+            unpack8(vw, vf);
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(ph[h], vf[e], acc[h][e]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ main kernel
+template <int D, int G>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        const DecodeParams p)
+{
+    using S = Shape<D, G>;
+    constexpr int LPT = S::LPT, DUP = S::DUP;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int nwarps = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = lane % LPT, grp = lane / LPT;
+
+    uint8_t *stages = smem + size_t(warp) * kStages * S::STAGE_BYTES;
+    StageMeta *metas =
+        reinterpret_cast<StageMeta *>(smem + size_t(nwarps) * kStages * S::STAGE_BYTES) + warp * kStages;
+    uint64_t *bars =
+        reinterpret_cast<uint64_t *>(smem + size_t(nwarps) * kStages * (S::STAGE_BYTES + sizeof(StageMeta))) +
+        warp * kStages;
+    int32_t *scan = reinterpret_cast<int32_t *>(smem + size_t(nwarps) * kStages *
+                                                           (S::STAGE_BYTES + sizeof(StageMeta) + 8));
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    tile_prefix_scan(p, scan, reinterpret_cast<int32_t *>(smem));
+
+    const int64_t T = int64_t(p.Hkv) * scan[p.B];
+    const int w = blockIdx.x * nwarps + warp;
+    // Never more workers than tiles, so every worker in [0, P) owns at least one tile
+    // (the merge kernel relies on this when it walks the workers of a sequence).
+    const int64_t P = T < p.num_workers ? T : p.num_workers;
+    if (w >= P) return;
+    const int64_t begin = int64_t(w) * T / P;
+    const int64_t end = int64_t(w + 1) * T / P;
+    const int ntiles = int(end - begin);
+    if (ntiles == 0) return;
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    const uint64_t policy = policy_evict_first();
+    const int box = p.bs < kTile ? p.bs : kTile;
+    const int nsub = kTile / box;
+
+    // Block-table prefetch: lane j holds the entries of the next tile k with k % 32 == j.
+    Walker fw = walker_locate(scan, p.B, p.Hkv, begin);
+    Walker iw = fw;
+    int32_t pf0 = -1, pf1 = -1, pfL = 0;
+    const int npre = ntiles < 32 ? ntiles : 32;
+    for (int j = 0; j < npre; ++j) {
+        if (lane == j) table_lookup(p, fw, nsub, pf0, pf1, pfL);
+        if (j + 1 < ntiles) walker_advance(fw, scan, p.Hkv, p.B);
+    }
+
+    auto issue = [&](int k, int s) {
+        const int src = k & 31;
+        const int32_t e0 = __shfl_sync(kFull, pf0, src);
+        const int32_t e1 = __shfl_sync(kFull, pf1, src);
+        const int32_t len = __shfl_sync(kFull, pfL, src);
+        if (k + 32 < ntiles) {
+            if (lane == src) table_lookup(p, fw, nsub, pf0, pf1, pfL);
+            if (k + 33 < ntiles) walker_advance(fw, scan, p.Hkv, p.B);
+        }
+        if (lane == 0) {
+            uint8_t *st = stages + s * S::STAGE_BYTES;
+            const int seg_start = (k == 0 || iw.t == 0) ? 1 : 0;
+            const int32_t pos0 = iw.t * kTile;
+            int32_t row0 = -1, row1 = -1;
+            if (e0 >= 0 && e0 < p.NB)
+                row0 = e0 * p.bs + (pos0 & (p.bs - 1));
+            else
+                flag_error(p.err, PKV_ERR_BLOCK_RANGE);
+            if (nsub == 2 && pos0 + box < len) {
+                if (e1 >= 0 && e1 < p.NB)
+                    row1 = e1 * p.bs;
+                else
+                    flag_error(p.err, PKV_ERR_BLOCK_RANGE);
+            }
+            const uint32_t sub_bytes = uint32_t(2 * box * D * 2);
+            const uint32_t bytes = (row0 >= 0 ? sub_bytes : 0u) + (row1 >= 0 ? sub_bytes : 0u) +
+                                   (seg_start ? uint32_t(S::Q_BYTES) : 0u);
+            StageMeta &mt = metas[s];
+            mt.b = iw.b;
+            mt.g = iw.g;
+            mt.t = iw.t;
+            mt.n = iw.n;
+            mt.L = len;
+            mt.seg_start = seg_start;
+            mbar_arrive_expect_tx(&bars[s], bytes);
+            if (row0 >= 0) {
+                tma_load_3d(st, &kmap, 0, iw.g, row0, &bars[s], policy);
+                tma_load_3d(st + S::KV_BYTES, &vmap, 0, iw.g, row0, &bars[s], policy);
+            }
+            if (row1 >= 0) {
+                tma_load_3d(st + box * D * 2, &kmap, 0, iw.g, row1, &bars[s], policy);
+                tma_load_3d(st + S::KV_BYTES + box * D * 2, &vmap, 0, iw.g, row1, &bars[s], policy);
+            }
+            if (seg_start)
+                bulk_load(st + 2 * S::KV_BYTES, p.q + (int64_t(iw.b) * p.Hq + int64_t(iw.g) * G) * D,
+                          S::Q_BYTES, &bars[s]);
+        }
+        if (k + 1 < ntiles) walker_advance(iw, scan, p.Hkv, p.B);
+    };
+
+    const int prologue = ntiles < kStages ? ntiles : kStages;
+    for (int k = 0; k < prologue; ++k) issue(k, k);
+
+    float qf[G][8], m[G], l[G], acc[G][8];
+    bool open = false;
+    int32_t seg_t0 = 0;
+    int k = 0;
+    for (; k < ntiles; ++k) {
+        const int s = k % kStages;
+        if (!mbar_wait_bounded(&bars[s], uint32_t(k / kStages) & 1u)) {
+            if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
+            break;
+        }
+        const StageMeta mt = metas[s];
+        const uint8_t *st = stages + s * S::STAGE_BYTES;
+        if (!open) {
+            open = true;
+            seg_t0 = mt.t;
+            const uint16_t *qs = reinterpret_cast<const uint16_t *>(st + 2 * S::KV_BYTES);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float f[8];
+                unpack8(*reinterpret_cast<const uint4 *>(qs + h * D + c * 8), f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    qf[h][e] = f[e] * p.scale_log2;
+                    acc[h][e] = 0.f;
+                }
+                m[h] = -INFINITY;
+                l[h] = 0.f;
+            }
+        }
+        const int valid = min(kTile, mt.L - mt.t * kTile);
+        attend_tile<D, G>(st, valid, qf, m, l, acc, c, grp);
+        __syncwarp();
+        if (k + kStages < ntiles) issue(k + kStages, s);
+
+        if (mt.t == mt.n - 1 || k == ntiles - 1) {
+            // close the segment: fold the token groups, then write out or leave a partial
+#pragma unroll
+            for (int mask = LPT; mask < 32; mask <<= 1)
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[h][e] += __shfl_xor_sync(kFull, acc[h][e], mask);
+            float lt[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) lt[h] = warp_sum(l[h]) * (1.0f / DUP);
+            if (seg_t0 == 0 && mt.t == mt.n - 1) {
+                if (grp == 0) {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float inv = 1.0f / lt[h];
+                        uint4 o;
+                        o.x = pack_bf16x2(acc[h][0] * inv, acc[h][1] * inv);
+                        o.y = pack_bf16x2(acc[h][2] * inv, acc[h][3] * inv);
+                        o.z = pack_bf16x2(acc[h][4] * inv, acc[h][5] * inv);
+                        o.w = pack_bf16x2(acc[h][6] * inv, acc[h][7] * inv);
+                        *reinterpret_cast<uint4 *>(p.out + (int64_t(mt.b) * p.Hq + int64_t(mt.g) * G + h) * D +
+                                                   c * 8) = o;
+                    }
+                }
+            } else {
+                const int64_t slot = int64_t(w) + int64_t(mt.b) * p.Hkv + mt.g;
+                if (grp == 0) {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + ((slot * G + h) * D + c * 8));
+                        dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+                        dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
+                    }
+                }
+                if (lane == 0)
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+                        reinterpret_cast<float2 *>(p.ws_ml)[slot * G + h] = make_float2(m[h], lt[h]);
+            }
+            open = false;
+        }
+    }
+    if (k < ntiles) {
+        // gave up on a wait: let every copy still in flight land before the CTA retires
+        for (int j = k; j < ntiles && j < k + kStages; ++j)
+            mbar_wait_bounded(&bars[j % kStages], uint32_t(j / kStages) & 1u);
+    }
+}
+
+// ------------------------------------------------------------------ split-K merge
+// One CTA per (b, g); thread (h, c4) merges 4 output values of query head g*G+h.
+template <int D, int G>
+__global__ void __launch_bounds__(G * D / 4)
+    paged_decode_merge_kernel(const DecodeParams p)
+{
+    const int bg = blockIdx.x;
+    const int b = bg / p.Hkv, g = bg - b * p.Hkv;
+    const int h = threadIdx.x / (D / 4), c4 = threadIdx.x % (D / 4);
+    uint16_t *o = p.out + (int64_t(b) * p.Hq + int64_t(g) * G + h) * D + c4 * 4;
+    const int32_t n = p.ws_prefix[b + 1] - p.ws_prefix[b];
+    if (n == 0) {  // empty (or rejected) sequence: zeros
+        *reinterpret_cast<uint2 *>(o) = make_uint2(0u, 0u);
+        return;
+    }
+    const int64_t T = int64_t(p.Hkv) * p.ws_prefix[p.B];
+    const int64_t start = int64_t(p.Hkv) * p.ws_prefix[b] + int64_t(g) * n;
+    const int64_t P = T < p.num_workers ? T : p.num_workers;  // same cap as the main kernel
+    const int64_t wf = ((start + 1) * P - 1) / T;  // worker holding the first tile
+    const int64_t wl = ((start + n) * P - 1) / T;  // worker holding the last tile
+    if (wf == wl) return;                           // written directly by the main kernel
+    const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);
+    float M = -INFINITY;
+    for (int64_t w = wf; w <= wl; ++w) M = fmaxf(M, ml[(w + bg) * G + h].x);
+    float lsum = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    for (int64_t w = wf; w <= wl; ++w) {
+        const float2 st = ml[(w + bg) * G + h];
+        const float f = ex2(st.x - M);
+        const float4 v = *reinterpret_cast<const float4 *>(p.ws_acc + ((w + bg) * G + h) * D + c4 * 4);
+        lsum = fmaf(f, st.y, lsum);
+        a0 = fmaf(f, v.x, a0);
+        a1 = fmaf(f, v.y, a1);
+        a2 = fmaf(f, v.z, a2);
+        a3 = fmaf(f, v.w, a3);
+    }
+    const float inv = 1.0f / lsum;
+    *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16x2(a0 * inv, a1 * inv), pack_bf16x2(a2 * inv, a3 * inv));
+}
+
+// ------------------------------------------------------------------ host side
+struct LaunchArgs {
+    DecodeParams p;
+    const void *k_cache, *v_cache;
+    int sm_count, max_smem;
+    int requested_workers;
+    cudaStream_t stream;
+};
+
+inline bool encode_cache_map(CUtensorMap *map, const void *base, int D, int Hkv, int64_t rows, int box_rows)
+{
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(Hkv), cuuint64_t(rows)};
+    const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(Hkv) * D * 2};
+    const cuuint32_t box[3] = {cuuint32_t(D), 1u, cuuint32_t(box_rows)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int G>
+size_t decode_smem_bytes(int nwarps, int B)
+{
+    using S = Shape<D, G>;
+    return size_t(nwarps) * kStages * (S::STAGE_BYTES + sizeof(StageMeta) + 8) + size_t(B + 1) * 4;
+}
+
+template <int D, int G>
+pkv_status launch_decode(LaunchArgs &a)
+{
+    int nwarps = kMaxWarps;
+    while (nwarps > 1 && decode_smem_bytes<D, G>(nwarps, a.p.B) > size_t(a.max_smem)) --nwarps;
+    const size_t smem = decode_smem_bytes<D, G>(nwarps, a.p.B);
+    if (smem > size_t(a.max_smem)) return PKV_EUNSUPPORTED;
+
+    int workers = a.requested_workers > 0 ? a.requested_workers : a.sm_count * nwarps;
+    if (workers > PKV_MAX_WORKERS) workers = PKV_MAX_WORKERS;
+    a.p.num_workers = workers;
+    const int grid = (workers + nwarps - 1) / nwarps;
+
+    const int box = a.p.bs < kTile ? a.p.bs : kTile;
+    CUtensorMap kmap, vmap;
+    const int64_t rows = int64_t(a.p.NB) * a.p.bs;
+    if (!encode_cache_map(&kmap, a.k_cache, D, a.p.Hkv, rows, box) ||
+        !encode_cache_map(&vmap, a.v_cache, D, a.p.Hkv, rows, box))
+        return PKV_ECUDA;
+
+    auto kern = paged_decode_kernel<D, G>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ECUDA;
+    }
+    kern<<<grid, nwarps * 32, smem, a.stream>>>(kmap, vmap, a.p);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ECUDA;
+    paged_decode_merge_kernel<D, G><<<a.p.B * a.p.Hkv, G * D / 4, 0, a.stream>>>(a.p);
+    return launch_status();
+}
+
+using LaunchFn = pkv_status (*)(LaunchArgs &);
+
+template <int D>
+LaunchFn pick_group(int G)
+{
+    switch (G) {
+    case 1: return launch_decode<D, 1>;
+    case 2: return launch_decode<D, 2>;
+    case 3: return launch_decode<D, 3>;
+    case 4: return launch_decode<D, 4>;
+    case 5: return launch_decode<D, 5>;
+    case 6: return launch_decode<D, 6>;
+    case 7: return launch_decode<D, 7>;
+    case 8: return launch_decode<D, 8>;
+    default: return nullptr;
+    }
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                                  int32_t head_dim)
+{
+    if (num_seqs < 0 || num_seqs > PKV_MAX_SEQS || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        num_q_heads % num_kv_heads != 0)
+        return 0;
+    return ws_layout(num_seqs, num_q_heads / num_kv_heads, num_kv_heads, head_dim).total;
+}
+
+extern "C" pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                       int32_t num_blocks, int32_t max_context_len, float scale, uint16_t *out,
+                                       void *workspace, size_t workspace_bytes, int32_t num_workers,
+                                       int32_t *err_word, pkv_stream_t stream)
+{
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+        head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 ||
+        num_workers < 0 || num_workers > PKV_MAX_WORKERS || !std::isfinite(scale))
+        return PKV_EINVAL;
+    if (num_seqs > PKV_MAX_SEQS) return PKV_EUNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_EUNSUPPORTED;
+    const int G = num_q_heads / num_kv_heads;
+    if (G > 8) return PKV_EUNSUPPORTED;
+    if (!is_pow2(block_size) || block_size < 8 || block_size > 1024) return PKV_EUNSUPPORTED;
+    if (int64_t(num_blocks) * block_size > INT32_MAX) return PKV_EUNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_EINVAL;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PKV_EINVAL;
+    const int64_t len_limit = std::min<int64_t>(max_context_len, int64_t(max_blocks_per_seq) * block_size);
+    const int64_t max_tiles = int64_t(num_seqs) * ((len_limit + kTile - 1) / kTile);
+    if (max_tiles > INT32_MAX) return PKV_EUNSUPPORTED;
+    if (num_workers > 0 && int64_t(num_kv_heads) * max_tiles / num_workers + 1 > INT32_MAX) return PKV_EUNSUPPORTED;
+    const WsLayout ws = ws_layout(num_seqs, G, num_kv_heads, head_dim);
+    if (!workspace || workspace_bytes < ws.total || !aligned16(workspace)) return PKV_EWORKSPACE;
+
+    DeviceInfo dev;
+    if (!current_device_info(&dev)) return PKV_ECUDA;
+
+    LaunchArgs a;
+    DecodeParams &p = a.p;
+    uint8_t *wsb = static_cast<uint8_t *>(workspace);
+    p.q = q;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = out;
+    p.ws_prefix = reinterpret_cast<int32_t *>(wsb + ws.prefix_off);
+    p.ws_ml = reinterpret_cast<float *>(wsb + ws.ml_off);
+    p.ws_acc = reinterpret_cast<float *>(wsb + ws.acc_off);
+    p.err = err_word;
+    p.B = num_seqs;
+    p.Hq = num_q_heads;
+    p.Hkv = num_kv_heads;
+    p.bs = block_size;
+    p.log2_bs = ilog2(block_size);
+    p.NB = num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.len_limit = int32_t(len_limit);
+    p.num_workers = 0;
+    p.scale_log2 = float(double(scale) * 1.4426950408889634);
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.sm_count = dev.sm_count;
+    a.max_smem = dev.max_smem_optin;
+    a.requested_workers = num_workers;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+
+    LaunchFn fn = head_dim == 64 ? pick_group<64>(G) : pick_group<128>(G);
+    if (!fn) return PKV_EUNSUPPORTED;
+    return fn(a);
+}

@@ -1,0 +1,48 @@
+// Host-side helpers shared by the pkv entry points: argument checks, the
+// per-device attribute cache and the driver entry point for tensor maps.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+inline int ilog2(int64_t x)
+{
+    int r = 0;
+    while ((int64_t(1) << (r + 1)) <= x) ++r;
+    return r;
+}
+
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+};
+
+// Attributes of the current device (cached per device id).  Returns false if
+// no device is current / visible.
+bool current_device_info(DeviceInfo *info);
+
+// cuTensorMapEncodeTiled obtained through the runtime's driver entry point
+// (no link-time dependency on libcuda).  nullptr if unavailable.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+inline pkv_status launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+}  // namespace pkv

@@ -1,0 +1,111 @@
+// Decode-step slot computation and the store_kvcache scatter.
+//
+// pkv_decode_slot_mapping: slot of the token each sequence appends --
+//   block_tables[b][pos / bs] * bs + pos % bs with pos = context_lens[b] - 1
+//   (nano-vLLM lab manual §5.2.3 / B.2.3; nano-vllm KV-cache post §3.1, §4.4).
+// pkv_kv_store: row slot_mapping[t] of k_cache / v_cache becomes a copy of
+//   k[t] / v[t]; slot -1 skips the row (MinivLLM review, "注意力内核的三个分支").
+//
+// Both are tiny, latency-bound launches.  The store moves whole cache rows
+// (num_kv_heads * head_dim bf16, 2 KiB for Qwen3-0.6B) with 16-byte vector
+// loads/stores: one CTA per token, consecutive threads on consecutive 16-byte
+// chunks of the row, so every warp access is a fully coalesced 512-byte run.
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+
+__global__ void decode_slot_mapping_kernel(const int32_t *__restrict__ block_tables, int32_t max_blocks,
+                                           const int32_t *__restrict__ context_lens, int32_t num_seqs,
+                                           int32_t block_size, int32_t log2_bs, int32_t num_blocks,
+                                           int32_t *__restrict__ slot_mapping, int32_t num_tokens,
+                                           int32_t *err)
+{
+    const int32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= num_tokens) return;
+    int32_t slot = -1;
+    if (t < num_seqs) {
+        const int32_t len = __ldg(context_lens + t);
+        if (len > 0) {
+            const int32_t pos = len - 1;
+            const int32_t logical = pos >> log2_bs;
+            if (logical >= max_blocks) {
+                flag_error(err, PKV_ERR_CONTEXT_RANGE);
+            } else {
+                const int32_t phys = __ldg(block_tables + static_cast<int64_t>(t) * max_blocks + logical);
+                if (phys < 0 || phys >= num_blocks)
+                    flag_error(err, PKV_ERR_BLOCK_RANGE);
+                else
+                    slot = phys * block_size + (pos & (block_size - 1));
+            }
+        } else if (len < 0) {
+            flag_error(err, PKV_ERR_CONTEXT_RANGE);
+        }
+    }
+    slot_mapping[t] = slot;
+}
+
+__global__ void kv_store_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                const int32_t *__restrict__ slot_mapping, uint4 *__restrict__ k_cache,
+                                uint4 *__restrict__ v_cache, int64_t num_slots, int32_t row_vecs, int32_t *err)
+{
+    const int32_t t = blockIdx.x;
+    const int64_t s = __ldg(slot_mapping + t);
+    if (s == -1) return;
+    if (s < 0 || s >= num_slots) {
+        if (threadIdx.x == 0) flag_error(err, PKV_ERR_SLOT_RANGE);
+        return;
+    }
+    const uint4 *ks = k + static_cast<int64_t>(t) * row_vecs;
+    const uint4 *vs = v + static_cast<int64_t>(t) * row_vecs;
+    uint4 *kd = k_cache + s * row_vecs;
+    uint4 *vd = v_cache + s * row_vecs;
+    for (int32_t i = threadIdx.x; i < row_vecs; i += blockDim.x) {
+        const uint4 a = __ldg(ks + i);
+        const uint4 b = __ldg(vs + i);
+        kd[i] = a;
+        vd[i] = b;
+    }
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" pkv_status pkv_decode_slot_mapping(const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                              const int32_t *context_lens, int32_t num_seqs, int32_t block_size,
+                                              int32_t num_blocks, int32_t *slot_mapping, int32_t num_tokens,
+                                              int32_t *err_word, pkv_stream_t stream)
+{
+    if (num_seqs < 0 || num_tokens < num_seqs || max_blocks_per_seq <= 0 || num_blocks <= 0) return PKV_EINVAL;
+    if (!is_pow2(block_size) || static_cast<int64_t>(num_blocks) * block_size > INT32_MAX) return PKV_EINVAL;
+    if (num_tokens == 0) return PKV_OK;
+    if (!slot_mapping || (num_seqs > 0 && (!block_tables || !context_lens))) return PKV_EINVAL;
+    const int threads = 128;
+    const int blocks = (num_tokens + threads - 1) / threads;
+    decode_slot_mapping_kernel<<<blocks, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        block_tables, max_blocks_per_seq, context_lens, num_seqs, block_size, ilog2(block_size), num_blocks,
+        slot_mapping, num_tokens, err_word);
+    return launch_status();
+}
+
+extern "C" pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, const int32_t *slot_mapping,
+                                   int32_t num_tokens, uint16_t *k_cache, uint16_t *v_cache, int32_t num_blocks,
+                                   int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int32_t *err_word,
+                                   pkv_stream_t stream)
+{
+    if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return PKV_EINVAL;
+    const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * 2;
+    if (row_bytes % 16 != 0 || row_bytes / 16 > INT32_MAX) return PKV_EINVAL;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_EINVAL;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
+    const int32_t row_vecs = static_cast<int32_t>(row_bytes / 16);
+    const int threads = row_vecs >= 256 ? 256 : ((row_vecs + 31) / 32) * 32;
+    kv_store_kernel<<<num_tokens, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v), slot_mapping,
+        reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache),
+        static_cast<int64_t>(num_blocks) * block_size, row_vecs, err_word);
+    return launch_status();
+}

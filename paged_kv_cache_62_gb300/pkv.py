@@ -1,0 +1,148 @@
+"""ctypes binding of ``libpkv.so`` (declared in ``include/pkv.h``).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Tensors are torch CUDA tensors (device memory and streams come from torch);
+shapes and dtypes are checked here, then raw device pointers go through the
+C ABI.  There is no fallback: if the library is missing or the tensors are not
+on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+OK, EINVAL, EUNSUPPORTED, ECUDA, EWORKSPACE, EBOUNDS = 0, -1, -2, -3, -4, -5
+ERR_SLOT_RANGE, ERR_BLOCK_RANGE, ERR_CONTEXT_RANGE, ERR_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+MAX_SEQS, MAX_WORKERS = 16384, 4096
+
+# name -> (restype, argtypes), mirroring include/pkv.h
+_P, _I32, _SZ, _F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+SIGNATURES = {
+    "pkv_abi_version": (ctypes.c_int, []),
+    "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pkv_decode_slot_mapping": (ctypes.c_int, [_P, _I32, _P, _I32, _I32, _I32, _P, _I32, _P, _P]),
+    "pkv_kv_store": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
+    "pkv_paged_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
+    "pkv_paged_decode": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
+                                        _F32, _P, _P, _SZ, _I32, _P, _P]),
+}
+
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libpkv.so (built by ``paged_kv_cache_62_gb300.build``); raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libpkv.so not found at {p}: build it with `python -m paged_kv_cache_62_gb300.build`")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().pkv_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise PkvError(status, what)
+
+
+def _dev(t: torch.Tensor, dtype, name: str, ndim: int | None = None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _opt(t) -> int | None:
+    return None if t is None else _dev(t, torch.int32, "err_word")
+
+
+def _stream(stream) -> int | None:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def decode_slot_mapping(block_tables: torch.Tensor, context_lens: torch.Tensor, block_size: int, num_blocks: int,
+                        slot_mapping: torch.Tensor, err_word: torch.Tensor | None = None, stream=None) -> None:
+    """Slot of each sequence's appended token (position context_len - 1); rows beyond the batch get -1."""
+    B, mb = block_tables.shape
+    _check(load().pkv_decode_slot_mapping(
+        _dev(block_tables, torch.int32, "block_tables", 2), mb, _dev(context_lens, torch.int32, "context_lens", 1),
+        B, int(block_size), int(num_blocks), _dev(slot_mapping, torch.int32, "slot_mapping", 1),
+        slot_mapping.numel(), _opt(err_word), _stream(stream)), "pkv_decode_slot_mapping")
+
+
+def kv_store(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+             v_cache: torch.Tensor, err_word: torch.Tensor | None = None, stream=None) -> None:
+    """store_kvcache: k_cache/v_cache[slot] = k/v[t] for every slot != -1."""
+    T, Hkv, D = k.shape
+    NB, bs, Hkv2, D2 = k_cache.shape
+    if v.shape != k.shape or v_cache.shape != k_cache.shape or (Hkv2, D2) != (Hkv, D) or slot_mapping.numel() != T:
+        raise ValueError("kv_store: shape mismatch")
+    _check(load().pkv_kv_store(
+        _dev(k, torch.bfloat16, "k", 3), _dev(v, torch.bfloat16, "v", 3),
+        _dev(slot_mapping, torch.int32, "slot_mapping", 1), T,
+        _dev(k_cache, torch.bfloat16, "k_cache", 4), _dev(v_cache, torch.bfloat16, "v_cache", 4),
+        NB, bs, Hkv, D, _opt(err_word), _stream(stream)), "pkv_kv_store")
+
+
+def paged_decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int) -> int:
+    n = load().pkv_paged_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim)
+    if n == 0:
+        raise PkvError(EINVAL, "pkv_paged_decode_workspace_size")
+    return int(n)
+
+
+def alloc_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, device=None) -> torch.Tensor:
+    n = paged_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                 context_lens: torch.Tensor, scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                 max_context_len: int | None = None, num_workers: int = 0, err_word: torch.Tensor | None = None,
+                 stream=None) -> None:
+    """Decode PagedAttention: out[b, h] = softmax(scale * q[b, h] K^T) V over the paged cache."""
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape or block_tables.shape[0] != B or context_lens.numel() != B \
+            or out.shape != q.shape:
+        raise ValueError("paged_decode: shape mismatch")
+    mb = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = mb * bs
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA uint8 tensor")
+    _check(load().pkv_paged_decode(
+        _dev(q, torch.bfloat16, "q", 3), _dev(k_cache, torch.bfloat16, "k_cache", 4),
+        _dev(v_cache, torch.bfloat16, "v_cache", 4), _dev(block_tables, torch.int32, "block_tables", 2), mb,
+        _dev(context_lens, torch.int32, "context_lens", 1), B, Hq, Hkv, D, bs, NB, int(max_context_len),
+        float(scale), _dev(out, torch.bfloat16, "out", 3), workspace.data_ptr(), workspace.numel(),
+        int(num_workers), _opt(err_word), _stream(stream)), "pkv_paged_decode")

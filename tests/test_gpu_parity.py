@@ -1,0 +1,289 @@
+"""GPU parity: the CUDA library through its C ABI against the CPU oracle.
+
+kv_store and the slot mapping must match bit for bit; paged_decode must stay
+within max-abs 2e-2 and mean-abs 2e-3 of the fp64 oracle (bf16 inputs, fp32
+accumulation, bf16 output).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_62_gb300 import pkv
+from paged_kv_cache_62_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS = 2e-2, 2e-3
+NTHREADS = 16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def err_word():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def check_close(got: torch.Tensor, want: np.ndarray, what: str):
+    g = got.float().cpu().double().numpy()
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    d = np.abs(g - want)
+    assert d.max() <= MAX_ABS and d.mean() <= MEAN_ABS, f"{what}: max {d.max():.3g} mean {d.mean():.3g}"
+    return d
+
+
+def run_decode(q, kc, vc, bt, lens, scale, max_ctx=None, num_workers=0, err=None):
+    B, Hq, D = q.shape
+    Hkv = kc.shape[2]
+    out = torch.full_like(q, float("nan"))
+    ws = pkv.alloc_workspace(B, Hq, Hkv, D)
+    ws.fill_(0xFF)   # a stale workspace must not matter
+    pkv.paged_decode(q, kc, vc, bt, lens, scale, out, ws, max_context_len=max_ctx, num_workers=num_workers,
+                     err_word=err)
+    return out
+
+
+def oracle_slots(wl):
+    s = oracle.decode_slot_mapping(wl.block_tables.cpu().numpy(), wl.context_lens.cpu().numpy(),
+                                   wl.spec.block_size, wl.num_tokens)
+    for t in wl.skip_tokens:
+        s[t] = -1
+    return s
+
+
+# --------------------------------------------------------------------------- the five workloads
+@pytest.mark.parametrize("name", W.ORDER)
+def test_slot_mapping_bit_exact(name):
+    wl = W.make(name, "cuda", layers=1)
+    err = err_word()
+    got = torch.full((wl.num_tokens,), 7, dtype=torch.int32, device="cuda")
+    pkv.decode_slot_mapping(wl.block_tables, wl.context_lens, wl.spec.block_size, wl.num_blocks, got, err)
+    want = oracle.decode_slot_mapping(wl.block_tables.cpu().numpy(), wl.context_lens.cpu().numpy(),
+                                      wl.spec.block_size, wl.num_tokens)
+    assert np.array_equal(got.cpu().numpy(), want)
+    assert err.item() == 0
+
+
+@pytest.mark.parametrize("name", W.ORDER)
+def test_store_then_decode(name):
+    """One decode step per layer: kv_store (bit-exact over the whole pool) then paged_decode."""
+    layers = None
+    check_layers = None
+    if name == "full_depth":
+        layers, check_layers = 3, {0, 2}
+    wl = W.make(name, "cuda", layers=layers)
+    s = wl.spec
+    bt_h, lens_h = wl.block_tables.cpu().numpy(), wl.context_lens.cpu().numpy()
+    slots_h = oracle_slots(wl)
+    slots = torch.from_numpy(slots_h).cuda()
+    err = err_word()
+    ws = pkv.alloc_workspace(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim)
+    for li, lay in enumerate(wl.layers):
+        kc_h, vc_h = W.bits(lay.k_cache), W.bits(lay.v_cache)
+        pkv.kv_store(lay.k_new, lay.v_new, slots, lay.k_cache, lay.v_cache, err)
+        out = torch.empty_like(lay.q)
+        pkv.paged_decode(lay.q, lay.k_cache, lay.v_cache, wl.block_tables, wl.context_lens, wl.scale, out, ws,
+                         max_context_len=int(lens_h.max()), err_word=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0, hex(err.item())
+        if check_layers is not None and li not in check_layers:
+            continue
+        oracle.kv_store(W.bits(lay.k_new), W.bits(lay.v_new), slots_h, kc_h, vc_h)
+        assert np.array_equal(W.bits(lay.k_cache), kc_h), "k_cache differs from the oracle store"
+        assert np.array_equal(W.bits(lay.v_cache), vc_h), "v_cache differs from the oracle store"
+        want = oracle.paged_decode(W.bits(lay.q), kc_h, vc_h, bt_h, lens_h, wl.scale, nthreads=NTHREADS)
+        check_close(out, want, f"{name} layer {li}")
+        del kc_h, vc_h
+
+
+# --------------------------------------------------------------------------- mini-vLLM-style matrix
+def synth(B, L, Hq, Hkv, D, bs, seed, lens=None, extra=5):
+    """Random paged problem with a shuffled pool and NaN canaries in unowned rows."""
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    rng = np.random.default_rng(seed)
+    lens = np.full(B, L, np.int64) if lens is None else np.asarray(lens, np.int64)
+    nblk = [-(-int(x) // bs) for x in lens]
+    NB = sum(nblk) + extra
+    perm = rng.permutation(NB)
+    mb = max(max(nblk), 1)
+    bt = np.full((B, mb), -1, np.int32)
+    cur = 0
+    filled = np.zeros(NB, np.int64)
+    for b in range(B):
+        for i in range(nblk[b]):
+            bt[b, i] = perm[cur]
+            filled[perm[cur]] = min(bs, int(lens[b]) - i * bs)
+            cur += 1
+    kc = torch.randn(NB, bs, Hkv, D, generator=g, device="cuda").bfloat16()
+    vc = torch.randn(NB, bs, Hkv, D, generator=g, device="cuda").bfloat16()
+    canary = torch.arange(bs, device="cuda").view(1, bs) >= torch.as_tensor(filled, device="cuda").view(NB, 1)
+    kc[canary] = float("nan")
+    vc[canary] = float("nan")
+    q = torch.randn(B, Hq, D, generator=g, device="cuda").bfloat16()
+    return q, kc, vc, torch.from_numpy(bt).cuda(), torch.from_numpy(lens.astype(np.int32)).cuda()
+
+
+def oracle_of(q, kc, vc, bt, lens, scale):
+    return oracle.paged_decode(W.bits(q), W.bits(kc), W.bits(vc), bt.cpu().numpy(), lens.cpu().numpy(), scale,
+                               nthreads=NTHREADS)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("heads", [(8, 2), (16, 4)])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("B", [1, 4, 16])
+def test_kernel_matrix(B, bs, heads, D):
+    Hq, Hkv = heads
+    for L in (1, 15, 16, 17, 128, 511, 1024):
+        q, kc, vc, bt, lens = synth(B, L, Hq, Hkv, D, bs, seed=B * 100000 + bs * 1000 + Hq * 10 + L + D)
+        scale = 1 / math.sqrt(D)
+        err = err_word()
+        out = run_decode(q, kc, vc, bt, lens, scale, err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        check_close(out, oracle_of(q, kc, vc, bt, lens, scale), f"B{B} L{L} bs{bs} {Hq}/{Hkv} D{D}")
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("D", [64, 128])
+def test_every_group_size(G, D):
+    Hkv = 2
+    lens = [1, 5, 16, 33, 200, 77]
+    q, kc, vc, bt, lens_t = synth(len(lens), 0, G * Hkv, Hkv, D, 16, seed=G * 7 + D, lens=lens)
+    out = run_decode(q, kc, vc, bt, lens_t, 0.1)
+    check_close(out, oracle_of(q, kc, vc, bt, lens_t, 0.1), f"G{G} D{D}")
+
+
+@pytest.mark.parametrize("workers", [1, 2, 3, 7, 64, 333, 4096])
+def test_forced_splits(workers):
+    """Spread the same batch over very different worker counts: exercises the split-K merge."""
+    lens = [1, 15, 17, 40, 300, 0, 1024, 2, 513]
+    q, kc, vc, bt, lens_t = synth(len(lens), 0, 16, 8, 128, 16, seed=workers, lens=lens)
+    want = oracle_of(q, kc, vc, bt, lens_t, 0.0884)
+    out = run_decode(q, kc, vc, bt, lens_t, 0.0884, num_workers=workers)
+    check_close(out, want, f"workers {workers}")
+    assert torch.all(out[lens.index(0)].float() == 0)
+
+
+def test_workers_do_not_change_results_much():
+    lens = [700, 1500, 33]
+    q, kc, vc, bt, lens_t = synth(len(lens), 0, 16, 8, 128, 256, seed=5, lens=lens)
+    a = run_decode(q, kc, vc, bt, lens_t, 0.0884, num_workers=1).float()
+    b = run_decode(q, kc, vc, bt, lens_t, 0.0884, num_workers=500).float()
+    assert (a - b).abs().max().item() <= 2e-2
+
+
+# --------------------------------------------------------------------------- closed forms on the GPU
+def test_worked_example_on_gpu():
+    """Lab manual appendix B.1.2 example, zero-padded to D=64, scattered through a shuffled table."""
+    D = 64
+    q = torch.zeros(1, 2, D); q[0, :, :2] = torch.tensor([1.0, 1.0])
+    k = torch.zeros(3, 1, D); k[:, 0, :2] = torch.tensor([[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]])
+    v = torch.zeros(3, 1, D); v[:, 0, :2] = torch.tensor([[1.0, 0.0], [0.0, 2.0], [1.0, 2.0]])
+    NB, bs = 6, 8
+    kc = torch.full((NB, bs, 1, D), float("nan")); vc = kc.clone()
+    kc[4, :3] = k; vc[4, :3] = v
+    bt = torch.tensor([[4]], dtype=torch.int32)
+    out = run_decode(q.bfloat16().cuda(), kc.bfloat16().cuda(), vc.bfloat16().cuda(), bt.cuda(),
+                     torch.tensor([3], dtype=torch.int32).cuda(), 1 / math.sqrt(2))
+    o = out.float().cpu()
+    for h in range(2):
+        assert abs(o[0, h, 0].item() - 0.75174492) < 4e-3   # bf16 output rounding
+        assert abs(o[0, h, 1].item() - 1.50348984) < 8e-3
+        assert torch.all(o[0, h, 2:] == 0)
+
+
+def test_context_one_returns_v_row_exactly():
+    q, kc, vc, bt, lens = synth(5, 1, 16, 8, 128, 16, seed=3)
+    out = run_decode(q, kc, vc, bt, lens, 0.0884)
+    for b in range(5):
+        p = bt[b, 0].item()
+        want = vc[p, 0].repeat_interleave(2, dim=0)
+        assert torch.equal(out[b].view(torch.int16), want.view(torch.int16))
+
+
+def test_uniform_v_gives_v():
+    q, kc, vc, bt, lens = synth(3, 300, 8, 2, 64, 16, seed=4)
+    row = torch.randn(2, 64, device="cuda").bfloat16()
+    vc[:] = row
+    out = run_decode(q, kc, vc, bt, lens, 0.125)
+    want = row.float().repeat_interleave(4, dim=0)
+    assert (out.float() - want).abs().max().item() <= 1e-2
+
+
+def test_shared_prefix_equals_duplicated_blocks():
+    lens = [100, 120]
+    q, kc, vc, bt, lens_t = synth(2, 0, 16, 8, 128, 16, seed=6, lens=lens)
+    # make seq 1's first 3 blocks copies of seq 0's, then point its table at seq 0's blocks
+    for i in range(3):
+        kc[bt[1, i]] = kc[bt[0, i]]
+        vc[bt[1, i]] = vc[bt[0, i]]
+    dup = run_decode(q, kc, vc, bt, lens_t, 0.0884)
+    bt2 = bt.clone()
+    bt2[1, :3] = bt[0, :3]
+    shared = run_decode(q, kc, vc, bt2, lens_t, 0.0884)
+    assert torch.equal(dup.view(torch.int16), shared.view(torch.int16))
+
+
+def test_zero_and_padding_rows():
+    lens = [0, 5, 0]
+    q, kc, vc, bt, lens_t = synth(3, 0, 8, 2, 64, 16, seed=9, lens=lens)
+    out = run_decode(q, kc, vc, bt, lens_t, 0.125)
+    assert torch.all(out[0].float() == 0) and torch.all(out[2].float() == 0)
+    check_close(out, oracle_of(q, kc, vc, bt, lens_t, 0.125), "zero rows")
+
+
+# --------------------------------------------------------------------------- device-side range errors
+def test_bad_slot_sets_error_and_writes_nothing_else():
+    NB, bs, Hkv, D = 8, 16, 2, 64
+    kc = torch.randn(NB, bs, Hkv, D, device="cuda").bfloat16(); vc = torch.randn_like(kc)
+    k = torch.randn(3, Hkv, D, device="cuda").bfloat16(); v = torch.randn_like(k)
+    before_k, before_v = kc.clone(), vc.clone()
+    slots = torch.tensor([NB * bs, -1, -7], dtype=torch.int32, device="cuda")
+    err = err_word()
+    pkv.kv_store(k, v, slots, kc, vc, err)
+    torch.cuda.synchronize()
+    assert err.item() & pkv.ERR_SLOT_RANGE
+    assert torch.equal(kc, before_k) and torch.equal(vc, before_v)
+
+
+def test_bad_block_id_sets_error_without_fault():
+    q, kc, vc, bt, lens = synth(2, 40, 8, 2, 64, 16, seed=10)
+    bt[1, 1] = kc.shape[0] + 100
+    err = err_word()
+    run_decode(q, kc, vc, bt, lens, 0.125, err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pkv.ERR_BLOCK_RANGE
+    # the context is still healthy
+    bt[1, 1] = bt[0, 0]
+    run_decode(q, kc, vc, bt, lens, 0.125)
+    torch.cuda.synchronize()
+
+
+def test_context_beyond_limit_sets_error_and_zeros():
+    q, kc, vc, bt, lens = synth(2, 40, 8, 2, 64, 16, seed=11)
+    err = err_word()
+    out = run_decode(q, kc, vc, bt, lens, 0.125, max_ctx=39, err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pkv.ERR_CONTEXT_RANGE
+    assert torch.all(out.float() == 0)
+
+
+def test_slot_mapping_range_errors():
+    bt = torch.tensor([[3, -1], [99, 1]], dtype=torch.int32, device="cuda")
+    lens = torch.tensor([40, 3], dtype=torch.int32, device="cuda")
+    slots = torch.empty(2, dtype=torch.int32, device="cuda")
+    err = err_word()
+    pkv.decode_slot_mapping(bt, lens, 16, 10, slots, err)
+    torch.cuda.synchronize()
+    assert slots.tolist() == [-1, -1]
+    assert err.item() & pkv.ERR_CONTEXT_RANGE and err.item() & pkv.ERR_BLOCK_RANGE
