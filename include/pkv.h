@@ -175,6 +175,41 @@ pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cache, const ui
                             float scale, uint16_t *out, void *workspace, size_t workspace_bytes,
                             int32_t num_workers, int32_t *err_word, pkv_stream_t stream);
 
+/*
+ * pkv_paged_decode_noalloc -- pkv_paged_decode for callers that cannot
+ * allocate device memory.  (The pages have no counterpart of this call; it
+ * exists for callers of this library.)
+ *
+ * Who needs it: an engine that handed (nearly) all free device memory to its
+ * KV block pool at start-up and has nothing left for a workspace, or a host
+ * framework whose plugin interface passes only inputs and outputs and forbids
+ * device allocations while it runs.  This call takes the same arguments as
+ * pkv_paged_decode minus the workspace and computes the same result; its
+ * scratch is a fixed array of PKV_NOALLOC_SCRATCH_BYTES inside the library,
+ * which every device that loads the library holds until the process exits.
+ * It allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ *
+ *   - Sizes whose workspace (pkv_paged_decode_workspace_size) exceeds
+ *     PKV_NOALLOC_SCRATCH_BYTES are rejected with PKV_EWORKSPACE before any
+ *     device work; everything else is validated as in pkv_paged_decode.
+ *   - The first call on a device looks up the array's device address (once,
+ *     with that device current); make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one array, and the array keeps
+ *     whatever the last call left in it (nothing in it needs to start at
+ *     zero).  Calls that overlap on the GPU -- on different streams, or from
+ *     different threads -- race on it: serialise them.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+pkv_status pkv_paged_decode_noalloc(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t *context_lens, int32_t num_seqs,
+                                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+                                    float scale, uint16_t *out, int32_t num_workers,
+                                    int32_t *err_word, pkv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

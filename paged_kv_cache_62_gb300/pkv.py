@@ -30,7 +30,10 @@ SIGNATURES = {
     "pkv_paged_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "pkv_paged_decode": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                                         _F32, _P, _P, _SZ, _I32, _P, _P]),
+    "pkv_paged_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                                                _I32, _F32, _P, _I32, _P, _P]),
 }
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 _lib = None
 
@@ -146,3 +149,29 @@ def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, 
         _dev(context_lens, torch.int32, "context_lens", 1), B, Hq, Hkv, D, bs, NB, int(max_context_len),
         float(scale), _dev(out, torch.bfloat16, "out", 3), workspace.data_ptr(), workspace.numel(),
         int(num_workers), _opt(err_word), _stream(stream)), "pkv_paged_decode")
+
+
+def paged_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                         context_lens: torch.Tensor, scale: float, out: torch.Tensor,
+                         max_context_len: int | None = None, num_workers: int = 0,
+                         err_word: torch.Tensor | None = None, stream=None) -> None:
+    """paged_decode without a caller workspace: the library's fixed per-device scratch is used.
+
+    For callers that cannot allocate device memory.  Calls that overlap on the
+    GPU share that scratch and race; the first call on a device should come
+    before any stream capture.
+    """
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape or block_tables.shape[0] != B or context_lens.numel() != B \
+            or out.shape != q.shape:
+        raise ValueError("paged_decode_noalloc: shape mismatch")
+    mb = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = mb * bs
+    _check(load().pkv_paged_decode_noalloc(
+        _dev(q, torch.bfloat16, "q", 3), _dev(k_cache, torch.bfloat16, "k_cache", 4),
+        _dev(v_cache, torch.bfloat16, "v_cache", 4), _dev(block_tables, torch.int32, "block_tables", 2), mb,
+        _dev(context_lens, torch.int32, "context_lens", 1), B, Hq, Hkv, D, bs, NB, int(max_context_len),
+        float(scale), _dev(out, torch.bfloat16, "out", 3), int(num_workers), _opt(err_word), _stream(stream)),
+        "pkv_paged_decode_noalloc")
