@@ -36,8 +36,8 @@
 namespace pkv {
 
 constexpr int kTile = 16;      // tokens per tile
-constexpr int kMaxWarps = 8;   // warps per CTA (one CTA per SM)
-constexpr int kStages = 3;     // ring depth per warp
+constexpr int kMaxWarps = 12;  // warps per CTA (one CTA per SM) for small groups
+constexpr int kStages = 2;     // ring depth per warp
 
 struct DecodeParams {
     const uint16_t *q;
@@ -66,6 +66,9 @@ struct Shape {
     static constexpr int Q_BYTES = G * D * 2;
     static constexpr int STAGE_BYTES = (2 * KV_BYTES + Q_BYTES + 127) / 128 * 128;
     static_assert(LPT >= NIT && DUP >= 1, "tile too large for the lane split");
+    // Warps per CTA: as many as the register file allows without spilling
+    // (one CTA of WARPS*32 threads per SM, so at most 65536 / (WARPS*32) registers each).
+    static constexpr int WARPS = (G <= 4 || (D == 64 && G <= 5)) ? kMaxWarps : 8;
 };
 
 struct WsLayout {
@@ -187,9 +190,24 @@ __device__ void tile_prefix_scan(const DecodeParams &p, int32_t *scan, int32_t *
 }
 
 // ------------------------------------------------------------------ one tile
+// Slack (log2 units) a score may exceed the running max before the running
+// state is rescaled: weights stay <= 2^kRescaleSlack, which fp32 holds with
+// ample room, and most tiles skip the warp max and the rescale entirely.
+constexpr float kRescaleSlack = 8.0f;
+
+__device__ __forceinline__ void unpack8x2(const uint4 w, float2 f[4])
+{
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = make_float2(__uint_as_float(u[i] << 16), __uint_as_float(u[i] & 0xffff0000u));
+}
+
+// One 16-token tile of one (sequence, kv head) for the G query heads of the group.
+// Element pairs are handled with the packed fp32 FMA (two independent
+// round-to-nearest fp32 FMAs per instruction).
 template <int D, int G>
-__device__ __forceinline__ void attend_tile(const uint8_t *st, int valid, const float (&qf)[G][8], float (&m)[G],
-                                            float (&l)[G], float (&acc)[G][8], int c, int grp)
+__device__ __forceinline__ void attend_tile(const uint8_t *st, int valid, const float2 (&q2)[G][4], float (&m)[G],
+                                            float (&l)[G], float2 (&acc)[G][4], int c, int grp)
 {
     using S = Shape<D, G>;
     constexpr int LPT = S::LPT, TPI = S::TPI, NIT = S::NIT, DUP = S::DUP;
@@ -201,15 +219,14 @@ __device__ __forceinline__ void attend_tile(const uint8_t *st, int valid, const 
 #pragma unroll
     for (int i = 0; i < NIT; ++i) {
         const int tok = i * TPI + grp;
-        const uint4 kw = *reinterpret_cast<const uint4 *>(Ks + tok * D + c * 8);
-        float kf[8];
-        unpack8(kw, kf);
+        float2 k2[4];
+        unpack8x2(*reinterpret_cast<const uint4 *>(Ks + tok * D + c * 8), k2);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            float s = 0.f;
+            float2 a = __fmul2_rn(q2[h][0], k2[0]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) s = fmaf(qf[h][e], kf[e], s);
-            part[h][i] = s;
+            for (int j = 1; j < 4; ++j) a = __ffma2_rn(q2[h][j], k2[j], a);
+            part[h][i] = a.x + a.y;
         }
     }
     // reduce-scatter over the LPT lanes of a token: afterwards lane c holds the
@@ -238,13 +255,20 @@ __device__ __forceinline__ void attend_tile(const uint8_t *st, int valid, const 
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         const float s = ok ? part[h][0] : -INFINITY;
-        const float mn = fmaxf(m[h], warp_max(s));  // finite: every tile holds a valid token
-        const float alpha = ex2(m[h] - mn);         // 0 on the first tile (m = -inf)
-        pr[h] = ok ? ex2(s - mn) : 0.f;
-        l[h] = l[h] * alpha + pr[h];
+        // Online softmax (m, l, acc).  The running max only moves when some
+        // score passes it by more than the slack; the first tile always moves it
+        // (m = -inf, and every tile holds at least one valid token).
+        if (__any_sync(kFull, s > m[h] + kRescaleSlack)) {
+            const float mn = fmaxf(m[h], warp_max(s));
+            const float alpha = ex2(m[h] - mn);  // 0 on the first tile
+            l[h] *= alpha;
+            const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[h][e] *= alpha;
-        m[h] = mn;
+            for (int j = 0; j < 4; ++j) acc[h][j] = __fmul2_rn(acc[h][j], a2);
+            m[h] = mn;
+        }
+        pr[h] = ok ? ex2(s - m[h]) : 0.f;
+        l[h] += pr[h];
     }
     // P.V: the weight of token i*TPI + grp sits in lane grp*LPT + i*DUP
 #pragma unroll
@@ -254,20 +278,21 @@ __device__ __forceinline__ void attend_tile(const uint8_t *st, int valid, const 
 #pragma unroll
         for (int h = 0; h < G; ++h) ph[h] = __shfl_sync(kFull, pr[h], grp * LPT + i * DUP);
         if (tok < valid) {  // rows past L may hold anything, even NaN: never touch them
-            const uint4 vw = *reinterpret_cast<const uint4 *>(Vs + tok * D + c * 8);
-            float vf[8];
-            unpack8(vw, vf);
+            float2 v2[4];
+            unpack8x2(*reinterpret_cast<const uint4 *>(Vs + tok * D + c * 8), v2);
 #pragma unroll
-            for (int h = 0; h < G; ++h)
+            for (int h = 0; h < G; ++h) {
+                const float2 p2 = make_float2(ph[h], ph[h]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(ph[h], vf[e], acc[h][e]);
+                for (int j = 0; j < 4; ++j) acc[h][j] = __ffma2_rn(p2, v2[j], acc[h][j]);
+            }
         }
     }
 }
 
 // ------------------------------------------------------------------ main kernel
 template <int D, int G>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1)
+__global__ void __launch_bounds__(Shape<D, G>::WARPS * 32, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeParams p)
 {
@@ -291,6 +316,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
     }
+    griddep_launch_dependents();  // lets the merge kernel get scheduled; it waits for this grid
+    griddep_wait();               // inputs may come from the previous kernel in the stream
     tile_prefix_scan(p, scan, reinterpret_cast<int32_t *>(smem));
 
     const int64_t T = int64_t(p.Hkv) * scan[p.B];
@@ -378,7 +405,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     const int prologue = ntiles < kStages ? ntiles : kStages;
     for (int k = 0; k < prologue; ++k) issue(k, k);
 
-    float qf[G][8], m[G], l[G], acc[G][8];
+    float2 q2[G][4], acc[G][4];
+    float m[G], l[G];
     bool open = false;
     int32_t seg_t0 = 0;
     int k = 0;
@@ -396,19 +424,20 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             const uint16_t *qs = reinterpret_cast<const uint16_t *>(st + 2 * S::KV_BYTES);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                float f[8];
-                unpack8(*reinterpret_cast<const uint4 *>(qs + h * D + c * 8), f);
+                float2 f[4];
+                unpack8x2(*reinterpret_cast<const uint4 *>(qs + h * D + c * 8), f);
+                const float2 sc = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    qf[h][e] = f[e] * p.scale_log2;
-                    acc[h][e] = 0.f;
+                for (int j = 0; j < 4; ++j) {
+                    q2[h][j] = __fmul2_rn(f[j], sc);
+                    acc[h][j] = make_float2(0.f, 0.f);
                 }
                 m[h] = -INFINITY;
                 l[h] = 0.f;
             }
         }
         const int valid = min(kTile, mt.L - mt.t * kTile);
-        attend_tile<D, G>(st, valid, qf, m, l, acc, c, grp);
+        attend_tile<D, G>(st, valid, q2, m, l, acc, c, grp);
         __syncwarp();
         if (k + kStages < ntiles) issue(k + kStages, s);
 
@@ -419,7 +448,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 #pragma unroll
                 for (int h = 0; h < G; ++h)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[h][e] += __shfl_xor_sync(kFull, acc[h][e], mask);
+                    for (int j = 0; j < 4; ++j) {
+                        acc[h][j].x += __shfl_xor_sync(kFull, acc[h][j].x, mask);
+                        acc[h][j].y += __shfl_xor_sync(kFull, acc[h][j].y, mask);
+                    }
             float lt[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) lt[h] = warp_sum(l[h]) * (1.0f / DUP);
@@ -429,10 +461,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
                     for (int h = 0; h < G; ++h) {
                         const float inv = 1.0f / lt[h];
                         uint4 o;
-                        o.x = pack_bf16x2(acc[h][0] * inv, acc[h][1] * inv);
-                        o.y = pack_bf16x2(acc[h][2] * inv, acc[h][3] * inv);
-                        o.z = pack_bf16x2(acc[h][4] * inv, acc[h][5] * inv);
-                        o.w = pack_bf16x2(acc[h][6] * inv, acc[h][7] * inv);
+                        o.x = pack_bf16x2(acc[h][0].x * inv, acc[h][0].y * inv);
+                        o.y = pack_bf16x2(acc[h][1].x * inv, acc[h][1].y * inv);
+                        o.z = pack_bf16x2(acc[h][2].x * inv, acc[h][2].y * inv);
+                        o.w = pack_bf16x2(acc[h][3].x * inv, acc[h][3].y * inv);
                         *reinterpret_cast<uint4 *>(p.out + (int64_t(mt.b) * p.Hq + int64_t(mt.g) * G + h) * D +
                                                    c * 8) = o;
                     }
@@ -443,8 +475,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 #pragma unroll
                     for (int h = 0; h < G; ++h) {
                         float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + ((slot * G + h) * D + c * 8));
-                        dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-                        dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
+                        dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
+                        dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
                     }
                 }
                 if (lane == 0)
@@ -468,6 +500,8 @@ template <int D, int G>
 __global__ void __launch_bounds__(G * D / 4)
     paged_decode_merge_kernel(const DecodeParams p)
 {
+    griddep_launch_dependents();
+    griddep_wait();  // the main kernel's partials and prefix
     const int bg = blockIdx.x;
     const int b = bg / p.Hkv, g = bg - b * p.Hkv;
     const int h = threadIdx.x / (D / 4), c4 = threadIdx.x % (D / 4);
@@ -533,7 +567,7 @@ size_t decode_smem_bytes(int nwarps, int B)
 template <int D, int G>
 pkv_status launch_decode(LaunchArgs &a)
 {
-    int nwarps = kMaxWarps;
+    int nwarps = Shape<D, G>::WARPS;
     while (nwarps > 1 && decode_smem_bytes<D, G>(nwarps, a.p.B) > size_t(a.max_smem)) --nwarps;
     const size_t smem = decode_smem_bytes<D, G>(nwarps, a.p.B);
     if (smem > size_t(a.max_smem)) return PKV_EUNSUPPORTED;
@@ -555,9 +589,15 @@ pkv_status launch_decode(LaunchArgs &a)
         cudaGetLastError();
         return PKV_ECUDA;
     }
-    kern<<<grid, nwarps * 32, smem, a.stream>>>(kmap, vmap, a.p);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ECUDA;
-    paged_decode_merge_kernel<D, G><<<a.p.B * a.p.Hkv, G * D / 4, 0, a.stream>>>(a.p);
+    if (launch_pdl(kern, dim3(grid), dim3(nwarps * 32), smem, a.stream, kmap, vmap, a.p) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ECUDA;
+    }
+    if (launch_pdl(paged_decode_merge_kernel<D, G>, dim3(a.p.B * a.p.Hkv), dim3(G * D / 4), 0, a.stream, a.p) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ECUDA;
+    }
     return launch_status();
 }
 

@@ -83,6 +83,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return __all_sync(kFull, ok);
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every pkv kernel is launched with programmatic stream serialization: it may
+// start while the previous kernel in the stream is still running, so it calls
+// griddep_wait() before its first global-memory access (that waits for the
+// previous grid to complete and its writes to be visible), and it calls
+// griddep_launch_dependents() early so the next kernel can be scheduled.
+// Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 // 3-D tiled tensor copy global -> shared, completion counted on `bar`.
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int32_t c0, int32_t c1,

@@ -21,6 +21,8 @@ __global__ void decode_slot_mapping_kernel(const int32_t *__restrict__ block_tab
                                            int32_t *__restrict__ slot_mapping, int32_t num_tokens,
                                            int32_t *err)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     const int32_t t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= num_tokens) return;
     int32_t slot = -1;
@@ -49,6 +51,8 @@ __global__ void kv_store_kernel(const uint4 *__restrict__ k, const uint4 *__rest
                                 const int32_t *__restrict__ slot_mapping, uint4 *__restrict__ k_cache,
                                 uint4 *__restrict__ v_cache, int64_t num_slots, int32_t row_vecs, int32_t *err)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     const int32_t t = blockIdx.x;
     const int64_t s = __ldg(slot_mapping + t);
     if (s == -1) return;
@@ -83,9 +87,12 @@ extern "C" pkv_status pkv_decode_slot_mapping(const int32_t *block_tables, int32
     if (!slot_mapping || (num_seqs > 0 && (!block_tables || !context_lens))) return PKV_EINVAL;
     const int threads = 128;
     const int blocks = (num_tokens + threads - 1) / threads;
-    decode_slot_mapping_kernel<<<blocks, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        block_tables, max_blocks_per_seq, context_lens, num_seqs, block_size, ilog2(block_size), num_blocks,
-        slot_mapping, num_tokens, err_word);
+    if (launch_pdl(decode_slot_mapping_kernel, dim3(blocks), dim3(threads), 0, reinterpret_cast<cudaStream_t>(stream),
+                   block_tables, max_blocks_per_seq, context_lens, num_seqs, block_size, ilog2(block_size),
+                   num_blocks, slot_mapping, num_tokens, err_word) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ECUDA;
+    }
     return launch_status();
 }
 
@@ -103,9 +110,12 @@ extern "C" pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, const i
     if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
     const int32_t row_vecs = static_cast<int32_t>(row_bytes / 16);
     const int threads = row_vecs >= 256 ? 256 : ((row_vecs + 31) / 32) * 32;
-    kv_store_kernel<<<num_tokens, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v), slot_mapping,
-        reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache),
-        static_cast<int64_t>(num_blocks) * block_size, row_vecs, err_word);
+    if (launch_pdl(kv_store_kernel, dim3(num_tokens), dim3(threads), 0, reinterpret_cast<cudaStream_t>(stream),
+                   reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v), slot_mapping,
+                   reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache),
+                   static_cast<int64_t>(num_blocks) * block_size, row_vecs, err_word) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ECUDA;
+    }
     return launch_status();
 }
