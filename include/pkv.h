@@ -117,10 +117,12 @@ pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, const int32_t *slo
 
 /*
  * Bytes of device workspace that pkv_paged_decode needs for these sizes
- * (split-K partial states plus a small header).  Depends only on the
- * arguments; 0 means the sizes are invalid.  The workspace needs no
- * initialisation and holds nothing between calls; calls that may run at the
- * same time need separate workspaces.
+ * (split-K partial states plus one arrival counter per (sequence, kv head)).
+ * Depends only on the arguments; 0 means the sizes are invalid.  The
+ * workspace needs no initialisation: counters are tagged with a per-call
+ * generation, so leftovers from earlier calls (or garbage) count as zero, and
+ * a completed call leaves them at zero.  Calls that may run at the same time
+ * need separate workspaces.
  */
 size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                        int32_t num_kv_heads, int32_t head_dim);
@@ -165,7 +167,10 @@ size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
  * num_blocks * block_size < 2^31.
  * Work is split evenly over the workers by 16-token tiles, so one sequence
  * may be spread over several workers; their partial softmax states are
- * merged by a second kernel (split-K / flash-decoding).
+ * merged in the same kernel by the worker that finishes last (split-K /
+ * flash-decoding).  Each kernel is launched with programmatic stream
+ * serialization and waits on the device for the previous kernel in the stream
+ * before it reads any input.
  */
 pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                             const int32_t *block_tables, int32_t max_blocks_per_seq,

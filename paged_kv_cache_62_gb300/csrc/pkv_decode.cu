@@ -25,9 +25,12 @@
 //    warp max, exponentials are ex2 on log2e-prescaled scores, and P.V uses
 //    the same lane split with fp32 accumulators.
 //  * A warp whose tile range covers a whole (b, g) writes bf16 output
-//    directly; otherwise it leaves its (m, l, acc) in the workspace and the
-//    merge kernel combines the pieces (split-K / flash-decoding).
+//    directly; otherwise it leaves its (m, l, acc) in the workspace and counts
+//    itself in on a per-(b, g) counter; the warp that brings in the last piece
+//    merges them all (split-K / flash-decoding without a second kernel).
 #include <algorithm>
+#include <atomic>
+#include <type_traits>
 #include <cmath>
 
 #include "pkv_device.cuh"
@@ -44,12 +47,13 @@ struct DecodeParams {
     const int32_t *block_tables;
     const int32_t *context_lens;
     uint16_t *out;
-    int32_t *ws_prefix;  // [B + 1] tile prefix (written by CTA 0, read by the merge)
+    unsigned long long *ws_count;  // [B * Hkv] arrival counters: (call generation << 32) | pieces arrived
     float *ws_ml;        // [slots][G][2] (m, l) per partial
     float *ws_acc;       // [slots][G][D] unnormalised accumulators
     int32_t *err;
     int32_t B, Hq, Hkv, bs, log2_bs, NB, max_blocks, len_limit, num_workers;
     float scale_log2;    // scale * log2(e)
+    uint32_t gen;        // generation of this call (tags the arrival counters)
 };
 
 struct alignas(16) StageMeta {
@@ -72,7 +76,7 @@ struct Shape {
 };
 
 struct WsLayout {
-    size_t prefix_off, ml_off, acc_off, total;
+    size_t count_off, ml_off, acc_off, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -81,8 +85,8 @@ inline WsLayout ws_layout(int32_t B, int32_t G, int32_t Hkv, int32_t D)
 {
     const size_t slots = size_t(PKV_MAX_WORKERS) + size_t(B) * size_t(Hkv);
     WsLayout w;
-    w.prefix_off = 0;
-    w.ml_off = align256(size_t(B + 1) * 4);
+    w.count_off = 0;
+    w.ml_off = align256(size_t(B) * size_t(Hkv) * 8);
     w.acc_off = w.ml_off + align256(slots * size_t(G) * 2 * 4);
     w.total = w.acc_off + slots * size_t(G) * size_t(D) * 4;
     return w;
@@ -138,7 +142,7 @@ __device__ __forceinline__ void table_lookup(const DecodeParams &p, const Walker
     len = __ldg(p.context_lens + w.b);
 }
 
-// Tiles per sequence -> exclusive prefix in scan[0..B]; CTA 0 also publishes it.
+// Tiles per sequence -> exclusive prefix in scan[0..B].
 // `tmp` needs 32 ints of shared memory that is free during the call.
 __device__ void tile_prefix_scan(const DecodeParams &p, int32_t *scan, int32_t *tmp)
 {
@@ -185,8 +189,6 @@ __device__ void tile_prefix_scan(const DecodeParams &p, int32_t *scan, int32_t *
     }
     if (lo < hi && hi == p.B) scan[p.B] = run;
     __syncthreads();
-    if (blockIdx.x == 0)
-        for (int i = tid; i <= p.B; i += nt) p.ws_prefix[i] = scan[i];
 }
 
 // ------------------------------------------------------------------ one tile
@@ -290,6 +292,95 @@ __device__ __forceinline__ void attend_tile(const uint8_t *st, int valid, const 
     }
 }
 
+// ------------------------------------------------------------------ split-K merge (a6)
+// Count one more piece of (b, g) in.  The counter word is (call generation << 32)
+// | pieces; a word from another call (other generation, or leftover garbage)
+// counts as zero, so the workspace never needs clearing.  Returns 1 for the
+// piece that completes the set (and resets the word to 0 for the next call).
+__device__ __forceinline__ int arrive_last(unsigned long long *ctr, uint32_t gen, uint32_t pieces, int32_t *err)
+{
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(ctr);
+    for (int it = 0; it < (1 << 20); ++it) {
+        const uint32_t n = (uint32_t(cur >> 32) == gen) ? uint32_t(cur) + 1u : 1u;
+        const unsigned long long next = (static_cast<unsigned long long>(gen) << 32) | n;
+        const unsigned long long seen = atomicCAS(ctr, cur, next);
+        if (seen == cur) {
+            if (n != pieces) return 0;
+            atomicExch(ctr, 0ull);
+            return 1;
+        }
+        cur = seen;
+    }
+    flag_error(err, PKV_ERR_WAIT_TIMEOUT);  // unreachable in practice: a handful of warps contend
+    return 0;
+}
+
+// Merge the partial states of workers wf..wl for (b, g):
+//   M = max m_i,  l = sum 2^(m_i - M) l_i,  out = sum 2^(m_i - M) acc_i / l
+// (the online-softmax algebra; m in log2 units).  The pieces were written by
+// other SMs, so they are read through L2 (ld.global.cg), BATCH pieces at a
+// time with independent loads, folded into a running (M, l, acc).
+template <int D, int G>
+__device__ __forceinline__ void merge_pieces(const DecodeParams &p, int64_t bg, int64_t wf, int64_t wl, int b, int g,
+                                             int lane)
+{
+    constexpr int PER = D / 32;                               // output values per lane
+    constexpr int BATCH = G <= 2 ? 4 : (G <= 4 ? 2 : 1);      // pieces loaded together
+    using Vec = typename std::conditional<PER == 4, float4, float2>::type;
+    const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);
+    float M[G], lsum[G], a[G][PER];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        M[h] = -INFINITY;
+        lsum[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) a[h][e] = 0.f;
+    }
+    for (int64_t w0 = wf; w0 <= wl; w0 += BATCH) {
+        float2 st[BATCH][G];
+        Vec v[BATCH][G];
+#pragma unroll
+        for (int k = 0; k < BATCH; ++k) {
+            const int64_t slot = (w0 + k <= wl ? w0 + k : wl) + bg;  // clamp: a repeated piece gets weight 0 below
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                st[k][h] = __ldcg(ml + slot * G + h);
+                v[k][h] = __ldcg(reinterpret_cast<const Vec *>(p.ws_acc + (slot * G + h) * D + lane * PER));
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float mb = M[h];
+#pragma unroll
+            for (int k = 0; k < BATCH; ++k)
+                if (w0 + k <= wl) mb = fmaxf(mb, st[k][h].x);
+            const float r = ex2(M[h] - mb);  // 0 while nothing has been folded in (M = -inf)
+            lsum[h] *= r;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) a[h][e] *= r;
+#pragma unroll
+            for (int k = 0; k < BATCH; ++k) {
+                const float f = (w0 + k <= wl) ? ex2(st[k][h].x - mb) : 0.f;
+                lsum[h] = fmaf(f, st[k][h].y, lsum[h]);
+                const float *x = reinterpret_cast<const float *>(&v[k][h]);
+#pragma unroll
+                for (int e = 0; e < PER; ++e) a[h][e] = fmaf(f, x[e], a[h][e]);
+            }
+            M[h] = mb;
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const float inv = 1.0f / lsum[h];
+        uint16_t *o = p.out + (int64_t(b) * p.Hq + int64_t(g) * G + h) * D + lane * PER;
+        if constexpr (PER == 4)
+            *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16x2(a[h][0] * inv, a[h][1] * inv),
+                                                       pack_bf16x2(a[h][2] * inv, a[h][3] * inv));
+        else
+            *reinterpret_cast<uint32_t *>(o) = pack_bf16x2(a[h][0] * inv, a[h][1] * inv);
+    }
+}
+
 // ------------------------------------------------------------------ main kernel
 template <int D, int G>
 __global__ void __launch_bounds__(Shape<D, G>::WARPS * 32, 1)
@@ -316,14 +407,19 @@ __global__ void __launch_bounds__(Shape<D, G>::WARPS * 32, 1)
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
     }
-    griddep_launch_dependents();  // lets the merge kernel get scheduled; it waits for this grid
+    griddep_launch_dependents();  // lets the next kernel in the stream get scheduled; it waits for this grid
     griddep_wait();               // inputs may come from the previous kernel in the stream
     tile_prefix_scan(p, scan, reinterpret_cast<int32_t *>(smem));
 
     const int64_t T = int64_t(p.Hkv) * scan[p.B];
+    // Sequences without tiles (L == 0, or a rejected length) get zeros; CTAs share the job.
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x)
+        if (scan[b + 1] == scan[b])
+            for (int i = threadIdx.x; i < p.Hq * D / 8; i += blockDim.x)
+                reinterpret_cast<uint4 *>(p.out + int64_t(b) * p.Hq * D)[i] = make_uint4(0u, 0u, 0u, 0u);
     const int w = blockIdx.x * nwarps + warp;
     // Never more workers than tiles, so every worker in [0, P) owns at least one tile
-    // (the merge kernel relies on this when it walks the workers of a sequence).
+    // (the merge relies on this when it walks the workers of a sequence).
     const int64_t P = T < p.num_workers ? T : p.num_workers;
     if (w >= P) return;
     const int64_t begin = int64_t(w) * T / P;
@@ -483,6 +579,20 @@ __global__ void __launch_bounds__(Shape<D, G>::WARPS * 32, 1)
 #pragma unroll
                     for (int h = 0; h < G; ++h)
                         reinterpret_cast<float2 *>(p.ws_ml)[slot * G + h] = make_float2(m[h], lt[h]);
+                // Publish the piece, then count it in; the warp that brings in the last
+                // piece of this (b, g) merges them all.
+                __threadfence();
+                __syncwarp();
+                const int64_t bg = int64_t(mt.b) * p.Hkv + mt.g;
+                const int64_t start = int64_t(p.Hkv) * scan[mt.b] + int64_t(mt.g) * mt.n;
+                const int64_t wf = ((start + 1) * P - 1) / T;     // worker holding the first tile
+                const int64_t wl = ((start + mt.n) * P - 1) / T;  // worker holding the last tile
+                int last = 0;
+                if (lane == 0) last = arrive_last(p.ws_count + bg, p.gen, uint32_t(wl - wf + 1), p.err);
+                if (__shfl_sync(kFull, last, 0)) {
+                    __threadfence();
+                    merge_pieces<D, G>(p, bg, wf, wl, mt.b, mt.g, lane);
+                }
             }
             open = false;
         }
@@ -492,47 +602,6 @@ __global__ void __launch_bounds__(Shape<D, G>::WARPS * 32, 1)
         for (int j = k; j < ntiles && j < k + kStages; ++j)
             mbar_wait_bounded(&bars[j % kStages], uint32_t(j / kStages) & 1u);
     }
-}
-
-// ------------------------------------------------------------------ split-K merge
-// One CTA per (b, g); thread (h, c4) merges 4 output values of query head g*G+h.
-template <int D, int G>
-__global__ void __launch_bounds__(G * D / 4)
-    paged_decode_merge_kernel(const DecodeParams p)
-{
-    griddep_launch_dependents();
-    griddep_wait();  // the main kernel's partials and prefix
-    const int bg = blockIdx.x;
-    const int b = bg / p.Hkv, g = bg - b * p.Hkv;
-    const int h = threadIdx.x / (D / 4), c4 = threadIdx.x % (D / 4);
-    uint16_t *o = p.out + (int64_t(b) * p.Hq + int64_t(g) * G + h) * D + c4 * 4;
-    const int32_t n = p.ws_prefix[b + 1] - p.ws_prefix[b];
-    if (n == 0) {  // empty (or rejected) sequence: zeros
-        *reinterpret_cast<uint2 *>(o) = make_uint2(0u, 0u);
-        return;
-    }
-    const int64_t T = int64_t(p.Hkv) * p.ws_prefix[p.B];
-    const int64_t start = int64_t(p.Hkv) * p.ws_prefix[b] + int64_t(g) * n;
-    const int64_t P = T < p.num_workers ? T : p.num_workers;  // same cap as the main kernel
-    const int64_t wf = ((start + 1) * P - 1) / T;  // worker holding the first tile
-    const int64_t wl = ((start + n) * P - 1) / T;  // worker holding the last tile
-    if (wf == wl) return;                           // written directly by the main kernel
-    const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);
-    float M = -INFINITY;
-    for (int64_t w = wf; w <= wl; ++w) M = fmaxf(M, ml[(w + bg) * G + h].x);
-    float lsum = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    for (int64_t w = wf; w <= wl; ++w) {
-        const float2 st = ml[(w + bg) * G + h];
-        const float f = ex2(st.x - M);
-        const float4 v = *reinterpret_cast<const float4 *>(p.ws_acc + ((w + bg) * G + h) * D + c4 * 4);
-        lsum = fmaf(f, st.y, lsum);
-        a0 = fmaf(f, v.x, a0);
-        a1 = fmaf(f, v.y, a1);
-        a2 = fmaf(f, v.z, a2);
-        a3 = fmaf(f, v.w, a3);
-    }
-    const float inv = 1.0f / lsum;
-    *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16x2(a0 * inv, a1 * inv), pack_bf16x2(a2 * inv, a3 * inv));
 }
 
 // ------------------------------------------------------------------ host side
@@ -590,11 +659,6 @@ pkv_status launch_decode(LaunchArgs &a)
         return PKV_ECUDA;
     }
     if (launch_pdl(kern, dim3(grid), dim3(nwarps * 32), smem, a.stream, kmap, vmap, a.p) != cudaSuccess) {
-        cudaGetLastError();
-        return PKV_ECUDA;
-    }
-    if (launch_pdl(paged_decode_merge_kernel<D, G>, dim3(a.p.B * a.p.Hkv), dim3(G * D / 4), 0, a.stream, a.p) !=
-        cudaSuccess) {
         cudaGetLastError();
         return PKV_ECUDA;
     }
@@ -670,7 +734,7 @@ extern "C" pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cach
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.out = out;
-    p.ws_prefix = reinterpret_cast<int32_t *>(wsb + ws.prefix_off);
+    p.ws_count = reinterpret_cast<unsigned long long *>(wsb + ws.count_off);
     p.ws_ml = reinterpret_cast<float *>(wsb + ws.ml_off);
     p.ws_acc = reinterpret_cast<float *>(wsb + ws.acc_off);
     p.err = err_word;
@@ -684,6 +748,8 @@ extern "C" pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cach
     p.len_limit = int32_t(len_limit);
     p.num_workers = 0;
     p.scale_log2 = float(double(scale) * 1.4426950408889634);
+    static std::atomic<uint32_t> generation{0};
+    p.gen = generation.fetch_add(1u, std::memory_order_relaxed) + 1u;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
     a.sm_count = dev.sm_count;

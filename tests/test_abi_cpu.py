@@ -56,9 +56,10 @@ def test_workspace_size_host_arithmetic(lib):
     assert f(-1, 16, 8, 128) == 0
     assert f(64, 16, 6, 128) == 0          # 16 % 6 != 0
     assert f(pkv.MAX_SEQS + 1, 16, 8, 128) == 0
-    # holds every split-K partial: (max workers + B*Hkv) slots of G*(D + 2) floats, plus the prefix
+    # holds every split-K partial: (max workers + B*Hkv) slots of G*(D + 2) floats, plus a 64-bit
+    # arrival counter per (sequence, kv head)
     B, Hq, Hkv, D = 64, 16, 8, 128
-    assert f(B, Hq, Hkv, D) >= (pkv.MAX_WORKERS + B * Hkv) * (Hq // Hkv) * (D + 2) * 4 + (B + 1) * 4
+    assert f(B, Hq, Hkv, D) >= (pkv.MAX_WORKERS + B * Hkv) * (Hq // Hkv) * (D + 2) * 4 + B * Hkv * 8
 
 
 NULL = None
