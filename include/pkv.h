@@ -10,7 +10,8 @@
  *
  * Conventions shared by every entry point
  *   - All array pointers are DEVICE pointers owned by the caller.  The library
- *     allocates no memory, keeps no per-call state and never synchronises the
+ *     allocates no device memory, keeps no state that affects results (only
+ *     host-side memos such as encoded tensor maps) and never synchronises the
  *     stream.  Work is enqueued asynchronously on `stream` (NULL = the legacy
  *     default stream); the return code covers only host-side argument checks
  *     and the launch itself.
@@ -32,6 +33,12 @@
 
 #include <stddef.h>
 #include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -56,10 +63,15 @@ typedef enum {
 #define PKV_ERR_WAIT_TIMEOUT 0x8  /* a bounded wait on an asynchronous copy gave up                    */
 
 /* Version of this ABI (bumped on any incompatible change). */
-int pkv_abi_version(void);
+PKV_API int pkv_abi_version(void);
 
 /* Static text for a pkv_status value (never NULL). */
-const char *pkv_status_string(int status);
+PKV_API const char *pkv_status_string(int status);
+
+/* Why the most recent call on this host thread returned PKV_ECUDA: the CUDA
+ * call that failed and its error text ("" if none yet).  The text stays
+ * valid until the next failing call on the same thread. */
+PKV_API const char *pkv_last_cuda_error(void);
 
 /*
  * pkv_decode_slot_mapping -- the cache slot of the token each sequence
@@ -84,7 +96,7 @@ const char *pkv_status_string(int status);
  * A context length that does not fit its table row, or a table entry outside
  * [0, num_blocks), yields -1 for that row and sets the matching err bit.
  */
-pkv_status pkv_decode_slot_mapping(const int32_t *block_tables, int32_t max_blocks_per_seq,
+PKV_API pkv_status pkv_decode_slot_mapping(const int32_t *block_tables, int32_t max_blocks_per_seq,
                                    const int32_t *context_lens, int32_t num_seqs,
                                    int32_t block_size, int32_t num_blocks,
                                    int32_t *slot_mapping, int32_t num_tokens,
@@ -110,21 +122,24 @@ pkv_status pkv_decode_slot_mapping(const int32_t *block_tables, int32_t max_bloc
  * PKV_ERR_SLOT_RANGE.  head_dim * num_kv_heads * 2 bytes must be a multiple
  * of 16.  num_tokens == 0 is a no-op.
  */
-pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, const int32_t *slot_mapping,
+PKV_API pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, const int32_t *slot_mapping,
                         int32_t num_tokens, uint16_t *k_cache, uint16_t *v_cache,
                         int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                         int32_t head_dim, int32_t *err_word, pkv_stream_t stream);
 
 /*
  * Bytes of device workspace that pkv_paged_decode needs for these sizes
- * (split-K partial states plus one arrival counter per (sequence, kv head)).
- * Depends only on the arguments; 0 means the sizes are invalid.  The
- * workspace needs no initialisation: counters are tagged with a per-call
- * generation, so leftovers from earlier calls (or garbage) count as zero, and
- * a completed call leaves them at zero.  Calls that may run at the same time
- * need separate workspaces.
+ * (split-K partial states, one arrival counter per (sequence, kv head), and a
+ * small load-balance record).  Depends only on the arguments; 0 means the
+ * sizes are invalid.  The workspace needs no initialisation: counters and
+ * claims are tagged with a per-call generation, so leftovers from earlier
+ * calls (or garbage) count as zero.  Between calls it keeps per-SM speed
+ * estimates that size each SM's share of the next call; they affect only
+ * speed, never results.  Calls that may run at the same time need separate
+ * workspaces; reusing one workspace for consecutive calls on a stream lets
+ * the estimates settle.
  */
-size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+PKV_API size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                        int32_t num_kv_heads, int32_t head_dim);
 
 /* Upper limits of pkv_paged_decode. */
@@ -159,9 +174,11 @@ size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
  *   out           [num_seqs, num_q_heads, head_dim] bf16, rounded to nearest
  *   workspace     device buffer of at least
  *                 pkv_paged_decode_workspace_size(...) bytes, 16-byte aligned
- *   num_workers   0 = one worker per resident warp of the device (the
- *                 default); otherwise the number of warps the tokens are
- *                 split over, 1..PKV_MAX_WORKERS (testing and tuning).
+ *   num_workers   0 (the default): one CTA per SM; each SM takes a share of
+ *                 the tiles sized by the speed it showed in earlier calls on
+ *                 this workspace, split evenly over its warps.  Otherwise a
+ *                 fixed, even split over about num_workers warps,
+ *                 1..PKV_MAX_WORKERS (testing and tuning).
  * Supported: head_dim in {64, 128}; num_q_heads / num_kv_heads in 1..8;
  * block_size a power of two in [8, 1024]; num_seqs <= PKV_MAX_SEQS;
  * num_blocks * block_size < 2^31.
@@ -172,7 +189,7 @@ size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
  * serialization and waits on the device for the previous kernel in the stream
  * before it reads any input.
  */
-pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+PKV_API pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                             const int32_t *block_tables, int32_t max_blocks_per_seq,
                             const int32_t *context_lens, int32_t num_seqs,
                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -207,7 +224,7 @@ pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cache, const ui
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
-pkv_status pkv_paged_decode_noalloc(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+PKV_API pkv_status pkv_paged_decode_noalloc(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                                     const int32_t *block_tables, int32_t max_blocks_per_seq,
                                     const int32_t *context_lens, int32_t num_seqs,
                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,

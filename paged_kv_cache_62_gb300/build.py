@@ -20,8 +20,10 @@ LIB_PATH = os.path.join(HERE, "libpkv.so")
 SOURCES = ["pkv_api.cu", "pkv_store.cu", "pkv_decode.cu"]
 HEADERS = ["pkv_device.cuh", "pkv_host.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
-         "-Xcompiler", "-Wall"]
+# Hidden visibility: only the PKV_API (extern "C") entry points are exported, so
+# internal statics never merge with those of another copy of the library.
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+         "--expt-relaxed-constexpr", "-Xcompiler", "-Wall"]
 
 
 def nvcc() -> str:

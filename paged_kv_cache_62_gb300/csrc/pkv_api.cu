@@ -1,26 +1,38 @@
 // Library-wide entry points (version, status strings) and host helpers.
+#include <cstdio>
 #include <mutex>
 
 #include "pkv_host.h"
 
 namespace pkv {
 
+static thread_local char g_last_cuda_error[256] = "";
+
+void record_cuda_error(const char *where, const char *what)
+{
+    std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", where, what);
+}
+
 bool current_device_info(DeviceInfo *info)
 {
     static std::mutex mu;
     static DeviceInfo cache[64];
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
         cudaGetLastError();
+        record_cuda_error("cudaGetDevice", e != cudaSuccess ? cudaGetErrorString(e) : "device index out of range");
         return false;
     }
     std::lock_guard<std::mutex> lock(mu);
     DeviceInfo &c = cache[dev];
     if (c.device != dev) {
         int sms = 0, smem = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        cudaError_t a = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (a == cudaSuccess) a = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (a != cudaSuccess) {
             cudaGetLastError();
+            record_cuda_error("cudaDeviceGetAttribute", cudaGetErrorString(a));
             return false;
         }
         c.sm_count = sms;
@@ -50,6 +62,8 @@ EncodeTiledFn encode_tiled_fn()
 }  // namespace pkv
 
 extern "C" int pkv_abi_version(void) { return 1; }
+
+extern "C" const char *pkv_last_cuda_error(void) { return pkv::g_last_cuda_error; }
 
 extern "C" const char *pkv_status_string(int status)
 {

@@ -30,7 +30,11 @@
 //    merges them all (split-K / flash-decoding without a second kernel).
 #include <algorithm>
 #include <atomic>
+#include <cstdio>
+#include <mutex>
 #include <type_traits>
+#include <unordered_map>
+#include <vector>
 #include <cmath>
 
 #include "pkv_device.cuh"
@@ -42,18 +46,38 @@ constexpr int kTile = 16;      // tokens per tile
 constexpr int kMaxWarps = 12;  // warps per CTA (one CTA per SM) for small groups
 constexpr int kStages = 2;     // ring depth per warp
 
+// ------------------------------------------------------------------ load balance state
+// The tile list is cut into one slice per SM id, each slice into equal
+// per-warp ranges.  In the adaptive mode the slices' sizes follow what the
+// previous call on this workspace saw: a slice that finished late gets a
+// little less work, one that finished early a little more (SMs of a GB300
+// stream HBM at noticeably different, but stable, rates).  This only moves
+// work around: any table contents, garbage included, give correct results.
+constexpr int kMaxSlots = 512;  // slices: SM ids (adaptive) or CTAs (fixed split)
+constexpr uint32_t kTableMagic = 0x62616c31u;
+
+struct BalanceState {
+    float weight[2][kMaxSlots];           // weight a slice had in the call that wrote the entry (0: no SM)
+    float elapsed[2][kMaxSlots];          // its run time in us (<= 0: present, nothing measured)
+    uint32_t tag[2][kMaxSlots];           // (call number of the writer) ^ kTableMagic
+    unsigned long long claim[kMaxSlots];  // (gen << 32) | 1 once a CTA took the slice this call
+};
+
 struct DecodeParams {
     const uint16_t *q;
     const int32_t *block_tables;
     const int32_t *context_lens;
     uint16_t *out;
-    unsigned long long *ws_count;  // [B * Hkv] arrival counters: (call generation << 32) | pieces arrived
+    unsigned long long *ws_count;  // [B * Hkv] arrival counters: (call generation << 32) | tiles arrived
     float *ws_ml;        // [slots][G][2] (m, l) per partial
     float *ws_acc;       // [slots][G][D] unnormalised accumulators
+    BalanceState *ws_bal;  // per-SM speed estimates, claims, call counter
     int32_t *err;
-    int32_t B, Hq, Hkv, bs, log2_bs, NB, max_blocks, len_limit, num_workers;
-    float scale_log2;    // scale * log2(e)
-    uint32_t gen;        // generation of this call (tags the arrival counters)
+    int32_t B, Hq, Hkv, bs, log2_bs, NB, max_blocks, len_limit;
+    int32_t num_workers;  // > 0: fixed split over ceil(num_workers / warps) CTAs; 0: adaptive split by SM
+    float scale_log2;     // scale * log2(e)
+    uint32_t gen;         // generation of this call (tags counters and claims)
+    uint32_t call;        // number of this call on this workspace: call & 1 picks the table half written
 };
 
 struct alignas(16) StageMeta {
@@ -72,21 +96,26 @@ struct Shape {
     static_assert(LPT >= NIT && DUP >= 1, "tile too large for the lane split");
     // Warps per CTA: as many as the register file allows without spilling
     // (one CTA of WARPS*32 threads per SM, so at most 65536 / (WARPS*32) registers each).
-    static constexpr int WARPS = (G <= 4 || (D == 64 && G <= 5)) ? kMaxWarps : 8;
+    static constexpr int WARPS = (G <= 3 || (D == 64 && G <= 5)) ? kMaxWarps : 8;
 };
 
 struct WsLayout {
-    size_t count_off, ml_off, acc_off, total;
+    size_t bal_off, count_off, ml_off, acc_off, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Piece slots: one per (worker, sequence, kv head) boundary.  Worker ids
+// (slice * warps + warp) stay below kWorkerIds in both modes.
+constexpr size_t kWorkerIds = size_t(PKV_MAX_WORKERS) + 64;
+
 inline WsLayout ws_layout(int32_t B, int32_t G, int32_t Hkv, int32_t D)
 {
-    const size_t slots = size_t(PKV_MAX_WORKERS) + size_t(B) * size_t(Hkv);
+    const size_t slots = kWorkerIds + size_t(B) * size_t(Hkv);
     WsLayout w;
-    w.count_off = 0;
-    w.ml_off = align256(size_t(B) * size_t(Hkv) * 8);
+    w.bal_off = 0;
+    w.count_off = align256(sizeof(BalanceState));
+    w.ml_off = w.count_off + align256(size_t(B) * size_t(Hkv) * 8);
     w.acc_off = w.ml_off + align256(slots * size_t(G) * 2 * 4);
     w.total = w.acc_off + slots * size_t(G) * size_t(D) * 4;
     return w;
@@ -292,20 +321,206 @@ __device__ __forceinline__ void attend_tile(const uint8_t *st, int valid, const 
     }
 }
 
+// ------------------------------------------------------------------ partition
+// Worker u = slice * nwarps + j owns the tiles
+//   [bound[s] + len * j / nwarps, bound[s] + len * (j + 1) / nwarps),  len = bound[s+1] - bound[s].
+// Worker ids grow with tile index, so a piece's workspace slot u + (b * Hkv + g)
+// is unique (each step along the tile list raises u, or (b, g), or both).
+struct Partition {
+    const long long *bound;  // [nslots + 1] in shared memory
+    int nslots, nwarps;
+
+    __device__ __forceinline__ void range(long long u, long long &b, long long &e) const
+    {
+        const int s = int(u / nwarps), j = int(u - (long long)s * nwarps);
+        const long long lo = bound[s], len = bound[s + 1] - lo;
+        b = lo + len * j / nwarps;
+        e = lo + len * (j + 1) / nwarps;
+    }
+    // The (non-empty) worker that owns tile x, 0 <= x < bound[nslots].
+    __device__ __forceinline__ long long worker_of(long long x) const
+    {
+        int lo = 0, hi = nslots;  // bound[lo] <= x < bound[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (bound[mid] <= x)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const long long b0 = bound[lo], len = bound[lo + 1] - b0;
+        return (long long)lo * nwarps + ((x - b0 + 1) * nwarps - 1) / len;
+    }
+};
+
+// ------------------------------------------------------------------ load balance
+__device__ __forceinline__ unsigned smid()
+{
+    unsigned v;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
+    return v;
+}
+
+__device__ __forceinline__ unsigned nsmid()
+{
+    unsigned v;
+    asm volatile("mov.u32 %0, %%nsmid;" : "=r"(v));
+    return v;
+}
+
+// Sum of one float per thread over the CTA (fixed order: identical in every CTA).
+__device__ __forceinline__ float block_sum(float v, float *red)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int i = 0; i < nw; ++i) t += red[i];
+    return t;
+}
+
+// Slice bounds of this call.  Adaptive mode: each slice entry of the table
+// half written by the previous call on this workspace (call - 1) keeps its
+// weight scaled by clamp(mean elapsed / its elapsed, 0.8, 1.25) (weight 0: an
+// SM id without a CTA); entries from any other call count as unknown (weight
+// 1).  Fixed mode: equal weights.  Every CTA computes the same bounds from the
+// same inputs in the same order; leaves the weights in w[].
+__device__ void build_partition(const DecodeParams &p, bool adaptive, int nslots, long long T, long long *bound,
+                                float *w, float *red)
+{
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int rp = int(p.call & 1u) ^ 1;
+    const uint32_t want = (p.call - 1u) ^ kTableMagic;
+    // pass 1: raw weights (kept in w) and elapsed times (kept in bound[] as float bits)
+    float tsum = 0.f, tcnt = 0.f;
+    float *el = reinterpret_cast<float *>(bound);
+    for (int i = tid; i < nslots; i += nt) {
+        float x = 1.0f, t = 0.f;
+        // plain L2 loads: this half of the table is not written during this call
+        if (adaptive && __ldcg(&p.ws_bal->tag[rp][i]) == want) {
+            x = __ldcg(&p.ws_bal->weight[rp][i]);
+            t = __ldcg(&p.ws_bal->elapsed[rp][i]);
+            if (!(x >= 0.f) || !(x < 1.0e6f)) x = 1.0f;
+            if (!(t < 1.0e9f)) t = 0.f;
+            if (x > 0.f && t > 0.f) {
+                tsum += t;
+                tcnt += 1.f;
+            }
+        }
+        w[i] = x;
+        el[i] = t;
+    }
+    tsum = block_sum(tsum, red);
+    tcnt = block_sum(tcnt, red);
+    const float tmean = tcnt > 0.f ? tsum / tcnt : 0.f;
+    // pass 2: scale by the finishing-time ratio, then bound every weight to [1/4, 4] x mean
+    float wsum = 0.f, wcnt = 0.f;
+    for (int i = tid; i < nslots; i += nt) {
+        float x = w[i];
+        const float t = el[i];
+        if (x > 0.f && t > 0.f && tmean > 0.f) x *= fminf(fmaxf(tmean / t, 0.8f), 1.25f);
+        w[i] = x;
+        if (x > 0.f) {
+            wsum += x;
+            wcnt += 1.f;
+        }
+    }
+    wsum = block_sum(wsum, red);
+    wcnt = block_sum(wcnt, red);
+    const float wmean = wcnt > 0.f ? wsum / wcnt : 1.0f;
+    for (int i = tid; i < nslots; i += nt) {
+        float x = wcnt > 0.f ? w[i] / wmean : 1.0f;  // mean 1 over present slices; none: equal weights
+        if (x > 0.f) x = fminf(fmaxf(x, 0.25f), 4.0f);
+        w[i] = x;
+    }
+    __syncthreads();
+    // bounds: float prefix of the weights -> 2^20 tickets -> tiles (a shift, no division)
+    if (tid < 32) {
+        const int per = (nslots + 31) / 32;
+        const int lo = min(nslots, tid * per), hi = min(nslots, lo + per);
+        float run = 0.f;
+        for (int i = lo; i < hi; ++i) run += w[i];
+        float incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float v = __shfl_up_sync(kFull, incl, o);
+            if (tid >= o) incl += v;
+        }
+        const float total = __shfl_sync(kFull, incl, 31);
+        float acc = incl - run;
+        for (int i = lo; i < hi; ++i) {
+            long long pre = total > 0.f ? (long long)(acc / total * 1048576.0f) : (long long)i * 1048576 / nslots;
+            pre = pre < 0 ? 0 : (pre > 1048576 ? 1048576 : pre);
+            bound[i] = (T * pre) >> 20;
+            acc += w[i];
+        }
+        __syncwarp();
+        if (tid == 0) bound[nslots] = T;
+    }
+    // bounds are monotone: the float prefix only grows and pre is clamped to [0, 2^20]
+    __syncthreads();
+}
+
+__device__ __forceinline__ bool try_claim(unsigned long long *word, uint32_t gen)
+{
+    const unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(word);
+    if (uint32_t(cur >> 32) == gen) return false;
+    return atomicCAS(word, cur, (static_cast<unsigned long long>(gen) << 32) | 1ull) == cur;
+}
+
+// Warp-collective: claim a non-empty slice that no CTA took yet, among the
+// slices this CTA looks after (s = blockIdx.x + k * gridDim.x).  -1 if none.
+// With `record`, also writes the balance entries of the looked-after slices
+// that are empty this call (nobody else writes them): present if an SM
+// claimed it, absent otherwise.
+__device__ int claim_leftover(const DecodeParams &p, const long long *bound, int nslots, int wp, bool record)
+{
+    const int lane = threadIdx.x & 31;
+    for (int k0 = 0; blockIdx.x + (long long)k0 * gridDim.x < nslots; k0 += 32) {
+        const long long s = blockIdx.x + (long long)(k0 + lane) * gridDim.x;
+        bool cand = false;
+        if (s < nslots) {
+            const unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(&p.ws_bal->claim[s]);
+            const bool claimed = uint32_t(cur >> 32) == p.gen;
+            if (bound[s + 1] > bound[s]) {
+                cand = !claimed;
+            } else if (record) {
+                p.ws_bal->weight[wp][s] = claimed ? 1.0f : 0.0f;
+                p.ws_bal->elapsed[wp][s] = claimed ? -1.0f : 0.0f;
+                p.ws_bal->tag[wp][s] = p.call ^ kTableMagic;
+            }
+        }
+        unsigned m = __ballot_sync(kFull, cand);
+        while (m) {
+            const int l = __ffs(m) - 1;
+            int ok = 0;
+            if (lane == l) ok = try_claim(&p.ws_bal->claim[s], p.gen);
+            if (__shfl_sync(kFull, ok, l)) return int(__shfl_sync(kFull, s, l));
+            m &= m - 1;
+        }
+    }
+    return -1;
+}
+
 // ------------------------------------------------------------------ split-K merge (a6)
-// Count one more piece of (b, g) in.  The counter word is (call generation << 32)
-// | pieces; a word from another call (other generation, or leftover garbage)
-// counts as zero, so the workspace never needs clearing.  Returns 1 for the
-// piece that completes the set (and resets the word to 0 for the next call).
-__device__ __forceinline__ int arrive_last(unsigned long long *ctr, uint32_t gen, uint32_t pieces, int32_t *err)
+// Count the `tiles` of one piece of (b, g) in.  The counter word is (call
+// generation << 32) | tiles arrived; a word from another call (other
+// generation, or leftover garbage) counts as zero, so the workspace never
+// needs clearing.  Returns 1 for the piece that completes the pair's `total`
+// tiles (and resets the word to 0).  Counting tiles, not pieces, lets any
+// partition of the tile list merge correctly.
+__device__ __forceinline__ int arrive_last(unsigned long long *ctr, uint32_t gen, uint32_t tiles, uint32_t total,
+                                           int32_t *err)
 {
     unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(ctr);
     for (int it = 0; it < (1 << 20); ++it) {
-        const uint32_t n = (uint32_t(cur >> 32) == gen) ? uint32_t(cur) + 1u : 1u;
+        const uint32_t n = ((uint32_t(cur >> 32) == gen) ? uint32_t(cur) : 0u) + tiles;
         const unsigned long long next = (static_cast<unsigned long long>(gen) << 32) | n;
         const unsigned long long seen = atomicCAS(ctr, cur, next);
         if (seen == cur) {
-            if (n != pieces) return 0;
+            if (n != total) return 0;
             atomicExch(ctr, 0ull);
             return 1;
         }
@@ -315,14 +530,14 @@ __device__ __forceinline__ int arrive_last(unsigned long long *ctr, uint32_t gen
     return 0;
 }
 
-// Merge the partial states of workers wf..wl for (b, g):
+// Merge the partial states of (b, g) held by the non-empty workers uf..ul:
 //   M = max m_i,  l = sum 2^(m_i - M) l_i,  out = sum 2^(m_i - M) acc_i / l
 // (the online-softmax algebra; m in log2 units).  The pieces were written by
 // other SMs, so they are read through L2 (ld.global.cg), BATCH pieces at a
 // time with independent loads, folded into a running (M, l, acc).
 template <int D, int G>
-__device__ __forceinline__ void merge_pieces(const DecodeParams &p, int64_t bg, int64_t wf, int64_t wl, int b, int g,
-                                             int lane)
+__device__ __forceinline__ void merge_pieces(const DecodeParams &p, const Partition &part, long long bg, long long uf,
+                                             long long ul, int b, int g, int lane)
 {
     constexpr int PER = D / 32;                               // output values per lane
     constexpr int BATCH = G <= 2 ? 4 : (G <= 4 ? 2 : 1);      // pieces loaded together
@@ -336,12 +551,16 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int64_t bg, 
 #pragma unroll
         for (int e = 0; e < PER; ++e) a[h][e] = 0.f;
     }
-    for (int64_t w0 = wf; w0 <= wl; w0 += BATCH) {
+    for (long long u0 = uf; u0 <= ul; u0 += BATCH) {
         float2 st[BATCH][G];
         Vec v[BATCH][G];
+        bool use[BATCH];
 #pragma unroll
         for (int k = 0; k < BATCH; ++k) {
-            const int64_t slot = (w0 + k <= wl ? w0 + k : wl) + bg;  // clamp: a repeated piece gets weight 0 below
+            long long rb = 0, re = 0;
+            if (u0 + k <= ul) part.range(u0 + k, rb, re);
+            use[k] = re > rb;                               // empty workers wrote nothing
+            const long long slot = (use[k] ? u0 + k : uf) + bg;
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 st[k][h] = __ldcg(ml + slot * G + h);
@@ -353,14 +572,14 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int64_t bg, 
             float mb = M[h];
 #pragma unroll
             for (int k = 0; k < BATCH; ++k)
-                if (w0 + k <= wl) mb = fmaxf(mb, st[k][h].x);
+                if (use[k]) mb = fmaxf(mb, st[k][h].x);
             const float r = ex2(M[h] - mb);  // 0 while nothing has been folded in (M = -inf)
             lsum[h] *= r;
 #pragma unroll
             for (int e = 0; e < PER; ++e) a[h][e] *= r;
 #pragma unroll
             for (int k = 0; k < BATCH; ++k) {
-                const float f = (w0 + k <= wl) ? ex2(st[k][h].x - mb) : 0.f;
+                const float f = use[k] ? ex2(st[k][h].x - mb) : 0.f;
                 lsum[h] = fmaf(f, st[k][h].y, lsum[h]);
                 const float *x = reinterpret_cast<const float *>(&v[k][h]);
 #pragma unroll
@@ -394,14 +613,20 @@ __global__ void __launch_bounds__(Shape<D, G>::WARPS * 32, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = lane % LPT, grp = lane / LPT;
 
+    // shared memory: per-warp stage rings, their metadata and barriers, the
+    // slice bounds, the sanitised slice weights, a few scalars, the tile prefix
     uint8_t *stages = smem + size_t(warp) * kStages * S::STAGE_BYTES;
     StageMeta *metas =
         reinterpret_cast<StageMeta *>(smem + size_t(nwarps) * kStages * S::STAGE_BYTES) + warp * kStages;
     uint64_t *bars =
         reinterpret_cast<uint64_t *>(smem + size_t(nwarps) * kStages * (S::STAGE_BYTES + sizeof(StageMeta))) +
         warp * kStages;
-    int32_t *scan = reinterpret_cast<int32_t *>(smem + size_t(nwarps) * kStages *
-                                                           (S::STAGE_BYTES + sizeof(StageMeta) + 8));
+    long long *bound = reinterpret_cast<long long *>(smem + size_t(nwarps) * kStages *
+                                                                (S::STAGE_BYTES + sizeof(StageMeta) + 8));
+    float *wts = reinterpret_cast<float *>(bound + kMaxSlots + 1);
+    float *red = wts + kMaxSlots;
+    int *slice_sh = reinterpret_cast<int *>(red + 32);  // [0] slice to run next, [1] this CTA's own slice
+    int32_t *scan = reinterpret_cast<int32_t *>(slice_sh + 4);
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&kmap);
@@ -411,196 +636,268 @@ __global__ void __launch_bounds__(Shape<D, G>::WARPS * 32, 1)
     griddep_wait();               // inputs may come from the previous kernel in the stream
     tile_prefix_scan(p, scan, reinterpret_cast<int32_t *>(smem));
 
-    const int64_t T = int64_t(p.Hkv) * scan[p.B];
+    const long long T = (long long)p.Hkv * scan[p.B];
     // Sequences without tiles (L == 0, or a rejected length) get zeros; CTAs share the job.
     for (int b = blockIdx.x; b < p.B; b += gridDim.x)
         if (scan[b + 1] == scan[b])
             for (int i = threadIdx.x; i < p.Hq * D / 8; i += blockDim.x)
                 reinterpret_cast<uint4 *>(p.out + int64_t(b) * p.Hq * D)[i] = make_uint4(0u, 0u, 0u, 0u);
-    const int w = blockIdx.x * nwarps + warp;
-    // Never more workers than tiles, so every worker in [0, P) owns at least one tile
-    // (the merge relies on this when it walks the workers of a sequence).
-    const int64_t P = T < p.num_workers ? T : p.num_workers;
-    if (w >= P) return;
-    const int64_t begin = int64_t(w) * T / P;
-    const int64_t end = int64_t(w + 1) * T / P;
-    const int ntiles = int(end - begin);
-    if (ntiles == 0) return;
+
+    // Slices: one per SM id, sized by measured speed (adaptive), or one per CTA (fixed split).
+    const bool adaptive = p.num_workers == 0;
+    int nslots = int(gridDim.x);
+    if (adaptive) {
+        nslots = int(min(nsmid(), unsigned(kMaxSlots)));
+        nslots = min(nslots, int(kWorkerIds / nwarps));
+    }
+    const int wp = int(p.call & 1u);  // this call writes one half of the balance table, reads the other
+    build_partition(p, adaptive, nslots, T, bound, wts, red);
+    const Partition part{bound, nslots, nwarps};
 
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
     }
-    __syncwarp();
+    if (warp == 0) {
+        int home = -1;
+        if (lane == 0) {
+            if (!adaptive)
+                home = int(blockIdx.x);
+            else if (int(smid()) < nslots && try_claim(&p.ws_bal->claim[smid()], p.gen))
+                home = int(smid());
+        }
+        home = __shfl_sync(kFull, home, 0);
+        const int first = (home < 0 && adaptive) ? claim_leftover(p, bound, nslots, wp, false) : home;
+        if (lane == 0) {
+            slice_sh[0] = first;
+            slice_sh[1] = home;
+        }
+    }
+    __syncthreads();
 
     const uint64_t policy = policy_evict_first();
     const int box = p.bs < kTile ? p.bs : kTile;
     const int nsub = kTile / box;
+    uint32_t kk = 0;     // tiles this warp has consumed: selects ring stage and barrier phase
+    bool dead = false;   // a wait timed out: do no more work
 
-    // Block-table prefetch: lane j holds the entries of the next tile k with k % 32 == j.
-    Walker fw = walker_locate(scan, p.B, p.Hkv, begin);
-    Walker iw = fw;
-    int32_t pf0 = -1, pf1 = -1, pfL = 0;
-    const int npre = ntiles < 32 ? ntiles : 32;
-    for (int j = 0; j < npre; ++j) {
-        if (lane == j) table_lookup(p, fw, nsub, pf0, pf1, pfL);
-        if (j + 1 < ntiles) walker_advance(fw, scan, p.Hkv, p.B);
-    }
+    // One worker's tile range [begin, end); u is the worker id (sets the piece slots).
+    auto run_range = [&](long long begin, long long end, long long u) {
+        const int ntiles = int(end - begin);
 
-    auto issue = [&](int k, int s) {
-        const int src = k & 31;
-        const int32_t e0 = __shfl_sync(kFull, pf0, src);
-        const int32_t e1 = __shfl_sync(kFull, pf1, src);
-        const int32_t len = __shfl_sync(kFull, pfL, src);
-        if (k + 32 < ntiles) {
-            if (lane == src) table_lookup(p, fw, nsub, pf0, pf1, pfL);
-            if (k + 33 < ntiles) walker_advance(fw, scan, p.Hkv, p.B);
-        }
-        if (lane == 0) {
-            uint8_t *st = stages + s * S::STAGE_BYTES;
-            const int seg_start = (k == 0 || iw.t == 0) ? 1 : 0;
-            const int32_t pos0 = iw.t * kTile;
-            int32_t row0 = -1, row1 = -1;
-            if (e0 >= 0 && e0 < p.NB)
-                row0 = e0 * p.bs + (pos0 & (p.bs - 1));
-            else
-                flag_error(p.err, PKV_ERR_BLOCK_RANGE);
-            if (nsub == 2 && pos0 + box < len) {
-                if (e1 >= 0 && e1 < p.NB)
-                    row1 = e1 * p.bs;
+        // Block-table prefetch in batches of 32 tiles: lane j of `cur` holds the
+        // table entries (and context length) of tile kb + j of the current batch;
+        // `nxt` is loaded, all lanes at once, one batch ahead.  Two register sets,
+        // because the scoreboard tracks a register for the whole warp: a fresh
+        // load into the register that the next shuffle reads would stall it.
+        Walker fw = walker_locate(scan, p.B, p.Hkv, begin);  // first tile not yet prefetched
+        Walker iw = fw;                                       // next tile to issue
+        int32_t cur0 = -1, cur1 = -1, curL = 0, nxt0 = -1, nxt1 = -1, nxtL = 0;
+        auto prefetch_batch = [&](int kb) {  // tiles [kb, kb + 32) -> nxt; fw moves on to kb + 32
+            Walker mine = fw;
+    #pragma unroll 1
+            for (int j = 0; j < 32 && kb + j < ntiles; ++j) {
+                if (lane == j) mine = fw;
+                if (kb + j + 1 < ntiles) walker_advance(fw, scan, p.Hkv, p.B);
+            }
+            if (kb + lane < ntiles) table_lookup(p, mine, nsub, nxt0, nxt1, nxtL);
+        };
+        prefetch_batch(0);
+        cur0 = nxt0;
+        cur1 = nxt1;
+        curL = nxtL;
+        if (ntiles > 32) prefetch_batch(32);
+
+        auto issue = [&](int k, int s) {
+            const int src = k & 31;
+            if (src == 0 && k > 0) {  // batch boundary: nxt was loaded 32 tiles ago
+                cur0 = nxt0;
+                cur1 = nxt1;
+                curL = nxtL;
+                if (k + 32 < ntiles) prefetch_batch(k + 32);
+            }
+            const int32_t e0 = __shfl_sync(kFull, cur0, src);
+            const int32_t e1 = __shfl_sync(kFull, cur1, src);
+            const int32_t len = __shfl_sync(kFull, curL, src);
+            if (lane == 0) {
+                uint8_t *st = stages + s * S::STAGE_BYTES;
+                const int seg_start = (k == 0 || iw.t == 0) ? 1 : 0;
+                const int32_t pos0 = iw.t * kTile;
+                int32_t row0 = -1, row1 = -1;
+                if (e0 >= 0 && e0 < p.NB)
+                    row0 = e0 * p.bs + (pos0 & (p.bs - 1));
                 else
                     flag_error(p.err, PKV_ERR_BLOCK_RANGE);
+                if (nsub == 2 && pos0 + box < len) {
+                    if (e1 >= 0 && e1 < p.NB)
+                        row1 = e1 * p.bs;
+                    else
+                        flag_error(p.err, PKV_ERR_BLOCK_RANGE);
+                }
+                const uint32_t sub_bytes = uint32_t(2 * box * D * 2);
+                const uint32_t bytes = (row0 >= 0 ? sub_bytes : 0u) + (row1 >= 0 ? sub_bytes : 0u) +
+                                       (seg_start ? uint32_t(S::Q_BYTES) : 0u);
+                StageMeta &mt = metas[s];
+                mt.b = iw.b;
+                mt.g = iw.g;
+                mt.t = iw.t;
+                mt.n = iw.n;
+                mt.L = len;
+                mt.seg_start = seg_start;
+                mbar_arrive_expect_tx(&bars[s], bytes);
+                if (row0 >= 0) {
+                    tma_load_3d(st, &kmap, 0, iw.g, row0, &bars[s], policy);
+                    tma_load_3d(st + S::KV_BYTES, &vmap, 0, iw.g, row0, &bars[s], policy);
+                }
+                if (row1 >= 0) {
+                    tma_load_3d(st + box * D * 2, &kmap, 0, iw.g, row1, &bars[s], policy);
+                    tma_load_3d(st + S::KV_BYTES + box * D * 2, &vmap, 0, iw.g, row1, &bars[s], policy);
+                }
+                if (seg_start)
+                    bulk_load(st + 2 * S::KV_BYTES, p.q + (int64_t(iw.b) * p.Hq + int64_t(iw.g) * G) * D,
+                              S::Q_BYTES, &bars[s]);
             }
-            const uint32_t sub_bytes = uint32_t(2 * box * D * 2);
-            const uint32_t bytes = (row0 >= 0 ? sub_bytes : 0u) + (row1 >= 0 ? sub_bytes : 0u) +
-                                   (seg_start ? uint32_t(S::Q_BYTES) : 0u);
-            StageMeta &mt = metas[s];
-            mt.b = iw.b;
-            mt.g = iw.g;
-            mt.t = iw.t;
-            mt.n = iw.n;
-            mt.L = len;
-            mt.seg_start = seg_start;
-            mbar_arrive_expect_tx(&bars[s], bytes);
-            if (row0 >= 0) {
-                tma_load_3d(st, &kmap, 0, iw.g, row0, &bars[s], policy);
-                tma_load_3d(st + S::KV_BYTES, &vmap, 0, iw.g, row0, &bars[s], policy);
+            if (k + 1 < ntiles) walker_advance(iw, scan, p.Hkv, p.B);
+        };
+
+        const int prologue = ntiles < kStages ? ntiles : kStages;
+        for (int k = 0; k < prologue; ++k) issue(k, int((kk + k) % kStages));
+
+        float2 q2[G][4], acc[G][4];
+        float m[G], l[G];
+        bool open = false;
+        int32_t seg_t0 = 0;
+        int k = 0;
+        for (; k < ntiles; ++k) {
+            const int s = int((kk + k) % kStages);
+            if (!mbar_wait_bounded(&bars[s], uint32_t((kk + k) / kStages) & 1u)) {
+                if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
+                break;
             }
-            if (row1 >= 0) {
-                tma_load_3d(st + box * D * 2, &kmap, 0, iw.g, row1, &bars[s], policy);
-                tma_load_3d(st + S::KV_BYTES + box * D * 2, &vmap, 0, iw.g, row1, &bars[s], policy);
+            const StageMeta mt = metas[s];
+            const uint8_t *st = stages + s * S::STAGE_BYTES;
+            if (!open) {
+                open = true;
+                seg_t0 = mt.t;
+                const uint16_t *qs = reinterpret_cast<const uint16_t *>(st + 2 * S::KV_BYTES);
+    #pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float2 f[4];
+                    unpack8x2(*reinterpret_cast<const uint4 *>(qs + h * D + c * 8), f);
+                    const float2 sc = make_float2(p.scale_log2, p.scale_log2);
+    #pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        q2[h][j] = __fmul2_rn(f[j], sc);
+                        acc[h][j] = make_float2(0.f, 0.f);
+                    }
+                    m[h] = -INFINITY;
+                    l[h] = 0.f;
+                }
             }
-            if (seg_start)
-                bulk_load(st + 2 * S::KV_BYTES, p.q + (int64_t(iw.b) * p.Hq + int64_t(iw.g) * G) * D,
-                          S::Q_BYTES, &bars[s]);
+            const int valid = min(kTile, mt.L - mt.t * kTile);
+            attend_tile<D, G>(st, valid, q2, m, l, acc, c, grp);
+            __syncwarp();
+            if (k + kStages < ntiles) issue(k + kStages, s);
+
+            if (mt.t == mt.n - 1 || k == ntiles - 1) {
+                // close the segment: fold the token groups, then write out or leave a partial
+    #pragma unroll
+                for (int mask = LPT; mask < 32; mask <<= 1)
+    #pragma unroll
+                    for (int h = 0; h < G; ++h)
+    #pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            acc[h][j].x += __shfl_xor_sync(kFull, acc[h][j].x, mask);
+                            acc[h][j].y += __shfl_xor_sync(kFull, acc[h][j].y, mask);
+                        }
+                float lt[G];
+    #pragma unroll
+                for (int h = 0; h < G; ++h) lt[h] = warp_sum(l[h]) * (1.0f / DUP);
+                const int piece_tiles = mt.t - seg_t0 + 1;
+                if (piece_tiles == mt.n) {  // this warp ran the whole (b, g): write the output
+                    if (grp == 0) {
+    #pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            const float inv = 1.0f / lt[h];
+                            uint4 o;
+                            o.x = pack_bf16x2(acc[h][0].x * inv, acc[h][0].y * inv);
+                            o.y = pack_bf16x2(acc[h][1].x * inv, acc[h][1].y * inv);
+                            o.z = pack_bf16x2(acc[h][2].x * inv, acc[h][2].y * inv);
+                            o.w = pack_bf16x2(acc[h][3].x * inv, acc[h][3].y * inv);
+                            *reinterpret_cast<uint4 *>(p.out + (int64_t(mt.b) * p.Hq + int64_t(mt.g) * G + h) * D +
+                                                       c * 8) = o;
+                        }
+                    }
+                } else {
+                    const int64_t slot = u + int64_t(mt.b) * p.Hkv + mt.g;
+                    if (grp == 0) {
+    #pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + ((slot * G + h) * D + c * 8));
+                            dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
+                            dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
+                        }
+                    }
+                    if (lane == 0)
+    #pragma unroll
+                        for (int h = 0; h < G; ++h)
+                            reinterpret_cast<float2 *>(p.ws_ml)[slot * G + h] = make_float2(m[h], lt[h]);
+                    // Publish the piece, then count it in; the warp that brings in the last
+                    // piece of this (b, g) merges them all.
+                    __threadfence();
+                    __syncwarp();
+                    const int64_t bg = int64_t(mt.b) * p.Hkv + mt.g;
+                    int last = 0;
+                    if (lane == 0)
+                        last = arrive_last(p.ws_count + bg, p.gen, uint32_t(piece_tiles), uint32_t(mt.n), p.err);
+                    if (__shfl_sync(kFull, last, 0)) {
+                        __threadfence();
+                        const long long x0 = (long long)p.Hkv * scan[mt.b] + (long long)mt.g * mt.n;
+                        merge_pieces<D, G>(p, part, bg, part.worker_of(x0), part.worker_of(x0 + mt.n - 1), mt.b,
+                                           mt.g, lane);
+                    }
+                }
+                open = false;
+            }
         }
-        if (k + 1 < ntiles) walker_advance(iw, scan, p.Hkv, p.B);
+        if (k < ntiles) {
+            // gave up on a wait: let every copy still in flight land, then stop for good
+            for (int j = k; j < ntiles && j < k + kStages; ++j)
+                mbar_wait_bounded(&bars[(kk + j) % kStages], uint32_t((kk + j) / kStages) & 1u);
+            dead = true;
+        }
+        kk += uint32_t(ntiles);
+
     };
 
-    const int prologue = ntiles < kStages ? ntiles : kStages;
-    for (int k = 0; k < prologue; ++k) issue(k, k);
-
-    float2 q2[G][4], acc[G][4];
-    float m[G], l[G];
-    bool open = false;
-    int32_t seg_t0 = 0;
-    int k = 0;
-    for (; k < ntiles; ++k) {
-        const int s = k % kStages;
-        if (!mbar_wait_bounded(&bars[s], uint32_t(k / kStages) & 1u)) {
-            if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
-            break;
-        }
-        const StageMeta mt = metas[s];
-        const uint8_t *st = stages + s * S::STAGE_BYTES;
-        if (!open) {
-            open = true;
-            seg_t0 = mt.t;
-            const uint16_t *qs = reinterpret_cast<const uint16_t *>(st + 2 * S::KV_BYTES);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float2 f[4];
-                unpack8x2(*reinterpret_cast<const uint4 *>(qs + h * D + c * 8), f);
-                const float2 sc = make_float2(p.scale_log2, p.scale_log2);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    q2[h][j] = __fmul2_rn(f[j], sc);
-                    acc[h][j] = make_float2(0.f, 0.f);
+    unsigned long long t_home = 0;
+    for (;;) {
+        const int slice = slice_sh[0];
+        if (slice < 0) break;
+        const bool home = slice == slice_sh[1];
+        if (home && threadIdx.x == 0) t_home = global_ns();
+        const long long u = (long long)slice * nwarps + warp;
+        long long rb, re;
+        part.range(u, rb, re);
+        if (re > rb && !dead) run_range(rb, re, u);
+        __syncthreads();
+        if (warp == 0) {
+            int next = -1;
+            if (adaptive) {
+                if (lane == 0 && bound[slice + 1] > bound[slice]) {
+                    // record for the next call: the weight this slice had and how long it took,
+                    // or "absent" when an SM id without a CTA of its own left it to this CTA
+                    const float us = float(global_ns() - t_home) * 1e-3f;
+                    p.ws_bal->weight[wp][slice] = home ? wts[slice] : 0.f;
+                    p.ws_bal->elapsed[wp][slice] = home ? fmaxf(us, 1e-3f) : 0.f;
+                    p.ws_bal->tag[wp][slice] = p.call ^ kTableMagic;
                 }
-                m[h] = -INFINITY;
-                l[h] = 0.f;
+                next = claim_leftover(p, bound, nslots, wp, true);
             }
+            if (lane == 0) slice_sh[0] = next;
         }
-        const int valid = min(kTile, mt.L - mt.t * kTile);
-        attend_tile<D, G>(st, valid, q2, m, l, acc, c, grp);
-        __syncwarp();
-        if (k + kStages < ntiles) issue(k + kStages, s);
-
-        if (mt.t == mt.n - 1 || k == ntiles - 1) {
-            // close the segment: fold the token groups, then write out or leave a partial
-#pragma unroll
-            for (int mask = LPT; mask < 32; mask <<= 1)
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        acc[h][j].x += __shfl_xor_sync(kFull, acc[h][j].x, mask);
-                        acc[h][j].y += __shfl_xor_sync(kFull, acc[h][j].y, mask);
-                    }
-            float lt[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) lt[h] = warp_sum(l[h]) * (1.0f / DUP);
-            if (seg_t0 == 0 && mt.t == mt.n - 1) {
-                if (grp == 0) {
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const float inv = 1.0f / lt[h];
-                        uint4 o;
-                        o.x = pack_bf16x2(acc[h][0].x * inv, acc[h][0].y * inv);
-                        o.y = pack_bf16x2(acc[h][1].x * inv, acc[h][1].y * inv);
-                        o.z = pack_bf16x2(acc[h][2].x * inv, acc[h][2].y * inv);
-                        o.w = pack_bf16x2(acc[h][3].x * inv, acc[h][3].y * inv);
-                        *reinterpret_cast<uint4 *>(p.out + (int64_t(mt.b) * p.Hq + int64_t(mt.g) * G + h) * D +
-                                                   c * 8) = o;
-                    }
-                }
-            } else {
-                const int64_t slot = int64_t(w) + int64_t(mt.b) * p.Hkv + mt.g;
-                if (grp == 0) {
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + ((slot * G + h) * D + c * 8));
-                        dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
-                        dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
-                    }
-                }
-                if (lane == 0)
-#pragma unroll
-                    for (int h = 0; h < G; ++h)
-                        reinterpret_cast<float2 *>(p.ws_ml)[slot * G + h] = make_float2(m[h], lt[h]);
-                // Publish the piece, then count it in; the warp that brings in the last
-                // piece of this (b, g) merges them all.
-                __threadfence();
-                __syncwarp();
-                const int64_t bg = int64_t(mt.b) * p.Hkv + mt.g;
-                const int64_t start = int64_t(p.Hkv) * scan[mt.b] + int64_t(mt.g) * mt.n;
-                const int64_t wf = ((start + 1) * P - 1) / T;     // worker holding the first tile
-                const int64_t wl = ((start + mt.n) * P - 1) / T;  // worker holding the last tile
-                int last = 0;
-                if (lane == 0) last = arrive_last(p.ws_count + bg, p.gen, uint32_t(wl - wf + 1), p.err);
-                if (__shfl_sync(kFull, last, 0)) {
-                    __threadfence();
-                    merge_pieces<D, G>(p, bg, wf, wl, mt.b, mt.g, lane);
-                }
-            }
-            open = false;
-        }
-    }
-    if (k < ntiles) {
-        // gave up on a wait: let every copy still in flight land before the CTA retires
-        for (int j = k; j < ntiles && j < k + kStages; ++j)
-            mbar_wait_bounded(&bars[j % kStages], uint32_t(j / kStages) & 1u);
+        __syncthreads();
     }
 }
 
@@ -608,7 +905,7 @@ __global__ void __launch_bounds__(Shape<D, G>::WARPS * 32, 1)
 struct LaunchArgs {
     DecodeParams p;
     const void *k_cache, *v_cache;
-    int sm_count, max_smem;
+    int device, sm_count, max_smem;
     int requested_workers;
     cudaStream_t stream;
 };
@@ -616,21 +913,102 @@ struct LaunchArgs {
 inline bool encode_cache_map(CUtensorMap *map, const void *base, int D, int Hkv, int64_t rows, int box_rows)
 {
     EncodeTiledFn enc = encode_tiled_fn();
-    if (!enc) return false;
+    if (!enc) {
+        record_cuda_error("cuTensorMapEncodeTiled", "driver entry point unavailable");
+        return false;
+    }
     const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(Hkv), cuuint64_t(rows)};
     const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(Hkv) * D * 2};
     const cuuint32_t box[3] = {cuuint32_t(D), 1u, cuuint32_t(box_rows)};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[64];
+        std::snprintf(msg, sizeof msg, "CUresult %d", int(r));
+        record_cuda_error("cuTensorMapEncodeTiled", msg);
+        return false;
+    }
+    return true;
+}
+
+// Tensor maps encode only (base address, shape, strides, box), so a map made
+// once for a cache tensor stays valid for every later call on it; keep the
+// most recent ones (an engine binds one k_cache / v_cache view per layer, as in
+// the nano-vllm KV-cache post, §3.2).
+inline bool cached_cache_map(CUtensorMap *map, int dev, const void *base, int D, int Hkv, int64_t rows, int box_rows)
+{
+    struct Entry {
+        int dev;
+        const void *base;
+        int D, Hkv;
+        int64_t rows;
+        int box;
+        CUtensorMap map;
+    };
+    constexpr size_t kMaxEntries = 256;
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    for (size_t i = 0; i < cache.size(); ++i) {
+        const Entry &e = cache[i];
+        if (e.dev == dev && e.base == base && e.D == D && e.Hkv == Hkv && e.rows == rows && e.box == box_rows) {
+            *map = e.map;
+            return true;
+        }
+    }
+    if (!encode_cache_map(map, base, D, Hkv, rows, box_rows)) return false;
+    if (cache.size() >= kMaxEntries) cache.erase(cache.begin());
+    cache.push_back(Entry{dev, base, D, Hkv, rows, box_rows, *map});
+    return true;
+}
+
+// cudaFuncSetAttribute once per device and kernel variant (it is a host-side
+// driver call; repeating it on every launch costs microseconds).  Keyed on
+// <D, G>: every variant has the same function-pointer type, so the memo must
+// be per instantiation.
+template <int D, int G, typename Kernel>
+inline bool ensure_smem_attribute(Kernel kern, int dev, size_t smem)
+{
+    static std::mutex mu;
+    static size_t configured[64] = {};
+    if (dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (configured[dev] >= smem) return true;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        record_cuda_error("cudaFuncSetAttribute", cudaGetErrorString(e));
+        return false;
+    }
+    configured[dev] = smem;
+    return true;
+}
+
+// Number of this call on this workspace (per device).  The kernel keeps its
+// load-balance table in the workspace, one half written per call: this number
+// picks the half, and the previous call's entries are recognised by its
+// number minus one.  A host-side memo only: losing it costs one call of
+// balance, never results.
+inline uint32_t next_call_number(int dev, const void *workspace)
+{
+    static std::mutex mu;
+    static std::unordered_map<uintptr_t, uint32_t> calls[64];
+    if (dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    auto &m = calls[dev];
+    if (m.size() > 65536) m.clear();
+    return ++m[reinterpret_cast<uintptr_t>(workspace)];
 }
 
 template <int D, int G>
 size_t decode_smem_bytes(int nwarps, int B)
 {
     using S = Shape<D, G>;
-    return size_t(nwarps) * kStages * (S::STAGE_BYTES + sizeof(StageMeta) + 8) + size_t(B + 1) * 4;
+    return size_t(nwarps) * kStages * (S::STAGE_BYTES + sizeof(StageMeta) + 8)  // rings, metadata, barriers
+           + size_t(kMaxSlots + 1) * 8 + size_t(kMaxSlots) * 4 + 32 * 4 + 16     // bounds, weights, scalars
+           + size_t(B + 1) * 4;                                                  // tile prefix
 }
 
 template <int D, int G>
@@ -641,28 +1019,31 @@ pkv_status launch_decode(LaunchArgs &a)
     const size_t smem = decode_smem_bytes<D, G>(nwarps, a.p.B);
     if (smem > size_t(a.max_smem)) return PKV_EUNSUPPORTED;
 
-    int workers = a.requested_workers > 0 ? a.requested_workers : a.sm_count * nwarps;
-    if (workers > PKV_MAX_WORKERS) workers = PKV_MAX_WORKERS;
-    a.p.num_workers = workers;
-    const int grid = (workers + nwarps - 1) / nwarps;
+    // Adaptive split: one CTA per SM, slices keyed by SM id.  Fixed split: the
+    // requested worker count rounded up to whole CTAs.
+    int grid = a.sm_count;
+    a.p.num_workers = 0;
+    if (a.requested_workers > 0) {
+        grid = (a.requested_workers + nwarps - 1) / nwarps;
+        if (grid > kMaxSlots) grid = kMaxSlots;
+        a.p.num_workers = a.requested_workers;
+    }
 
     const int box = a.p.bs < kTile ? a.p.bs : kTile;
     CUtensorMap kmap, vmap;
     const int64_t rows = int64_t(a.p.NB) * a.p.bs;
-    if (!encode_cache_map(&kmap, a.k_cache, D, a.p.Hkv, rows, box) ||
-        !encode_cache_map(&vmap, a.v_cache, D, a.p.Hkv, rows, box))
+    if (!cached_cache_map(&kmap, a.device, a.k_cache, D, a.p.Hkv, rows, box) ||
+        !cached_cache_map(&vmap, a.device, a.v_cache, D, a.p.Hkv, rows, box))
         return PKV_ECUDA;
 
     auto kern = paged_decode_kernel<D, G>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess) {
+    if (!ensure_smem_attribute<D, G>(kern, a.device, smem)) return PKV_ECUDA;
+    const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(nwarps * 32), smem, a.stream, kmap, vmap, a.p);
+    if (e != cudaSuccess) {
         cudaGetLastError();
-        return PKV_ECUDA;
+        return cuda_fail("paged_decode_kernel launch", e);
     }
-    if (launch_pdl(kern, dim3(grid), dim3(nwarps * 32), smem, a.stream, kmap, vmap, a.p) != cudaSuccess) {
-        cudaGetLastError();
-        return PKV_ECUDA;
-    }
-    return launch_status();
+    return launch_status("paged_decode_kernel launch");
 }
 
 using LaunchFn = pkv_status (*)(LaunchArgs &);
@@ -735,6 +1116,7 @@ extern "C" pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cach
     p.context_lens = context_lens;
     p.out = out;
     p.ws_count = reinterpret_cast<unsigned long long *>(wsb + ws.count_off);
+    p.ws_bal = reinterpret_cast<BalanceState *>(wsb + ws.bal_off);
     p.ws_ml = reinterpret_cast<float *>(wsb + ws.ml_off);
     p.ws_acc = reinterpret_cast<float *>(wsb + ws.acc_off);
     p.err = err_word;
@@ -750,8 +1132,10 @@ extern "C" pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cach
     p.scale_log2 = float(double(scale) * 1.4426950408889634);
     static std::atomic<uint32_t> generation{0};
     p.gen = generation.fetch_add(1u, std::memory_order_relaxed) + 1u;
+    p.call = next_call_number(dev.device, workspace);
     a.k_cache = k_cache;
     a.v_cache = v_cache;
+    a.device = dev.device;
     a.sm_count = dev.sm_count;
     a.max_smem = dev.max_smem_optin;
     a.requested_workers = num_workers;
@@ -784,16 +1168,20 @@ static void *static_scratch_address(pkv_status *status)
     static std::mutex mu;
     static void *addr[64] = {};
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
         cudaGetLastError();
+        record_cuda_error("cudaGetDevice", e != cudaSuccess ? cudaGetErrorString(e) : "device index out of range");
         *status = PKV_ECUDA;
         return nullptr;
     }
     std::lock_guard<std::mutex> lock(mu);
     if (!addr[dev]) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) {
+        const cudaError_t se = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (se != cudaSuccess || !p) {
             cudaGetLastError();
+            record_cuda_error("cudaGetSymbolAddress", se != cudaSuccess ? cudaGetErrorString(se) : "null address");
             *status = PKV_ECUDA;
             return nullptr;
         }

@@ -61,9 +61,21 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-inline pkv_status launch_status()
+// Remember why a call is about to return PKV_ECUDA (per host thread), for
+// pkv_last_cuda_error().
+void record_cuda_error(const char *where, const char *what);
+
+inline pkv_status cuda_fail(const char *where, cudaError_t e)
 {
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+    record_cuda_error(where, cudaGetErrorString(e));
+    return PKV_ECUDA;
+}
+
+// Status of the launch just made (clears the runtime's sticky launch error).
+inline pkv_status launch_status(const char *where)
+{
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PKV_OK : cuda_fail(where, e);
 }
 
 }  // namespace pkv

@@ -87,13 +87,15 @@ extern "C" pkv_status pkv_decode_slot_mapping(const int32_t *block_tables, int32
     if (!slot_mapping || (num_seqs > 0 && (!block_tables || !context_lens))) return PKV_EINVAL;
     const int threads = 128;
     const int blocks = (num_tokens + threads - 1) / threads;
-    if (launch_pdl(decode_slot_mapping_kernel, dim3(blocks), dim3(threads), 0, reinterpret_cast<cudaStream_t>(stream),
+    const cudaError_t e =
+        launch_pdl(decode_slot_mapping_kernel, dim3(blocks), dim3(threads), 0, reinterpret_cast<cudaStream_t>(stream),
                    block_tables, max_blocks_per_seq, context_lens, num_seqs, block_size, ilog2(block_size),
-                   num_blocks, slot_mapping, num_tokens, err_word) != cudaSuccess) {
+                   num_blocks, slot_mapping, num_tokens, err_word);
+    if (e != cudaSuccess) {
         cudaGetLastError();
-        return PKV_ECUDA;
+        return cuda_fail("decode_slot_mapping_kernel launch", e);
     }
-    return launch_status();
+    return launch_status("decode_slot_mapping_kernel launch");
 }
 
 extern "C" pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, const int32_t *slot_mapping,
@@ -110,12 +112,14 @@ extern "C" pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, const i
     if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
     const int32_t row_vecs = static_cast<int32_t>(row_bytes / 16);
     const int threads = row_vecs >= 256 ? 256 : ((row_vecs + 31) / 32) * 32;
-    if (launch_pdl(kv_store_kernel, dim3(num_tokens), dim3(threads), 0, reinterpret_cast<cudaStream_t>(stream),
+    const cudaError_t e =
+        launch_pdl(kv_store_kernel, dim3(num_tokens), dim3(threads), 0, reinterpret_cast<cudaStream_t>(stream),
                    reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v), slot_mapping,
                    reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache),
-                   static_cast<int64_t>(num_blocks) * block_size, row_vecs, err_word) != cudaSuccess) {
+                   static_cast<int64_t>(num_blocks) * block_size, row_vecs, err_word);
+    if (e != cudaSuccess) {
         cudaGetLastError();
-        return PKV_ECUDA;
+        return cuda_fail("kv_store_kernel launch", e);
     }
-    return launch_status();
+    return launch_status("kv_store_kernel launch");
 }

@@ -25,6 +25,7 @@ _P, _I32, _SZ, _F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c
 SIGNATURES = {
     "pkv_abi_version": (ctypes.c_int, []),
     "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pkv_last_cuda_error": (ctypes.c_char_p, []),
     "pkv_decode_slot_mapping": (ctypes.c_int, [_P, _I32, _P, _I32, _I32, _I32, _P, _I32, _P, _P]),
     "pkv_kv_store": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
     "pkv_paged_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
@@ -40,7 +41,8 @@ _lib = None
 
 class PkvError(RuntimeError):
     def __init__(self, status: int, what: str):
-        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        detail = f" [{load().pkv_last_cuda_error().decode()}]" if status == ECUDA else ""
+        super().__init__(f"{what}: {status_string(status)} (status {status}){detail}")
         self.status = status
 
 
