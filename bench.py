@@ -50,6 +50,27 @@ def dist_env():
     return ws, rank, local
 
 
+def rank_seed(workload: str, rank: int) -> int:
+    """Seed of this rank's batch: every rank runs its own, different batch (weak scaling)."""
+    from paged_kv_cache_62_gb300 import workloads
+    return workloads.SEED_BASE + workloads.ORDER.index(workload) + 1000 * rank
+
+
+def reduce_over_ranks(x: float, op: str, device) -> float:
+    """max / min of a per-rank scalar over all ranks (identity for one process)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.MIN)
+    return float(t.item())
+
+
+def job_bandwidth(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank moves bytes_per_rank_step per step; the step time is the slowest rank's."""
+    return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -158,8 +179,7 @@ def run_pkv(args):
     __graft_entry__.build()
     from paged_kv_cache_62_gb300 import pkv, workloads
 
-    wl = workloads.make(args.workload, dev, seed=workloads.SEED_BASE + workloads.ORDER.index(args.workload)
-                        + 1000 * rank)
+    wl = workloads.make(args.workload, dev, seed=rank_seed(args.workload, rank))
     s = wl.spec
     B, Hq, Hkv, D = s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim
     max_ctx = int(wl.lens_host().max())
@@ -196,10 +216,7 @@ def run_pkv(args):
         torch.cuda.synchronize()
         per = (time.perf_counter() - tw) / 10
         args.steps = int(min(50000, max(50, 2.0 / per)))
-        if ws > 1:
-            t = torch.tensor([args.steps], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MIN)
-            args.steps = int(t.item())
+        args.steps = int(reduce_over_ranks(args.steps, "min", dev))
 
     nlay = len(wl.layers)
     dec_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nlay)]
@@ -221,10 +238,7 @@ def run_pkv(args):
     ms = t0.elapsed_time(t1) / args.steps
     dec_ms = [a.elapsed_time(b) for row in dec_ev for (a, b) in row]
     dec_mean_ms = float(np.mean(dec_ms))
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_over_ranks(ms, "max", dev)
 
     # ---- end to end: host buffers in, host result out, through the same public calls
     host = {
@@ -266,16 +280,13 @@ def run_pkv(args):
     for _ in range(e2e_steps):
         e2e_step()
     e2e_ms = (time.perf_counter() - te) * 1e3 / e2e_steps
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_over_ranks(e2e_ms, "max", dev)
     torch.cuda.synchronize()
     assert err.item() == 0, f"device error word {err.item():#x}"
 
     nb = step_bytes(wl)
     peak, peak_kind = hbm_peak()
-    gbs = nb["step"] * ws / (ms * 1e-3) / 1e9
+    gbs = job_bandwidth(nb["step"], ws, ms)
     dec_gbs = nb["decode"] / (dec_mean_ms * 1e-3) / 1e9
     traffic = traffic_from_profile() if args.workload == "qwen3_0p6b" else None
     line = {
@@ -307,7 +318,7 @@ def run_pkv(args):
                      "algorithmic_bytes_per_launch": nb["decode"], "mean_launch_us": round(dec_mean_ms * 1e3, 2),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
-        "e2e": {"value": round(nb["step"] * ws / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(job_bandwidth(nb["step"], ws, e2e_ms), 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "note": "pinned host q/k/v/block_tables/context_lens in, bf16 out back, stream sync every step"},
         "clocks": clocks.summary(),
