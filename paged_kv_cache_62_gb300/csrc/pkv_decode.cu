@@ -9,53 +9,64 @@
 // state (m, l, acc) of the README.
 //
 // How (GB300 design):
-//  * The work is the list of 16-token tiles of every (sequence, kv head) pair,
-//    in (b, g, tile) order.  Every CTA rebuilds the per-sequence tile prefix
-//    sum in shared memory, and worker warp w takes tiles
-//    [w*T/P, (w+1)*T/P) -- an even split of the whole batch over all resident
-//    warps, so long and short sequences balance without a host round trip.
-//  * Each warp is its own pipeline: lane 0 issues TMA tensor copies (one K and
-//    one V box of 16 tokens x head_dim for the warp's kv head) into a 3-stage
-//    ring of shared-memory tiles, completion tracked by mbarrier transaction
-//    counts.  Block-table entries for tile k+32 are fetched while tile k is
-//    issued (one register per lane), so table lookups never stall the ring.
-//  * One K/V read serves all G query heads of the group.  A token row is
-//    split over D/8 lanes (16 bytes each); the per-lane partial dot products
-//    of a tile are finished by a shuffle reduce-scatter, the softmax max is a
-//    warp max, exponentials are ex2 on log2e-prescaled scores, and P.V uses
-//    the same lane split with fp32 accumulators.
-//  * A warp whose tile range covers a whole (b, g) writes bf16 output
-//    directly; otherwise it leaves its (m, l, acc) in the workspace and counts
-//    itself in on a per-(b, g) counter; the warp that brings in the last piece
-//    merges them all (split-K / flash-decoding without a second kernel).
+//  * Kv heads are taken in groups of HG (the largest divisor of Hkv <= 8).  A
+//    unit of work is TOKS = TW * SUB consecutive tokens of one (sequence,
+//    head group), TW = 16 tokens per warp and SUB = 8 / HG warps per head
+//    (see team_warps): whole contiguous cache rows of the group, moved by
+//    one TMA tensor copy per physical-block span into a shared-memory stage.
+//  * One CTA per SM: a producer warp streams units through a ring of 2-4
+//    stages (mbarrier transaction counts for "full", consumer arrivals for
+//    "empty"); HG * SUB consumer warps take one TW-token slice of one kv head
+//    each, so every consumer works on every stage and the CTA's warps finish
+//    together.  Block-table entries for 32 boxes at a time are fetched by the
+//    producer's lanes one batch ahead; q rows arrive by bulk copy in a
+//    separate 2-slot ring.
+//  * A consumer serves all G query heads of its kv head from one K/V read: a
+//    token row is split over D/8 lanes (16 bytes each), partial dot products
+//    are finished by a shuffle reduce-scatter, the softmax max is a warp vote
+//    plus (rarely) a warp max, exponentials are ex2 of log2e-prescaled scores,
+//    and P.V uses the same lane split with packed fp32 FMAs.
+//  * The batch's unit list is cut into one slice per SM id, each slice's size
+//    following the finishing times the previous call on the workspace saw.
+//    A CTA whose slice covers a whole (sequence, head group) writes bf16
+//    output directly; otherwise it leaves per-head partial states (m, l, acc)
+//    in the workspace and counts its units in on a per-(sequence, kv head)
+//    counter; the CTA that completes the count merges the pieces (split-K /
+//    flash-decoding without a second kernel).
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdio>
 #include <mutex>
 #include <type_traits>
 #include <unordered_map>
 #include <vector>
-#include <cmath>
 
 #include "pkv_device.cuh"
 #include "pkv_host.h"
 
 namespace pkv {
 
-constexpr int kTile = 16;      // tokens per tile
-constexpr int kMaxWarps = 12;  // warps per CTA (one CTA per SM) for small groups
-constexpr int kStages = 2;     // ring depth per warp
-
-// ------------------------------------------------------------------ load balance state
-// The tile list is cut into one slice per SM id, each slice into equal
-// per-warp ranges.  In the adaptive mode the slices' sizes follow what the
-// previous call on this workspace saw: a slice that finished late gets a
-// little less work, one that finished early a little more (SMs of a GB300
-// stream HBM at noticeably different, but stable, rates).  This only moves
-// work around: any table contents, garbage included, give correct results.
-constexpr int kMaxSlots = 512;  // slices: SM ids (adaptive) or CTAs (fixed split)
+constexpr int kMaxStages = 4;     // ring depth
+constexpr int kMaxSlots = 512;    // slices: SM ids (adaptive) or CTAs (fixed split)
 constexpr uint32_t kTableMagic = 0x62616c31u;
 
+// Consumer warps per CTA and tokens each takes from a stage (a stage holds
+// team_warps * warp_tokens token rows of head_dim, 64 KiB for head_dim 128).
+// Measured on the Qwen3-0.6B-shaped batch: 8 warps x 16 tokens with three
+// 64 KiB stages beats 16 warps x 8 tokens (17 warps leave 96 registers a
+// thread, and the G = 2 loop spills) and 8 warps x 8 tokens with six 32 KiB
+// stages (twice the per-stage overhead per token).  Kept as functions of the
+// group size so that a group-specific choice stays a one-line change.
+__host__ __device__ constexpr int team_warps(int) { return 8; }
+__host__ __device__ constexpr int warp_tokens(int) { return 16; }
+
+// ------------------------------------------------------------------ load balance state
+// In the adaptive mode a slice's size follows what the previous call on this
+// workspace saw: a slice that finished late gets a little less work, one
+// that finished early a little more (SMs of a GB300 stream HBM at noticeably
+// different, but stable, rates).  This only moves work around: any table
+// contents, garbage included, give correct results.
 struct BalanceState {
     float weight[2][kMaxSlots];           // weight a slice had in the call that wrote the entry (0: no SM)
     float elapsed[2][kMaxSlots];          // its run time in us (<= 0: present, nothing measured)
@@ -68,36 +79,101 @@ struct DecodeParams {
     const int32_t *block_tables;
     const int32_t *context_lens;
     uint16_t *out;
-    unsigned long long *ws_count;  // [B * Hkv] arrival counters: (call generation << 32) | tiles arrived
-    float *ws_ml;        // [slots][G][2] (m, l) per partial
-    float *ws_acc;       // [slots][G][D] unnormalised accumulators
-    BalanceState *ws_bal;  // per-SM speed estimates, claims, call counter
+    unsigned long long *ws_count;  // [B * Hkv] arrival counters: (call generation << 32) | units arrived
+    float *ws_ml;                  // [slots][G][2] (m, l) per partial
+    float *ws_acc;                 // [slots][G][D] unnormalised accumulators
+    BalanceState *ws_bal;
     int32_t *err;
     int32_t B, Hq, Hkv, bs, log2_bs, NB, max_blocks, len_limit;
-    int32_t num_workers;  // > 0: fixed split over ceil(num_workers / warps) CTAs; 0: adaptive split by SM
-    float scale_log2;     // scale * log2(e)
-    uint32_t gen;         // generation of this call (tags counters and claims)
-    uint32_t call;        // number of this call on this workspace: call & 1 picks the table half written
+    int32_t hg, nhg, sub, toks;  // kv heads per group, groups, warp slices per head, tokens per unit
+    int32_t boxtok, nbox;        // tokens per TMA box (min(toks, bs)) and boxes per unit
+    int32_t nst, cons, lg_nbox;  // ring stages, consumer warps (hg * sub), log2(nbox)
+    int32_t num_workers;         // > 0: fixed split over about num_workers / consumers CTAs; 0: adaptive
+    float scale_log2;            // scale * log2(e)
+    uint32_t gen;                // generation of this call (tags counters and claims)
+    uint32_t call;               // number of this call on this workspace: call & 1 picks the table half written
 };
 
-struct alignas(16) StageMeta {
-    int32_t b, g, t, n, L, seg_start, pad0, pad1;
+// What the producer tells the consumers about the unit in a stage.
+struct alignas(16) UnitMeta {
+    int32_t b, g, u, n;            // unit u of the n units of (b, group g); b < 0: no more work
+    int32_t L, flags, slice, pad;  // context length of b, kFirst | kLast | kSliceEnd, slice of the unit
 };
+constexpr int kFirst = 1;     // first unit of (b, g) in this slice
+constexpr int kLast = 2;      // last unit of (b, g) in this slice
+constexpr int kSliceEnd = 4;  // last unit of the slice
 
 template <int D, int G>
 struct Shape {
+    static constexpr int TW = warp_tokens(G);  // tokens per warp tile
     static constexpr int LPT = D / 8;          // lanes per token row (16 bytes each)
     static constexpr int TPI = 32 / LPT;       // tokens per warp step
-    static constexpr int NIT = kTile / TPI;    // steps per tile
+    static constexpr int NIT = TW / TPI;       // steps per tile
     static constexpr int DUP = LPT / NIT;      // lanes that end up holding each score
-    static constexpr int KV_BYTES = kTile * D * 2;
-    static constexpr int Q_BYTES = G * D * 2;
-    static constexpr int STAGE_BYTES = (2 * KV_BYTES + Q_BYTES + 127) / 128 * 128;
-    static_assert(LPT >= NIT && DUP >= 1, "tile too large for the lane split");
-    // Warps per CTA: as many as the register file allows without spilling
-    // (one CTA of WARPS*32 threads per SM, so at most 65536 / (WARPS*32) registers each).
-    static constexpr int WARPS = (G <= 3 || (D == 64 && G <= 5)) ? kMaxWarps : 8;
+    static_assert(LPT >= NIT && DUP >= 1 && NIT >= 1, "tile does not fit the lane split");
 };
+
+// Shared-memory layout, computed the same way on the host (size) and device (offsets).
+struct CtaLayout {
+    uint32_t kv_bytes, stage_bytes, q_bytes, comb_bytes;
+    uint32_t off_q, off_comb, off_meta, off_bar, off_bound, off_wts, off_red, off_sh, off_scan, total;
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// Floats per state in the combine buffer: G * (D + 2) rounded up to a
+// multiple of 4, so every block (and its float4 rows) is 16-byte aligned.
+__host__ __device__ inline int comb_stride(int D, int G) { return int(align_up(uint32_t(G * (D + 2)), 4)); }
+
+__host__ __device__ inline CtaLayout cta_layout(int D, int G, int hg, int sub, int nst, int B)
+{
+    CtaLayout l;
+    const int toks = warp_tokens(G) * sub;
+    l.kv_bytes = uint32_t(toks * hg * D * 2);
+    l.stage_bytes = align_up(2 * l.kv_bytes, 128);
+    l.q_bytes = align_up(uint32_t(hg * G * D * 2), 128);
+    // states of the non-leading warps of every head (the leader keeps its own in registers)
+    l.comb_bytes = sub > 1 ? align_up(uint32_t(hg * (sub - 1) * comb_stride(D, G) * 4), 128) : 0u;
+    uint32_t o = uint32_t(nst) * l.stage_bytes;
+    l.off_q = o;
+    o += 2 * l.q_bytes;
+    l.off_comb = o;
+    o += l.comb_bytes;
+    l.off_meta = o;
+    o += uint32_t(nst) * uint32_t(sizeof(UnitMeta));
+    l.off_bar = o;
+    o += uint32_t(2 * nst + 6) * 8;  // full / empty per stage, q full / empty x2, combine full / free
+    l.off_bound = align_up(o, 16);
+    o = l.off_bound + (kMaxSlots + 1) * 8;
+    l.off_wts = o;
+    o += kMaxSlots * 4;
+    l.off_red = o;
+    o += 64 * 4;
+    l.off_sh = o;
+    o += 32;
+    l.off_scan = o;
+    o += uint32_t(B + 1) * 4;
+    l.total = o;
+    return l;
+}
+
+// Kv-head grouping: HG = the largest divisor of Hkv that is <= 8; the warps
+// of a CTA split as HG heads x SUB token slices, SUB the largest power of two
+// <= team_warps(G) / HG (a power of two, so a unit is a whole number of
+// power-of-two TMA boxes).
+inline int head_group(int Hkv)
+{
+    for (int g = 8; g > 1; --g)
+        if (Hkv % g == 0) return g;
+    return 1;
+}
+
+inline int warp_slices(int G, int hg)
+{
+    int s = 1;
+    while (2 * s * hg <= team_warps(G)) s *= 2;
+    return s;
+}
 
 struct WsLayout {
     size_t bal_off, count_off, ml_off, acc_off, total;
@@ -105,13 +181,11 @@ struct WsLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Piece slots: one per (worker, sequence, kv head) boundary.  Worker ids
-// (slice * warps + warp) stay below kWorkerIds in both modes.
-constexpr size_t kWorkerIds = size_t(PKV_MAX_WORKERS) + 64;
-
+// Piece slots: (slice + b * nhg + group) * hg + head-in-group, one per piece.
 inline WsLayout ws_layout(int32_t B, int32_t G, int32_t Hkv, int32_t D)
 {
-    const size_t slots = kWorkerIds + size_t(B) * size_t(Hkv);
+    const int hg = head_group(Hkv);
+    const size_t slots = (size_t(kMaxSlots) + size_t(B) * size_t(Hkv / hg)) * size_t(hg);
     WsLayout w;
     w.bal_off = 0;
     w.count_off = align256(sizeof(BalanceState));
@@ -121,16 +195,18 @@ inline WsLayout ws_layout(int32_t B, int32_t G, int32_t Hkv, int32_t D)
     return w;
 }
 
-// ------------------------------------------------------------------ work list walking
+// ------------------------------------------------------------------ unit list walking
+// Units in (b, group, u) order; scan[b] = sum over earlier sequences of their
+// units per group, so the list holds nhg * scan[B] units.
 struct Walker {
-    int32_t b, g, t, n;
+    int32_t b, g, u, n;
 };
 
-__device__ __forceinline__ void walker_advance(Walker &w, const int32_t *scan, int32_t Hkv, int32_t B)
+__device__ __forceinline__ void walker_advance(Walker &w, const int32_t *scan, int32_t nhg, int32_t B)
 {
-    if (++w.t < w.n) return;
-    w.t = 0;
-    if (++w.g < Hkv) return;
+    if (++w.u < w.n) return;
+    w.u = 0;
+    if (++w.g < nhg) return;
     w.g = 0;
     do {
         ++w.b;
@@ -138,13 +214,13 @@ __device__ __forceinline__ void walker_advance(Walker &w, const int32_t *scan, i
     } while (w.n == 0);
 }
 
-// Position of global tile x (0 <= x < Hkv * scan[B]).
-__device__ __forceinline__ Walker walker_locate(const int32_t *scan, int32_t B, int32_t Hkv, int64_t x)
+// Position of unit x (0 <= x < nhg * scan[B]).
+__device__ __forceinline__ Walker walker_locate(const int32_t *scan, int32_t B, int32_t nhg, long long x)
 {
-    int lo = 0, hi = B;  // Hkv*scan[lo] <= x < Hkv*scan[hi]
+    int lo = 0, hi = B;  // nhg*scan[lo] <= x < nhg*scan[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (int64_t(Hkv) * scan[mid] <= x)
+        if ((long long)nhg * scan[mid] <= x)
             lo = mid;
         else
             hi = mid;
@@ -152,28 +228,15 @@ __device__ __forceinline__ Walker walker_locate(const int32_t *scan, int32_t B, 
     Walker w;
     w.b = lo;
     w.n = scan[lo + 1] - scan[lo];
-    const int64_t rem = x - int64_t(Hkv) * scan[lo];
-    w.g = int32_t(rem / w.n);
-    w.t = int32_t(rem - int64_t(w.g) * w.n);
+    const int32_t rem = int32_t(x - (long long)nhg * scan[lo]);  // < nhg * n <= total units < 2^31
+    w.g = rem / w.n;
+    w.u = rem - w.g * w.n;
     return w;
 }
 
-__device__ __forceinline__ void table_lookup(const DecodeParams &p, const Walker &w, int nsub, int32_t &e0,
-                                             int32_t &e1, int32_t &len)
-{
-    const int32_t *row = p.block_tables + int64_t(w.b) * p.max_blocks;
-    const int32_t pos0 = w.t * kTile;
-    e0 = __ldg(row + (pos0 >> p.log2_bs));
-    if (nsub == 2) {
-        const int32_t lb1 = (pos0 + kTile / 2) >> p.log2_bs;
-        e1 = lb1 < p.max_blocks ? __ldg(row + lb1) : -1;
-    }
-    len = __ldg(p.context_lens + w.b);
-}
-
-// Tiles per sequence -> exclusive prefix in scan[0..B].
+// Units per sequence -> exclusive prefix in scan[0..B].
 // `tmp` needs 32 ints of shared memory that is free during the call.
-__device__ void tile_prefix_scan(const DecodeParams &p, int32_t *scan, int32_t *tmp)
+__device__ void unit_prefix_scan(const DecodeParams &p, int32_t *scan, int32_t *tmp)
 {
     const int tid = threadIdx.x, nt = blockDim.x;
     const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
@@ -186,7 +249,7 @@ __device__ void tile_prefix_scan(const DecodeParams &p, int32_t *scan, int32_t *
         if (len < 0 || len > p.len_limit) {
             if (blockIdx.x == 0) flag_error(p.err, PKV_ERR_CONTEXT_RANGE);
         } else {
-            n = (len + kTile - 1) / kTile;
+            n = (len + p.toks - 1) / p.toks;
         }
         scan[i] = n;
         sum += n;
@@ -233,17 +296,17 @@ __device__ __forceinline__ void unpack8x2(const uint4 w, float2 f[4])
     for (int i = 0; i < 4; ++i) f[i] = make_float2(__uint_as_float(u[i] << 16), __uint_as_float(u[i] & 0xffff0000u));
 }
 
-// One 16-token tile of one (sequence, kv head) for the G query heads of the group.
-// Element pairs are handled with the packed fp32 FMA (two independent
-// round-to-nearest fp32 FMAs per instruction).
+// One TW-token tile of one (sequence, kv head) for the G query heads of the
+// group: Ks / Vs point at the tile's first K / V row, consecutive tokens are
+// `stride` elements apart.  Element pairs are handled with the packed fp32 FMA
+// (two independent round-to-nearest fp32 FMAs per instruction).
 template <int D, int G>
-__device__ __forceinline__ void attend_tile(const uint8_t *st, int valid, const float2 (&q2)[G][4], float (&m)[G],
-                                            float (&l)[G], float2 (&acc)[G][4], int c, int grp)
+__device__ __forceinline__ void attend_tile(const uint16_t *Ks, const uint16_t *Vs, int stride, int valid,
+                                            const float2 (&q2)[G][4], float (&m)[G], float (&l)[G],
+                                            float2 (&acc)[G][4], int c, int grp)
 {
     using S = Shape<D, G>;
     constexpr int LPT = S::LPT, TPI = S::TPI, NIT = S::NIT, DUP = S::DUP;
-    const uint16_t *Ks = reinterpret_cast<const uint16_t *>(st);
-    const uint16_t *Vs = reinterpret_cast<const uint16_t *>(st + S::KV_BYTES);
 
     // scores: lane (grp, c) forms the 8-element partial dot products of tokens i*TPI + grp
     float part[G][NIT];
@@ -251,7 +314,7 @@ __device__ __forceinline__ void attend_tile(const uint8_t *st, int valid, const 
     for (int i = 0; i < NIT; ++i) {
         const int tok = i * TPI + grp;
         float2 k2[4];
-        unpack8x2(*reinterpret_cast<const uint4 *>(Ks + tok * D + c * 8), k2);
+        unpack8x2(*reinterpret_cast<const uint4 *>(Ks + tok * stride + c * 8), k2);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             float2 a = __fmul2_rn(q2[h][0], k2[0]);
@@ -310,7 +373,7 @@ __device__ __forceinline__ void attend_tile(const uint8_t *st, int valid, const 
         for (int h = 0; h < G; ++h) ph[h] = __shfl_sync(kFull, pr[h], grp * LPT + i * DUP);
         if (tok < valid) {  // rows past L may hold anything, even NaN: never touch them
             float2 v2[4];
-            unpack8x2(*reinterpret_cast<const uint4 *>(Vs + tok * D + c * 8), v2);
+            unpack8x2(*reinterpret_cast<const uint4 *>(Vs + tok * stride + c * 8), v2);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 const float2 p2 = make_float2(ph[h], ph[h]);
@@ -320,38 +383,6 @@ __device__ __forceinline__ void attend_tile(const uint8_t *st, int valid, const 
         }
     }
 }
-
-// ------------------------------------------------------------------ partition
-// Worker u = slice * nwarps + j owns the tiles
-//   [bound[s] + len * j / nwarps, bound[s] + len * (j + 1) / nwarps),  len = bound[s+1] - bound[s].
-// Worker ids grow with tile index, so a piece's workspace slot u + (b * Hkv + g)
-// is unique (each step along the tile list raises u, or (b, g), or both).
-struct Partition {
-    const long long *bound;  // [nslots + 1] in shared memory
-    int nslots, nwarps;
-
-    __device__ __forceinline__ void range(long long u, long long &b, long long &e) const
-    {
-        const int s = int(u / nwarps), j = int(u - (long long)s * nwarps);
-        const long long lo = bound[s], len = bound[s + 1] - lo;
-        b = lo + len * j / nwarps;
-        e = lo + len * (j + 1) / nwarps;
-    }
-    // The (non-empty) worker that owns tile x, 0 <= x < bound[nslots].
-    __device__ __forceinline__ long long worker_of(long long x) const
-    {
-        int lo = 0, hi = nslots;  // bound[lo] <= x < bound[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (bound[mid] <= x)
-                lo = mid;
-            else
-                hi = mid;
-        }
-        const long long b0 = bound[lo], len = bound[lo + 1] - b0;
-        return (long long)lo * nwarps + ((x - b0 + 1) * nwarps - 1) / len;
-    }
-};
 
 // ------------------------------------------------------------------ load balance
 __device__ __forceinline__ unsigned smid()
@@ -368,17 +399,54 @@ __device__ __forceinline__ unsigned nsmid()
     return v;
 }
 
-// Sum of one float per thread over the CTA (fixed order: identical in every CTA).
-__device__ __forceinline__ float block_sum(float v, float *red)
+// Sums of two floats per thread over the CTA (fixed order: identical in every
+// CTA).  `red` holds 2 * 32 floats.
+__device__ __forceinline__ float2 block_sum2(float2 v, float *red)
 {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    v = warp_sum(v);
+    v.x = warp_sum(v.x);
+    v.y = warp_sum(v.y);
     __syncthreads();
-    if (lane == 0) red[wid] = v;
+    if (lane == 0) {
+        red[2 * wid] = v.x;
+        red[2 * wid + 1] = v.y;
+    }
     __syncthreads();
-    float t = 0.f;
-    for (int i = 0; i < nw; ++i) t += red[i];
+    float2 t = make_float2(0.f, 0.f);
+    for (int i = 0; i < nw; ++i) {
+        t.x += red[2 * i];
+        t.y += red[2 * i + 1];
+    }
     return t;
+}
+
+// The previous call's balance entries this thread reads in build_partition
+// (slices tid and tid + blockDim.x), loaded up front so that their memory
+// round trip overlaps the context-length loads of unit_prefix_scan.
+struct BalanceIn {
+    float w[2], t[2];
+    uint32_t tag[2];
+};
+static_assert(2 * (8 + 1) * 32 >= kMaxSlots, "two balance entries per thread must cover every slice");
+
+__device__ __forceinline__ BalanceIn load_balance(const DecodeParams &p, bool adaptive, int nslots)
+{
+    BalanceIn in;
+    const int rp = int(p.call & 1u) ^ 1;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int i = threadIdx.x + k * blockDim.x;
+        in.w[k] = 1.0f;
+        in.t[k] = 0.f;
+        in.tag[k] = 0u;
+        if (adaptive && i < nslots) {
+            // plain L2 loads: this half of the table is not written during this call
+            in.tag[k] = __ldcg(&p.ws_bal->tag[rp][i]);
+            in.w[k] = __ldcg(&p.ws_bal->weight[rp][i]);
+            in.t[k] = __ldcg(&p.ws_bal->elapsed[rp][i]);
+        }
+    }
+    return in;
 }
 
 // Slice bounds of this call.  Adaptive mode: each slice entry of the table
@@ -388,20 +456,21 @@ __device__ __forceinline__ float block_sum(float v, float *red)
 // 1).  Fixed mode: equal weights.  Every CTA computes the same bounds from the
 // same inputs in the same order; leaves the weights in w[].
 __device__ void build_partition(const DecodeParams &p, bool adaptive, int nslots, long long T, long long *bound,
-                                float *w, float *red)
+                                float *w, float *red, const BalanceIn &in)
 {
     const int tid = threadIdx.x, nt = blockDim.x;
-    const int rp = int(p.call & 1u) ^ 1;
     const uint32_t want = (p.call - 1u) ^ kTableMagic;
     // pass 1: raw weights (kept in w) and elapsed times (kept in bound[] as float bits)
     float tsum = 0.f, tcnt = 0.f;
     float *el = reinterpret_cast<float *>(bound);
-    for (int i = tid; i < nslots; i += nt) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int i = tid + k * nt;
+        if (i >= nslots) break;
         float x = 1.0f, t = 0.f;
-        // plain L2 loads: this half of the table is not written during this call
-        if (adaptive && __ldcg(&p.ws_bal->tag[rp][i]) == want) {
-            x = __ldcg(&p.ws_bal->weight[rp][i]);
-            t = __ldcg(&p.ws_bal->elapsed[rp][i]);
+        if (adaptive && in.tag[k] == want) {
+            x = in.w[k];
+            t = in.t[k];
             if (!(x >= 0.f) || !(x < 1.0e6f)) x = 1.0f;
             if (!(t < 1.0e9f)) t = 0.f;
             if (x > 0.f && t > 0.f) {
@@ -412,8 +481,9 @@ __device__ void build_partition(const DecodeParams &p, bool adaptive, int nslots
         w[i] = x;
         el[i] = t;
     }
-    tsum = block_sum(tsum, red);
-    tcnt = block_sum(tcnt, red);
+    const float2 tt = block_sum2(make_float2(tsum, tcnt), red);
+    tsum = tt.x;
+    tcnt = tt.y;
     const float tmean = tcnt > 0.f ? tsum / tcnt : 0.f;
     // pass 2: scale by the finishing-time ratio, then bound every weight to [1/4, 4] x mean
     float wsum = 0.f, wcnt = 0.f;
@@ -427,8 +497,9 @@ __device__ void build_partition(const DecodeParams &p, bool adaptive, int nslots
             wcnt += 1.f;
         }
     }
-    wsum = block_sum(wsum, red);
-    wcnt = block_sum(wcnt, red);
+    const float2 ww = block_sum2(make_float2(wsum, wcnt), red);
+    wsum = ww.x;
+    wcnt = ww.y;
     const float wmean = wcnt > 0.f ? wsum / wcnt : 1.0f;
     for (int i = tid; i < nslots; i += nt) {
         float x = wcnt > 0.f ? w[i] / wmean : 1.0f;  // mean 1 over present slices; none: equal weights
@@ -505,18 +576,18 @@ __device__ int claim_leftover(const DecodeParams &p, const long long *bound, int
 }
 
 // ------------------------------------------------------------------ split-K merge (a6)
-// Count the `tiles` of one piece of (b, g) in.  The counter word is (call
-// generation << 32) | tiles arrived; a word from another call (other
+// Count the `units` of one piece of (b, kv head) in.  The counter word is
+// (call generation << 32) | units arrived; a word from another call (other
 // generation, or leftover garbage) counts as zero, so the workspace never
 // needs clearing.  Returns 1 for the piece that completes the pair's `total`
-// tiles (and resets the word to 0).  Counting tiles, not pieces, lets any
-// partition of the tile list merge correctly.
-__device__ __forceinline__ int arrive_last(unsigned long long *ctr, uint32_t gen, uint32_t tiles, uint32_t total,
+// units (and resets the word to 0).  Counting units, not pieces, lets any
+// partition of the unit list merge correctly.
+__device__ __forceinline__ int arrive_last(unsigned long long *ctr, uint32_t gen, uint32_t units, uint32_t total,
                                            int32_t *err)
 {
     unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(ctr);
     for (int it = 0; it < (1 << 20); ++it) {
-        const uint32_t n = ((uint32_t(cur >> 32) == gen) ? uint32_t(cur) : 0u) + tiles;
+        const uint32_t n = ((uint32_t(cur >> 32) == gen) ? uint32_t(cur) : 0u) + units;
         const unsigned long long next = (static_cast<unsigned long long>(gen) << 32) | n;
         const unsigned long long seen = atomicCAS(ctr, cur, next);
         if (seen == cur) {
@@ -526,107 +597,123 @@ __device__ __forceinline__ int arrive_last(unsigned long long *ctr, uint32_t gen
         }
         cur = seen;
     }
-    flag_error(err, PKV_ERR_WAIT_TIMEOUT);  // unreachable in practice: a handful of warps contend
+    flag_error(err, PKV_ERR_WAIT_TIMEOUT);  // unreachable in practice: a handful of CTAs contend
     return 0;
 }
 
-// Merge the partial states of (b, g) held by the non-empty workers uf..ul:
+// Slice that holds unit x (non-empty by construction), 0 <= x < bound[nslots].
+__device__ __forceinline__ int slice_of(const long long *bound, int nslots, long long x)
+{
+    int lo = 0, hi = nslots;  // bound[lo] <= x < bound[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (bound[mid] <= x)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// Merge the partial states of (b, kv head kvh) left by the non-empty slices
+// sf..sl, piece slots (s + sigma) * hg + h:
 //   M = max m_i,  l = sum 2^(m_i - M) l_i,  out = sum 2^(m_i - M) acc_i / l
 // (the online-softmax algebra; m in log2 units).  The pieces were written by
 // other SMs, so they are read through L2 (ld.global.cg), BATCH pieces at a
 // time with independent loads, folded into a running (M, l, acc).
 template <int D, int G>
-__device__ __forceinline__ void merge_pieces(const DecodeParams &p, const Partition &part, long long bg, long long uf,
-                                             long long ul, int b, int g, int lane)
+__device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long long *bound, int sf, int sl,
+                                             long long sigma, int h, int b, int kvh, int lane)
 {
-    constexpr int PER = D / 32;                               // output values per lane
-    constexpr int BATCH = G <= 2 ? 4 : (G <= 4 ? 2 : 1);      // pieces loaded together
+    constexpr int PER = D / 32;                           // output values per lane
+    constexpr int BATCH = G <= 2 ? 4 : (G <= 4 ? 2 : 1);  // pieces loaded together
     using Vec = typename std::conditional<PER == 4, float4, float2>::type;
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);
     float M[G], lsum[G], a[G][PER];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        M[h] = -INFINITY;
-        lsum[h] = 0.f;
+    for (int hh = 0; hh < G; ++hh) {
+        M[hh] = -INFINITY;
+        lsum[hh] = 0.f;
 #pragma unroll
-        for (int e = 0; e < PER; ++e) a[h][e] = 0.f;
+        for (int e = 0; e < PER; ++e) a[hh][e] = 0.f;
     }
-    for (long long u0 = uf; u0 <= ul; u0 += BATCH) {
+    for (int s0 = sf; s0 <= sl; s0 += BATCH) {
         float2 st[BATCH][G];
         Vec v[BATCH][G];
         bool use[BATCH];
 #pragma unroll
         for (int k = 0; k < BATCH; ++k) {
-            long long rb = 0, re = 0;
-            if (u0 + k <= ul) part.range(u0 + k, rb, re);
-            use[k] = re > rb;                               // empty workers wrote nothing
-            const long long slot = (use[k] ? u0 + k : uf) + bg;
+            const int s = s0 + k;
+            use[k] = s <= sl && bound[s + 1] > bound[s];  // empty slices left nothing
+            const long long slot = ((use[k] ? s : sf) + sigma) * p.hg + h;
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                st[k][h] = __ldcg(ml + slot * G + h);
-                v[k][h] = __ldcg(reinterpret_cast<const Vec *>(p.ws_acc + (slot * G + h) * D + lane * PER));
+            for (int hh = 0; hh < G; ++hh) {
+                st[k][hh] = __ldcg(ml + slot * G + hh);
+                v[k][hh] = __ldcg(reinterpret_cast<const Vec *>(p.ws_acc + (slot * G + hh) * D + lane * PER));
             }
         }
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float mb = M[h];
+        for (int hh = 0; hh < G; ++hh) {
+            float mb = M[hh];
 #pragma unroll
             for (int k = 0; k < BATCH; ++k)
-                if (use[k]) mb = fmaxf(mb, st[k][h].x);
-            const float r = ex2(M[h] - mb);  // 0 while nothing has been folded in (M = -inf)
-            lsum[h] *= r;
+                if (use[k]) mb = fmaxf(mb, st[k][hh].x);
+            const float r = ex2(M[hh] - mb);  // 0 while nothing has been folded in (M = -inf)
+            lsum[hh] *= r;
 #pragma unroll
-            for (int e = 0; e < PER; ++e) a[h][e] *= r;
+            for (int e = 0; e < PER; ++e) a[hh][e] *= r;
 #pragma unroll
             for (int k = 0; k < BATCH; ++k) {
-                const float f = use[k] ? ex2(st[k][h].x - mb) : 0.f;
-                lsum[h] = fmaf(f, st[k][h].y, lsum[h]);
-                const float *x = reinterpret_cast<const float *>(&v[k][h]);
+                const float f = use[k] ? ex2(st[k][hh].x - mb) : 0.f;
+                lsum[hh] = fmaf(f, st[k][hh].y, lsum[hh]);
+                const float *x = reinterpret_cast<const float *>(&v[k][hh]);
 #pragma unroll
-                for (int e = 0; e < PER; ++e) a[h][e] = fmaf(f, x[e], a[h][e]);
+                for (int e = 0; e < PER; ++e) a[hh][e] = fmaf(f, x[e], a[hh][e]);
             }
-            M[h] = mb;
+            M[hh] = mb;
         }
     }
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        const float inv = 1.0f / lsum[h];
-        uint16_t *o = p.out + (int64_t(b) * p.Hq + int64_t(g) * G + h) * D + lane * PER;
+    for (int hh = 0; hh < G; ++hh) {
+        const float inv = 1.0f / lsum[hh];
+        uint16_t *o = p.out + (int64_t(b) * p.Hq + int64_t(kvh) * G + hh) * D + lane * PER;
         if constexpr (PER == 4)
-            *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16x2(a[h][0] * inv, a[h][1] * inv),
-                                                       pack_bf16x2(a[h][2] * inv, a[h][3] * inv));
+            *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16x2(a[hh][0] * inv, a[hh][1] * inv),
+                                                       pack_bf16x2(a[hh][2] * inv, a[hh][3] * inv));
         else
-            *reinterpret_cast<uint32_t *>(o) = pack_bf16x2(a[h][0] * inv, a[h][1] * inv);
+            *reinterpret_cast<uint32_t *>(o) = pack_bf16x2(a[hh][0] * inv, a[hh][1] * inv);
     }
 }
 
 // ------------------------------------------------------------------ main kernel
+// Block: p.cons consumer warps (warp w: kv head w / sub of the group, TW-token
+// slice w % sub of every unit) and one producer warp (warp p.cons).
 template <int D, int G>
-__global__ void __launch_bounds__(Shape<D, G>::WARPS * 32, 1)
+__global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeParams p)
 {
     using S = Shape<D, G>;
-    constexpr int LPT = S::LPT, DUP = S::DUP;
+    constexpr int LPT = S::LPT, DUP = S::DUP, TW = S::TW;
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int nwarps = blockDim.x >> 5;
+    const CtaLayout lay = cta_layout(D, G, p.hg, p.sub, p.nst, p.B);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = lane % LPT, grp = lane / LPT;
 
-    // shared memory: per-warp stage rings, their metadata and barriers, the
-    // slice bounds, the sanitised slice weights, a few scalars, the tile prefix
-    uint8_t *stages = smem + size_t(warp) * kStages * S::STAGE_BYTES;
-    StageMeta *metas =
-        reinterpret_cast<StageMeta *>(smem + size_t(nwarps) * kStages * S::STAGE_BYTES) + warp * kStages;
-    uint64_t *bars =
-        reinterpret_cast<uint64_t *>(smem + size_t(nwarps) * kStages * (S::STAGE_BYTES + sizeof(StageMeta))) +
-        warp * kStages;
-    long long *bound = reinterpret_cast<long long *>(smem + size_t(nwarps) * kStages *
-                                                                (S::STAGE_BYTES + sizeof(StageMeta) + 8));
-    float *wts = reinterpret_cast<float *>(bound + kMaxSlots + 1);
-    float *red = wts + kMaxSlots;
-    int *slice_sh = reinterpret_cast<int *>(red + 32);  // [0] slice to run next, [1] this CTA's own slice
-    int32_t *scan = reinterpret_cast<int32_t *>(slice_sh + 4);
+    uint8_t *stage0 = smem;
+    uint8_t *qbuf = smem + lay.off_q;
+    float *comb = reinterpret_cast<float *>(smem + lay.off_comb);
+    UnitMeta *metas = reinterpret_cast<UnitMeta *>(smem + lay.off_meta);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.off_bar);  // [nst] stage loaded (tx count)
+    uint64_t *empty = full + p.nst;                                     // [nst] stage released by consumers
+    uint64_t *qfull = empty + p.nst;                                    // [2] q rows loaded
+    uint64_t *qempty = qfull + 2;                                       // [2] q rows taken by consumers
+    uint64_t *cfull = qempty + 2;                                       // states written for a combine
+    uint64_t *cfree = cfull + 1;                                        // combine buffer read again
+    long long *bound = reinterpret_cast<long long *>(smem + lay.off_bound);
+    float *wts = reinterpret_cast<float *>(smem + lay.off_wts);
+    float *red = reinterpret_cast<float *>(smem + lay.off_red);
+    int *sh = reinterpret_cast<int *>(smem + lay.off_sh);  // [0] own slice, [2..3] its start time
+    int32_t *scan = reinterpret_cast<int32_t *>(smem + lay.off_scan);
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&kmap);
@@ -634,270 +721,367 @@ __global__ void __launch_bounds__(Shape<D, G>::WARPS * 32, 1)
     }
     griddep_launch_dependents();  // lets the next kernel in the stream get scheduled; it waits for this grid
     griddep_wait();               // inputs may come from the previous kernel in the stream
-    tile_prefix_scan(p, scan, reinterpret_cast<int32_t *>(smem));
 
-    const long long T = (long long)p.Hkv * scan[p.B];
-    // Sequences without tiles (L == 0, or a rejected length) get zeros; CTAs share the job.
+    // Slices: one per SM id, sized by measured finishing times (adaptive), or one per CTA (fixed).
+    const bool adaptive = p.num_workers == 0;
+    int nslots = int(gridDim.x);
+    if (adaptive) nslots = int(min(nsmid(), unsigned(kMaxSlots)));
+    const int wp = int(p.call & 1u);  // this call writes one half of the balance table, reads the other
+    // The set-up's global reads are all issued here, so together they cost one memory round
+    // trip: the claim on this SM id's slice (an exchange: the first CTA of this call to run on
+    // the SM id finds another generation there), the previous call's balance entries and, in
+    // unit_prefix_scan, the context lengths.
+    const unsigned my_sm = smid();
+    unsigned long long home_word = static_cast<unsigned long long>(p.gen) << 32;
+    if (threadIdx.x == 0 && adaptive && int(my_sm) < nslots)
+        home_word = atomicExch(&p.ws_bal->claim[my_sm], (static_cast<unsigned long long>(p.gen) << 32) | 1ull);
+    const BalanceIn bal_in = load_balance(p, adaptive, nslots);
+    unit_prefix_scan(p, scan, reinterpret_cast<int32_t *>(smem));
+    const long long T = (long long)p.nhg * scan[p.B];
+
+    // Sequences without units (L == 0, or a rejected length) get zeros; CTAs share the job.
     for (int b = blockIdx.x; b < p.B; b += gridDim.x)
         if (scan[b + 1] == scan[b])
             for (int i = threadIdx.x; i < p.Hq * D / 8; i += blockDim.x)
                 reinterpret_cast<uint4 *>(p.out + int64_t(b) * p.Hq * D)[i] = make_uint4(0u, 0u, 0u, 0u);
 
-    // Slices: one per SM id, sized by measured speed (adaptive), or one per CTA (fixed split).
-    const bool adaptive = p.num_workers == 0;
-    int nslots = int(gridDim.x);
-    if (adaptive) {
-        nslots = int(min(nsmid(), unsigned(kMaxSlots)));
-        nslots = min(nslots, int(kWorkerIds / nwarps));
-    }
-    const int wp = int(p.call & 1u);  // this call writes one half of the balance table, reads the other
-    build_partition(p, adaptive, nslots, T, bound, wts, red);
-    const Partition part{bound, nslots, nwarps};
+    build_partition(p, adaptive, nslots, T, bound, wts, red, bal_in);
 
-    if (lane == 0) {
-#pragma unroll
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.nst; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], uint32_t(p.cons));
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qempty[i], uint32_t(p.cons));
+        }
+        mbar_init(cfull, uint32_t(p.cons - p.hg));  // the non-leading warps' states
+        mbar_init(cfree, uint32_t(p.hg));           // read again by the leaders
         fence_barrier_init();
-    }
-    if (warp == 0) {
         int home = -1;
-        if (lane == 0) {
-            if (!adaptive)
-                home = int(blockIdx.x);
-            else if (int(smid()) < nslots && try_claim(&p.ws_bal->claim[smid()], p.gen))
-                home = int(smid());
-        }
-        home = __shfl_sync(kFull, home, 0);
-        const int first = (home < 0 && adaptive) ? claim_leftover(p, bound, nslots, wp, false) : home;
-        if (lane == 0) {
-            slice_sh[0] = first;
-            slice_sh[1] = home;
-        }
+        if (!adaptive)
+            home = int(blockIdx.x);
+        else if (uint32_t(home_word >> 32) != p.gen)
+            home = int(my_sm);
+        sh[0] = home;
     }
     __syncthreads();
 
-    const uint64_t policy = policy_evict_first();
-    const int box = p.bs < kTile ? p.bs : kTile;
-    const int nsub = kTile / box;
-    uint32_t kk = 0;     // tiles this warp has consumed: selects ring stage and barrier phase
-    bool dead = false;   // a wait timed out: do no more work
-
-    // One worker's tile range [begin, end); u is the worker id (sets the piece slots).
-    auto run_range = [&](long long begin, long long end, long long u) {
-        const int ntiles = int(end - begin);
-
-        // Block-table prefetch in batches of 32 tiles: lane j of `cur` holds the
-        // table entries (and context length) of tile kb + j of the current batch;
-        // `nxt` is loaded, all lanes at once, one batch ahead.  Two register sets,
-        // because the scoreboard tracks a register for the whole warp: a fresh
-        // load into the register that the next shuffle reads would stall it.
-        Walker fw = walker_locate(scan, p.B, p.Hkv, begin);  // first tile not yet prefetched
-        Walker iw = fw;                                       // next tile to issue
-        int32_t cur0 = -1, cur1 = -1, curL = 0, nxt0 = -1, nxt1 = -1, nxtL = 0;
-        auto prefetch_batch = [&](int kb) {  // tiles [kb, kb + 32) -> nxt; fw moves on to kb + 32
-            Walker mine = fw;
-    #pragma unroll 1
-            for (int j = 0; j < 32 && kb + j < ntiles; ++j) {
-                if (lane == j) mine = fw;
-                if (kb + j + 1 < ntiles) walker_advance(fw, scan, p.Hkv, p.B);
+    if (warp == p.cons) {
+        // ============================== producer warp ==============================
+        const uint64_t policy = policy_evict_first();
+        const uint32_t box_bytes = uint32_t(p.boxtok * p.hg * D * 2);
+        uint32_t kk = 0, segs = 0;  // units issued, q-ring uses
+        int rs = 0;                 // ring slot of unit kk (kk % nst, kept without a division)
+        uint32_t rph = 0;           // parity of that slot's use (kk / nst) & 1
+        bool dead = false;
+        int slice = sh[0];
+        if (slice < 0 && adaptive) slice = claim_leftover(p, bound, nslots, wp, false);
+        while (slice >= 0 && !dead) {
+            const long long lo = bound[slice], hi = bound[slice + 1];
+            if (lane == 0 && slice == sh[0])
+                *reinterpret_cast<unsigned long long *>(sh + 2) = global_ns();
+            const long long nunits = hi - lo, nboxes = nunits * p.nbox;
+            // Block-table prefetch, 32 boxes per batch: lane j of `cur` holds the entry (and the
+            // context length) of box kb + j; `nxt` is loaded one batch ahead.  Two register sets,
+            // because the scoreboard tracks a register for the whole warp.
+            Walker iw = nunits > 0 ? walker_locate(scan, p.B, p.nhg, lo) : Walker{0, 0, 0, 1};
+            int32_t cur_e = -1, cur_L = 0, nxt_e = -1, nxt_L = 0;
+            auto prefetch_batch = [&](long long kb) {  // boxes [kb, kb + 32) -> nxt, one per lane
+                const long long x = kb + lane;
+                if (x < nboxes) {
+                    const Walker mine = walker_locate(scan, p.B, p.nhg, lo + (x >> p.lg_nbox));
+                    const int32_t pos = mine.u * p.toks + int32_t(x & (p.nbox - 1)) * p.boxtok;
+                    // The entry is only used for pos < L, where pos / bs < max_blocks (lengths
+                    // beyond the table were rejected by the scan); clamping keeps the load in
+                    // the row and lets it go out together with the length's.
+                    const int32_t blk = min(pos >> p.log2_bs, p.max_blocks - 1);
+                    nxt_L = __ldg(p.context_lens + mine.b);
+                    nxt_e = __ldg(p.block_tables + (long long)mine.b * p.max_blocks + blk);
+                }
+            };
+            if (nunits > 0) {
+                prefetch_batch(0);
+                cur_e = nxt_e;
+                cur_L = nxt_L;
             }
-            if (kb + lane < ntiles) table_lookup(p, mine, nsub, nxt0, nxt1, nxtL);
-        };
-        prefetch_batch(0);
-        cur0 = nxt0;
-        cur1 = nxt1;
-        curL = nxtL;
-        if (ntiles > 32) prefetch_batch(32);
-
-        auto issue = [&](int k, int s) {
-            const int src = k & 31;
-            if (src == 0 && k > 0) {  // batch boundary: nxt was loaded 32 tiles ago
-                cur0 = nxt0;
-                cur1 = nxt1;
-                curL = nxtL;
-                if (k + 32 < ntiles) prefetch_batch(k + 32);
-            }
-            const int32_t e0 = __shfl_sync(kFull, cur0, src);
-            const int32_t e1 = __shfl_sync(kFull, cur1, src);
-            const int32_t len = __shfl_sync(kFull, curL, src);
-            if (lane == 0) {
-                uint8_t *st = stages + s * S::STAGE_BYTES;
-                const int seg_start = (k == 0 || iw.t == 0) ? 1 : 0;
-                const int32_t pos0 = iw.t * kTile;
-                int32_t row0 = -1, row1 = -1;
-                if (e0 >= 0 && e0 < p.NB)
-                    row0 = e0 * p.bs + (pos0 & (p.bs - 1));
-                else
-                    flag_error(p.err, PKV_ERR_BLOCK_RANGE);
-                if (nsub == 2 && pos0 + box < len) {
-                    if (e1 >= 0 && e1 < p.NB)
-                        row1 = e1 * p.bs;
+            for (long long k = 0; k < nunits; ++k) {
+                const long long kb0 = k * p.nbox;  // nbox is a power of two <= 16: batches start on units
+                if ((kb0 & 31) == 0 && k > 0) {
+                    cur_e = nxt_e;
+                    cur_L = nxt_L;
+                    if (kb0 + 32 < nboxes) prefetch_batch(kb0 + 32);
+                }
+                const int s = rs;
+                if (kk >= uint32_t(p.nst) && !mbar_wait_bounded(&empty[s], rph ^ 1u)) {
+                    dead = true;
+                    break;
+                }
+                const int src = int(kb0 & 31);
+                const int32_t len = __shfl_sync(kFull, cur_L, src);
+                const int32_t e = __shfl_sync(kFull, cur_e, (src + lane) & 31);  // lane j: box j's entry
+                const int flags = ((k == 0 || iw.u == 0) ? kFirst : 0) |
+                                  ((k == nunits - 1 || iw.u == iw.n - 1) ? kLast : 0) |
+                                  (k == nunits - 1 ? kSliceEnd : 0);
+                if (flags & kFirst) {  // q rows of this (b, group) for the consumers
+                    const int qs = int(segs & 1u);
+                    const uint32_t quse = segs >> 1;
+                    if (quse > 0 && !mbar_wait_bounded(&qempty[qs], (quse - 1) & 1u)) {
+                        dead = true;
+                        break;
+                    }
+                    if (lane == 0) {
+                        const uint32_t qb = uint32_t(p.hg * G * D * 2);
+                        mbar_arrive_expect_tx(&qfull[qs], qb);
+                        bulk_load(qbuf + qs * lay.q_bytes,
+                                  p.q + ((long long)iw.b * p.Hq + (long long)iw.g * p.hg * G) * D, qb, &qfull[qs]);
+                    }
+                    ++segs;
+                }
+                // box j of the unit: tokens [pos, pos + boxtok) of one physical block
+                const int32_t pos = iw.u * p.toks + lane * p.boxtok;
+                int32_t row = -1;
+                if (lane < p.nbox && pos < len) {
+                    if (e >= 0 && e < p.NB)
+                        row = e * p.bs + (pos & (p.bs - 1));
                     else
                         flag_error(p.err, PKV_ERR_BLOCK_RANGE);
                 }
-                const uint32_t sub_bytes = uint32_t(2 * box * D * 2);
-                const uint32_t bytes = (row0 >= 0 ? sub_bytes : 0u) + (row1 >= 0 ? sub_bytes : 0u) +
-                                       (seg_start ? uint32_t(S::Q_BYTES) : 0u);
-                StageMeta &mt = metas[s];
-                mt.b = iw.b;
-                mt.g = iw.g;
-                mt.t = iw.t;
-                mt.n = iw.n;
-                mt.L = len;
-                mt.seg_start = seg_start;
-                mbar_arrive_expect_tx(&bars[s], bytes);
-                if (row0 >= 0) {
-                    tma_load_3d(st, &kmap, 0, iw.g, row0, &bars[s], policy);
-                    tma_load_3d(st + S::KV_BYTES, &vmap, 0, iw.g, row0, &bars[s], policy);
+                const uint32_t nrows = __popc(__ballot_sync(kFull, row >= 0));
+                uint8_t *st = stage0 + s * lay.stage_bytes;
+                if (lane == 0) {
+                    UnitMeta &mt = metas[s];
+                    mt.b = iw.b;
+                    mt.g = iw.g;
+                    mt.u = iw.u;
+                    mt.n = iw.n;
+                    mt.L = len;
+                    mt.flags = flags;
+                    mt.slice = slice;
+                    mbar_arrive_expect_tx(&full[s], 2 * nrows * box_bytes);
                 }
-                if (row1 >= 0) {
-                    tma_load_3d(st + box * D * 2, &kmap, 0, iw.g, row1, &bars[s], policy);
-                    tma_load_3d(st + S::KV_BYTES + box * D * 2, &vmap, 0, iw.g, row1, &bars[s], policy);
+                __syncwarp();
+                if (row >= 0) {
+                    tma_load_3d(st + lane * box_bytes, &kmap, 0, iw.g * p.hg, row, &full[s], policy);
+                    tma_load_3d(st + lay.kv_bytes + lane * box_bytes, &vmap, 0, iw.g * p.hg, row, &full[s], policy);
                 }
-                if (seg_start)
-                    bulk_load(st + 2 * S::KV_BYTES, p.q + (int64_t(iw.b) * p.Hq + int64_t(iw.g) * G) * D,
-                              S::Q_BYTES, &bars[s]);
+                ++kk;
+                if (++rs == p.nst) {
+                    rs = 0;
+                    rph ^= 1u;
+                }
+                if (k + 1 < nunits) walker_advance(iw, scan, p.nhg, p.B);
+                if (k == 0 && nboxes > 32) prefetch_batch(32);  // after the first copies are on their way
             }
-            if (k + 1 < ntiles) walker_advance(iw, scan, p.Hkv, p.B);
-        };
+            slice = (adaptive && !dead) ? claim_leftover(p, bound, nslots, wp, true) : -1;
+        }
+        if (!dead) {  // end-of-work marker
+            if (kk < uint32_t(p.nst) || mbar_wait_bounded(&empty[rs], rph ^ 1u)) {
+                if (lane == 0) {
+                    metas[rs].b = -1;
+                    mbar_arrive(&full[rs]);
+                }
+                ++kk;
+            } else {
+                dead = true;
+            }
+        }
+        if (dead && lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
+        // let every copy this warp started land before the CTA can retire
+        for (uint32_t i = kk > uint32_t(p.nst) ? kk - uint32_t(p.nst) : 0u; i < kk; ++i)
+            mbar_wait_bounded(&full[i % uint32_t(p.nst)], (i / uint32_t(p.nst)) & 1u);
+        return;
+    }
 
-        const int prologue = ntiles < kStages ? ntiles : kStages;
-        for (int k = 0; k < prologue; ++k) issue(k, int((kk + k) % kStages));
-
-        float2 q2[G][4], acc[G][4];
-        float m[G], l[G];
-        bool open = false;
-        int32_t seg_t0 = 0;
-        int k = 0;
-        for (; k < ntiles; ++k) {
-            const int s = int((kk + k) % kStages);
-            if (!mbar_wait_bounded(&bars[s], uint32_t((kk + k) / kStages) & 1u)) {
+    // ============================== consumer warps ==============================
+    const int h = warp / p.sub, j = warp - h * p.sub;  // kv head in the group, token slice of the unit
+    const int c = lane % LPT, grp = lane / LPT;
+    const int stride = p.hg * D;                      // elements between consecutive tokens of a stage
+    const int home = sh[0];
+    uint32_t kk = 0, segs = 0, combs = 0;
+    int s = 0;           // ring slot of stage kk
+    uint32_t sph = 0;    // parity of its use
+    float2 q2[G][4], acc[G][4];
+    float m[G], l[G];
+    int u_first = 0;
+    for (;;) {
+        if (!mbar_wait_bounded(&full[s], sph)) {
+            if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
+            break;
+        }
+        const UnitMeta mt = metas[s];
+        if (mt.b < 0) break;
+        const uint8_t *st = stage0 + s * lay.stage_bytes;
+        if (mt.flags & kFirst) {
+            const int qs = int(segs & 1u);
+            if (!mbar_wait_bounded(&qfull[qs], (segs >> 1) & 1u)) {
                 if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
                 break;
             }
-            const StageMeta mt = metas[s];
-            const uint8_t *st = stages + s * S::STAGE_BYTES;
-            if (!open) {
-                open = true;
-                seg_t0 = mt.t;
-                const uint16_t *qs = reinterpret_cast<const uint16_t *>(st + 2 * S::KV_BYTES);
-    #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    float2 f[4];
-                    unpack8x2(*reinterpret_cast<const uint4 *>(qs + h * D + c * 8), f);
-                    const float2 sc = make_float2(p.scale_log2, p.scale_log2);
-    #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        q2[h][j] = __fmul2_rn(f[j], sc);
-                        acc[h][j] = make_float2(0.f, 0.f);
+            const uint16_t *qh = reinterpret_cast<const uint16_t *>(qbuf + qs * lay.q_bytes) + h * G * D;
+            const float2 sc = make_float2(p.scale_log2, p.scale_log2);
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                float2 f[4];
+                unpack8x2(*reinterpret_cast<const uint4 *>(qh + hh * D + c * 8), f);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    q2[hh][e] = __fmul2_rn(f[e], sc);
+                    acc[hh][e] = make_float2(0.f, 0.f);
+                }
+                m[hh] = -INFINITY;
+                l[hh] = 0.f;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&qempty[qs]);
+            ++segs;
+            u_first = mt.u;
+        }
+        const int tok0 = mt.u * p.toks + j * TW;
+        const int valid = min(TW, mt.L - tok0);
+        if (valid > 0) {
+            const uint16_t *Ks = reinterpret_cast<const uint16_t *>(st) + (j * TW * p.hg + h) * D;
+            const uint16_t *Vs = reinterpret_cast<const uint16_t *>(st + lay.kv_bytes) + (j * TW * p.hg + h) * D;
+            attend_tile<D, G>(Ks, Vs, stride, valid, q2, m, l, acc, c, grp);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        ++kk;
+        if (++s == p.nst) {
+            s = 0;
+            sph ^= 1u;
+        }
+
+        if (mt.flags & kLast) {
+            // close this warp's part of (b, group): fold the token groups
+#pragma unroll
+            for (int mask = LPT; mask < 32; mask <<= 1)
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[hh][e].x += __shfl_xor_sync(kFull, acc[hh][e].x, mask);
+                        acc[hh][e].y += __shfl_xor_sync(kFull, acc[hh][e].y, mask);
                     }
-                    m[h] = -INFINITY;
-                    l[h] = 0.f;
+            float lt[G];
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) lt[hh] = warp_sum(l[hh]) * (1.0f / DUP);
+            bool leader = true;
+            if (p.sub > 1) {
+                // the token slices of a kv head are combined by the head's first warp (j == 0):
+                // the others leave their states in shared memory
+                const uint32_t round = combs++;
+                const int cst = comb_stride(D, G);
+                leader = j == 0;
+                if (!leader) {
+                    if (round > 0 && !mbar_wait_bounded(cfree, (round - 1) & 1u)) break;
+                    float *mine = comb + (h * (p.sub - 1) + j - 1) * cst;
+                    if (grp == 0)
+#pragma unroll
+                        for (int hh = 0; hh < G; ++hh) {
+                            float4 *dst = reinterpret_cast<float4 *>(mine + hh * D + c * 8);
+                            dst[0] = make_float4(acc[hh][0].x, acc[hh][0].y, acc[hh][1].x, acc[hh][1].y);
+                            dst[1] = make_float4(acc[hh][2].x, acc[hh][2].y, acc[hh][3].x, acc[hh][3].y);
+                        }
+                    if (lane == 0)
+#pragma unroll
+                        for (int hh = 0; hh < G; ++hh) {
+                            mine[G * D + hh] = m[hh];
+                            mine[G * D + G + hh] = lt[hh];
+                        }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(cfull);
+                } else {
+                    if (!mbar_wait_bounded(cfull, round & 1u)) break;
+                    const float *others = comb + h * (p.sub - 1) * cst;
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh) {
+                        float M = m[hh];  // finite: the leader's slice starts every unit it saw
+                        for (int jj = 0; jj < p.sub - 1; ++jj) M = fmaxf(M, others[jj * cst + G * D + hh]);
+                        const float f0 = ex2(m[hh] - M);
+                        float ls = f0 * lt[hh];
+                        const float2 f02 = make_float2(f0, f0);
+                        float2 a[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) a[e] = __fmul2_rn(acc[hh][e], f02);
+                        for (int jj = 0; jj < p.sub - 1; ++jj) {
+                            const float *st2 = others + jj * cst;
+                            const float f = ex2(st2[G * D + hh] - M);  // 0 for a slice with no tokens
+                            ls = fmaf(f, st2[G * D + G + hh], ls);
+                            const float4 x0 = *reinterpret_cast<const float4 *>(st2 + hh * D + c * 8);
+                            const float4 x1 = *reinterpret_cast<const float4 *>(st2 + hh * D + c * 8 + 4);
+                            a[0] = make_float2(fmaf(f, x0.x, a[0].x), fmaf(f, x0.y, a[0].y));
+                            a[1] = make_float2(fmaf(f, x0.z, a[1].x), fmaf(f, x0.w, a[1].y));
+                            a[2] = make_float2(fmaf(f, x1.x, a[2].x), fmaf(f, x1.y, a[2].y));
+                            a[3] = make_float2(fmaf(f, x1.z, a[3].x), fmaf(f, x1.w, a[3].y));
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[hh][e] = a[e];
+                        m[hh] = M;
+                        lt[hh] = ls;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(cfree);
                 }
             }
-            const int valid = min(kTile, mt.L - mt.t * kTile);
-            attend_tile<D, G>(st, valid, q2, m, l, acc, c, grp);
-            __syncwarp();
-            if (k + kStages < ntiles) issue(k + kStages, s);
-
-            if (mt.t == mt.n - 1 || k == ntiles - 1) {
-                // close the segment: fold the token groups, then write out or leave a partial
-    #pragma unroll
-                for (int mask = LPT; mask < 32; mask <<= 1)
-    #pragma unroll
-                    for (int h = 0; h < G; ++h)
-    #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            acc[h][j].x += __shfl_xor_sync(kFull, acc[h][j].x, mask);
-                            acc[h][j].y += __shfl_xor_sync(kFull, acc[h][j].y, mask);
-                        }
-                float lt[G];
-    #pragma unroll
-                for (int h = 0; h < G; ++h) lt[h] = warp_sum(l[h]) * (1.0f / DUP);
-                const int piece_tiles = mt.t - seg_t0 + 1;
-                if (piece_tiles == mt.n) {  // this warp ran the whole (b, g): write the output
-                    if (grp == 0) {
-    #pragma unroll
-                        for (int h = 0; h < G; ++h) {
-                            const float inv = 1.0f / lt[h];
+            if (leader) {
+                const int kvh = mt.g * p.hg + h;
+                const int piece = mt.u - u_first + 1;
+                if (piece == mt.n) {  // this CTA ran the whole (b, group): write the output
+                    if (grp == 0)
+#pragma unroll
+                        for (int hh = 0; hh < G; ++hh) {
+                            const float inv = 1.0f / lt[hh];
                             uint4 o;
-                            o.x = pack_bf16x2(acc[h][0].x * inv, acc[h][0].y * inv);
-                            o.y = pack_bf16x2(acc[h][1].x * inv, acc[h][1].y * inv);
-                            o.z = pack_bf16x2(acc[h][2].x * inv, acc[h][2].y * inv);
-                            o.w = pack_bf16x2(acc[h][3].x * inv, acc[h][3].y * inv);
-                            *reinterpret_cast<uint4 *>(p.out + (int64_t(mt.b) * p.Hq + int64_t(mt.g) * G + h) * D +
+                            o.x = pack_bf16x2(acc[hh][0].x * inv, acc[hh][0].y * inv);
+                            o.y = pack_bf16x2(acc[hh][1].x * inv, acc[hh][1].y * inv);
+                            o.z = pack_bf16x2(acc[hh][2].x * inv, acc[hh][2].y * inv);
+                            o.w = pack_bf16x2(acc[hh][3].x * inv, acc[hh][3].y * inv);
+                            *reinterpret_cast<uint4 *>(p.out + ((long long)mt.b * p.Hq + (long long)kvh * G + hh) * D +
                                                        c * 8) = o;
                         }
-                    }
                 } else {
-                    const int64_t slot = u + int64_t(mt.b) * p.Hkv + mt.g;
-                    if (grp == 0) {
-    #pragma unroll
-                        for (int h = 0; h < G; ++h) {
-                            float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + ((slot * G + h) * D + c * 8));
-                            dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
-                            dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
+                    const long long sigma = (long long)mt.b * p.nhg + mt.g;
+                    const long long slot = (mt.slice + sigma) * p.hg + h;
+                    if (grp == 0)
+#pragma unroll
+                        for (int hh = 0; hh < G; ++hh) {
+                            float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + ((slot * G + hh) * D + c * 8));
+                            dst[0] = make_float4(acc[hh][0].x, acc[hh][0].y, acc[hh][1].x, acc[hh][1].y);
+                            dst[1] = make_float4(acc[hh][2].x, acc[hh][2].y, acc[hh][3].x, acc[hh][3].y);
                         }
-                    }
                     if (lane == 0)
-    #pragma unroll
-                        for (int h = 0; h < G; ++h)
-                            reinterpret_cast<float2 *>(p.ws_ml)[slot * G + h] = make_float2(m[h], lt[h]);
-                    // Publish the piece, then count it in; the warp that brings in the last
-                    // piece of this (b, g) merges them all.
+#pragma unroll
+                        for (int hh = 0; hh < G; ++hh)
+                            reinterpret_cast<float2 *>(p.ws_ml)[slot * G + hh] = make_float2(m[hh], lt[hh]);
+                    // publish the piece, then count its units in; the CTA that completes the
+                    // (b, kv head) merges all pieces
                     __threadfence();
                     __syncwarp();
-                    const int64_t bg = int64_t(mt.b) * p.Hkv + mt.g;
                     int last = 0;
                     if (lane == 0)
-                        last = arrive_last(p.ws_count + bg, p.gen, uint32_t(piece_tiles), uint32_t(mt.n), p.err);
+                        last = arrive_last(p.ws_count + (long long)mt.b * p.Hkv + kvh, p.gen, uint32_t(piece),
+                                           uint32_t(mt.n), p.err);
                     if (__shfl_sync(kFull, last, 0)) {
                         __threadfence();
-                        const long long x0 = (long long)p.Hkv * scan[mt.b] + (long long)mt.g * mt.n;
-                        merge_pieces<D, G>(p, part, bg, part.worker_of(x0), part.worker_of(x0 + mt.n - 1), mt.b,
-                                           mt.g, lane);
+                        const long long x0 = (long long)p.nhg * scan[mt.b] + (long long)mt.g * mt.n;
+                        merge_pieces<D, G>(p, bound, slice_of(bound, nslots, x0),
+                                           slice_of(bound, nslots, x0 + mt.n - 1), sigma, h, mt.b, kvh, lane);
                     }
                 }
-                open = false;
             }
         }
-        if (k < ntiles) {
-            // gave up on a wait: let every copy still in flight land, then stop for good
-            for (int j = k; j < ntiles && j < k + kStages; ++j)
-                mbar_wait_bounded(&bars[(kk + j) % kStages], uint32_t((kk + j) / kStages) & 1u);
-            dead = true;
+        if ((mt.flags & kSliceEnd) && adaptive && warp == 0 && lane == 0) {
+            // balance record for the next call: this slice's weight and run time, or "absent"
+            // when an SM id without a CTA of its own left the slice to this CTA
+            const bool own = mt.slice == home;
+            const float us =
+                float(global_ns() - *reinterpret_cast<volatile unsigned long long *>(sh + 2)) * 1e-3f;
+            p.ws_bal->weight[wp][mt.slice] = own ? wts[mt.slice] : 0.f;
+            p.ws_bal->elapsed[wp][mt.slice] = own ? fmaxf(us, 1e-3f) : 0.f;
+            p.ws_bal->tag[wp][mt.slice] = p.call ^ kTableMagic;
         }
-        kk += uint32_t(ntiles);
-
-    };
-
-    unsigned long long t_home = 0;
-    for (;;) {
-        const int slice = slice_sh[0];
-        if (slice < 0) break;
-        const bool home = slice == slice_sh[1];
-        if (home && threadIdx.x == 0) t_home = global_ns();
-        const long long u = (long long)slice * nwarps + warp;
-        long long rb, re;
-        part.range(u, rb, re);
-        if (re > rb && !dead) run_range(rb, re, u);
-        __syncthreads();
-        if (warp == 0) {
-            int next = -1;
-            if (adaptive) {
-                if (lane == 0 && bound[slice + 1] > bound[slice]) {
-                    // record for the next call: the weight this slice had and how long it took,
-                    // or "absent" when an SM id without a CTA of its own left it to this CTA
-                    const float us = float(global_ns() - t_home) * 1e-3f;
-                    p.ws_bal->weight[wp][slice] = home ? wts[slice] : 0.f;
-                    p.ws_bal->elapsed[wp][slice] = home ? fmaxf(us, 1e-3f) : 0.f;
-                    p.ws_bal->tag[wp][slice] = p.call ^ kTableMagic;
-                }
-                next = claim_leftover(p, bound, nslots, wp, true);
-            }
-            if (lane == 0) slice_sh[0] = next;
-        }
-        __syncthreads();
     }
 }
 
@@ -910,7 +1094,10 @@ struct LaunchArgs {
     cudaStream_t stream;
 };
 
-inline bool encode_cache_map(CUtensorMap *map, const void *base, int D, int Hkv, int64_t rows, int box_rows)
+// Tensor map over one cache: dims (head_dim, kv heads, NB * bs rows); a box is
+// box_rows tokens x box_heads kv heads x head_dim (whole contiguous rows of a head group).
+inline bool encode_cache_map(CUtensorMap *map, const void *base, int D, int Hkv, int64_t rows, int box_heads,
+                             int box_rows)
 {
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) {
@@ -919,7 +1106,7 @@ inline bool encode_cache_map(CUtensorMap *map, const void *base, int D, int Hkv,
     }
     const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(Hkv), cuuint64_t(rows)};
     const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(Hkv) * D * 2};
-    const cuuint32_t box[3] = {cuuint32_t(D), 1u, cuuint32_t(box_rows)};
+    const cuuint32_t box[3] = {cuuint32_t(D), cuuint32_t(box_heads), cuuint32_t(box_rows)};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -937,14 +1124,15 @@ inline bool encode_cache_map(CUtensorMap *map, const void *base, int D, int Hkv,
 // once for a cache tensor stays valid for every later call on it; keep the
 // most recent ones (an engine binds one k_cache / v_cache view per layer, as in
 // the nano-vllm KV-cache post, §3.2).
-inline bool cached_cache_map(CUtensorMap *map, int dev, const void *base, int D, int Hkv, int64_t rows, int box_rows)
+inline bool cached_cache_map(CUtensorMap *map, int dev, const void *base, int D, int Hkv, int64_t rows, int box_heads,
+                             int box_rows)
 {
     struct Entry {
         int dev;
         const void *base;
         int D, Hkv;
         int64_t rows;
-        int box;
+        int box_heads, box;
         CUtensorMap map;
     };
     constexpr size_t kMaxEntries = 256;
@@ -953,14 +1141,15 @@ inline bool cached_cache_map(CUtensorMap *map, int dev, const void *base, int D,
     std::lock_guard<std::mutex> lock(mu);
     for (size_t i = 0; i < cache.size(); ++i) {
         const Entry &e = cache[i];
-        if (e.dev == dev && e.base == base && e.D == D && e.Hkv == Hkv && e.rows == rows && e.box == box_rows) {
+        if (e.dev == dev && e.base == base && e.D == D && e.Hkv == Hkv && e.rows == rows && e.box_heads == box_heads &&
+            e.box == box_rows) {
             *map = e.map;
             return true;
         }
     }
-    if (!encode_cache_map(map, base, D, Hkv, rows, box_rows)) return false;
+    if (!encode_cache_map(map, base, D, Hkv, rows, box_heads, box_rows)) return false;
     if (cache.size() >= kMaxEntries) cache.erase(cache.begin());
-    cache.push_back(Entry{dev, base, D, Hkv, rows, box_rows, *map});
+    cache.push_back(Entry{dev, base, D, Hkv, rows, box_heads, box_rows, *map});
     return true;
 }
 
@@ -1003,42 +1192,36 @@ inline uint32_t next_call_number(int dev, const void *workspace)
 }
 
 template <int D, int G>
-size_t decode_smem_bytes(int nwarps, int B)
-{
-    using S = Shape<D, G>;
-    return size_t(nwarps) * kStages * (S::STAGE_BYTES + sizeof(StageMeta) + 8)  // rings, metadata, barriers
-           + size_t(kMaxSlots + 1) * 8 + size_t(kMaxSlots) * 4 + 32 * 4 + 16     // bounds, weights, scalars
-           + size_t(B + 1) * 4;                                                  // tile prefix
-}
-
-template <int D, int G>
 pkv_status launch_decode(LaunchArgs &a)
 {
-    int nwarps = Shape<D, G>::WARPS;
-    while (nwarps > 1 && decode_smem_bytes<D, G>(nwarps, a.p.B) > size_t(a.max_smem)) --nwarps;
-    const size_t smem = decode_smem_bytes<D, G>(nwarps, a.p.B);
-    if (smem > size_t(a.max_smem)) return PKV_EUNSUPPORTED;
+    DecodeParams &p = a.p;
+    // ring depth: as many stages (up to kMaxStages) as the shared memory holds
+    int nst = kMaxStages;
+    while (nst > 2 && cta_layout(D, G, p.hg, p.sub, nst, p.B).total > uint32_t(a.max_smem)) --nst;
+    const CtaLayout lay = cta_layout(D, G, p.hg, p.sub, nst, p.B);
+    if (lay.total > uint32_t(a.max_smem)) return PKV_EUNSUPPORTED;
+    p.nst = nst;
 
-    // Adaptive split: one CTA per SM, slices keyed by SM id.  Fixed split: the
-    // requested worker count rounded up to whole CTAs.
+    // Adaptive split: one CTA per SM, slices keyed by SM id.  Fixed split:
+    // about num_workers / consumers CTAs with equal slices.
     int grid = a.sm_count;
-    a.p.num_workers = 0;
+    p.num_workers = 0;
     if (a.requested_workers > 0) {
-        grid = (a.requested_workers + nwarps - 1) / nwarps;
+        grid = (a.requested_workers + p.cons - 1) / p.cons;
         if (grid > kMaxSlots) grid = kMaxSlots;
-        a.p.num_workers = a.requested_workers;
+        p.num_workers = a.requested_workers;
     }
+    if (grid > kMaxSlots) grid = kMaxSlots;
 
-    const int box = a.p.bs < kTile ? a.p.bs : kTile;
     CUtensorMap kmap, vmap;
-    const int64_t rows = int64_t(a.p.NB) * a.p.bs;
-    if (!cached_cache_map(&kmap, a.device, a.k_cache, D, a.p.Hkv, rows, box) ||
-        !cached_cache_map(&vmap, a.device, a.v_cache, D, a.p.Hkv, rows, box))
+    const int64_t rows = int64_t(p.NB) * p.bs;
+    if (!cached_cache_map(&kmap, a.device, a.k_cache, D, p.Hkv, rows, p.hg, p.boxtok) ||
+        !cached_cache_map(&vmap, a.device, a.v_cache, D, p.Hkv, rows, p.hg, p.boxtok))
         return PKV_ECUDA;
 
     auto kern = paged_decode_kernel<D, G>;
-    if (!ensure_smem_attribute<D, G>(kern, a.device, smem)) return PKV_ECUDA;
-    const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(nwarps * 32), smem, a.stream, kmap, vmap, a.p);
+    if (!ensure_smem_attribute<D, G>(kern, a.device, lay.total)) return PKV_ECUDA;
+    const cudaError_t e = launch_pdl(kern, dim3(grid), dim3((p.cons + 1) * 32), lay.total, a.stream, kmap, vmap, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return cuda_fail("paged_decode_kernel launch", e);
@@ -1099,9 +1282,9 @@ extern "C" pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cach
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_EINVAL;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PKV_EINVAL;
     const int64_t len_limit = std::min<int64_t>(max_context_len, int64_t(max_blocks_per_seq) * block_size);
-    const int64_t max_tiles = int64_t(num_seqs) * ((len_limit + kTile - 1) / kTile);
-    if (max_tiles > INT32_MAX) return PKV_EUNSUPPORTED;
-    if (num_workers > 0 && int64_t(num_kv_heads) * max_tiles / num_workers + 1 > INT32_MAX) return PKV_EUNSUPPORTED;
+    // unit counts (and positions in the unit list) are kept in 32 bits
+    const int64_t max_units = int64_t(num_kv_heads) * num_seqs * ((len_limit + 7) / 8);
+    if (max_units > INT32_MAX) return PKV_EUNSUPPORTED;
     const WsLayout ws = ws_layout(num_seqs, G, num_kv_heads, head_dim);
     if (!workspace || workspace_bytes < ws.total || !aligned16(workspace)) return PKV_EWORKSPACE;
 
@@ -1128,6 +1311,15 @@ extern "C" pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cach
     p.NB = num_blocks;
     p.max_blocks = max_blocks_per_seq;
     p.len_limit = int32_t(len_limit);
+    p.hg = head_group(num_kv_heads);
+    p.nhg = num_kv_heads / p.hg;
+    p.sub = warp_slices(G, p.hg);
+    p.toks = warp_tokens(G) * p.sub;
+    p.boxtok = std::min(p.toks, block_size);
+    p.nbox = p.toks / p.boxtok;
+    p.lg_nbox = ilog2(p.nbox);
+    p.cons = p.hg * p.sub;
+    p.nst = 2;
     p.num_workers = 0;
     p.scale_log2 = float(double(scale) * 1.4426950408889634);
     static std::atomic<uint32_t> generation{0};
