@@ -64,8 +64,8 @@ __host__ __device__ constexpr int warp_tokens(int) { return 16; }
 // ------------------------------------------------------------------ load balance state
 // In the adaptive mode a slice's size follows what the previous call on this
 // workspace saw: a slice that finished late gets a little less work, one
-// that finished early a little more (SMs of a GB300 stream HBM at noticeably
-// different, but stable, rates).  This only moves work around: any table
+// that finished early a little more (SMs of a GB300 stream HBM at somewhat
+// different rates).  This only moves work around: any table
 // contents, garbage included, give correct results.
 struct BalanceState {
     float weight[2][kMaxSlots];           // weight a slice had in the call that wrote the entry (0: no SM)
@@ -451,9 +451,11 @@ __device__ __forceinline__ BalanceIn load_balance(const DecodeParams &p, bool ad
 
 // Slice bounds of this call.  Adaptive mode: each slice entry of the table
 // half written by the previous call on this workspace (call - 1) keeps its
-// weight scaled by clamp(mean elapsed / its elapsed, 0.8, 1.25) (weight 0: an
-// SM id without a CTA); entries from any other call count as unknown (weight
-// 1).  Fixed mode: equal weights.  Every CTA computes the same bounds from the
+// weight scaled by clamp(sqrt(mean elapsed / its elapsed), 0.9, 1.12)
+// (weight 0: an SM id without a CTA) -- a damped step: a slice's time also
+// varies with the data it held, and the full step overcorrects (consecutive
+// calls' finishing times then anti-correlate); entries from any other call
+// count as unknown (weight 1).  Fixed mode: equal weights.  Every CTA computes the same bounds from the
 // same inputs in the same order; leaves the weights in w[].
 __device__ void build_partition(const DecodeParams &p, bool adaptive, int nslots, long long T, long long *bound,
                                 float *w, float *red, const BalanceIn &in)
@@ -490,7 +492,7 @@ __device__ void build_partition(const DecodeParams &p, bool adaptive, int nslots
     for (int i = tid; i < nslots; i += nt) {
         float x = w[i];
         const float t = el[i];
-        if (x > 0.f && t > 0.f && tmean > 0.f) x *= fminf(fmaxf(tmean / t, 0.8f), 1.25f);
+        if (x > 0.f && t > 0.f && tmean > 0.f) x *= fminf(fmaxf(sqrtf(tmean / t), 0.9f), 1.12f);
         w[i] = x;
         if (x > 0.f) {
             wsum += x;

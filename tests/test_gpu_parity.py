@@ -174,6 +174,27 @@ def test_forced_splits(workers):
     assert torch.all(out[lens.index(0)].float() == 0)
 
 
+@pytest.mark.parametrize("bs", [16, 256])
+def test_adaptive_split_over_repeated_calls(bs):
+    """Default split, eight calls on one workspace: each call sizes its per-SM slices from the
+    previous call's timings, so the partition (and the split-K pieces) change from call to call;
+    every call must match the oracle, whatever the partition it ended up with."""
+    rng = np.random.default_rng(62)
+    lens = rng.integers(1, 3000, size=40).tolist() + [0, 1, 8, 9, 127, 128, 129, 4096]
+    q, kc, vc, bt, lens_t = synth(len(lens), 0, 16, 8, 128, bs, seed=bs, lens=lens)
+    want = oracle_of(q, kc, vc, bt, lens_t, 0.0884)
+    B, Hq, D = q.shape
+    ws = pkv.alloc_workspace(B, Hq, kc.shape[2], D)
+    ws.fill_(0xFF)
+    err = err_word()
+    for call in range(8):
+        out = torch.full_like(q, float("nan"))
+        pkv.paged_decode(q, kc, vc, bt, lens_t, 0.0884, out, ws, num_workers=0, err_word=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0, hex(err.item())
+        check_close(out, want, f"call {call}")
+
+
 def test_workers_do_not_change_results_much():
     lens = [700, 1500, 33]
     q, kc, vc, bt, lens_t = synth(len(lens), 0, 16, 8, 128, 256, seed=5, lens=lens)
