@@ -61,6 +61,7 @@ typedef enum {
 #define PKV_ERR_BLOCK_RANGE 0x2   /* block table entry that must be read lies outside [0, num_blocks) */
 #define PKV_ERR_CONTEXT_RANGE 0x4 /* context_len < 0 or above min(max_context_len, max_blocks*block_size) */
 #define PKV_ERR_WAIT_TIMEOUT 0x8  /* a bounded wait on an asynchronous copy gave up                    */
+#define PKV_ERR_WORKSPACE 0x10    /* decode workspace control block not in a state this library left   */
 
 /* Version of this ABI (bumped on any incompatible change). */
 PKV_API int pkv_abi_version(void);
@@ -131,11 +132,16 @@ PKV_API pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, const int3
  * Bytes of device workspace that pkv_paged_decode needs for these sizes
  * (split-K partial states, one arrival counter per (sequence, kv head), and a
  * small load-balance record).  Depends only on the arguments; 0 means the
- * sizes are invalid.  The workspace needs no initialisation: counters and
- * claims are tagged with a per-call generation, so leftovers from earlier
- * calls (or garbage) count as zero.  Between calls it keeps per-SM speed
- * estimates that size each SM's share of the next call; they affect only
- * speed, never results.  Calls that may run at the same time need separate
+ * sizes are invalid.  The workspace must be zero-filled (cudaMemset) once
+ * before its first use; from then on the library keeps it consistent, for
+ * any sizes of later calls.  Its control block carries a call epoch that the
+ * last CTA of every call advances on the device, so nothing per call is
+ * baked into the launch and a captured CUDA graph may replay a call any
+ * number of times; the per-(sequence, kv head) arrival counters return to
+ * zero when a call completes; per-SM speed estimates size each SM's share of
+ * the next call (speed only, never results).  A control block that is not in
+ * a state the library left (not zero-filled before first use, overwritten)
+ * sets PKV_ERR_WORKSPACE.  Calls that may run at the same time need separate
  * workspaces; reusing one workspace for consecutive calls on a stream lets
  * the estimates settle.
  */

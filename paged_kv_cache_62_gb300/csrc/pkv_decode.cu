@@ -50,6 +50,7 @@ namespace pkv {
 constexpr int kMaxStages = 4;     // ring depth
 constexpr int kMaxSlots = 512;    // slices: SM ids (adaptive) or CTAs (fixed split)
 constexpr uint32_t kTableMagic = 0x62616c31u;
+constexpr uint32_t kEpochMagic = 0x65706f63u;
 
 // Consumer warps per CTA and tokens each takes from a stage (a stage holds
 // team_warps * warp_tokens token rows of head_dim, 64 KiB for head_dim 128).
@@ -72,6 +73,10 @@ struct BalanceState {
     float elapsed[2][kMaxSlots];          // its run time in us (<= 0: present, nothing measured)
     uint32_t tag[2][kMaxSlots];           // (call number of the writer) ^ kTableMagic
     unsigned long long claim[kMaxSlots];  // (gen << 32) | 1 once a CTA took the slice this call
+    // Control block.  Call number e of a workspace runs with gen = e + 1 (never 0, the value
+    // of zero-filled tags).  The last CTA of call e leaves epoch = e + 1, stamp =
+    // (e + 1) ^ kEpochMagic, done = 0; a zero-filled workspace reads as call 0.
+    uint32_t epoch, stamp, done, pad;
 };
 
 struct DecodeParams {
@@ -79,7 +84,7 @@ struct DecodeParams {
     const int32_t *block_tables;
     const int32_t *context_lens;
     uint16_t *out;
-    unsigned long long *ws_count;  // [B * Hkv] arrival counters: (call generation << 32) | units arrived
+    unsigned long long *ws_count;  // [B * Hkv] arrival counters: (gen << 32) | units arrived
     float *ws_ml;                  // [slots][G][2] (m, l) per partial
     float *ws_acc;                 // [slots][G][D] unnormalised accumulators
     BalanceState *ws_bal;
@@ -90,8 +95,6 @@ struct DecodeParams {
     int32_t nst, cons, lg_nbox;  // ring stages, consumer warps (hg * sub), log2(nbox)
     int32_t num_workers;         // > 0: fixed split over about num_workers / consumers CTAs; 0: adaptive
     float scale_log2;            // scale * log2(e)
-    uint32_t gen;                // generation of this call (tags counters and claims)
-    uint32_t call;               // number of this call on this workspace: call & 1 picks the table half written
 };
 
 // What the producer tells the consumers about the unit in a stage.
@@ -420,32 +423,35 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float *red)
     return t;
 }
 
-// The previous call's balance entries this thread reads in build_partition
-// (slices tid and tid + blockDim.x), loaded up front so that their memory
-// round trip overlaps the context-length loads of unit_prefix_scan.
+// The balance entries this thread reads in build_partition (slices tid and
+// tid + blockDim.x), loaded up front so that their memory round trip overlaps
+// the context-length loads of unit_prefix_scan.  Both table halves are
+// loaded, before this call's number is known; build_partition keeps the
+// entry whose tag names the previous call.
 struct BalanceIn {
-    float w[2], t[2];
-    uint32_t tag[2];
+    float w[2][2], t[2][2];  // [table half][entry k]
+    uint32_t tag[2][2];
 };
 static_assert(2 * (8 + 1) * 32 >= kMaxSlots, "two balance entries per thread must cover every slice");
 
 __device__ __forceinline__ BalanceIn load_balance(const DecodeParams &p, bool adaptive, int nslots)
 {
     BalanceIn in;
-    const int rp = int(p.call & 1u) ^ 1;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int i = threadIdx.x + k * blockDim.x;
-        in.w[k] = 1.0f;
-        in.t[k] = 0.f;
-        in.tag[k] = 0u;
-        if (adaptive && i < nslots) {
-            // plain L2 loads: this half of the table is not written during this call
-            in.tag[k] = __ldcg(&p.ws_bal->tag[rp][i]);
-            in.w[k] = __ldcg(&p.ws_bal->weight[rp][i]);
-            in.t[k] = __ldcg(&p.ws_bal->elapsed[rp][i]);
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int i = threadIdx.x + k * blockDim.x;
+            in.w[h][k] = 1.0f;
+            in.t[h][k] = 0.f;
+            in.tag[h][k] = 0u;
+            if (adaptive && i < nslots) {
+                // plain L2 loads; the half this call writes is told apart by its tag
+                in.tag[h][k] = __ldcg(&p.ws_bal->tag[h][i]);
+                in.w[h][k] = __ldcg(&p.ws_bal->weight[h][i]);
+                in.t[h][k] = __ldcg(&p.ws_bal->elapsed[h][i]);
+            }
         }
-    }
     return in;
 }
 
@@ -457,11 +463,11 @@ __device__ __forceinline__ BalanceIn load_balance(const DecodeParams &p, bool ad
 // calls' finishing times then anti-correlate); entries from any other call
 // count as unknown (weight 1).  Fixed mode: equal weights.  Every CTA computes the same bounds from the
 // same inputs in the same order; leaves the weights in w[].
-__device__ void build_partition(const DecodeParams &p, bool adaptive, int nslots, long long T, long long *bound,
-                                float *w, float *red, const BalanceIn &in)
+__device__ void build_partition(const DecodeParams &p, uint32_t gen, bool adaptive, int nslots, long long T,
+                                long long *bound, float *w, float *red, const BalanceIn &in)
 {
     const int tid = threadIdx.x, nt = blockDim.x;
-    const uint32_t want = (p.call - 1u) ^ kTableMagic;
+    const uint32_t want = (gen - 1u) ^ kTableMagic;
     // pass 1: raw weights (kept in w) and elapsed times (kept in bound[] as float bits)
     float tsum = 0.f, tcnt = 0.f;
     float *el = reinterpret_cast<float *>(bound);
@@ -470,9 +476,10 @@ __device__ void build_partition(const DecodeParams &p, bool adaptive, int nslots
         const int i = tid + k * nt;
         if (i >= nslots) break;
         float x = 1.0f, t = 0.f;
-        if (adaptive && in.tag[k] == want) {
-            x = in.w[k];
-            t = in.t[k];
+        const bool h1 = in.tag[1][k] == want;  // the half the previous call wrote (selects, no indexing)
+        if (adaptive && (h1 || in.tag[0][k] == want)) {
+            x = h1 ? in.w[1][k] : in.w[0][k];
+            t = h1 ? in.t[1][k] : in.t[0][k];
             if (!(x >= 0.f) || !(x < 1.0e6f)) x = 1.0f;
             if (!(t < 1.0e9f)) t = 0.f;
             if (x > 0.f && t > 0.f) {
@@ -548,7 +555,8 @@ __device__ __forceinline__ bool try_claim(unsigned long long *word, uint32_t gen
 // With `record`, also writes the balance entries of the looked-after slices
 // that are empty this call (nobody else writes them): present if an SM
 // claimed it, absent otherwise.
-__device__ int claim_leftover(const DecodeParams &p, const long long *bound, int nslots, int wp, bool record)
+__device__ int claim_leftover(const DecodeParams &p, uint32_t gen, const long long *bound, int nslots, int wp,
+                              bool record)
 {
     const int lane = threadIdx.x & 31;
     for (int k0 = 0; blockIdx.x + (long long)k0 * gridDim.x < nslots; k0 += 32) {
@@ -556,20 +564,20 @@ __device__ int claim_leftover(const DecodeParams &p, const long long *bound, int
         bool cand = false;
         if (s < nslots) {
             const unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(&p.ws_bal->claim[s]);
-            const bool claimed = uint32_t(cur >> 32) == p.gen;
+            const bool claimed = uint32_t(cur >> 32) == gen;
             if (bound[s + 1] > bound[s]) {
                 cand = !claimed;
             } else if (record) {
                 p.ws_bal->weight[wp][s] = claimed ? 1.0f : 0.0f;
                 p.ws_bal->elapsed[wp][s] = claimed ? -1.0f : 0.0f;
-                p.ws_bal->tag[wp][s] = p.call ^ kTableMagic;
+                p.ws_bal->tag[wp][s] = gen ^ kTableMagic;
             }
         }
         unsigned m = __ballot_sync(kFull, cand);
         while (m) {
             const int l = __ffs(m) - 1;
             int ok = 0;
-            if (lane == l) ok = try_claim(&p.ws_bal->claim[s], p.gen);
+            if (lane == l) ok = try_claim(&p.ws_bal->claim[s], gen);
             if (__shfl_sync(kFull, ok, l)) return int(__shfl_sync(kFull, s, l));
             m &= m - 1;
         }
@@ -579,10 +587,10 @@ __device__ int claim_leftover(const DecodeParams &p, const long long *bound, int
 
 // ------------------------------------------------------------------ split-K merge (a6)
 // Count the `units` of one piece of (b, kv head) in.  The counter word is
-// (call generation << 32) | units arrived; a word from another call (other
-// generation, or leftover garbage) counts as zero, so the workspace never
-// needs clearing.  Returns 1 for the piece that completes the pair's `total`
-// units (and resets the word to 0).  Counting units, not pieces, lets any
+// (gen << 32) | units arrived; a word from another call (another gen: a call
+// that gave up half-way, or the zero left by a completed one) counts as
+// zero.  Returns 1 for the piece that completes the pair's `total` units
+// (and resets the word to 0).  Counting units, not pieces, lets any
 // partition of the unit list merge correctly.
 __device__ __forceinline__ int arrive_last(unsigned long long *ctr, uint32_t gen, uint32_t units, uint32_t total,
                                            int32_t *err)
@@ -687,6 +695,21 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
     }
 }
 
+// Warp-collective, the last thing every warp of the CTA does: count the warp
+// out on a shared counter; the CTA's last warp counts the CTA out of the call,
+// and the call's last CTA (every other CTA has finished, so has read the
+// control block) leaves it ready for the next call.
+__device__ __forceinline__ void warp_exit(const DecodeParams &p, uint32_t epoch, int *ctas_warps_done, int nwarps)
+{
+    __syncwarp();
+    if ((threadIdx.x & 31) != 0) return;
+    if (atomicAdd(ctas_warps_done, 1) != nwarps - 1) return;
+    if (atomicAdd(&p.ws_bal->done, 1u) != gridDim.x - 1) return;
+    p.ws_bal->done = 0u;
+    p.ws_bal->epoch = epoch + 1u;
+    p.ws_bal->stamp = (epoch + 1u) ^ kEpochMagic;
+}
+
 // ------------------------------------------------------------------ main kernel
 // Block: p.cons consumer warps (warp w: kv head w / sub of the group, TW-token
 // slice w % sub of every unit) and one producer warp (warp p.cons).
@@ -714,7 +737,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     long long *bound = reinterpret_cast<long long *>(smem + lay.off_bound);
     float *wts = reinterpret_cast<float *>(smem + lay.off_wts);
     float *red = reinterpret_cast<float *>(smem + lay.off_red);
-    int *sh = reinterpret_cast<int *>(smem + lay.off_sh);  // [0] own slice, [2..3] its start time
+    int *sh = reinterpret_cast<int *>(smem + lay.off_sh);  // [0] own slice, [2..3] its start time, [6] warps done
     int32_t *scan = reinterpret_cast<int32_t *>(smem + lay.off_scan);
 
     if (threadIdx.x == 0) {
@@ -728,16 +751,21 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     const bool adaptive = p.num_workers == 0;
     int nslots = int(gridDim.x);
     if (adaptive) nslots = int(min(nsmid(), unsigned(kMaxSlots)));
-    const int wp = int(p.call & 1u);  // this call writes one half of the balance table, reads the other
-    // The set-up's global reads are all issued here, so together they cost one memory round
-    // trip: the claim on this SM id's slice (an exchange: the first CTA of this call to run on
-    // the SM id finds another generation there), the previous call's balance entries and, in
-    // unit_prefix_scan, the context lengths.
-    const unsigned my_sm = smid();
-    unsigned long long home_word = static_cast<unsigned long long>(p.gen) << 32;
-    if (threadIdx.x == 0 && adaptive && int(my_sm) < nslots)
-        home_word = atomicExch(&p.ws_bal->claim[my_sm], (static_cast<unsigned long long>(p.gen) << 32) | 1ull);
+    // The set-up's global reads are all issued here, so together they cost about one memory
+    // round trip: the workspace's control block (this call's number), the balance entries,
+    // the context lengths (in unit_prefix_scan) and, once the call number is in, the claim on
+    // this SM id's slice (an exchange: the first CTA of this call to run on the SM id finds
+    // another call's tag there), whose answer is needed only after the partition.
+    const uint32_t epoch = __ldcg(&p.ws_bal->epoch), stamp = __ldcg(&p.ws_bal->stamp);
     const BalanceIn bal_in = load_balance(p, adaptive, nslots);
+    const bool ctl_ok = stamp == (epoch ^ kEpochMagic) || (epoch == 0u && stamp == 0u);
+    const uint32_t gen = epoch + 1u;  // tags of this call; zero-filled words never match
+    const int wp = int(gen & 1u);     // this call writes one half of the balance table
+    const unsigned my_sm = smid();
+    unsigned long long home_word = static_cast<unsigned long long>(gen) << 32;
+    if (threadIdx.x == 0 && adaptive && int(my_sm) < nslots)
+        home_word = atomicExch(&p.ws_bal->claim[my_sm], (static_cast<unsigned long long>(gen) << 32) | 1ull);
+    if (!ctl_ok && blockIdx.x == 0 && threadIdx.x == 0) flag_error(p.err, PKV_ERR_WORKSPACE);
     unit_prefix_scan(p, scan, reinterpret_cast<int32_t *>(smem));
     const long long T = (long long)p.nhg * scan[p.B];
 
@@ -747,7 +775,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
             for (int i = threadIdx.x; i < p.Hq * D / 8; i += blockDim.x)
                 reinterpret_cast<uint4 *>(p.out + int64_t(b) * p.Hq * D)[i] = make_uint4(0u, 0u, 0u, 0u);
 
-    build_partition(p, adaptive, nslots, T, bound, wts, red, bal_in);
+    build_partition(p, gen, adaptive, nslots, T, bound, wts, red, bal_in);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.nst; ++i) {
@@ -764,9 +792,10 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         int home = -1;
         if (!adaptive)
             home = int(blockIdx.x);
-        else if (uint32_t(home_word >> 32) != p.gen)
+        else if (uint32_t(home_word >> 32) != gen)
             home = int(my_sm);
         sh[0] = home;
+        sh[6] = 0;
     }
     __syncthreads();
 
@@ -779,7 +808,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         uint32_t rph = 0;           // parity of that slot's use (kk / nst) & 1
         bool dead = false;
         int slice = sh[0];
-        if (slice < 0 && adaptive) slice = claim_leftover(p, bound, nslots, wp, false);
+        if (slice < 0 && adaptive) slice = claim_leftover(p, gen, bound, nslots, wp, false);
         while (slice >= 0 && !dead) {
             const long long lo = bound[slice], hi = bound[slice + 1];
             if (lane == 0 && slice == sh[0])
@@ -876,7 +905,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                 if (k + 1 < nunits) walker_advance(iw, scan, p.nhg, p.B);
                 if (k == 0 && nboxes > 32) prefetch_batch(32);  // after the first copies are on their way
             }
-            slice = (adaptive && !dead) ? claim_leftover(p, bound, nslots, wp, true) : -1;
+            slice = (adaptive && !dead) ? claim_leftover(p, gen, bound, nslots, wp, true) : -1;
         }
         if (!dead) {  // end-of-work marker
             if (kk < uint32_t(p.nst) || mbar_wait_bounded(&empty[rs], rph ^ 1u)) {
@@ -893,6 +922,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         // let every copy this warp started land before the CTA can retire
         for (uint32_t i = kk > uint32_t(p.nst) ? kk - uint32_t(p.nst) : 0u; i < kk; ++i)
             mbar_wait_bounded(&full[i % uint32_t(p.nst)], (i / uint32_t(p.nst)) & 1u);
+        warp_exit(p, epoch, sh + 6, p.cons + 1);
         return;
     }
 
@@ -1063,7 +1093,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                     __syncwarp();
                     int last = 0;
                     if (lane == 0)
-                        last = arrive_last(p.ws_count + (long long)mt.b * p.Hkv + kvh, p.gen, uint32_t(piece),
+                        last = arrive_last(p.ws_count + (long long)mt.b * p.Hkv + kvh, gen, uint32_t(piece),
                                            uint32_t(mt.n), p.err);
                     if (__shfl_sync(kFull, last, 0)) {
                         __threadfence();
@@ -1082,9 +1112,10 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                 float(global_ns() - *reinterpret_cast<volatile unsigned long long *>(sh + 2)) * 1e-3f;
             p.ws_bal->weight[wp][mt.slice] = own ? wts[mt.slice] : 0.f;
             p.ws_bal->elapsed[wp][mt.slice] = own ? fmaxf(us, 1e-3f) : 0.f;
-            p.ws_bal->tag[wp][mt.slice] = p.call ^ kTableMagic;
+            p.ws_bal->tag[wp][mt.slice] = gen ^ kTableMagic;
         }
     }
+    warp_exit(p, epoch, sh + 6, p.cons + 1);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1175,22 +1206,6 @@ inline bool ensure_smem_attribute(Kernel kern, int dev, size_t smem)
     }
     configured[dev] = smem;
     return true;
-}
-
-// Number of this call on this workspace (per device).  The kernel keeps its
-// load-balance table in the workspace, one half written per call: this number
-// picks the half, and the previous call's entries are recognised by its
-// number minus one.  A host-side memo only: losing it costs one call of
-// balance, never results.
-inline uint32_t next_call_number(int dev, const void *workspace)
-{
-    static std::mutex mu;
-    static std::unordered_map<uintptr_t, uint32_t> calls[64];
-    if (dev < 0 || dev >= 64) return 0;
-    std::lock_guard<std::mutex> lock(mu);
-    auto &m = calls[dev];
-    if (m.size() > 65536) m.clear();
-    return ++m[reinterpret_cast<uintptr_t>(workspace)];
 }
 
 template <int D, int G>
@@ -1324,9 +1339,6 @@ extern "C" pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cach
     p.nst = 2;
     p.num_workers = 0;
     p.scale_log2 = float(double(scale) * 1.4426950408889634);
-    static std::atomic<uint32_t> generation{0};
-    p.gen = generation.fetch_add(1u, std::memory_order_relaxed) + 1u;
-    p.call = next_call_number(dev.device, workspace);
     a.k_cache = k_cache;
     a.v_cache = v_cache;
     a.device = dev.device;

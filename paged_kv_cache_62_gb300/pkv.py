@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
 OK, EINVAL, EUNSUPPORTED, ECUDA, EWORKSPACE, EBOUNDS = 0, -1, -2, -3, -4, -5
-ERR_SLOT_RANGE, ERR_BLOCK_RANGE, ERR_CONTEXT_RANGE, ERR_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+ERR_SLOT_RANGE, ERR_BLOCK_RANGE, ERR_CONTEXT_RANGE, ERR_WAIT_TIMEOUT, ERR_WORKSPACE = 0x1, 0x2, 0x4, 0x8, 0x10
 MAX_SEQS, MAX_WORKERS = 16384, 4096
 
 # name -> (restype, argtypes), mirroring include/pkv.h
@@ -126,8 +126,9 @@ def paged_decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: i
 
 
 def alloc_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, device=None) -> torch.Tensor:
+    """A decode workspace, zero-filled as the library requires before its first use."""
     n = paged_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim)
-    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
 def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,

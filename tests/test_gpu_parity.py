@@ -45,11 +45,24 @@ def run_decode(q, kc, vc, bt, lens, scale, max_ctx=None, num_workers=0, err=None
     B, Hq, D = q.shape
     Hkv = kc.shape[2]
     out = torch.full_like(q, float("nan"))
-    ws = pkv.alloc_workspace(B, Hq, Hkv, D)
-    ws.fill_(0xFF)   # a stale workspace must not matter
+    ws = shared_workspace(B, Hq, Hkv, D)  # left by earlier, differently sized calls: must not matter
     pkv.paged_decode(q, kc, vc, bt, lens, scale, out, ws, max_context_len=max_ctx, num_workers=num_workers,
                      err_word=err)
     return out
+
+
+_WS = {}
+
+
+def shared_workspace(B, Hq, Hkv, D):
+    """One zero-filled workspace per process, grown on demand and reused by every test that
+    does not bring its own: each call finds the state the previous (other-sized) call left."""
+    need = pkv.paged_decode_workspace_size(B, Hq, Hkv, D)
+    ws = _WS.get("ws")
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(max(need, 64 << 20), dtype=torch.uint8, device="cuda")
+        _WS["ws"] = ws
+    return ws
 
 
 def oracle_slots(wl):
@@ -185,7 +198,6 @@ def test_adaptive_split_over_repeated_calls(bs):
     want = oracle_of(q, kc, vc, bt, lens_t, 0.0884)
     B, Hq, D = q.shape
     ws = pkv.alloc_workspace(B, Hq, kc.shape[2], D)
-    ws.fill_(0xFF)
     err = err_word()
     for call in range(8):
         out = torch.full_like(q, float("nan"))
@@ -193,6 +205,50 @@ def test_adaptive_split_over_repeated_calls(bs):
         torch.cuda.synchronize()
         assert err.item() == 0, hex(err.item())
         check_close(out, want, f"call {call}")
+
+
+def test_cuda_graph_replay():
+    """The call captured once in a CUDA graph and replayed with new queries and lengths: nothing
+    per call is baked into the launch (the call epoch lives in the workspace), so every replay
+    must match the oracle, adaptive split included."""
+    lens0 = [700, 1500, 33, 2047, 1, 300, 999, 64] * 3
+    q, kc, vc, bt, lens_t = synth(len(lens0), 0, 16, 8, 128, 16, seed=11, lens=lens0)
+    B, Hq, D = q.shape
+    ws = pkv.alloc_workspace(B, Hq, kc.shape[2], D)
+    err = err_word()
+    out = torch.empty_like(q)
+    mx = int(max(lens0))
+    for _ in range(3):  # warm up (tensor maps, attributes) outside the capture
+        pkv.paged_decode(q, kc, vc, bt, lens_t, 0.0884, out, ws, max_context_len=mx, err_word=err)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pkv.paged_decode(q, kc, vc, bt, lens_t, 0.0884, out, ws, max_context_len=mx, err_word=err)
+    rng = np.random.default_rng(3)
+    for rep_i in range(5):
+        q.copy_(torch.randn(q.shape, generator=torch.Generator(device="cuda").manual_seed(rep_i), device="cuda")
+                .to(torch.bfloat16))
+        new = np.minimum(np.asarray(lens0) - rng.integers(0, 20, size=B), mx).clip(min=0)
+        lens_t.copy_(torch.as_tensor(new, dtype=torch.int32))
+        g.replay()
+        torch.cuda.synchronize()
+        assert err.item() == 0, hex(err.item())
+        check_close(out, oracle_of(q, kc, vc, bt, lens_t, 0.0884), f"replay {rep_i}")
+
+
+def test_workspace_not_zero_filled_is_reported():
+    """A workspace whose control block the library did not leave (here: all bytes 0xFF) sets
+    PKV_ERR_WORKSPACE; the call still ends normally."""
+    lens = [100, 200, 300]
+    q, kc, vc, bt, lens_t = synth(len(lens), 0, 16, 8, 128, 16, seed=9, lens=lens)
+    B, Hq, D = q.shape
+    ws = pkv.alloc_workspace(B, Hq, kc.shape[2], D)
+    ws.fill_(0xFF)
+    err = err_word()
+    out = torch.empty_like(q)
+    pkv.paged_decode(q, kc, vc, bt, lens_t, 0.0884, out, ws, err_word=err)
+    torch.cuda.synchronize()
+    assert err.item() & pkv.ERR_WORKSPACE
 
 
 def test_workers_do_not_change_results_much():
