@@ -190,16 +190,17 @@ def run_pkv(args):
     stream = torch.cuda.current_stream(dev)
     launches_per_step = 1 + 3 * len(wl.layers)
 
-    def step(dec_events=None):
-        pkv.decode_slot_mapping(wl.block_tables, wl.context_lens, s.block_size, wl.num_blocks, slots, err, stream)
+    def step(dec_events=None, st=None):
+        st = stream if st is None else st
+        pkv.decode_slot_mapping(wl.block_tables, wl.context_lens, s.block_size, wl.num_blocks, slots, err, st)
         for li, lay in enumerate(wl.layers):
-            pkv.kv_store(lay.k_new, lay.v_new, slots, lay.k_cache, lay.v_cache, err, stream)
+            pkv.kv_store(lay.k_new, lay.v_new, slots, lay.k_cache, lay.v_cache, err, st)
             if dec_events is not None:
-                dec_events[li][0].record(stream)
+                dec_events[li][0].record(st)
             pkv.paged_decode(lay.q, lay.k_cache, lay.v_cache, wl.block_tables, wl.context_lens, wl.scale,
-                             outs[li], wsbuf, max_context_len=max_ctx, err_word=err, stream=stream)
+                             outs[li], wsbuf, max_context_len=max_ctx, err_word=err, stream=st)
             if dec_events is not None:
-                dec_events[li][1].record(stream)
+                dec_events[li][1].record(st)
 
     def barrier():
         if ws > 1:
@@ -239,6 +240,26 @@ def run_pkv(args):
     dec_ms = [a.elapsed_time(b) for row in dec_ev for (a, b) in row]
     dec_mean_ms = float(np.mean(dec_ms))
     ms = reduce_over_ranks(ms, "max", dev)
+
+    # ---- the same step captured once as a CUDA graph and replayed (how a serving engine runs its
+    # decode step): no host work between launches, and each kernel's set-up overlaps the previous
+    # kernel's tail through programmatic dependent launch.  Same inputs, same workspace.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(st=torch.cuda.current_stream(dev))
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    g_steps = max(10, min(args.steps, 20000))
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    g0.record(stream)
+    for _ in range(g_steps):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    g_ms = reduce_over_ranks(g0.elapsed_time(g1) / g_steps, "max", dev)
+    assert err.item() == 0, f"device error word {err.item():#x}"
 
     # ---- end to end: host buffers in, host result out, through the same public calls
     host = {
@@ -321,8 +342,15 @@ def run_pkv(args):
         "e2e": {"value": round(job_bandwidth(nb["step"], ws, e2e_ms), 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "note": "pinned host q/k/v/block_tables/context_lens in, bf16 out back, stream sync every step"},
+        "graph": {"value": round(job_bandwidth(nb["step"], ws, g_ms), 1), "unit": "GB/s",
+                  "ms_per_step": round(g_ms, 5), "steps": g_steps,
+                  "note": "the step captured once as a CUDA graph and replayed back to back (CUDA events around "
+                          "all replays); the headline value above is plain stream launches"},
         "clocks": clocks.summary(),
     }
+    if args.workload == "long_mixed":
+        line["config"]["unique_kv_bytes_per_launch"] = wl.kv_bytes_unique()
+        line["config"]["logical_kv_bytes_per_launch"] = wl.kv_bytes_logical()
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
     if rank == 0:
@@ -384,7 +412,18 @@ def cpu_baseline(wl, budget_s=12.0):
     row = s.num_kv_heads * s.head_dim * 2
     nbytes = int(lens_s.sum()) * row * 2 + seqs * s.num_q_heads * s.head_dim * 4 + seqs * row * 4
     per_step = per_layer * s.layers
+    # the same oracle on one thread, over a smaller prefix (about a quarter of the budget)
+    seqs1 = int(max(1, min(seqs, seqs * (budget_s / 4) / (per_layer * cores))))
+    t = time.perf_counter()
+    oracle_step(wl, lays, bt, lens, seqs1, 1)
+    dt1 = max(time.perf_counter() - t, 1e-6)
+    lens_1 = lens[:seqs1].astype(np.int64)
+    nbytes1 = int(lens_1.sum()) * row * 2 + seqs1 * s.num_q_heads * s.head_dim * 4 + seqs1 * row * 4
+    single = {"value": round(nbytes1 / dt1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+              "seq_steps_per_sec": round(seqs1 / (dt1 * s.layers), 3),
+              "sample": f"first {seqs1} sequences, one repetition in {dt1:.1f} s"}
     return {"value": round(nbytes / per_layer / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "single_thread": single,
             "seq_steps_per_sec": round(seqs / per_step, 3), "seconds_per_step": round(per_step, 4),
             "sample": f"first {seqs} of {s.num_seqs} sequences of the {s.name} batch"
                       + (f", layer 0 of {s.layers} (time x{s.layers} per step)" if s.layers > 1 else "")
