@@ -261,6 +261,34 @@ def run_pkv(args):
     g_ms = reduce_over_ranks(g0.elapsed_time(g1) / g_steps, "max", dev)
     assert err.item() == 0, f"device error word {err.item():#x}"
 
+    # ---- copy-on-write block copies (pkv_copy_blocks) on this workload's pool: owned blocks copied
+    # into blocks no sequence holds, as many pairs as there are such blocks (up to 256)
+    cow = None
+    bt_h = wl.block_tables.cpu().numpy()
+    owned = np.unique(bt_h[bt_h >= 0])
+    free_ids = np.setdiff1d(np.arange(wl.num_blocks), owned)
+    n_cow = int(min(256, len(free_ids), len(owned)))
+    if n_cow >= 8:
+        lay0 = wl.layers[0]
+        cow_pairs = torch.from_numpy(np.stack([owned[:n_cow], free_ids[:n_cow]], 1).astype(np.int32)).to(dev)
+        for _ in range(3):
+            pkv.copy_blocks(lay0.k_cache, lay0.v_cache, cow_pairs, err, stream)
+        torch.cuda.synchronize()
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+        for c0, c1 in cev:
+            c0.record(stream)
+            pkv.copy_blocks(lay0.k_cache, lay0.v_cache, cow_pairs, err, stream)
+            c1.record(stream)
+        torch.cuda.synchronize()
+        assert err.item() == 0, f"device error word {err.item():#x}"
+        cow_us = float(np.mean([c0.elapsed_time(c1) for c0, c1 in cev])) * 1e3
+        block_bytes = s.block_size * Hkv * D * 2
+        cow_bytes = n_cow * 2 * block_bytes * 2  # K and V blocks, each read once and written once
+        cow = {"kernel": "pkv_copy_blocks (copy_blocks_kernel)", "pairs": n_cow, "block_bytes": block_bytes,
+               "bytes_per_launch": cow_bytes, "mean_launch_us": round(cow_us, 2),
+               "achieved": round(cow_bytes / (cow_us * 1e-6) / 1e9, 1), "unit": "GB/s",
+               "note": "bytes read + written; peak is the measured copy bandwidth (read + write)"}
+
     # ---- end to end: host buffers in, host result out, through the same public calls
     host = {
         "q": [lay.q.cpu().pin_memory() for lay in wl.layers],
@@ -348,6 +376,10 @@ def run_pkv(args):
                           "all replays); the headline value above is plain stream launches"},
         "clocks": clocks.summary(),
     }
+    if cow is not None:
+        cow["peak"] = peak
+        cow["frac"] = round(cow["achieved"] / peak, 4)
+        line["cow_copy"] = cow
     if args.workload == "long_mixed":
         line["config"]["unique_kv_bytes_per_launch"] = wl.kv_bytes_unique()
         line["config"]["logical_kv_bytes_per_launch"] = wl.kv_bytes_logical()

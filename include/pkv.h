@@ -53,7 +53,8 @@ typedef enum {
     PKV_EUNSUPPORTED = -2, /* valid request outside the compiled variants      */
     PKV_ECUDA = -3,        /* a CUDA runtime/driver call or launch failed      */
     PKV_EWORKSPACE = -4,   /* workspace missing or smaller than required       */
-    PKV_EBOUNDS = -5       /* reserved for host-visible range errors           */
+    PKV_EBOUNDS = -5,      /* reserved for host-visible range errors           */
+    PKV_EFULL = -6         /* block allocator: not enough free blocks          */
 } pkv_status;
 
 /* Bits ORed into *err_word by the kernels. */
@@ -238,6 +239,91 @@ PKV_API pkv_status pkv_paged_decode_noalloc(const uint16_t *q, const uint16_t *k
                                     int32_t block_size, int32_t num_blocks, int32_t max_context_len,
                                     float scale, uint16_t *out, int32_t num_workers,
                                     int32_t *err_word, pkv_stream_t stream);
+
+/*
+ * pkv_copy_blocks -- batched copy-on-write block copies.
+ *
+ * Defined by the nano-vllm KV-cache post (§2.2: sequences that share a
+ * physical block keep sharing it until one of them writes a different token
+ * there; that write first copies the block to a new one) and the mini-vLLM
+ * README (§1: copy-on-write of a half-full shared block).  For every pair i,
+ * physical block dst = pairs[2i + 1] of k_cache and of v_cache becomes a bit
+ * copy of block src = pairs[2i] (block_size rows x num_kv_heads x head_dim
+ * bf16 values each); src == dst leaves the block as it is.
+ *
+ *   k_cache,
+ *   v_cache   [num_blocks, block_size, num_kv_heads, head_dim] bf16, device
+ *   pairs     [num_pairs][2] int32 (src, dst), device
+ * The dst blocks of one call must be distinct and must not be the src of
+ * another pair of the same call (the copies run concurrently); a pair with an
+ * id outside [0, num_blocks) is skipped and sets PKV_ERR_BLOCK_RANGE.
+ * block_size * num_kv_heads * head_dim * 2 must be a multiple of 16 bytes.
+ * Memory-bound: it reads and writes 2 * block bytes per pair.
+ */
+PKV_API pkv_status pkv_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, const int32_t *pairs,
+                                   int32_t num_pairs, int32_t num_blocks, int32_t block_size,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t *err_word,
+                                   pkv_stream_t stream);
+
+/*
+ * Host-side block allocator: which physical blocks hold each sequence's
+ * tokens, with reference counts for shared blocks (the nano-vllm KV-cache
+ * post, §3.3 "BlockManager 的设计").  The free list is a FIFO of block ids,
+ * initially 0, 1, ..., num_blocks - 1: allocation takes from the front,
+ * release appends to the back (§3.3.1).  A block's reference count is the
+ * number of sequences whose table holds it.  Which blocks may be shared
+ * (prefix hashing in the post, §3.4) is the caller's decision: sharing is
+ * explicit.  Not thread-safe: one allocator per host thread, or a lock.
+ * Sequence ids are any int32 >= 0 not in use.  On any error the allocator is
+ * left as it was.
+ */
+typedef struct pkv_block_allocator pkv_block_allocator;
+
+/* A pool of num_blocks blocks of block_size tokens.  NULL on bad sizes. */
+PKV_API pkv_block_allocator *pkv_allocator_create(int32_t num_blocks, int32_t block_size);
+PKV_API void pkv_allocator_destroy(pkv_block_allocator *a);
+
+/* A new sequence of num_tokens tokens (its prefill): its first shared_blocks
+ * blocks are the first shared_blocks blocks of sequence parent_id (each one's
+ * count + 1, the post's REUSE path, §3.3.3), the rest are fresh blocks from
+ * the front of the free list.  Shared blocks must be whole blocks the parent
+ * holds and must not include the block of the sequence's last token
+ * (shared_blocks * block_size < num_tokens).  PKV_EFULL if the free list is
+ * too short; PKV_EINVAL for an id in use, an unknown parent or a bad count. */
+PKV_API pkv_status pkv_allocator_add(pkv_block_allocator *a, int32_t seq_id, int32_t num_tokens,
+                                     int32_t parent_id, int32_t shared_blocks);
+
+/* child_id becomes a copy of parent_id: the same tokens and table, every
+ * block's count + 1 (parallel sampling, beam search: §2.2 of the post). */
+PKV_API pkv_status pkv_allocator_fork(pkv_block_allocator *a, int32_t parent_id, int32_t child_id);
+
+/* One decode step of seq_id: its new token goes to position p = its token
+ * count.  If p % block_size == 0 the token opens a fresh block (the post's
+ * may_append, §3.3.4).  Otherwise, if its last block is shared (count > 1),
+ * copy-on-write: a fresh block replaces it in this sequence's table, the old
+ * block's count drops by one, and (*cow_src, *cow_dst) name the copy that
+ * pkv_copy_blocks must make before the token is stored; else both are -1.
+ * cow_src / cow_dst may be NULL.  PKV_EFULL if a block is needed and none
+ * is free. */
+PKV_API pkv_status pkv_allocator_append(pkv_block_allocator *a, int32_t seq_id, int32_t *cow_src,
+                                        int32_t *cow_dst);
+
+/* The sequence ends (or is preempted): its table is walked backwards and
+ * every block's count drops by one; a block at zero goes to the back of the
+ * free list (§3.3.5). */
+PKV_API pkv_status pkv_allocator_free(pkv_block_allocator *a, int32_t seq_id);
+
+/* Free blocks; a block's count (-1 for a bad id); a sequence's tokens (-1 if unknown). */
+PKV_API int32_t pkv_allocator_num_free(const pkv_block_allocator *a);
+PKV_API int32_t pkv_allocator_ref_count(const pkv_block_allocator *a, int32_t block_id);
+PKV_API int32_t pkv_allocator_num_tokens(const pkv_block_allocator *a, int32_t seq_id);
+
+/* Decode inputs for a batch, in host memory: row i of block_tables
+ * [n][max_blocks] is the table of seq_ids[i], -1 padded; context_lens[i]
+ * (may be NULL) its token count.  PKV_EINVAL if a sequence is unknown or
+ * holds more than max_blocks blocks (nothing is written then). */
+PKV_API pkv_status pkv_allocator_tables(const pkv_block_allocator *a, const int32_t *seq_ids, int32_t n,
+                                        int32_t *block_tables, int32_t max_blocks, int32_t *context_lens);
 
 #ifdef __cplusplus
 }

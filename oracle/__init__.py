@@ -62,6 +62,7 @@ def _load():
     lib.oracle_partial_state.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f64,
                                          i32, i32, P, P, P]
     lib.oracle_merge_states.argtypes = [P, P, P, i32, i32, P]
+    lib.oracle_copy_blocks.argtypes = [P, P, P, i32, i32, i64]
     for name in ("oracle_slot_of", "oracle_decode_slot_mapping", "oracle_kv_store",
                  "oracle_paged_decode", "oracle_partial_state", "oracle_merge_states"):
         getattr(lib, name).restype = ctypes.c_int
@@ -117,6 +118,19 @@ def kv_store(k_bits, v_bits, slot_mapping, k_cache_bits, v_cache_bits) -> None:
     num_slots = k_cache_bits.shape[0] * k_cache_bits.shape[1]
     _check(_load().oracle_kv_store(_ptr(k), _ptr(v), _ptr(slots), T, _ptr(k_cache_bits), _ptr(v_cache_bits),
                                    num_slots, row), "kv_store")
+
+
+def copy_blocks(k_cache_bits, v_cache_bits, pairs) -> None:
+    """In place: for each (src, dst) row of ``pairs`` in order, block dst of both caches becomes a bit
+    copy of block src.  Raises on an id outside the pool (the other pairs are still applied)."""
+    for c in (k_cache_bits, v_cache_bits):
+        if c.dtype != np.uint16 or not c.flags.c_contiguous:
+            raise OracleError("caches must be C-contiguous uint16 arrays")
+    pr = _c(np.asarray(pairs, np.int32).reshape(-1, 2), np.int32)
+    NB = k_cache_bits.shape[0]
+    elems = int(np.prod(k_cache_bits.shape[1:]))
+    _check(_load().oracle_copy_blocks(_ptr(k_cache_bits), _ptr(v_cache_bits), _ptr(pr), pr.shape[0], NB, elems),
+           "copy_blocks")
 
 
 def paged_decode(q_bits, k_cache_bits, v_cache_bits, block_tables, context_lens, scale: float,

@@ -25,7 +25,8 @@
  *  [P4] "大模型推理引擎学习入门-2：带你理解 nano-vllm 的 KV Cache 以及 Paged
  *       Attention", §3.1 (slot = block_table[i] * block_size + offset, per-layer
  *       k_cache/v_cache views), §3.5 (slot_mapping), §4.4 (decode example:
- *       context_lens [431, 434] -> slot_mapping [430, 689]).
+ *       context_lens [431, 434] -> slot_mapping [430, 689]), §2.2 (shared
+ *       blocks are copied before a divergent write: copy-on-write).
  *
  * Numbers: K/V/q are bf16 bit patterns (uint16), widened exactly to double.
  * Every sum, exp and division is done in double.  The attention uses the
@@ -122,6 +123,31 @@ int oracle_kv_store(const uint16_t *k, const uint16_t *v, const int32_t *slot_ma
         if (s < 0 || s >= num_slots) { rc = ORACLE_EBOUNDS; continue; }
         memcpy(k_cache + s * row_elems, k + (int64_t)t * row_elems, sizeof(uint16_t) * (size_t)row_elems);
         memcpy(v_cache + s * row_elems, v + (int64_t)t * row_elems, sizeof(uint16_t) * (size_t)row_elems);
+    }
+    return rc;
+}
+
+/* ---------------------------------------------------------------------------
+ * Copy-on-write block copy ([P4] §2.2: before a sequence writes into a
+ * physical block that other sequences share, the block is copied to a new one;
+ * [P2] §1: copy-on-write of a half-full shared block).  For each pair i in
+ * order, physical block dst = pairs[2i + 1] of both caches becomes a bit copy
+ * of block src = pairs[2i] (all block_size x Hkv x D values); src == dst
+ * leaves it as it is.  An id outside [0, num_blocks) makes the pair skipped
+ * and the call return ORACLE_EBOUNDS.  block_elems = block_size * Hkv * D.
+ * ------------------------------------------------------------------------- */
+int oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, const int32_t *pairs, int32_t num_pairs,
+                       int32_t num_blocks, int64_t block_elems)
+{
+    if (!k_cache || !v_cache || (num_pairs > 0 && !pairs)) return ORACLE_EINVAL;
+    if (num_pairs < 0 || num_blocks <= 0 || block_elems <= 0) return ORACLE_EINVAL;
+    int rc = ORACLE_OK;
+    for (int32_t i = 0; i < num_pairs; ++i) {
+        const int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) { rc = ORACLE_EBOUNDS; continue; }
+        if (src == dst) continue;
+        memcpy(k_cache + dst * block_elems, k_cache + src * block_elems, sizeof(uint16_t) * (size_t)block_elems);
+        memcpy(v_cache + dst * block_elems, v_cache + src * block_elems, sizeof(uint16_t) * (size_t)block_elems);
     }
     return rc;
 }

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(HERE, "libpkv.so")
-SOURCES = ["pkv_api.cu", "pkv_store.cu", "pkv_decode.cu"]
+SOURCES = ["pkv_api.cu", "pkv_store.cu", "pkv_decode.cu", "pkv_alloc.cpp"]
 HEADERS = ["pkv_device.cuh", "pkv_host.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # Hidden visibility: only the PKV_API (extern "C") entry points are exported, so
@@ -47,7 +47,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
         objs.append(o)
         if force or ptxas_info or _stale(o, [s] + hdrs):
             cmd = [nvcc(), *ARCH, *FLAGS, "-I", include, "-c", s, "-o", o]

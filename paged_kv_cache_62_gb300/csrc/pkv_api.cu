@@ -74,6 +74,7 @@ extern "C" const char *pkv_status_string(int status)
     case PKV_ECUDA: return "CUDA call or kernel launch failed";
     case PKV_EWORKSPACE: return "workspace missing or too small";
     case PKV_EBOUNDS: return "index out of range";
+    case PKV_EFULL: return "not enough free blocks";
     default: return "unknown pkv status";
     }
 }

@@ -6,10 +6,16 @@
 // pkv_kv_store: row slot_mapping[t] of k_cache / v_cache becomes a copy of
 //   k[t] / v[t]; slot -1 skips the row (MinivLLM review, "注意力内核的三个分支").
 //
-// Both are tiny, latency-bound launches.  The store moves whole cache rows
+// pkv_copy_blocks: copy-on-write block copies, block dst of both caches
+//   becomes a bit copy of block src (nano-vllm KV-cache post §2.2; mini-vLLM
+//   README §1, copy-on-write of a half-full shared block).
+//
+// The first two are tiny, latency-bound launches.  The store moves whole cache rows
 // (num_kv_heads * head_dim bf16, 2 KiB for Qwen3-0.6B) with 16-byte vector
 // loads/stores: one CTA per token, consecutive threads on consecutive 16-byte
 // chunks of the row, so every warp access is a fully coalesced 512-byte run.
+#include <algorithm>
+
 #include "pkv_device.cuh"
 #include "pkv_host.h"
 
@@ -72,6 +78,53 @@ __global__ void kv_store_kernel(const uint4 *__restrict__ k, const uint4 *__rest
     }
 }
 
+// Copy-on-write block copies.  The work is cut into 16 KiB chunks of one
+// block of one cache; a persistent grid walks the chunks, every thread keeping
+// four 16-byte loads in flight (the copy is bound by HBM read + write).  Loads
+// go through L2 only and stores are marked streaming: the copied bytes are
+// not needed again by this kernel.
+constexpr int kCopyThreads = 256;
+constexpr int kCopyVecs = 4;                                 // 16-byte vectors in flight per thread
+constexpr int64_t kChunkVecs = kCopyThreads * kCopyVecs;     // vectors per chunk (16 KiB)
+
+__global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(uint4 *__restrict__ k_cache,
+                                                                   uint4 *__restrict__ v_cache,
+                                                                   const int32_t *__restrict__ pairs,
+                                                                   int32_t num_pairs, int32_t num_blocks,
+                                                                   int64_t block_vecs, int64_t chunks_per_block,
+                                                                   int32_t *err)
+{
+    griddep_launch_dependents();
+    griddep_wait();
+    const int64_t total = int64_t(num_pairs) * 2 * chunks_per_block;
+    for (int64_t c = blockIdx.x; c < total; c += gridDim.x) {
+        const int64_t pc = c / chunks_per_block;  // (pair, cache)
+        const int64_t part = c - pc * chunks_per_block;
+        const int32_t i = int32_t(pc >> 1);
+        const int32_t src = __ldg(pairs + 2 * i), dst = __ldg(pairs + 2 * i + 1);
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            if (threadIdx.x == 0 && (pc & 1) == 0 && part == 0) flag_error(err, PKV_ERR_BLOCK_RANGE);
+            continue;
+        }
+        if (src == dst) continue;
+        uint4 *base = (pc & 1) ? v_cache : k_cache;
+        const uint4 *from = base + int64_t(src) * block_vecs;
+        uint4 *to = base + int64_t(dst) * block_vecs;
+        const int64_t v0 = part * kChunkVecs + threadIdx.x;
+        uint4 x[kCopyVecs];
+#pragma unroll
+        for (int j = 0; j < kCopyVecs; ++j) {
+            const int64_t v = v0 + int64_t(j) * kCopyThreads;
+            if (v < block_vecs) x[j] = __ldcg(from + v);
+        }
+#pragma unroll
+        for (int j = 0; j < kCopyVecs; ++j) {
+            const int64_t v = v0 + int64_t(j) * kCopyThreads;
+            if (v < block_vecs) __stcs(to + v, x[j]);
+        }
+    }
+}
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -122,4 +175,34 @@ extern "C" pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, const i
         return cuda_fail("kv_store_kernel launch", e);
     }
     return launch_status("kv_store_kernel launch");
+}
+
+extern "C" pkv_status pkv_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, const int32_t *pairs,
+                                      int32_t num_pairs, int32_t num_blocks, int32_t block_size,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t *err_word,
+                                      pkv_stream_t stream)
+{
+    if (num_pairs < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return PKV_EINVAL;
+    const int64_t block_bytes = int64_t(block_size) * num_kv_heads * head_dim * 2;
+    if (block_bytes % 16 != 0) return PKV_EINVAL;
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !pairs) return PKV_EINVAL;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
+    DeviceInfo dev;
+    if (!current_device_info(&dev)) return PKV_ECUDA;
+    const int64_t block_vecs = block_bytes / 16;
+    const int64_t chunks_per_block = (block_vecs + kChunkVecs - 1) / kChunkVecs;
+    const int64_t total = int64_t(num_pairs) * 2 * chunks_per_block;
+    // persistent grid: up to 8 CTAs of 256 threads per SM, never more CTAs than chunks
+    const int64_t grid = std::min<int64_t>(total, int64_t(dev.sm_count) * 8);
+    const cudaError_t e = launch_pdl(copy_blocks_kernel, dim3(unsigned(grid)), dim3(kCopyThreads), 0,
+                                     reinterpret_cast<cudaStream_t>(stream), reinterpret_cast<uint4 *>(k_cache),
+                                     reinterpret_cast<uint4 *>(v_cache), pairs, num_pairs, num_blocks, block_vecs,
+                                     chunks_per_block, err_word);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return cuda_fail("copy_blocks_kernel launch", e);
+    }
+    return launch_status("copy_blocks_kernel launch");
 }

@@ -16,7 +16,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
-OK, EINVAL, EUNSUPPORTED, ECUDA, EWORKSPACE, EBOUNDS = 0, -1, -2, -3, -4, -5
+OK, EINVAL, EUNSUPPORTED, ECUDA, EWORKSPACE, EBOUNDS, EFULL = 0, -1, -2, -3, -4, -5, -6
 ERR_SLOT_RANGE, ERR_BLOCK_RANGE, ERR_CONTEXT_RANGE, ERR_WAIT_TIMEOUT, ERR_WORKSPACE = 0x1, 0x2, 0x4, 0x8, 0x10
 MAX_SEQS, MAX_WORKERS = 16384, 4096
 
@@ -33,6 +33,17 @@ SIGNATURES = {
                                         _F32, _P, _P, _SZ, _I32, _P, _P]),
     "pkv_paged_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                                 _I32, _F32, _P, _I32, _P, _P]),
+    "pkv_copy_blocks": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P]),
+    "pkv_allocator_create": (_P, [_I32, _I32]),
+    "pkv_allocator_destroy": (None, [_P]),
+    "pkv_allocator_add": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32]),
+    "pkv_allocator_fork": (ctypes.c_int, [_P, _I32, _I32]),
+    "pkv_allocator_append": (ctypes.c_int, [_P, _I32, _P, _P]),
+    "pkv_allocator_free": (ctypes.c_int, [_P, _I32]),
+    "pkv_allocator_num_free": (_I32, [_P]),
+    "pkv_allocator_ref_count": (_I32, [_P, _I32]),
+    "pkv_allocator_num_tokens": (_I32, [_P, _I32]),
+    "pkv_allocator_tables": (ctypes.c_int, [_P, _P, _I32, _P, _I32, _P]),
 }
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
@@ -178,3 +189,73 @@ def paged_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
         _dev(context_lens, torch.int32, "context_lens", 1), B, Hq, Hkv, D, bs, NB, int(max_context_len),
         float(scale), _dev(out, torch.bfloat16, "out", 3), int(num_workers), _opt(err_word), _stream(stream)),
         "pkv_paged_decode_noalloc")
+
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, pairs: torch.Tensor,
+                err_word: torch.Tensor | None = None, stream=None) -> None:
+    """Copy-on-write copies: for each row (src, dst) of ``pairs`` (int32 [n, 2], device), block dst of
+    both caches becomes a bit copy of block src."""
+    NB, bs, Hkv, D = k_cache.shape
+    if v_cache.shape != k_cache.shape or pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("copy_blocks: shape mismatch")
+    _check(load().pkv_copy_blocks(
+        _dev(k_cache, torch.bfloat16, "k_cache", 4), _dev(v_cache, torch.bfloat16, "v_cache", 4),
+        _dev(pairs, torch.int32, "pairs", 2), pairs.shape[0], NB, bs, Hkv, D, _opt(err_word), _stream(stream)),
+        "pkv_copy_blocks")
+
+
+class BlockAllocator:
+    """Host-side block allocator of the library (reference counts, copy-on-write; see include/pkv.h)."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._lib = load()
+        self._h = self._lib.pkv_allocator_create(int(num_blocks), int(block_size))
+        if not self._h:
+            raise ValueError(f"pkv_allocator_create({num_blocks}, {block_size}) failed")
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.pkv_allocator_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add(self, seq_id: int, num_tokens: int, parent_id: int = -1, shared_blocks: int = 0) -> None:
+        _check(self._lib.pkv_allocator_add(self._h, seq_id, num_tokens, parent_id, shared_blocks),
+               "pkv_allocator_add")
+
+    def fork(self, parent_id: int, child_id: int) -> None:
+        _check(self._lib.pkv_allocator_fork(self._h, parent_id, child_id), "pkv_allocator_fork")
+
+    def append(self, seq_id: int) -> tuple[int, int]:
+        """One token for seq_id; returns the (src, dst) copy-on-write pair, (-1, -1) if none."""
+        src, dst = ctypes.c_int32(-1), ctypes.c_int32(-1)
+        _check(self._lib.pkv_allocator_append(self._h, seq_id, ctypes.byref(src), ctypes.byref(dst)),
+               "pkv_allocator_append")
+        return src.value, dst.value
+
+    def free(self, seq_id: int) -> None:
+        _check(self._lib.pkv_allocator_free(self._h, seq_id), "pkv_allocator_free")
+
+    def num_free(self) -> int:
+        return self._lib.pkv_allocator_num_free(self._h)
+
+    def ref_count(self, block_id: int) -> int:
+        return self._lib.pkv_allocator_ref_count(self._h, block_id)
+
+    def num_tokens(self, seq_id: int) -> int:
+        return self._lib.pkv_allocator_num_tokens(self._h, seq_id)
+
+    def tables(self, seq_ids, max_blocks: int):
+        """(block_tables int32 [n, max_blocks] -1 padded, context_lens int32 [n]) as host tensors."""
+        ids = torch.as_tensor(list(seq_ids), dtype=torch.int32)
+        bt = torch.empty(len(ids), max_blocks, dtype=torch.int32)
+        lens = torch.empty(len(ids), dtype=torch.int32)
+        _check(self._lib.pkv_allocator_tables(self._h, ids.data_ptr(), len(ids), bt.data_ptr(), int(max_blocks),
+                                              lens.data_ptr()), "pkv_allocator_tables")
+        return bt, lens

@@ -394,6 +394,32 @@ def test_kv_store_bit_copy_and_skip():
         oracle.kv_store(k, v, np.array([80, -1, -1, -1, -1, -1], np.int32), kc, vc)
 
 
+def test_copy_blocks_bit_copy_and_copy_on_write_semantics():
+    """Block copies (copy-on-write, nano-vllm KV-cache post §2.2): numpy whole-block assignment decides
+    the bytes; a sequence whose table points at the copy attends exactly like one pointing at the
+    original; src == dst changes nothing; a bad id is refused while the other pairs still apply."""
+    rng = np.random.default_rng(15)
+    NB, bs, Hkv, D = 12, 8, 2, 64
+    kc = rand_bits(rng, (NB, bs, Hkv, D)); vc = rand_bits(rng, (NB, bs, Hkv, D))
+    kc0, vc0 = kc.copy(), vc.copy()
+    pairs = np.array([[3, 7], [5, 5], [0, 11]], np.int32)
+    oracle.copy_blocks(kc, vc, pairs)
+    want_k, want_v = kc0.copy(), vc0.copy()
+    want_k[[7, 11]] = kc0[[3, 0]]
+    want_v[[7, 11]] = vc0[[3, 0]]
+    assert np.array_equal(kc, want_k) and np.array_equal(vc, want_v)
+    # attention through [..., 3] equals attention through [..., 7] bit for bit
+    q = rand_bits(rng, (1, 4, D))
+    L = np.array([2 * bs + 5], np.int32)
+    a = oracle.paged_decode(q, kc, vc, np.array([[1, 2, 3]], np.int32), L, 0.125)
+    b = oracle.paged_decode(q, kc, vc, np.array([[1, 2, 7]], np.int32), L, 0.125)
+    assert np.array_equal(a, b)
+    kc1 = kc.copy()
+    with pytest.raises(oracle.OracleError):
+        oracle.copy_blocks(kc, vc, np.array([[2, 12], [4, 9]], np.int32))
+    assert np.array_equal(kc[9], kc1[4]) and np.array_equal(np.delete(kc, 9, 0), np.delete(kc1, 9, 0))
+
+
 def test_generator_structure():
     """Generator invariants the parity tests rely on (no arithmetic under test involved)."""
     for name in ("tiny", "qwen25_0p5b"):
