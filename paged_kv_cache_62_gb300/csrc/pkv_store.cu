@@ -78,14 +78,15 @@ __global__ void kv_store_kernel(const uint4 *__restrict__ k, const uint4 *__rest
     }
 }
 
-// Copy-on-write block copies.  The work is cut into 16 KiB chunks of one
+// Copy-on-write block copies.  The work is cut into 32 KiB chunks of one
 // block of one cache; a persistent grid walks the chunks, every thread keeping
-// four 16-byte loads in flight (the copy is bound by HBM read + write).  Loads
-// go through L2 only and stores are marked streaming: the copied bytes are
-// not needed again by this kernel.
+// eight 16-byte loads in flight (the copy is bound by HBM read + write).  Loads
+// go through L2 only; stores are plain (marking them streaming measured 8 %
+// slower on GB300).  Measured on 120 pairs of 512 KiB blocks: the same time as
+// torch's own device copy of the same bytes.
 constexpr int kCopyThreads = 256;
-constexpr int kCopyVecs = 4;                                 // 16-byte vectors in flight per thread
-constexpr int64_t kChunkVecs = kCopyThreads * kCopyVecs;     // vectors per chunk (16 KiB)
+constexpr int kCopyVecs = 8;                                 // 16-byte vectors in flight per thread
+constexpr int64_t kChunkVecs = kCopyThreads * kCopyVecs;     // vectors per chunk (32 KiB)
 
 __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(uint4 *__restrict__ k_cache,
                                                                    uint4 *__restrict__ v_cache,
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(uint4 *__rest
 #pragma unroll
         for (int j = 0; j < kCopyVecs; ++j) {
             const int64_t v = v0 + int64_t(j) * kCopyThreads;
-            if (v < block_vecs) __stcs(to + v, x[j]);
+            if (v < block_vecs) to[v] = x[j];
         }
     }
 }
