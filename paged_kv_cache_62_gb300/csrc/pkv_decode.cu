@@ -9,10 +9,11 @@
 // state (m, l, acc) of the README.
 //
 // How (GB300 design):
-//  * Kv heads are taken in groups of HG (the largest divisor of Hkv <= 8).  A
-//    unit of work is TOKS = TW * SUB consecutive tokens of one (sequence,
-//    head group), TW = 16 tokens per warp and SUB = 8 / HG warps per head
-//    (see team_warps): whole contiguous cache rows of the group, moved by
+//  * Kv heads are taken in groups of HG (the largest divisor of Hkv that is
+//    at most the CTA's consumer warps, 8, or 4 for groups of 5+ query heads).
+//    A unit of work is TOKS = TW * SUB consecutive tokens of one (sequence,
+//    head group), TW = 16 tokens per warp and SUB warps per head (see
+//    team_warps): whole contiguous cache rows of the group, moved by
 //    one TMA tensor copy per physical-block span into a shared-memory stage.
 //  * One CTA per SM: a producer warp streams units through a ring of 2-4
 //    stages (mbarrier transaction counts for "full", consumer arrivals for
@@ -57,9 +58,12 @@ constexpr uint32_t kEpochMagic = 0x65706f63u;
 // Measured on the Qwen3-0.6B-shaped batch: 8 warps x 16 tokens with three
 // 64 KiB stages beats 16 warps x 8 tokens (17 warps leave 96 registers a
 // thread, and the G = 2 loop spills) and 8 warps x 8 tokens with six 32 KiB
-// stages (twice the per-stage overhead per token).  Kept as functions of the
-// group size so that a group-specific choice stays a one-line change.
-__host__ __device__ constexpr int team_warps(int) { return 8; }
+// stages (twice the per-stage overhead per token).  Groups of 5 or more query
+// heads keep 16G accumulator and query registers a lane: with 8 consumers
+// plus the producer, three warps share an SM sub-partition's 16K registers
+// (168 a thread) and those groups spill; with 4 consumers at most two do
+// (255 a thread).
+__host__ __device__ constexpr int team_warps(int G) { return G >= 5 ? 4 : 8; }
 __host__ __device__ constexpr int warp_tokens(int) { return 16; }
 
 // ------------------------------------------------------------------ load balance state
@@ -160,13 +164,13 @@ __host__ __device__ inline CtaLayout cta_layout(int D, int G, int hg, int sub, i
     return l;
 }
 
-// Kv-head grouping: HG = the largest divisor of Hkv that is <= 8; the warps
-// of a CTA split as HG heads x SUB token slices, SUB the largest power of two
-// <= team_warps(G) / HG (a power of two, so a unit is a whole number of
-// power-of-two TMA boxes).
-inline int head_group(int Hkv)
+// Kv-head grouping: HG = the largest divisor of Hkv that is <= team_warps(G);
+// the warps of a CTA split as HG heads x SUB token slices, SUB the largest
+// power of two <= team_warps(G) / HG (a power of two, so a unit is a whole
+// number of power-of-two TMA boxes).
+inline int head_group(int Hkv, int G)
 {
-    for (int g = 8; g > 1; --g)
+    for (int g = team_warps(G); g > 1; --g)
         if (Hkv % g == 0) return g;
     return 1;
 }
@@ -187,7 +191,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // Piece slots: (slice + b * nhg + group) * hg + head-in-group, one per piece.
 inline WsLayout ws_layout(int32_t B, int32_t G, int32_t Hkv, int32_t D)
 {
-    const int hg = head_group(Hkv);
+    const int hg = head_group(Hkv, G);
     const size_t slots = (size_t(kMaxSlots) + size_t(B) * size_t(Hkv / hg)) * size_t(hg);
     WsLayout w;
     w.bal_off = 0;
@@ -636,7 +640,7 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
                                              long long sigma, int h, int b, int kvh, int lane)
 {
     constexpr int PER = D / 32;                           // output values per lane
-    constexpr int BATCH = G <= 2 ? 4 : (G <= 4 ? 2 : 1);  // pieces loaded together
+    constexpr int BATCH = G <= 2 ? 4 : (G <= 7 ? 2 : 1);  // pieces loaded together (G = 8 would spill)
     using Vec = typename std::conditional<PER == 4, float4, float2>::type;
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);
     float M[G], lsum[G], a[G][PER];
@@ -1328,7 +1332,7 @@ extern "C" pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cach
     p.NB = num_blocks;
     p.max_blocks = max_blocks_per_seq;
     p.len_limit = int32_t(len_limit);
-    p.hg = head_group(num_kv_heads);
+    p.hg = head_group(num_kv_heads, G);
     p.nhg = num_kv_heads / p.hg;
     p.sub = warp_slices(G, p.hg);
     p.toks = warp_tokens(G) * p.sub;
