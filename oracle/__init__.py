@@ -63,6 +63,10 @@ def _load():
                                          i32, i32, P, P, P]
     lib.oracle_merge_states.argtypes = [P, P, P, i32, i32, P]
     lib.oracle_copy_blocks.argtypes = [P, P, P, i32, i32, i64]
+    lib.oracle_e4m3_decode.argtypes = [P, i64, P]
+    lib.oracle_e4m3_encode.argtypes = [P, i64, P]
+    lib.oracle_kv_store_fp8.argtypes = [P, P, P, i32, P, P, i64, i32, i32, P, P]
+    lib.oracle_paged_decode_fp8.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, f64, P, i32]
     for name in ("oracle_slot_of", "oracle_decode_slot_mapping", "oracle_kv_store",
                  "oracle_paged_decode", "oracle_partial_state", "oracle_merge_states"):
         getattr(lib, name).restype = ctypes.c_int
@@ -118,6 +122,53 @@ def kv_store(k_bits, v_bits, slot_mapping, k_cache_bits, v_cache_bits) -> None:
     num_slots = k_cache_bits.shape[0] * k_cache_bits.shape[1]
     _check(_load().oracle_kv_store(_ptr(k), _ptr(v), _ptr(slots), T, _ptr(k_cache_bits), _ptr(v_cache_bits),
                                    num_slots, row), "kv_store")
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """float64 values of E4M3 codes (uint8), NaN for 0x7F / 0xFF."""
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _check(_load().oracle_e4m3_decode(_ptr(c), c.size, _ptr(out)), "e4m3_decode")
+    return out
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """E4M3 codes (uint8) of float32 values: nearest, ties to even, saturating at +-448."""
+    f = _c(x, np.float32)
+    out = np.empty(f.shape, np.uint8)
+    _check(_load().oracle_e4m3_encode(_ptr(f), f.size, _ptr(out)), "e4m3_encode")
+    return out
+
+
+def kv_store_fp8(k_bits, v_bits, slot_mapping, k_cache8, v_cache8, k_scale, v_scale) -> None:
+    """In-place store into E4M3 caches (uint8 [NB, bs, Hkv, D]) of bf16 rows divided by per-head scales."""
+    k = _c(k_bits, np.uint16)
+    v = _c(v_bits, np.uint16)
+    slots = _c(slot_mapping, np.int32)
+    ks, vs = _c(k_scale, np.float32), _c(v_scale, np.float32)
+    for c in (k_cache8, v_cache8):
+        if c.dtype != np.uint8 or not c.flags.c_contiguous:
+            raise OracleError("fp8 caches must be C-contiguous uint8 arrays")
+    NB, bs, Hkv, D = k_cache8.shape
+    _check(_load().oracle_kv_store_fp8(_ptr(k), _ptr(v), _ptr(slots), slots.size, _ptr(k_cache8), _ptr(v_cache8),
+                                       NB * bs, Hkv, D, _ptr(ks), _ptr(vs)), "kv_store_fp8")
+
+
+def paged_decode_fp8(q_bits, k_cache8, v_cache8, k_scale, v_scale, block_tables, context_lens, scale: float,
+                     nthreads: int = 1) -> np.ndarray:
+    """fp64 output [B, Hq, D] of decode attention over E4M3 caches with per-kv-head scales."""
+    q = _c(q_bits, np.uint16)
+    kc, vc = _c(k_cache8, np.uint8), _c(v_cache8, np.uint8)
+    ks, vs = _c(k_scale, np.float32), _c(v_scale, np.float32)
+    bt = _c(block_tables, np.int32)
+    ctx = _c(context_lens, np.int32)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = kc.shape
+    out = np.empty((B, Hq, D), np.float64)
+    _check(_load().oracle_paged_decode_fp8(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt), bt.shape[1],
+                                           _ptr(ctx), B, Hq, Hkv, D, bs, NB, float(scale), _ptr(out),
+                                           int(nthreads)), "paged_decode_fp8")
+    return out
 
 
 def copy_blocks(k_cache_bits, v_cache_bits, pairs) -> None:

@@ -53,6 +53,59 @@ static double bf16_bits_to_double(uint16_t bits)
     return (double)f;
 }
 
+/* ---------------------------------------------------------------------------
+ * 8-bit floating point E4M3, the "fp8 KV cache" the mini-vLLM README names as
+ * missing (§ "与 production vLLM 的关键差距"); the pages give no format, so
+ * this is the OCP 8-bit floating point E4M3 encoding that production engines
+ * store K/V in ("float8_e4m3fn"): sign bit, 4 exponent bits with bias 7,
+ * 3 mantissa bits; exponent field 0 holds subnormals m * 2^-9; no infinities;
+ * exponent 15 with mantissa 7 (0x7F / 0xFF) is NaN, so the largest finite
+ * magnitude is 1.75 * 2^8 = 448.
+ * ------------------------------------------------------------------------- */
+static double e4m3_to_double(uint8_t c)
+{
+    const int e = (c >> 3) & 0xF, m = c & 7;
+    const double sign = (c & 0x80) ? -1.0 : 1.0;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) return sign * ldexp((double)m, -9);
+    return sign * ldexp(1.0 + m / 8.0, e - 7);
+}
+
+/* Nearest finite E4M3 value to y, ties to the code with an even last bit
+ * (round to nearest even), magnitudes beyond 448 saturating to 448; NaN gives
+ * 0x7F.  Done by brute force over the 127 finite non-negative codes, which
+ * is the definition of rounding to the nearest representable value. */
+static uint8_t e4m3_from_float(float y)
+{
+    if (isnan(y)) return 0x7F;
+    const uint8_t sign = signbit(y) ? 0x80 : 0;
+    const double a = fabs((double)y);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double err = fabs(e4m3_to_double((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+int oracle_e4m3_decode(const uint8_t *codes, int64_t n, double *out)
+{
+    if ((n > 0 && (!codes || !out)) || n < 0) return ORACLE_EINVAL;
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_to_double(codes[i]);
+    return ORACLE_OK;
+}
+
+int oracle_e4m3_encode(const float *x, int64_t n, uint8_t *out)
+{
+    if ((n > 0 && (!x || !out)) || n < 0) return ORACLE_EINVAL;
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_from_float(x[i]);
+    return ORACLE_OK;
+}
+
 int oracle_version(void) { return 1; }
 
 /* ---------------------------------------------------------------------------
@@ -128,6 +181,38 @@ int oracle_kv_store(const uint16_t *k, const uint16_t *v, const int32_t *slot_ma
 }
 
 /* ---------------------------------------------------------------------------
+ * store_kvcache into an E4M3 cache: as oracle_kv_store, but element (h, d) of
+ * row t is stored as the E4M3 code of the binary32 quotient x / scale[h]
+ * (one IEEE single-precision division of the bf16 value by the kv head's
+ * scale, then the rounding of e4m3_from_float).  The per-kv-head scales k_scale
+ * and v_scale are the caller's (a calibrated max |x| / 448, say).
+ * ------------------------------------------------------------------------- */
+int oracle_kv_store_fp8(const uint16_t *k, const uint16_t *v, const int32_t *slot_mapping,
+                        int32_t num_tokens, uint8_t *k_cache, uint8_t *v_cache, int64_t num_slots,
+                        int32_t hkv, int32_t d, const float *k_scale, const float *v_scale)
+{
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale) return ORACLE_EINVAL;
+    if (num_tokens < 0 || num_slots < 0 || hkv <= 0 || d <= 0) return ORACLE_EINVAL;
+    const int64_t row = (int64_t)hkv * d;
+    int rc = ORACLE_OK;
+    for (int32_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s == -1) continue;
+        if (s < 0 || s >= num_slots) { rc = ORACLE_EBOUNDS; continue; }
+        for (int64_t i = 0; i < row; ++i) {
+            const int32_t h = (int32_t)(i / d);
+            const float xk = (float)bf16_bits_to_double(k[t * row + i]);
+            const float xv = (float)bf16_bits_to_double(v[t * row + i]);
+            const float qk = xk / k_scale[h];
+            const float qv = xv / v_scale[h];
+            k_cache[s * row + i] = e4m3_from_float(qk);
+            v_cache[s * row + i] = e4m3_from_float(qv);
+        }
+    }
+    return rc;
+}
+
+/* ---------------------------------------------------------------------------
  * Copy-on-write block copy ([P4] §2.2: before a sequence writes into a
  * physical block that other sequences share, the block is copied to a new one;
  * [P2] §1: copy-on-write of a half-full shared block).  For each pair i in
@@ -165,6 +250,8 @@ int oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, const int32_t *pair
  * ------------------------------------------------------------------------- */
 typedef struct {
     const uint16_t *q, *k_cache, *v_cache;
+    const uint8_t *k8, *v8;           /* E4M3 caches instead of bf16 (then k_cache, v_cache unused) */
+    const float *k_scale, *v_scale;   /* their per-kv-head scales */
     const int32_t *block_tables, *context_lens;
     int32_t num_seqs, hq, hkv, d, block_size, num_blocks, max_blocks;
     double scale;
@@ -172,6 +259,16 @@ typedef struct {
     int32_t nthreads, tid;
     int status;
 } decode_job;
+
+/* Element idx of the K (is_v = 0) or V cache, kv head g: a bf16 value, or an
+ * E4M3 code times the kv head's scale. */
+static double kv_elem(const decode_job *J, int is_v, int64_t idx, int32_t g)
+{
+    if (J->k8)
+        return is_v ? e4m3_to_double(J->v8[idx]) * (double)J->v_scale[g]
+                    : e4m3_to_double(J->k8[idx]) * (double)J->k_scale[g];
+    return bf16_bits_to_double(is_v ? J->v_cache[idx] : J->k_cache[idx]);
+}
 
 /* One (sequence, query head) item.  Returns 0 or ORACLE_EBOUNDS. */
 static int decode_one(const decode_job *J, int32_t b, int32_t h, double *scores)
@@ -196,7 +293,7 @@ static int decode_one(const decode_job *J, int32_t b, int32_t h, double *scores)
         int64_t base = (((int64_t)phys * J->block_size + j % J->block_size) * J->hkv + g) * d_all;
         double dot = 0.0;
         for (int32_t d = 0; d < d_all; ++d)
-            dot += bf16_bits_to_double(qv[d]) * bf16_bits_to_double(J->k_cache[base + d]);
+            dot += bf16_bits_to_double(qv[d]) * kv_elem(J, 0, base + d, g);
         scores[j] = J->scale * dot;
         if (scores[j] > m) m = scores[j];
     }
@@ -208,7 +305,7 @@ static int decode_one(const decode_job *J, int32_t b, int32_t h, double *scores)
         double w = exp(scores[j] - m);
         denom += w;
         for (int32_t d = 0; d < d_all; ++d)
-            o[d] += w * bf16_bits_to_double(J->v_cache[base + d]);
+            o[d] += w * kv_elem(J, 1, base + d, g);
     }
     for (int32_t d = 0; d < d_all; ++d) o[d] /= denom;
     return ORACLE_OK;
@@ -229,13 +326,43 @@ static void *decode_worker(void *arg)
     return NULL;
 }
 
+static int run_decode(decode_job proto, int32_t nthreads);
+
 int oracle_paged_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                         const int32_t *block_tables, int32_t max_blocks,
                         const int32_t *context_lens, int32_t num_seqs, int32_t hq,
                         int32_t hkv, int32_t d, int32_t block_size, int32_t num_blocks,
                         double scale, double *out, int32_t nthreads)
 {
-    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return ORACLE_EINVAL;
+    if (!k_cache || !v_cache) return ORACLE_EINVAL;
+    decode_job J = {q, k_cache, v_cache, NULL, NULL, NULL, NULL, block_tables, context_lens,
+                    num_seqs, hq, hkv, d, block_size, num_blocks, max_blocks, scale, out, 1, 0, ORACLE_OK};
+    return run_decode(J, nthreads);
+}
+
+/* The same attention over E4M3 caches: K_j, V_j are the codes' values times
+ * k_scale[g], v_scale[g] (per kv head), everything else as above. */
+int oracle_paged_decode_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                            const float *k_scale, const float *v_scale,
+                            const int32_t *block_tables, int32_t max_blocks,
+                            const int32_t *context_lens, int32_t num_seqs, int32_t hq,
+                            int32_t hkv, int32_t d, int32_t block_size, int32_t num_blocks,
+                            double scale, double *out, int32_t nthreads)
+{
+    if (!k_cache || !v_cache || !k_scale || !v_scale) return ORACLE_EINVAL;
+    decode_job J = {q, NULL, NULL, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                    num_seqs, hq, hkv, d, block_size, num_blocks, max_blocks, scale, out, 1, 0, ORACLE_OK};
+    return run_decode(J, nthreads);
+}
+
+static int run_decode(decode_job proto, int32_t nthreads)
+{
+    const uint16_t *q = proto.q;
+    const int32_t *block_tables = proto.block_tables, *context_lens = proto.context_lens;
+    const int32_t num_seqs = proto.num_seqs, hq = proto.hq, hkv = proto.hkv, d = proto.d;
+    const int32_t block_size = proto.block_size, max_blocks = proto.max_blocks;
+    double *out = proto.out;
+    if (!q || !block_tables || !context_lens || !out) return ORACLE_EINVAL;
     if (num_seqs < 0 || hq <= 0 || hkv <= 0 || d <= 0 || block_size <= 0 || max_blocks <= 0)
         return ORACLE_EINVAL;
     if (hq % hkv != 0) return ORACLE_EINVAL; /* [P2] §5: the group size must divide */
@@ -245,10 +372,10 @@ int oracle_paged_decode(const uint16_t *q, const uint16_t *k_cache, const uint16
     decode_job jobs[256];
     pthread_t threads[256];
     for (int32_t t = 0; t < nthreads; ++t) {
-        decode_job J = {q, k_cache, v_cache, block_tables, context_lens,
-                        num_seqs, hq, hkv, d, block_size, num_blocks, max_blocks,
-                        scale, out, nthreads, t, ORACLE_OK};
-        jobs[t] = J;
+        jobs[t] = proto;
+        jobs[t].nthreads = nthreads;
+        jobs[t].tid = t;
+        jobs[t].status = ORACLE_OK;
     }
     if (nthreads == 1) {
         decode_worker(&jobs[0]);

@@ -420,6 +420,82 @@ def test_copy_blocks_bit_copy_and_copy_on_write_semantics():
     assert np.array_equal(kc[9], kc1[4]) and np.array_equal(np.delete(kc, 9, 0), np.delete(kc1, 9, 0))
 
 
+def test_e4m3_codes_are_the_ocp_format():
+    """Published constants of OCP E4M3 ("float8_e4m3fn"): 0x7E = 448 (largest), 0x08 = 2^-6 (smallest
+    normal), 0x01 = 2^-9 (smallest subnormal), 0x38 = 1, 0x7F / 0xFF NaN, no infinities; the 127
+    non-negative finite codes increase strictly; encode(decode(c)) == c for every finite code."""
+    v = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    assert v[0x7E] == 448.0 and v[0xFE] == -448.0 and v[0x08] == 2.0 ** -6 and v[0x01] == 2.0 ** -9
+    assert v[0x38] == 1.0 and v[0x40] == 2.0 and v[0x00] == 0.0 and np.signbit(v[0x80])
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and np.isfinite(np.delete(v, [0x7F, 0xFF])).all()
+    assert np.all(np.diff(v[:0x7F]) > 0)
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(v[finite].astype(np.float32)), finite)
+
+
+def test_e4m3_encode_is_torchs_rounding_in_range_and_saturates_beyond():
+    """In range the oracle's rounding equals torch's float8_e4m3fn cast (a library routine), ties
+    included; beyond 448 it saturates to +-448 (the GPU conversion's satfinite mode), where torch's
+    cast gives NaN from 464 on."""
+    rng = np.random.default_rng(16)
+    x = np.concatenate([(rng.standard_normal(100000) * 40).astype(np.float32),
+                        (rng.standard_normal(20000) * 2.0 ** -8).astype(np.float32),
+                        np.array([1.0625, 1.1875, -1.0625, 2 ** -10, 3 * 2 ** -10, 272, 304, 447.9, 448],
+                                 np.float32)])
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x), want)
+    big = np.array([448.5, 463.9, 464.0, 1e9, -500.0, np.inf, -np.inf], np.float32)
+    assert oracle.e4m3_encode(big).tolist() == [0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0x7E, 0xFE]
+
+
+def test_kv_store_fp8_quantises_by_head_scale():
+    """Each stored code is torch's float8 cast of the binary32 quotient x / scale[kv head]; slot -1
+    writes nothing; a row is written whole."""
+    rng = np.random.default_rng(17)
+    NB, bs, Hkv, D, T = 6, 8, 2, 64, 5
+    kc = rng.integers(0, 255, (NB, bs, Hkv, D), dtype=np.uint8); vc = kc.copy()
+    k = rand_bits(rng, (T, Hkv, D)); v = rand_bits(rng, (T, Hkv, D))
+    ks = np.array([0.01, 0.75], np.float32); vs = np.array([0.3, 2.0 ** -3], np.float32)
+    slots = np.array([3, -1, 47, 12, 0], np.int32)
+    kc0, vc0 = kc.copy(), vc.copy()
+    oracle.kv_store_fp8(k, v, slots, kc, vc, ks, vs)
+    f32 = lambda b: torch.from_numpy(b.astype(np.int32) << 16).view(torch.float32)
+    qk = (f32(k) / torch.from_numpy(ks).view(1, Hkv, 1)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    qv = (f32(v) / torch.from_numpy(vs).view(1, Hkv, 1)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    want_k, want_v = kc0.reshape(NB * bs, Hkv, D).copy(), vc0.reshape(NB * bs, Hkv, D).copy()
+    keep = slots >= 0
+    want_k[slots[keep]] = qk[keep]
+    want_v[slots[keep]] = qv[keep]
+    assert np.array_equal(kc.reshape(NB * bs, Hkv, D), want_k)
+    assert np.array_equal(vc.reshape(NB * bs, Hkv, D), want_v)
+
+
+def test_fp8_decode_is_attention_over_the_dequantised_cache():
+    """With power-of-two scales every dequantised value is exact in bf16, so the fp8 decode must equal
+    the bf16 oracle on the dequantised caches; doubling k_scale while halving the attention scale changes
+    nothing, doubling v_scale doubles the output -- exactly."""
+    rng = np.random.default_rng(18)
+    NB, bs, Hkv, D, B, G = 9, 16, 2, 64, 3, 4
+    kc = rng.integers(0, 0x7F, (NB, bs, Hkv, D), dtype=np.uint8) | (rng.integers(0, 2, (NB, bs, Hkv, D),
+                                                                                  dtype=np.uint8) << 7)
+    vc = rng.integers(0, 0x7F, (NB, bs, Hkv, D), dtype=np.uint8)
+    kc[kc == 0xFF] = 0xFE
+    ks = np.array([2.0 ** -4, 0.5], np.float32); vs = np.array([1.0, 2.0 ** -2], np.float32)
+    q = rand_bits(rng, (B, G * Hkv, D))
+    bt = rng.permutation(NB)[:B * 3].reshape(B, 3).astype(np.int32)
+    lens = np.array([40, 1, 33], np.int32)
+    got = oracle.paged_decode_fp8(q, kc, vc, ks, vs, bt, lens, 0.125)
+    deq = lambda c, s: torch.from_numpy((oracle.e4m3_decode(c) * s.reshape(1, 1, Hkv, 1)).astype(np.float32))
+    kb = deq(kc, ks).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    vb = deq(vc, vs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.e4m3_decode(kc) * ks.reshape(1, 1, Hkv, 1),
+                          torch.from_numpy(kb.view(np.int16)).view(torch.bfloat16).double().numpy())
+    want = oracle.paged_decode(q, kb, vb, bt, lens, 0.125)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
+    assert np.array_equal(oracle.paged_decode_fp8(q, kc, vc, ks * 2, vs, bt, lens, 0.0625), got)
+    assert np.array_equal(oracle.paged_decode_fp8(q, kc, vc, ks, vs * 2, bt, lens, 0.125), 2 * got)
+
+
 def test_generator_structure():
     """Generator invariants the parity tests rely on (no arithmetic under test involved)."""
     for name in ("tiny", "qwen25_0p5b"):
