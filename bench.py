@@ -147,6 +147,17 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def kernel_source_sha() -> str:
+    """SHA-256 over the sources the decode kernel is compiled from (the kernel header, its entry-point
+    file and the device helpers), in that order."""
+    csrc = os.path.join(ROOT, "paged_kv_cache_62_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("pkv_decode_kernel.cuh", "pkv_decode.cu", "pkv_device.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def traffic_from_profile():
     """DRAM bytes per paged_decode launch from the committed ncu summary, if it matches the current source."""
     try:
@@ -156,8 +167,7 @@ def traffic_from_profile():
                 if ":" in line and not line.startswith("#"):
                     k, _, v = line.partition(":")
                     kv[k.strip()] = v.strip()
-        src = os.path.join(ROOT, "paged_kv_cache_62_gb300", "csrc", "pkv_decode.cu")
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        sha = kernel_source_sha()
         if kv.get("src_sha256") != sha:
             return None
         return float(kv["dram_bytes_per_launch"])
@@ -289,6 +299,42 @@ def run_pkv(args):
                "achieved": round(cow_bytes / (cow_us * 1e-6) / 1e9, 1), "unit": "GB/s",
                "note": "bytes read + written; peak is the measured copy bandwidth (read + write)"}
 
+    # ---- the same decode over E4M3 (fp8) caches: layer 0's caches quantised per kv head
+    # (scale = max |x| / 448), the same queries, tables and lengths
+    fp8 = None
+    if not args.no_fp8:
+        lay0 = wl.layers[0]
+        fin = lambda x: torch.nan_to_num(x.float(), nan=0.0)
+        ks8 = (fin(lay0.k_cache).abs().amax(dim=(0, 1, 3)) / 448).clamp_min(1e-6).contiguous()
+        vs8 = (fin(lay0.v_cache).abs().amax(dim=(0, 1, 3)) / 448).clamp_min(1e-6).contiguous()
+        q8 = lambda x, sc: (x.float() / sc.view(1, 1, -1, 1)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn) \
+            .view(torch.uint8).contiguous()  # NaN canaries stay NaN (clamp keeps NaN)
+        kc8, vc8 = q8(lay0.k_cache, ks8), q8(lay0.v_cache, vs8)
+        out8 = torch.empty_like(outs[0])
+
+        def dec8():
+            pkv.paged_decode_fp8(lay0.q, kc8, vc8, ks8, vs8, wl.block_tables, wl.context_lens, wl.scale, out8,
+                                 wsbuf, max_context_len=max_ctx, err_word=err, stream=stream)
+        for _ in range(5):
+            dec8()
+        torch.cuda.synchronize()
+        n8 = max(20, min(args.steps, 500))
+        fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n8)]
+        for c0, c1 in fev:
+            c0.record(stream)
+            dec8()
+            c1.record(stream)
+        torch.cuda.synchronize()
+        assert err.item() == 0, f"device error word {err.item():#x}"
+        us8 = float(np.mean([c0.elapsed_time(c1) for c0, c1 in fev])) * 1e3
+        nb0 = step_bytes(wl)
+        bytes8 = nb0["decode"] - nb0["decode_kv_only"] // 2  # K/V at one byte an element
+        fp8 = {"kernel": "pkv_paged_decode_fp8 (paged_decode_kernel, E4M3 caches)", "bytes_per_launch": bytes8,
+               "mean_launch_us": round(us8, 2), "achieved": round(bytes8 / (us8 * 1e-6) / 1e9, 1), "unit": "GB/s",
+               "seq_steps_per_sec_decode_only": round(B / (us8 * 1e-6), 1),
+               "speedup_vs_bf16_decode": round(dec_mean_ms * 1e3 / us8, 3),
+               "note": "layer 0 of the workload, caches quantised per kv head (scale = max|x| / 448)"}
+
     # ---- end to end: host buffers in, host result out, through the same public calls
     host = {
         "q": [lay.q.cpu().pin_memory() for lay in wl.layers],
@@ -376,6 +422,10 @@ def run_pkv(args):
                           "all replays); the headline value above is plain stream launches"},
         "clocks": clocks.summary(),
     }
+    if fp8 is not None:
+        fp8["peak"] = peak
+        fp8["frac"] = round(fp8["achieved"] / peak, 4)
+        line["fp8"] = fp8
     if cow is not None:
         cow["peak"] = peak
         cow["frac"] = round(cow["achieved"] / peak, 4)
@@ -514,6 +564,7 @@ def main():
     ap.add_argument("--workload", default="qwen3_0p6b")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the E4M3-cache decode measurement")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -241,6 +241,47 @@ PKV_API pkv_status pkv_paged_decode_noalloc(const uint16_t *q, const uint16_t *k
                                     int32_t *err_word, pkv_stream_t stream);
 
 /*
+ * E4M3 (fp8) KV cache.  The mini-vLLM README lists "no FP8 KV" among its gaps
+ * to production vLLM (§ "与 production vLLM 的关键差距") and gives no format;
+ * this library stores the OCP 8-bit floating point E4M3 encoding
+ * ("float8_e4m3fn": sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * largest finite 448, no infinities, 0x7F / 0xFF NaN) with one scale per kv
+ * head for K and one for V, both caller-chosen device float32 arrays
+ * [num_kv_heads] (for example a calibrated max |x| / 448): an element x is
+ * stored as the code of x / scale and read back as value(code) * scale.
+ * Caches hold one byte per element: [num_blocks, block_size, num_kv_heads,
+ * head_dim] uint8, half the bytes of the bf16 layout.
+ *
+ * pkv_kv_store_fp8 -- pkv_kv_store into E4M3 caches: row slot_mapping[t]
+ * becomes the codes of k[t] / k_scale (per kv head) -- one IEEE binary32
+ * division of the bf16 value, then round to nearest even, saturating at
+ * +-448 (NaN stays NaN).  Slot -1 and range errors as pkv_kv_store;
+ * head_dim must be a multiple of 8.
+ */
+PKV_API pkv_status pkv_kv_store_fp8(const uint16_t *k, const uint16_t *v, const int32_t *slot_mapping,
+                                    int32_t num_tokens, uint8_t *k_cache, uint8_t *v_cache,
+                                    int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                    int32_t head_dim, const float *k_scale, const float *v_scale,
+                                    int32_t *err_word, pkv_stream_t stream);
+
+/*
+ * pkv_paged_decode_fp8 -- pkv_paged_decode over E4M3 caches: K_j and V_j are
+ * the codes' values times k_scale / v_scale of their kv head; everything else
+ * (shapes, workspace, num_workers, errors, supported sizes) as
+ * pkv_paged_decode.  The K scale is folded into the query prescale and the V
+ * scale into the final division (both exact up to fp32 rounding), so the
+ * inner loop reads one byte per element.
+ */
+PKV_API pkv_status pkv_paged_decode_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                        const float *k_scale, const float *v_scale,
+                                        const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t *context_lens, int32_t num_seqs,
+                                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+                                        float scale, uint16_t *out, void *workspace, size_t workspace_bytes,
+                                        int32_t num_workers, int32_t *err_word, pkv_stream_t stream);
+
+/*
  * pkv_copy_blocks -- batched copy-on-write block copies.
  *
  * Defined by the nano-vllm KV-cache post (§2.2: sequences that share a

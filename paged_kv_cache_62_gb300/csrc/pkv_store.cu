@@ -6,6 +6,9 @@
 // pkv_kv_store: row slot_mapping[t] of k_cache / v_cache becomes a copy of
 //   k[t] / v[t]; slot -1 skips the row (MinivLLM review, "注意力内核的三个分支").
 //
+// pkv_kv_store_fp8: the same scatter into E4M3 caches, each element stored as
+//   the E4M3 code of x / scale[kv head] (an IEEE binary32 division, then the
+//   conversion's round to nearest even, saturating at +-448).
 // pkv_copy_blocks: copy-on-write block copies, block dst of both caches
 //   becomes a bit copy of block src (nano-vllm KV-cache post §2.2; mini-vLLM
 //   README §1, copy-on-write of a half-full shared block).
@@ -75,6 +78,47 @@ __global__ void kv_store_kernel(const uint4 *__restrict__ k, const uint4 *__rest
         const uint4 b = __ldg(vs + i);
         kd[i] = a;
         vd[i] = b;
+    }
+}
+
+// Eight bf16 values divided by s, as eight E4M3 codes (element e in byte e).
+__device__ __forceinline__ uint2 quantise8_e4m3(const uint4 w, float s)
+{
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    uint32_t out[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = __fdiv_rn(__uint_as_float(u[i] << 16), s);          // element 2i
+        const float hi = __fdiv_rn(__uint_as_float(u[i] & 0xffff0000u), s);  // element 2i + 1
+        uint16_t pair;  // the conversion puts its first source in the upper byte
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(hi), "f"(lo));
+        out[i >> 1] |= uint32_t(pair) << (16 * (i & 1));
+    }
+    return make_uint2(out[0], out[1]);
+}
+
+// One CTA per token; thread i quantises the 8-element group i of the row
+// (group i belongs to kv head i / (D / 8)).
+__global__ void kv_store_fp8_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                    const int32_t *__restrict__ slot_mapping, uint2 *__restrict__ k_cache,
+                                    uint2 *__restrict__ v_cache, int64_t num_slots, int32_t row_groups,
+                                    int32_t head_groups, const float *__restrict__ k_scale,
+                                    const float *__restrict__ v_scale, int32_t *err)
+{
+    griddep_launch_dependents();
+    griddep_wait();
+    const int32_t t = blockIdx.x;
+    const int64_t s = __ldg(slot_mapping + t);
+    if (s == -1) return;
+    if (s < 0 || s >= num_slots) {
+        if (threadIdx.x == 0) flag_error(err, PKV_ERR_SLOT_RANGE);
+        return;
+    }
+    for (int32_t i = threadIdx.x; i < row_groups; i += blockDim.x) {
+        const int32_t h = i / head_groups;
+        const int64_t src = int64_t(t) * row_groups + i, dst = s * row_groups + i;
+        k_cache[dst] = quantise8_e4m3(__ldg(k + src), __ldg(k_scale + h));
+        v_cache[dst] = quantise8_e4m3(__ldg(v + src), __ldg(v_scale + h));
     }
 }
 
@@ -206,4 +250,30 @@ extern "C" pkv_status pkv_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, cons
         return cuda_fail("copy_blocks_kernel launch", e);
     }
     return launch_status("copy_blocks_kernel launch");
+}
+
+extern "C" pkv_status pkv_kv_store_fp8(const uint16_t *k, const uint16_t *v, const int32_t *slot_mapping,
+                                       int32_t num_tokens, uint8_t *k_cache, uint8_t *v_cache, int32_t num_blocks,
+                                       int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                       const float *k_scale, const float *v_scale, int32_t *err_word,
+                                       pkv_stream_t stream)
+{
+    if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return PKV_EINVAL;
+    if (head_dim % 8 != 0 || int64_t(num_kv_heads) * head_dim / 8 > INT32_MAX) return PKV_EINVAL;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale) return PKV_EINVAL;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
+    const int32_t row_groups = num_kv_heads * (head_dim / 8);
+    const int threads = row_groups >= 256 ? 256 : ((row_groups + 31) / 32) * 32;
+    const cudaError_t e =
+        launch_pdl(kv_store_fp8_kernel, dim3(num_tokens), dim3(threads), 0, reinterpret_cast<cudaStream_t>(stream),
+                   reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v), slot_mapping,
+                   reinterpret_cast<uint2 *>(k_cache), reinterpret_cast<uint2 *>(v_cache),
+                   static_cast<int64_t>(num_blocks) * block_size, row_groups, head_dim / 8, k_scale, v_scale, err_word);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return cuda_fail("kv_store_fp8_kernel launch", e);
+    }
+    return launch_status("kv_store_fp8_kernel launch");
 }

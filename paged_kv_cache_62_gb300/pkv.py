@@ -34,6 +34,9 @@ SIGNATURES = {
     "pkv_paged_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                                 _I32, _F32, _P, _I32, _P, _P]),
     "pkv_copy_blocks": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P]),
+    "pkv_kv_store_fp8": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]),
+    "pkv_paged_decode_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                                            _I32, _F32, _P, _P, _SZ, _I32, _P, _P]),
     "pkv_allocator_create": (_P, [_I32, _I32]),
     "pkv_allocator_destroy": (None, [_P]),
     "pkv_allocator_add": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32]),
@@ -259,3 +262,39 @@ class BlockAllocator:
         _check(self._lib.pkv_allocator_tables(self._h, ids.data_ptr(), len(ids), bt.data_ptr(), int(max_blocks),
                                               lens.data_ptr()), "pkv_allocator_tables")
         return bt, lens
+
+
+def kv_store_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                 v_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                 err_word: torch.Tensor | None = None, stream=None) -> None:
+    """kv_store into E4M3 caches (uint8 [NB, bs, Hkv, D]) with per-kv-head float32 scales."""
+    T, Hkv, D = k.shape
+    NB, bs, Hkv2, D2 = k_cache.shape
+    if (Hkv2, D2) != (Hkv, D) or v.shape != k.shape or v_cache.shape != k_cache.shape or slot_mapping.numel() != T \
+            or k_scale.numel() != Hkv or v_scale.numel() != Hkv:
+        raise ValueError("kv_store_fp8: shape mismatch")
+    _check(load().pkv_kv_store_fp8(
+        _dev(k, torch.bfloat16, "k", 3), _dev(v, torch.bfloat16, "v", 3), _dev(slot_mapping, torch.int32, "slot_mapping"),
+        T, _dev(k_cache, torch.uint8, "k_cache", 4), _dev(v_cache, torch.uint8, "v_cache", 4), NB, bs, Hkv, D,
+        _dev(k_scale, torch.float32, "k_scale"), _dev(v_scale, torch.float32, "v_scale"), _opt(err_word),
+        _stream(stream)), "pkv_kv_store_fp8")
+
+
+def paged_decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
+                     v_scale: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                     out: torch.Tensor, workspace: torch.Tensor, max_context_len: int | None = None,
+                     num_workers: int = 0, err_word: torch.Tensor | None = None, stream=None) -> None:
+    """paged_decode over E4M3 caches (uint8 [NB, bs, Hkv, D]) with per-kv-head float32 scales."""
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape or block_tables.shape[0] != B or context_lens.numel() != B \
+            or out.shape != q.shape or k_scale.numel() != Hkv or v_scale.numel() != Hkv:
+        raise ValueError("paged_decode_fp8: shape mismatch")
+    mx = int(block_tables.shape[1]) * bs if max_context_len is None else int(max_context_len)
+    _check(load().pkv_paged_decode_fp8(
+        _dev(q, torch.bfloat16, "q", 3), _dev(k_cache, torch.uint8, "k_cache", 4), _dev(v_cache, torch.uint8, "v_cache", 4),
+        _dev(k_scale, torch.float32, "k_scale"), _dev(v_scale, torch.float32, "v_scale"),
+        _dev(block_tables, torch.int32, "block_tables", 2), block_tables.shape[1],
+        _dev(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs, NB, mx, float(scale),
+        _dev(out, torch.bfloat16, "out", 3), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        int(num_workers), _opt(err_word), _stream(stream)), "pkv_paged_decode_fp8")
