@@ -89,9 +89,9 @@ def step_bytes(wl) -> dict:
     row = Hkv * D * 2
     decode = int(lens.sum()) * row * 2 + B * Hq * D * 2 * 2          # K+V rows read, q read, out written
     decode_index = B * 4 + int(sum(-(-int(L) // s.block_size) for L in lens)) * 4
-    t_valid = B - len(wl.skip_tokens)
-    store = t_valid * row * 2 * 2 + wl.num_tokens * 4                 # k,v read + cache rows written + slots
-    slots = B * 4 * 2 + wl.num_tokens * 4
+    # the step stores each sequence's new token with the fused slot + store kernel (pkv_decode_store)
+    store = B * row * 2 * 2 + B * 4 * 2                               # k,v read + cache rows written; len + entry
+    slots = 0
     L = s.layers
     return {"decode": decode + decode_index, "store": store, "slots": slots,
             "step": L * (decode + decode_index + store) + slots, "decode_kv_only": int(lens.sum()) * row * 2}
@@ -193,18 +193,21 @@ def run_pkv(args):
     s = wl.spec
     B, Hq, Hkv, D = s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim
     max_ctx = int(wl.lens_host().max())
-    slots = torch.empty(wl.num_tokens, dtype=torch.int32, device=dev)
     outs = [torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev) for _ in wl.layers]
     wsbuf = pkv.alloc_workspace(B, Hq, Hkv, D, dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 1 + 3 * len(wl.layers)
+    launches_per_step = 2 * len(wl.layers)
+    # one new token per sequence: rows [0, B) of the step's k / v (the workload's extra padding rows are
+    # for the unfused kv_store's slot -1 path and are not stored by a decode step)
+    k_step = [lay.k_new[:B].contiguous() for lay in wl.layers]
+    v_step = [lay.v_new[:B].contiguous() for lay in wl.layers]
 
     def step(dec_events=None, st=None):
         st = stream if st is None else st
-        pkv.decode_slot_mapping(wl.block_tables, wl.context_lens, s.block_size, wl.num_blocks, slots, err, st)
         for li, lay in enumerate(wl.layers):
-            pkv.kv_store(lay.k_new, lay.v_new, slots, lay.k_cache, lay.v_cache, err, st)
+            pkv.decode_store(k_step[li], v_step[li], wl.block_tables, wl.context_lens, lay.k_cache, lay.v_cache,
+                             err_word=err, stream=st)
             if dec_events is not None:
                 dec_events[li][0].record(st)
             pkv.paged_decode(lay.q, lay.k_cache, lay.v_cache, wl.block_tables, wl.context_lens, wl.scale,
@@ -338,15 +341,15 @@ def run_pkv(args):
     # ---- end to end: host buffers in, host result out, through the same public calls
     host = {
         "q": [lay.q.cpu().pin_memory() for lay in wl.layers],
-        "k": [lay.k_new.cpu().pin_memory() for lay in wl.layers],
-        "v": [lay.v_new.cpu().pin_memory() for lay in wl.layers],
+        "k": [t.cpu().pin_memory() for t in k_step],
+        "v": [t.cpu().pin_memory() for t in v_step],
         "bt": wl.block_tables.cpu().pin_memory(),
         "lens": wl.context_lens.cpu().pin_memory(),
         "out": [torch.empty(B, Hq, D, dtype=torch.bfloat16).pin_memory() for _ in wl.layers],
     }
     d_q = [torch.empty_like(lay.q) for lay in wl.layers]
-    d_k = [torch.empty_like(lay.k_new) for lay in wl.layers]
-    d_v = [torch.empty_like(lay.v_new) for lay in wl.layers]
+    d_k = [torch.empty_like(t) for t in k_step]
+    d_v = [torch.empty_like(t) for t in v_step]
     d_bt = torch.empty_like(wl.block_tables)
     d_lens = torch.empty_like(wl.context_lens)
     h2d = sum(t.numel() * t.element_size() for k in ("q", "k", "v") for t in host[k]) + \
@@ -356,12 +359,11 @@ def run_pkv(args):
     def e2e_step():
         d_bt.copy_(host["bt"], non_blocking=True)
         d_lens.copy_(host["lens"], non_blocking=True)
-        pkv.decode_slot_mapping(d_bt, d_lens, s.block_size, wl.num_blocks, slots, err, stream)
         for li, lay in enumerate(wl.layers):
             d_q[li].copy_(host["q"][li], non_blocking=True)
             d_k[li].copy_(host["k"][li], non_blocking=True)
             d_v[li].copy_(host["v"][li], non_blocking=True)
-            pkv.kv_store(d_k[li], d_v[li], slots, lay.k_cache, lay.v_cache, err, stream)
+            pkv.decode_store(d_k[li], d_v[li], d_bt, d_lens, lay.k_cache, lay.v_cache, err_word=err, stream=stream)
             pkv.paged_decode(d_q[li], lay.k_cache, lay.v_cache, d_bt, d_lens, wl.scale, outs[li], wsbuf,
                              max_context_len=max_ctx, err_word=err, stream=stream)
             host["out"][li].copy_(outs[li], non_blocking=True)

@@ -130,6 +130,33 @@ PKV_API pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, const int3
                         int32_t head_dim, int32_t *err_word, pkv_stream_t stream);
 
 /*
+ * pkv_decode_store -- a decode step's store in one launch: the slot of each
+ * sequence's new token (pkv_decode_slot_mapping) and the store of its K and V
+ * rows there (pkv_kv_store), fused.
+ *
+ * Row b of k and v (one new token per sequence) goes to the slot of position
+ * context_lens[b] - 1: block_tables[b][pos / block_size] * block_size +
+ * pos % block_size (nano-vLLM lab manual §5.2.3, nano-vllm KV-cache post §4.4;
+ * store as in the MinivLLM review, "注意力内核的三个分支").  A sequence with
+ * context_lens[b] == 0 is a padding row: nothing is written.
+ *
+ *   k, v          [num_seqs, num_kv_heads, head_dim] bf16
+ *   block_tables  [num_seqs, max_blocks_per_seq] int32; context_lens [num_seqs]
+ *   k_cache,
+ *   v_cache       [num_blocks, block_size, num_kv_heads, head_dim] bf16
+ *   slot_mapping  may be NULL; else [num_seqs] int32 receives the slots (-1
+ *                 for padding rows and rejected ones)
+ * Errors as the two calls it fuses (PKV_ERR_CONTEXT_RANGE, PKV_ERR_BLOCK_RANGE;
+ * the row is then skipped).  block_size a power of two; head_dim *
+ * num_kv_heads * 2 bytes a multiple of 16.
+ */
+PKV_API pkv_status pkv_decode_store(const uint16_t *k, const uint16_t *v, const int32_t *block_tables,
+                                    int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                                    uint16_t *k_cache, uint16_t *v_cache, int32_t num_blocks,
+                                    int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t *slot_mapping, int32_t *err_word, pkv_stream_t stream);
+
+/*
  * Bytes of device workspace that pkv_paged_decode needs for these sizes
  * (split-K partial states, one arrival counter per (sequence, kv head), and a
  * small load-balance record).  Depends only on the arguments; 0 means the

@@ -6,6 +6,8 @@
 // pkv_kv_store: row slot_mapping[t] of k_cache / v_cache becomes a copy of
 //   k[t] / v[t]; slot -1 skips the row (MinivLLM review, "注意力内核的三个分支").
 //
+// pkv_decode_store: both in one launch for a decode step (one new token per
+//   sequence, at position context_lens[b] - 1).
 // pkv_kv_store_fp8: the same scatter into E4M3 caches, each element stored as
 //   the E4M3 code of x / scale[kv head] (an IEEE binary32 division, then the
 //   conversion's round to nearest even, saturating at +-448).
@@ -78,6 +80,50 @@ __global__ void kv_store_kernel(const uint4 *__restrict__ k, const uint4 *__rest
         const uint4 b = __ldg(vs + i);
         kd[i] = a;
         vd[i] = b;
+    }
+}
+
+// A decode step's store in one launch: CTA b computes the slot of position
+// L_b - 1 (every thread loads the same length and table entry, so no
+// barrier is needed) and copies row b of k and v there.
+__global__ void decode_store_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                    const int32_t *__restrict__ block_tables, int32_t max_blocks,
+                                    const int32_t *__restrict__ context_lens, int32_t block_size, int32_t log2_bs,
+                                    int32_t num_blocks, uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                                    int32_t row_vecs, int32_t *__restrict__ slot_mapping, int32_t *err)
+{
+    griddep_launch_dependents();
+    griddep_wait();
+    const int32_t b = blockIdx.x;
+    const int32_t len = __ldg(context_lens + b);
+    int64_t slot = -1;
+    if (len > 0) {
+        const int32_t pos = len - 1;
+        const int32_t logical = pos >> log2_bs;
+        if (logical >= max_blocks) {
+            if (threadIdx.x == 0) flag_error(err, PKV_ERR_CONTEXT_RANGE);
+        } else {
+            const int32_t phys = __ldg(block_tables + int64_t(b) * max_blocks + logical);
+            if (phys < 0 || phys >= num_blocks) {
+                if (threadIdx.x == 0) flag_error(err, PKV_ERR_BLOCK_RANGE);
+            } else {
+                slot = int64_t(phys) * block_size + (pos & (block_size - 1));
+            }
+        }
+    } else if (len < 0 && threadIdx.x == 0) {
+        flag_error(err, PKV_ERR_CONTEXT_RANGE);
+    }
+    if (slot_mapping && threadIdx.x == 0) slot_mapping[b] = int32_t(slot);
+    if (slot < 0) return;
+    const uint4 *ks = k + int64_t(b) * row_vecs;
+    const uint4 *vs = v + int64_t(b) * row_vecs;
+    uint4 *kd = k_cache + slot * row_vecs;
+    uint4 *vd = v_cache + slot * row_vecs;
+    for (int32_t i = threadIdx.x; i < row_vecs; i += blockDim.x) {
+        const uint4 a = __ldg(ks + i);
+        const uint4 c = __ldg(vs + i);
+        kd[i] = a;
+        vd[i] = c;
     }
 }
 
@@ -276,4 +322,33 @@ extern "C" pkv_status pkv_kv_store_fp8(const uint16_t *k, const uint16_t *v, con
         return cuda_fail("kv_store_fp8_kernel launch", e);
     }
     return launch_status("kv_store_fp8_kernel launch");
+}
+
+extern "C" pkv_status pkv_decode_store(const uint16_t *k, const uint16_t *v, const int32_t *block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                                       uint16_t *k_cache, uint16_t *v_cache, int32_t num_blocks, int32_t block_size,
+                                       int32_t num_kv_heads, int32_t head_dim, int32_t *slot_mapping,
+                                       int32_t *err_word, pkv_stream_t stream)
+{
+    if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return PKV_EINVAL;
+    if (!is_pow2(block_size) || static_cast<int64_t>(num_blocks) * block_size > INT32_MAX) return PKV_EINVAL;
+    const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * 2;
+    if (row_bytes % 16 != 0 || row_bytes / 16 > INT32_MAX) return PKV_EINVAL;
+    if (num_seqs == 0) return PKV_OK;
+    if (!k || !v || !block_tables || !context_lens || !k_cache || !v_cache) return PKV_EINVAL;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
+    const int32_t row_vecs = static_cast<int32_t>(row_bytes / 16);
+    const int threads = row_vecs >= 256 ? 256 : ((row_vecs + 31) / 32) * 32;
+    const cudaError_t e =
+        launch_pdl(decode_store_kernel, dim3(num_seqs), dim3(threads), 0, reinterpret_cast<cudaStream_t>(stream),
+                   reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v), block_tables,
+                   max_blocks_per_seq, context_lens, block_size, ilog2(block_size), num_blocks,
+                   reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache), row_vecs, slot_mapping,
+                   err_word);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return cuda_fail("decode_store_kernel launch", e);
+    }
+    return launch_status("decode_store_kernel launch");
 }

@@ -34,6 +34,7 @@ SIGNATURES = {
     "pkv_paged_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                                 _I32, _F32, _P, _I32, _P, _P]),
     "pkv_copy_blocks": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P]),
+    "pkv_decode_store": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P]),
     "pkv_kv_store_fp8": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]),
     "pkv_paged_decode_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                             _I32, _F32, _P, _P, _SZ, _I32, _P, _P]),
@@ -298,3 +299,21 @@ def paged_decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         _dev(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs, NB, mx, float(scale),
         _dev(out, torch.bfloat16, "out", 3), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
         int(num_workers), _opt(err_word), _stream(stream)), "pkv_paged_decode_fp8")
+
+
+def decode_store(k: torch.Tensor, v: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                 k_cache: torch.Tensor, v_cache: torch.Tensor, slot_mapping: torch.Tensor | None = None,
+                 err_word: torch.Tensor | None = None, stream=None) -> None:
+    """A decode step's slot computation and store in one launch (row b -> position context_lens[b] - 1)."""
+    B, Hkv, D = k.shape
+    NB, bs, Hkv2, D2 = k_cache.shape
+    if (Hkv2, D2) != (Hkv, D) or v.shape != k.shape or v_cache.shape != k_cache.shape or \
+            block_tables.shape[0] != B or context_lens.numel() != B or \
+            (slot_mapping is not None and slot_mapping.numel() != B):
+        raise ValueError("decode_store: shape mismatch")
+    sm = None if slot_mapping is None else _dev(slot_mapping, torch.int32, "slot_mapping")
+    _check(load().pkv_decode_store(
+        _dev(k, torch.bfloat16, "k", 3), _dev(v, torch.bfloat16, "v", 3), _dev(block_tables, torch.int32, "block_tables", 2),
+        block_tables.shape[1], _dev(context_lens, torch.int32, "context_lens"), B,
+        _dev(k_cache, torch.bfloat16, "k_cache", 4), _dev(v_cache, torch.bfloat16, "v_cache", 4), NB, bs, Hkv, D, sm,
+        _opt(err_word), _stream(stream)), "pkv_decode_store")

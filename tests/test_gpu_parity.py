@@ -118,6 +118,31 @@ def test_store_then_decode(name):
         del kc_h, vc_h
 
 
+@pytest.mark.parametrize("name", W.ORDER)
+def test_fused_decode_store_bit_exact(name):
+    """pkv_decode_store (slot of position L - 1, then the store, in one launch) against the oracle's
+    slot mapping and store; one sequence turned into a padding row (context_len 0) writes nothing."""
+    wl = W.make(name, "cuda", layers=1)
+    s, lay = wl.spec, wl.layers[0]
+    B = s.num_seqs
+    lens = wl.context_lens.clone()
+    lens[B // 2] = 0
+    lens_h = lens.cpu().numpy()
+    bt_h = wl.block_tables.cpu().numpy()
+    kc_h, vc_h = W.bits(lay.k_cache), W.bits(lay.v_cache)
+    slots = torch.full((B,), 7, dtype=torch.int32, device="cuda")
+    err = err_word()
+    pkv.decode_store(lay.k_new[:B].contiguous(), lay.v_new[:B].contiguous(), wl.block_tables, lens, lay.k_cache,
+                     lay.v_cache, slots, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    want = oracle.decode_slot_mapping(bt_h, lens_h, s.block_size, B)
+    assert want[B // 2] == -1
+    assert np.array_equal(slots.cpu().numpy(), want)
+    oracle.kv_store(W.bits(lay.k_new)[:B], W.bits(lay.v_new)[:B], want, kc_h, vc_h)
+    assert np.array_equal(W.bits(lay.k_cache), kc_h) and np.array_equal(W.bits(lay.v_cache), vc_h)
+
+
 # --------------------------------------------------------------------------- mini-vLLM-style matrix
 def synth(B, L, Hq, Hkv, D, bs, seed, lens=None, extra=5):
     """Random paged problem with a shuffled pool and NaN canaries in unowned rows."""
