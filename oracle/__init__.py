@@ -66,6 +66,7 @@ def _load():
     lib.oracle_e4m3_decode.argtypes = [P, i64, P]
     lib.oracle_e4m3_encode.argtypes = [P, i64, P]
     lib.oracle_kv_store_fp8.argtypes = [P, P, P, i32, P, P, i64, i32, i32, P, P]
+    lib.oracle_paged_attention.argtypes = [P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, f64, P, i32]
     lib.oracle_paged_decode_fp8.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, f64, P, i32]
     for name in ("oracle_slot_of", "oracle_decode_slot_mapping", "oracle_kv_store",
                  "oracle_paged_decode", "oracle_partial_state", "oracle_merge_states"):
@@ -168,6 +169,27 @@ def paged_decode_fp8(q_bits, k_cache8, v_cache8, k_scale, v_scale, block_tables,
     _check(_load().oracle_paged_decode_fp8(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt), bt.shape[1],
                                            _ptr(ctx), B, Hq, Hkv, D, bs, NB, float(scale), _ptr(out),
                                            int(nthreads)), "paged_decode_fp8")
+    return out
+
+
+def paged_attention(q_bits, k_cache_bits, v_cache_bits, block_tables, cu_seqlens_q, context_lens, scale: float,
+                    nthreads: int = 1) -> np.ndarray:
+    """fp64 output [T, Hq, D]: causal attention of each sequence's last n new tokens (query rows
+    cu_seqlens_q[b] .. cu_seqlens_q[b+1]) over its L = context_lens[b] cached tokens."""
+    q = _c(q_bits, np.uint16)
+    kc, vc = _c(k_cache_bits, np.uint16), _c(v_cache_bits, np.uint16)
+    bt = _c(block_tables, np.int32)
+    cu = _c(cu_seqlens_q, np.int32)
+    ctx = _c(context_lens, np.int32)
+    T, Hq, D = q.shape
+    B = ctx.size
+    if cu.size != B + 1 or int(cu[-1]) != T:
+        raise OracleError("cu_seqlens_q must have B + 1 entries ending at the number of query rows")
+    NB, bs, Hkv, _ = kc.shape
+    out = np.empty((T, Hq, D), np.float64)
+    _check(_load().oracle_paged_attention(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cu), _ptr(ctx), B,
+                                          Hq, Hkv, D, bs, NB, float(scale), _ptr(out), int(nthreads)),
+           "paged_attention")
     return out
 
 

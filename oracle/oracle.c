@@ -253,6 +253,7 @@ typedef struct {
     const uint8_t *k8, *v8;           /* E4M3 caches instead of bf16 (then k_cache, v_cache unused) */
     const float *k_scale, *v_scale;   /* their per-kv-head scales */
     const int32_t *block_tables, *context_lens;
+    const int32_t *row_seq;           /* query row -> sequence whose table it reads (NULL: the row itself) */
     int32_t num_seqs, hq, hkv, d, block_size, num_blocks, max_blocks;
     double scale;
     double *out;
@@ -283,7 +284,7 @@ static int decode_one(const decode_job *J, int32_t b, int32_t h, double *scores)
     if (len < 0 || (int64_t)len > (int64_t)J->max_blocks * J->block_size) return ORACLE_EBOUNDS;
 
     const uint16_t *qv = J->q + ((int64_t)b * J->hq + h) * d_all;
-    const int32_t *row = J->block_tables + (int64_t)b * J->max_blocks;
+    const int32_t *row = J->block_tables + (int64_t)(J->row_seq ? J->row_seq[b] : b) * J->max_blocks;
 
     /* pass 1: scores and their maximum */
     double m = -INFINITY;
@@ -335,9 +336,51 @@ int oracle_paged_decode(const uint16_t *q, const uint16_t *k_cache, const uint16
                         double scale, double *out, int32_t nthreads)
 {
     if (!k_cache || !v_cache) return ORACLE_EINVAL;
-    decode_job J = {q, k_cache, v_cache, NULL, NULL, NULL, NULL, block_tables, context_lens,
+    decode_job J = {q, k_cache, v_cache, NULL, NULL, NULL, NULL, block_tables, context_lens, NULL,
                     num_seqs, hq, hkv, d, block_size, num_blocks, max_blocks, scale, out, 1, 0, ORACLE_OK};
     return run_decode(J, nthreads);
+}
+
+/* ---------------------------------------------------------------------------
+ * Paged attention with several new tokens per sequence (chunked prefill over a
+ * cached prefix, or a mixed batch of prefills and decodes): sequence b holds
+ * L = context_lens[b] tokens in the cache, the last n = cu_seqlens_q[b+1] -
+ * cu_seqlens_q[b] of them new; its query row r = cu_seqlens_q[b] + i (i < n)
+ * sits at position p = L - n + i and attends the keys j <= p (causal
+ * attention over the cached prefix and the new tokens before it: the
+ * nano-vllm KV-cache post §3.5 builds the slots of such a chunk, the mini-vLLM
+ * README names the prefill with a cached prefix as the next step).  Each row
+ * is the decode definition above with context length p + 1 and sequence b's
+ * block table.  q, out: [T, Hq, D] with T = cu_seqlens_q[B].  n > L, or a
+ * decreasing cu_seqlens_q, is ORACLE_EINVAL.
+ * ------------------------------------------------------------------------- */
+int oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                           const int32_t *block_tables, int32_t max_blocks, const int32_t *cu_seqlens_q,
+                           const int32_t *context_lens, int32_t num_seqs, int32_t hq, int32_t hkv, int32_t d,
+                           int32_t block_size, int32_t num_blocks, double scale, double *out, int32_t nthreads)
+{
+    if (!cu_seqlens_q || !context_lens || num_seqs < 0 || cu_seqlens_q[0] != 0) return ORACLE_EINVAL;
+    const int32_t T = cu_seqlens_q[num_seqs];
+    int32_t *row_seq = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+    int32_t *row_len = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+    if (!row_seq || !row_len) { free(row_seq); free(row_len); return ORACLE_EINVAL; }
+    int rc = ORACLE_OK;
+    for (int32_t b = 0; b < num_seqs && rc == ORACLE_OK; ++b) {
+        const int32_t n = cu_seqlens_q[b + 1] - cu_seqlens_q[b], L = context_lens[b];
+        if (n < 0 || n > L) { rc = ORACLE_EINVAL; break; }
+        for (int32_t i = 0; i < n; ++i) {
+            row_seq[cu_seqlens_q[b] + i] = b;
+            row_len[cu_seqlens_q[b] + i] = L - n + i + 1;
+        }
+    }
+    if (rc == ORACLE_OK) {
+        decode_job J = {q, k_cache, v_cache, NULL, NULL, NULL, NULL, block_tables, row_len, row_seq,
+                        T, hq, hkv, d, block_size, num_blocks, max_blocks, scale, out, 1, 0, ORACLE_OK};
+        rc = run_decode(J, nthreads);
+    }
+    free(row_seq);
+    free(row_len);
+    return rc;
 }
 
 /* The same attention over E4M3 caches: K_j, V_j are the codes' values times
@@ -350,7 +393,7 @@ int oracle_paged_decode_fp8(const uint16_t *q, const uint8_t *k_cache, const uin
                             double scale, double *out, int32_t nthreads)
 {
     if (!k_cache || !v_cache || !k_scale || !v_scale) return ORACLE_EINVAL;
-    decode_job J = {q, NULL, NULL, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+    decode_job J = {q, NULL, NULL, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, NULL,
                     num_seqs, hq, hkv, d, block_size, num_blocks, max_blocks, scale, out, 1, 0, ORACLE_OK};
     return run_decode(J, nthreads);
 }

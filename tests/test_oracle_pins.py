@@ -496,6 +496,39 @@ def test_fp8_decode_is_attention_over_the_dequantised_cache():
     assert np.array_equal(oracle.paged_decode_fp8(q, kc, vc, ks, vs * 2, bt, lens, 0.125), 2 * got)
 
 
+@pytest.mark.parametrize("Hq,Hkv,D,bs", [(4, 2, 64, 16), (8, 8, 128, 8)])
+def test_paged_attention_is_causal_sdpa_over_the_sequence(Hq, Hkv, D, bs):
+    """Chunked prefill / mixed batch: the last n tokens of each sequence attend causally over all its
+    L cached tokens.  Against torch's scaled_dot_product_attention (fp64, is_causal) run on the whole
+    contiguous sequence with every token as a query, keeping the last n query rows; n = L (a whole
+    prefill), 1 < n < L (a chunk after a cached prefix) and n = 1 (a decode) are all in the batch."""
+    rng = np.random.default_rng(Hq + D)
+    lens = [37, 16, 50, 1, 29]
+    news = [37, 5, 1, 1, 12]
+    seqs_k = [rand_bits(rng, (L, Hkv, D)) for L in lens]
+    seqs_v = [rand_bits(rng, (L, Hkv, D)) for L in lens]
+    kc, vc, bt = paged_from_contiguous(seqs_k, seqs_v, bs, rng)
+    cu = np.concatenate([[0], np.cumsum(news)]).astype(np.int32)
+    qs = [rand_bits(rng, (L, Hq, D)) for L in lens]            # a query for every token; the last n are used
+    q = np.concatenate([qq[L - n:] for qq, L, n in zip(qs, lens, news)])
+    got = oracle.paged_attention(q, kc, vc, bt, cu, np.array(lens, np.int32), 0.125)
+    for b, (L, n) in enumerate(zip(lens, news)):
+        qq = torch.from_numpy(bits_to_f64(qs[b])).permute(1, 0, 2).unsqueeze(0)          # [1, Hq, L, D]
+        k = torch.from_numpy(bits_to_f64(seqs_k[b])).permute(1, 0, 2).unsqueeze(0).repeat_interleave(Hq // Hkv, 1)
+        v = torch.from_numpy(bits_to_f64(seqs_v[b])).permute(1, 0, 2).unsqueeze(0).repeat_interleave(Hq // Hkv, 1)
+        want = torch.nn.functional.scaled_dot_product_attention(qq, k, v, scale=0.125, is_causal=True)
+        want = want[0, :, L - n:, :].permute(1, 0, 2).numpy()                            # [n, Hq, D]
+        np.testing.assert_allclose(got[cu[b]:cu[b + 1]], want, rtol=1e-10, atol=1e-12)
+    # one new token per sequence is the decode definition
+    ones = np.arange(len(lens) + 1, dtype=np.int32)
+    qd = rand_bits(rng, (len(lens), Hq, D))
+    assert np.array_equal(oracle.paged_attention(qd, kc, vc, bt, ones, np.array(lens, np.int32), 0.125),
+                          oracle.paged_decode(qd, kc, vc, bt, np.array(lens, np.int32), 0.125))
+    with pytest.raises(oracle.OracleError):
+        oracle.paged_attention(q[:2], kc, vc, bt, np.array([0, 2, 2, 2, 2, 2], np.int32),
+                               np.array([1, 1, 1, 1, 1], np.int32), 0.125)   # 2 new tokens in a length-1 sequence
+
+
 def test_generator_structure():
     """Generator invariants the parity tests rely on (no arithmetic under test involved)."""
     for name in ("tiny", "qwen25_0p5b"):
