@@ -274,6 +274,43 @@ def run_pkv(args):
     g_ms = reduce_over_ranks(g0.elapsed_time(g1) / g_steps, "max", dev)
     assert err.item() == 0, f"device error word {err.item():#x}"
 
+    # ---- several new tokens per sequence (pkv_paged_attention): layer 0 with the last 4 tokens of every
+    # sequence as queries (a speculative-decoding verify step), causal over each sequence's cache
+    mixed = None
+    if not args.no_fp8:
+        lay0 = wl.layers[0]
+        nq = 4
+        lens_h = wl.lens_host().astype(np.int64)
+        if lens_h.min() >= nq:
+            cu = torch.arange(0, (B + 1) * nq, nq, dtype=torch.int32, device=dev)
+            qm = torch.randn(B * nq, Hq, D, device=dev).bfloat16()
+            outm = torch.empty_like(qm)
+            wsm = pkv.alloc_attention_workspace(B * nq, Hq, Hkv, D, dev)
+
+            def att():
+                pkv.paged_attention(qm, lay0.k_cache, lay0.v_cache, wl.block_tables, cu, wl.context_lens, wl.scale,
+                                    outm, wsm, max_context_len=max_ctx, err_word=err, stream=stream)
+            for _ in range(5):
+                att()
+            torch.cuda.synchronize()
+            mev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+            for c0, c1 in mev:
+                c0.record(stream)
+                att()
+                c1.record(stream)
+            torch.cuda.synchronize()
+            assert err.item() == 0, f"device error word {err.item():#x}"
+            us_m = float(np.mean([c0.elapsed_time(c1) for c0, c1 in mev])) * 1e3
+            row = Hkv * D * 2 * 2
+            unique = int(lens_h.sum()) * row
+            streamed = int(sum(L - nq + 1 + i for L in lens_h for i in range(nq))) * row
+            mixed = {"kernel": "pkv_paged_attention (expand_rows_kernel + paged_decode_kernel, one row per query)",
+                     "query_rows": B * nq, "new_tokens_per_sequence": nq, "mean_call_us": round(us_m, 2),
+                     "unique_kv_bytes": unique, "streamed_kv_bytes": streamed,
+                     "unique_gbs": round(unique / (us_m * 1e-6) / 1e9, 1),
+                     "streamed_gbs": round(streamed / (us_m * 1e-6) / 1e9, 1),
+                     "note": "each query row streams its own keys; L2 catches part of the re-reads"}
+
     # ---- copy-on-write block copies (pkv_copy_blocks) on this workload's pool: owned blocks copied
     # into blocks no sequence holds, as many pairs as there are such blocks (up to 256)
     cow = None
@@ -424,6 +461,8 @@ def run_pkv(args):
                           "all replays); the headline value above is plain stream launches"},
         "clocks": clocks.summary(),
     }
+    if mixed is not None:
+        line["mixed"] = mixed
     if fp8 is not None:
         fp8["peak"] = peak
         fp8["frac"] = round(fp8["achieved"] / peak, 4)

@@ -268,6 +268,45 @@ PKV_API pkv_status pkv_paged_decode_noalloc(const uint16_t *q, const uint16_t *k
                                     int32_t *err_word, pkv_stream_t stream);
 
 /*
+ * pkv_paged_attention -- paged attention for several new tokens per sequence:
+ * a chunk of a prefill over a cached prefix, or a batch that mixes prefill
+ * chunks with decode steps (one new token).
+ *
+ * The nano-vllm KV-cache post (§3.5) builds the slots of such a chunk and the
+ * mini-vLLM README names the prefill over a cached prefix as the next step.
+ * Sequence b holds L = context_lens[b] tokens in the cache (the chunk's K/V
+ * already stored there, pkv_kv_store), the last n = cu_seqlens_q[b+1] -
+ * cu_seqlens_q[b] of them new; query row r = cu_seqlens_q[b] + i (i < n) sits
+ * at position L - n + i and attends causally the keys j <= L - n + i:
+ *     out[r, h] = sum_{j<=p} softmax_j(scale * q[r, h] . K_j) V_j,  p = L - n + i,
+ * K_j, V_j read through sequence b's block table row as in pkv_paged_decode.
+ *
+ *   q, out        [num_rows, num_q_heads, head_dim] bf16, num_rows =
+ *                 cu_seqlens_q[num_seqs] (the host-known row count)
+ *   cu_seqlens_q  [num_seqs + 1] int32, device, non-decreasing from 0
+ *   context_lens  [num_seqs] int32, device: cached tokens per sequence,
+ *                 new ones included
+ *   workspace     pkv_paged_attention_workspace_size(num_rows, ...) bytes,
+ *                 zero-filled before first use (as pkv_paged_decode's)
+ * Rows inconsistent with the offsets (n > L, rows outside every sequence's
+ * range) give zeros and PKV_ERR_CONTEXT_RANGE.  num_rows <= PKV_MAX_SEQS;
+ * other limits, num_workers and errors as pkv_paged_decode.  Each query row
+ * streams its own keys (the decode kernel, one row per query): right for
+ * mixed batches with short runs of new tokens; a long prefill re-reads its
+ * prefix once per query row.
+ */
+PKV_API size_t pkv_paged_attention_workspace_size(int32_t num_rows, int32_t num_q_heads,
+                                                  int32_t num_kv_heads, int32_t head_dim);
+PKV_API pkv_status pkv_paged_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                                       int32_t num_seqs, int32_t num_rows, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                       int32_t num_blocks, int32_t max_context_len, float scale,
+                                       uint16_t *out, void *workspace, size_t workspace_bytes,
+                                       int32_t num_workers, int32_t *err_word, pkv_stream_t stream);
+
+/*
  * E4M3 (fp8) KV cache.  The mini-vLLM README lists "no FP8 KV" among its gaps
  * to production vLLM (§ "与 production vLLM 的关键差距") and gives no format;
  * this library stores the OCP 8-bit floating point E4M3 encoding

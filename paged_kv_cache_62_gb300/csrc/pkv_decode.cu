@@ -17,7 +17,8 @@ extern "C" size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_
 // Shared by the bf16 and the E4M3 entry points (k_scale / v_scale: the
 // latter's per-kv-head scales, device arrays).
 static pkv_status decode_call(bool fp8, const uint16_t *q, const void *k_cache, const void *v_cache,
-                              const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                              const float *k_scale, const float *v_scale, const int32_t *row_seq,
+                              const int32_t *block_tables,
                               int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                               int32_t num_blocks, int32_t max_context_len, float scale, uint16_t *out,
@@ -81,6 +82,7 @@ static pkv_status decode_call(bool fp8, const uint16_t *q, const void *k_cache, 
     p.scale_log2 = float(double(scale) * 1.4426950408889634);
     p.k_scale = k_scale;
     p.v_scale = v_scale;
+    p.row_seq = row_seq;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
     a.device = dev.device;
@@ -103,7 +105,8 @@ extern "C" pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cach
                                        void *workspace, size_t workspace_bytes, int32_t num_workers,
                                        int32_t *err_word, pkv_stream_t stream)
 {
-    return decode_call(false, q, k_cache, v_cache, nullptr, nullptr, block_tables, max_blocks_per_seq, context_lens,
+    return decode_call(false, q, k_cache, v_cache, nullptr, nullptr, nullptr, block_tables, max_blocks_per_seq,
+                       context_lens,
                        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale,
                        out, workspace, workspace_bytes, num_workers, err_word, stream);
 }
@@ -117,7 +120,8 @@ extern "C" pkv_status pkv_paged_decode_fp8(const uint16_t *q, const uint8_t *k_c
                                            size_t workspace_bytes, int32_t num_workers, int32_t *err_word,
                                            pkv_stream_t stream)
 {
-    return decode_call(true, q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq, context_lens,
+    return decode_call(true, q, k_cache, v_cache, k_scale, v_scale, nullptr, block_tables, max_blocks_per_seq,
+                       context_lens,
                        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale,
                        out, workspace, workspace_bytes, num_workers, err_word, stream);
 }
@@ -189,4 +193,85 @@ extern "C" pkv_status pkv_paged_decode_noalloc(const uint16_t *q, const uint16_t
     return pkv_paged_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                             num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, out,
                             scratch, kStaticScratchBytes, num_workers, err_word, stream);
+}
+
+// ------------------------------------------------------------------ several query rows per sequence
+namespace pkv {
+
+// Query row r = cu_seqlens_q[b] + i of sequence b (n = cu_seqlens_q[b+1] -
+// cu_seqlens_q[b] new tokens, L = context_lens[b] in the cache) sits at
+// position L - n + i: it reads sequence b's table with context length
+// L - n + i + 1.  One thread per row finds its sequence by binary search over
+// cu_seqlens_q, so every row gets a sequence in [0, num_seqs) even when the
+// offsets are inconsistent; such rows (not inside their sequence's range,
+// n > L, offsets not starting at 0) get length 0 (zero output) and
+// PKV_ERR_CONTEXT_RANGE.
+__global__ void expand_rows_kernel(const int32_t *__restrict__ cu_seqlens_q, const int32_t *__restrict__ context_lens,
+                                   int32_t num_seqs, int32_t num_rows, int32_t *__restrict__ row_seq,
+                                   int32_t *__restrict__ row_len, int32_t *err)
+{
+    griddep_launch_dependents();
+    griddep_wait();
+    const int32_t r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= num_rows) return;
+    int32_t lo = 0, hi = num_seqs;  // the last b with cu_seqlens_q[b] <= r
+    while (hi - lo > 1) {
+        const int32_t mid = (lo + hi) >> 1;
+        if (__ldg(cu_seqlens_q + mid) <= r)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const int32_t r0 = __ldg(cu_seqlens_q + lo), r1 = __ldg(cu_seqlens_q + lo + 1), L = __ldg(context_lens + lo);
+    const int32_t n = r1 - r0;
+    const bool ok = __ldg(cu_seqlens_q) == 0 && r0 <= r && r < r1 && n <= L;
+    if (!ok) flag_error(err, PKV_ERR_CONTEXT_RANGE);
+    row_seq[r] = lo;
+    row_len[r] = ok ? L - n + (r - r0) + 1 : 0;
+}
+
+inline size_t rows_bytes(int32_t num_rows) { return align256(size_t(num_rows) * 4); }
+
+}  // namespace pkv
+
+extern "C" size_t pkv_paged_attention_workspace_size(int32_t num_rows, int32_t num_q_heads, int32_t num_kv_heads,
+                                                     int32_t head_dim)
+{
+    const size_t base = pkv_paged_decode_workspace_size(num_rows, num_q_heads, num_kv_heads, head_dim);
+    if (base == 0) return 0;
+    return align256(base) + 2 * rows_bytes(num_rows);
+}
+
+extern "C" pkv_status pkv_paged_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                          const int32_t *cu_seqlens_q, const int32_t *context_lens, int32_t num_seqs,
+                                          int32_t num_rows, int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                          int32_t max_context_len, float scale, uint16_t *out, void *workspace,
+                                          size_t workspace_bytes, int32_t num_workers, int32_t *err_word,
+                                          pkv_stream_t stream)
+{
+    if (num_seqs < 0 || num_rows < 0) return PKV_EINVAL;
+    if (num_rows == 0) return PKV_OK;
+    if (num_seqs == 0 || !cu_seqlens_q || !context_lens) return PKV_EINVAL;
+    const size_t need = pkv_paged_attention_workspace_size(num_rows, num_q_heads, num_kv_heads, head_dim);
+    if (need == 0) return num_rows > PKV_MAX_SEQS ? PKV_EUNSUPPORTED : PKV_EINVAL;
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PKV_EWORKSPACE;
+    // the rows' (sequence, length) arrays sit after the decode workspace
+    uint8_t *wsb = static_cast<uint8_t *>(workspace);
+    const size_t dec_bytes = align256(pkv_paged_decode_workspace_size(num_rows, num_q_heads, num_kv_heads, head_dim));
+    int32_t *row_seq = reinterpret_cast<int32_t *>(wsb + dec_bytes);
+    int32_t *row_len = reinterpret_cast<int32_t *>(wsb + dec_bytes + rows_bytes(num_rows));
+    const cudaError_t e = launch_pdl(expand_rows_kernel, dim3((num_rows + 255) / 256), dim3(256), 0,
+                                     reinterpret_cast<cudaStream_t>(stream), cu_seqlens_q, context_lens, num_seqs,
+                                     num_rows, row_seq, row_len, err_word);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return cuda_fail("expand_rows_kernel launch", e);
+    }
+    const pkv_status st = launch_status("expand_rows_kernel launch");
+    if (st != PKV_OK) return st;
+    return decode_call(false, q, k_cache, v_cache, nullptr, nullptr, row_seq, block_tables, max_blocks_per_seq,
+                       row_len, num_rows, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_context_len, scale, out, workspace, dec_bytes, num_workers, err_word, stream);
 }

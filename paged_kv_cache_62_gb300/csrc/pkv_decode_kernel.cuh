@@ -107,6 +107,8 @@ struct DecodeParams {
     int32_t num_workers;         // > 0: fixed split over about num_workers / consumers CTAs; 0: adaptive
     float scale_log2;            // scale * log2(e)
     const float *k_scale, *v_scale;  // E4M3 caches: per-kv-head scales (unused for bf16 caches)
+    const int32_t *row_seq;          // several query rows per sequence: row -> the sequence whose table it
+                                     // reads (null: row b reads table row b)
 };
 
 // What the producer tells the consumers about the unit in a stage.
@@ -874,7 +876,8 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                     // the row and lets it go out together with the length's.
                     const int32_t blk = min(pos >> p.log2_bs, p.max_blocks - 1);
                     nxt_L = __ldg(p.context_lens + mine.b);
-                    nxt_e = __ldg(p.block_tables + (long long)mine.b * p.max_blocks + blk);
+                    const int32_t trow = p.row_seq ? __ldg(p.row_seq + mine.b) : mine.b;
+                    nxt_e = __ldg(p.block_tables + (long long)trow * p.max_blocks + blk);
                 }
             };
             if (nunits > 0) {

@@ -1,0 +1,114 @@
+"""GPU parity of pkv_paged_attention (several new tokens per sequence: prefill
+chunks over a cached prefix mixed with decode steps) against the CPU oracle,
+within the decode tolerance (max-abs 2e-2, mean-abs 2e-3)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_62_gb300 import pkv
+from paged_kv_cache_62_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS = 2e-2, 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def check_close(got, want, what):
+    g = got.float().cpu().double().numpy()
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    d = np.abs(g - want)
+    assert d.max() <= MAX_ABS and d.mean() <= MEAN_ABS, f"{what}: max {d.max():.3g} mean {d.mean():.3g}"
+
+
+def mixed_batch(lens, news, Hq, Hkv, D, bs, seed):
+    """Shuffled bf16 pool with NaN canaries in unowned rows, and queries for each sequence's new tokens."""
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    rng = np.random.default_rng(seed)
+    nblk = [-(-L // bs) for L in lens]
+    NB = sum(nblk) + 4
+    perm = rng.permutation(NB)
+    bt = np.full((len(lens), max(nblk)), -1, np.int32)
+    filled = np.zeros(NB, np.int64)
+    cur = 0
+    for b, L in enumerate(lens):
+        for i in range(nblk[b]):
+            bt[b, i] = perm[cur]
+            filled[perm[cur]] = min(bs, L - i * bs)
+            cur += 1
+    kc = torch.randn(NB, bs, Hkv, D, generator=g, device="cuda").bfloat16()
+    vc = torch.randn(NB, bs, Hkv, D, generator=g, device="cuda").bfloat16()
+    canary = torch.arange(bs, device="cuda").view(1, bs) >= torch.as_tensor(filled, device="cuda").view(NB, 1)
+    kc[canary] = float("nan")
+    vc[canary] = float("nan")
+    cu = np.concatenate([[0], np.cumsum(news)]).astype(np.int32)
+    q = torch.randn(int(cu[-1]), Hq, D, generator=g, device="cuda").bfloat16()
+    return (q, kc, vc, torch.from_numpy(bt).cuda(), torch.from_numpy(cu).cuda(),
+            torch.tensor(lens, dtype=torch.int32, device="cuda"))
+
+
+def oracle_of(q, kc, vc, bt, cu, lens, scale):
+    return oracle.paged_attention(W.bits(q), W.bits(kc), W.bits(vc), bt.cpu().numpy(), cu.cpu().numpy(),
+                                  lens.cpu().numpy(), scale, nthreads=16)
+
+
+def run(q, kc, vc, bt, cu, lens, scale, workers=0, ws=None, err=None):
+    T, Hq, D = q.shape
+    out = torch.full_like(q, float("nan"))
+    ws = pkv.alloc_attention_workspace(T, Hq, kc.shape[2], D) if ws is None else ws
+    pkv.paged_attention(q, kc, vc, bt, cu, lens, scale, out, ws, num_workers=workers, err_word=err)
+    return out
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,bs", [(16, 8, 128, 16), (14, 2, 64, 16), (8, 2, 64, 256), (16, 4, 128, 8)])
+def test_mixed_prefill_chunks_and_decodes(Hq, Hkv, D, bs):
+    lens = [300, 17, 1, 700, 129, 64, 2000, 5]
+    news = [300, 17, 1, 1, 40, 64, 3, 2]      # whole prefills, prefill chunks after a cached prefix, decodes
+    q, kc, vc, bt, cu, lens_t = mixed_batch(lens, news, Hq, Hkv, D, bs, seed=Hq + D + bs)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run(q, kc, vc, bt, cu, lens_t, 0.0884, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    check_close(out, oracle_of(q, kc, vc, bt, cu, lens_t, 0.0884), f"{Hq}/{Hkv} D{D} bs{bs}")
+
+
+@pytest.mark.parametrize("workers", [1, 7, 500])
+def test_forced_splits_and_repeated_calls(workers):
+    lens = [900, 33, 400, 1]
+    news = [100, 33, 2, 1]
+    q, kc, vc, bt, cu, lens_t = mixed_batch(lens, news, 16, 8, 128, 16, seed=workers)
+    want = oracle_of(q, kc, vc, bt, cu, lens_t, 0.0884)
+    check_close(run(q, kc, vc, bt, cu, lens_t, 0.0884, workers=workers), want, f"workers {workers}")
+    ws = pkv.alloc_attention_workspace(q.shape[0], 16, 8, 128)
+    for call in range(3):  # the default split over one workspace, call after call
+        check_close(run(q, kc, vc, bt, cu, lens_t, 0.0884, ws=ws), want, f"call {call}")
+
+
+def test_inconsistent_offsets_give_zeros_and_an_error():
+    lens = [10, 20]
+    news = [3, 4]
+    q, kc, vc, bt, cu, lens_t = mixed_batch(lens, news, 8, 2, 64, 16, seed=1)
+    bad_lens = torch.tensor([2, 20], dtype=torch.int32, device="cuda")   # 3 new tokens in a length-2 sequence
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run(q, kc, vc, bt, cu, bad_lens, 0.125, err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pkv.ERR_CONTEXT_RANGE
+    assert torch.all(out[:3].float() == 0)
+    want = oracle.paged_attention(W.bits(q)[3:], W.bits(kc), W.bits(vc), bt.cpu().numpy()[1:],
+                                  np.array([0, 4], np.int32), np.array([20], np.int32), 0.125)
+    check_close(out[3:], want, "the consistent sequence")
+    short = torch.tensor([0, 3, 5], dtype=torch.int32, device="cuda")   # offsets end before the last rows
+    err.zero_()
+    out = run(q, kc, vc, bt, short, lens_t, 0.125, err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pkv.ERR_CONTEXT_RANGE
+    assert torch.all(out[5:].float() == 0)
