@@ -131,3 +131,52 @@ def test_binding_refuses_cpu_tensors(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         pkv.load(str(tmp_path / "libpkv.so"))
+
+
+def test_newer_entry_points_validate_on_the_host(lib):
+    """Rejected before any CUDA call (FAKE pointers are never dereferenced), or no-ops when empty."""
+    # pkv_decode_store(k, v, bt, max_blocks, lens, B, kc, vc, NB, bs, Hkv, D, slots, err, stream)
+    ds = lib.pkv_decode_store
+    assert ds(FAKE, FAKE, FAKE, 4, FAKE, 2, FAKE, FAKE, 10, 12, 8, 128, NULL, NULL, NULL) == pkv.EINVAL   # bs not 2^k
+    assert ds(NULL, FAKE, FAKE, 4, FAKE, 2, FAKE, FAKE, 10, 16, 8, 128, NULL, NULL, NULL) == pkv.EINVAL
+    assert ds(FAKE + 8, FAKE, FAKE, 4, FAKE, 2, FAKE, FAKE, 10, 16, 8, 128, NULL, NULL, NULL) == pkv.EINVAL
+    assert ds(NULL, NULL, NULL, 4, NULL, 0, NULL, NULL, 10, 16, 8, 128, NULL, NULL, NULL) == pkv.OK
+    # pkv_kv_store_fp8(k, v, slots, T, kc8, vc8, NB, bs, Hkv, D, ks, vs, err, stream)
+    kf = lib.pkv_kv_store_fp8
+    assert kf(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 10, 16, 8, 128, NULL, FAKE, NULL, NULL) == pkv.EINVAL     # no k_scale
+    assert kf(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 10, 16, 8, 60, FAKE, FAKE, NULL, NULL) == pkv.EINVAL      # D % 8
+    assert kf(NULL, NULL, NULL, 0, NULL, NULL, 10, 16, 8, 128, NULL, NULL, NULL, NULL) == pkv.OK
+    # pkv_paged_decode_fp8 shares pkv_paged_decode's checks and needs both scales
+    fd = lib.pkv_paged_decode_fp8
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 2, 16, 8, 128, 16, 10, 64, 0.1, FAKE, FAKE, 1 << 30, 0,
+            NULL, NULL]
+    bad = list(args); bad[3] = NULL
+    assert fd(*bad) == pkv.EINVAL
+    bad = list(args); bad[11] = 96
+    assert fd(*bad) == pkv.EUNSUPPORTED
+    # pkv_copy_blocks(kc, vc, pairs, n, NB, bs, Hkv, D, err, stream)
+    cb = lib.pkv_copy_blocks
+    assert cb(FAKE, FAKE, NULL, 3, 10, 16, 8, 128, NULL, NULL) == pkv.EINVAL
+    assert cb(FAKE, FAKE, FAKE, -1, 10, 16, 8, 128, NULL, NULL) == pkv.EINVAL
+    assert cb(FAKE, FAKE, FAKE, 3, 10, 1, 1, 4, NULL, NULL) == pkv.EINVAL                              # 8-byte blocks
+    assert cb(NULL, NULL, NULL, 0, 10, 16, 8, 128, NULL, NULL) == pkv.OK
+    # pkv_paged_attention(q, kc, vc, bt, max_blocks, cu, lens, B, rows, Hq, Hkv, D, bs, NB, maxctx, scale, out,
+    #                     ws, ws_bytes, workers, err, stream)
+    pa = lib.pkv_paged_attention
+    att = [FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 5, 16, 8, 128, 16, 10, 64, 0.1, FAKE, FAKE, 1 << 30, 0, NULL,
+           NULL]
+    bad = list(att); bad[5] = NULL
+    assert pa(*bad) == pkv.EINVAL                                                                       # no offsets
+    bad = list(att); bad[18] = 64
+    assert pa(*bad) == pkv.EWORKSPACE
+    bad = list(att); bad[8] = pkv.MAX_SEQS + 1
+    assert pa(*bad) == pkv.EUNSUPPORTED
+    bad = list(att); bad[8] = 0
+    assert pa(*bad) == pkv.OK                                                                           # no rows
+
+
+def test_attention_workspace_holds_the_rows(lib):
+    f, g = lib.pkv_paged_attention_workspace_size, lib.pkv_paged_decode_workspace_size
+    for rows in (1, 7, 256, 4096):
+        assert f(rows, 16, 8, 128) >= g(rows, 16, 8, 128) + 2 * 4 * rows
+    assert f(-1, 16, 8, 128) == 0 and f(4, 16, 6, 128) == 0
