@@ -287,9 +287,9 @@ def run_pkv(args):
             outm = torch.empty_like(qm)
             wsm = pkv.alloc_attention_workspace(B * nq, Hq, Hkv, D, dev)
 
-            def att():
-                pkv.paged_attention(qm, lay0.k_cache, lay0.v_cache, wl.block_tables, cu, wl.context_lens, wl.scale,
-                                    outm, wsm, max_context_len=max_ctx, err_word=err, stream=stream)
+            def att():  # every sequence has nq new tokens: their queries share one pass over its keys
+                pkv.paged_attention(qm, lay0.k_cache, lay0.v_cache, wl.block_tables, None, wl.context_lens, wl.scale,
+                                    outm, wsm, max_context_len=max_ctx, err_word=err, stream=stream, new_per_seq=nq)
             for _ in range(5):
                 att()
             torch.cuda.synchronize()
@@ -304,12 +304,14 @@ def run_pkv(args):
             row = Hkv * D * 2 * 2
             unique = int(lens_h.sum()) * row
             streamed = int(sum(L - nq + 1 + i for L in lens_h for i in range(nq))) * row
-            mixed = {"kernel": "pkv_paged_attention (expand_rows_kernel + paged_decode_kernel, one row per query)",
+            mixed = {"kernel": "pkv_paged_attention (paged_decode_kernel, the 4 queries of a sequence as 4 x G "
+                               "virtual heads over one pass of its keys)",
                      "query_rows": B * nq, "new_tokens_per_sequence": nq, "mean_call_us": round(us_m, 2),
                      "unique_kv_bytes": unique, "streamed_kv_bytes": streamed,
                      "unique_gbs": round(unique / (us_m * 1e-6) / 1e9, 1),
                      "streamed_gbs": round(streamed / (us_m * 1e-6) / 1e9, 1),
-                     "note": "each query row streams its own keys; L2 catches part of the re-reads"}
+                     "note": "K/V read once per sequence; streamed_* counts one pass per query row, for comparison "
+                             "with running the rows separately"}
 
     # ---- copy-on-write block copies (pkv_copy_blocks) on this workload's pool: owned blocks copied
     # into blocks no sequence holds, as many pairs as there are such blocks (up to 256)

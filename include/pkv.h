@@ -288,12 +288,19 @@ PKV_API pkv_status pkv_paged_decode_noalloc(const uint16_t *q, const uint16_t *k
  *                 new ones included
  *   workspace     pkv_paged_attention_workspace_size(num_rows, ...) bytes,
  *                 zero-filled before first use (as pkv_paged_decode's)
+ *   new_per_seq   0: the offsets cu_seqlens_q say how many new tokens each
+ *                 sequence has.  n > 0: every sequence has exactly n
+ *                 (rows b * n .. b * n + n - 1, num_rows = num_seqs * n;
+ *                 cu_seqlens_q may be NULL) -- a speculative-decoding verify
+ *                 step, say.  Then, when n * (num_q_heads / num_kv_heads) <= 8,
+ *                 the n queries of a sequence share one pass over its keys:
+ *                 each K/V row is read once for all of them.
  * Rows inconsistent with the offsets (n > L, rows outside every sequence's
  * range) give zeros and PKV_ERR_CONTEXT_RANGE.  num_rows <= PKV_MAX_SEQS;
- * other limits, num_workers and errors as pkv_paged_decode.  Each query row
- * streams its own keys (the decode kernel, one row per query): right for
- * mixed batches with short runs of new tokens; a long prefill re-reads its
- * prefix once per query row.
+ * other limits, num_workers and errors as pkv_paged_decode.  Otherwise each
+ * query row streams its own keys (the decode kernel, one row per query):
+ * right for mixed batches with short runs of new tokens; a long prefill
+ * re-reads its prefix once per query row.
  */
 PKV_API size_t pkv_paged_attention_workspace_size(int32_t num_rows, int32_t num_q_heads,
                                                   int32_t num_kv_heads, int32_t head_dim);
@@ -303,8 +310,9 @@ PKV_API pkv_status pkv_paged_attention(const uint16_t *q, const uint16_t *k_cach
                                        int32_t num_seqs, int32_t num_rows, int32_t num_q_heads,
                                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                        int32_t num_blocks, int32_t max_context_len, float scale,
-                                       uint16_t *out, void *workspace, size_t workspace_bytes,
-                                       int32_t num_workers, int32_t *err_word, pkv_stream_t stream);
+                                       uint16_t *out, int32_t new_per_seq, void *workspace,
+                                       size_t workspace_bytes, int32_t num_workers, int32_t *err_word,
+                                       pkv_stream_t stream);
 
 /*
  * E4M3 (fp8) KV cache.  The mini-vLLM README lists "no FP8 KV" among its gaps

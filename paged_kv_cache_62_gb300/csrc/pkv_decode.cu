@@ -15,8 +15,11 @@ extern "C" size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_
 }
 
 // Shared by the bf16 and the E4M3 entry points (k_scale / v_scale: the
-// latter's per-kv-head scales, device arrays).
-static pkv_status decode_call(bool fp8, const uint16_t *q, const void *k_cache, const void *v_cache,
+// latter's per-kv-head scales, device arrays).  qn > 1: every sequence has qn
+// new tokens whose queries (rows b * qn + i of q / out) share the sequence's
+// K/V stream as qn * G virtual heads of a kv head; context_lens are then the
+// sequences' whole lengths.
+static pkv_status decode_call(bool fp8, int32_t qn, const uint16_t *q, const void *k_cache, const void *v_cache,
                               const float *k_scale, const float *v_scale, const int32_t *row_seq,
                               const int32_t *block_tables,
                               int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
@@ -31,7 +34,9 @@ static pkv_status decode_call(bool fp8, const uint16_t *q, const void *k_cache, 
         return PKV_EINVAL;
     if (num_seqs > PKV_MAX_SEQS) return PKV_EUNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return PKV_EUNSUPPORTED;
-    const int G = num_q_heads / num_kv_heads;
+    if (qn < 1) return PKV_EINVAL;
+    const int gq = num_q_heads / num_kv_heads;  // query heads per kv head
+    const int G = gq * qn;                      // virtual heads per kv head sharing one K/V stream
     if (G > 8) return PKV_EUNSUPPORTED;
     if (!is_pow2(block_size) || block_size < 8 || block_size > 1024) return PKV_EUNSUPPORTED;
     if (int64_t(num_blocks) * block_size > INT32_MAX) return PKV_EUNSUPPORTED;
@@ -83,6 +88,8 @@ static pkv_status decode_call(bool fp8, const uint16_t *q, const void *k_cache, 
     p.k_scale = k_scale;
     p.v_scale = v_scale;
     p.row_seq = row_seq;
+    p.qn = qn;
+    p.gq = gq;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
     a.device = dev.device;
@@ -105,7 +112,7 @@ extern "C" pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cach
                                        void *workspace, size_t workspace_bytes, int32_t num_workers,
                                        int32_t *err_word, pkv_stream_t stream)
 {
-    return decode_call(false, q, k_cache, v_cache, nullptr, nullptr, nullptr, block_tables, max_blocks_per_seq,
+    return decode_call(false, 1, q, k_cache, v_cache, nullptr, nullptr, nullptr, block_tables, max_blocks_per_seq,
                        context_lens,
                        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale,
                        out, workspace, workspace_bytes, num_workers, err_word, stream);
@@ -120,7 +127,7 @@ extern "C" pkv_status pkv_paged_decode_fp8(const uint16_t *q, const uint8_t *k_c
                                            size_t workspace_bytes, int32_t num_workers, int32_t *err_word,
                                            pkv_stream_t stream)
 {
-    return decode_call(true, q, k_cache, v_cache, k_scale, v_scale, nullptr, block_tables, max_blocks_per_seq,
+    return decode_call(true, 1, q, k_cache, v_cache, k_scale, v_scale, nullptr, block_tables, max_blocks_per_seq,
                        context_lens,
                        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale,
                        out, workspace, workspace_bytes, num_workers, err_word, stream);
@@ -206,25 +213,36 @@ namespace pkv {
 // offsets are inconsistent; such rows (not inside their sequence's range,
 // n > L, offsets not starting at 0) get length 0 (zero output) and
 // PKV_ERR_CONTEXT_RANGE.
-__global__ void expand_rows_kernel(const int32_t *__restrict__ cu_seqlens_q, const int32_t *__restrict__ context_lens,
-                                   int32_t num_seqs, int32_t num_rows, int32_t *__restrict__ row_seq,
-                                   int32_t *__restrict__ row_len, int32_t *err)
+// With cu_seqlens_q null, every sequence has new_per_seq rows (row r belongs to
+// sequence r / new_per_seq).
+__global__ void expand_rows_kernel(const int32_t *__restrict__ cu_seqlens_q, int32_t new_per_seq,
+                                   const int32_t *__restrict__ context_lens, int32_t num_seqs, int32_t num_rows,
+                                   int32_t *__restrict__ row_seq, int32_t *__restrict__ row_len, int32_t *err)
 {
     griddep_launch_dependents();
     griddep_wait();
     const int32_t r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= num_rows) return;
-    int32_t lo = 0, hi = num_seqs;  // the last b with cu_seqlens_q[b] <= r
-    while (hi - lo > 1) {
-        const int32_t mid = (lo + hi) >> 1;
-        if (__ldg(cu_seqlens_q + mid) <= r)
-            lo = mid;
-        else
-            hi = mid;
+    int32_t lo = 0, r0 = 0, r1 = 0;
+    if (cu_seqlens_q) {
+        int32_t hi = num_seqs;  // the last b with cu_seqlens_q[b] <= r
+        while (hi - lo > 1) {
+            const int32_t mid = (lo + hi) >> 1;
+            if (__ldg(cu_seqlens_q + mid) <= r)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        r0 = __ldg(cu_seqlens_q + lo);
+        r1 = __ldg(cu_seqlens_q + lo + 1);
+    } else {
+        lo = min(r / new_per_seq, num_seqs - 1);
+        r0 = lo * new_per_seq;
+        r1 = r0 + new_per_seq;
     }
-    const int32_t r0 = __ldg(cu_seqlens_q + lo), r1 = __ldg(cu_seqlens_q + lo + 1), L = __ldg(context_lens + lo);
+    const int32_t L = __ldg(context_lens + lo);
     const int32_t n = r1 - r0;
-    const bool ok = __ldg(cu_seqlens_q) == 0 && r0 <= r && r < r1 && n <= L;
+    const bool ok = (!cu_seqlens_q || __ldg(cu_seqlens_q) == 0) && r0 <= r && r < r1 && n <= L;
     if (!ok) flag_error(err, PKV_ERR_CONTEXT_RANGE);
     row_seq[r] = lo;
     row_len[r] = ok ? L - n + (r - r0) + 1 : 0;
@@ -239,7 +257,11 @@ extern "C" size_t pkv_paged_attention_workspace_size(int32_t num_rows, int32_t n
 {
     const size_t base = pkv_paged_decode_workspace_size(num_rows, num_q_heads, num_kv_heads, head_dim);
     if (base == 0) return 0;
-    return align256(base) + 2 * rows_bytes(num_rows);
+    size_t need = align256(base) + 2 * rows_bytes(num_rows);  // one row per query
+    // queries sharing a stream: qn * G virtual heads over at most num_rows / qn sequences
+    for (int32_t qn = 2; (num_q_heads / num_kv_heads) * qn <= 8; ++qn)
+        need = std::max(need, pkv_paged_decode_workspace_size(num_rows, num_q_heads * qn, num_kv_heads, head_dim));
+    return need;
 }
 
 extern "C" pkv_status pkv_paged_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
@@ -247,31 +269,39 @@ extern "C" pkv_status pkv_paged_attention(const uint16_t *q, const uint16_t *k_c
                                           const int32_t *cu_seqlens_q, const int32_t *context_lens, int32_t num_seqs,
                                           int32_t num_rows, int32_t num_q_heads, int32_t num_kv_heads,
                                           int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                                          int32_t max_context_len, float scale, uint16_t *out, void *workspace,
-                                          size_t workspace_bytes, int32_t num_workers, int32_t *err_word,
-                                          pkv_stream_t stream)
+                                          int32_t max_context_len, float scale, uint16_t *out, int32_t new_per_seq,
+                                          void *workspace, size_t workspace_bytes, int32_t num_workers,
+                                          int32_t *err_word, pkv_stream_t stream)
 {
-    if (num_seqs < 0 || num_rows < 0) return PKV_EINVAL;
+    if (num_seqs < 0 || num_rows < 0 || new_per_seq < 0) return PKV_EINVAL;
     if (num_rows == 0) return PKV_OK;
-    if (num_seqs == 0 || !cu_seqlens_q || !context_lens) return PKV_EINVAL;
+    if (num_seqs == 0 || !context_lens || (new_per_seq == 0 && !cu_seqlens_q)) return PKV_EINVAL;
+    if (new_per_seq > 0 && int64_t(num_seqs) * new_per_seq != num_rows) return PKV_EINVAL;
+    if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0) return PKV_EINVAL;
     const size_t need = pkv_paged_attention_workspace_size(num_rows, num_q_heads, num_kv_heads, head_dim);
     if (need == 0) return num_rows > PKV_MAX_SEQS ? PKV_EUNSUPPORTED : PKV_EINVAL;
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PKV_EWORKSPACE;
+    if (new_per_seq > 1 && (num_q_heads / num_kv_heads) * new_per_seq <= 8)
+        // the n new tokens of a sequence share its K/V stream: read once, n * G virtual heads
+        return decode_call(false, new_per_seq, q, k_cache, v_cache, nullptr, nullptr, nullptr, block_tables,
+                           max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                           block_size, num_blocks, max_context_len, scale, out, workspace, workspace_bytes,
+                           num_workers, err_word, stream);
     // the rows' (sequence, length) arrays sit after the decode workspace
     uint8_t *wsb = static_cast<uint8_t *>(workspace);
     const size_t dec_bytes = align256(pkv_paged_decode_workspace_size(num_rows, num_q_heads, num_kv_heads, head_dim));
     int32_t *row_seq = reinterpret_cast<int32_t *>(wsb + dec_bytes);
     int32_t *row_len = reinterpret_cast<int32_t *>(wsb + dec_bytes + rows_bytes(num_rows));
     const cudaError_t e = launch_pdl(expand_rows_kernel, dim3((num_rows + 255) / 256), dim3(256), 0,
-                                     reinterpret_cast<cudaStream_t>(stream), cu_seqlens_q, context_lens, num_seqs,
-                                     num_rows, row_seq, row_len, err_word);
+                                     reinterpret_cast<cudaStream_t>(stream), new_per_seq > 0 ? nullptr : cu_seqlens_q,
+                                     new_per_seq, context_lens, num_seqs, num_rows, row_seq, row_len, err_word);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return cuda_fail("expand_rows_kernel launch", e);
     }
     const pkv_status st = launch_status("expand_rows_kernel launch");
     if (st != PKV_OK) return st;
-    return decode_call(false, q, k_cache, v_cache, nullptr, nullptr, row_seq, block_tables, max_blocks_per_seq,
+    return decode_call(false, 1, q, k_cache, v_cache, nullptr, nullptr, row_seq, block_tables, max_blocks_per_seq,
                        row_len, num_rows, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                        max_context_len, scale, out, workspace, dec_bytes, num_workers, err_word, stream);
 }

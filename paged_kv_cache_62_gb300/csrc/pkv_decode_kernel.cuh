@@ -109,6 +109,10 @@ struct DecodeParams {
     const float *k_scale, *v_scale;  // E4M3 caches: per-kv-head scales (unused for bf16 caches)
     const int32_t *row_seq;          // several query rows per sequence: row -> the sequence whose table it
                                      // reads (null: row b reads table row b)
+    // Several new tokens per sequence sharing one K/V stream: the kernel's G "heads" of a kv head are
+    // qn queries x gq query heads (virtual head hh = query hh / gq, head hh % gq); query i of sequence b
+    // is q / out row b * qn + i and sees the keys before position L - qn + i + 1.  Decode: qn = 1, gq = G.
+    int32_t qn, gq;
 };
 
 // What the producer tells the consumers about the unit in a stage.
@@ -352,7 +356,7 @@ __device__ __forceinline__ void load8(const uint8_t *base, int e, float2 f[4])
 template <int D, int G, bool FP8>
 __device__ __forceinline__ void attend_tile(const uint8_t *Ks, const uint8_t *Vs, int stride, int valid,
                                             const float2 (&q2)[G][4], float (&m)[G], float (&l)[G],
-                                            float2 (&acc)[G][4], int c, int grp)
+                                            float2 (&acc)[G][4], int c, int grp, int rem, int qtail, int gq)
 {
     using S = Shape<D, G>;
     constexpr int LPT = S::LPT, TPI = S::TPI, NIT = S::NIT, DUP = S::DUP;
@@ -397,10 +401,13 @@ __device__ __forceinline__ void attend_tile(const uint8_t *Ks, const uint8_t *Vs
     float pr[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-        const float s = ok ? part[h][0] : -INFINITY;
+        // several queries per stream: query h / gq sees qtail - h / gq fewer of the sequence's last
+        // tokens (rem: tokens of the sequence from this tile's first on, not clamped to the tile)
+        const bool okh = qtail > 0 ? tok_s < min(valid, rem - (qtail - h / gq)) : ok;
+        const float s = okh ? part[h][0] : -INFINITY;
         // Online softmax (m, l, acc).  The running max only moves when some
-        // score passes it by more than the slack; the first tile always moves it
-        // (m = -inf, and every tile holds at least one valid token).
+        // score passes it by more than the slack; the first tile with a valid token
+        // for the head always moves it (m = -inf before it).
         if (__any_sync(kFull, s > m[h] + kRescaleSlack)) {
             const float mn = fmaxf(m[h], warp_max(s));
             const float alpha = ex2(m[h] - mn);  // 0 on the first tile
@@ -410,7 +417,7 @@ __device__ __forceinline__ void attend_tile(const uint8_t *Ks, const uint8_t *Vs
             for (int j = 0; j < 4; ++j) acc[h][j] = __fmul2_rn(acc[h][j], a2);
             m[h] = mn;
         }
-        pr[h] = ok ? ex2(s - m[h]) : 0.f;
+        pr[h] = okh ? ex2(s - m[h]) : 0.f;
         l[h] += pr[h];
     }
     // P.V: the weight of token i*TPI + grp sits in lane grp*LPT + i*DUP
@@ -714,13 +721,15 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
 #pragma unroll
             for (int k = 0; k < BATCH; ++k)
                 if (use[k]) mb = fmaxf(mb, st[k][hh].x);
-            const float r = ex2(M[hh] - mb);  // 0 while nothing has been folded in (M = -inf)
+            // 0 while nothing has been folded in (M = -inf); a head with no valid token in any piece
+            // so far (several queries per stream) keeps its zero state
+            const float r = mb == -INFINITY ? 1.0f : ex2(M[hh] - mb);
             lsum[hh] *= r;
 #pragma unroll
             for (int e = 0; e < PER; ++e) a[hh][e] *= r;
 #pragma unroll
             for (int k = 0; k < BATCH; ++k) {
-                const float f = use[k] ? ex2(st[k][hh].x - mb) : 0.f;
+                const float f = (use[k] && st[k][hh].x != -INFINITY) ? ex2(st[k][hh].x - mb) : 0.f;
                 lsum[hh] = fmaf(f, st[k][hh].y, lsum[hh]);
                 const float *x = reinterpret_cast<const float *>(&v[k][hh]);
 #pragma unroll
@@ -732,7 +741,8 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
         const float inv = (FP8 ? __ldg(p.v_scale + kvh) : 1.0f) / lsum[hh];
-        uint16_t *o = p.out + (int64_t(b) * p.Hq + int64_t(kvh) * G + hh) * D + lane * PER;
+        uint16_t *o = p.out + ((int64_t(b) * p.qn + hh / p.gq) * p.Hq + int64_t(kvh) * p.gq + hh % p.gq) * D +
+                      lane * PER;
         if constexpr (PER == 4)
             *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16x2(a[hh][0] * inv, a[hh][1] * inv),
                                                        pack_bf16x2(a[hh][2] * inv, a[hh][3] * inv));
@@ -910,11 +920,26 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                         dead = true;
                         break;
                     }
-                    if (lane == 0) {
-                        const uint32_t qb = uint32_t(p.hg * G * D * 2);
-                        mbar_arrive_expect_tx(&qfull[qs], qb);
-                        bulk_load(qbuf + qs * lay.q_bytes,
-                                  p.q + ((long long)iw.b * p.Hq + (long long)iw.g * p.hg * G) * D, qb, &qfull[qs]);
+                    const uint32_t qb = uint32_t(p.hg * G * D * 2);
+                    if (p.qn == 1) {  // the group's G * hg query rows are contiguous
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(&qfull[qs], qb);
+                            bulk_load(qbuf + qs * lay.q_bytes,
+                                      p.q + ((long long)iw.b * p.Hq + (long long)iw.g * p.hg * G) * D, qb,
+                                      &qfull[qs]);
+                        }
+                    } else {
+                        // qn queries: kv head h's virtual heads i * gq .. i * gq + gq - 1 come from row
+                        // b * qn + i; one copy of gq rows per (h, i), lane t copying pair t
+                        if (lane == 0) mbar_arrive_expect_tx(&qfull[qs], qb);
+                        __syncwarp();
+                        for (int t = lane; t < p.hg * p.qn; t += 32) {
+                            const int hh = t / p.qn, qi = t - hh * p.qn;
+                            bulk_load(qbuf + qs * lay.q_bytes + size_t((hh * G + qi * p.gq) * D) * 2,
+                                      p.q + (((long long)iw.b * p.qn + qi) * p.Hq +
+                                             (long long)(iw.g * p.hg + hh) * p.gq) * D,
+                                      uint32_t(p.gq * D * 2), &qfull[qs]);
+                        }
                     }
                     ++segs;
                 }
@@ -1029,7 +1054,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         if (valid > 0) {
             const int e0 = (j * TW * p.hg + h) * D;  // element offset of this warp's first row in the stage
             attend_tile<D, G, FP8>(st + e0 * ES, st + lay.kv_bytes + e0 * ES, stride, valid, q2, m, l, acc, c,
-                                   grp);
+                                   grp, mt.L - tok0, p.qn - 1, p.gq);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -1083,9 +1108,12 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                     const float *others = comb + h * (p.sub - 1) * cst;
 #pragma unroll
                     for (int hh = 0; hh < G; ++hh) {
-                        float M = m[hh];  // finite: the leader's slice starts every unit it saw
+                        float M = m[hh];
                         for (int jj = 0; jj < p.sub - 1; ++jj) M = fmaxf(M, others[jj * cst + G * D + hh]);
-                        const float f0 = ex2(m[hh] - M);
+                        // M = -inf only when no slice saw a valid token for this head (several queries
+                        // per stream, a piece past the query's last key): the state stays zero
+                        const bool none = M == -INFINITY;
+                        const float f0 = none ? 0.f : ex2(m[hh] - M);
                         float ls = f0 * lt[hh];
                         const float2 f02 = make_float2(f0, f0);
                         float2 a[4];
@@ -1093,7 +1121,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                         for (int e = 0; e < 4; ++e) a[e] = __fmul2_rn(acc[hh][e], f02);
                         for (int jj = 0; jj < p.sub - 1; ++jj) {
                             const float *st2 = others + jj * cst;
-                            const float f = ex2(st2[G * D + hh] - M);  // 0 for a slice with no tokens
+                            const float f = none ? 0.f : ex2(st2[G * D + hh] - M);  // 0 for a slice with no tokens
                             ls = fmaf(f, st2[G * D + G + hh], ls);
                             const float4 x0 = *reinterpret_cast<const float4 *>(st2 + hh * D + c * 8);
                             const float4 x1 = *reinterpret_cast<const float4 *>(st2 + hh * D + c * 8 + 4);
@@ -1124,8 +1152,9 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                             o.y = pack_bf16x2(acc[hh][1].x * inv, acc[hh][1].y * inv);
                             o.z = pack_bf16x2(acc[hh][2].x * inv, acc[hh][2].y * inv);
                             o.w = pack_bf16x2(acc[hh][3].x * inv, acc[hh][3].y * inv);
-                            *reinterpret_cast<uint4 *>(p.out + ((long long)mt.b * p.Hq + (long long)kvh * G + hh) * D +
-                                                       c * 8) = o;
+                            *reinterpret_cast<uint4 *>(
+                                p.out + (((long long)mt.b * p.qn + hh / p.gq) * p.Hq + (long long)kvh * p.gq + hh % p.gq) * D +
+                                c * 8) = o;
                         }
                 } else {
                     const long long sigma = (long long)mt.b * p.nhg + mt.g;

@@ -36,7 +36,7 @@ SIGNATURES = {
     "pkv_copy_blocks": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P]),
     "pkv_paged_attention_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "pkv_paged_attention": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
-                                           _I32, _F32, _P, _P, _SZ, _I32, _P, _P]),
+                                           _I32, _F32, _P, _I32, _P, _SZ, _I32, _P, _P]),
     "pkv_decode_store": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P]),
     "pkv_kv_store_fp8": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]),
     "pkv_paged_decode_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
@@ -331,22 +331,25 @@ def alloc_attention_workspace(num_rows: int, num_q_heads: int, num_kv_heads: int
 
 
 def paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
-                    cu_seqlens_q: torch.Tensor, context_lens: torch.Tensor, scale: float, out: torch.Tensor,
+                    cu_seqlens_q: torch.Tensor | None, context_lens: torch.Tensor, scale: float, out: torch.Tensor,
                     workspace: torch.Tensor, max_context_len: int | None = None, num_workers: int = 0,
-                    err_word: torch.Tensor | None = None, stream=None) -> None:
-    """Causal paged attention of each sequence's new tokens (rows cu_seqlens_q[b]..cu_seqlens_q[b+1]) over
-    its context_lens[b] cached tokens."""
+                    err_word: torch.Tensor | None = None, stream=None, new_per_seq: int = 0) -> None:
+    """Causal paged attention of each sequence's new tokens (rows cu_seqlens_q[b]..cu_seqlens_q[b+1], or
+    b*n..b*n+n-1 with new_per_seq = n) over its context_lens[b] cached tokens."""
     T, Hq, D = q.shape
     NB, bs, Hkv, D2 = k_cache.shape
     B = context_lens.numel()
-    if D2 != D or v_cache.shape != k_cache.shape or block_tables.shape[0] != B or cu_seqlens_q.numel() != B + 1 \
-            or out.shape != q.shape:
+    if D2 != D or v_cache.shape != k_cache.shape or block_tables.shape[0] != B or out.shape != q.shape \
+            or (cu_seqlens_q is None and new_per_seq <= 0) \
+            or (cu_seqlens_q is not None and cu_seqlens_q.numel() != B + 1):
         raise ValueError("paged_attention: shape mismatch")
+    cu = None if cu_seqlens_q is None else _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q")
     mx = int(block_tables.shape[1]) * bs if max_context_len is None else int(max_context_len)
     _check(load().pkv_paged_attention(
         _dev(q, torch.bfloat16, "q", 3), _dev(k_cache, torch.bfloat16, "k_cache", 4),
         _dev(v_cache, torch.bfloat16, "v_cache", 4), _dev(block_tables, torch.int32, "block_tables", 2),
-        block_tables.shape[1], _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q"),
+        block_tables.shape[1], cu,
         _dev(context_lens, torch.int32, "context_lens"), B, T, Hq, Hkv, D, bs, NB, mx, float(scale),
-        _dev(out, torch.bfloat16, "out", 3), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _dev(out, torch.bfloat16, "out", 3), int(new_per_seq), _dev(workspace, torch.uint8, "workspace"),
+        workspace.numel(),
         int(num_workers), _opt(err_word), _stream(stream)), "pkv_paged_attention")

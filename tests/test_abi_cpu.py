@@ -163,12 +163,14 @@ def test_newer_entry_points_validate_on_the_host(lib):
     # pkv_paged_attention(q, kc, vc, bt, max_blocks, cu, lens, B, rows, Hq, Hkv, D, bs, NB, maxctx, scale, out,
     #                     ws, ws_bytes, workers, err, stream)
     pa = lib.pkv_paged_attention
-    att = [FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 5, 16, 8, 128, 16, 10, 64, 0.1, FAKE, FAKE, 1 << 30, 0, NULL,
-           NULL]
+    att = [FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 5, 16, 8, 128, 16, 10, 64, 0.1, FAKE, 0, FAKE, 1 << 30, 0,
+           NULL, NULL]
     bad = list(att); bad[5] = NULL
     assert pa(*bad) == pkv.EINVAL                                                                       # no offsets
-    bad = list(att); bad[18] = 64
+    bad = list(att); bad[19] = 64
     assert pa(*bad) == pkv.EWORKSPACE
+    bad = list(att); bad[17] = 3                                                                        # 2 * 3 != 5 rows
+    assert pa(*bad) == pkv.EINVAL
     bad = list(att); bad[8] = pkv.MAX_SEQS + 1
     assert pa(*bad) == pkv.EUNSUPPORTED
     bad = list(att); bad[8] = 0

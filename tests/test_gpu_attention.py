@@ -112,3 +112,28 @@ def test_inconsistent_offsets_give_zeros_and_an_error():
     torch.cuda.synchronize()
     assert err.item() & pkv.ERR_CONTEXT_RANGE
     assert torch.all(out[5:].float() == 0)
+
+
+@pytest.mark.parametrize("n,Hq,Hkv,D,bs,workers", [(2, 16, 8, 128, 16, 0), (3, 16, 8, 128, 256, 0),
+                                                   (4, 16, 8, 128, 16, 0), (4, 16, 8, 128, 8, 333),
+                                                   (8, 4, 4, 64, 16, 0), (4, 14, 2, 64, 16, 1),
+                                                   (5, 16, 8, 128, 16, 0)])
+def test_uniform_new_tokens_share_one_pass(n, Hq, Hkv, D, bs, workers):
+    """Every sequence with n new tokens (new_per_seq = n): when n * G <= 8 the n queries are n * G virtual
+    heads of a kv head over one pass of its keys, each with its own causal bound -- including pieces of a
+    split where some virtual head sees no key at all; otherwise the rows run one by one."""
+    rng = np.random.default_rng(n * 100 + Hq + bs)
+    lens = rng.integers(n, 1500, size=12).tolist() + [n, n + 1, 16 + n - 1]
+    news = [n] * len(lens)
+    q, kc, vc, bt, cu, lens_t = mixed_batch(lens, news, Hq, Hkv, D, bs, seed=n + D)
+    want = oracle_of(q, kc, vc, bt, cu, lens_t, 0.0884)
+    T = q.shape[0]
+    ws = pkv.alloc_attention_workspace(T, Hq, Hkv, D)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for call in range(2):
+        out = torch.full_like(q, float("nan"))
+        pkv.paged_attention(q, kc, vc, bt, None, lens_t, 0.0884, out, ws, num_workers=workers, err_word=err,
+                            new_per_seq=n)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        check_close(out, want, f"n {n} call {call}")
