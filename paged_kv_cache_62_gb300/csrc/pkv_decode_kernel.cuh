@@ -85,8 +85,9 @@ struct BalanceState {
     uint32_t tag[2][kMaxSlots];           // (call number of the writer) ^ kTableMagic
     unsigned long long claim[kMaxSlots];  // (gen << 32) | 1 once a CTA took the slice this call
     // Control block.  Call number e of a workspace runs with gen = e + 1 (never 0, the value
-    // of zero-filled tags).  The last CTA of call e leaves epoch = e + 1, stamp =
-    // (e + 1) ^ kEpochMagic, done = 0; a zero-filled workspace reads as call 0.
+    // of zero-filled tags).  `done` counts the CTAs of the call that have read the block; the
+    // one that completes the count leaves epoch = e + 1, stamp = (e + 1) ^ kEpochMagic,
+    // done = 0.  A zero-filled workspace reads as call 0.
     uint32_t epoch, stamp, done, pad;
 };
 
@@ -751,21 +752,6 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
     }
 }
 
-// Warp-collective, the last thing every warp of the CTA does: count the warp
-// out on a shared counter; the CTA's last warp counts the CTA out of the call,
-// and the call's last CTA (every other CTA has finished, so has read the
-// control block) leaves it ready for the next call.
-__device__ __forceinline__ void warp_exit(const DecodeParams &p, uint32_t epoch, int *ctas_warps_done, int nwarps)
-{
-    __syncwarp();
-    if ((threadIdx.x & 31) != 0) return;
-    if (atomicAdd(ctas_warps_done, 1) != nwarps - 1) return;
-    if (atomicAdd(&p.ws_bal->done, 1u) != gridDim.x - 1) return;
-    p.ws_bal->done = 0u;
-    p.ws_bal->epoch = epoch + 1u;
-    p.ws_bal->stamp = (epoch + 1u) ^ kEpochMagic;
-}
-
 // ------------------------------------------------------------------ main kernel
 // Block: p.cons consumer warps (warp w: kv head w / sub of the group, TW-token
 // slice w % sub of every unit) and one producer warp (warp p.cons).
@@ -794,7 +780,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     long long *bound = reinterpret_cast<long long *>(smem + lay.off_bound);
     float *wts = reinterpret_cast<float *>(smem + lay.off_wts);
     float *red = reinterpret_cast<float *>(smem + lay.off_red);
-    int *sh = reinterpret_cast<int *>(smem + lay.off_sh);  // [0] own slice, [2..3] its start time, [6] warps done
+    int *sh = reinterpret_cast<int *>(smem + lay.off_sh);  // [0] own slice, [2..3] its start time
     int32_t *scan = reinterpret_cast<int32_t *>(smem + lay.off_scan);
 
     if (threadIdx.x == 0) {
@@ -852,7 +838,6 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         else if (uint32_t(home_word >> 32) != gen)
             home = int(my_sm);
         sh[0] = home;
-        sh[6] = 0;
     }
     __syncthreads();
 
@@ -995,7 +980,18 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         // let every copy this warp started land before the CTA can retire
         for (uint32_t i = kk > uint32_t(p.nst) ? kk - uint32_t(p.nst) : 0u; i < kk; ++i)
             mbar_wait_bounded(&full[i % uint32_t(p.nst)], (i / uint32_t(p.nst)) & 1u);
-        warp_exit(p, epoch, sh + 6, p.cons + 1);
+        // Count this CTA in: every thread of it read the control block long ago (the fence orders
+        // those reads before the count).  The CTA that completes the count leaves the block ready
+        // for the next call.  This is the producer's last act, while the consumers still work
+        // through the stages in flight, so the round trip is off the kernel's critical path.
+        if (lane == 0) {
+            __threadfence();
+            if (atomicAdd(&p.ws_bal->done, 1u) == gridDim.x - 1) {
+                p.ws_bal->done = 0u;
+                p.ws_bal->epoch = epoch + 1u;
+                p.ws_bal->stamp = (epoch + 1u) ^ kEpochMagic;
+            }
+        }
         return;
     }
 
@@ -1198,7 +1194,6 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
             p.ws_bal->tag[wp][mt.slice] = gen ^ kTableMagic;
         }
     }
-    warp_exit(p, epoch, sh + 6, p.cons + 1);
 }
 
 // ------------------------------------------------------------------ host side
