@@ -436,9 +436,10 @@ def run_pkv(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "f32",  # the arithmetic (fp32 products and sums); K/V, q and out are stored as bf16
         "data": "synthetic (seeded N(0,1) bf16 K/V/q, shuffled block pool, NaN canaries in unowned rows)",
-        "config": {"workload": f"{args.workload}: {s.description}", "layers": s.layers, "batch_per_gpu": B,
+        "config": {"workload": f"{args.workload}: {s.description}", "storage": "bf16", "layers": s.layers,
+                   "batch_per_gpu": B,
                    "q_heads": Hq, "kv_heads": Hkv, "head_dim": D, "block_size": s.block_size,
                    "mean_context_len": float(wl.lens_host().mean()), "parallelism": f"replicas x{ws}",
                    "l2": f"inputs larger than L2 (KV pool {2 * wl.layers[0].k_cache.numel() * 2 / 2**20:.0f} MiB"
