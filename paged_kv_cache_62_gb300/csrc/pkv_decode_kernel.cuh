@@ -61,16 +61,12 @@ constexpr uint32_t kTableMagic = 0x62616c31u;
 constexpr uint32_t kEpochMagic = 0x65706f63u;
 
 // Consumer warps per CTA and tokens each takes from a stage (a stage holds
-// team_warps * warp_tokens token rows of head_dim, 64 KiB for head_dim 128).
-// Measured on the Qwen3-0.6B-shaped batch: 8 warps x 16 tokens with three
-// 64 KiB stages beats 16 warps x 8 tokens (17 warps leave 96 registers a
-// thread, and the G = 2 loop spills) and 8 warps x 8 tokens with six 32 KiB
-// stages (twice the per-stage overhead per token).  Groups of 5 or more query
-// heads keep 16G accumulator and query registers a lane: with 8 consumers
-// plus the producer, three warps share an SM sub-partition's 16K registers
-// (168 a thread) and those groups spill; with 4 consumers at most two do
-// (255 a thread).
-__host__ __device__ constexpr int team_warps(int G) { return G >= 5 ? 4 : 8; }
+// team_warps * warp_tokens token rows of head_dim, 64 KiB for bf16 and
+// head_dim 128).  A warp's tile is 16 tokens, the n extent of two m16n8k16
+// score products and the k extent of one output product; a warp's registers
+// do not grow with the group size (G query heads are rows of one MMA tile),
+// so every group size runs 8 consumers.
+__host__ __device__ constexpr int team_warps(int) { return 8; }
 __host__ __device__ constexpr int warp_tokens(int) { return 16; }
 
 // ------------------------------------------------------------------ load balance state
@@ -114,6 +110,10 @@ struct DecodeParams {
     // qn queries x gq query heads (virtual head hh = query hh / gq, head hh % gq); query i of sequence b
     // is q / out row b * qn + i and sees the keys before position L - qn + i + 1.  Decode: qn = 1, gq = G.
     int32_t qn, gq;
+    // Shape of the cache tensor maps: 0 = one 4-D copy per box and cache (dims: row chunk, token, row
+    // part, kv head); 1 = one 3-D copy per box, cache, kv head and row part (dims: row chunk,
+    // kv head x part, token), where the driver does not take the 4-D map's stride order.
+    int32_t split_copies;
 };
 
 // What the producer tells the consumers about the unit in a stage.
@@ -124,16 +124,6 @@ struct alignas(16) UnitMeta {
 constexpr int kFirst = 1;     // first unit of (b, g) in this slice
 constexpr int kLast = 2;      // last unit of (b, g) in this slice
 constexpr int kSliceEnd = 4;  // last unit of the slice
-
-template <int D, int G>
-struct Shape {
-    static constexpr int TW = warp_tokens(G);  // tokens per warp tile
-    static constexpr int LPT = D / 8;          // lanes per token row (16 bytes each)
-    static constexpr int TPI = 32 / LPT;       // tokens per warp step
-    static constexpr int NIT = TW / TPI;       // steps per tile
-    static constexpr int DUP = LPT / NIT;      // lanes that end up holding each score
-    static_assert(LPT >= NIT && DUP >= 1 && NIT >= 1, "tile does not fit the lane split");
-};
 
 // Shared-memory layout, computed the same way on the host (size) and device (offsets).
 struct CtaLayout {
@@ -153,7 +143,7 @@ __host__ __device__ inline CtaLayout cta_layout(int D, int G, int es, int hg, in
     CtaLayout l;
     const int toks = warp_tokens(G) * sub;
     l.kv_bytes = uint32_t(toks * hg * D * es);
-    l.stage_bytes = align_up(2 * l.kv_bytes, 128);
+    l.stage_bytes = align_up(2 * l.kv_bytes, 1024);  // stages start on the 1024-byte swizzle period
     l.q_bytes = align_up(uint32_t(hg * G * D * 2), 128);
     // states of the non-leading warps of every head (the leader keeps its own in registers)
     l.comb_bytes = sub > 1 ? align_up(uint32_t(hg * (sub - 1) * comb_stride(D, G) * 4), 128) : 0u;
@@ -309,134 +299,191 @@ static __device__ void unit_prefix_scan(const DecodeParams &p, int32_t *scan, in
 // ------------------------------------------------------------------ one tile
 // Slack (log2 units) a score may exceed the running max before the running
 // state is rescaled: weights stay <= 2^kRescaleSlack, which fp32 holds with
-// ample room, and most tiles skip the warp max and the rescale entirely.
+// ample room, and most tiles skip the rescale entirely.
 constexpr float kRescaleSlack = 8.0f;
 
-__device__ __forceinline__ void unpack8x2(const uint4 w, float2 f[4])
+// Stage layout.  The producer copies a cached row (one token, one kv head) as
+// NP parts of RB bytes, one TMA box per (box of boxtok tokens, kv head, part),
+// so the boxtok rows of a part are consecutive RB-byte rows of shared memory,
+// swizzled by the copy: 16-byte chunk c of row R lands at chunk c ^ (R & 7)
+// (128-byte rows) or c ^ ((R >> 1) & 3) (64-byte rows, 64-dim E4M3 caches).
+// The chunks of eight consecutive tokens then sit in eight different bank
+// groups, and one ldmatrix reads them without a conflict.
+template <int D, bool FP8>
+struct Tc {
+    static constexpr int ES = FP8 ? 1 : 2;              // bytes per cached element
+    static constexpr int ROWB = D * ES;                 // bytes per cached row
+    static constexpr int RB = ROWB >= 128 ? 128 : 64;   // bytes per shared-memory row
+    static constexpr int NP = ROWB / RB;                // parts per cached row
+    static constexpr int NCP = ROWB / 32;               // 16-byte chunk pairs per row (one ldmatrix.x4 each)
+    static constexpr int KS = D / 16;                   // k-steps of the score product
+    static constexpr int MT = D / 16;                   // m-tiles of the output product
+};
+
+__host__ __device__ constexpr int row_bytes_smem(int D, int es) { return D * es >= 128 ? 128 : 64; }
+
+template <int RB>
+__device__ __forceinline__ uint32_t swizzled_chunk(uint32_t c, uint32_t R)
 {
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) f[i] = make_float2(__uint_as_float(u[i] << 16), __uint_as_float(u[i] & 0xffff0000u));
+    return RB == 128 ? (c ^ (R & 7u)) : (c ^ ((R >> 1) & 3u));
 }
 
-// Eight E4M3 codes (bytes 0..7 of w, element e in byte e) -> four fp32
-// pairs: the hardware conversion to f16 pairs (exact: every E4M3 value is a
-// normal f16 or zero), then f16 -> fp32 (exact).
-__device__ __forceinline__ void unpack8x2_e4m3(const uint2 w, float2 f[4])
+// Byte offsets, from a stage's K (or V) region, of the 16-byte row pieces this
+// lane hands to ldmatrix for the warp's 16 tokens (token j * 16 + tl of the
+// unit): tl = 8 * (lane / 16) + lane % 8, chunk 2i + (lane / 8) % 2 of the row.
+// Matrix q of an .x4 load is then (tokens 0-7 | 8-15) x (chunk 2i | 2i + 1)
+// for q = 0 (0-7, 2i), 1 (0-7, 2i+1), 2 (8-15, 2i), 3 (8-15, 2i+1).
+template <int D, bool FP8>
+__device__ __forceinline__ void lane_offsets(uint32_t (&off)[Tc<D, FP8>::NCP], int lane, int j, int h, int hg,
+                                             int boxtok)
 {
-    const uint32_t u[2] = {w.x, w.y};
+    using T = Tc<D, FP8>;
+    const int tl = ((lane >> 4) << 3) | (lane & 7), e = (lane >> 3) & 1;
+    const int t = j * 16 + tl;
+    const int lg = __ffs(boxtok) - 1;
+    const int bi = t >> lg, r = t & (boxtok - 1);
+    const uint32_t box_bytes = uint32_t(boxtok * hg * T::ROWB);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        uint32_t h0, h1;  // f16 pairs of bytes (1, 0) and (3, 2)
-        asm("{.reg .b16 lo, hi;\n\t"
-            "mov.b32 {lo, hi}, %2;\n\t"
-            "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
-            "cvt.rn.f16x2.e4m3x2 %1, hi;}"
-            : "=r"(h0), "=r"(h1) : "r"(u[i]));
-        f[2 * i] = __half22float2(*reinterpret_cast<const __half2 *>(&h0));
-        f[2 * i + 1] = __half22float2(*reinterpret_cast<const __half2 *>(&h1));
+    for (int i = 0; i < T::NCP; ++i) {
+        const int gc = 2 * i + e;
+        const int pp = gc / (T::RB / 16), cc = gc % (T::RB / 16);
+        const uint32_t R = uint32_t((h * T::NP + pp) * boxtok + r);
+        off[i] = uint32_t(bi) * box_bytes + R * T::RB + (swizzled_chunk<T::RB>(uint32_t(cc), R) << 4);
     }
 }
 
-// Eight consecutive cached elements starting at element `e` of `base` as fp32 pairs.
+// Head dim held by output fragment element (m-tile mt, half: 0 for c0/c1,
+// 1 for c2/c3) of the thread in row group g = lane / 4.  bf16 caches: the
+// transposed V tile puts dim 16 mt + g in rows g and 16 mt + 8 + g in rows
+// g + 8; E4M3 caches: dims 16 mt + 2g and 16 mt + 2g + 1 (the byte pairs of
+// a 16-bit transpose, split by a byte permute).
 template <bool FP8>
-__device__ __forceinline__ void load8(const uint8_t *base, int e, float2 f[4])
+__device__ __forceinline__ int dim_of(int mt, int half, int g)
 {
-    if constexpr (FP8)
-        unpack8x2_e4m3(*reinterpret_cast<const uint2 *>(base + e), f);
-    else
-        unpack8x2(*reinterpret_cast<const uint4 *>(base + 2 * e), f);
+    return FP8 ? 16 * mt + 2 * g + half : 16 * mt + 8 * half + g;
 }
 
-// One TW-token tile of one (sequence, kv head) for the G query heads of the
-// group: Ks / Vs point at the tile's first K / V row, consecutive tokens are
-// `stride` elements apart (bf16 values, or E4M3 codes whose kv-head scales
-// the caller has folded into q2 and the final division).  Element pairs are
-// handled with the packed fp32 FMA (two independent round-to-nearest fp32
-// FMAs per instruction).
-template <int D, int G, bool FP8>
-__device__ __forceinline__ void attend_tile(const uint8_t *Ks, const uint8_t *Vs, int stride, int valid,
-                                            const float2 (&q2)[G][4], float (&m)[G], float (&l)[G],
-                                            float2 (&acc)[G][4], int c, int grp, int rem, int qtail, int gq)
+__device__ __forceinline__ uint32_t f16x2_of(float lo, float hi)
 {
-    using S = Shape<D, G>;
-    constexpr int LPT = S::LPT, TPI = S::TPI, NIT = S::NIT, DUP = S::DUP;
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
 
-    // scores: lane (grp, c) forms the 8-element partial dot products of tokens i*TPI + grp
-    float part[G][NIT];
+// One 16-token tile of one (sequence, kv head) for its G query heads
+// (virtual heads) on the tensor cores, m16n8k16 with fp32 accumulators:
+//   S^T = Q K^T    rows: query heads (row g = lane / 4; rows G..15 are zero),
+//                  columns: 8 tokens per n-tile, k: head dims;
+//   P = 2^(S - m)  the online-softmax weights of the thread's row;
+//   O^T += V^T P^T rows: head dims, columns: query heads, k: tokens.
+// The S^T accumulator fragment of the two n-tiles is, register for register,
+// the P^T operand fragment of the second product, so P never leaves the
+// registers.  kb / vb: shared addresses of the stage's K and V regions.  lim:
+// tokens below it count for this thread's row (causal bound of its query);
+// TAIL: tokens from `valid` on are not the sequence's (their rows may hold
+// anything, even NaN), so their V values are zeroed before the product.
+// E4M3 caches run the products in f16 (every E4M3 value is exact in f16);
+// the kv head's K scale is in ksc, its V scale is applied by the caller.
+template <int D, bool FP8, bool TAIL>
+__device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb, const uint32_t (&off)[Tc<D, FP8>::NCP],
+                                            const uint32_t (&qa)[Tc<D, FP8>::KS][2], float ksc, int lim, int valid,
+                                            float &m, float &l, float (&o)[Tc<D, FP8>::MT][4], int lane)
+{
+    using T = Tc<D, FP8>;
+    const int r4 = lane & 3;
+    float sa[2][2][4];  // [chain][n-tile][fragment]: two accumulation chains halve the MMA dependency depth
 #pragma unroll
-    for (int i = 0; i < NIT; ++i) {
-        const int tok = i * TPI + grp;
-        float2 k2[4];
-        load8<FP8>(Ks, tok * stride + c * 8, k2);
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float2 a = __fmul2_rn(q2[h][0], k2[0]);
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int j = 1; j < 4; ++j) a = __ffma2_rn(q2[h][j], k2[j], a);
-            part[h][i] = a.x + a.y;
+            for (int e = 0; e < 4; ++e) sa[c][nt][e] = 0.f;
+#pragma unroll
+    for (int i = 0; i < T::NCP; ++i) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(kb + off[i], r0, r1, r2, r3);
+        if constexpr (!FP8) {
+            // chunks 2i, 2i+1 = dims 16i..16i+15 = k-step i; r0/r1 tokens 0-7, r2/r3 tokens 8-15
+            mma_bf16_16816(sa[i & 1][0], qa[i][0], 0u, qa[i][1], 0u, r0, r1);
+            mma_bf16_16816(sa[i & 1][1], qa[i][0], 0u, qa[i][1], 0u, r2, r3);
+        } else {
+            // chunk 2i (2i+1) = k-step 2i (2i+1); a register holds four codes 4r..4r+3 of a token:
+            // dims (4r, 4r+1) are k-slots (2r, 2r+1), dims (4r+2, 4r+3) k-slots (2r+8, 2r+9)
+            mma_f16_16816(sa[0][0], qa[2 * i][0], 0u, qa[2 * i][1], 0u, e4m3x2_to_f16x2(r0),
+                          e4m3x2_to_f16x2(r0 >> 16));
+            mma_f16_16816(sa[0][1], qa[2 * i][0], 0u, qa[2 * i][1], 0u, e4m3x2_to_f16x2(r2),
+                          e4m3x2_to_f16x2(r2 >> 16));
+            mma_f16_16816(sa[1][0], qa[2 * i + 1][0], 0u, qa[2 * i + 1][1], 0u, e4m3x2_to_f16x2(r1),
+                          e4m3x2_to_f16x2(r1 >> 16));
+            mma_f16_16816(sa[1][1], qa[2 * i + 1][0], 0u, qa[2 * i + 1][1], 0u, e4m3x2_to_f16x2(r3),
+                          e4m3x2_to_f16x2(r3 >> 16));
         }
     }
-    // reduce-scatter over the LPT lanes of a token: afterwards lane c holds the
-    // full score of step c / DUP
+    // the thread's scores: row g, tokens 8 nt + 2 r4 + e (fragment elements c0, c1 of n-tile nt)
+    float x[4];
+    bool ok[4];
 #pragma unroll
-    for (int cnt = NIT, mask = LPT / 2; cnt > 1; cnt >>= 1, mask >>= 1) {
-        const bool upper = (c & mask) != 0;
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int j = 0; j < cnt / 2; ++j) {
+        for (int e = 0; e < 2; ++e) {
+            const int k = 2 * nt + e;
+            ok[k] = 8 * nt + 2 * r4 + e < lim;
+            x[k] = ok[k] ? (sa[0][nt][e] + sa[1][nt][e]) * ksc : -INFINITY;
+        }
+    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));  // the four threads of a row
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+    // Online softmax (m, l, acc).  The running max only moves when some score passes it by more
+    // than the slack; the first tile with a valid token for the row always moves it (m = -inf).
+    if (__any_sync(kFull, mx > m + kRescaleSlack)) {
+        const float mn = fmaxf(m, mx);
+        const float alpha = mn == -INFINITY ? 1.0f : ex2(m - mn);  // 0 on the row's first valid tile
+        l *= alpha;
+        m = mn;
+        // output columns 2 r4 and 2 r4 + 1 are the rows of threads 8 r4 and 8 r4 + 4
+        const float a0 = __shfl_sync(kFull, alpha, 8 * r4), a1 = __shfl_sync(kFull, alpha, 8 * r4 + 4);
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float send = upper ? part[h][j] : part[h][j + cnt / 2];
-                const float keep = upper ? part[h][j + cnt / 2] : part[h][j];
-                part[h][j] = keep + __shfl_xor_sync(kFull, send, mask);
-            }
+        for (int mt = 0; mt < T::MT; ++mt) {
+            o[mt][0] *= a0;
+            o[mt][1] *= a1;
+            o[mt][2] *= a0;
+            o[mt][3] *= a1;
         }
     }
+    float pr[4];
 #pragma unroll
-    for (int mask = DUP / 2; mask > 0; mask >>= 1)
-#pragma unroll
-        for (int h = 0; h < G; ++h) part[h][0] += __shfl_xor_sync(kFull, part[h][0], mask);
+    for (int k = 0; k < 4; ++k) pr[k] = ok[k] ? ex2(x[k] - m) : 0.f;
+    l += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+    const uint32_t pb0 = FP8 ? f16x2_of(pr[0], pr[1]) : pack_bf16x2(pr[0], pr[1]);
+    const uint32_t pb1 = FP8 ? f16x2_of(pr[2], pr[3]) : pack_bf16x2(pr[2], pr[3]);
 
-    const int tok_s = (c / DUP) * TPI + grp;
-    const bool ok = tok_s < valid;
-    float pr[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        // several queries per stream: query h / gq sees qtail - h / gq fewer of the sequence's last
-        // tokens (rem: tokens of the sequence from this tile's first on, not clamped to the tile)
-        const bool okh = qtail > 0 ? tok_s < min(valid, rem - (qtail - h / gq)) : ok;
-        const float s = okh ? part[h][0] : -INFINITY;
-        // Online softmax (m, l, acc).  The running max only moves when some
-        // score passes it by more than the slack; the first tile with a valid token
-        // for the head always moves it (m = -inf before it).
-        if (__any_sync(kFull, s > m[h] + kRescaleSlack)) {
-            const float mn = fmaxf(m[h], warp_max(s));
-            const float alpha = ex2(m[h] - mn);  // 0 on the first tile
-            l[h] *= alpha;
-            const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[h][j] = __fmul2_rn(acc[h][j], a2);
-            m[h] = mn;
-        }
-        pr[h] = okh ? ex2(s - m[h]) : 0.f;
-        l[h] += pr[h];
+    // transposed V tiles: the low half of a register is token 2 r4 (8 + 2 r4), the high half the next one
+    uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
+    if constexpr (TAIL) {
+        keep0 = (2 * r4 < valid ? 0x0000ffffu : 0u) | (2 * r4 + 1 < valid ? 0xffff0000u : 0u);
+        keep1 = (2 * r4 + 8 < valid ? 0x0000ffffu : 0u) | (2 * r4 + 9 < valid ? 0xffff0000u : 0u);
     }
-    // P.V: the weight of token i*TPI + grp sits in lane grp*LPT + i*DUP
 #pragma unroll
-    for (int i = 0; i < NIT; ++i) {
-        const int tok = i * TPI + grp;
-        float ph[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) ph[h] = __shfl_sync(kFull, pr[h], grp * LPT + i * DUP);
-        if (tok < valid) {  // rows past L may hold anything, even NaN: never touch them
-            float2 v2[4];
-            load8<FP8>(Vs, tok * stride + c * 8, v2);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float2 p2 = make_float2(ph[h], ph[h]);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[h][j] = __ffma2_rn(p2, v2[j], acc[h][j]);
-            }
+    for (int i = 0; i < T::NCP; ++i) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_t(vb + off[i], r0, r1, r2, r3);
+        if constexpr (TAIL) {
+            r0 &= keep0;
+            r1 &= keep0;
+            r2 &= keep1;
+            r3 &= keep1;
+        }
+        if constexpr (!FP8) {
+            // m-tile i: dims 16i + g (r0: tokens 0-7, r2: tokens 8-15) and 16i + 8 + g (r1, r3)
+            mma_bf16_16816(o[i], r0, r1, r2, r3, pb0, pb1);
+        } else {
+            // a register holds (token 2r4: dims 2g, 2g+1 | token 2r4+1: dims 2g, 2g+1) of a 16-dim
+            // chunk; the byte permute pairs the two tokens per dim: low half dim 2g, high half dim 2g+1
+            const uint32_t x0 = __byte_perm(r0, 0u, 0x3120), x1 = __byte_perm(r1, 0u, 0x3120);
+            const uint32_t x2 = __byte_perm(r2, 0u, 0x3120), x3 = __byte_perm(r3, 0u, 0x3120);
+            mma_f16_16816(o[2 * i], e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x2),
+                          e4m3x2_to_f16x2(x2 >> 16), pb0, pb1);
+            mma_f16_16816(o[2 * i + 1], e4m3x2_to_f16x2(x1), e4m3x2_to_f16x2(x1 >> 16), e4m3x2_to_f16x2(x3),
+                          e4m3x2_to_f16x2(x3 >> 16), pb0, pb1);
         }
     }
 }
@@ -760,8 +807,6 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeParams p)
 {
-    using S = Shape<D, G>;
-    constexpr int LPT = S::LPT, DUP = S::DUP, TW = S::TW;
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int ES = FP8 ? 1 : 2;  // bytes per cached element
     const CtaLayout lay = cta_layout(D, G, ES, p.hg, p.sub, p.nst, p.B);
@@ -845,6 +890,10 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         // ============================== producer warp ==============================
         const uint64_t policy = policy_evict_first();
         const uint32_t box_bytes = uint32_t(p.boxtok * p.hg * D * ES);
+        constexpr int NPART = Tc<D, FP8>::NP;
+        const int nsub = p.hg * NPART;                                  // copies per box and cache
+        const int nreq = p.nbox * nsub * 2;                             // copies per unit
+        const uint32_t part_bytes = uint32_t(p.boxtok * Tc<D, FP8>::RB);  // one (kv head, part) of a box
         uint32_t kk = 0, segs = 0;  // units issued, q-ring uses
         int rs = 0;                 // ring slot of unit kk (kk % nst, kept without a division)
         uint32_t rph = 0;           // parity of that slot's use (kk / nst) & 1
@@ -951,9 +1000,25 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                     mbar_arrive_expect_tx(&full[s], 2 * nrows * box_bytes);
                 }
                 __syncwarp();
-                if (row >= 0) {
-                    tma_load_3d(st + lane * box_bytes, &kmap, 0, iw.g * p.hg, row, &full[s], policy);
-                    tma_load_3d(st + lay.kv_bytes + lane * box_bytes, &vmap, 0, iw.g * p.hg, row, &full[s], policy);
+                if (!p.split_copies) {  // box j: lane j, one copy per cache
+                    if (row >= 0) {
+                        tma_load_4d(st + lane * box_bytes, &kmap, 0, row, 0, iw.g * p.hg, &full[s], policy);
+                        tma_load_4d(st + lay.kv_bytes + lane * box_bytes, &vmap, 0, row, 0, iw.g * p.hg, &full[s],
+                                    policy);
+                    }
+                } else {
+                // one copy per (box, cache, kv head, row part), spread over the lanes; box j's row
+                // is in lane j
+                for (int q0 = 0; q0 < nreq; q0 += 32) {
+                    const int qi = q0 + lane;
+                    const int bi = qi / (2 * nsub), rest = qi - bi * 2 * nsub;
+                    const int brow = __shfl_sync(kFull, row, bi & 31);
+                    if (qi < nreq && brow >= 0) {
+                        const int vside = rest >= nsub ? 1 : 0, hp = rest - vside * nsub;  // hp = h * NP + part
+                        tma_load_3d(st + vside * lay.kv_bytes + bi * box_bytes + hp * part_bytes,
+                                    vside ? &vmap : &kmap, 0, iw.g * p.hg * NPART + hp, brow, &full[s], policy);
+                    }
+                }
                 }
                 ++kk;
                 if (++rs == p.nst) {
@@ -996,15 +1061,22 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     }
 
     // ============================== consumer warps ==============================
+    using TC = Tc<D, FP8>;
     const int h = warp / p.sub, j = warp - h * p.sub;  // kv head in the group, token slice of the unit
-    const int c = lane % LPT, grp = lane / LPT;
-    const int stride = p.hg * D;                      // elements between consecutive tokens of a stage
+    const int g8 = lane >> 2, r4 = lane & 3;           // fragment row group and column pair of the thread
     const int home = sh[0];
+    uint32_t off[TC::NCP];
+    lane_offsets<D, FP8>(off, lane, j, h, p.hg, p.boxtok);
+    const uint32_t stage_addr = smem_u32(stage0);
+    // several queries per stream: the query of row g8 sees `shift` fewer of the sequence's last tokens
+    const int shift = (p.qn - 1) - g8 / p.gq;
     uint32_t kk = 0, segs = 0, combs = 0;
     int s = 0;           // ring slot of stage kk
     uint32_t sph = 0;    // parity of its use
-    float2 q2[G][4], acc[G][4];
-    float m[G], l[G];
+    uint32_t qa[TC::KS][2];
+    float o[TC::MT][4];
+    float m = -INFINITY, l = 0.f;
+    float ksc = p.scale_log2;
     float vsc = 1.0f;  // E4M3 caches: the kv head's V scale, applied in the final division
     int u_first = 0;
     for (;;) {
@@ -1014,10 +1086,9 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         }
         const UnitMeta mt = metas[s];
         if (mt.b < 0) break;
-        const uint8_t *st = stage0 + s * lay.stage_bytes;
         if (mt.flags & kFirst) {
             const int qs = int(segs & 1u);
-            float ksc = p.scale_log2;  // E4M3 caches: the kv head's K scale folds into the query prescale
+            ksc = p.scale_log2;  // E4M3 caches: the kv head's K scale joins the score scale
             if constexpr (FP8) {
                 ksc *= __ldg(p.k_scale + mt.g * p.hg + h);
                 vsc = __ldg(p.v_scale + mt.g * p.hg + h);
@@ -1026,31 +1097,43 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                 if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
                 break;
             }
-            const uint16_t *qh = reinterpret_cast<const uint16_t *>(qbuf + qs * lay.q_bytes) + h * G * D;
-            const float2 sc = make_float2(ksc, ksc);
+            // Q operand fragments of row g8 (zero rows past G): k-step ks holds dims 16 ks + 2 r4 (+1)
+            // and 16 ks + 8 + 2 r4 (+1) (bf16), or 16 ks + 4 r4 (+1) and 16 ks + 4 r4 + 2 (+3) (E4M3 order)
+            const uint16_t *qr = reinterpret_cast<const uint16_t *>(qbuf + qs * lay.q_bytes) + (h * G + g8) * D;
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                float2 f[4];
-                unpack8x2(*reinterpret_cast<const uint4 *>(qh + hh * D + c * 8), f);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    q2[hh][e] = __fmul2_rn(f[e], sc);
-                    acc[hh][e] = make_float2(0.f, 0.f);
+            for (int ks = 0; ks < TC::KS; ++ks) {
+                qa[ks][0] = qa[ks][1] = 0u;
+                if (g8 < G) {
+                    if constexpr (!FP8) {
+                        qa[ks][0] = *reinterpret_cast<const uint32_t *>(qr + 16 * ks + 2 * r4);
+                        qa[ks][1] = *reinterpret_cast<const uint32_t *>(qr + 16 * ks + 8 + 2 * r4);
+                    } else {
+                        const uint2 w = *reinterpret_cast<const uint2 *>(qr + 16 * ks + 4 * r4);
+                        qa[ks][0] = f16x2_of(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+                        qa[ks][1] = f16x2_of(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+                    }
                 }
-                m[hh] = -INFINITY;
-                l[hh] = 0.f;
             }
+#pragma unroll
+            for (int mi = 0; mi < TC::MT; ++mi)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[mi][e] = 0.f;
+            m = -INFINITY;
+            l = 0.f;
             __syncwarp();
             if (lane == 0) mbar_arrive(&qempty[qs]);
             ++segs;
             u_first = mt.u;
         }
-        const int tok0 = mt.u * p.toks + j * TW;
-        const int valid = min(TW, mt.L - tok0);
+        const int tok0 = mt.u * p.toks + j * 16;
+        const int valid = min(16, mt.L - tok0);
         if (valid > 0) {
-            const int e0 = (j * TW * p.hg + h) * D;  // element offset of this warp's first row in the stage
-            attend_tile<D, G, FP8>(st + e0 * ES, st + lay.kv_bytes + e0 * ES, stride, valid, q2, m, l, acc, c,
-                                   grp, mt.L - tok0, p.qn - 1, p.gq);
+            const uint32_t kb = stage_addr + uint32_t(s) * lay.stage_bytes;
+            const int lim = min(valid, mt.L - tok0 - shift);
+            if (valid == 16)
+                attend_tile<D, FP8, false>(kb, kb + lay.kv_bytes, off, qa, ksc, lim, valid, m, l, o, lane);
+            else
+                attend_tile<D, FP8, true>(kb, kb + lay.kv_bytes, off, qa, ksc, lim, valid, m, l, o, lane);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -1061,75 +1144,75 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         }
 
         if (mt.flags & kLast) {
-            // close this warp's part of (b, group): fold the token groups
-#pragma unroll
-            for (int mask = LPT; mask < 32; mask <<= 1)
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        acc[hh][e].x += __shfl_xor_sync(kFull, acc[hh][e].x, mask);
-                        acc[hh][e].y += __shfl_xor_sync(kFull, acc[hh][e].y, mask);
-                    }
-            float lt[G];
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) lt[hh] = warp_sum(l[hh]) * (1.0f / DUP);
+            // close this warp's part of (b, group).  Row state -> column state: the thread's output
+            // columns are query heads 2 r4 + e (e = 0, 1), whose rows belong to threads 8 r4 + 4e.
+            float lt = l + __shfl_xor_sync(kFull, l, 1);
+            lt += __shfl_xor_sync(kFull, lt, 2);
+            float mc[2], lc[2];
+            mc[0] = __shfl_sync(kFull, m, 8 * r4);
+            mc[1] = __shfl_sync(kFull, m, 8 * r4 + 4);
+            lc[0] = __shfl_sync(kFull, lt, 8 * r4);
+            lc[1] = __shfl_sync(kFull, lt, 8 * r4 + 4);
             bool leader = true;
             if (p.sub > 1) {
                 // the token slices of a kv head are combined by the head's first warp (j == 0):
-                // the others leave their states in shared memory
+                // the others leave their states in shared memory ([G][D] sums, then G maxima, G sums)
                 const uint32_t round = combs++;
                 const int cst = comb_stride(D, G);
                 leader = j == 0;
                 if (!leader) {
                     if (round > 0 && !mbar_wait_bounded(cfree, (round - 1) & 1u)) break;
                     float *mine = comb + (h * (p.sub - 1) + j - 1) * cst;
-                    if (grp == 0)
 #pragma unroll
-                        for (int hh = 0; hh < G; ++hh) {
-                            float4 *dst = reinterpret_cast<float4 *>(mine + hh * D + c * 8);
-                            dst[0] = make_float4(acc[hh][0].x, acc[hh][0].y, acc[hh][1].x, acc[hh][1].y);
-                            dst[1] = make_float4(acc[hh][2].x, acc[hh][2].y, acc[hh][3].x, acc[hh][3].y);
-                        }
-                    if (lane == 0)
+                    for (int e = 0; e < 2; ++e) {
+                        const int hh = 2 * r4 + e;
+                        if (hh < G) {
 #pragma unroll
-                        for (int hh = 0; hh < G; ++hh) {
-                            mine[G * D + hh] = m[hh];
-                            mine[G * D + G + hh] = lt[hh];
+                            for (int mi = 0; mi < TC::MT; ++mi)
+#pragma unroll
+                                for (int half = 0; half < 2; ++half)
+                                    mine[hh * D + dim_of<FP8>(mi, half, g8)] = o[mi][2 * half + e];
+                            if (g8 == 0) {
+                                mine[G * D + hh] = mc[e];
+                                mine[G * D + G + hh] = lc[e];
+                            }
                         }
+                    }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(cfull);
                 } else {
                     if (!mbar_wait_bounded(cfull, round & 1u)) break;
                     const float *others = comb + h * (p.sub - 1) * cst;
 #pragma unroll
-                    for (int hh = 0; hh < G; ++hh) {
-                        float M = m[hh];
-                        for (int jj = 0; jj < p.sub - 1; ++jj) M = fmaxf(M, others[jj * cst + G * D + hh]);
-                        // M = -inf only when no slice saw a valid token for this head (several queries
-                        // per stream, a piece past the query's last key): the state stays zero
-                        const bool none = M == -INFINITY;
-                        const float f0 = none ? 0.f : ex2(m[hh] - M);
-                        float ls = f0 * lt[hh];
-                        const float2 f02 = make_float2(f0, f0);
-                        float2 a[4];
+                    for (int e = 0; e < 2; ++e) {
+                        const int hh = 2 * r4 + e;
+                        if (hh < G) {
+                            float M = mc[e];
+                            for (int jj = 0; jj < p.sub - 1; ++jj) M = fmaxf(M, others[jj * cst + G * D + hh]);
+                            // M = -inf only when no slice saw a valid token for this head (several
+                            // queries per stream, a piece past the query's last key): the state stays zero
+                            const bool none = M == -INFINITY;
+                            const float f0 = none ? 0.f : ex2(mc[e] - M);
+                            float ls = f0 * lc[e];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) a[e] = __fmul2_rn(acc[hh][e], f02);
-                        for (int jj = 0; jj < p.sub - 1; ++jj) {
-                            const float *st2 = others + jj * cst;
-                            const float f = none ? 0.f : ex2(st2[G * D + hh] - M);  // 0 for a slice with no tokens
-                            ls = fmaf(f, st2[G * D + G + hh], ls);
-                            const float4 x0 = *reinterpret_cast<const float4 *>(st2 + hh * D + c * 8);
-                            const float4 x1 = *reinterpret_cast<const float4 *>(st2 + hh * D + c * 8 + 4);
-                            a[0] = make_float2(fmaf(f, x0.x, a[0].x), fmaf(f, x0.y, a[0].y));
-                            a[1] = make_float2(fmaf(f, x0.z, a[1].x), fmaf(f, x0.w, a[1].y));
-                            a[2] = make_float2(fmaf(f, x1.x, a[2].x), fmaf(f, x1.y, a[2].y));
-                            a[3] = make_float2(fmaf(f, x1.z, a[3].x), fmaf(f, x1.w, a[3].y));
+                            for (int mi = 0; mi < TC::MT; ++mi) {
+                                o[mi][e] *= f0;
+                                o[mi][2 + e] *= f0;
+                            }
+                            for (int jj = 0; jj < p.sub - 1; ++jj) {
+                                const float *st2 = others + jj * cst;
+                                const float f = none ? 0.f : ex2(st2[G * D + hh] - M);  // 0: a slice without tokens
+                                ls = fmaf(f, st2[G * D + G + hh], ls);
+#pragma unroll
+                                for (int mi = 0; mi < TC::MT; ++mi)
+#pragma unroll
+                                    for (int half = 0; half < 2; ++half)
+                                        o[mi][2 * half + e] =
+                                            fmaf(f, st2[hh * D + dim_of<FP8>(mi, half, g8)], o[mi][2 * half + e]);
+                            }
+                            mc[e] = M;
+                            lc[e] = ls;
                         }
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[hh][e] = a[e];
-                        m[hh] = M;
-                        lt[hh] = ls;
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(cfree);
@@ -1139,33 +1222,46 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                 const int kvh = mt.g * p.hg + h;
                 const int piece = mt.u - u_first + 1;
                 if (piece == mt.n) {  // this CTA ran the whole (b, group): write the output
-                    if (grp == 0)
 #pragma unroll
-                        for (int hh = 0; hh < G; ++hh) {
-                            const float inv = vsc / lt[hh];
-                            uint4 o;
-                            o.x = pack_bf16x2(acc[hh][0].x * inv, acc[hh][0].y * inv);
-                            o.y = pack_bf16x2(acc[hh][1].x * inv, acc[hh][1].y * inv);
-                            o.z = pack_bf16x2(acc[hh][2].x * inv, acc[hh][2].y * inv);
-                            o.w = pack_bf16x2(acc[hh][3].x * inv, acc[hh][3].y * inv);
-                            *reinterpret_cast<uint4 *>(
-                                p.out + (((long long)mt.b * p.qn + hh / p.gq) * p.Hq + (long long)kvh * p.gq + hh % p.gq) * D +
-                                c * 8) = o;
+                    for (int e = 0; e < 2; ++e) {
+                        const int hh = 2 * r4 + e;
+                        if (hh < G) {
+                            const float inv = vsc / lc[e];
+                            uint16_t *orow = p.out + (((long long)mt.b * p.qn + hh / p.gq) * p.Hq +
+                                                      (long long)kvh * p.gq + hh % p.gq) * D;
+#pragma unroll
+                            for (int mi = 0; mi < TC::MT; ++mi) {
+                                if constexpr (FP8) {
+                                    *reinterpret_cast<uint32_t *>(orow + dim_of<FP8>(mi, 0, g8)) =
+                                        pack_bf16x2(o[mi][e] * inv, o[mi][2 + e] * inv);
+                                } else {
+                                    orow[dim_of<FP8>(mi, 0, g8)] = uint16_t(pack_bf16x2(o[mi][e] * inv, 0.f));
+                                    orow[dim_of<FP8>(mi, 1, g8)] = uint16_t(pack_bf16x2(o[mi][2 + e] * inv, 0.f));
+                                }
+                            }
                         }
+                    }
                 } else {
                     const long long sigma = (long long)mt.b * p.nhg + mt.g;
                     const long long slot = (mt.slice + sigma) * p.hg + h;
-                    if (grp == 0)
 #pragma unroll
-                        for (int hh = 0; hh < G; ++hh) {
-                            float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + ((slot * G + hh) * D + c * 8));
-                            dst[0] = make_float4(acc[hh][0].x, acc[hh][0].y, acc[hh][1].x, acc[hh][1].y);
-                            dst[1] = make_float4(acc[hh][2].x, acc[hh][2].y, acc[hh][3].x, acc[hh][3].y);
+                    for (int e = 0; e < 2; ++e) {
+                        const int hh = 2 * r4 + e;
+                        if (hh < G) {
+                            float *dst = p.ws_acc + (slot * G + hh) * D;
+#pragma unroll
+                            for (int mi = 0; mi < TC::MT; ++mi) {
+                                if constexpr (FP8) {
+                                    *reinterpret_cast<float2 *>(dst + dim_of<FP8>(mi, 0, g8)) =
+                                        make_float2(o[mi][e], o[mi][2 + e]);
+                                } else {
+                                    dst[dim_of<FP8>(mi, 0, g8)] = o[mi][e];
+                                    dst[dim_of<FP8>(mi, 1, g8)] = o[mi][2 + e];
+                                }
+                            }
+                            if (g8 == 0) reinterpret_cast<float2 *>(p.ws_ml)[slot * G + hh] = make_float2(mc[e], lc[e]);
                         }
-                    if (lane == 0)
-#pragma unroll
-                        for (int hh = 0; hh < G; ++hh)
-                            reinterpret_cast<float2 *>(p.ws_ml)[slot * G + hh] = make_float2(m[hh], lt[hh]);
+                    }
                     // publish the piece, then count its units in; the CTA that completes the
                     // (b, kv head) merges all pieces
                     __threadfence();
@@ -1182,6 +1278,14 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                     }
                 }
             }
+            // The segment's state is spent (the next segment starts with kFirst and sets it again);
+            // clearing it here tells the compiler so, and it keeps none of it through the merge.
+#pragma unroll
+            for (int ks = 0; ks < TC::KS; ++ks) qa[ks][0] = qa[ks][1] = 0u;
+#pragma unroll
+            for (int mi = 0; mi < TC::MT; ++mi)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[mi][e] = 0.f;
         }
         if ((mt.flags & kSliceEnd) && adaptive && warp == 0 && lane == 0) {
             // balance record for the next call: this slice's weight and run time, or "absent"
@@ -1205,29 +1309,46 @@ struct LaunchArgs {
     cudaStream_t stream;
 };
 
-// Tensor map over one cache: dims (head_dim, kv heads, NB * bs rows); a box is
-// box_rows tokens x box_heads kv heads x head_dim (whole contiguous rows of a head group).
+// Tensor map over one cache, each cached row (token, kv head) seen as parts of
+// RB bytes (RB / es elements).  split = 0: dims (RB / es, NB * bs rows, parts,
+// Hkv), a box is box_rows tokens x all parts x box_heads kv heads, landing in
+// shared memory as [kv head][part][token][RB bytes]; split = 1: dims (RB / es,
+// Hkv * parts, rows), a box is box_rows tokens of one part of one kv head.
+// Either way the copy swizzles RB-byte rows (see the stage layout at Tc).
 inline bool encode_cache_map(CUtensorMap *map, const void *base, bool fp8, int D, int Hkv, int64_t rows,
-                             int box_heads, int box_rows)
+                             int box_heads, int box_rows, int split)
 {
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) {
         record_cuda_error("cuTensorMapEncodeTiled", "driver entry point unavailable");
         return false;
     }
-    const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(Hkv), cuuint64_t(rows)};
-    const cuuint64_t es = fp8 ? 1 : 2;  // bytes per element
-    const cuuint64_t strides[2] = {cuuint64_t(D) * es, cuuint64_t(Hkv) * D * es};
-    const cuuint32_t box[3] = {cuuint32_t(D), cuuint32_t(box_heads), cuuint32_t(box_rows)};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    const CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                           const_cast<void *>(base), dims, strides, box,
-                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const int es = fp8 ? 1 : 2;  // bytes per element
+    const int rb = row_bytes_smem(D, es), parts = D * es / rb;
+    const cuuint64_t row_stride = cuuint64_t(Hkv) * D * es;
+    CUresult r;
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapSwizzle sw = rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!split) {
+        const cuuint64_t dims[4] = {cuuint64_t(rb / es), cuuint64_t(rows), cuuint64_t(parts), cuuint64_t(Hkv)};
+        const cuuint64_t strides[3] = {row_stride, cuuint64_t(rb), cuuint64_t(D) * es};
+        const cuuint32_t box[4] = {cuuint32_t(rb / es), cuuint32_t(box_rows), cuuint32_t(parts), cuuint32_t(box_heads)};
+        r = enc(map, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[3] = {cuuint64_t(rb / es), cuuint64_t(Hkv) * parts, cuuint64_t(rows)};
+        const cuuint64_t strides[2] = {cuuint64_t(rb), row_stride};
+        const cuuint32_t box[3] = {cuuint32_t(rb / es), 1u, cuuint32_t(box_rows)};
+        r = enc(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS) {
-        char msg[64];
-        std::snprintf(msg, sizeof msg, "CUresult %d", int(r));
-        record_cuda_error("cuTensorMapEncodeTiled", msg);
+        if (split) {  // the 4-D map is only a first try (see launch_decode)
+            char msg[64];
+            std::snprintf(msg, sizeof msg, "CUresult %d", int(r));
+            record_cuda_error("cuTensorMapEncodeTiled", msg);
+        }
         return false;
     }
     return true;
@@ -1238,7 +1359,7 @@ inline bool encode_cache_map(CUtensorMap *map, const void *base, bool fp8, int D
 // most recent ones (an engine binds one k_cache / v_cache view per layer, as in
 // the nano-vllm KV-cache post, §3.2).
 inline bool cached_cache_map(CUtensorMap *map, int dev, const void *base, bool fp8, int D, int Hkv, int64_t rows,
-                             int box_heads, int box_rows)
+                             int box_heads, int box_rows, int split)
 {
     struct Entry {
         int dev;
@@ -1246,7 +1367,7 @@ inline bool cached_cache_map(CUtensorMap *map, int dev, const void *base, bool f
         bool fp8;
         int D, Hkv;
         int64_t rows;
-        int box_heads, box;
+        int box_heads, box, split;
         CUtensorMap map;
     };
     constexpr size_t kMaxEntries = 256;
@@ -1256,14 +1377,14 @@ inline bool cached_cache_map(CUtensorMap *map, int dev, const void *base, bool f
     for (size_t i = 0; i < cache.size(); ++i) {
         const Entry &e = cache[i];
         if (e.dev == dev && e.base == base && e.fp8 == fp8 && e.D == D && e.Hkv == Hkv && e.rows == rows &&
-            e.box_heads == box_heads && e.box == box_rows) {
+            e.box_heads == box_heads && e.box == box_rows && e.split == split) {
             *map = e.map;
             return true;
         }
     }
-    if (!encode_cache_map(map, base, fp8, D, Hkv, rows, box_heads, box_rows)) return false;
+    if (!encode_cache_map(map, base, fp8, D, Hkv, rows, box_heads, box_rows, split)) return false;
     if (cache.size() >= kMaxEntries) cache.erase(cache.begin());
-    cache.push_back(Entry{dev, base, fp8, D, Hkv, rows, box_heads, box_rows, *map});
+    cache.push_back(Entry{dev, base, fp8, D, Hkv, rows, box_heads, box_rows, split, *map});
     return true;
 }
 
@@ -1314,9 +1435,20 @@ pkv_status launch_decode(LaunchArgs &a)
 
     CUtensorMap kmap, vmap;
     const int64_t rows = int64_t(p.NB) * p.bs;
-    if (!cached_cache_map(&kmap, a.device, a.k_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok) ||
-        !cached_cache_map(&vmap, a.device, a.v_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok))
-        return PKV_ECUDA;
+    // one 4-D copy per box where the driver takes that map (its strides are not in increasing
+    // order), else one copy per kv head and row part; a refusal is remembered
+    static std::atomic<bool> four_d_refused{false};
+    p.split_copies = four_d_refused.load() ? 1 : 0;
+    if (!p.split_copies && (!cached_cache_map(&kmap, a.device, a.k_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok, 0) ||
+                            !cached_cache_map(&vmap, a.device, a.v_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok, 0))) {
+        four_d_refused.store(true);
+        p.split_copies = 1;
+    }
+    if (p.split_copies) {
+        if (!cached_cache_map(&kmap, a.device, a.k_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok, 1) ||
+            !cached_cache_map(&vmap, a.device, a.v_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok, 1))
+            return PKV_ECUDA;
+    }
 
     auto kern = paged_decode_kernel<D, G, FP8>;
     if (!ensure_smem_attribute<D, G, FP8>(kern, a.device, lay.total)) return PKV_ECUDA;
