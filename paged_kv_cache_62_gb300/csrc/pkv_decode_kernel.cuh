@@ -10,11 +10,11 @@
 //
 // How (GB300 design):
 //  * Kv heads are taken in groups of HG (the largest divisor of Hkv that is
-//    at most the CTA's consumer warps, 8, or 4 for groups of 5+ query heads).
-//    A unit of work is TOKS = TW * SUB consecutive tokens of one (sequence,
-//    head group), TW = 16 tokens per warp and SUB warps per head (see
-//    team_warps): whole contiguous cache rows of the group, moved by
-//    one TMA tensor copy per physical-block span into a shared-memory stage.
+//    at most the CTA's 8 consumer warps).  A unit of work is TOKS = TW * SUB
+//    consecutive tokens of one (sequence, head group), TW = 16 tokens per
+//    warp and SUB warps per head (see team_warps): the group's cache rows,
+//    moved by one 4-D TMA tensor copy per physical-block span and cache into
+//    a shared-memory stage as 128-byte-swizzled rows (see Tc).
 //  * One CTA per SM: a producer warp streams units through a ring of 2-4
 //    stages (mbarrier transaction counts for "full", consumer arrivals for
 //    "empty"); HG * SUB consumer warps take one TW-token slice of one kv head
@@ -22,11 +22,12 @@
 //    together.  Block-table entries for 32 boxes at a time are fetched by the
 //    producer's lanes one batch ahead; q rows arrive by bulk copy in a
 //    separate 2-slot ring.
-//  * A consumer serves all G query heads of its kv head from one K/V read: a
-//    token row is split over D/8 lanes (16 bytes each), partial dot products
-//    are finished by a shuffle reduce-scatter, the softmax max is a warp vote
-//    plus (rarely) a warp max, exponentials are ex2 of log2e-prescaled scores,
-//    and P.V uses the same lane split with packed fp32 FMAs.
+//  * A consumer serves all G query heads of its kv head from one K/V read,
+//    on the warp-level tensor cores: S^T = Q K^T and O^T += V^T P^T as
+//    m16n8k16 MMAs with fp32 accumulators, K and V fed by ldmatrix from the
+//    swizzled stage, P kept in registers (see attend_tile); the online
+//    softmax rescales only when a score passes the running max by a slack,
+//    and exponentials are ex2 of log2e-prescaled scores.
 //  * The batch's unit list is cut into one slice per SM id, each slice's size
 //    following the finishing times the previous call on the workspace saw.
 //    A CTA whose slice covers a whole (sequence, head group) writes bf16
@@ -369,6 +370,14 @@ __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// f16 pair, magnitudes past the f16 range saturating to +-65504 (NaN stays NaN).
+__device__ __forceinline__ uint32_t f16x2_sat(float lo, float hi)
+{
+    uint32_t h;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
+    return h;
+}
+
 // One 16-token tile of one (sequence, kv head) for its G query heads
 // (virtual heads) on the tensor cores, m16n8k16 with fp32 accumulators:
 //   S^T = Q K^T    rows: query heads (row g = lane / 4; rows G..15 are zero),
@@ -381,8 +390,10 @@ __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi)
 // tokens below it count for this thread's row (causal bound of its query);
 // TAIL: tokens from `valid` on are not the sequence's (their rows may hold
 // anything, even NaN), so their V values are zeroed before the product.
-// E4M3 caches run the products in f16 (every E4M3 value is exact in f16);
-// the kv head's K scale is in ksc, its V scale is applied by the caller.
+// E4M3 caches run the products in f16 (every E4M3 value is exact in f16, and
+// so is every bf16 query element of magnitude 2^-14 .. 65504; smaller ones
+// keep f16's subnormal steps of 2^-24, larger ones saturate at 65504); the
+// kv head's K scale is in ksc, its V scale is applied by the caller.
 template <int D, bool FP8, bool TAIL>
 __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb, const uint32_t (&off)[Tc<D, FP8>::NCP],
                                             const uint32_t (&qa)[Tc<D, FP8>::KS][2], float ksc, int lim, int valid,
@@ -1109,8 +1120,8 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                         qa[ks][1] = *reinterpret_cast<const uint32_t *>(qr + 16 * ks + 8 + 2 * r4);
                     } else {
                         const uint2 w = *reinterpret_cast<const uint2 *>(qr + 16 * ks + 4 * r4);
-                        qa[ks][0] = f16x2_of(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
-                        qa[ks][1] = f16x2_of(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+                        qa[ks][0] = f16x2_sat(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+                        qa[ks][1] = f16x2_sat(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
                     }
                 }
             }
