@@ -77,7 +77,7 @@ static pkv_status decode_call(bool fp8, int32_t qn, const uint16_t *q, const voi
     p.hg = head_group(num_kv_heads, G);
     p.nhg = num_kv_heads / p.hg;
     p.sub = warp_slices(G, p.hg);
-    p.toks = warp_tokens(G) * p.sub;
+    p.toks = warp_tokens(G, fp8) * p.sub;
     p.boxtok = std::min(p.toks, block_size);
     p.nbox = p.toks / p.boxtok;
     p.lg_nbox = ilog2(p.nbox);

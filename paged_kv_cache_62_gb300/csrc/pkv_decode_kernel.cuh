@@ -62,13 +62,16 @@ constexpr uint32_t kTableMagic = 0x62616c31u;
 constexpr uint32_t kEpochMagic = 0x65706f63u;
 
 // Consumer warps per CTA and tokens each takes from a stage (a stage holds
-// team_warps * warp_tokens token rows of head_dim, 64 KiB for bf16 and
-// head_dim 128).  A warp's tile is 16 tokens, the n extent of two m16n8k16
-// score products and the k extent of one output product; a warp's registers
-// do not grow with the group size (G query heads are rows of one MMA tile),
-// so every group size runs 8 consumers.
+// team_warps * warp_tokens token rows of head_dim: 64 KiB for head_dim 128).
+// A warp's tile is made of 16-token sub-tiles, each the n extent of two
+// m16n8k16 score products and the k extent of one output product: one for
+// bf16 caches, two for E4M3 caches (the same bytes a stage; two independent
+// sub-tiles give the consumer twice the independent MMA chains, and the
+// widening of E4M3 codes makes that path consumer-bound).  A warp's
+// registers do not grow with the group size (G query heads are rows of one
+// MMA tile), so every group size runs 8 consumers.
 __host__ __device__ constexpr int team_warps(int) { return 8; }
-__host__ __device__ constexpr int warp_tokens(int) { return 16; }
+__host__ __device__ constexpr int warp_tokens(int, bool fp8) { return fp8 ? 32 : 16; }
 
 // ------------------------------------------------------------------ load balance state
 // In the adaptive mode a slice's size follows what the previous call on this
@@ -142,7 +145,7 @@ __host__ __device__ inline int comb_stride(int D, int G) { return int(align_up(u
 __host__ __device__ inline CtaLayout cta_layout(int D, int G, int es, int hg, int sub, int nst, int B)
 {
     CtaLayout l;
-    const int toks = warp_tokens(G) * sub;
+    const int toks = warp_tokens(G, es == 1) * sub;
     l.kv_bytes = uint32_t(toks * hg * D * es);
     l.stage_bytes = align_up(2 * l.kv_bytes, 1024);  // stages start on the 1024-byte swizzle period
     l.q_bytes = align_up(uint32_t(hg * G * D * 2), 128);
@@ -319,6 +322,8 @@ struct Tc {
     static constexpr int NCP = ROWB / 32;               // 16-byte chunk pairs per row (one ldmatrix.x4 each)
     static constexpr int KS = D / 16;                   // k-steps of the score product
     static constexpr int MT = D / 16;                   // m-tiles of the output product
+    static constexpr int NT = FP8 ? 2 : 1;              // 16-token sub-tiles of a warp's tile
+    static constexpr int TW = 16 * NT;                  // tokens of a warp's tile (warp_tokens)
 };
 
 __host__ __device__ constexpr int row_bytes_smem(int D, int es) { return D * es >= 128 ? 128 : 64; }
@@ -330,26 +335,30 @@ __device__ __forceinline__ uint32_t swizzled_chunk(uint32_t c, uint32_t R)
 }
 
 // Byte offsets, from a stage's K (or V) region, of the 16-byte row pieces this
-// lane hands to ldmatrix for the warp's 16 tokens (token j * 16 + tl of the
-// unit): tl = 8 * (lane / 16) + lane % 8, chunk 2i + (lane / 8) % 2 of the row.
-// Matrix q of an .x4 load is then (tokens 0-7 | 8-15) x (chunk 2i | 2i + 1)
-// for q = 0 (0-7, 2i), 1 (0-7, 2i+1), 2 (8-15, 2i), 3 (8-15, 2i+1).
+// lane hands to ldmatrix for sub-tile st of the warp's tile (token
+// j * TW + 16 st + tl of the unit): tl = 8 * (lane / 16) + lane % 8, chunk
+// 2i + (lane / 8) % 2 of the row.  Matrix q of an .x4 load is then
+// (tokens 0-7 | 8-15 of the sub-tile) x (chunk 2i | 2i + 1) for q = 0 (0-7, 2i),
+// 1 (0-7, 2i+1), 2 (8-15, 2i), 3 (8-15, 2i+1).
 template <int D, bool FP8>
-__device__ __forceinline__ void lane_offsets(uint32_t (&off)[Tc<D, FP8>::NCP], int lane, int j, int h, int hg,
-                                             int boxtok)
+__device__ __forceinline__ void lane_offsets(uint32_t (&off)[Tc<D, FP8>::NT][Tc<D, FP8>::NCP], int lane, int j,
+                                             int h, int hg, int boxtok)
 {
     using T = Tc<D, FP8>;
     const int tl = ((lane >> 4) << 3) | (lane & 7), e = (lane >> 3) & 1;
-    const int t = j * 16 + tl;
     const int lg = __ffs(boxtok) - 1;
-    const int bi = t >> lg, r = t & (boxtok - 1);
     const uint32_t box_bytes = uint32_t(boxtok * hg * T::ROWB);
 #pragma unroll
-    for (int i = 0; i < T::NCP; ++i) {
-        const int gc = 2 * i + e;
-        const int pp = gc / (T::RB / 16), cc = gc % (T::RB / 16);
-        const uint32_t R = uint32_t((h * T::NP + pp) * boxtok + r);
-        off[i] = uint32_t(bi) * box_bytes + R * T::RB + (swizzled_chunk<T::RB>(uint32_t(cc), R) << 4);
+    for (int st = 0; st < T::NT; ++st) {
+        const int t = j * T::TW + 16 * st + tl;
+        const int bi = t >> lg, r = t & (boxtok - 1);
+#pragma unroll
+        for (int i = 0; i < T::NCP; ++i) {
+            const int gc = 2 * i + e;
+            const int pp = gc / (T::RB / 16), cc = gc % (T::RB / 16);
+            const uint32_t R = uint32_t((h * T::NP + pp) * boxtok + r);
+            off[st][i] = uint32_t(bi) * box_bytes + R * T::RB + (swizzled_chunk<T::RB>(uint32_t(cc), R) << 4);
+        }
     }
 }
 
@@ -378,69 +387,86 @@ __device__ __forceinline__ uint32_t f16x2_sat(float lo, float hi)
     return h;
 }
 
-// One 16-token tile of one (sequence, kv head) for its G query heads
-// (virtual heads) on the tensor cores, m16n8k16 with fp32 accumulators:
+// One warp tile (NT sub-tiles of 16 tokens) of one (sequence, kv head) for its
+// G query heads (virtual heads) on the tensor cores, m16n8k16 with fp32
+// accumulators:
 //   S^T = Q K^T    rows: query heads (row g = lane / 4; rows G..15 are zero),
 //                  columns: 8 tokens per n-tile, k: head dims;
 //   P = 2^(S - m)  the online-softmax weights of the thread's row;
 //   O^T += V^T P^T rows: head dims, columns: query heads, k: tokens.
-// The S^T accumulator fragment of the two n-tiles is, register for register,
-// the P^T operand fragment of the second product, so P never leaves the
-// registers.  kb / vb: shared addresses of the stage's K and V regions.  lim:
-// tokens below it count for this thread's row (causal bound of its query);
-// TAIL: tokens from `valid` on are not the sequence's (their rows may hold
-// anything, even NaN), so their V values are zeroed before the product.
-// E4M3 caches run the products in f16 (every E4M3 value is exact in f16, and
-// so is every bf16 query element of magnitude 2^-14 .. 65504; smaller ones
-// keep f16's subnormal steps of 2^-24, larger ones saturate at 65504); the
-// kv head's K scale is in ksc, its V scale is applied by the caller.
+// The S^T accumulator fragment of a sub-tile's two n-tiles is, register for
+// register, the P^T operand fragment of its output product, so P never leaves
+// the registers.  kb / vb: shared addresses of the stage's K and V regions.
+// lim: tokens (from the tile's first) below it count for this thread's row
+// (the causal bound of its query); TAIL: tokens from `valid` on are not the
+// sequence's (their rows may hold anything, even NaN), so their V values are
+// zeroed before the product.  E4M3 caches run the products in f16 (every
+// E4M3 value is exact in f16, and so is every bf16 query element of
+// magnitude 2^-14 .. 65504; smaller ones keep f16's subnormal steps of 2^-24,
+// larger ones saturate at 65504); the kv head's K scale is in ksc, its V
+// scale is applied by the caller.
 template <int D, bool FP8, bool TAIL>
-__device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb, const uint32_t (&off)[Tc<D, FP8>::NCP],
+__device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
+                                            const uint32_t (&off)[Tc<D, FP8>::NT][Tc<D, FP8>::NCP],
                                             const uint32_t (&qa)[Tc<D, FP8>::KS][2], float ksc, int lim, int valid,
                                             float &m, float &l, float (&o)[Tc<D, FP8>::MT][4], int lane)
 {
     using T = Tc<D, FP8>;
+    constexpr int NT = T::NT;
+    constexpr int CH = NT == 1 ? 2 : 1;  // accumulation chains per n-tile (bf16: halves the MMA dependency depth)
     const int r4 = lane & 3;
-    float sa[2][2][4];  // [chain][n-tile][fragment]: two accumulation chains halve the MMA dependency depth
+    float sa[NT][CH][2][4];  // [sub-tile][chain][n-tile][fragment]
 #pragma unroll
-    for (int c = 0; c < 2; ++c)
+    for (int st = 0; st < NT; ++st)
+#pragma unroll
+        for (int c = 0; c < CH; ++c)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sa[st][c][nt][e] = 0.f;
+#pragma unroll
+    for (int i = 0; i < T::NCP; ++i) {
+#pragma unroll
+        for (int st = 0; st < NT; ++st) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(kb + off[st][i], r0, r1, r2, r3);
+            if constexpr (!FP8) {
+                // chunks 2i, 2i+1 = dims 16i..16i+15 = k-step i; r0/r1 tokens 0-7, r2/r3 tokens 8-15
+                mma_bf16_16816(sa[st][i % CH][0], qa[i][0], 0u, qa[i][1], 0u, r0, r1);
+                mma_bf16_16816(sa[st][i % CH][1], qa[i][0], 0u, qa[i][1], 0u, r2, r3);
+            } else {
+                // chunk 2i (2i+1) = k-step 2i (2i+1); a register holds four codes 4r..4r+3 of a
+                // token: dims (4r, 4r+1) are k-slots (2r, 2r+1), dims (4r+2, 4r+3) k-slots (2r+8, 2r+9)
+                uint32_t b[4][2];
+                e4m3x4_to_f16x2x2(r0, b[0][0], b[0][1]);
+                e4m3x4_to_f16x2x2(r1, b[1][0], b[1][1]);
+                e4m3x4_to_f16x2x2(r2, b[2][0], b[2][1]);
+                e4m3x4_to_f16x2x2(r3, b[3][0], b[3][1]);
+                mma_f16_16816(sa[st][0][0], qa[2 * i][0], 0u, qa[2 * i][1], 0u, b[0][0], b[0][1]);
+                mma_f16_16816(sa[st][0][1], qa[2 * i][0], 0u, qa[2 * i][1], 0u, b[2][0], b[2][1]);
+                mma_f16_16816(sa[st][CH - 1][0], qa[2 * i + 1][0], 0u, qa[2 * i + 1][1], 0u, b[1][0], b[1][1]);
+                mma_f16_16816(sa[st][CH - 1][1], qa[2 * i + 1][0], 0u, qa[2 * i + 1][1], 0u, b[3][0], b[3][1]);
+            }
+        }
+    }
+    // the thread's scores: row g, tokens 16 st + 8 nt + 2 r4 + e (fragment elements c0, c1 of n-tile nt)
+    float x[NT * 4];
+    bool ok[NT * 4];
+#pragma unroll
+    for (int st = 0; st < NT; ++st)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sa[c][nt][e] = 0.f;
+            for (int e = 0; e < 2; ++e) {
+                const int k = 4 * st + 2 * nt + e;
+                float sum = sa[st][0][nt][e];
+                if constexpr (CH == 2) sum += sa[st][1][nt][e];
+                ok[k] = 16 * st + 8 * nt + 2 * r4 + e < lim;
+                x[k] = ok[k] ? sum * ksc : -INFINITY;
+            }
+    float mx = x[0];
 #pragma unroll
-    for (int i = 0; i < T::NCP; ++i) {
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4(kb + off[i], r0, r1, r2, r3);
-        if constexpr (!FP8) {
-            // chunks 2i, 2i+1 = dims 16i..16i+15 = k-step i; r0/r1 tokens 0-7, r2/r3 tokens 8-15
-            mma_bf16_16816(sa[i & 1][0], qa[i][0], 0u, qa[i][1], 0u, r0, r1);
-            mma_bf16_16816(sa[i & 1][1], qa[i][0], 0u, qa[i][1], 0u, r2, r3);
-        } else {
-            // chunk 2i (2i+1) = k-step 2i (2i+1); a register holds four codes 4r..4r+3 of a token:
-            // dims (4r, 4r+1) are k-slots (2r, 2r+1), dims (4r+2, 4r+3) k-slots (2r+8, 2r+9)
-            mma_f16_16816(sa[0][0], qa[2 * i][0], 0u, qa[2 * i][1], 0u, e4m3x2_to_f16x2(r0),
-                          e4m3x2_to_f16x2(r0 >> 16));
-            mma_f16_16816(sa[0][1], qa[2 * i][0], 0u, qa[2 * i][1], 0u, e4m3x2_to_f16x2(r2),
-                          e4m3x2_to_f16x2(r2 >> 16));
-            mma_f16_16816(sa[1][0], qa[2 * i + 1][0], 0u, qa[2 * i + 1][1], 0u, e4m3x2_to_f16x2(r1),
-                          e4m3x2_to_f16x2(r1 >> 16));
-            mma_f16_16816(sa[1][1], qa[2 * i + 1][0], 0u, qa[2 * i + 1][1], 0u, e4m3x2_to_f16x2(r3),
-                          e4m3x2_to_f16x2(r3 >> 16));
-        }
-    }
-    // the thread's scores: row g, tokens 8 nt + 2 r4 + e (fragment elements c0, c1 of n-tile nt)
-    float x[4];
-    bool ok[4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int k = 2 * nt + e;
-            ok[k] = 8 * nt + 2 * r4 + e < lim;
-            x[k] = ok[k] ? (sa[0][nt][e] + sa[1][nt][e]) * ksc : -INFINITY;
-        }
-    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    for (int k = 1; k < NT * 4; ++k) mx = fmaxf(mx, x[k]);
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));  // the four threads of a row
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
     // Online softmax (m, l, acc).  The running max only moves when some score passes it by more
@@ -460,41 +486,51 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb, const uint
             o[mt][3] *= a1;
         }
     }
-    float pr[4];
+    float pr[NT * 4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) pr[k] = ok[k] ? ex2(x[k] - m) : 0.f;
-    l += (pr[0] + pr[1]) + (pr[2] + pr[3]);
-    const uint32_t pb0 = FP8 ? f16x2_of(pr[0], pr[1]) : pack_bf16x2(pr[0], pr[1]);
-    const uint32_t pb1 = FP8 ? f16x2_of(pr[2], pr[3]) : pack_bf16x2(pr[2], pr[3]);
+    for (int k = 0; k < NT * 4; ++k) pr[k] = ok[k] ? ex2(x[k] - m) : 0.f;
+    float ps = 0.f;
+#pragma unroll
+    for (int k = 0; k < NT * 4; ++k) ps += pr[k];
+    l += ps;
 
-    // transposed V tiles: the low half of a register is token 2 r4 (8 + 2 r4), the high half the next one
-    uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
-    if constexpr (TAIL) {
-        keep0 = (2 * r4 < valid ? 0x0000ffffu : 0u) | (2 * r4 + 1 < valid ? 0xffff0000u : 0u);
-        keep1 = (2 * r4 + 8 < valid ? 0x0000ffffu : 0u) | (2 * r4 + 9 < valid ? 0xffff0000u : 0u);
-    }
 #pragma unroll
-    for (int i = 0; i < T::NCP; ++i) {
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4_t(vb + off[i], r0, r1, r2, r3);
+    for (int st = 0; st < NT; ++st) {
+        const uint32_t pb0 = FP8 ? f16x2_of(pr[4 * st], pr[4 * st + 1]) : pack_bf16x2(pr[4 * st], pr[4 * st + 1]);
+        const uint32_t pb1 =
+            FP8 ? f16x2_of(pr[4 * st + 2], pr[4 * st + 3]) : pack_bf16x2(pr[4 * st + 2], pr[4 * st + 3]);
+        // transposed V tiles: the low half of a register is token 2 r4 (8 + 2 r4) of the sub-tile, the
+        // high half the next one
+        uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
         if constexpr (TAIL) {
-            r0 &= keep0;
-            r1 &= keep0;
-            r2 &= keep1;
-            r3 &= keep1;
+            const int v0 = valid - 16 * st;
+            keep0 = (2 * r4 < v0 ? 0x0000ffffu : 0u) | (2 * r4 + 1 < v0 ? 0xffff0000u : 0u);
+            keep1 = (2 * r4 + 8 < v0 ? 0x0000ffffu : 0u) | (2 * r4 + 9 < v0 ? 0xffff0000u : 0u);
         }
-        if constexpr (!FP8) {
-            // m-tile i: dims 16i + g (r0: tokens 0-7, r2: tokens 8-15) and 16i + 8 + g (r1, r3)
-            mma_bf16_16816(o[i], r0, r1, r2, r3, pb0, pb1);
-        } else {
-            // a register holds (token 2r4: dims 2g, 2g+1 | token 2r4+1: dims 2g, 2g+1) of a 16-dim
-            // chunk; the byte permute pairs the two tokens per dim: low half dim 2g, high half dim 2g+1
-            const uint32_t x0 = __byte_perm(r0, 0u, 0x3120), x1 = __byte_perm(r1, 0u, 0x3120);
-            const uint32_t x2 = __byte_perm(r2, 0u, 0x3120), x3 = __byte_perm(r3, 0u, 0x3120);
-            mma_f16_16816(o[2 * i], e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x2),
-                          e4m3x2_to_f16x2(x2 >> 16), pb0, pb1);
-            mma_f16_16816(o[2 * i + 1], e4m3x2_to_f16x2(x1), e4m3x2_to_f16x2(x1 >> 16), e4m3x2_to_f16x2(x3),
-                          e4m3x2_to_f16x2(x3 >> 16), pb0, pb1);
+#pragma unroll
+        for (int i = 0; i < T::NCP; ++i) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_t(vb + off[st][i], r0, r1, r2, r3);
+            if constexpr (TAIL) {
+                r0 &= keep0;
+                r1 &= keep0;
+                r2 &= keep1;
+                r3 &= keep1;
+            }
+            if constexpr (!FP8) {
+                // m-tile i: dims 16i + g (r0: tokens 0-7, r2: tokens 8-15) and 16i + 8 + g (r1, r3)
+                mma_bf16_16816(o[i], r0, r1, r2, r3, pb0, pb1);
+            } else {
+                // a register holds (token 2r4: dims 2g, 2g+1 | token 2r4+1: dims 2g, 2g+1) of a 16-dim
+                // chunk; the byte permute pairs the two tokens per dim: low half dim 2g, high half dim 2g+1
+                uint32_t a[4][2];
+                e4m3x4_to_f16x2x2(__byte_perm(r0, 0u, 0x3120), a[0][0], a[0][1]);
+                e4m3x4_to_f16x2x2(__byte_perm(r1, 0u, 0x3120), a[1][0], a[1][1]);
+                e4m3x4_to_f16x2x2(__byte_perm(r2, 0u, 0x3120), a[2][0], a[2][1]);
+                e4m3x4_to_f16x2x2(__byte_perm(r3, 0u, 0x3120), a[3][0], a[3][1]);
+                mma_f16_16816(o[2 * i], a[0][0], a[0][1], a[2][0], a[2][1], pb0, pb1);
+                mma_f16_16816(o[2 * i + 1], a[1][0], a[1][1], a[3][0], a[3][1], pb0, pb1);
+            }
         }
     }
 }
@@ -1076,7 +1112,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     const int h = warp / p.sub, j = warp - h * p.sub;  // kv head in the group, token slice of the unit
     const int g8 = lane >> 2, r4 = lane & 3;           // fragment row group and column pair of the thread
     const int home = sh[0];
-    uint32_t off[TC::NCP];
+    uint32_t off[TC::NT][TC::NCP];
     lane_offsets<D, FP8>(off, lane, j, h, p.hg, p.boxtok);
     const uint32_t stage_addr = smem_u32(stage0);
     // several queries per stream: the query of row g8 sees `shift` fewer of the sequence's last tokens
@@ -1136,12 +1172,12 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
             ++segs;
             u_first = mt.u;
         }
-        const int tok0 = mt.u * p.toks + j * 16;
-        const int valid = min(16, mt.L - tok0);
+        const int tok0 = mt.u * p.toks + j * TC::TW;
+        const int valid = min(TC::TW, mt.L - tok0);
         if (valid > 0) {
             const uint32_t kb = stage_addr + uint32_t(s) * lay.stage_bytes;
             const int lim = min(valid, mt.L - tok0 - shift);
-            if (valid == 16)
+            if (valid == TC::TW)
                 attend_tile<D, FP8, false>(kb, kb + lay.kv_bytes, off, qa, ksc, lim, valid, m, l, o, lane);
             else
                 attend_tile<D, FP8, true>(kb, kb + lay.kv_bytes, off, qa, ksc, lim, valid, m, l, o, lane);

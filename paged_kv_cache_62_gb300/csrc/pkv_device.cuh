@@ -173,15 +173,15 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two E4M3 codes (the low byte is element 0) -> f16 pair (element 0 in the low half); exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
+// Four E4M3 codes (byte e is element e) -> f16 pairs (elements 0, 1) and
+// (elements 2, 3), the lower element in the low half; exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t codes, uint32_t &lo, uint32_t &hi)
 {
-    uint32_t h;
-    asm("{.reg .b16 c;\n\t"
-        "cvt.u16.u32 c, %1;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, c;}"
-        : "=r"(h) : "r"(two_codes));
-    return h;
+    asm("{.reg .b16 a, b;\n\t"
+        "mov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, b;}"
+        : "=r"(lo), "=r"(hi) : "r"(codes));
 }
 
 // D = A (16x16 bf16, row) * B (16x8 bf16, col) + D, fp32 accumulators.
