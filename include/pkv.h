@@ -292,15 +292,17 @@ PKV_API pkv_status pkv_paged_decode_noalloc(const uint16_t *q, const uint16_t *k
  *                 sequence has.  n > 0: every sequence has exactly n
  *                 (rows b * n .. b * n + n - 1, num_rows = num_seqs * n;
  *                 cu_seqlens_q may be NULL) -- a speculative-decoding verify
- *                 step, say.  Then, when n * (num_q_heads / num_kv_heads) <= 8,
- *                 the n queries of a sequence share one pass over its keys:
- *                 each K/V row is read once for all of them.
+ *                 step, say.
+ * Consecutive queries of a sequence share passes over its keys: with
+ * G = num_q_heads / num_kv_heads, chunks of Q = max(1, 8 / G) queries (the
+ * last one of a sequence possibly shorter) each read the keys the chunk's
+ * last query sees once for all its Q * G (query, head) pairs, every query
+ * keeping its own causal bound; a decode row is a chunk of one.  So a
+ * sequence of n new tokens over L cached ones streams about
+ * (n / Q) * L key rows, not n * L.
  * Rows inconsistent with the offsets (n > L, rows outside every sequence's
  * range) give zeros and PKV_ERR_CONTEXT_RANGE.  num_rows <= PKV_MAX_SEQS;
- * other limits, num_workers and errors as pkv_paged_decode.  Otherwise each
- * query row streams its own keys (the decode kernel, one row per query):
- * right for mixed batches with short runs of new tokens; a long prefill
- * re-reads its prefix once per query row.
+ * other limits, num_workers and errors as pkv_paged_decode.
  */
 PKV_API size_t pkv_paged_attention_workspace_size(int32_t num_rows, int32_t num_q_heads,
                                                   int32_t num_kv_heads, int32_t head_dim);

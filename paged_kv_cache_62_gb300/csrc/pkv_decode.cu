@@ -15,13 +15,15 @@ extern "C" size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_
 }
 
 // Shared by the bf16 and the E4M3 entry points (k_scale / v_scale: the
-// latter's per-kv-head scales, device arrays).  qn > 1: every sequence has qn
-// new tokens whose queries (rows b * qn + i of q / out) share the sequence's
-// K/V stream as qn * G virtual heads of a kv head; context_lens are then the
-// sequences' whole lengths.
+// latter's per-kv-head scales, device arrays).  qn > 1: entry b holds up to qn
+// queries that share its K/V stream as qn * G virtual heads of a kv head --
+// with row_cnt null, every entry is a sequence with qn new tokens (q / out rows
+// b * qn + i; context_lens the sequences' whole lengths); otherwise entry b
+// holds row_cnt[b] queries at rows b + i (row_seq[b]: its sequence,
+// context_lens[b]: the length its last query sees).
 static pkv_status decode_call(bool fp8, int32_t qn, const uint16_t *q, const void *k_cache, const void *v_cache,
                               const float *k_scale, const float *v_scale, const int32_t *row_seq,
-                              const int32_t *block_tables,
+                              const int32_t *row_cnt, const int32_t *block_tables,
                               int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                               int32_t num_blocks, int32_t max_context_len, float scale, uint16_t *out,
@@ -90,6 +92,8 @@ static pkv_status decode_call(bool fp8, int32_t qn, const uint16_t *q, const voi
     p.row_seq = row_seq;
     p.qn = qn;
     p.gq = gq;
+    p.row_cnt = row_cnt;
+    p.qstride = row_cnt ? 1 : qn;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
     a.device = dev.device;
@@ -112,10 +116,10 @@ extern "C" pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cach
                                        void *workspace, size_t workspace_bytes, int32_t num_workers,
                                        int32_t *err_word, pkv_stream_t stream)
 {
-    return decode_call(false, 1, q, k_cache, v_cache, nullptr, nullptr, nullptr, block_tables, max_blocks_per_seq,
-                       context_lens,
-                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale,
-                       out, workspace, workspace_bytes, num_workers, err_word, stream);
+    return decode_call(false, 1, q, k_cache, v_cache, nullptr, nullptr, nullptr, nullptr, block_tables,
+                       max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, max_context_len, scale, out, workspace, workspace_bytes, num_workers, err_word,
+                       stream);
 }
 
 extern "C" pkv_status pkv_paged_decode_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
@@ -127,8 +131,8 @@ extern "C" pkv_status pkv_paged_decode_fp8(const uint16_t *q, const uint8_t *k_c
                                            size_t workspace_bytes, int32_t num_workers, int32_t *err_word,
                                            pkv_stream_t stream)
 {
-    return decode_call(true, 1, q, k_cache, v_cache, k_scale, v_scale, nullptr, block_tables, max_blocks_per_seq,
-                       context_lens,
+    return decode_call(true, 1, q, k_cache, v_cache, k_scale, v_scale, nullptr, nullptr, block_tables,
+                       max_blocks_per_seq, context_lens,
                        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale,
                        out, workspace, workspace_bytes, num_workers, err_word, stream);
 }
@@ -207,17 +211,22 @@ namespace pkv {
 
 // Query row r = cu_seqlens_q[b] + i of sequence b (n = cu_seqlens_q[b+1] -
 // cu_seqlens_q[b] new tokens, L = context_lens[b] in the cache) sits at
-// position L - n + i: it reads sequence b's table with context length
-// L - n + i + 1.  One thread per row finds its sequence by binary search over
-// cu_seqlens_q, so every row gets a sequence in [0, num_seqs) even when the
-// offsets are inconsistent; such rows (not inside their sequence's range,
-// n > L, offsets not starting at 0) get length 0 (zero output) and
-// PKV_ERR_CONTEXT_RANGE.
-// With cu_seqlens_q null, every sequence has new_per_seq rows (row r belongs to
-// sequence r / new_per_seq).
+// position L - n + i: it sees the L - n + i + 1 keys before it.  The rows of
+// a sequence are cut into chunks of up to qg consecutive queries that share
+// one K/V stream; a chunk is entry r of the decode kernel, r the row of its
+// first query: row_seq[r] = b, row_cnt[r] = its query count, row_len[r] = the
+// keys its last query sees.  Rows that start no chunk get row_cnt = 0 and
+// row_len = 0 (no work, no output).  One thread per row finds its sequence by
+// binary search over cu_seqlens_q, so every row gets a sequence in
+// [0, num_seqs) even when the offsets are inconsistent; such rows (not inside
+// their sequence's range, n > L, offsets not starting at 0) are entries of
+// their own or their chunk's with length 0 (zero output) and set
+// PKV_ERR_CONTEXT_RANGE.  With cu_seqlens_q null, every sequence has
+// new_per_seq rows (row r belongs to sequence r / new_per_seq).
 __global__ void expand_rows_kernel(const int32_t *__restrict__ cu_seqlens_q, int32_t new_per_seq,
                                    const int32_t *__restrict__ context_lens, int32_t num_seqs, int32_t num_rows,
-                                   int32_t *__restrict__ row_seq, int32_t *__restrict__ row_len, int32_t *err)
+                                   int32_t qg, int32_t *__restrict__ row_seq, int32_t *__restrict__ row_len,
+                                   int32_t *__restrict__ row_cnt, int32_t *err)
 {
     griddep_launch_dependents();
     griddep_wait();
@@ -241,14 +250,28 @@ __global__ void expand_rows_kernel(const int32_t *__restrict__ cu_seqlens_q, int
         r1 = r0 + new_per_seq;
     }
     const int32_t L = __ldg(context_lens + lo);
-    const int32_t n = r1 - r0;
-    const bool ok = (!cu_seqlens_q || __ldg(cu_seqlens_q) == 0) && r0 <= r && r < r1 && n <= L;
+    const int32_t n = r1 - r0, i = r - r0;
+    const bool inside = r0 <= r && r < r1;
+    const bool ok = (!cu_seqlens_q || __ldg(cu_seqlens_q) == 0) && inside && n <= L;
     if (!ok) flag_error(err, PKV_ERR_CONTEXT_RANGE);
+    int32_t cnt = 1, len = 0;  // a row outside its sequence's range: an entry of its own, zero output
+    if (inside) {
+        cnt = i % qg == 0 ? min(qg, n - i) : 0;
+        len = ok && cnt > 0 ? L - n + i + cnt : 0;
+    }
     row_seq[r] = lo;
-    row_len[r] = ok ? L - n + (r - r0) + 1 : 0;
+    row_len[r] = len;
+    row_cnt[r] = cnt;
 }
 
 inline size_t rows_bytes(int32_t num_rows) { return align256(size_t(num_rows) * 4); }
+
+// Queries per chunk: as many as keep the chunk's qg * G virtual heads within
+// the 8 rows of the MMA tile that the kernel uses.
+inline int32_t chunk_queries(int32_t num_q_heads, int32_t num_kv_heads)
+{
+    return std::max(1, 8 / (num_q_heads / num_kv_heads));
+}
 
 }  // namespace pkv
 
@@ -257,11 +280,12 @@ extern "C" size_t pkv_paged_attention_workspace_size(int32_t num_rows, int32_t n
 {
     const size_t base = pkv_paged_decode_workspace_size(num_rows, num_q_heads, num_kv_heads, head_dim);
     if (base == 0) return 0;
-    size_t need = align256(base) + 2 * rows_bytes(num_rows);  // one row per query
-    // queries sharing a stream: qn * G virtual heads over at most num_rows / qn sequences
-    for (int32_t qn = 2; (num_q_heads / num_kv_heads) * qn <= 8; ++qn)
-        need = std::max(need, pkv_paged_decode_workspace_size(num_rows, num_q_heads * qn, num_kv_heads, head_dim));
-    return need;
+    // decode workspace for entries of up to qg queries (qg * G virtual heads), one entry per row,
+    // then the three row arrays
+    size_t dec = base;
+    for (int32_t qn = 2; qn <= chunk_queries(num_q_heads, num_kv_heads); ++qn)
+        dec = std::max(dec, pkv_paged_decode_workspace_size(num_rows, num_q_heads * qn, num_kv_heads, head_dim));
+    return align256(dec) + 3 * rows_bytes(num_rows);
 }
 
 extern "C" pkv_status pkv_paged_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
@@ -281,27 +305,31 @@ extern "C" pkv_status pkv_paged_attention(const uint16_t *q, const uint16_t *k_c
     const size_t need = pkv_paged_attention_workspace_size(num_rows, num_q_heads, num_kv_heads, head_dim);
     if (need == 0) return num_rows > PKV_MAX_SEQS ? PKV_EUNSUPPORTED : PKV_EINVAL;
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PKV_EWORKSPACE;
-    if (new_per_seq > 1 && (num_q_heads / num_kv_heads) * new_per_seq <= 8)
-        // the n new tokens of a sequence share its K/V stream: read once, n * G virtual heads
-        return decode_call(false, new_per_seq, q, k_cache, v_cache, nullptr, nullptr, nullptr, block_tables,
-                           max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                           block_size, num_blocks, max_context_len, scale, out, workspace, workspace_bytes,
-                           num_workers, err_word, stream);
-    // the rows' (sequence, length) arrays sit after the decode workspace
+    const int32_t qg = chunk_queries(num_q_heads, num_kv_heads);
+    if (new_per_seq > 1 && new_per_seq <= qg)
+        // every sequence's n new tokens share its K/V stream: read once, n * G virtual heads
+        return decode_call(false, new_per_seq, q, k_cache, v_cache, nullptr, nullptr, nullptr, nullptr,
+                           block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                           head_dim, block_size, num_blocks, max_context_len, scale, out, workspace,
+                           workspace_bytes, num_workers, err_word, stream);
+    // chunks of up to qg queries of a sequence, one entry per row; the row arrays sit after the
+    // decode workspace
     uint8_t *wsb = static_cast<uint8_t *>(workspace);
-    const size_t dec_bytes = align256(pkv_paged_decode_workspace_size(num_rows, num_q_heads, num_kv_heads, head_dim));
+    const size_t dec_bytes = need - 3 * rows_bytes(num_rows);
     int32_t *row_seq = reinterpret_cast<int32_t *>(wsb + dec_bytes);
     int32_t *row_len = reinterpret_cast<int32_t *>(wsb + dec_bytes + rows_bytes(num_rows));
+    int32_t *row_cnt = reinterpret_cast<int32_t *>(wsb + dec_bytes + 2 * rows_bytes(num_rows));
     const cudaError_t e = launch_pdl(expand_rows_kernel, dim3((num_rows + 255) / 256), dim3(256), 0,
                                      reinterpret_cast<cudaStream_t>(stream), new_per_seq > 0 ? nullptr : cu_seqlens_q,
-                                     new_per_seq, context_lens, num_seqs, num_rows, row_seq, row_len, err_word);
+                                     new_per_seq, context_lens, num_seqs, num_rows, qg, row_seq, row_len, row_cnt,
+                                     err_word);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return cuda_fail("expand_rows_kernel launch", e);
     }
     const pkv_status st = launch_status("expand_rows_kernel launch");
     if (st != PKV_OK) return st;
-    return decode_call(false, 1, q, k_cache, v_cache, nullptr, nullptr, row_seq, block_tables, max_blocks_per_seq,
-                       row_len, num_rows, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
-                       max_context_len, scale, out, workspace, dec_bytes, num_workers, err_word, stream);
+    return decode_call(false, qg, q, k_cache, v_cache, nullptr, nullptr, row_seq, row_cnt, block_tables,
+                       max_blocks_per_seq, row_len, num_rows, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, max_context_len, scale, out, workspace, dec_bytes, num_workers, err_word, stream);
 }

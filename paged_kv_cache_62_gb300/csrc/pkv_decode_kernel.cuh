@@ -111,19 +111,19 @@ struct DecodeParams {
     const int32_t *row_seq;          // several query rows per sequence: row -> the sequence whose table it
                                      // reads (null: row b reads table row b)
     // Several new tokens per sequence sharing one K/V stream: the kernel's G "heads" of a kv head are
-    // qn queries x gq query heads (virtual head hh = query hh / gq, head hh % gq); query i of sequence b
-    // is q / out row b * qn + i and sees the keys before position L - qn + i + 1.  Decode: qn = 1, gq = G.
-    int32_t qn, gq;
-    // Shape of the cache tensor maps: 0 = one 4-D copy per box and cache (dims: row chunk, token, row
-    // part, kv head); 1 = one 3-D copy per box, cache, kv head and row part (dims: row chunk,
-    // kv head x part, token), where the driver does not take the 4-D map's stride order.
-    int32_t split_copies;
+    // qn queries x gq query heads (virtual head hh = query hh / gq, head hh % gq).  Entry b holds
+    // cnt <= qn queries (row_cnt[b], or qn where row_cnt is null); its query i is q / out row
+    // b * qstride + i and sees the keys before position L - cnt + i + 1 (L: entry b's context length).
+    // Decode: qn = 1, gq = G, qstride = 1.
+    int32_t qn, gq, qstride;
+    const int32_t *row_cnt;
 };
 
 // What the producer tells the consumers about the unit in a stage.
 struct alignas(16) UnitMeta {
     int32_t b, g, u, n;            // unit u of the n units of (b, group g); b < 0: no more work
-    int32_t L, flags, slice, pad;  // context length of b, kFirst | kLast | kSliceEnd, slice of the unit
+    int32_t L, flags, slice, cnt;  // context length of b, kFirst | kLast | kSliceEnd, slice of the unit,
+                                   // queries of entry b
 };
 constexpr int kFirst = 1;     // first unit of (b, g) in this slice
 constexpr int kLast = 2;      // last unit of (b, g) in this slice
@@ -263,7 +263,9 @@ static __device__ void unit_prefix_scan(const DecodeParams &p, int32_t *scan, in
     for (int i = lo; i < hi; ++i) {
         const int32_t len = __ldg(p.context_lens + i);
         int32_t n = 0;
-        if (len < 0 || len > p.len_limit) {
+        // several queries of a sequence sharing a stream need at least one key each (the row
+        // arrays of a chunked call are built that way; a same-n call can break it)
+        if (len < 0 || len > p.len_limit || (!p.row_cnt && p.qn > 1 && len < p.qn)) {
             if (blockIdx.x == 0) flag_error(p.err, PKV_ERR_CONTEXT_RANGE);
         } else {
             n = (len + p.toks - 1) / p.toks;
@@ -306,11 +308,13 @@ static __device__ void unit_prefix_scan(const DecodeParams &p, int32_t *scan, in
 // ample room, and most tiles skip the rescale entirely.
 constexpr float kRescaleSlack = 8.0f;
 
-// Stage layout.  The producer copies a cached row (one token, one kv head) as
-// NP parts of RB bytes, one TMA box per (box of boxtok tokens, kv head, part),
-// so the boxtok rows of a part are consecutive RB-byte rows of shared memory,
-// swizzled by the copy: 16-byte chunk c of row R lands at chunk c ^ (R & 7)
-// (128-byte rows) or c ^ ((R >> 1) & 3) (64-byte rows, 64-dim E4M3 caches).
+// Stage layout.  The producer copies the cached rows (one token, one kv head)
+// of a box of boxtok tokens and HG kv heads as NP parts of RB bytes each, one
+// 4-D TMA copy per box and cache landing as [kv head][part][token][RB bytes],
+// so the boxtok rows of a (kv head, part) are consecutive RB-byte rows of
+// shared memory, swizzled by the copy: 16-byte chunk c of row R lands at
+// chunk c ^ (R & 7) (128-byte rows) or c ^ ((R >> 1) & 3) (64-byte rows,
+// 64-dim E4M3 caches).
 // The chunks of eight consecutive tokens then sit in eight different bank
 // groups, and one ldmatrix reads them without a conflict.
 template <int D, bool FP8>
@@ -774,14 +778,15 @@ __device__ __forceinline__ int slice_of(const long long *bound, int nslots, long
 }
 
 // Merge the partial states of (b, kv head kvh) left by the non-empty slices
-// sf..sl, piece slots (s + sigma) * hg + h:
+// sf..sl, piece slots (s + sigma) * hg + h, and write the outputs of the
+// entry's nvh virtual heads that are queries:
 //   M = max m_i,  l = sum 2^(m_i - M) l_i,  out = sum 2^(m_i - M) acc_i / l
 // (the online-softmax algebra; m in log2 units).  The pieces were written by
 // other SMs, so they are read through L2 (ld.global.cg), BATCH pieces at a
 // time with independent loads, folded into a running (M, l, acc).
 template <int D, int G, bool FP8>
 __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long long *bound, int sf, int sl,
-                                             long long sigma, int h, int b, int kvh, int lane)
+                                             long long sigma, int h, int b, int kvh, int nvh, int lane)
 {
     constexpr int PER = D / 32;                           // output values per lane
     constexpr int BATCH = G <= 2 ? 4 : (G <= 7 ? 2 : 1);  // pieces loaded together (G = 8 would spill)
@@ -835,8 +840,9 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
     }
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
+        if (hh >= nvh) break;  // virtual heads past the entry's queries
         const float inv = (FP8 ? __ldg(p.v_scale + kvh) : 1.0f) / lsum[hh];
-        uint16_t *o = p.out + ((int64_t(b) * p.qn + hh / p.gq) * p.Hq + int64_t(kvh) * p.gq + hh % p.gq) * D +
+        uint16_t *o = p.out + ((int64_t(b) * p.qstride + hh / p.gq) * p.Hq + int64_t(kvh) * p.gq + hh % p.gq) * D +
                       lane * PER;
         if constexpr (PER == 4)
             *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16x2(a[hh][0] * inv, a[hh][1] * inv),
@@ -904,11 +910,14 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     unit_prefix_scan(p, scan, reinterpret_cast<int32_t *>(smem));
     const long long T = (long long)p.nhg * scan[p.B];
 
-    // Sequences without units (L == 0, or a rejected length) get zeros; CTAs share the job.
+    // Entries without units (L == 0, or a rejected length) get zeros in their query rows; CTAs
+    // share the job.
     for (int b = blockIdx.x; b < p.B; b += gridDim.x)
-        if (scan[b + 1] == scan[b])
-            for (int i = threadIdx.x; i < p.Hq * D / 8; i += blockDim.x)
-                reinterpret_cast<uint4 *>(p.out + int64_t(b) * p.Hq * D)[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (scan[b + 1] == scan[b]) {
+            const int rows = p.row_cnt ? __ldg(p.row_cnt + b) : p.qn;
+            uint4 *o = reinterpret_cast<uint4 *>(p.out + int64_t(b) * p.qstride * p.Hq * D);
+            for (int i = threadIdx.x; i < rows * p.Hq * D / 8; i += blockDim.x) o[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
 
     build_partition(p, gen, adaptive, nslots, T, bound, wts, red, bal_in);
 
@@ -937,10 +946,6 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         // ============================== producer warp ==============================
         const uint64_t policy = policy_evict_first();
         const uint32_t box_bytes = uint32_t(p.boxtok * p.hg * D * ES);
-        constexpr int NPART = Tc<D, FP8>::NP;
-        const int nsub = p.hg * NPART;                                  // copies per box and cache
-        const int nreq = p.nbox * nsub * 2;                             // copies per unit
-        const uint32_t part_bytes = uint32_t(p.boxtok * Tc<D, FP8>::RB);  // one (kv head, part) of a box
         uint32_t kk = 0, segs = 0;  // units issued, q-ring uses
         int rs = 0;                 // ring slot of unit kk (kk % nst, kept without a division)
         uint32_t rph = 0;           // parity of that slot's use (kk / nst) & 1
@@ -956,7 +961,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
             // context length) of box kb + j; `nxt` is loaded one batch ahead.  Two register sets,
             // because the scoreboard tracks a register for the whole warp.
             Walker iw = nunits > 0 ? walker_locate(scan, p.B, p.nhg, lo) : Walker{0, 0, 0, 1};
-            int32_t cur_e = -1, cur_L = 0, nxt_e = -1, nxt_L = 0;
+            int32_t cur_e = -1, cur_L = 0, cur_c = 1, nxt_e = -1, nxt_L = 0, nxt_c = 1;
             auto prefetch_batch = [&](long long kb) {  // boxes [kb, kb + 32) -> nxt, one per lane
                 const long long x = kb + lane;
                 if (x < nboxes) {
@@ -967,6 +972,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                     // the row and lets it go out together with the length's.
                     const int32_t blk = min(pos >> p.log2_bs, p.max_blocks - 1);
                     nxt_L = __ldg(p.context_lens + mine.b);
+                    nxt_c = p.row_cnt ? __ldg(p.row_cnt + mine.b) : p.qn;
                     const int32_t trow = p.row_seq ? __ldg(p.row_seq + mine.b) : mine.b;
                     nxt_e = __ldg(p.block_tables + (long long)trow * p.max_blocks + blk);
                 }
@@ -975,12 +981,14 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                 prefetch_batch(0);
                 cur_e = nxt_e;
                 cur_L = nxt_L;
+                cur_c = nxt_c;
             }
             for (long long k = 0; k < nunits; ++k) {
-                const long long kb0 = k * p.nbox;  // nbox is a power of two <= 16: batches start on units
+                const long long kb0 = k * p.nbox;  // nbox is a power of two <= 32: batches start on units
                 if ((kb0 & 31) == 0 && k > 0) {
                     cur_e = nxt_e;
                     cur_L = nxt_L;
+                    cur_c = nxt_c;
                     if (kb0 + 32 < nboxes) prefetch_batch(kb0 + 32);
                 }
                 const int s = rs;
@@ -990,6 +998,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                 }
                 const int src = int(kb0 & 31);
                 const int32_t len = __shfl_sync(kFull, cur_L, src);
+                const int32_t cnt = __shfl_sync(kFull, cur_c, src);
                 const int32_t e = __shfl_sync(kFull, cur_e, (src + lane) & 31);  // lane j: box j's entry
                 const int flags = ((k == 0 || iw.u == 0) ? kFirst : 0) |
                                   ((k == nunits - 1 || iw.u == iw.n - 1) ? kLast : 0) |
@@ -1001,8 +1010,8 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                         dead = true;
                         break;
                     }
-                    const uint32_t qb = uint32_t(p.hg * G * D * 2);
                     if (p.qn == 1) {  // the group's G * hg query rows are contiguous
+                        const uint32_t qb = uint32_t(p.hg * G * D * 2);
                         if (lane == 0) {
                             mbar_arrive_expect_tx(&qfull[qs], qb);
                             bulk_load(qbuf + qs * lay.q_bytes,
@@ -1010,14 +1019,15 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                                       &qfull[qs]);
                         }
                     } else {
-                        // qn queries: kv head h's virtual heads i * gq .. i * gq + gq - 1 come from row
-                        // b * qn + i; one copy of gq rows per (h, i), lane t copying pair t
-                        if (lane == 0) mbar_arrive_expect_tx(&qfull[qs], qb);
+                        // cnt queries: kv head h's virtual heads i * gq .. i * gq + gq - 1 come from row
+                        // b * qstride + i; one copy of gq rows per (h, i < cnt), lane t copying pair t
+                        // (the slots of virtual heads past cnt * gq are not loaded: the consumers zero them)
+                        if (lane == 0) mbar_arrive_expect_tx(&qfull[qs], uint32_t(p.hg * cnt * p.gq * D * 2));
                         __syncwarp();
-                        for (int t = lane; t < p.hg * p.qn; t += 32) {
-                            const int hh = t / p.qn, qi = t - hh * p.qn;
+                        for (int t = lane; t < p.hg * cnt; t += 32) {
+                            const int hh = t / cnt, qi = t - hh * cnt;
                             bulk_load(qbuf + qs * lay.q_bytes + size_t((hh * G + qi * p.gq) * D) * 2,
-                                      p.q + (((long long)iw.b * p.qn + qi) * p.Hq +
+                                      p.q + (((long long)iw.b * p.qstride + qi) * p.Hq +
                                              (long long)(iw.g * p.hg + hh) * p.gq) * D,
                                       uint32_t(p.gq * D * 2), &qfull[qs]);
                         }
@@ -1044,28 +1054,14 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                     mt.L = len;
                     mt.flags = flags;
                     mt.slice = slice;
+                    mt.cnt = cnt;
                     mbar_arrive_expect_tx(&full[s], 2 * nrows * box_bytes);
                 }
                 __syncwarp();
-                if (!p.split_copies) {  // box j: lane j, one copy per cache
-                    if (row >= 0) {
-                        tma_load_4d(st + lane * box_bytes, &kmap, 0, row, 0, iw.g * p.hg, &full[s], policy);
-                        tma_load_4d(st + lay.kv_bytes + lane * box_bytes, &vmap, 0, row, 0, iw.g * p.hg, &full[s],
-                                    policy);
-                    }
-                } else {
-                // one copy per (box, cache, kv head, row part), spread over the lanes; box j's row
-                // is in lane j
-                for (int q0 = 0; q0 < nreq; q0 += 32) {
-                    const int qi = q0 + lane;
-                    const int bi = qi / (2 * nsub), rest = qi - bi * 2 * nsub;
-                    const int brow = __shfl_sync(kFull, row, bi & 31);
-                    if (qi < nreq && brow >= 0) {
-                        const int vside = rest >= nsub ? 1 : 0, hp = rest - vside * nsub;  // hp = h * NP + part
-                        tma_load_3d(st + vside * lay.kv_bytes + bi * box_bytes + hp * part_bytes,
-                                    vside ? &vmap : &kmap, 0, iw.g * p.hg * NPART + hp, brow, &full[s], policy);
-                    }
-                }
+                if (row >= 0) {  // box j: lane j, one copy per cache
+                    tma_load_4d(st + lane * box_bytes, &kmap, 0, row, 0, iw.g * p.hg, &full[s], policy);
+                    tma_load_4d(st + lay.kv_bytes + lane * box_bytes, &vmap, 0, row, 0, iw.g * p.hg, &full[s],
+                                policy);
                 }
                 ++kk;
                 if (++rs == p.nst) {
@@ -1115,8 +1111,10 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     uint32_t off[TC::NT][TC::NCP];
     lane_offsets<D, FP8>(off, lane, j, h, p.hg, p.boxtok);
     const uint32_t stage_addr = smem_u32(stage0);
-    // several queries per stream: the query of row g8 sees `shift` fewer of the sequence's last tokens
-    const int shift = (p.qn - 1) - g8 / p.gq;
+    // several queries per stream: the query of row g8 sees `shift` fewer of the entry's last tokens
+    // (set per entry: the entry's last query sees them all)
+    int shift = 0;
+    int nvh = G;  // virtual heads of the entry that are queries (the rest are zero rows)
     uint32_t kk = 0, segs = 0, combs = 0;
     int s = 0;           // ring slot of stage kk
     uint32_t sph = 0;    // parity of its use
@@ -1144,13 +1142,15 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                 if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
                 break;
             }
-            // Q operand fragments of row g8 (zero rows past G): k-step ks holds dims 16 ks + 2 r4 (+1)
+            nvh = mt.cnt * p.gq;
+            shift = (mt.cnt - 1) - g8 / p.gq;
+            // Q operand fragments of row g8 (zero rows past nvh): k-step ks holds dims 16 ks + 2 r4 (+1)
             // and 16 ks + 8 + 2 r4 (+1) (bf16), or 16 ks + 4 r4 (+1) and 16 ks + 4 r4 + 2 (+3) (E4M3 order)
             const uint16_t *qr = reinterpret_cast<const uint16_t *>(qbuf + qs * lay.q_bytes) + (h * G + g8) * D;
 #pragma unroll
             for (int ks = 0; ks < TC::KS; ++ks) {
                 qa[ks][0] = qa[ks][1] = 0u;
-                if (g8 < G) {
+                if (g8 < nvh) {
                     if constexpr (!FP8) {
                         qa[ks][0] = *reinterpret_cast<const uint32_t *>(qr + 16 * ks + 2 * r4);
                         qa[ks][1] = *reinterpret_cast<const uint32_t *>(qr + 16 * ks + 8 + 2 * r4);
@@ -1272,9 +1272,9 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int hh = 2 * r4 + e;
-                        if (hh < G) {
+                        if (hh < nvh) {
                             const float inv = vsc / lc[e];
-                            uint16_t *orow = p.out + (((long long)mt.b * p.qn + hh / p.gq) * p.Hq +
+                            uint16_t *orow = p.out + (((long long)mt.b * p.qstride + hh / p.gq) * p.Hq +
                                                       (long long)kvh * p.gq + hh % p.gq) * D;
 #pragma unroll
                             for (int mi = 0; mi < TC::MT; ++mi) {
@@ -1321,7 +1321,8 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                         __threadfence();
                         const long long x0 = (long long)p.nhg * scan[mt.b] + (long long)mt.g * mt.n;
                         merge_pieces<D, G, FP8>(p, bound, slice_of(bound, nslots, x0),
-                                           slice_of(bound, nslots, x0 + mt.n - 1), sigma, h, mt.b, kvh, lane);
+                                                slice_of(bound, nslots, x0 + mt.n - 1), sigma, h, mt.b, kvh,
+                                                nvh, lane);
                     }
                 }
             }
@@ -1357,13 +1358,13 @@ struct LaunchArgs {
 };
 
 // Tensor map over one cache, each cached row (token, kv head) seen as parts of
-// RB bytes (RB / es elements).  split = 0: dims (RB / es, NB * bs rows, parts,
-// Hkv), a box is box_rows tokens x all parts x box_heads kv heads, landing in
-// shared memory as [kv head][part][token][RB bytes]; split = 1: dims (RB / es,
-// Hkv * parts, rows), a box is box_rows tokens of one part of one kv head.
-// Either way the copy swizzles RB-byte rows (see the stage layout at Tc).
+// RB bytes (RB / es elements): dims (RB / es, NB * bs rows, parts, Hkv) with
+// byte strides (Hkv * D * es, RB, D * es) -- not increasing, which the
+// driver takes.  A box is box_rows tokens x all parts x box_heads kv heads and
+// lands in shared memory as [kv head][part][token][RB bytes], the copy
+// swizzling the RB-byte rows (see the stage layout at Tc).
 inline bool encode_cache_map(CUtensorMap *map, const void *base, bool fp8, int D, int Hkv, int64_t rows,
-                             int box_heads, int box_rows, int split)
+                             int box_heads, int box_rows)
 {
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) {
@@ -1372,30 +1373,18 @@ inline bool encode_cache_map(CUtensorMap *map, const void *base, bool fp8, int D
     }
     const int es = fp8 ? 1 : 2;  // bytes per element
     const int rb = row_bytes_smem(D, es), parts = D * es / rb;
-    const cuuint64_t row_stride = cuuint64_t(Hkv) * D * es;
-    CUresult r;
+    const cuuint64_t dims[4] = {cuuint64_t(rb / es), cuuint64_t(rows), cuuint64_t(parts), cuuint64_t(Hkv)};
+    const cuuint64_t strides[3] = {cuuint64_t(Hkv) * D * es, cuuint64_t(rb), cuuint64_t(D) * es};
+    const cuuint32_t box[4] = {cuuint32_t(rb / es), cuuint32_t(box_rows), cuuint32_t(parts), cuuint32_t(box_heads)};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const CUtensorMapSwizzle sw = rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if (!split) {
-        const cuuint64_t dims[4] = {cuuint64_t(rb / es), cuuint64_t(rows), cuuint64_t(parts), cuuint64_t(Hkv)};
-        const cuuint64_t strides[3] = {row_stride, cuuint64_t(rb), cuuint64_t(D) * es};
-        const cuuint32_t box[4] = {cuuint32_t(rb / es), cuuint32_t(box_rows), cuuint32_t(parts), cuuint32_t(box_heads)};
-        r = enc(map, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {
-        const cuuint64_t dims[3] = {cuuint64_t(rb / es), cuuint64_t(Hkv) * parts, cuuint64_t(rows)};
-        const cuuint64_t strides[2] = {cuuint64_t(rb), row_stride};
-        const cuuint32_t box[3] = {cuuint32_t(rb / es), 1u, cuuint32_t(box_rows)};
-        r = enc(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    }
+    const CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                           const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
-        if (split) {  // the 4-D map is only a first try (see launch_decode)
-            char msg[64];
-            std::snprintf(msg, sizeof msg, "CUresult %d", int(r));
-            record_cuda_error("cuTensorMapEncodeTiled", msg);
-        }
+        char msg[64];
+        std::snprintf(msg, sizeof msg, "CUresult %d", int(r));
+        record_cuda_error("cuTensorMapEncodeTiled", msg);
         return false;
     }
     return true;
@@ -1406,7 +1395,7 @@ inline bool encode_cache_map(CUtensorMap *map, const void *base, bool fp8, int D
 // most recent ones (an engine binds one k_cache / v_cache view per layer, as in
 // the nano-vllm KV-cache post, §3.2).
 inline bool cached_cache_map(CUtensorMap *map, int dev, const void *base, bool fp8, int D, int Hkv, int64_t rows,
-                             int box_heads, int box_rows, int split)
+                             int box_heads, int box_rows)
 {
     struct Entry {
         int dev;
@@ -1414,7 +1403,7 @@ inline bool cached_cache_map(CUtensorMap *map, int dev, const void *base, bool f
         bool fp8;
         int D, Hkv;
         int64_t rows;
-        int box_heads, box, split;
+        int box_heads, box;
         CUtensorMap map;
     };
     constexpr size_t kMaxEntries = 256;
@@ -1424,14 +1413,14 @@ inline bool cached_cache_map(CUtensorMap *map, int dev, const void *base, bool f
     for (size_t i = 0; i < cache.size(); ++i) {
         const Entry &e = cache[i];
         if (e.dev == dev && e.base == base && e.fp8 == fp8 && e.D == D && e.Hkv == Hkv && e.rows == rows &&
-            e.box_heads == box_heads && e.box == box_rows && e.split == split) {
+            e.box_heads == box_heads && e.box == box_rows) {
             *map = e.map;
             return true;
         }
     }
-    if (!encode_cache_map(map, base, fp8, D, Hkv, rows, box_heads, box_rows, split)) return false;
+    if (!encode_cache_map(map, base, fp8, D, Hkv, rows, box_heads, box_rows)) return false;
     if (cache.size() >= kMaxEntries) cache.erase(cache.begin());
-    cache.push_back(Entry{dev, base, fp8, D, Hkv, rows, box_heads, box_rows, split, *map});
+    cache.push_back(Entry{dev, base, fp8, D, Hkv, rows, box_heads, box_rows, *map});
     return true;
 }
 
@@ -1482,20 +1471,9 @@ pkv_status launch_decode(LaunchArgs &a)
 
     CUtensorMap kmap, vmap;
     const int64_t rows = int64_t(p.NB) * p.bs;
-    // one 4-D copy per box where the driver takes that map (its strides are not in increasing
-    // order), else one copy per kv head and row part; a refusal is remembered
-    static std::atomic<bool> four_d_refused{false};
-    p.split_copies = four_d_refused.load() ? 1 : 0;
-    if (!p.split_copies && (!cached_cache_map(&kmap, a.device, a.k_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok, 0) ||
-                            !cached_cache_map(&vmap, a.device, a.v_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok, 0))) {
-        four_d_refused.store(true);
-        p.split_copies = 1;
-    }
-    if (p.split_copies) {
-        if (!cached_cache_map(&kmap, a.device, a.k_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok, 1) ||
-            !cached_cache_map(&vmap, a.device, a.v_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok, 1))
-            return PKV_ECUDA;
-    }
+    if (!cached_cache_map(&kmap, a.device, a.k_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok) ||
+        !cached_cache_map(&vmap, a.device, a.v_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok))
+        return PKV_ECUDA;
 
     auto kern = paged_decode_kernel<D, G, FP8>;
     if (!ensure_smem_attribute<D, G, FP8>(kern, a.device, lay.total)) return PKV_ECUDA;

@@ -103,17 +103,6 @@ __device__ __forceinline__ void griddep_launch_dependents()
 }
 
 // ---------------------------------------------------------------- TMA
-// 3-D tiled tensor copy global -> shared, completion counted on `bar`.
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int32_t c0, int32_t c1,
-                                            int32_t c2, uint64_t *bar, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
 // 4-D tiled tensor copy global -> shared, completion counted on `bar`.
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int32_t c0, int32_t c1,
                                             int32_t c2, int32_t c3, uint64_t *bar, uint64_t policy)

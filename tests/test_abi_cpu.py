@@ -178,7 +178,11 @@ def test_newer_entry_points_validate_on_the_host(lib):
 
 
 def test_attention_workspace_holds_the_rows(lib):
+    """One decode entry per row with up to max(1, 8 // G) queries (qg * G virtual heads), then the
+    three row arrays (sequence, length, query count)."""
     f, g = lib.pkv_paged_attention_workspace_size, lib.pkv_paged_decode_workspace_size
     for rows in (1, 7, 256, 4096):
-        assert f(rows, 16, 8, 128) >= g(rows, 16, 8, 128) + 2 * 4 * rows
+        for hq, hkv, d in ((16, 8, 128), (6, 2, 64), (8, 8, 64), (14, 2, 64)):
+            qg = max(1, 8 // (hq // hkv))
+            assert f(rows, hq, hkv, d) >= g(rows, hq * qg, hkv, d) + 3 * 4 * rows
     assert f(-1, 16, 8, 128) == 0 and f(4, 16, 6, 128) == 0

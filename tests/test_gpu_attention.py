@@ -114,6 +114,47 @@ def test_inconsistent_offsets_give_zeros_and_an_error():
     assert torch.all(out[5:].float() == 0)
 
 
+@pytest.mark.parametrize("Hq,Hkv,D,bs,workers", [(8, 8, 64, 16, 0), (6, 2, 64, 16, 0), (6, 2, 64, 8, 77),
+                                                 (16, 8, 128, 256, 0), (32, 8, 128, 16, 500)])
+def test_long_prefill_chunks_share_passes(Hq, Hkv, D, bs, workers):
+    """Prefill chunks of many tokens after a cached prefix: consecutive queries of a sequence go in
+    chunks of max(1, 8 // G) (G = 1: 8, G = 3: 2, G = 2: 4, G = 4: 2), the last chunk of a sequence
+    shorter; every query keeps its own causal bound."""
+    lens = [700, 129, 1, 333, 64, 1200]
+    news = [250, 129, 1, 7, 33, 5]          # whole prefill, partial chunks, a decode
+    q, kc, vc, bt, cu, lens_t = mixed_batch(lens, news, Hq, Hkv, D, bs, seed=Hq * 7 + bs)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    want = oracle_of(q, kc, vc, bt, cu, lens_t, 0.0884)
+    ws = pkv.alloc_attention_workspace(q.shape[0], Hq, Hkv, D)
+    for call in range(2):
+        out = run(q, kc, vc, bt, cu, lens_t, 0.0884, workers=workers, ws=ws, err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        check_close(out, want, f"{Hq}/{Hkv} bs{bs} call {call}")
+
+
+def test_same_n_with_a_too_short_sequence():
+    """new_per_seq = n with a sequence of fewer than n cached tokens: its rows are zero and the
+    error word says so; the other sequences are exact (the n queries share one pass)."""
+    n = 3
+    lens = [40, 2, 0, 90]
+    good = [0, 3]
+    q, kc, vc, bt, cu, lens_t = mixed_batch([40, 3, 3, 90], [n] * 4, 16, 8, 128, 16, seed=5)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full_like(q, float("nan"))
+    ws = pkv.alloc_attention_workspace(q.shape[0], 16, 8, 128)
+    pkv.paged_attention(q, kc, vc, bt, None, lens_t, 0.0884, out, ws, err_word=err, new_per_seq=n)
+    torch.cuda.synchronize()
+    assert err.item() & pkv.ERR_CONTEXT_RANGE
+    assert torch.all(out[n:3 * n].float() == 0)
+    for b in good:
+        rows = slice(b * n, b * n + n)
+        want = oracle.paged_attention(W.bits(q)[rows], W.bits(kc), W.bits(vc), bt.cpu().numpy()[b:b + 1],
+                                      np.array([0, n], np.int32), np.array([lens[b]], np.int32), 0.0884)
+        check_close(out[rows], want, f"sequence {b}")
+
+
 @pytest.mark.parametrize("n,Hq,Hkv,D,bs,workers", [(2, 16, 8, 128, 16, 0), (3, 16, 8, 128, 256, 0),
                                                    (4, 16, 8, 128, 16, 0), (4, 16, 8, 128, 8, 333),
                                                    (8, 4, 4, 64, 16, 0), (4, 14, 2, 64, 16, 1),
