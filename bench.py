@@ -313,6 +313,43 @@ def run_pkv(args):
                      "note": "K/V read once per sequence; streamed_* counts one pass per query row, for comparison "
                              "with running the rows separately"}
 
+        # the last npf tokens of every sequence as one prefill chunk over its cached prefix (offsets
+        # given): consecutive queries share passes in chunks of max(1, 8 // G)
+        npf = 64
+        if lens_h.min() >= npf and B * npf <= 16384:
+            cu_p = torch.arange(0, (B + 1) * npf, npf, dtype=torch.int32, device=dev)
+            qp = torch.randn(B * npf, Hq, D, device=dev).bfloat16()
+            outp = torch.empty_like(qp)
+            wsp = pkv.alloc_attention_workspace(B * npf, Hq, Hkv, D, dev)
+
+            def pre():
+                pkv.paged_attention(qp, lay0.k_cache, lay0.v_cache, wl.block_tables, cu_p, wl.context_lens,
+                                    wl.scale, outp, wsp, max_context_len=max_ctx, err_word=err, stream=stream)
+            for _ in range(5):
+                pre()
+            torch.cuda.synchronize()
+            pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(30)]
+            for c0, c1 in pev:
+                c0.record(stream)
+                pre()
+                c1.record(stream)
+            torch.cuda.synchronize()
+            assert err.item() == 0, f"device error word {err.item():#x}"
+            us_p = float(np.mean([c0.elapsed_time(c1) for c0, c1 in pev])) * 1e3
+            row = Hkv * D * 2 * 2
+            qg = max(1, 8 // (Hq // Hkv))
+            chunk_rows = int(sum(L - npf + min(c + qg, npf) for L in lens_h for c in range(0, npf, qg))) * row
+            per_query = int(sum(L - npf + 1 + i for L in lens_h for i in range(npf))) * row
+            mixed = dict(mixed or {})
+            mixed["prefill_chunk"] = {
+                "kernel": "pkv_paged_attention (expand_rows_kernel + paged_decode_kernel, chunks of %d queries)" % qg,
+                "query_rows": B * npf, "new_tokens_per_sequence": npf, "mean_call_us": round(us_p, 2),
+                "chunk_streamed_kv_bytes": chunk_rows, "per_query_kv_bytes": per_query,
+                "chunk_streamed_gbs": round(chunk_rows / (us_p * 1e-6) / 1e9, 1),
+                "note": "the last %d tokens of every sequence as a prefill chunk over its cached prefix; "
+                        "chunk_streamed counts one pass per query chunk (what the kernel reads), per_query one "
+                        "pass per query row" % npf}
+
     # ---- copy-on-write block copies (pkv_copy_blocks) on this workload's pool: owned blocks copied
     # into blocks no sequence holds, as many pairs as there are such blocks (up to 256)
     cow = None
