@@ -198,11 +198,25 @@ struct WsLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Piece slots: (slice + b * nhg + group) * hg + head-in-group, one per piece.
+// Piece slots.  Only a segment (an entry's units of one head group) that
+// crosses a slice boundary leaves pieces, and a slice holds at most two of
+// them: its first segment (the one holding the slice's first unit, when it
+// began in an earlier slice or goes on into a later one) and its last
+// segment (going on into the next slice).  Two numberings, whichever needs
+// fewer slots:
+//   by entry (B * nhg < kMaxSlots): (slice + b * nhg + group) * hg + h,
+//     injective because slices and segments are both ordered along the
+//     unit list;
+//   by slice (otherwise): (2 slice + [not the slice's first segment]) * hg + h,
+//     2 * kMaxSlots * hg slots whatever the batch.
+__host__ __device__ inline bool slots_by_slice(int32_t B, int32_t nhg) { return int64_t(B) * nhg >= kMaxSlots; }
+
 inline WsLayout ws_layout(int32_t B, int32_t G, int32_t Hkv, int32_t D)
 {
     const int hg = head_group(Hkv, G);
-    const size_t slots = (size_t(kMaxSlots) + size_t(B) * size_t(Hkv / hg)) * size_t(hg);
+    const size_t slots = (slots_by_slice(B, Hkv / hg) ? 2 * size_t(kMaxSlots)
+                                                       : size_t(kMaxSlots) + size_t(B) * size_t(Hkv / hg)) *
+                         size_t(hg);
     WsLayout w;
     w.bal_off = 0;
     w.count_off = align256(sizeof(BalanceState));
@@ -778,7 +792,9 @@ __device__ __forceinline__ int slice_of(const long long *bound, int nslots, long
 }
 
 // Merge the partial states of (b, kv head kvh) left by the non-empty slices
-// sf..sl, piece slots (s + sigma) * hg + h, and write the outputs of the
+// sf..sl (the segment's first unit is x0) from their piece slots (see
+// ws_layout: by slice, f = 1 only in slice sf when the segment is not that
+// slice's first, x0 > bound[sf]), and write the outputs of the
 // entry's nvh virtual heads that are queries:
 //   M = max m_i,  l = sum 2^(m_i - M) l_i,  out = sum 2^(m_i - M) acc_i / l
 // (the online-softmax algebra; m in log2 units).  The pieces were written by
@@ -786,7 +802,7 @@ __device__ __forceinline__ int slice_of(const long long *bound, int nslots, long
 // time with independent loads, folded into a running (M, l, acc).
 template <int D, int G, bool FP8>
 __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long long *bound, int sf, int sl,
-                                             long long sigma, int h, int b, int kvh, int nvh, int lane)
+                                             long long x0, int g, int h, int b, int kvh, int nvh, int lane)
 {
     constexpr int PER = D / 32;                           // output values per lane
     constexpr int BATCH = G <= 2 ? 4 : (G <= 7 ? 2 : 1);  // pieces loaded together (G = 8 would spill)
@@ -808,7 +824,10 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
         for (int k = 0; k < BATCH; ++k) {
             const int s = s0 + k;
             use[k] = s <= sl && bound[s + 1] > bound[s];  // empty slices left nothing
-            const long long slot = ((use[k] ? s : sf) + sigma) * p.hg + h;
+            const int sk = use[k] ? s : sf;
+            const long long slot = (slots_by_slice(p.B, p.nhg)
+                                        ? 2LL * sk + ((sk == sf && x0 != bound[sf]) ? 1 : 0)
+                                        : sk + (long long)b * p.nhg + g) * p.hg + h;
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
                 st[k][hh] = __ldcg(ml + slot * G + hh);
@@ -1289,8 +1308,13 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                         }
                     }
                 } else {
-                    const long long sigma = (long long)mt.b * p.nhg + mt.g;
-                    const long long slot = (mt.slice + sigma) * p.hg + h;
+                    // the segment is its slice's first when it began in an earlier slice or at the
+                    // slice's first unit (see ws_layout)
+                    const long long x0 = (long long)p.nhg * scan[mt.b] + (long long)mt.g * mt.n;
+                    const bool first = u_first > 0 || x0 == bound[mt.slice];
+                    const long long slot = (slots_by_slice(p.B, p.nhg)
+                                                ? 2LL * mt.slice + (first ? 0 : 1)
+                                                : mt.slice + (long long)mt.b * p.nhg + mt.g) * p.hg + h;
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int hh = 2 * r4 + e;
@@ -1319,10 +1343,9 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                                            uint32_t(mt.n), p.err);
                     if (__shfl_sync(kFull, last, 0)) {
                         __threadfence();
-                        const long long x0 = (long long)p.nhg * scan[mt.b] + (long long)mt.g * mt.n;
                         merge_pieces<D, G, FP8>(p, bound, slice_of(bound, nslots, x0),
-                                                slice_of(bound, nslots, x0 + mt.n - 1), sigma, h, mt.b, kvh,
-                                                nvh, lane);
+                                                slice_of(bound, nslots, x0 + mt.n - 1), x0, mt.g, h, mt.b,
+                                                kvh, nvh, lane);
                     }
                 }
             }

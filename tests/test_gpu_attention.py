@@ -133,6 +133,21 @@ def test_long_prefill_chunks_share_passes(Hq, Hkv, D, bs, workers):
         check_close(out, want, f"{Hq}/{Hkv} bs{bs} call {call}")
 
 
+@pytest.mark.parametrize("workers", [0, 250])
+def test_prefill_batch_past_512_entries(workers):
+    """More than 512 query rows (entries): split-K pieces numbered by slice; whole prefills, chunks
+    after a prefix and decodes."""
+    lens = [900, 400, 333, 64, 1, 2000, 17] + [50 + 7 * i for i in range(40)]
+    news = [300, 400, 200, 10, 1, 3, 17] + [1] * 40
+    q, kc, vc, bt, cu, lens_t = mixed_batch(lens, news, 16, 8, 64, 16, seed=950 + workers)
+    assert q.shape[0] > 512
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run(q, kc, vc, bt, cu, lens_t, 0.125, workers=workers, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    check_close(out, oracle_of(q, kc, vc, bt, cu, lens_t, 0.125), f"workers {workers}")
+
+
 def test_same_n_with_a_too_short_sequence():
     """new_per_seq = n with a sequence of fewer than n cached tokens: its rows are zero and the
     error word says so; the other sequences are exact (the n queries share one pass)."""

@@ -212,6 +212,25 @@ def test_forced_splits(workers):
     assert torch.all(out[lens.index(0)].float() == 0)
 
 
+@pytest.mark.parametrize("workers", [0, 97, 4096])
+def test_many_sequences_slice_numbered_pieces(workers):
+    """B * (kv head groups) >= 512: split-K pieces are numbered by slice (two per slice) instead of by
+    sequence; long and short sequences mixed so that pieces start and end inside slices."""
+    rng = np.random.default_rng(640 + workers)
+    lens = rng.integers(0, 400, size=640)
+    lens[::37] = 1500
+    q, kc, vc, bt, lens_t = synth(len(lens), 0, 16, 8, 64, 16, seed=workers + 3, lens=lens)
+    want = oracle_of(q, kc, vc, bt, lens_t, 0.125)
+    ws = shared_workspace(len(lens), 16, 8, 64)
+    err = err_word()
+    for call in range(2):
+        out = torch.full_like(q, float("nan"))
+        pkv.paged_decode(q, kc, vc, bt, lens_t, 0.125, out, ws, num_workers=workers, err_word=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        check_close(out, want, f"workers {workers} call {call}")
+
+
 @pytest.mark.parametrize("bs", [16, 256])
 def test_adaptive_split_over_repeated_calls(bs):
     """Default split, eight calls on one workspace: each call sizes its per-SM slices from the
