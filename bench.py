@@ -337,18 +337,19 @@ def run_pkv(args):
             assert err.item() == 0, f"device error word {err.item():#x}"
             us_p = float(np.mean([c0.elapsed_time(c1) for c0, c1 in pev])) * 1e3
             row = Hkv * D * 2 * 2
-            qg = max(1, 8 // (Hq // Hkv))
-            chunk_rows = int(sum(L - npf + min(c + qg, npf) for L in lens_h for c in range(0, npf, qg))) * row
+            qe = max(1, 8 // (Hq // Hkv)) * 8  # queries of a query-split entry: 8 warps x max(1, 8 // G)
+            chunk_rows = int(sum(L - npf + min(c + qe, npf) for L in lens_h for c in range(0, npf, qe))) * row
             per_query = int(sum(L - npf + 1 + i for L in lens_h for i in range(npf))) * row
             mixed = dict(mixed or {})
             mixed["prefill_chunk"] = {
-                "kernel": "pkv_paged_attention (expand_rows_kernel + paged_decode_kernel, chunks of %d queries)" % qg,
+                "kernel": "pkv_paged_attention (expand_rows_kernel + paged_decode_kernel query-split, %d queries "
+                          "share each K/V pass)" % qe,
                 "query_rows": B * npf, "new_tokens_per_sequence": npf, "mean_call_us": round(us_p, 2),
                 "chunk_streamed_kv_bytes": chunk_rows, "per_query_kv_bytes": per_query,
                 "chunk_streamed_gbs": round(chunk_rows / (us_p * 1e-6) / 1e9, 1),
                 "note": "the last %d tokens of every sequence as a prefill chunk over its cached prefix; "
-                        "chunk_streamed counts one pass per query chunk (what the kernel reads), per_query one "
-                        "pass per query row" % npf}
+                        "chunk_streamed counts one K/V pass per group of queries sharing it (what the kernel "
+                        "reads), per_query one pass per query row" % npf}
 
     # ---- copy-on-write block copies (pkv_copy_blocks) on this workload's pool: owned blocks copied
     # into blocks no sequence holds, as many pairs as there are such blocks (up to 256)

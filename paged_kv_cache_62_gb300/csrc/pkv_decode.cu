@@ -21,7 +21,7 @@ extern "C" size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_
 // b * qn + i; context_lens the sequences' whole lengths); otherwise entry b
 // holds row_cnt[b] queries at rows b + i (row_seq[b]: its sequence,
 // context_lens[b]: the length its last query sees).
-static pkv_status decode_call(bool fp8, int32_t qn, const uint16_t *q, const void *k_cache, const void *v_cache,
+static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, const void *k_cache, const void *v_cache,
                               const float *k_scale, const float *v_scale, const int32_t *row_seq,
                               const int32_t *row_cnt, const int32_t *block_tables,
                               int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
@@ -50,7 +50,8 @@ static pkv_status decode_call(bool fp8, int32_t qn, const uint16_t *q, const voi
     // unit counts (and positions in the unit list) are kept in 32 bits
     const int64_t max_units = int64_t(num_kv_heads) * num_seqs * ((len_limit + 7) / 8);
     if (max_units > INT32_MAX) return PKV_EUNSUPPORTED;
-    const WsLayout ws = ws_layout(num_seqs, G, num_kv_heads, head_dim);
+    if (qs && (fp8 || !row_cnt)) return PKV_EINVAL;  // query-split entries are chunks of bf16 calls
+    const WsLayout ws = ws_layout(num_seqs, G, num_kv_heads, head_dim, qs);
     if (!workspace || workspace_bytes < ws.total || !aligned16(workspace)) return PKV_EWORKSPACE;
 
     DeviceInfo dev;
@@ -76,10 +77,10 @@ static pkv_status decode_call(bool fp8, int32_t qn, const uint16_t *q, const voi
     p.NB = num_blocks;
     p.max_blocks = max_blocks_per_seq;
     p.len_limit = int32_t(len_limit);
-    p.hg = head_group(num_kv_heads, G);
+    p.hg = qs ? 1 : head_group(num_kv_heads, G);
     p.nhg = num_kv_heads / p.hg;
-    p.sub = warp_slices(G, p.hg);
-    p.toks = warp_tokens(G, fp8) * p.sub;
+    p.sub = qs ? team_warps(G) : warp_slices(G, p.hg);
+    p.toks = warp_tokens(G, fp8, qs) * (qs ? 1 : p.sub);
     p.boxtok = std::min(p.toks, block_size);
     p.nbox = p.toks / p.boxtok;
     p.lg_nbox = ilog2(p.nbox);
@@ -102,8 +103,9 @@ static pkv_status decode_call(bool fp8, int32_t qn, const uint16_t *q, const voi
     a.requested_workers = num_workers;
     a.stream = reinterpret_cast<cudaStream_t>(stream);
 
-    LaunchFn fn = fp8 ? pick_decode_fp8(head_dim, G) : (head_dim == 64 ? pick_group<64, false>(G)
-                                                                        : pick_group<128, false>(G));
+    LaunchFn fn = fp8  ? pick_decode_fp8(head_dim, G)
+                  : qs ? pick_decode_qs(head_dim, G)
+                       : (head_dim == 64 ? pick_group<64, false, false>(G) : pick_group<128, false, false>(G));
     if (!fn) return PKV_EUNSUPPORTED;
     return fn(a);
 }
@@ -116,7 +118,7 @@ extern "C" pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cach
                                        void *workspace, size_t workspace_bytes, int32_t num_workers,
                                        int32_t *err_word, pkv_stream_t stream)
 {
-    return decode_call(false, 1, q, k_cache, v_cache, nullptr, nullptr, nullptr, nullptr, block_tables,
+    return decode_call(false, false, 1, q, k_cache, v_cache, nullptr, nullptr, nullptr, nullptr, block_tables,
                        max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                        num_blocks, max_context_len, scale, out, workspace, workspace_bytes, num_workers, err_word,
                        stream);
@@ -131,7 +133,7 @@ extern "C" pkv_status pkv_paged_decode_fp8(const uint16_t *q, const uint8_t *k_c
                                            size_t workspace_bytes, int32_t num_workers, int32_t *err_word,
                                            pkv_stream_t stream)
 {
-    return decode_call(true, 1, q, k_cache, v_cache, k_scale, v_scale, nullptr, nullptr, block_tables,
+    return decode_call(true, false, 1, q, k_cache, v_cache, k_scale, v_scale, nullptr, nullptr, block_tables,
                        max_blocks_per_seq, context_lens,
                        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale,
                        out, workspace, workspace_bytes, num_workers, err_word, stream);
@@ -212,7 +214,7 @@ namespace pkv {
 // Query row r = cu_seqlens_q[b] + i of sequence b (n = cu_seqlens_q[b+1] -
 // cu_seqlens_q[b] new tokens, L = context_lens[b] in the cache) sits at
 // position L - n + i: it sees the L - n + i + 1 keys before it.  The rows of
-// a sequence are cut into chunks of up to qg consecutive queries that share
+// a sequence are cut into chunks of up to `chunk` consecutive queries that share
 // one K/V stream; a chunk is entry r of the decode kernel, r the row of its
 // first query: row_seq[r] = b, row_cnt[r] = its query count, row_len[r] = the
 // keys its last query sees.  Rows that start no chunk get row_cnt = 0 and
@@ -225,7 +227,7 @@ namespace pkv {
 // new_per_seq rows (row r belongs to sequence r / new_per_seq).
 __global__ void expand_rows_kernel(const int32_t *__restrict__ cu_seqlens_q, int32_t new_per_seq,
                                    const int32_t *__restrict__ context_lens, int32_t num_seqs, int32_t num_rows,
-                                   int32_t qg, int32_t *__restrict__ row_seq, int32_t *__restrict__ row_len,
+                                   int32_t chunk, int32_t *__restrict__ row_seq, int32_t *__restrict__ row_len,
                                    int32_t *__restrict__ row_cnt, int32_t *err)
 {
     griddep_launch_dependents();
@@ -252,11 +254,11 @@ __global__ void expand_rows_kernel(const int32_t *__restrict__ cu_seqlens_q, int
     const int32_t L = __ldg(context_lens + lo);
     const int32_t n = r1 - r0, i = r - r0;
     const bool inside = r0 <= r && r < r1;
-    const bool ok = (!cu_seqlens_q || __ldg(cu_seqlens_q) == 0) && inside && n <= L;
+    const bool ok = (!cu_seqlens_q || __ldg(cu_seqlens_q) == 0) && inside && n <= L && r1 <= num_rows;
     if (!ok) flag_error(err, PKV_ERR_CONTEXT_RANGE);
     int32_t cnt = 1, len = 0;  // a row outside its sequence's range: an entry of its own, zero output
     if (inside) {
-        cnt = i % qg == 0 ? min(qg, n - i) : 0;
+        cnt = i % chunk == 0 ? min(min(chunk, n - i), num_rows - r) : 0;  // never past the last row
         len = ok && cnt > 0 ? L - n + i + cnt : 0;
     }
     row_seq[r] = lo;
@@ -266,11 +268,18 @@ __global__ void expand_rows_kernel(const int32_t *__restrict__ cu_seqlens_q, int
 
 inline size_t rows_bytes(int32_t num_rows) { return align256(size_t(num_rows) * 4); }
 
-// Queries per chunk: as many as keep the chunk's qg * G virtual heads within
-// the 8 rows of the MMA tile that the kernel uses.
+// Queries per warp: as many as keep its qg * G virtual heads within the 8
+// rows of the MMA tile that the kernel uses.  A query-split entry holds the
+// queries of all team_warps warps of its CTA.
 inline int32_t chunk_queries(int32_t num_q_heads, int32_t num_kv_heads)
 {
     return std::max(1, 8 / (num_q_heads / num_kv_heads));
+}
+
+inline int32_t entry_queries(int32_t num_q_heads, int32_t num_kv_heads)
+{
+    const int32_t qg = chunk_queries(num_q_heads, num_kv_heads);
+    return qg * team_warps(qg * (num_q_heads / num_kv_heads));
 }
 
 }  // namespace pkv
@@ -280,10 +289,11 @@ extern "C" size_t pkv_paged_attention_workspace_size(int32_t num_rows, int32_t n
 {
     const size_t base = pkv_paged_decode_workspace_size(num_rows, num_q_heads, num_kv_heads, head_dim);
     if (base == 0) return 0;
-    // decode workspace for entries of up to qg queries (qg * G virtual heads), one entry per row,
-    // then the three row arrays
-    size_t dec = base;
-    for (int32_t qn = 2; qn <= chunk_queries(num_q_heads, num_kv_heads); ++qn)
+    // decode workspace: same-n calls (entries of n <= qg queries, n * G virtual heads), or one
+    // query-split entry per row (qg * G virtual heads per warp); then the three row arrays
+    const int32_t gq = num_q_heads / num_kv_heads, qg = chunk_queries(num_q_heads, num_kv_heads);
+    size_t dec = std::max(base, ws_layout(num_rows, gq * qg, num_kv_heads, head_dim, true).total);
+    for (int32_t qn = 2; qn <= qg; ++qn)
         dec = std::max(dec, pkv_paged_decode_workspace_size(num_rows, num_q_heads * qn, num_kv_heads, head_dim));
     return align256(dec) + 3 * rows_bytes(num_rows);
 }
@@ -308,12 +318,13 @@ extern "C" pkv_status pkv_paged_attention(const uint16_t *q, const uint16_t *k_c
     const int32_t qg = chunk_queries(num_q_heads, num_kv_heads);
     if (new_per_seq > 1 && new_per_seq <= qg)
         // every sequence's n new tokens share its K/V stream: read once, n * G virtual heads
-        return decode_call(false, new_per_seq, q, k_cache, v_cache, nullptr, nullptr, nullptr, nullptr,
+        return decode_call(false, false, new_per_seq, q, k_cache, v_cache, nullptr, nullptr, nullptr, nullptr,
                            block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
                            head_dim, block_size, num_blocks, max_context_len, scale, out, workspace,
                            workspace_bytes, num_workers, err_word, stream);
-    // chunks of up to qg queries of a sequence, one entry per row; the row arrays sit after the
-    // decode workspace
+    // query-split entries: chunks of up to qg * team_warps queries of a sequence (each warp of the
+    // CTA takes qg of them, all warps on the same K/V tiles), one entry per row; the row arrays sit
+    // after the decode workspace
     uint8_t *wsb = static_cast<uint8_t *>(workspace);
     const size_t dec_bytes = need - 3 * rows_bytes(num_rows);
     int32_t *row_seq = reinterpret_cast<int32_t *>(wsb + dec_bytes);
@@ -321,7 +332,8 @@ extern "C" pkv_status pkv_paged_attention(const uint16_t *q, const uint16_t *k_c
     int32_t *row_cnt = reinterpret_cast<int32_t *>(wsb + dec_bytes + 2 * rows_bytes(num_rows));
     const cudaError_t e = launch_pdl(expand_rows_kernel, dim3((num_rows + 255) / 256), dim3(256), 0,
                                      reinterpret_cast<cudaStream_t>(stream), new_per_seq > 0 ? nullptr : cu_seqlens_q,
-                                     new_per_seq, context_lens, num_seqs, num_rows, qg, row_seq, row_len, row_cnt,
+                                     new_per_seq, context_lens, num_seqs, num_rows,
+                                     entry_queries(num_q_heads, num_kv_heads), row_seq, row_len, row_cnt,
                                      err_word);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -329,7 +341,7 @@ extern "C" pkv_status pkv_paged_attention(const uint16_t *q, const uint16_t *k_c
     }
     const pkv_status st = launch_status("expand_rows_kernel launch");
     if (st != PKV_OK) return st;
-    return decode_call(false, qg, q, k_cache, v_cache, nullptr, nullptr, row_seq, row_cnt, block_tables,
+    return decode_call(false, true, qg, q, k_cache, v_cache, nullptr, nullptr, row_seq, row_cnt, block_tables,
                        max_blocks_per_seq, row_len, num_rows, num_q_heads, num_kv_heads, head_dim, block_size,
                        num_blocks, max_context_len, scale, out, workspace, dec_bytes, num_workers, err_word, stream);
 }

@@ -6,8 +6,8 @@ namespace pkv {
 
 LaunchFn pick_decode_fp8(int D, int G)
 {
-    if (D == 64) return pick_group<64, true>(G);
-    if (D == 128) return pick_group<128, true>(G);
+    if (D == 64) return pick_group<64, true, false>(G);
+    if (D == 128) return pick_group<128, true, false>(G);
     return nullptr;
 }
 

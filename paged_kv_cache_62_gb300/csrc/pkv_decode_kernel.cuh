@@ -56,7 +56,7 @@
 
 namespace pkv {
 
-constexpr int kMaxStages = 4;     // ring depth
+constexpr int kMaxStages = 16;    // ring depth (as many as fit: 3 of 64 KiB, 12 of 16 KiB)
 constexpr int kMaxSlots = 512;    // slices: SM ids (adaptive) or CTAs (fixed split)
 constexpr uint32_t kTableMagic = 0x62616c31u;
 constexpr uint32_t kEpochMagic = 0x65706f63u;
@@ -71,7 +71,10 @@ constexpr uint32_t kEpochMagic = 0x65706f63u;
 // registers do not grow with the group size (G query heads are rows of one
 // MMA tile), so every group size runs 8 consumers.
 __host__ __device__ constexpr int team_warps(int) { return 8; }
-__host__ __device__ constexpr int warp_tokens(int, bool fp8) { return fp8 ? 32 : 16; }
+// Query-split CTAs (qs; long runs of new tokens, see paged_decode_kernel)
+// take 32-token tiles too: one kv head's stage is small, and every warp
+// works on every token.
+__host__ __device__ constexpr int warp_tokens(int, bool fp8, bool qs = false) { return fp8 || qs ? 32 : 16; }
 
 // ------------------------------------------------------------------ load balance state
 // In the adaptive mode a slice's size follows what the previous call on this
@@ -141,16 +144,19 @@ __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x
 // multiple of 4, so every block (and its float4 rows) is 16-byte aligned.
 __host__ __device__ inline int comb_stride(int D, int G) { return int(align_up(uint32_t(G * (D + 2)), 4)); }
 
-// es: bytes per cached element (2 for bf16, 1 for E4M3).
-__host__ __device__ inline CtaLayout cta_layout(int D, int G, int es, int hg, int sub, int nst, int B)
+// es: bytes per cached element (2 for bf16, 1 for E4M3); qs: query-split
+// CTA (all sub warps of a kv head on the same tokens, each with its own G
+// virtual heads).
+__host__ __device__ inline CtaLayout cta_layout(int D, int G, int es, int hg, int sub, int nst, int B,
+                                                bool qs = false)
 {
     CtaLayout l;
-    const int toks = warp_tokens(G, es == 1) * sub;
+    const int toks = warp_tokens(G, es == 1, qs) * (qs ? 1 : sub);
     l.kv_bytes = uint32_t(toks * hg * D * es);
     l.stage_bytes = align_up(2 * l.kv_bytes, 1024);  // stages start on the 1024-byte swizzle period
-    l.q_bytes = align_up(uint32_t(hg * G * D * 2), 128);
+    l.q_bytes = align_up(uint32_t(hg * (qs ? sub : 1) * G * D * 2), 128);
     // states of the non-leading warps of every head (the leader keeps its own in registers)
-    l.comb_bytes = sub > 1 ? align_up(uint32_t(hg * (sub - 1) * comb_stride(D, G) * 4), 128) : 0u;
+    l.comb_bytes = sub > 1 && !qs ? align_up(uint32_t(hg * (sub - 1) * comb_stride(D, G) * 4), 128) : 0u;
     uint32_t o = uint32_t(nst) * l.stage_bytes;
     l.off_q = o;
     o += 2 * l.q_bytes;
@@ -209,18 +215,21 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 //     unit list;
 //   by slice (otherwise): (2 slice + [not the slice's first segment]) * hg + h,
 //     2 * kMaxSlots * hg slots whatever the batch.
+// Query-split CTAs (qs) keep one piece per warp: slot * team_warps + warp,
+// and one arrival counter per (entry, kv head, warp).
 __host__ __device__ inline bool slots_by_slice(int32_t B, int32_t nhg) { return int64_t(B) * nhg >= kMaxSlots; }
 
-inline WsLayout ws_layout(int32_t B, int32_t G, int32_t Hkv, int32_t D)
+inline WsLayout ws_layout(int32_t B, int32_t G, int32_t Hkv, int32_t D, bool qs = false)
 {
-    const int hg = head_group(Hkv, G);
+    const int hg = qs ? 1 : head_group(Hkv, G);
+    const size_t subq = qs ? size_t(team_warps(G)) : 1;
     const size_t slots = (slots_by_slice(B, Hkv / hg) ? 2 * size_t(kMaxSlots)
                                                        : size_t(kMaxSlots) + size_t(B) * size_t(Hkv / hg)) *
-                         size_t(hg);
+                         size_t(hg) * subq;
     WsLayout w;
     w.bal_off = 0;
     w.count_off = align256(sizeof(BalanceState));
-    w.ml_off = w.count_off + align256(size_t(B) * size_t(Hkv) * 8);
+    w.ml_off = w.count_off + align256(size_t(B) * size_t(Hkv) * subq * 8);
     w.acc_off = w.ml_off + align256(slots * size_t(G) * 2 * 4);
     w.total = w.acc_off + slots * size_t(G) * size_t(D) * 4;
     return w;
@@ -331,7 +340,7 @@ constexpr float kRescaleSlack = 8.0f;
 // 64-dim E4M3 caches).
 // The chunks of eight consecutive tokens then sit in eight different bank
 // groups, and one ldmatrix reads them without a conflict.
-template <int D, bool FP8>
+template <int D, bool FP8, bool QS = false>
 struct Tc {
     static constexpr int ES = FP8 ? 1 : 2;              // bytes per cached element
     static constexpr int ROWB = D * ES;                 // bytes per cached row
@@ -340,7 +349,7 @@ struct Tc {
     static constexpr int NCP = ROWB / 32;               // 16-byte chunk pairs per row (one ldmatrix.x4 each)
     static constexpr int KS = D / 16;                   // k-steps of the score product
     static constexpr int MT = D / 16;                   // m-tiles of the output product
-    static constexpr int NT = FP8 ? 2 : 1;              // 16-token sub-tiles of a warp's tile
+    static constexpr int NT = FP8 || QS ? 2 : 1;        // 16-token sub-tiles of a warp's tile
     static constexpr int TW = 16 * NT;                  // tokens of a warp's tile (warp_tokens)
 };
 
@@ -358,11 +367,11 @@ __device__ __forceinline__ uint32_t swizzled_chunk(uint32_t c, uint32_t R)
 // 2i + (lane / 8) % 2 of the row.  Matrix q of an .x4 load is then
 // (tokens 0-7 | 8-15 of the sub-tile) x (chunk 2i | 2i + 1) for q = 0 (0-7, 2i),
 // 1 (0-7, 2i+1), 2 (8-15, 2i), 3 (8-15, 2i+1).
-template <int D, bool FP8>
-__device__ __forceinline__ void lane_offsets(uint32_t (&off)[Tc<D, FP8>::NT][Tc<D, FP8>::NCP], int lane, int j,
-                                             int h, int hg, int boxtok)
+template <int D, bool FP8, bool QS>
+__device__ __forceinline__ void lane_offsets(uint32_t (&off)[Tc<D, FP8, QS>::NT][Tc<D, FP8, QS>::NCP], int lane,
+                                             int j, int h, int hg, int boxtok)
 {
-    using T = Tc<D, FP8>;
+    using T = Tc<D, FP8, QS>;
     const int tl = ((lane >> 4) << 3) | (lane & 7), e = (lane >> 3) & 1;
     const int lg = __ffs(boxtok) - 1;
     const uint32_t box_bytes = uint32_t(boxtok * hg * T::ROWB);
@@ -423,13 +432,14 @@ __device__ __forceinline__ uint32_t f16x2_sat(float lo, float hi)
 // magnitude 2^-14 .. 65504; smaller ones keep f16's subnormal steps of 2^-24,
 // larger ones saturate at 65504); the kv head's K scale is in ksc, its V
 // scale is applied by the caller.
-template <int D, bool FP8, bool TAIL>
+template <int D, bool FP8, bool QS, bool TAIL>
 __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
-                                            const uint32_t (&off)[Tc<D, FP8>::NT][Tc<D, FP8>::NCP],
-                                            const uint32_t (&qa)[Tc<D, FP8>::KS][2], float ksc, int lim, int valid,
-                                            float &m, float &l, float (&o)[Tc<D, FP8>::MT][4], int lane)
+                                            const uint32_t (&off)[Tc<D, FP8, QS>::NT][Tc<D, FP8, QS>::NCP],
+                                            const uint32_t (&qa)[Tc<D, FP8, QS>::KS][2], float ksc, int lim,
+                                            int valid, float &m, float &l, float (&o)[Tc<D, FP8, QS>::MT][4],
+                                            int lane)
 {
-    using T = Tc<D, FP8>;
+    using T = Tc<D, FP8, QS>;
     constexpr int NT = T::NT;
     constexpr int CH = NT == 1 ? 2 : 1;  // accumulation chains per n-tile (bf16: halves the MMA dependency depth)
     const int r4 = lane & 3;
@@ -800,12 +810,12 @@ __device__ __forceinline__ int slice_of(const long long *bound, int nslots, long
 // (the online-softmax algebra; m in log2 units).  The pieces were written by
 // other SMs, so they are read through L2 (ld.global.cg), BATCH pieces at a
 // time with independent loads, folded into a running (M, l, acc).
-template <int D, int G, bool FP8>
+template <int D, int G, bool FP8, bool QS>
 __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long long *bound, int sf, int sl,
-                                             long long x0, int g, int h, int b, int kvh, int nvh, int lane)
+                                             long long x0, int g, int h, int jq, int b, int kvh, int nvh, int lane)
 {
     constexpr int PER = D / 32;                           // output values per lane
-    constexpr int BATCH = G <= 2 ? 4 : (G <= 7 ? 2 : 1);  // pieces loaded together (G = 8 would spill)
+    constexpr int BATCH = G <= 2 ? 4 : (G <= 5 ? 2 : 1);  // pieces loaded together (more would spill)
     using Vec = typename std::conditional<PER == 4, float4, float2>::type;
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);
     float M[G], lsum[G], a[G][PER];
@@ -825,9 +835,9 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
             const int s = s0 + k;
             use[k] = s <= sl && bound[s + 1] > bound[s];  // empty slices left nothing
             const int sk = use[k] ? s : sf;
-            const long long slot = (slots_by_slice(p.B, p.nhg)
-                                        ? 2LL * sk + ((sk == sf && x0 != bound[sf]) ? 1 : 0)
-                                        : sk + (long long)b * p.nhg + g) * p.hg + h;
+            const long long slot = ((slots_by_slice(p.B, p.nhg)
+                                         ? 2LL * sk + ((sk == sf && x0 != bound[sf]) ? 1 : 0)
+                                         : sk + (long long)b * p.nhg + g) * p.hg + h) * (QS ? p.sub : 1) + jq;
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
                 st[k][hh] = __ldcg(ml + slot * G + hh);
@@ -861,8 +871,8 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
     for (int hh = 0; hh < G; ++hh) {
         if (hh >= nvh) break;  // virtual heads past the entry's queries
         const float inv = (FP8 ? __ldg(p.v_scale + kvh) : 1.0f) / lsum[hh];
-        uint16_t *o = p.out + ((int64_t(b) * p.qstride + hh / p.gq) * p.Hq + int64_t(kvh) * p.gq + hh % p.gq) * D +
-                      lane * PER;
+        uint16_t *o = p.out + ((int64_t(b) * p.qstride + jq * p.qn + hh / p.gq) * p.Hq + int64_t(kvh) * p.gq +
+                               hh % p.gq) * D + lane * PER;
         if constexpr (PER == 4)
             *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16x2(a[hh][0] * inv, a[hh][1] * inv),
                                                        pack_bf16x2(a[hh][2] * inv, a[hh][3] * inv));
@@ -872,16 +882,20 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
 }
 
 // ------------------------------------------------------------------ main kernel
-// Block: p.cons consumer warps (warp w: kv head w / sub of the group, TW-token
-// slice w % sub of every unit) and one producer warp (warp p.cons).
-template <int D, int G, bool FP8>
+// Block: p.cons consumer warps and one producer warp (warp p.cons).  Consumer
+// warp w takes kv head w / sub of the group and, per unit, either the TW-token
+// slice w % sub (QS false: a unit is TW * sub tokens) or all TW tokens for
+// its own qn queries w % sub of the entry's (QS true, hg = 1: the query-split
+// CTA for long runs of new tokens, where the entry's up to sub * qn queries
+// share every K/V tile).
+template <int D, int G, bool FP8, bool QS>
 __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int ES = FP8 ? 1 : 2;  // bytes per cached element
-    const CtaLayout lay = cta_layout(D, G, ES, p.hg, p.sub, p.nst, p.B);
+    const CtaLayout lay = cta_layout(D, G, ES, p.hg, p.sub, p.nst, p.B, QS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     uint8_t *stage0 = smem;
@@ -1029,7 +1043,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                         dead = true;
                         break;
                     }
-                    if (p.qn == 1) {  // the group's G * hg query rows are contiguous
+                    if (p.qn == 1 && !QS) {  // the group's G * hg query rows are contiguous
                         const uint32_t qb = uint32_t(p.hg * G * D * 2);
                         if (lane == 0) {
                             mbar_arrive_expect_tx(&qfull[qs], qb);
@@ -1040,7 +1054,9 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                     } else {
                         // cnt queries: kv head h's virtual heads i * gq .. i * gq + gq - 1 come from row
                         // b * qstride + i; one copy of gq rows per (h, i < cnt), lane t copying pair t
-                        // (the slots of virtual heads past cnt * gq are not loaded: the consumers zero them)
+                        // (the slots of virtual heads past cnt * gq are not loaded: the consumers zero them).
+                        // Query-split (hg = 1): query i is virtual head (i % qn) * gq.. of warp i / qn,
+                        // whose G rows start at (i / qn) * G = (i - i % qn) * gq: the same offset i * gq.
                         if (lane == 0) mbar_arrive_expect_tx(&qfull[qs], uint32_t(p.hg * cnt * p.gq * D * 2));
                         __syncwarp();
                         for (int t = lane; t < p.hg * cnt; t += 32) {
@@ -1123,12 +1139,14 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     }
 
     // ============================== consumer warps ==============================
-    using TC = Tc<D, FP8>;
-    const int h = warp / p.sub, j = warp - h * p.sub;  // kv head in the group, token slice of the unit
+    using TC = Tc<D, FP8, QS>;
+    const int h = warp / p.sub, j = warp - h * p.sub;  // kv head in the group, slice of the unit or queries
+    const int jt = QS ? 0 : j;                         // token slice of the unit
+    const int jq = QS ? j : 0;                         // block of qn queries of the entry
     const int g8 = lane >> 2, r4 = lane & 3;           // fragment row group and column pair of the thread
     const int home = sh[0];
     uint32_t off[TC::NT][TC::NCP];
-    lane_offsets<D, FP8>(off, lane, j, h, p.hg, p.boxtok);
+    lane_offsets<D, FP8, QS>(off, lane, jt, h, p.hg, p.boxtok);
     const uint32_t stage_addr = smem_u32(stage0);
     // several queries per stream: the query of row g8 sees `shift` fewer of the entry's last tokens
     // (set per entry: the entry's last query sees them all)
@@ -1161,11 +1179,12 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                 if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
                 break;
             }
-            nvh = mt.cnt * p.gq;
-            shift = (mt.cnt - 1) - g8 / p.gq;
+            nvh = max(0, min(p.qn, mt.cnt - jq * p.qn)) * p.gq;
+            shift = (mt.cnt - 1) - (jq * p.qn + g8 / p.gq);
             // Q operand fragments of row g8 (zero rows past nvh): k-step ks holds dims 16 ks + 2 r4 (+1)
             // and 16 ks + 8 + 2 r4 (+1) (bf16), or 16 ks + 4 r4 (+1) and 16 ks + 4 r4 + 2 (+3) (E4M3 order)
-            const uint16_t *qr = reinterpret_cast<const uint16_t *>(qbuf + qs * lay.q_bytes) + (h * G + g8) * D;
+            const uint16_t *qr =
+                reinterpret_cast<const uint16_t *>(qbuf + qs * lay.q_bytes) + ((h * (QS ? p.sub : 1) + jq) * G + g8) * D;
 #pragma unroll
             for (int ks = 0; ks < TC::KS; ++ks) {
                 qa[ks][0] = qa[ks][1] = 0u;
@@ -1191,15 +1210,15 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
             ++segs;
             u_first = mt.u;
         }
-        const int tok0 = mt.u * p.toks + j * TC::TW;
+        const int tok0 = mt.u * p.toks + jt * TC::TW;
         const int valid = min(TC::TW, mt.L - tok0);
-        if (valid > 0) {
+        if (valid > 0 && nvh > 0) {
             const uint32_t kb = stage_addr + uint32_t(s) * lay.stage_bytes;
             const int lim = min(valid, mt.L - tok0 - shift);
             if (valid == TC::TW)
-                attend_tile<D, FP8, false>(kb, kb + lay.kv_bytes, off, qa, ksc, lim, valid, m, l, o, lane);
+                attend_tile<D, FP8, QS, false>(kb, kb + lay.kv_bytes, off, qa, ksc, lim, valid, m, l, o, lane);
             else
-                attend_tile<D, FP8, true>(kb, kb + lay.kv_bytes, off, qa, ksc, lim, valid, m, l, o, lane);
+                attend_tile<D, FP8, QS, true>(kb, kb + lay.kv_bytes, off, qa, ksc, lim, valid, m, l, o, lane);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -1209,9 +1228,10 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
             sph ^= 1u;
         }
 
-        if (mt.flags & kLast) {
-            // close this warp's part of (b, group).  Row state -> column state: the thread's output
-            // columns are query heads 2 r4 + e (e = 0, 1), whose rows belong to threads 8 r4 + 4e.
+        if ((mt.flags & kLast) && nvh > 0) {
+            // close this warp's part of (b, group) (a query-split warp without queries has none).
+            // Row state -> column state: the thread's output columns are query heads 2 r4 + e
+            // (e = 0, 1), whose rows belong to threads 8 r4 + 4e.
             float lt = l + __shfl_xor_sync(kFull, l, 1);
             lt += __shfl_xor_sync(kFull, lt, 2);
             float mc[2], lc[2];
@@ -1220,7 +1240,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
             lc[0] = __shfl_sync(kFull, lt, 8 * r4);
             lc[1] = __shfl_sync(kFull, lt, 8 * r4 + 4);
             bool leader = true;
-            if (p.sub > 1) {
+            if (!QS && p.sub > 1) {
                 // the token slices of a kv head are combined by the head's first warp (j == 0):
                 // the others leave their states in shared memory ([G][D] sums, then G maxima, G sums)
                 const uint32_t round = combs++;
@@ -1293,7 +1313,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                         const int hh = 2 * r4 + e;
                         if (hh < nvh) {
                             const float inv = vsc / lc[e];
-                            uint16_t *orow = p.out + (((long long)mt.b * p.qstride + hh / p.gq) * p.Hq +
+                            uint16_t *orow = p.out + (((long long)mt.b * p.qstride + jq * p.qn + hh / p.gq) * p.Hq +
                                                       (long long)kvh * p.gq + hh % p.gq) * D;
 #pragma unroll
                             for (int mi = 0; mi < TC::MT; ++mi) {
@@ -1312,9 +1332,10 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                     // slice's first unit (see ws_layout)
                     const long long x0 = (long long)p.nhg * scan[mt.b] + (long long)mt.g * mt.n;
                     const bool first = u_first > 0 || x0 == bound[mt.slice];
-                    const long long slot = (slots_by_slice(p.B, p.nhg)
-                                                ? 2LL * mt.slice + (first ? 0 : 1)
-                                                : mt.slice + (long long)mt.b * p.nhg + mt.g) * p.hg + h;
+                    const long long slot = ((slots_by_slice(p.B, p.nhg)
+                                                 ? 2LL * mt.slice + (first ? 0 : 1)
+                                                 : mt.slice + (long long)mt.b * p.nhg + mt.g) * p.hg + h) *
+                                               (QS ? p.sub : 1) + jq;
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int hh = 2 * r4 + e;
@@ -1339,13 +1360,13 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                     __syncwarp();
                     int last = 0;
                     if (lane == 0)
-                        last = arrive_last(p.ws_count + (long long)mt.b * p.Hkv + kvh, gen, uint32_t(piece),
-                                           uint32_t(mt.n), p.err);
+                        last = arrive_last(p.ws_count + ((long long)mt.b * p.Hkv + kvh) * (QS ? p.sub : 1) + jq,
+                                           gen, uint32_t(piece), uint32_t(mt.n), p.err);
                     if (__shfl_sync(kFull, last, 0)) {
                         __threadfence();
-                        merge_pieces<D, G, FP8>(p, bound, slice_of(bound, nslots, x0),
-                                                slice_of(bound, nslots, x0 + mt.n - 1), x0, mt.g, h, mt.b,
-                                                kvh, nvh, lane);
+                        merge_pieces<D, G, FP8, QS>(p, bound, slice_of(bound, nslots, x0),
+                                                    slice_of(bound, nslots, x0 + mt.n - 1), x0, mt.g, h, jq, mt.b,
+                                                    kvh, nvh, lane);
                     }
                 }
             }
@@ -1451,7 +1472,7 @@ inline bool cached_cache_map(CUtensorMap *map, int dev, const void *base, bool f
 // driver call; repeating it on every launch costs microseconds).  Keyed on
 // <D, G, FP8>: every variant has the same function-pointer type, so the memo
 // must be per instantiation.
-template <int D, int G, bool FP8, typename Kernel>
+template <int D, int G, bool FP8, bool QS, typename Kernel>
 inline bool ensure_smem_attribute(Kernel kern, int dev, size_t smem)
 {
     static std::mutex mu;
@@ -1469,15 +1490,15 @@ inline bool ensure_smem_attribute(Kernel kern, int dev, size_t smem)
     return true;
 }
 
-template <int D, int G, bool FP8>
+template <int D, int G, bool FP8, bool QS>
 pkv_status launch_decode(LaunchArgs &a)
 {
     DecodeParams &p = a.p;
     // ring depth: as many stages (up to kMaxStages) as the shared memory holds
     int nst = kMaxStages;
     constexpr int ES = FP8 ? 1 : 2;
-    while (nst > 2 && cta_layout(D, G, ES, p.hg, p.sub, nst, p.B).total > uint32_t(a.max_smem)) --nst;
-    const CtaLayout lay = cta_layout(D, G, ES, p.hg, p.sub, nst, p.B);
+    while (nst > 2 && cta_layout(D, G, ES, p.hg, p.sub, nst, p.B, QS).total > uint32_t(a.max_smem)) --nst;
+    const CtaLayout lay = cta_layout(D, G, ES, p.hg, p.sub, nst, p.B, QS);
     if (lay.total > uint32_t(a.max_smem)) return PKV_EUNSUPPORTED;
     p.nst = nst;
 
@@ -1498,8 +1519,8 @@ pkv_status launch_decode(LaunchArgs &a)
         !cached_cache_map(&vmap, a.device, a.v_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok))
         return PKV_ECUDA;
 
-    auto kern = paged_decode_kernel<D, G, FP8>;
-    if (!ensure_smem_attribute<D, G, FP8>(kern, a.device, lay.total)) return PKV_ECUDA;
+    auto kern = paged_decode_kernel<D, G, FP8, QS>;
+    if (!ensure_smem_attribute<D, G, FP8, QS>(kern, a.device, lay.total)) return PKV_ECUDA;
     const cudaError_t e = launch_pdl(kern, dim3(grid), dim3((p.cons + 1) * 32), lay.total, a.stream, kmap, vmap, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -1510,25 +1531,26 @@ pkv_status launch_decode(LaunchArgs &a)
 
 using LaunchFn = pkv_status (*)(LaunchArgs &);
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool QS>
 LaunchFn pick_group(int G)
 {
     switch (G) {
-    case 1: return launch_decode<D, 1, FP8>;
-    case 2: return launch_decode<D, 2, FP8>;
-    case 3: return launch_decode<D, 3, FP8>;
-    case 4: return launch_decode<D, 4, FP8>;
-    case 5: return launch_decode<D, 5, FP8>;
-    case 6: return launch_decode<D, 6, FP8>;
-    case 7: return launch_decode<D, 7, FP8>;
-    case 8: return launch_decode<D, 8, FP8>;
+    case 1: return launch_decode<D, 1, FP8, QS>;
+    case 2: return launch_decode<D, 2, FP8, QS>;
+    case 3: return launch_decode<D, 3, FP8, QS>;
+    case 4: return launch_decode<D, 4, FP8, QS>;
+    case 5: return launch_decode<D, 5, FP8, QS>;
+    case 6: return launch_decode<D, 6, FP8, QS>;
+    case 7: return launch_decode<D, 7, FP8, QS>;
+    case 8: return launch_decode<D, 8, FP8, QS>;
     default: return nullptr;
     }
 }
 
-// Launchers of the E4M3-cache kernels (defined in pkv_decode_fp8.cu, a
-// translation unit of its own so that the two kernel families build in
-// parallel).
+// Launchers of the E4M3-cache kernels and of the query-split bf16 kernels
+// (defined in pkv_decode_fp8.cu and pkv_decode_qs.cu, translation units of
+// their own so that the kernel families build in parallel).
 LaunchFn pick_decode_fp8(int D, int G);
+LaunchFn pick_decode_qs(int D, int G);
 
 }  // namespace pkv
