@@ -210,13 +210,15 @@ PKV_API size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_h
  *                 pkv_paged_decode_workspace_size(...) bytes, 16-byte aligned
  *   num_workers   0 (the default): one CTA per SM; each SM takes a
  *                 contiguous share of the work sized by the speed it showed
- *                 in earlier calls on this workspace.  Otherwise a fixed,
- *                 even split over about num_workers consumer warps (CTAs of
- *                 8 warps), 1..PKV_MAX_WORKERS (testing and tuning).
+ *                 in earlier calls on this workspace -- or, when the call
+ *                 has fewer units (bounded with max_context_len) than the
+ *                 GPU has SMs, one CTA per unit.  Otherwise a fixed, even
+ *                 split over about num_workers consumer warps (CTAs of 8
+ *                 warps), 1..PKV_MAX_WORKERS (testing and tuning).
  * Supported: head_dim in {64, 128}; num_q_heads / num_kv_heads in 1..8;
  * block_size a power of two in [8, 1024]; num_seqs <= PKV_MAX_SEQS;
  * num_blocks * block_size < 2^31.
- * The work list is (sequence, kv-head group, 16 to 128-token unit); each
+ * The work list is (sequence, kv-head group, 16 to 256-token unit); each
  * CTA takes a contiguous range of it, so one sequence may be spread over
  * several CTAs; their partial softmax states are merged in the same kernel
  * by the CTA that completes the sequence's count (split-K /
