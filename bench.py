@@ -89,12 +89,12 @@ def step_bytes(wl) -> dict:
     row = Hkv * D * 2
     decode = int(lens.sum()) * row * 2 + B * Hq * D * 2 * 2          # K+V rows read, q read, out written
     decode_index = B * 4 + int(sum(-(-int(L) // s.block_size) for L in lens)) * 4
-    # the step stores each sequence's new token with the fused slot + store kernel (pkv_decode_store)
-    store = B * row * 2 * 2 + B * 4 * 2                               # k,v read + cache rows written; len + entry
-    slots = 0
+    # the step stores each sequence's new token in the decode launch itself (pkv_paged_decode_store):
+    # its k, v rows read and its cache rows written (the length and table entry are in decode_index)
+    store = B * row * 2 * 2
     L = s.layers
-    return {"decode": decode + decode_index, "store": store, "slots": slots,
-            "step": L * (decode + decode_index + store) + slots, "decode_kv_only": int(lens.sum()) * row * 2}
+    return {"decode": decode + decode_index, "store": store, "fused": decode + decode_index + store,
+            "step": L * (decode + decode_index + store), "decode_kv_only": int(lens.sum()) * row * 2}
 
 
 class ClockSampler:
@@ -197,7 +197,7 @@ def run_pkv(args):
     wsbuf = pkv.alloc_workspace(B, Hq, Hkv, D, dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 2 * len(wl.layers)
+    launches_per_step = len(wl.layers)
     # one new token per sequence: rows [0, B) of the step's k / v (the workload's extra padding rows are
     # for the unfused kv_store's slot -1 path and are not stored by a decode step)
     k_step = [lay.k_new[:B].contiguous() for lay in wl.layers]
@@ -206,12 +206,12 @@ def run_pkv(args):
     def step(dec_events=None, st=None):
         st = stream if st is None else st
         for li, lay in enumerate(wl.layers):
-            pkv.decode_store(k_step[li], v_step[li], wl.block_tables, wl.context_lens, lay.k_cache, lay.v_cache,
-                             err_word=err, stream=st)
+            # one launch per layer: the new token's K/V stored into the cache and attended
             if dec_events is not None:
                 dec_events[li][0].record(st)
-            pkv.paged_decode(lay.q, lay.k_cache, lay.v_cache, wl.block_tables, wl.context_lens, wl.scale,
-                             outs[li], wsbuf, max_context_len=max_ctx, err_word=err, stream=st)
+            pkv.paged_decode_store(lay.q, k_step[li], v_step[li], lay.k_cache, lay.v_cache, wl.block_tables,
+                                   wl.context_lens, wl.scale, outs[li], wsbuf, max_context_len=max_ctx,
+                                   err_word=err, stream=st)
             if dec_events is not None:
                 dec_events[li][1].record(st)
 
@@ -440,9 +440,8 @@ def run_pkv(args):
             d_q[li].copy_(host["q"][li], non_blocking=True)
             d_k[li].copy_(host["k"][li], non_blocking=True)
             d_v[li].copy_(host["v"][li], non_blocking=True)
-            pkv.decode_store(d_k[li], d_v[li], d_bt, d_lens, lay.k_cache, lay.v_cache, err_word=err, stream=stream)
-            pkv.paged_decode(d_q[li], lay.k_cache, lay.v_cache, d_bt, d_lens, wl.scale, outs[li], wsbuf,
-                             max_context_len=max_ctx, err_word=err, stream=stream)
+            pkv.paged_decode_store(d_q[li], d_k[li], d_v[li], lay.k_cache, lay.v_cache, d_bt, d_lens, wl.scale,
+                                   outs[li], wsbuf, max_context_len=max_ctx, err_word=err, stream=stream)
             host["out"][li].copy_(outs[li], non_blocking=True)
         stream.synchronize()
 
@@ -461,7 +460,7 @@ def run_pkv(args):
     nb = step_bytes(wl)
     peak, peak_kind = hbm_peak()
     gbs = job_bandwidth(nb["step"], ws, ms)
-    dec_gbs = nb["decode"] / (dec_mean_ms * 1e-3) / 1e9
+    dec_gbs = nb["fused"] / (dec_mean_ms * 1e-3) / 1e9
     traffic = traffic_from_profile() if args.workload == "qwen3_0p6b" else None
     line = {
         "metric": METRIC,
@@ -487,10 +486,11 @@ def run_pkv(args):
                         "nominal_8TBps": round(100 * gbs / ws / NOMINAL_HBM_GBS, 2)},
         "algorithmic_bytes_per_step": nb["step"],
         "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"kernel": "pkv_paged_decode (paged_decode_kernel + merge)", "bound": "hbm",
+        "roofline": {"kernel": "pkv_paged_decode_store (paged_decode_kernel: store of the new token, attention, "
+                               "split-K merge)", "bound": "hbm",
                      "achieved": round(dec_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(dec_gbs / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": nb["decode"], "mean_launch_us": round(dec_mean_ms * 1e3, 2),
+                     "algorithmic_bytes_per_launch": nb["fused"], "mean_launch_us": round(dec_mean_ms * 1e3, 2),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": round(job_bandwidth(nb["step"], ws, e2e_ms), 1), "unit": "GB/s",

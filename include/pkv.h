@@ -235,6 +235,32 @@ PKV_API pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cache, 
                             int32_t num_workers, int32_t *err_word, pkv_stream_t stream);
 
 /*
+ * pkv_paged_decode_store -- a decode step's store and attention in one
+ * launch: pkv_decode_store followed by pkv_paged_decode, with the same
+ * results (cache bit for bit, outputs within the decode tolerance).
+ *
+ * Row b of k_new and v_new ([num_seqs, num_kv_heads, head_dim] bf16, 16-byte
+ * aligned) is the K and V of sequence b's token at position
+ * context_lens[b] - 1 (already counted in context_lens): it is written to
+ * that position's cache row (block_tables[b][pos / block_size] * block_size +
+ * pos % block_size), and the attention uses it.  slot_mapping may be NULL;
+ * else [num_seqs] int32 receives the rows written (-1 for padding rows,
+ * rejected lengths and rejected block ids).  The block holding a sequence's
+ * new token must not be shared with another sequence of the call (copy-on-
+ * write gives every sequence its own last block).  Other arguments, limits
+ * and errors as pkv_paged_decode; PKV_ERR_BLOCK_RANGE also covers the new
+ * token's block (nothing stored then).
+ */
+PKV_API pkv_status pkv_paged_decode_store(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                                          uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_tables,
+                                          int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                          int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                          int32_t max_context_len, float scale, uint16_t *out,
+                                          int32_t *slot_mapping, void *workspace, size_t workspace_bytes,
+                                          int32_t num_workers, int32_t *err_word, pkv_stream_t stream);
+
+/*
  * pkv_paged_decode_noalloc -- pkv_paged_decode for callers that cannot
  * allocate device memory.  (The pages have no counterpart of this call; it
  * exists for callers of this library.)

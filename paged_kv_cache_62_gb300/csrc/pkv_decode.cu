@@ -28,7 +28,8 @@ static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, 
                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                               int32_t num_blocks, int32_t max_context_len, float scale, uint16_t *out,
                               void *workspace, size_t workspace_bytes, int32_t num_workers, int32_t *err_word,
-                              pkv_stream_t stream)
+                              pkv_stream_t stream, const uint16_t *k_new = nullptr, const uint16_t *v_new = nullptr,
+                              int32_t *slot_out = nullptr)
 {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
         head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 ||
@@ -51,6 +52,9 @@ static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, 
     const int64_t max_units = int64_t(num_kv_heads) * num_seqs * ((len_limit + 7) / 8);
     if (max_units > INT32_MAX) return PKV_EUNSUPPORTED;
     if (qs && (fp8 || !row_cnt)) return PKV_EINVAL;  // query-split entries are chunks of bf16 calls
+    if ((k_new || v_new) && (fp8 || qs || qn != 1 || row_seq || !k_new || !v_new || !aligned16(k_new) ||
+                             !aligned16(v_new)))
+        return PKV_EINVAL;  // the fused store goes with a bf16 decode
     const WsLayout ws = ws_layout(num_seqs, G, num_kv_heads, head_dim, qs);
     if (!workspace || workspace_bytes < ws.total || !aligned16(workspace)) return PKV_EWORKSPACE;
 
@@ -94,6 +98,11 @@ static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, 
     p.qn = qn;
     p.gq = gq;
     p.row_cnt = row_cnt;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache_w = static_cast<uint16_t *>(const_cast<void *>(k_cache));
+    p.v_cache_w = static_cast<uint16_t *>(const_cast<void *>(v_cache));
+    p.slot_out = k_new ? slot_out : nullptr;
     p.qstride = row_cnt ? 1 : qn;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
@@ -129,6 +138,22 @@ extern "C" pkv_status pkv_paged_decode(const uint16_t *q, const uint16_t *k_cach
                        max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                        num_blocks, max_context_len, scale, out, workspace, workspace_bytes, num_workers, err_word,
                        stream);
+}
+
+extern "C" pkv_status pkv_paged_decode_store(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                                             uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_tables,
+                                             int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                             int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                             int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                             int32_t max_context_len, float scale, uint16_t *out,
+                                             int32_t *slot_mapping, void *workspace, size_t workspace_bytes,
+                                             int32_t num_workers, int32_t *err_word, pkv_stream_t stream)
+{
+    if (num_seqs > 0 && (!k_new || !v_new)) return PKV_EINVAL;
+    return decode_call(false, false, 1, q, k_cache, v_cache, nullptr, nullptr, nullptr, nullptr, block_tables,
+                       max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, max_context_len, scale, out, workspace, workspace_bytes, num_workers, err_word,
+                       stream, k_new, v_new, slot_mapping);
 }
 
 extern "C" pkv_status pkv_paged_decode_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,

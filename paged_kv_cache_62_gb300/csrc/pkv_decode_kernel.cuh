@@ -120,6 +120,13 @@ struct DecodeParams {
     // Decode: qn = 1, gq = G, qstride = 1.
     int32_t qn, gq, qstride;
     const int32_t *row_cnt;
+    // Store fused into a decode (bf16, qn = 1): row b of k_new / v_new [B, Hkv, D] is the K/V of
+    // sequence b's token at position L - 1; the kernel writes it to that token's cache row (k_cache_w /
+    // v_cache_w, [NB * bs, Hkv, D]) and attends with it; slot_out[b] (nullable) receives the row (-1
+    // when nothing was stored).  k_new null: a plain decode.
+    const uint16_t *k_new, *v_new;
+    uint16_t *k_cache_w, *v_cache_w;
+    int32_t *slot_out;
 };
 
 // What the producer tells the consumers about the unit in a stage.
@@ -127,6 +134,7 @@ struct alignas(16) UnitMeta {
     int32_t b, g, u, n;            // unit u of the n units of (b, group g); b < 0: no more work
     int32_t L, flags, slice, cnt;  // context length of b, kFirst | kLast | kSliceEnd, slice of the unit,
                                    // queries of entry b
+    int32_t newrow, pad[3];        // fused store: cache row of token L - 1 if the unit holds it, else -1
 };
 constexpr int kFirst = 1;     // first unit of (b, g) in this slice
 constexpr int kLast = 2;      // last unit of (b, g) in this slice
@@ -947,6 +955,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     // share the job.
     for (int b = blockIdx.x; b < p.B; b += gridDim.x)
         if (scan[b + 1] == scan[b]) {
+            if (p.slot_out && threadIdx.x == 0) p.slot_out[b] = -1;  // fused store: nothing stored
             const int rows = p.row_cnt ? __ldg(p.row_cnt + b) : p.qn;
             uint4 *o = reinterpret_cast<uint4 *>(p.out + int64_t(b) * p.qstride * p.Hq * D);
             for (int i = threadIdx.x; i < rows * p.Hq * D / 8; i += blockDim.x) o[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -1079,6 +1088,16 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                         flag_error(p.err, PKV_ERR_BLOCK_RANGE);
                 }
                 const uint32_t nrows = __popc(__ballot_sync(kFull, row >= 0));
+                // fused store: the cache row of the sequence's new token (position L - 1), if this unit
+                // holds it (-1 where its block id was rejected)
+                int32_t newrow = -1;
+                const int32_t u0 = iw.u * p.toks;
+                if (p.k_new && len - 1 >= u0 && len - 1 < u0 + p.toks) {
+                    const int32_t off = len - 1 - u0;
+                    const int32_t rb = __shfl_sync(kFull, row, off >> (__ffs(p.boxtok) - 1));
+                    newrow = rb >= 0 ? rb + (off & (p.boxtok - 1)) : -1;
+                    if (lane == 0 && iw.g == 0 && p.slot_out) p.slot_out[iw.b] = newrow;
+                }
                 uint8_t *st = stage0 + s * lay.stage_bytes;
                 if (lane == 0) {
                     UnitMeta &mt = metas[s];
@@ -1090,6 +1109,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                     mt.flags = flags;
                     mt.slice = slice;
                     mt.cnt = cnt;
+                    mt.newrow = newrow;
                     mbar_arrive_expect_tx(&full[s], 2 * nrows * box_bytes);
                 }
                 __syncwarp();
@@ -1160,6 +1180,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     float m = -INFINITY, l = 0.f;
     float ksc = p.scale_log2;
     float vsc = 1.0f;  // E4M3 caches: the kv head's V scale, applied in the final division
+    uint2 kn = make_uint2(0u, 0u), vn = make_uint2(0u, 0u);  // fused store: 4 elements of the new K / V row
     int u_first = 0;
     for (;;) {
         if (!mbar_wait_bounded(&full[s], sph)) {
@@ -1178,6 +1199,13 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
             if (!mbar_wait_bounded(&qfull[qs], (segs >> 1) & 1u)) {
                 if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
                 break;
+            }
+            if constexpr (!FP8 && !QS) {
+                if (p.k_new && lane < D / 4) {  // the segment's new K/V row, used at its last tile
+                    const long long e = ((long long)mt.b * p.Hkv + mt.g * p.hg + h) * D + lane * 4;
+                    kn = __ldg(reinterpret_cast<const uint2 *>(p.k_new + e));
+                    vn = __ldg(reinterpret_cast<const uint2 *>(p.v_new + e));
+                }
             }
             nvh = max(0, min(p.qn, mt.cnt - jq * p.qn)) * p.gq;
             shift = (mt.cnt - 1) - (jq * p.qn + g8 / p.gq);
@@ -1214,6 +1242,30 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         const int valid = min(TC::TW, mt.L - tok0);
         if (valid > 0 && nvh > 0) {
             const uint32_t kb = stage_addr + uint32_t(s) * lay.stage_bytes;
+            if constexpr (!FP8 && !QS) {
+                // fused store: the tile holding the new token takes its K/V row from k_new / v_new (the
+                // cache row the copy brought is the previous content) and writes it to the cache; no
+                // other CTA reads that row in this kernel (the block of a sequence's last token is its own)
+                const int tl = mt.L - 1 - tok0;
+                if (p.k_new && mt.newrow >= 0 && tl >= 0 && tl < TC::TW) {
+                    if (lane < D / 4) {
+                        const int t = jt * TC::TW + tl, lg = __ffs(p.boxtok) - 1;
+                        const int bi = t >> lg, r = t & (p.boxtok - 1);
+                        const int byte = lane * 8, pp = byte / TC::RB, within = byte % TC::RB;
+                        const uint32_t R = uint32_t((h * TC::NP + pp) * p.boxtok + r);
+                        const uint32_t o = uint32_t(bi * p.boxtok * p.hg * TC::ROWB) + R * TC::RB +
+                                           (swizzled_chunk<TC::RB>(uint32_t(within >> 4), R) << 4) + (within & 15);
+                        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(kb + o), "r"(kn.x), "r"(kn.y) : "memory");
+                        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(kb + lay.kv_bytes + o), "r"(vn.x),
+                                     "r"(vn.y) : "memory");
+                        const long long e = ((long long)mt.newrow * p.Hkv + mt.g * p.hg + h) * D + lane * 4;
+                        *reinterpret_cast<uint2 *>(p.k_cache_w + e) = kn;
+                        *reinterpret_cast<uint2 *>(p.v_cache_w + e) = vn;
+                        fence_proxy_async_smem();  // the ring's next copy into this stage comes after
+                    }
+                    __syncwarp();
+                }
+            }
             const int lim = min(valid, mt.L - tok0 - shift);
             if (valid == TC::TW)
                 attend_tile<D, FP8, QS, false>(kb, kb + lay.kv_bytes, off, qa, ksc, lim, valid, m, l, o, lane);

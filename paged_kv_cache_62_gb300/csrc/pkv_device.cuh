@@ -137,6 +137,9 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return pol;
 }
 
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // ---------------------------------------------------------------- warp-level tensor core (mma.sync)
 // Four 8x8 b16 matrices from shared memory; lane l gives the address of row
 // l % 8 of matrix l / 8 (16 bytes).  .trans transposes each matrix.

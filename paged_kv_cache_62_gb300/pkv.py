@@ -31,6 +31,8 @@ SIGNATURES = {
     "pkv_paged_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "pkv_paged_decode": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                                         _F32, _P, _P, _SZ, _I32, _P, _P]),
+    "pkv_paged_decode_store": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
+                                              _I32, _I32, _F32, _P, _P, _P, _SZ, _I32, _P, _P]),
     "pkv_paged_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                                 _I32, _F32, _P, _I32, _P, _P]),
     "pkv_copy_blocks": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P]),
@@ -170,6 +172,35 @@ def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, 
         _dev(context_lens, torch.int32, "context_lens", 1), B, Hq, Hkv, D, bs, NB, int(max_context_len),
         float(scale), _dev(out, torch.bfloat16, "out", 3), workspace.data_ptr(), workspace.numel(),
         int(num_workers), _opt(err_word), _stream(stream)), "pkv_paged_decode")
+
+
+def paged_decode_store(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                       v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                       out: torch.Tensor, workspace: torch.Tensor, slot_mapping: torch.Tensor | None = None,
+                       max_context_len: int | None = None, num_workers: int = 0,
+                       err_word: torch.Tensor | None = None, stream=None) -> None:
+    """A decode step in one launch: store row b of k_new / v_new at position context_lens[b] - 1 of
+    sequence b and attend over 0..context_lens[b] - 1 (pkv_decode_store + pkv_paged_decode)."""
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape or block_tables.shape[0] != B or context_lens.numel() != B \
+            or out.shape != q.shape or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) \
+            or (slot_mapping is not None and slot_mapping.numel() != B):
+        raise ValueError("paged_decode_store: shape mismatch")
+    mb = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = mb * bs
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA uint8 tensor")
+    _check(load().pkv_paged_decode_store(
+        _dev(q, torch.bfloat16, "q", 3), _dev(k_new, torch.bfloat16, "k_new", 3),
+        _dev(v_new, torch.bfloat16, "v_new", 3), _dev(k_cache, torch.bfloat16, "k_cache", 4),
+        _dev(v_cache, torch.bfloat16, "v_cache", 4), _dev(block_tables, torch.int32, "block_tables", 2), mb,
+        _dev(context_lens, torch.int32, "context_lens", 1), B, Hq, Hkv, D, bs, NB, int(max_context_len),
+        float(scale), _dev(out, torch.bfloat16, "out", 3),
+        None if slot_mapping is None else _dev(slot_mapping, torch.int32, "slot_mapping", 1),
+        workspace.data_ptr(), workspace.numel(), int(num_workers), _opt(err_word), _stream(stream)),
+        "pkv_paged_decode_store")
 
 
 def paged_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,

@@ -143,6 +143,62 @@ def test_fused_decode_store_bit_exact(name):
     assert np.array_equal(W.bits(lay.k_cache), kc_h) and np.array_equal(W.bits(lay.v_cache), vc_h)
 
 
+@pytest.mark.parametrize("name", W.ORDER)
+def test_decode_and_store_in_one_launch(name):
+    """pkv_paged_decode_store: the store (slots and cache bit for bit, as the oracle's slot mapping and
+    store) and the attention over the stored token (within the decode tolerance of the oracle's decode
+    on the stored caches) in one launch; a padding row (context_len 0) stores nothing and gives zeros."""
+    wl = W.make(name, "cuda", layers=1)
+    s, lay = wl.spec, wl.layers[0]
+    B = s.num_seqs
+    lens = wl.context_lens.clone()
+    lens[B // 2] = 0
+    lens_h = lens.cpu().numpy()
+    bt_h = wl.block_tables.cpu().numpy()
+    kc_h, vc_h = W.bits(lay.k_cache), W.bits(lay.v_cache)
+    k_new, v_new = lay.k_new[:B].contiguous(), lay.v_new[:B].contiguous()
+    slots = torch.full((B,), 7, dtype=torch.int32, device="cuda")
+    out = torch.full_like(lay.q, float("nan"))
+    ws = shared_workspace(B, s.num_q_heads, s.num_kv_heads, s.head_dim)
+    err = err_word()
+    pkv.paged_decode_store(lay.q, k_new, v_new, lay.k_cache, lay.v_cache, wl.block_tables, lens, wl.scale, out, ws,
+                           slot_mapping=slots, max_context_len=int(lens_h.max()), err_word=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0, hex(err.item())
+    want_slots = oracle.decode_slot_mapping(bt_h, lens_h, s.block_size, B)
+    assert np.array_equal(slots.cpu().numpy(), want_slots)
+    oracle.kv_store(W.bits(k_new), W.bits(v_new), want_slots, kc_h, vc_h)
+    assert np.array_equal(W.bits(lay.k_cache), kc_h) and np.array_equal(W.bits(lay.v_cache), vc_h)
+    want = oracle.paged_decode(W.bits(lay.q), kc_h, vc_h, bt_h, lens_h, wl.scale, nthreads=NTHREADS)
+    check_close(out, want, name)
+    assert torch.all(out[B // 2].float() == 0)
+
+
+@pytest.mark.parametrize("workers", [1, 7, 333])
+def test_decode_and_store_split_over_workers(workers):
+    """The fused store where the new token's unit lands in a later slice than the sequence's first
+    units (forced splits), over block sizes 8 and 16 (several boxes per unit)."""
+    for bs in (8, 16):
+        lens = [1, 15, 16, 17, 300, 1024, 2, 513]
+        q, kc, vc, bt, lens_t = synth(len(lens), 0, 16, 8, 128, bs, seed=workers * 10 + bs, lens=lens)
+        g = torch.Generator(device="cuda").manual_seed(workers + bs)
+        k_new = torch.randn(len(lens), 8, 128, generator=g, device="cuda").bfloat16()
+        v_new = torch.randn(len(lens), 8, 128, generator=g, device="cuda").bfloat16()
+        kc_h, vc_h = W.bits(kc), W.bits(vc)
+        ws = shared_workspace(len(lens), 16, 8, 128)
+        out = torch.empty_like(q)
+        err = err_word()
+        pkv.paged_decode_store(q, k_new, v_new, kc, vc, bt, lens_t, 0.0884, out, ws, num_workers=workers, err_word=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        slots = oracle.decode_slot_mapping(bt.cpu().numpy(), np.asarray(lens, np.int32), bs, len(lens))
+        oracle.kv_store(W.bits(k_new), W.bits(v_new), slots, kc_h, vc_h)
+        assert np.array_equal(W.bits(kc), kc_h) and np.array_equal(W.bits(vc), vc_h)
+        want = oracle.paged_decode(W.bits(q), kc_h, vc_h, bt.cpu().numpy(), np.asarray(lens, np.int32), 0.0884,
+                                   nthreads=NTHREADS)
+        check_close(out, want, f"workers {workers} bs {bs}")
+
+
 # --------------------------------------------------------------------------- mini-vLLM-style matrix
 def synth(B, L, Hq, Hkv, D, bs, seed, lens=None, extra=5):
     """Random paged problem with a shuffled pool and NaN canaries in unowned rows."""
