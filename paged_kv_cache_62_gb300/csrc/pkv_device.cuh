@@ -194,38 +194,10 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-// Eight bf16 values (one 16-byte word) -> fp32.  A bf16 is the top half of
-// an fp32, so widening is a shift (low element) or a mask (high element).
-__device__ __forceinline__ void unpack8(const uint4 w, float f[8])
-{
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(u[i] << 16);
-        f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
-    }
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
-}
-
-__device__ __forceinline__ uint4 lds128(const void *p)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(smem_u32(p)));
-    return v;
-}
-
-__device__ __forceinline__ float warp_max(float v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
-    return v;
 }
 
 __device__ __forceinline__ float warp_sum(float v)
