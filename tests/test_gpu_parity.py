@@ -287,6 +287,25 @@ def test_many_sequences_slice_numbered_pieces(workers):
         check_close(out, want, f"workers {workers} call {call}")
 
 
+def test_alternating_batches_on_one_workspace():
+    """Two different batches (other tables, lengths and pools) decoded in turn on one workspace: each
+    call finds the previous call's balance table and L2 warm-up hints, which describe the other batch,
+    and must still give exact results."""
+    rng = np.random.default_rng(77)
+    a = synth(48, 0, 16, 8, 128, 256, seed=5, lens=rng.integers(300, 3000, size=48))
+    b = synth(40, 0, 16, 8, 128, 256, seed=6, lens=rng.integers(1, 2500, size=40))
+    want = [oracle_of(*x[:5], 0.0884) for x in (a, b)]
+    ws = pkv.alloc_workspace(48, 16, 8, 128)
+    err = err_word()
+    for call in range(6):
+        q, kc, vc, bt, lens_t = a if call % 2 == 0 else b
+        out = torch.full_like(q, float("nan"))
+        pkv.paged_decode(q, kc, vc, bt, lens_t, 0.0884, out, ws, err_word=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        check_close(out, want[call % 2], f"call {call}")
+
+
 @pytest.mark.parametrize("bs", [16, 256])
 def test_adaptive_split_over_repeated_calls(bs):
     """Default split, eight calls on one workspace: each call sizes its per-SM slices from the
