@@ -337,7 +337,7 @@ def run_pkv(args):
             assert err.item() == 0, f"device error word {err.item():#x}"
             us_p = float(np.mean([c0.elapsed_time(c1) for c0, c1 in pev])) * 1e3
             row = Hkv * D * 2 * 2
-            qe = max(1, 8 // (Hq // Hkv)) * 8  # queries of a query-split entry: 8 warps x max(1, 8 // G)
+            qe = max(1, 16 // (Hq // Hkv)) * 8  # queries of a query-split entry: 8 warps x max(1, 16 // G)
             chunk_rows = int(sum(L - npf + min(c + qe, npf) for L in lens_h for c in range(0, npf, qe))) * row
             per_query = int(sum(L - npf + 1 + i for L in lens_h for i in range(npf))) * row
             mixed = dict(mixed or {})

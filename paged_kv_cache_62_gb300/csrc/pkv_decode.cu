@@ -40,7 +40,7 @@ static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, 
     if (qn < 1) return PKV_EINVAL;
     const int gq = num_q_heads / num_kv_heads;  // query heads per kv head
     const int G = gq * qn;                      // virtual heads per kv head sharing one K/V stream
-    if (G > 8) return PKV_EUNSUPPORTED;
+    if (G > (qs ? 16 : 8)) return PKV_EUNSUPPORTED;  // virtual heads per warp: the MMA tile's rows
     if (!is_pow2(block_size) || block_size < 8 || block_size > 1024) return PKV_EUNSUPPORTED;
     if (int64_t(num_blocks) * block_size > INT32_MAX) return PKV_EUNSUPPORTED;
     if (num_seqs == 0) return PKV_OK;
@@ -300,17 +300,23 @@ __global__ void expand_rows_kernel(const int32_t *__restrict__ cu_seqlens_q, int
 
 inline size_t rows_bytes(int32_t num_rows) { return align256(size_t(num_rows) * 4); }
 
-// Queries per warp: as many as keep its qg * G virtual heads within the 8
-// rows of the MMA tile that the kernel uses.  A query-split entry holds the
-// queries of all team_warps warps of its CTA.
-inline int32_t chunk_queries(int32_t num_q_heads, int32_t num_kv_heads)
+// Queries per warp: as many as keep its qg * G virtual heads within the rows
+// of the MMA tile it uses: 8 for a regular CTA (same-n entries), 16 for a
+// query-split one.  A query-split entry holds the queries of all team_warps
+// warps of its CTA.
+inline int32_t chunk_queries(int32_t num_q_heads, int32_t num_kv_heads, int32_t rows = 8)
 {
-    return std::max(1, 8 / (num_q_heads / num_kv_heads));
+    return std::max(1, rows / (num_q_heads / num_kv_heads));
+}
+
+inline int32_t qs_queries(int32_t num_q_heads, int32_t num_kv_heads)
+{
+    return chunk_queries(num_q_heads, num_kv_heads, 16);
 }
 
 inline int32_t entry_queries(int32_t num_q_heads, int32_t num_kv_heads)
 {
-    const int32_t qg = chunk_queries(num_q_heads, num_kv_heads);
+    const int32_t qg = qs_queries(num_q_heads, num_kv_heads);
     return qg * team_warps(qg * (num_q_heads / num_kv_heads));
 }
 
@@ -324,7 +330,8 @@ extern "C" size_t pkv_paged_attention_workspace_size(int32_t num_rows, int32_t n
     // decode workspace: same-n calls (entries of n <= qg queries, n * G virtual heads), or one
     // query-split entry per row (qg * G virtual heads per warp); then the three row arrays
     const int32_t gq = num_q_heads / num_kv_heads, qg = chunk_queries(num_q_heads, num_kv_heads);
-    size_t dec = std::max(base, ws_layout(num_rows, gq * qg, num_kv_heads, head_dim, true).total);
+    size_t dec = std::max(base, ws_layout(num_rows, gq * qs_queries(num_q_heads, num_kv_heads), num_kv_heads,
+                                          head_dim, true).total);
     for (int32_t qn = 2; qn <= qg; ++qn)
         dec = std::max(dec, pkv_paged_decode_workspace_size(num_rows, num_q_heads * qn, num_kv_heads, head_dim));
     return align256(dec) + 3 * rows_bytes(num_rows);
@@ -373,7 +380,7 @@ extern "C" pkv_status pkv_paged_attention(const uint16_t *q, const uint16_t *k_c
     }
     const pkv_status st = launch_status("expand_rows_kernel launch");
     if (st != PKV_OK) return st;
-    return decode_call(false, true, qg, q, k_cache, v_cache, nullptr, nullptr, row_seq, row_cnt, block_tables,
+    return decode_call(false, true, qs_queries(num_q_heads, num_kv_heads), q, k_cache, v_cache, nullptr, nullptr, row_seq, row_cnt, block_tables,
                        max_blocks_per_seq, row_len, num_rows, num_q_heads, num_kv_heads, head_dim, block_size,
                        num_blocks, max_context_len, scale, out, workspace, dec_bytes, num_workers, err_word, stream);
 }

@@ -369,6 +369,7 @@ struct Tc {
     static constexpr int MT = D / 16;                   // m-tiles of the output product
     static constexpr int NT = FP8 || QS ? 2 : 1;        // 16-token sub-tiles of a warp's tile
     static constexpr int TW = 16 * NT;                  // tokens of a warp's tile (warp_tokens)
+    static constexpr int HR = QS ? 2 : 1;               // 8-row halves of the MMA tile holding virtual heads
 };
 
 __host__ __device__ constexpr int row_bytes_smem(int D, int es) { return D * es >= 128 ? 128 : 64; }
@@ -433,34 +434,41 @@ __device__ __forceinline__ uint32_t f16x2_sat(float lo, float hi)
 }
 
 // One warp tile (NT sub-tiles of 16 tokens) of one (sequence, kv head) for its
-// G query heads (virtual heads) on the tensor cores, m16n8k16 with fp32
+// query heads (virtual heads) on the tensor cores, m16n8k16 with fp32
 // accumulators:
-//   S^T = Q K^T    rows: query heads (row g = lane / 4; rows G..15 are zero),
-//                  columns: 8 tokens per n-tile, k: head dims;
-//   P = 2^(S - m)  the online-softmax weights of the thread's row;
-//   O^T += V^T P^T rows: head dims, columns: query heads, k: tokens.
+//   S^T = Q K^T    rows: virtual heads (the thread's rows are g = lane / 4
+//                  and, with HR = 2, g + 8; rows past the warp's heads are
+//                  zero), columns: 8 tokens per n-tile, k: head dims;
+//   P = 2^(S - m)  the online-softmax weights of the thread's rows;
+//   O^T += V^T P^T rows: head dims, columns: 8 virtual heads per half
+//                  (HR halves), k: tokens.
 // The S^T accumulator fragment of a sub-tile's two n-tiles is, register for
-// register, the P^T operand fragment of its output product, so P never leaves
-// the registers.  kb / vb: shared addresses of the stage's K and V regions.
-// lim: tokens (from the tile's first) below it count for this thread's row
-// (the causal bound of its query); TAIL: tokens from `valid` on are not the
-// sequence's (their rows may hold anything, even NaN), so their V values are
-// zeroed before the product.  E4M3 caches run the products in f16 (every
-// E4M3 value is exact in f16, and so is every bf16 query element of
-// magnitude 2^-14 .. 65504; smaller ones keep f16's subnormal steps of 2^-24,
-// larger ones saturate at 65504); the kv head's K scale is in ksc, its V
-// scale is applied by the caller.
+// register, the P^T operand fragment of its output product (rows 0-7 for
+// half 0, rows 8-15 for half 1), so P never leaves the registers.  kb / vb:
+// shared addresses of the stage's K and V regions.  lim[hr]: tokens (from the
+// tile's first) below it count for the thread's row of half hr (the causal
+// bound of its query); TAIL: tokens from `valid` on are not the sequence's
+// (their rows may hold anything, even NaN), so their V values are zeroed
+// before the product.  E4M3 caches run the products in f16 (every E4M3 value
+// is exact in f16, and so is every bf16 query element of magnitude
+// 2^-14 .. 65504; smaller ones keep f16's subnormal steps of 2^-24, larger
+// ones saturate at 65504); the kv head's K scale is in ksc, its V scale is
+// applied by the caller.
 template <int D, bool FP8, bool QS, bool TAIL>
 __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
                                             const uint32_t (&off)[Tc<D, FP8, QS>::NT][Tc<D, FP8, QS>::NCP],
-                                            const uint32_t (&qa)[Tc<D, FP8, QS>::KS][2], float ksc, int lim,
-                                            int valid, float &m, float &l, float (&o)[Tc<D, FP8, QS>::MT][4],
-                                            int lane)
+                                            const uint32_t (&qa)[Tc<D, FP8, QS>::KS][2 * Tc<D, FP8, QS>::HR],
+                                            float ksc, const int (&lim)[Tc<D, FP8, QS>::HR], int valid,
+                                            float (&m)[Tc<D, FP8, QS>::HR], float (&l)[Tc<D, FP8, QS>::HR],
+                                            float (&o)[Tc<D, FP8, QS>::MT][Tc<D, FP8, QS>::HR][4], int lane)
 {
     using T = Tc<D, FP8, QS>;
-    constexpr int NT = T::NT;
+    constexpr int NT = T::NT, HR = T::HR;
     constexpr int CH = NT == 1 ? 2 : 1;  // accumulation chains per n-tile (bf16: halves the MMA dependency depth)
     const int r4 = lane & 3;
+    // A operand of k-step ks: rows g (qa[ks][0], [1]) and g + 8 (qa[ks][2], [3], zero when HR = 1)
+    auto a1 = [&](int ks) { return HR == 2 ? qa[ks][2 % (2 * HR)] : 0u; };
+    auto a3 = [&](int ks) { return HR == 2 ? qa[ks][3 % (2 * HR)] : 0u; };
     float sa[NT][CH][2][4];  // [sub-tile][chain][n-tile][fragment]
 #pragma unroll
     for (int st = 0; st < NT; ++st)
@@ -478,8 +486,8 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
             ldsm_x4(kb + off[st][i], r0, r1, r2, r3);
             if constexpr (!FP8) {
                 // chunks 2i, 2i+1 = dims 16i..16i+15 = k-step i; r0/r1 tokens 0-7, r2/r3 tokens 8-15
-                mma_bf16_16816(sa[st][i % CH][0], qa[i][0], 0u, qa[i][1], 0u, r0, r1);
-                mma_bf16_16816(sa[st][i % CH][1], qa[i][0], 0u, qa[i][1], 0u, r2, r3);
+                mma_bf16_16816(sa[st][i % CH][0], qa[i][0], a1(i), qa[i][1], a3(i), r0, r1);
+                mma_bf16_16816(sa[st][i % CH][1], qa[i][0], a1(i), qa[i][1], a3(i), r2, r3);
             } else {
                 // chunk 2i (2i+1) = k-step 2i (2i+1); a register holds four codes 4r..4r+3 of a
                 // token: dims (4r, 4r+1) are k-slots (2r, 2r+1), dims (4r+2, 4r+3) k-slots (2r+8, 2r+9)
@@ -488,63 +496,84 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
                 e4m3x4_to_f16x2x2(r1, b[1][0], b[1][1]);
                 e4m3x4_to_f16x2x2(r2, b[2][0], b[2][1]);
                 e4m3x4_to_f16x2x2(r3, b[3][0], b[3][1]);
-                mma_f16_16816(sa[st][0][0], qa[2 * i][0], 0u, qa[2 * i][1], 0u, b[0][0], b[0][1]);
-                mma_f16_16816(sa[st][0][1], qa[2 * i][0], 0u, qa[2 * i][1], 0u, b[2][0], b[2][1]);
-                mma_f16_16816(sa[st][CH - 1][0], qa[2 * i + 1][0], 0u, qa[2 * i + 1][1], 0u, b[1][0], b[1][1]);
-                mma_f16_16816(sa[st][CH - 1][1], qa[2 * i + 1][0], 0u, qa[2 * i + 1][1], 0u, b[3][0], b[3][1]);
+                mma_f16_16816(sa[st][0][0], qa[2 * i][0], a1(2 * i), qa[2 * i][1], a3(2 * i), b[0][0], b[0][1]);
+                mma_f16_16816(sa[st][0][1], qa[2 * i][0], a1(2 * i), qa[2 * i][1], a3(2 * i), b[2][0], b[2][1]);
+                mma_f16_16816(sa[st][CH - 1][0], qa[2 * i + 1][0], a1(2 * i + 1), qa[2 * i + 1][1],
+                              a3(2 * i + 1), b[1][0], b[1][1]);
+                mma_f16_16816(sa[st][CH - 1][1], qa[2 * i + 1][0], a1(2 * i + 1), qa[2 * i + 1][1],
+                              a3(2 * i + 1), b[3][0], b[3][1]);
             }
         }
     }
-    // the thread's scores: row g, tokens 16 st + 8 nt + 2 r4 + e (fragment elements c0, c1 of n-tile nt)
-    float x[NT * 4];
-    bool ok[NT * 4];
+    // the thread's scores: row g (half 0, fragment elements c0, c1) and row g + 8 (half 1, c2, c3),
+    // tokens 16 st + 8 nt + 2 r4 + e
+    float x[HR][NT * 4];
+    bool ok[HR][NT * 4];
 #pragma unroll
-    for (int st = 0; st < NT; ++st)
+    for (int hr = 0; hr < HR; ++hr)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int st = 0; st < NT; ++st)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int k = 4 * st + 2 * nt + e;
-                float sum = sa[st][0][nt][e];
-                if constexpr (CH == 2) sum += sa[st][1][nt][e];
-                ok[k] = 16 * st + 8 * nt + 2 * r4 + e < lim;
-                x[k] = ok[k] ? sum * ksc : -INFINITY;
-            }
-    float mx = x[0];
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int k = 1; k < NT * 4; ++k) mx = fmaxf(mx, x[k]);
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));  // the four threads of a row
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+                for (int e = 0; e < 2; ++e) {
+                    const int k = 4 * st + 2 * nt + e;
+                    float sum = sa[st][0][nt][2 * hr + e];
+                    if constexpr (CH == 2) sum += sa[st][1][nt][2 * hr + e];
+                    ok[hr][k] = 16 * st + 8 * nt + 2 * r4 + e < lim[hr];
+                    x[hr][k] = ok[hr][k] ? sum * ksc : -INFINITY;
+                }
+    float mx[HR];
+    bool grow = false;
+#pragma unroll
+    for (int hr = 0; hr < HR; ++hr) {
+        mx[hr] = x[hr][0];
+#pragma unroll
+        for (int k = 1; k < NT * 4; ++k) mx[hr] = fmaxf(mx[hr], x[hr][k]);
+        mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(kFull, mx[hr], 1));  // the four threads of a row
+        mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(kFull, mx[hr], 2));
+        grow |= mx[hr] > m[hr] + kRescaleSlack;
+    }
     // Online softmax (m, l, acc).  The running max only moves when some score passes it by more
     // than the slack; the first tile with a valid token for the row always moves it (m = -inf).
-    if (__any_sync(kFull, mx > m + kRescaleSlack)) {
-        const float mn = fmaxf(m, mx);
-        const float alpha = mn == -INFINITY ? 1.0f : ex2(m - mn);  // 0 on the row's first valid tile
-        l *= alpha;
-        m = mn;
-        // output columns 2 r4 and 2 r4 + 1 are the rows of threads 8 r4 and 8 r4 + 4
-        const float a0 = __shfl_sync(kFull, alpha, 8 * r4), a1 = __shfl_sync(kFull, alpha, 8 * r4 + 4);
+    if (__any_sync(kFull, grow)) {
 #pragma unroll
-        for (int mt = 0; mt < T::MT; ++mt) {
-            o[mt][0] *= a0;
-            o[mt][1] *= a1;
-            o[mt][2] *= a0;
-            o[mt][3] *= a1;
+        for (int hr = 0; hr < HR; ++hr) {
+            const float mn = fmaxf(m[hr], mx[hr]);
+            const float alpha = mn == -INFINITY ? 1.0f : ex2(m[hr] - mn);  // 0 on the row's first valid tile
+            l[hr] *= alpha;
+            m[hr] = mn;
+            // output columns 2 r4 and 2 r4 + 1 of half hr are the rows of threads 8 r4 and 8 r4 + 4
+            const float a0 = __shfl_sync(kFull, alpha, 8 * r4), a1v = __shfl_sync(kFull, alpha, 8 * r4 + 4);
+#pragma unroll
+            for (int mt = 0; mt < T::MT; ++mt) {
+                o[mt][hr][0] *= a0;
+                o[mt][hr][1] *= a1v;
+                o[mt][hr][2] *= a0;
+                o[mt][hr][3] *= a1v;
+            }
         }
     }
-    float pr[NT * 4];
+    uint32_t pb[HR][NT][2];
 #pragma unroll
-    for (int k = 0; k < NT * 4; ++k) pr[k] = ok[k] ? ex2(x[k] - m) : 0.f;
-    float ps = 0.f;
+    for (int hr = 0; hr < HR; ++hr) {
+        float pr[NT * 4];
 #pragma unroll
-    for (int k = 0; k < NT * 4; ++k) ps += pr[k];
-    l += ps;
+        for (int k = 0; k < NT * 4; ++k) pr[k] = ok[hr][k] ? ex2(x[hr][k] - m[hr]) : 0.f;
+        float ps = 0.f;
+#pragma unroll
+        for (int k = 0; k < NT * 4; ++k) ps += pr[k];
+        l[hr] += ps;
+#pragma unroll
+        for (int st = 0; st < NT; ++st) {
+            pb[hr][st][0] = FP8 ? f16x2_of(pr[4 * st], pr[4 * st + 1]) : pack_bf16x2(pr[4 * st], pr[4 * st + 1]);
+            pb[hr][st][1] =
+                FP8 ? f16x2_of(pr[4 * st + 2], pr[4 * st + 3]) : pack_bf16x2(pr[4 * st + 2], pr[4 * st + 3]);
+        }
+    }
 
 #pragma unroll
     for (int st = 0; st < NT; ++st) {
-        const uint32_t pb0 = FP8 ? f16x2_of(pr[4 * st], pr[4 * st + 1]) : pack_bf16x2(pr[4 * st], pr[4 * st + 1]);
-        const uint32_t pb1 =
-            FP8 ? f16x2_of(pr[4 * st + 2], pr[4 * st + 3]) : pack_bf16x2(pr[4 * st + 2], pr[4 * st + 3]);
         // transposed V tiles: the low half of a register is token 2 r4 (8 + 2 r4) of the sub-tile, the
         // high half the next one
         uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
@@ -565,7 +594,8 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
             }
             if constexpr (!FP8) {
                 // m-tile i: dims 16i + g (r0: tokens 0-7, r2: tokens 8-15) and 16i + 8 + g (r1, r3)
-                mma_bf16_16816(o[i], r0, r1, r2, r3, pb0, pb1);
+#pragma unroll
+                for (int hr = 0; hr < HR; ++hr) mma_bf16_16816(o[i][hr], r0, r1, r2, r3, pb[hr][st][0], pb[hr][st][1]);
             } else {
                 // a register holds (token 2r4: dims 2g, 2g+1 | token 2r4+1: dims 2g, 2g+1) of a 16-dim
                 // chunk; the byte permute pairs the two tokens per dim: low half dim 2g, high half dim 2g+1
@@ -574,8 +604,12 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
                 e4m3x4_to_f16x2x2(__byte_perm(r1, 0u, 0x3120), a[1][0], a[1][1]);
                 e4m3x4_to_f16x2x2(__byte_perm(r2, 0u, 0x3120), a[2][0], a[2][1]);
                 e4m3x4_to_f16x2x2(__byte_perm(r3, 0u, 0x3120), a[3][0], a[3][1]);
-                mma_f16_16816(o[2 * i], a[0][0], a[0][1], a[2][0], a[2][1], pb0, pb1);
-                mma_f16_16816(o[2 * i + 1], a[1][0], a[1][1], a[3][0], a[3][1], pb0, pb1);
+#pragma unroll
+                for (int hr = 0; hr < HR; ++hr) {
+                    mma_f16_16816(o[2 * i][hr], a[0][0], a[0][1], a[2][0], a[2][1], pb[hr][st][0], pb[hr][st][1]);
+                    mma_f16_16816(o[2 * i + 1][hr], a[1][0], a[1][1], a[3][0], a[3][1], pb[hr][st][0],
+                                  pb[hr][st][1]);
+                }
             }
         }
     }
@@ -832,70 +866,75 @@ template <int D, int G, bool FP8, bool QS>
 __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long long *bound, int sf, int sl,
                                              long long x0, int g, int h, int jq, int b, int kvh, int nvh, int lane)
 {
-    constexpr int PER = D / 32;                           // output values per lane
-    constexpr int BATCH = G <= 2 ? 4 : (G <= 5 ? 2 : 1);  // pieces loaded together (more would spill)
+    constexpr int PER = D / 32;                                // output values per lane
+    constexpr int HB = G < 8 ? G : 8;                          // heads merged together (more would spill)
+    constexpr int BATCH = HB <= 2 ? 4 : (HB <= 5 ? 2 : 1);     // pieces loaded together
     using Vec = typename std::conditional<PER == 4, float4, float2>::type;
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);
-    float M[G], lsum[G], a[G][PER];
+    for (int h0 = 0; h0 < nvh; h0 += HB) {  // virtual heads past the entry's queries are not written
+        float M[HB], lsum[HB], a[HB][PER];
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-        M[hh] = -INFINITY;
-        lsum[hh] = 0.f;
+        for (int i = 0; i < HB; ++i) {
+            M[i] = -INFINITY;
+            lsum[i] = 0.f;
 #pragma unroll
-        for (int e = 0; e < PER; ++e) a[hh][e] = 0.f;
-    }
-    for (int s0 = sf; s0 <= sl; s0 += BATCH) {
-        float2 st[BATCH][G];
-        Vec v[BATCH][G];
-        bool use[BATCH];
-#pragma unroll
-        for (int k = 0; k < BATCH; ++k) {
-            const int s = s0 + k;
-            use[k] = s <= sl && bound[s + 1] > bound[s];  // empty slices left nothing
-            const int sk = use[k] ? s : sf;
-            const long long slot = ((slots_by_slice(p.B, p.nhg)
-                                         ? 2LL * sk + ((sk == sf && x0 != bound[sf]) ? 1 : 0)
-                                         : sk + (long long)b * p.nhg + g) * p.hg + h) * (QS ? p.sub : 1) + jq;
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                st[k][hh] = __ldcg(ml + slot * G + hh);
-                v[k][hh] = __ldcg(reinterpret_cast<const Vec *>(p.ws_acc + (slot * G + hh) * D + lane * PER));
-            }
+            for (int e = 0; e < PER; ++e) a[i][e] = 0.f;
         }
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-            float mb = M[hh];
-#pragma unroll
-            for (int k = 0; k < BATCH; ++k)
-                if (use[k]) mb = fmaxf(mb, st[k][hh].x);
-            // 0 while nothing has been folded in (M = -inf); a head with no valid token in any piece
-            // so far (several queries per stream) keeps its zero state
-            const float r = mb == -INFINITY ? 1.0f : ex2(M[hh] - mb);
-            lsum[hh] *= r;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) a[hh][e] *= r;
+        for (int s0 = sf; s0 <= sl; s0 += BATCH) {
+            float2 st[BATCH][HB];
+            Vec v[BATCH][HB];
+            bool use[BATCH];
 #pragma unroll
             for (int k = 0; k < BATCH; ++k) {
-                const float f = (use[k] && st[k][hh].x != -INFINITY) ? ex2(st[k][hh].x - mb) : 0.f;
-                lsum[hh] = fmaf(f, st[k][hh].y, lsum[hh]);
-                const float *x = reinterpret_cast<const float *>(&v[k][hh]);
+                const int s = s0 + k;
+                use[k] = s <= sl && bound[s + 1] > bound[s];  // empty slices left nothing
+                const int sk = use[k] ? s : sf;
+                const long long slot = ((slots_by_slice(p.B, p.nhg)
+                                             ? 2LL * sk + ((sk == sf && x0 != bound[sf]) ? 1 : 0)
+                                             : sk + (long long)b * p.nhg + g) * p.hg + h) * (QS ? p.sub : 1) + jq;
 #pragma unroll
-                for (int e = 0; e < PER; ++e) a[hh][e] = fmaf(f, x[e], a[hh][e]);
+                for (int i = 0; i < HB; ++i) {
+                    const int hh = min(h0 + i, G - 1);  // a block past G re-reads the last head (not written)
+                    st[k][i] = __ldcg(ml + slot * G + hh);
+                    v[k][i] = __ldcg(reinterpret_cast<const Vec *>(p.ws_acc + (slot * G + hh) * D + lane * PER));
+                }
             }
-            M[hh] = mb;
-        }
-    }
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-        if (hh >= nvh) break;  // virtual heads past the entry's queries
-        const float inv = (FP8 ? __ldg(p.v_scale + kvh) : 1.0f) / lsum[hh];
-        uint16_t *o = p.out + ((int64_t(b) * p.qstride + jq * p.qn + hh / p.gq) * p.Hq + int64_t(kvh) * p.gq +
-                               hh % p.gq) * D + lane * PER;
-        if constexpr (PER == 4)
-            *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16x2(a[hh][0] * inv, a[hh][1] * inv),
-                                                       pack_bf16x2(a[hh][2] * inv, a[hh][3] * inv));
-        else
-            *reinterpret_cast<uint32_t *>(o) = pack_bf16x2(a[hh][0] * inv, a[hh][1] * inv);
+            for (int i = 0; i < HB; ++i) {
+                float mb = M[i];
+#pragma unroll
+                for (int k = 0; k < BATCH; ++k)
+                    if (use[k]) mb = fmaxf(mb, st[k][i].x);
+                // 0 while nothing has been folded in (M = -inf); a head with no valid token in any piece
+                // so far (several queries per stream) keeps its zero state
+                const float r = mb == -INFINITY ? 1.0f : ex2(M[i] - mb);
+                lsum[i] *= r;
+#pragma unroll
+                for (int e = 0; e < PER; ++e) a[i][e] *= r;
+#pragma unroll
+                for (int k = 0; k < BATCH; ++k) {
+                    const float f = (use[k] && st[k][i].x != -INFINITY) ? ex2(st[k][i].x - mb) : 0.f;
+                    lsum[i] = fmaf(f, st[k][i].y, lsum[i]);
+                    const float *x = reinterpret_cast<const float *>(&v[k][i]);
+#pragma unroll
+                    for (int e = 0; e < PER; ++e) a[i][e] = fmaf(f, x[e], a[i][e]);
+                }
+                M[i] = mb;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < HB; ++i) {
+            const int hh = h0 + i;
+            if (hh >= nvh) break;
+            const float inv = (FP8 ? __ldg(p.v_scale + kvh) : 1.0f) / lsum[i];
+            uint16_t *o = p.out + ((int64_t(b) * p.qstride + jq * p.qn + hh / p.gq) * p.Hq + int64_t(kvh) * p.gq +
+                                   hh % p.gq) * D + lane * PER;
+            if constexpr (PER == 4)
+                *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16x2(a[i][0] * inv, a[i][1] * inv),
+                                                           pack_bf16x2(a[i][2] * inv, a[i][3] * inv));
+            else
+                *reinterpret_cast<uint32_t *>(o) = pack_bf16x2(a[i][0] * inv, a[i][1] * inv);
+        }
     }
 }
 
@@ -1202,16 +1241,23 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     uint32_t off[TC::NT][TC::NCP];
     lane_offsets<D, FP8, QS>(off, lane, jt, h, p.hg, p.boxtok);
     const uint32_t stage_addr = smem_u32(stage0);
-    // several queries per stream: the query of row g8 sees `shift` fewer of the entry's last tokens
-    // (set per entry: the entry's last query sees them all)
-    int shift = 0;
-    int nvh = G;  // virtual heads of the entry that are queries (the rest are zero rows)
+    constexpr int HR = TC::HR;  // halves of the MMA tile's rows that hold virtual heads
+    // several queries per stream: the query of row g8 + 8 hr sees shift[hr] fewer of the entry's last
+    // tokens (set per entry: the entry's last query sees them all)
+    int shift[HR];
+    int nvh = G;  // virtual heads of this warp that are queries (the rest are zero rows)
     uint32_t kk = 0, segs = 0, combs = 0;
     int s = 0;           // ring slot of stage kk
     uint32_t sph = 0;    // parity of its use
-    uint32_t qa[TC::KS][2];
-    float o[TC::MT][4];
-    float m = -INFINITY, l = 0.f;
+    uint32_t qa[TC::KS][2 * HR];
+    float o[TC::MT][HR][4];
+    float m[HR], l[HR];
+#pragma unroll
+    for (int hr = 0; hr < HR; ++hr) {
+        shift[hr] = 0;
+        m[hr] = -INFINITY;
+        l[hr] = 0.f;
+    }
     float ksc = p.scale_log2;
     float vsc = 1.0f;  // E4M3 caches: the kv head's V scale, applied in the final division
     uint2 kn = make_uint2(0u, 0u), vn = make_uint2(0u, 0u);  // fused store: 4 elements of the new K / V row
@@ -1242,31 +1288,38 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                 }
             }
             nvh = max(0, min(p.qn, mt.cnt - jq * p.qn)) * p.gq;
-            shift = (mt.cnt - 1) - (jq * p.qn + g8 / p.gq);
-            // Q operand fragments of row g8 (zero rows past nvh): k-step ks holds dims 16 ks + 2 r4 (+1)
-            // and 16 ks + 8 + 2 r4 (+1) (bf16), or 16 ks + 4 r4 (+1) and 16 ks + 4 r4 + 2 (+3) (E4M3 order)
-            const uint16_t *qr =
-                reinterpret_cast<const uint16_t *>(qbuf + qs * lay.q_bytes) + ((h * (QS ? p.sub : 1) + jq) * G + g8) * D;
+            // Q operand fragments of rows g8 (qa[ks][0], [1]) and g8 + 8 (qa[ks][2], [3]; HR = 2), zero
+            // past nvh: k-step ks holds dims 16 ks + 2 r4 (+1) and 16 ks + 8 + 2 r4 (+1) (bf16), or
+            // 16 ks + 4 r4 (+1) and 16 ks + 4 r4 + 2 (+3) (E4M3 order)
+            const uint16_t *qw =
+                reinterpret_cast<const uint16_t *>(qbuf + qs * lay.q_bytes) + (h * (QS ? p.sub : 1) + jq) * G * D;
 #pragma unroll
-            for (int ks = 0; ks < TC::KS; ++ks) {
-                qa[ks][0] = qa[ks][1] = 0u;
-                if (g8 < nvh) {
-                    if constexpr (!FP8) {
-                        qa[ks][0] = *reinterpret_cast<const uint32_t *>(qr + 16 * ks + 2 * r4);
-                        qa[ks][1] = *reinterpret_cast<const uint32_t *>(qr + 16 * ks + 8 + 2 * r4);
-                    } else {
-                        const uint2 w = *reinterpret_cast<const uint2 *>(qr + 16 * ks + 4 * r4);
-                        qa[ks][0] = f16x2_sat(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
-                        qa[ks][1] = f16x2_sat(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+            for (int hr = 0; hr < HR; ++hr) {
+                const int row = g8 + 8 * hr;
+                shift[hr] = (mt.cnt - 1) - (jq * p.qn + row / p.gq);
+                const uint16_t *qr = qw + row * D;
+#pragma unroll
+                for (int ks = 0; ks < TC::KS; ++ks) {
+                    qa[ks][2 * hr] = qa[ks][2 * hr + 1] = 0u;
+                    if (row < nvh) {
+                        if constexpr (!FP8) {
+                            qa[ks][2 * hr] = *reinterpret_cast<const uint32_t *>(qr + 16 * ks + 2 * r4);
+                            qa[ks][2 * hr + 1] = *reinterpret_cast<const uint32_t *>(qr + 16 * ks + 8 + 2 * r4);
+                        } else {
+                            const uint2 w = *reinterpret_cast<const uint2 *>(qr + 16 * ks + 4 * r4);
+                            qa[ks][2 * hr] = f16x2_sat(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+                            qa[ks][2 * hr + 1] =
+                                f16x2_sat(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+                        }
                     }
                 }
+#pragma unroll
+                for (int mi = 0; mi < TC::MT; ++mi)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[mi][hr][e] = 0.f;
+                m[hr] = -INFINITY;
+                l[hr] = 0.f;
             }
-#pragma unroll
-            for (int mi = 0; mi < TC::MT; ++mi)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) o[mi][e] = 0.f;
-            m = -INFINITY;
-            l = 0.f;
             __syncwarp();
             if (lane == 0) mbar_arrive(&qempty[qs]);
             ++segs;
@@ -1300,7 +1353,9 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                     __syncwarp();
                 }
             }
-            const int lim = min(valid, mt.L - tok0 - shift);
+            int lim[HR];
+#pragma unroll
+            for (int hr = 0; hr < HR; ++hr) lim[hr] = min(valid, mt.L - tok0 - shift[hr]);
             if (valid == TC::TW)
                 attend_tile<D, FP8, QS, false>(kb, kb + lay.kv_bytes, off, qa, ksc, lim, valid, m, l, o, lane);
             else
@@ -1316,78 +1371,84 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
 
         if ((mt.flags & kLast) && nvh > 0) {
             // close this warp's part of (b, group) (a query-split warp without queries has none).
-            // Row state -> column state: the thread's output columns are query heads 2 r4 + e
-            // (e = 0, 1), whose rows belong to threads 8 r4 + 4e.
-            float lt = l + __shfl_xor_sync(kFull, l, 1);
-            lt += __shfl_xor_sync(kFull, lt, 2);
-            float mc[2], lc[2];
-            mc[0] = __shfl_sync(kFull, m, 8 * r4);
-            mc[1] = __shfl_sync(kFull, m, 8 * r4 + 4);
-            lc[0] = __shfl_sync(kFull, lt, 8 * r4);
-            lc[1] = __shfl_sync(kFull, lt, 8 * r4 + 4);
+            // Row state -> column state: the thread's output columns of half hr are virtual heads
+            // 8 hr + 2 r4 + e (e = 0, 1), whose rows belong to threads 8 r4 + 4e (their half-hr row).
+            float mc[HR][2], lc[HR][2];
+#pragma unroll
+            for (int hr = 0; hr < HR; ++hr) {
+                float lt = l[hr] + __shfl_xor_sync(kFull, l[hr], 1);
+                lt += __shfl_xor_sync(kFull, lt, 2);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    mc[hr][e] = __shfl_sync(kFull, m[hr], 8 * r4 + 4 * e);
+                    lc[hr][e] = __shfl_sync(kFull, lt, 8 * r4 + 4 * e);
+                }
+            }
             bool leader = true;
-            if (!QS && p.sub > 1) {
-                // the token slices of a kv head are combined by the head's first warp (j == 0):
-                // the others leave their states in shared memory ([G][D] sums, then G maxima, G sums)
-                const uint32_t round = combs++;
-                const int cst = comb_stride(D, G);
-                leader = j == 0;
-                if (!leader) {
-                    if (round > 0 && !mbar_wait_bounded(cfree, (round - 1) & 1u)) break;
-                    float *mine = comb + (h * (p.sub - 1) + j - 1) * cst;
+            if constexpr (!QS) {
+                if (p.sub > 1) {
+                    // the token slices of a kv head are combined by the head's first warp (j == 0):
+                    // the others leave their states in shared memory ([G][D] sums, then G maxima, G sums)
+                    const uint32_t round = combs++;
+                    const int cst = comb_stride(D, G);
+                    leader = j == 0;
+                    if (!leader) {
+                        if (round > 0 && !mbar_wait_bounded(cfree, (round - 1) & 1u)) break;
+                        float *mine = comb + (h * (p.sub - 1) + j - 1) * cst;
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int hh = 2 * r4 + e;
-                        if (hh < G) {
-#pragma unroll
-                            for (int mi = 0; mi < TC::MT; ++mi)
-#pragma unroll
-                                for (int half = 0; half < 2; ++half)
-                                    mine[hh * D + dim_of<FP8>(mi, half, g8)] = o[mi][2 * half + e];
-                            if (g8 == 0) {
-                                mine[G * D + hh] = mc[e];
-                                mine[G * D + G + hh] = lc[e];
-                            }
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(cfull);
-                } else {
-                    if (!mbar_wait_bounded(cfull, round & 1u)) break;
-                    const float *others = comb + h * (p.sub - 1) * cst;
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int hh = 2 * r4 + e;
-                        if (hh < G) {
-                            float M = mc[e];
-                            for (int jj = 0; jj < p.sub - 1; ++jj) M = fmaxf(M, others[jj * cst + G * D + hh]);
-                            // M = -inf only when no slice saw a valid token for this head (several
-                            // queries per stream, a piece past the query's last key): the state stays zero
-                            const bool none = M == -INFINITY;
-                            const float f0 = none ? 0.f : ex2(mc[e] - M);
-                            float ls = f0 * lc[e];
-#pragma unroll
-                            for (int mi = 0; mi < TC::MT; ++mi) {
-                                o[mi][e] *= f0;
-                                o[mi][2 + e] *= f0;
-                            }
-                            for (int jj = 0; jj < p.sub - 1; ++jj) {
-                                const float *st2 = others + jj * cst;
-                                const float f = none ? 0.f : ex2(st2[G * D + hh] - M);  // 0: a slice without tokens
-                                ls = fmaf(f, st2[G * D + G + hh], ls);
+                        for (int e = 0; e < 2; ++e) {
+                            const int hh = 2 * r4 + e;
+                            if (hh < G) {
 #pragma unroll
                                 for (int mi = 0; mi < TC::MT; ++mi)
 #pragma unroll
                                     for (int half = 0; half < 2; ++half)
-                                        o[mi][2 * half + e] =
-                                            fmaf(f, st2[hh * D + dim_of<FP8>(mi, half, g8)], o[mi][2 * half + e]);
+                                        mine[hh * D + dim_of<FP8>(mi, half, g8)] = o[mi][0][2 * half + e];
+                                if (g8 == 0) {
+                                    mine[G * D + hh] = mc[0][e];
+                                    mine[G * D + G + hh] = lc[0][e];
+                                }
                             }
-                            mc[e] = M;
-                            lc[e] = ls;
                         }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(cfull);
+                    } else {
+                        if (!mbar_wait_bounded(cfull, round & 1u)) break;
+                        const float *others = comb + h * (p.sub - 1) * cst;
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int hh = 2 * r4 + e;
+                            if (hh < G) {
+                                float M = mc[0][e];
+                                for (int jj = 0; jj < p.sub - 1; ++jj) M = fmaxf(M, others[jj * cst + G * D + hh]);
+                                // M = -inf only when no slice saw a valid token for this head (several
+                                // queries per stream, a piece past the query's last key): the state stays zero
+                                const bool none = M == -INFINITY;
+                                const float f0 = none ? 0.f : ex2(mc[0][e] - M);
+                                float ls = f0 * lc[0][e];
+#pragma unroll
+                                for (int mi = 0; mi < TC::MT; ++mi) {
+                                    o[mi][0][e] *= f0;
+                                    o[mi][0][2 + e] *= f0;
+                                }
+                                for (int jj = 0; jj < p.sub - 1; ++jj) {
+                                    const float *st2 = others + jj * cst;
+                                    const float f = none ? 0.f : ex2(st2[G * D + hh] - M);  // 0: a slice without tokens
+                                    ls = fmaf(f, st2[G * D + G + hh], ls);
+#pragma unroll
+                                    for (int mi = 0; mi < TC::MT; ++mi)
+#pragma unroll
+                                        for (int half = 0; half < 2; ++half)
+                                            o[mi][0][2 * half + e] = fmaf(f, st2[hh * D + dim_of<FP8>(mi, half, g8)],
+                                                                          o[mi][0][2 * half + e]);
+                                }
+                                mc[0][e] = M;
+                                lc[0][e] = ls;
+                            }
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(cfree);
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(cfree);
                 }
             }
             if (leader) {
@@ -1395,24 +1456,27 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                 const int piece = mt.u - u_first + 1;
                 if (piece == mt.n) {  // this CTA ran the whole (b, group): write the output
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int hh = 2 * r4 + e;
-                        if (hh < nvh) {
-                            const float inv = vsc / lc[e];
-                            uint16_t *orow = p.out + (((long long)mt.b * p.qstride + jq * p.qn + hh / p.gq) * p.Hq +
-                                                      (long long)kvh * p.gq + hh % p.gq) * D;
+                    for (int hr = 0; hr < HR; ++hr)
 #pragma unroll
-                            for (int mi = 0; mi < TC::MT; ++mi) {
-                                if constexpr (FP8) {
-                                    *reinterpret_cast<uint32_t *>(orow + dim_of<FP8>(mi, 0, g8)) =
-                                        pack_bf16x2(o[mi][e] * inv, o[mi][2 + e] * inv);
-                                } else {
-                                    orow[dim_of<FP8>(mi, 0, g8)] = uint16_t(pack_bf16x2(o[mi][e] * inv, 0.f));
-                                    orow[dim_of<FP8>(mi, 1, g8)] = uint16_t(pack_bf16x2(o[mi][2 + e] * inv, 0.f));
+                        for (int e = 0; e < 2; ++e) {
+                            const int hh = 8 * hr + 2 * r4 + e;
+                            if (hh < nvh) {
+                                const float inv = vsc / lc[hr][e];
+                                uint16_t *orow = p.out + (((long long)mt.b * p.qstride + jq * p.qn + hh / p.gq) * p.Hq +
+                                                          (long long)kvh * p.gq + hh % p.gq) * D;
+#pragma unroll
+                                for (int mi = 0; mi < TC::MT; ++mi) {
+                                    if constexpr (FP8) {
+                                        *reinterpret_cast<uint32_t *>(orow + dim_of<FP8>(mi, 0, g8)) =
+                                            pack_bf16x2(o[mi][hr][e] * inv, o[mi][hr][2 + e] * inv);
+                                    } else {
+                                        orow[dim_of<FP8>(mi, 0, g8)] = uint16_t(pack_bf16x2(o[mi][hr][e] * inv, 0.f));
+                                        orow[dim_of<FP8>(mi, 1, g8)] =
+                                            uint16_t(pack_bf16x2(o[mi][hr][2 + e] * inv, 0.f));
+                                    }
                                 }
                             }
                         }
-                    }
                 } else {
                     // the segment is its slice's first when it began in an earlier slice or at the
                     // slice's first unit (see ws_layout)
@@ -1423,23 +1487,26 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                                                  : mt.slice + (long long)mt.b * p.nhg + mt.g) * p.hg + h) *
                                                (QS ? p.sub : 1) + jq;
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int hh = 2 * r4 + e;
-                        if (hh < G) {
-                            float *dst = p.ws_acc + (slot * G + hh) * D;
+                    for (int hr = 0; hr < HR; ++hr)
 #pragma unroll
-                            for (int mi = 0; mi < TC::MT; ++mi) {
-                                if constexpr (FP8) {
-                                    *reinterpret_cast<float2 *>(dst + dim_of<FP8>(mi, 0, g8)) =
-                                        make_float2(o[mi][e], o[mi][2 + e]);
-                                } else {
-                                    dst[dim_of<FP8>(mi, 0, g8)] = o[mi][e];
-                                    dst[dim_of<FP8>(mi, 1, g8)] = o[mi][2 + e];
+                        for (int e = 0; e < 2; ++e) {
+                            const int hh = 8 * hr + 2 * r4 + e;
+                            if (hh < G) {
+                                float *dst = p.ws_acc + (slot * G + hh) * D;
+#pragma unroll
+                                for (int mi = 0; mi < TC::MT; ++mi) {
+                                    if constexpr (FP8) {
+                                        *reinterpret_cast<float2 *>(dst + dim_of<FP8>(mi, 0, g8)) =
+                                            make_float2(o[mi][hr][e], o[mi][hr][2 + e]);
+                                    } else {
+                                        dst[dim_of<FP8>(mi, 0, g8)] = o[mi][hr][e];
+                                        dst[dim_of<FP8>(mi, 1, g8)] = o[mi][hr][2 + e];
+                                    }
                                 }
+                                if (g8 == 0)
+                                    reinterpret_cast<float2 *>(p.ws_ml)[slot * G + hh] = make_float2(mc[hr][e], lc[hr][e]);
                             }
-                            if (g8 == 0) reinterpret_cast<float2 *>(p.ws_ml)[slot * G + hh] = make_float2(mc[e], lc[e]);
                         }
-                    }
                     // publish the piece, then count its units in; the CTA that completes the
                     // (b, kv head) merges all pieces
                     __threadfence();
@@ -1459,11 +1526,15 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
             // The segment's state is spent (the next segment starts with kFirst and sets it again);
             // clearing it here tells the compiler so, and it keeps none of it through the merge.
 #pragma unroll
-            for (int ks = 0; ks < TC::KS; ++ks) qa[ks][0] = qa[ks][1] = 0u;
+            for (int ks = 0; ks < TC::KS; ++ks)
+#pragma unroll
+                for (int c = 0; c < 2 * HR; ++c) qa[ks][c] = 0u;
 #pragma unroll
             for (int mi = 0; mi < TC::MT; ++mi)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) o[mi][e] = 0.f;
+                for (int hr = 0; hr < HR; ++hr)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[mi][hr][e] = 0.f;
         }
         if ((mt.flags & kSliceEnd) && adaptive && warp == 0 && lane == 0) {
             // balance record for the next call: this slice's weight and run time, or "absent"
