@@ -62,8 +62,9 @@ constexpr uint32_t kTableMagic = 0x62616c31u;
 constexpr uint32_t kEpochMagic = 0x65706f63u;
 constexpr int32_t kHintMagic = 0x6869;
 // Units of a slice's first block warmed into L2 at the start of a call (measured on the Qwen3-0.6B-shaped
-// batch, 64 KiB units: 3 -> 94.6 us, 6 -> 93.1, 8 -> 92.6, 12 -> 92.0 per call; none: 96.5).
-constexpr int kHintUnits = 12;
+// batch, 64 KiB units: 3 -> 94.6 us, 6 -> 93.1, 8 -> 92.6, 12 -> 92.0 per call; none: 96.5; 16, the whole
+// 256-token block, about 0.3 us less than 12 graph-replayed).
+constexpr int kHintUnits = 16;
 
 // Consumer warps per CTA and tokens each takes from a stage (a stage holds
 // team_warps * warp_tokens token rows of head_dim: 64 KiB for head_dim 128).
