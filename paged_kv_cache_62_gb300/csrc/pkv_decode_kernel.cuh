@@ -93,7 +93,7 @@ struct BalanceState {
     uint32_t tag[2][kMaxSlots];           // (call number of the writer) ^ kTableMagic
     unsigned long long claim[kMaxSlots];  // (gen << 32) | 1 once a CTA took the slice this call
     // First copy of each SM id's own slice in the call that wrote the entry: (cache row, kv head
-    // coordinate, gen ^ kHintMagic, sequence b) and (logical block of the row in b's table, 0, 0, 0).
+    // coordinate, gen ^ kHintMagic, sequence b) and (logical block of the row in b's table, b's length, 0, 0).
     // The next call warms L2 with the rows from there to the end of that block while it sets up (a
     // slice's first unit moves little from one decode step to the next), if b's table still maps
     // that logical block to the row's block.  Only a hint; any contents are safe.
@@ -990,7 +990,10 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                 h0.x >= 0 && h0.x < p.NB * p.bs && h0.y >= 0 && h0.y + p.hg <= p.Hkv &&
                 __ldg(p.block_tables + (long long)h0.w * p.max_blocks + h1.x) == (h0.x >> p.log2_bs)) {
                 const int32_t in_block = h0.x & (p.bs - 1);
-                for (int i = 0; i < kHintUnits && in_block + (i + 1) * p.toks <= p.bs; ++i) {
+                // rows of the block the sequence holds now (one decode step later: one more)
+                const int32_t held = min(p.bs, h1.y + 1 - h1.x * p.bs);
+                for (int i = 0; i < kHintUnits && in_block + i * p.toks < held && in_block + (i + 1) * p.toks <= p.bs;
+                     ++i) {
                     tma_prefetch_4d(&kmap, 0, h0.x + i * p.toks, 0, h0.y);
                     tma_prefetch_4d(&vmap, 0, h0.x + i * p.toks, 0, h0.y);
                 }
@@ -1185,7 +1188,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                 if (k == 0 && lane == 0 && adaptive && !p.row_seq && slice == sh[0] && row >= 0 &&
                     my_sm < unsigned(kMaxSlots)) {
                     p.ws_bal->hint[my_sm][0] = make_int4(row, iw.g * p.hg, int32_t(gen) ^ kHintMagic, iw.b);
-                    p.ws_bal->hint[my_sm][1] = make_int4((iw.u * p.toks) >> p.log2_bs, 0, 0, 0);
+                    p.ws_bal->hint[my_sm][1] = make_int4((iw.u * p.toks) >> p.log2_bs, len, 0, 0);
                 }
                 if (row >= 0) {  // box j: lane j, one copy per cache
                     tma_load_4d(st + lane * box_bytes, &kmap, 0, row, 0, iw.g * p.hg, &full[s], policy);
