@@ -215,7 +215,8 @@ PKV_API size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_h
  *                 GPU has SMs, one CTA per unit.  Otherwise a fixed, even
  *                 split over about num_workers consumer warps (CTAs of 8
  *                 warps), 1..PKV_MAX_WORKERS (testing and tuning).
- * Supported: head_dim in {64, 128}; num_q_heads / num_kv_heads in 1..8;
+ * Supported: head_dim in {64, 128}; num_q_heads / num_kv_heads in 1..16
+ * (bf16 caches; 1..8 for E4M3 caches);
  * block_size a power of two in [8, 1024]; num_seqs <= PKV_MAX_SEQS;
  * num_blocks * block_size < 2^31.
  * The work list is (sequence, kv-head group, 16 to 256-token unit); each

@@ -40,7 +40,7 @@ static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, 
     if (qn < 1) return PKV_EINVAL;
     const int gq = num_q_heads / num_kv_heads;  // query heads per kv head
     const int G = gq * qn;                      // virtual heads per kv head sharing one K/V stream
-    if (G > (qs ? 16 : 8)) return PKV_EUNSUPPORTED;  // virtual heads per warp: the MMA tile's rows
+    if (G > (fp8 ? 8 : 16)) return PKV_EUNSUPPORTED;  // virtual heads per warp: the MMA tile's rows
     if (!is_pow2(block_size) || block_size < 8 || block_size > 1024) return PKV_EUNSUPPORTED;
     if (int64_t(num_blocks) * block_size > INT32_MAX) return PKV_EUNSUPPORTED;
     if (num_seqs == 0) return PKV_OK;
@@ -119,9 +119,10 @@ static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, 
     }
     a.stream = reinterpret_cast<cudaStream_t>(stream);
 
-    LaunchFn fn = fp8  ? pick_decode_fp8(head_dim, G)
-                  : qs ? pick_decode_qs(head_dim, G)
-                       : (head_dim == 64 ? pick_group<64, false, false>(G) : pick_group<128, false, false>(G));
+    LaunchFn fn = fp8    ? pick_decode_fp8(head_dim, G)
+                  : qs   ? pick_decode_qs(head_dim, G)
+                  : G > 8 ? pick_decode_wide(head_dim, G)
+                         : (head_dim == 64 ? pick_group<64, false, false>(G) : pick_group<128, false, false>(G));
     if (!fn) return PKV_EUNSUPPORTED;
     return fn(a);
 }
@@ -328,12 +329,12 @@ extern "C" size_t pkv_paged_attention_workspace_size(int32_t num_rows, int32_t n
     const size_t base = pkv_paged_decode_workspace_size(num_rows, num_q_heads, num_kv_heads, head_dim);
     if (base == 0) return 0;
     // decode workspace: same-n calls (entries of n <= qg queries, n * G virtual heads), or one
-    // query-split entry per row (qg * G virtual heads per warp); then the three row arrays
-    const int32_t gq = num_q_heads / num_kv_heads, qg = chunk_queries(num_q_heads, num_kv_heads);
-    size_t dec = std::max(base, ws_layout(num_rows, gq * qs_queries(num_q_heads, num_kv_heads), num_kv_heads,
-                                          head_dim, true).total);
+    // chunk entry per row (qg * G virtual heads a warp, on a regular or a query-split CTA); then the
+    // three row arrays
+    const int32_t gq = num_q_heads / num_kv_heads, qg = qs_queries(num_q_heads, num_kv_heads);
+    size_t dec = std::max(base, ws_layout(num_rows, gq * qg, num_kv_heads, head_dim, true).total);
     for (int32_t qn = 2; qn <= qg; ++qn)
-        dec = std::max(dec, pkv_paged_decode_workspace_size(num_rows, num_q_heads * qn, num_kv_heads, head_dim));
+        dec = std::max(dec, ws_layout(num_rows, gq * qn, num_kv_heads, head_dim).total);
     return align256(dec) + 3 * rows_bytes(num_rows);
 }
 
@@ -354,16 +355,21 @@ extern "C" pkv_status pkv_paged_attention(const uint16_t *q, const uint16_t *k_c
     const size_t need = pkv_paged_attention_workspace_size(num_rows, num_q_heads, num_kv_heads, head_dim);
     if (need == 0) return num_rows > PKV_MAX_SEQS ? PKV_EUNSUPPORTED : PKV_EINVAL;
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PKV_EWORKSPACE;
-    const int32_t qg = chunk_queries(num_q_heads, num_kv_heads);
+    // Up to qg queries of a sequence fit one regular CTA warp's MMA tile (qg * G <= 16 virtual heads):
+    // the CTA's warps split the K/V tokens, as in decode.  Longer runs of new tokens go to query-split
+    // CTAs, whose warps split an entry of up to 8 * qg queries and share every K/V tile.
+    const int32_t qg = qs_queries(num_q_heads, num_kv_heads);
     if (new_per_seq > 1 && new_per_seq <= qg)
         // every sequence's n new tokens share its K/V stream: read once, n * G virtual heads
         return decode_call(false, false, new_per_seq, q, k_cache, v_cache, nullptr, nullptr, nullptr, nullptr,
                            block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
                            head_dim, block_size, num_blocks, max_context_len, scale, out, workspace,
                            workspace_bytes, num_workers, err_word, stream);
-    // query-split entries: chunks of up to qg * team_warps queries of a sequence (each warp of the
-    // CTA takes qg of them, all warps on the same K/V tiles), one entry per row; the row arrays sit
-    // after the decode workspace
+    // chunks of a sequence's queries, one entry per row; few new tokens per sequence on average (at
+    // most two regular chunks): chunks of qg on regular CTAs, else chunks of 8 * qg on query-split ones.
+    // The row arrays sit after the decode workspace.
+    const bool qs = int64_t(num_rows) > 2 * int64_t(qg) * num_seqs;
+    const int32_t chunk = qs ? entry_queries(num_q_heads, num_kv_heads) : qg;
     uint8_t *wsb = static_cast<uint8_t *>(workspace);
     const size_t dec_bytes = need - 3 * rows_bytes(num_rows);
     int32_t *row_seq = reinterpret_cast<int32_t *>(wsb + dec_bytes);
@@ -371,16 +377,15 @@ extern "C" pkv_status pkv_paged_attention(const uint16_t *q, const uint16_t *k_c
     int32_t *row_cnt = reinterpret_cast<int32_t *>(wsb + dec_bytes + 2 * rows_bytes(num_rows));
     const cudaError_t e = launch_pdl(expand_rows_kernel, dim3((num_rows + 255) / 256), dim3(256), 0,
                                      reinterpret_cast<cudaStream_t>(stream), new_per_seq > 0 ? nullptr : cu_seqlens_q,
-                                     new_per_seq, context_lens, num_seqs, num_rows,
-                                     entry_queries(num_q_heads, num_kv_heads), row_seq, row_len, row_cnt,
-                                     err_word);
+                                     new_per_seq, context_lens, num_seqs, num_rows, chunk, row_seq, row_len,
+                                     row_cnt, err_word);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return cuda_fail("expand_rows_kernel launch", e);
     }
     const pkv_status st = launch_status("expand_rows_kernel launch");
     if (st != PKV_OK) return st;
-    return decode_call(false, true, qs_queries(num_q_heads, num_kv_heads), q, k_cache, v_cache, nullptr, nullptr, row_seq, row_cnt, block_tables,
+    return decode_call(false, qs, qg, q, k_cache, v_cache, nullptr, nullptr, row_seq, row_cnt, block_tables,
                        max_blocks_per_seq, row_len, num_rows, num_q_heads, num_kv_heads, head_dim, block_size,
                        num_blocks, max_context_len, scale, out, workspace, dec_bytes, num_workers, err_word, stream);
 }

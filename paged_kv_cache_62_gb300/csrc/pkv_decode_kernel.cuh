@@ -359,7 +359,9 @@ constexpr float kRescaleSlack = 8.0f;
 // 64-dim E4M3 caches).
 // The chunks of eight consecutive tokens then sit in eight different bank
 // groups, and one ldmatrix reads them without a conflict.
-template <int D, bool FP8, bool QS = false>
+// HR: 8-row halves of the MMA tile that hold a warp's virtual heads (2 when
+// a warp has more than 8).
+template <int D, bool FP8, bool QS = false, int HR_ = 1>
 struct Tc {
     static constexpr int ES = FP8 ? 1 : 2;              // bytes per cached element
     static constexpr int ROWB = D * ES;                 // bytes per cached row
@@ -370,7 +372,7 @@ struct Tc {
     static constexpr int MT = D / 16;                   // m-tiles of the output product
     static constexpr int NT = FP8 || QS ? 2 : 1;        // 16-token sub-tiles of a warp's tile
     static constexpr int TW = 16 * NT;                  // tokens of a warp's tile (warp_tokens)
-    static constexpr int HR = QS ? 2 : 1;               // 8-row halves of the MMA tile holding virtual heads
+    static constexpr int HR = HR_;                      // 8-row halves of the MMA tile holding virtual heads
 };
 
 __host__ __device__ constexpr int row_bytes_smem(int D, int es) { return D * es >= 128 ? 128 : 64; }
@@ -455,15 +457,15 @@ __device__ __forceinline__ uint32_t f16x2_sat(float lo, float hi)
 // 2^-14 .. 65504; smaller ones keep f16's subnormal steps of 2^-24, larger
 // ones saturate at 65504); the kv head's K scale is in ksc, its V scale is
 // applied by the caller.
-template <int D, bool FP8, bool QS, bool TAIL>
+template <int D, bool FP8, bool QS, int HR_, bool TAIL>
 __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
-                                            const uint32_t (&off)[Tc<D, FP8, QS>::NT][Tc<D, FP8, QS>::NCP],
-                                            const uint32_t (&qa)[Tc<D, FP8, QS>::KS][2 * Tc<D, FP8, QS>::HR],
-                                            float ksc, const int (&lim)[Tc<D, FP8, QS>::HR], int valid,
-                                            float (&m)[Tc<D, FP8, QS>::HR], float (&l)[Tc<D, FP8, QS>::HR],
-                                            float (&o)[Tc<D, FP8, QS>::MT][Tc<D, FP8, QS>::HR][4], int lane)
+                                            const uint32_t (&off)[Tc<D, FP8, QS, HR_>::NT][Tc<D, FP8, QS, HR_>::NCP],
+                                            const uint32_t (&qa)[Tc<D, FP8, QS, HR_>::KS][2 * Tc<D, FP8, QS, HR_>::HR],
+                                            float ksc, const int (&lim)[Tc<D, FP8, QS, HR_>::HR], int valid,
+                                            float (&m)[Tc<D, FP8, QS, HR_>::HR], float (&l)[Tc<D, FP8, QS, HR_>::HR],
+                                            float (&o)[Tc<D, FP8, QS, HR_>::MT][Tc<D, FP8, QS, HR_>::HR][4], int lane)
 {
-    using T = Tc<D, FP8, QS>;
+    using T = Tc<D, FP8, QS, HR_>;
     constexpr int NT = T::NT, HR = T::HR;
     constexpr int CH = NT == 1 ? 2 : 1;  // accumulation chains per n-tile (bf16: halves the MMA dependency depth)
     const int r4 = lane & 3;
@@ -1236,7 +1238,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     }
 
     // ============================== consumer warps ==============================
-    using TC = Tc<D, FP8, QS>;
+    using TC = Tc<D, FP8, QS, (G > 8 ? 2 : 1)>;
     const int h = warp / p.sub, j = warp - h * p.sub;  // kv head in the group, slice of the unit or queries
     const int jt = QS ? 0 : j;                         // token slice of the unit
     const int jq = QS ? j : 0;                         // block of qn queries of the entry
@@ -1361,9 +1363,9 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
 #pragma unroll
             for (int hr = 0; hr < HR; ++hr) lim[hr] = min(valid, mt.L - tok0 - shift[hr]);
             if (valid == TC::TW)
-                attend_tile<D, FP8, QS, false>(kb, kb + lay.kv_bytes, off, qa, ksc, lim, valid, m, l, o, lane);
+                attend_tile<D, FP8, QS, TC::HR, false>(kb, kb + lay.kv_bytes, off, qa, ksc, lim, valid, m, l, o, lane);
             else
-                attend_tile<D, FP8, QS, true>(kb, kb + lay.kv_bytes, off, qa, ksc, lim, valid, m, l, o, lane);
+                attend_tile<D, FP8, QS, TC::HR, true>(kb, kb + lay.kv_bytes, off, qa, ksc, lim, valid, m, l, o, lane);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -1400,56 +1402,63 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                         if (round > 0 && !mbar_wait_bounded(cfree, (round - 1) & 1u)) break;
                         float *mine = comb + (h * (p.sub - 1) + j - 1) * cst;
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int hh = 2 * r4 + e;
-                            if (hh < G) {
+                        for (int hr = 0; hr < HR; ++hr)
 #pragma unroll
-                                for (int mi = 0; mi < TC::MT; ++mi)
+                            for (int e = 0; e < 2; ++e) {
+                                const int hh = 8 * hr + 2 * r4 + e;
+                                if (hh < G) {
 #pragma unroll
-                                    for (int half = 0; half < 2; ++half)
-                                        mine[hh * D + dim_of<FP8>(mi, half, g8)] = o[mi][0][2 * half + e];
-                                if (g8 == 0) {
-                                    mine[G * D + hh] = mc[0][e];
-                                    mine[G * D + G + hh] = lc[0][e];
+                                    for (int mi = 0; mi < TC::MT; ++mi)
+#pragma unroll
+                                        for (int half = 0; half < 2; ++half)
+                                            mine[hh * D + dim_of<FP8>(mi, half, g8)] = o[mi][hr][2 * half + e];
+                                    if (g8 == 0) {
+                                        mine[G * D + hh] = mc[hr][e];
+                                        mine[G * D + G + hh] = lc[hr][e];
+                                    }
                                 }
                             }
-                        }
                         __syncwarp();
                         if (lane == 0) mbar_arrive(cfull);
                     } else {
                         if (!mbar_wait_bounded(cfull, round & 1u)) break;
                         const float *others = comb + h * (p.sub - 1) * cst;
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int hh = 2 * r4 + e;
-                            if (hh < G) {
-                                float M = mc[0][e];
-                                for (int jj = 0; jj < p.sub - 1; ++jj) M = fmaxf(M, others[jj * cst + G * D + hh]);
-                                // M = -inf only when no slice saw a valid token for this head (several
-                                // queries per stream, a piece past the query's last key): the state stays zero
-                                const bool none = M == -INFINITY;
-                                const float f0 = none ? 0.f : ex2(mc[0][e] - M);
-                                float ls = f0 * lc[0][e];
+                        for (int hr = 0; hr < HR; ++hr)
 #pragma unroll
-                                for (int mi = 0; mi < TC::MT; ++mi) {
-                                    o[mi][0][e] *= f0;
-                                    o[mi][0][2 + e] *= f0;
+                            for (int e = 0; e < 2; ++e) {
+                                const int hh = 8 * hr + 2 * r4 + e;
+                                if (hh < G) {
+                                    float M = mc[hr][e];
+                                    for (int jj = 0; jj < p.sub - 1; ++jj)
+                                        M = fmaxf(M, others[jj * cst + G * D + hh]);
+                                    // M = -inf only when no slice saw a valid token for this head (several
+                                    // queries per stream, a piece past the query's last key): the state stays zero
+                                    const bool none = M == -INFINITY;
+                                    const float f0 = none ? 0.f : ex2(mc[hr][e] - M);
+                                    float ls = f0 * lc[hr][e];
+#pragma unroll
+                                    for (int mi = 0; mi < TC::MT; ++mi) {
+                                        o[mi][hr][e] *= f0;
+                                        o[mi][hr][2 + e] *= f0;
+                                    }
+                                    for (int jj = 0; jj < p.sub - 1; ++jj) {
+                                        const float *st2 = others + jj * cst;
+                                        // 0: a slice without tokens
+                                        const float f = none ? 0.f : ex2(st2[G * D + hh] - M);
+                                        ls = fmaf(f, st2[G * D + G + hh], ls);
+#pragma unroll
+                                        for (int mi = 0; mi < TC::MT; ++mi)
+#pragma unroll
+                                            for (int half = 0; half < 2; ++half)
+                                                o[mi][hr][2 * half + e] =
+                                                    fmaf(f, st2[hh * D + dim_of<FP8>(mi, half, g8)],
+                                                         o[mi][hr][2 * half + e]);
+                                    }
+                                    mc[hr][e] = M;
+                                    lc[hr][e] = ls;
                                 }
-                                for (int jj = 0; jj < p.sub - 1; ++jj) {
-                                    const float *st2 = others + jj * cst;
-                                    const float f = none ? 0.f : ex2(st2[G * D + hh] - M);  // 0: a slice without tokens
-                                    ls = fmaf(f, st2[G * D + G + hh], ls);
-#pragma unroll
-                                    for (int mi = 0; mi < TC::MT; ++mi)
-#pragma unroll
-                                        for (int half = 0; half < 2; ++half)
-                                            o[mi][0][2 * half + e] = fmaf(f, st2[hh * D + dim_of<FP8>(mi, half, g8)],
-                                                                          o[mi][0][2 * half + e]);
-                                }
-                                mc[0][e] = M;
-                                lc[0][e] = ls;
                             }
-                        }
                         __syncwarp();
                         if (lane == 0) mbar_arrive(cfree);
                     }
@@ -1708,10 +1717,12 @@ LaunchFn pick_group(int G)
     }
 }
 
-// Launchers of the E4M3-cache kernels and of the query-split bf16 kernels
-// (defined in pkv_decode_fp8.cu and pkv_decode_qs.cu, translation units of
-// their own so that the kernel families build in parallel).
+// Launchers of the E4M3-cache kernels, the query-split bf16 kernels and the
+// regular bf16 kernels for 9 to 16 virtual heads (defined in
+// pkv_decode_fp8.cu, pkv_decode_qs.cu and pkv_decode_wide.cu, translation
+// units of their own so that the kernel families build in parallel).
 LaunchFn pick_decode_fp8(int D, int G);
 LaunchFn pick_decode_qs(int D, int G);
+LaunchFn pick_decode_wide(int D, int G);  // regular bf16 CTAs, 9 to 16 virtual heads (pkv_decode_wide.cu)
 
 }  // namespace pkv

@@ -79,7 +79,7 @@ def decode_args(**kw):
     (dict(out=NULL), pkv.EINVAL),
     (dict(Hq=12), pkv.EINVAL),                 # 12 % 8
     (dict(D=96), pkv.EUNSUPPORTED),
-    (dict(Hq=72, Hkv=8), pkv.EUNSUPPORTED),    # group of 9
+    (dict(Hq=136, Hkv=8), pkv.EUNSUPPORTED),   # group of 17 (bf16 caches take up to 16)
     (dict(bs=12), pkv.EUNSUPPORTED),
     (dict(bs=4), pkv.EUNSUPPORTED),
     (dict(bs=2048), pkv.EUNSUPPORTED),

@@ -148,6 +148,21 @@ def test_prefill_batch_past_512_entries(workers):
     check_close(out, oracle_of(q, kc, vc, bt, cu, lens_t, 0.125), f"workers {workers}")
 
 
+@pytest.mark.parametrize("Hq,Hkv,D,workers", [(16, 8, 128, 0), (16, 8, 128, 97), (14, 2, 64, 0), (8, 8, 64, 0)])
+def test_short_runs_of_new_tokens_on_regular_ctas(Hq, Hkv, D, workers):
+    """A batch of short runs (speculative verify steps and decodes, offsets given, at most two chunks of
+    16 / G queries per sequence on average): chunks on regular CTAs, up to 16 (query, head) pairs a warp."""
+    rng = np.random.default_rng(Hq + Hkv + workers)
+    news = rng.integers(1, 9, size=24).tolist()
+    lens = [int(n) + int(x) for n, x in zip(news, rng.integers(0, 1500, size=24))]
+    q, kc, vc, bt, cu, lens_t = mixed_batch(lens, news, Hq, Hkv, D, 16, seed=Hq * 3 + workers)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run(q, kc, vc, bt, cu, lens_t, 0.0884, workers=workers, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    check_close(out, oracle_of(q, kc, vc, bt, cu, lens_t, 0.0884), f"{Hq}/{Hkv} D{D} workers {workers}")
+
+
 def test_same_n_with_a_too_short_sequence():
     """new_per_seq = n with a sequence of fewer than n cached tokens: its rows are zero and the
     error word says so; the other sequences are exact (the n queries share one pass)."""
@@ -173,11 +188,14 @@ def test_same_n_with_a_too_short_sequence():
 @pytest.mark.parametrize("n,Hq,Hkv,D,bs,workers", [(2, 16, 8, 128, 16, 0), (3, 16, 8, 128, 256, 0),
                                                    (4, 16, 8, 128, 16, 0), (4, 16, 8, 128, 8, 333),
                                                    (8, 4, 4, 64, 16, 0), (4, 14, 2, 64, 16, 1),
-                                                   (5, 16, 8, 128, 16, 0)])
+                                                   (5, 16, 8, 128, 16, 0), (8, 16, 8, 128, 16, 0),
+                                                   (8, 16, 8, 128, 256, 250), (16, 8, 8, 64, 16, 0),
+                                                   (12, 16, 8, 128, 16, 77), (6, 12, 2, 128, 8, 0)])
 def test_uniform_new_tokens_share_one_pass(n, Hq, Hkv, D, bs, workers):
-    """Every sequence with n new tokens (new_per_seq = n): when n * G <= 8 the n queries are n * G virtual
-    heads of a kv head over one pass of its keys, each with its own causal bound -- including pieces of a
-    split where some virtual head sees no key at all; otherwise the rows run one by one."""
+    """Every sequence with n new tokens (new_per_seq = n): when n * G <= 16 the n queries are n * G virtual
+    heads of a kv head over one pass of its keys (both 8-row halves of the MMA tile past 8), each with its
+    own causal bound -- including pieces of a split where some virtual head sees no key at all; longer runs
+    go in chunks (of 16 / G queries on regular CTAs, or of 8 x that on query-split CTAs)."""
     rng = np.random.default_rng(n * 100 + Hq + bs)
     lens = rng.integers(n, 1500, size=12).tolist() + [n, n + 1, 16 + n - 1]
     news = [n] * len(lens)

@@ -247,7 +247,7 @@ def test_kernel_matrix(B, bs, heads, D):
         check_close(out, oracle_of(q, kc, vc, bt, lens, scale), f"B{B} L{L} bs{bs} {Hq}/{Hkv} D{D}")
 
 
-@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 16])
 @pytest.mark.parametrize("D", [64, 128])
 def test_every_group_size(G, D):
     Hkv = 2
