@@ -323,13 +323,14 @@ PKV_API pkv_status pkv_paged_decode_noalloc(const uint16_t *q, const uint16_t *k
  *                 cu_seqlens_q may be NULL) -- a speculative-decoding verify
  *                 step, say.
  * Consecutive queries of a sequence share passes over its keys: with
- * G = num_q_heads / num_kv_heads, chunks of Q = 8 * max(1, 16 / G) queries
- * (64 at G = 2; the last one of a sequence possibly shorter) each read the
- * keys the chunk's last query sees once for all its Q * G (query, head)
- * pairs, every query keeping its own causal bound; a decode row is a chunk
- * of one.  So a sequence of n new tokens over L cached ones streams about
- * (n / Q) * L key rows, not n * L.  With new_per_seq = n and
- * n * G <= 8, each sequence is one such pass without the expansion kernel.
+ * G = num_q_heads / num_kv_heads and q = max(1, 16 / G), chunks of Q
+ * queries (the last one of a sequence possibly shorter) each read the keys
+ * the chunk's last query sees once for all its Q * G (query, head) pairs,
+ * every query keeping its own causal bound; Q = q when the call has at most
+ * 2q new tokens per sequence on average, else Q = 8q (64 at G = 2).  A
+ * sequence of n new tokens over L cached ones so streams about (n / Q) * L
+ * key rows, not n * L.  With new_per_seq = n <= q, each sequence is one such
+ * pass without the expansion kernel.
  * Rows inconsistent with the offsets (n > L, rows outside every sequence's
  * range) give zeros and PKV_ERR_CONTEXT_RANGE.  num_rows <= PKV_MAX_SEQS;
  * other limits, num_workers and errors as pkv_paged_decode.
