@@ -274,34 +274,42 @@ def run_pkv(args):
     g_ms = reduce_over_ranks(g0.elapsed_time(g1) / g_steps, "max", dev)
     assert err.item() == 0, f"device error word {err.item():#x}"
 
-    # ---- several new tokens per sequence (pkv_paged_attention): layer 0 with the last 4 tokens of every
-    # sequence as queries (a speculative-decoding verify step), causal over each sequence's cache
+    # ---- several new tokens per sequence (pkv_paged_attention) on layer 0, causal over each sequence's
+    # cache: the last nq tokens of every sequence as queries
     mixed = None
     if not args.no_fp8:
         lay0 = wl.layers[0]
-        nq = 4
         lens_h = wl.lens_host().astype(np.int64)
-        if lens_h.min() >= nq:
-            cu = torch.arange(0, (B + 1) * nq, nq, dtype=torch.int32, device=dev)
-            qm = torch.randn(B * nq, Hq, D, device=dev).bfloat16()
-            outm = torch.empty_like(qm)
-            wsm = pkv.alloc_attention_workspace(B * nq, Hq, Hkv, D, dev)
+        row = Hkv * D * 2 * 2
 
-            def att():  # every sequence has nq new tokens: their queries share one pass over its keys
-                pkv.paged_attention(qm, lay0.k_cache, lay0.v_cache, wl.block_tables, None, wl.context_lens, wl.scale,
-                                    outm, wsm, max_context_len=max_ctx, err_word=err, stream=stream, new_per_seq=nq)
+        def time_attention(nq, offsets, reps):
+            """Mean us of a pkv_paged_attention call with nq new tokens per sequence (given by offsets, or
+            as new_per_seq = nq)."""
+            cu = torch.arange(0, (B + 1) * nq, nq, dtype=torch.int32, device=dev) if offsets else None
+            qa = torch.randn(B * nq, Hq, D, device=dev).bfloat16()
+            oa = torch.empty_like(qa)
+            wsa = pkv.alloc_attention_workspace(B * nq, Hq, Hkv, D, dev)
+
+            def call():
+                pkv.paged_attention(qa, lay0.k_cache, lay0.v_cache, wl.block_tables, cu, wl.context_lens, wl.scale,
+                                    oa, wsa, max_context_len=max_ctx, err_word=err, stream=stream,
+                                    new_per_seq=0 if offsets else nq)
             for _ in range(5):
-                att()
+                call()
             torch.cuda.synchronize()
-            mev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
-            for c0, c1 in mev:
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for c0, c1 in evs:
                 c0.record(stream)
-                att()
+                call()
                 c1.record(stream)
             torch.cuda.synchronize()
             assert err.item() == 0, f"device error word {err.item():#x}"
-            us_m = float(np.mean([c0.elapsed_time(c1) for c0, c1 in mev])) * 1e3
-            row = Hkv * D * 2 * 2
+            return float(np.mean([c0.elapsed_time(c1) for c0, c1 in evs])) * 1e3
+
+        nq = 4
+        if lens_h.min() >= nq:
+            # a speculative-decoding verify step: the 4 queries of a sequence as 4 x G virtual heads
+            us_m = time_attention(nq, False, 50)
             unique = int(lens_h.sum()) * row
             streamed = int(sum(L - nq + 1 + i for L in lens_h for i in range(nq))) * row
             mixed = {"kernel": "pkv_paged_attention (paged_decode_kernel, the 4 queries of a sequence as 4 x G "
@@ -312,32 +320,23 @@ def run_pkv(args):
                      "streamed_gbs": round(streamed / (us_m * 1e-6) / 1e9, 1),
                      "note": "K/V read once per sequence; streamed_* counts one pass per query row, for comparison "
                              "with running the rows separately"}
-
-        # the last npf tokens of every sequence as one prefill chunk over its cached prefix (offsets
-        # given): consecutive queries share passes in chunks of max(1, 8 // G)
+        nv = 8
+        if lens_h.min() >= nv:
+            # a verify step with the offsets given: chunks of max(1, 16 // G) queries on regular CTAs
+            us_v = time_attention(nv, True, 50)
+            unique = int(lens_h.sum()) * row
+            mixed = dict(mixed or {})
+            mixed["verify_offsets"] = {
+                "kernel": "pkv_paged_attention (expand_rows_kernel + paged_decode_kernel, chunks of up to "
+                          "16 / G queries)", "query_rows": B * nv, "new_tokens_per_sequence": nv,
+                "mean_call_us": round(us_v, 2), "unique_kv_bytes": unique,
+                "unique_gbs": round(unique / (us_v * 1e-6) / 1e9, 1)}
         npf = 64
         if lens_h.min() >= npf and B * npf <= 16384:
-            cu_p = torch.arange(0, (B + 1) * npf, npf, dtype=torch.int32, device=dev)
-            qp = torch.randn(B * npf, Hq, D, device=dev).bfloat16()
-            outp = torch.empty_like(qp)
-            wsp = pkv.alloc_attention_workspace(B * npf, Hq, Hkv, D, dev)
-
-            def pre():
-                pkv.paged_attention(qp, lay0.k_cache, lay0.v_cache, wl.block_tables, cu_p, wl.context_lens,
-                                    wl.scale, outp, wsp, max_context_len=max_ctx, err_word=err, stream=stream)
-            for _ in range(5):
-                pre()
-            torch.cuda.synchronize()
-            pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(30)]
-            for c0, c1 in pev:
-                c0.record(stream)
-                pre()
-                c1.record(stream)
-            torch.cuda.synchronize()
-            assert err.item() == 0, f"device error word {err.item():#x}"
-            us_p = float(np.mean([c0.elapsed_time(c1) for c0, c1 in pev])) * 1e3
-            row = Hkv * D * 2 * 2
-            qe = max(1, 16 // (Hq // Hkv)) * 8  # queries of a query-split entry: 8 warps x max(1, 16 // G)
+            # the last npf tokens of every sequence as one prefill chunk over its cached prefix (offsets
+            # given): query-split CTAs, 8 x max(1, 16 // G) queries per K/V pass
+            us_p = time_attention(npf, True, 30)
+            qe = max(1, 16 // (Hq // Hkv)) * 8
             chunk_rows = int(sum(L - npf + min(c + qe, npf) for L in lens_h for c in range(0, npf, qe))) * row
             per_query = int(sum(L - npf + 1 + i for L in lens_h for i in range(npf))) * row
             mixed = dict(mixed or {})
