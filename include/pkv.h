@@ -389,6 +389,25 @@ PKV_API pkv_status pkv_paged_decode_fp8(const uint16_t *q, const uint8_t *k_cach
                                         int32_t num_workers, int32_t *err_word, pkv_stream_t stream);
 
 /*
+ * pkv_paged_decode_store_fp8 -- pkv_paged_decode_store over E4M3 caches:
+ * row b of k_new / v_new (bf16, [num_seqs, num_kv_heads, head_dim], 16-byte
+ * aligned) is quantised exactly as pkv_kv_store_fp8 does (the E4M3 code of
+ * x / scale[kv head]), stored at position context_lens[b] - 1 and attended
+ * over with the other codes (as pkv_paged_decode_fp8).  Same result as
+ * pkv_decode_slot_mapping + pkv_kv_store_fp8 + pkv_paged_decode_fp8;
+ * arguments, slot_mapping and errors as pkv_paged_decode_store.
+ */
+PKV_API pkv_status pkv_paged_decode_store_fp8(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                                              uint8_t *k_cache, uint8_t *v_cache, const float *k_scale,
+                                              const float *v_scale, const int32_t *block_tables,
+                                              int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                              int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                              int32_t max_context_len, float scale, uint16_t *out,
+                                              int32_t *slot_mapping, void *workspace, size_t workspace_bytes,
+                                              int32_t num_workers, int32_t *err_word, pkv_stream_t stream);
+
+/*
  * pkv_copy_blocks -- batched copy-on-write block copies.
  *
  * Defined by the nano-vllm KV-cache post (§2.2: sequences that share a

@@ -52,9 +52,9 @@ static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, 
     const int64_t max_units = int64_t(num_kv_heads) * num_seqs * ((len_limit + 7) / 8);
     if (max_units > INT32_MAX) return PKV_EUNSUPPORTED;
     if (qs && (fp8 || !row_cnt)) return PKV_EINVAL;  // query-split entries are chunks of bf16 calls
-    if ((k_new || v_new) && (fp8 || qs || qn != 1 || row_seq || !k_new || !v_new || !aligned16(k_new) ||
+    if ((k_new || v_new) && (qs || qn != 1 || row_seq || !k_new || !v_new || !aligned16(k_new) ||
                              !aligned16(v_new)))
-        return PKV_EINVAL;  // the fused store goes with a bf16 decode
+        return PKV_EINVAL;  // the fused store goes with a decode
     const WsLayout ws = ws_layout(num_seqs, G, num_kv_heads, head_dim, qs);
     if (!workspace || workspace_bytes < ws.total || !aligned16(workspace)) return PKV_EWORKSPACE;
 
@@ -100,8 +100,8 @@ static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, 
     p.row_cnt = row_cnt;
     p.k_new = k_new;
     p.v_new = v_new;
-    p.k_cache_w = static_cast<uint16_t *>(const_cast<void *>(k_cache));
-    p.v_cache_w = static_cast<uint16_t *>(const_cast<void *>(v_cache));
+    p.k_cache_w = static_cast<uint8_t *>(const_cast<void *>(k_cache));
+    p.v_cache_w = static_cast<uint8_t *>(const_cast<void *>(v_cache));
     p.slot_out = k_new ? slot_out : nullptr;
     p.qstride = row_cnt ? 1 : qn;
     a.k_cache = k_cache;
@@ -152,6 +152,23 @@ extern "C" pkv_status pkv_paged_decode_store(const uint16_t *q, const uint16_t *
 {
     if (num_seqs > 0 && (!k_new || !v_new)) return PKV_EINVAL;
     return decode_call(false, false, 1, q, k_cache, v_cache, nullptr, nullptr, nullptr, nullptr, block_tables,
+                       max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, max_context_len, scale, out, workspace, workspace_bytes, num_workers, err_word,
+                       stream, k_new, v_new, slot_mapping);
+}
+
+extern "C" pkv_status pkv_paged_decode_store_fp8(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                                                 uint8_t *k_cache, uint8_t *v_cache, const float *k_scale,
+                                                 const float *v_scale, const int32_t *block_tables,
+                                                 int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                                 int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                                 int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                                 int32_t max_context_len, float scale, uint16_t *out,
+                                                 int32_t *slot_mapping, void *workspace, size_t workspace_bytes,
+                                                 int32_t num_workers, int32_t *err_word, pkv_stream_t stream)
+{
+    if (num_seqs > 0 && (!k_new || !v_new)) return PKV_EINVAL;
+    return decode_call(true, false, 1, q, k_cache, v_cache, k_scale, v_scale, nullptr, nullptr, block_tables,
                        max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                        num_blocks, max_context_len, scale, out, workspace, workspace_bytes, num_workers, err_word,
                        stream, k_new, v_new, slot_mapping);

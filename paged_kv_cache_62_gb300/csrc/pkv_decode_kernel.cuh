@@ -131,12 +131,13 @@ struct DecodeParams {
     // Decode: qn = 1, gq = G, qstride = 1.
     int32_t qn, gq, qstride;
     const int32_t *row_cnt;
-    // Store fused into a decode (bf16, qn = 1): row b of k_new / v_new [B, Hkv, D] is the K/V of
-    // sequence b's token at position L - 1; the kernel writes it to that token's cache row (k_cache_w /
-    // v_cache_w, [NB * bs, Hkv, D]) and attends with it; slot_out[b] (nullable) receives the row (-1
-    // when nothing was stored).  k_new null: a plain decode.
+    // Store fused into a decode (qn = 1): row b of k_new / v_new [B, Hkv, D] (bf16) is the K/V of
+    // sequence b's token at position L - 1; the kernel writes it (E4M3 caches: its codes under the kv
+    // head's scales) to that token's cache row (k_cache_w / v_cache_w, [NB * bs, Hkv, D] elements) and
+    // attends with it; slot_out[b] (nullable) receives the row (-1 when nothing was stored).  k_new
+    // null: a plain decode.
     const uint16_t *k_new, *v_new;
-    uint16_t *k_cache_w, *v_cache_w;
+    uint8_t *k_cache_w, *v_cache_w;
     int32_t *slot_out;
 };
 
@@ -1266,7 +1267,8 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     }
     float ksc = p.scale_log2;
     float vsc = 1.0f;  // E4M3 caches: the kv head's V scale, applied in the final division
-    uint2 kn = make_uint2(0u, 0u), vn = make_uint2(0u, 0u);  // fused store: 4 elements of the new K / V row
+    // fused store: this lane's 8 bytes of the new K / V row (4 bf16 elements, or 8 E4M3 codes)
+    uint2 kn = make_uint2(0u, 0u), vn = make_uint2(0u, 0u);
     int u_first = 0;
     for (;;) {
         if (!mbar_wait_bounded(&full[s], sph)) {
@@ -1286,11 +1288,19 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                 if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
                 break;
             }
-            if constexpr (!FP8 && !QS) {
-                if (p.k_new && lane < D / 4) {  // the segment's new K/V row, used at its last tile
-                    const long long e = ((long long)mt.b * p.Hkv + mt.g * p.hg + h) * D + lane * 4;
-                    kn = __ldg(reinterpret_cast<const uint2 *>(p.k_new + e));
-                    vn = __ldg(reinterpret_cast<const uint2 *>(p.v_new + e));
+            if constexpr (!QS) {
+                if (p.k_new && lane < TC::ROWB / 8) {  // the segment's new K/V row, used at its last tile
+                    const long long row0 = ((long long)mt.b * p.Hkv + mt.g * p.hg + h) * D;
+                    if constexpr (!FP8) {
+                        kn = __ldg(reinterpret_cast<const uint2 *>(p.k_new + row0 + lane * 4));
+                        vn = __ldg(reinterpret_cast<const uint2 *>(p.v_new + row0 + lane * 4));
+                    } else {  // quantised as pkv_kv_store_fp8 does
+                        const int kvh = mt.g * p.hg + h;
+                        kn = quantise8_e4m3(__ldg(reinterpret_cast<const uint4 *>(p.k_new + row0 + lane * 8)),
+                                            __ldg(p.k_scale + kvh));
+                        vn = quantise8_e4m3(__ldg(reinterpret_cast<const uint4 *>(p.v_new + row0 + lane * 8)),
+                                            __ldg(p.v_scale + kvh));
+                    }
                 }
             }
             nvh = max(0, min(p.qn, mt.cnt - jq * p.qn)) * p.gq;
@@ -1335,13 +1345,13 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         const int valid = min(TC::TW, mt.L - tok0);
         if (valid > 0 && nvh > 0) {
             const uint32_t kb = stage_addr + uint32_t(s) * lay.stage_bytes;
-            if constexpr (!FP8 && !QS) {
+            if constexpr (!QS) {
                 // fused store: the tile holding the new token takes its K/V row from k_new / v_new (the
                 // cache row the copy brought is the previous content) and writes it to the cache; no
                 // other CTA reads that row in this kernel (the block of a sequence's last token is its own)
                 const int tl = mt.L - 1 - tok0;
                 if (p.k_new && mt.newrow >= 0 && tl >= 0 && tl < TC::TW) {
-                    if (lane < D / 4) {
+                    if (lane < TC::ROWB / 8) {
                         const int t = jt * TC::TW + tl, lg = __ffs(p.boxtok) - 1;
                         const int bi = t >> lg, r = t & (p.boxtok - 1);
                         const int byte = lane * 8, pp = byte / TC::RB, within = byte % TC::RB;
@@ -1351,7 +1361,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                         asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(kb + o), "r"(kn.x), "r"(kn.y) : "memory");
                         asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(kb + lay.kv_bytes + o), "r"(vn.x),
                                      "r"(vn.y) : "memory");
-                        const long long e = ((long long)mt.newrow * p.Hkv + mt.g * p.hg + h) * D + lane * 4;
+                        const long long e = ((long long)mt.newrow * p.Hkv + mt.g * p.hg + h) * TC::ROWB + byte;
                         *reinterpret_cast<uint2 *>(p.k_cache_w + e) = kn;
                         *reinterpret_cast<uint2 *>(p.v_cache_w + e) = vn;
                         fence_proxy_async_smem();  // the ring's next copy into this stage comes after

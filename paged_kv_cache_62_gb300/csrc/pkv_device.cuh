@@ -204,6 +204,23 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
+// Eight bf16 values divided by s (IEEE binary32 division), as eight E4M3
+// codes (element e in byte e): round to nearest even, saturating at +-448.
+__device__ __forceinline__ uint2 quantise8_e4m3(const uint4 w, float s)
+{
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    uint32_t out[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = __fdiv_rn(__uint_as_float(u[i] << 16), s);          // element 2i
+        const float hi = __fdiv_rn(__uint_as_float(u[i] & 0xffff0000u), s);  // element 2i + 1
+        uint16_t pair;  // the conversion puts its first source in the upper byte
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(hi), "f"(lo));
+        out[i >> 1] |= uint32_t(pair) << (16 * (i & 1));
+    }
+    return make_uint2(out[0], out[1]);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

@@ -127,22 +127,6 @@ __global__ void decode_store_kernel(const uint4 *__restrict__ k, const uint4 *__
     }
 }
 
-// Eight bf16 values divided by s, as eight E4M3 codes (element e in byte e).
-__device__ __forceinline__ uint2 quantise8_e4m3(const uint4 w, float s)
-{
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-    uint32_t out[2] = {0u, 0u};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float lo = __fdiv_rn(__uint_as_float(u[i] << 16), s);          // element 2i
-        const float hi = __fdiv_rn(__uint_as_float(u[i] & 0xffff0000u), s);  // element 2i + 1
-        uint16_t pair;  // the conversion puts its first source in the upper byte
-        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(hi), "f"(lo));
-        out[i >> 1] |= uint32_t(pair) << (16 * (i & 1));
-    }
-    return make_uint2(out[0], out[1]);
-}
-
 // One CTA per token; thread i quantises the 8-element group i of the row
 // (group i belongs to kv head i / (D / 8)).
 __global__ void kv_store_fp8_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,

@@ -33,6 +33,8 @@ SIGNATURES = {
                                         _F32, _P, _P, _SZ, _I32, _P, _P]),
     "pkv_paged_decode_store": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
                                               _I32, _I32, _F32, _P, _P, _P, _SZ, _I32, _P, _P]),
+    "pkv_paged_decode_store_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
+                                                  _I32, _I32, _I32, _I32, _F32, _P, _P, _P, _SZ, _I32, _P, _P]),
     "pkv_paged_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                                 _I32, _F32, _P, _I32, _P, _P]),
     "pkv_copy_blocks": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P]),
@@ -201,6 +203,38 @@ def paged_decode_store(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor
         None if slot_mapping is None else _dev(slot_mapping, torch.int32, "slot_mapping", 1),
         workspace.data_ptr(), workspace.numel(), int(num_workers), _opt(err_word), _stream(stream)),
         "pkv_paged_decode_store")
+
+
+def paged_decode_store_fp8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                           v_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, out: torch.Tensor,
+                           workspace: torch.Tensor, slot_mapping: torch.Tensor | None = None,
+                           max_context_len: int | None = None, num_workers: int = 0,
+                           err_word: torch.Tensor | None = None, stream=None) -> None:
+    """paged_decode_store over E4M3 caches (uint8 [NB, bs, Hkv, D]) with per-kv-head float32 scales: the new
+    rows (bf16) are quantised as kv_store_fp8 does, stored and attended in one launch."""
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape or block_tables.shape[0] != B or context_lens.numel() != B \
+            or out.shape != q.shape or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) \
+            or k_scale.numel() != Hkv or v_scale.numel() != Hkv \
+            or (slot_mapping is not None and slot_mapping.numel() != B):
+        raise ValueError("paged_decode_store_fp8: shape mismatch")
+    mb = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = mb * bs
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA uint8 tensor")
+    _check(load().pkv_paged_decode_store_fp8(
+        _dev(q, torch.bfloat16, "q", 3), _dev(k_new, torch.bfloat16, "k_new", 3),
+        _dev(v_new, torch.bfloat16, "v_new", 3), _dev(k_cache, torch.uint8, "k_cache", 4),
+        _dev(v_cache, torch.uint8, "v_cache", 4), _dev(k_scale, torch.float32, "k_scale"),
+        _dev(v_scale, torch.float32, "v_scale"), _dev(block_tables, torch.int32, "block_tables", 2), mb,
+        _dev(context_lens, torch.int32, "context_lens", 1), B, Hq, Hkv, D, bs, NB, int(max_context_len),
+        float(scale), _dev(out, torch.bfloat16, "out", 3),
+        None if slot_mapping is None else _dev(slot_mapping, torch.int32, "slot_mapping", 1),
+        workspace.data_ptr(), workspace.numel(), int(num_workers), _opt(err_word), _stream(stream)),
+        "pkv_paged_decode_store_fp8")
 
 
 def paged_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,

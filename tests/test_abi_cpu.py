@@ -149,6 +149,12 @@ def test_newer_entry_points_validate_on_the_host(lib):
     assert pds(FAKE, FAKE + 8, FAKE, FAKE, FAKE, *tail) == pkv.EINVAL      # k_new not 16-byte aligned
     assert pds(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 0, 16, 8, 128, 16, 10, 64, 0.1, FAKE, NULL, FAKE,
                1 << 30, 0, NULL, NULL) == pkv.OK                          # empty batch
+    # pkv_paged_decode_store_fp8(q, k_new, v_new, kc8, vc8, ks, vs, bt, max_blocks, lens, B, Hq, Hkv, D, bs, NB,
+    #                            max_ctx, scale, out, slots, ws, ws_bytes, workers, err, stream)
+    pf = lib.pkv_paged_decode_store_fp8
+    tail8 = [FAKE, 4, FAKE, 2, 16, 8, 128, 16, 10, 64, 0.1, FAKE, NULL, FAKE, 1 << 30, 0, NULL, NULL]
+    assert pf(FAKE, NULL, FAKE, FAKE, FAKE, FAKE, FAKE, *tail8) == pkv.EINVAL     # no k_new
+    assert pf(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, *tail8) == pkv.EINVAL     # no k_scale
     # pkv_kv_store_fp8(k, v, slots, T, kc8, vc8, NB, bs, Hkv, D, ks, vs, err, stream)
     kf = lib.pkv_kv_store_fp8
     assert kf(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 10, 16, 8, 128, NULL, FAKE, NULL, NULL) == pkv.EINVAL     # no k_scale

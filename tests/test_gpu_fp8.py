@@ -180,3 +180,35 @@ def test_qwen3_shaped_batch_in_fp8():
     want = oracle.paged_decode_fp8(W.bits(lay.q), kh, vh, ks.cpu().numpy(), vs.cpu().numpy(),
                                    wl.block_tables.cpu().numpy(), wl.lens_host(), wl.scale, nthreads=NTHREADS)
     check_close(out, want, "qwen3_0p6b fp8")
+
+
+@pytest.mark.parametrize("workers", [0, 7, 333])
+@pytest.mark.parametrize("D,bs", [(128, 16), (64, 8), (128, 256)])
+def test_decode_and_store_fp8_in_one_launch(workers, D, bs):
+    """pkv_paged_decode_store_fp8: the new rows quantised and stored as pkv_kv_store_fp8 would (codes bit
+    for bit, against the oracle), the attention over the stored codes within the decode tolerance, slots
+    as the oracle's slot mapping; a padding row (context_len 0) stores nothing and gives zeros."""
+    lens = [1, 15, 16, 17, 300, 0, 1024, 2, 513]
+    B, Hq, Hkv = len(lens), 16, 8
+    q, kc, vc, ks, vs, bt, lens_t = synth_fp8(B, Hq, Hkv, D, bs, seed=workers + D + bs, lens=lens)
+    g = torch.Generator(device="cuda").manual_seed(workers + 1)
+    k_new = (torch.randn(B, Hkv, D, generator=g, device="cuda") * 0.01).bfloat16()
+    v_new = (torch.randn(B, Hkv, D, generator=g, device="cuda") * 0.01).bfloat16()
+    k_new[0, 0, :3] = torch.tensor([1e4, -1e4, 0.0]).bfloat16()   # saturation
+    kh, vh = kc.cpu().numpy().copy(), vc.cpu().numpy().copy()
+    slots = torch.full((B,), 7, dtype=torch.int32, device="cuda")
+    out = torch.full_like(q, float("nan"))
+    ws = pkv.alloc_workspace(B, Hq, Hkv, D)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_decode_store_fp8(q, k_new, v_new, kc, vc, ks, vs, bt, lens_t, 0.0884, out, ws, slot_mapping=slots,
+                               num_workers=workers, err_word=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    want_slots = oracle.decode_slot_mapping(bt.cpu().numpy(), np.asarray(lens, np.int32), bs, B)
+    assert np.array_equal(slots.cpu().numpy(), want_slots)
+    oracle.kv_store_fp8(W.bits(k_new), W.bits(v_new), want_slots, kh, vh, ks.cpu().numpy(), vs.cpu().numpy())
+    assert np.array_equal(kc.cpu().numpy(), kh) and np.array_equal(vc.cpu().numpy(), vh)
+    want = oracle.paged_decode_fp8(W.bits(q), kh, vh, ks.cpu().numpy(), vs.cpu().numpy(), bt.cpu().numpy(),
+                                   np.asarray(lens, np.int32), 0.0884, nthreads=NTHREADS)
+    check_close(out, want, f"workers {workers} D{D} bs{bs}")
+    assert torch.all(out[lens.index(0)].float() == 0)
