@@ -12,10 +12,12 @@
 //  * Kv heads are taken in groups of HG (the largest divisor of Hkv that is
 //    at most the CTA's 8 consumer warps).  A unit of work is TOKS = TW * SUB
 //    consecutive tokens of one (sequence, head group), TW = 16 tokens per
-//    warp and SUB warps per head (see team_warps): the group's cache rows,
-//    moved by one 4-D TMA tensor copy per physical-block span and cache into
-//    a shared-memory stage as 128-byte-swizzled rows (see Tc).
-//  * One CTA per SM: a producer warp streams units through a ring of 2-4
+//    warp (32 for E4M3 caches) and SUB warps per head (see team_warps): the
+//    group's cache rows, moved by one 4-D TMA tensor copy per physical-block
+//    span and cache into a shared-memory stage as 128-byte-swizzled rows (see
+//    Tc).  Each CTA warms L2 with its first units while it sets up (see
+//    BalanceState::hint).
+//  * One CTA per SM: a producer warp streams units through a ring of 2-16
 //    stages (mbarrier transaction counts for "full", consumer arrivals for
 //    "empty"); HG * SUB consumer warps take one TW-token slice of one kv head
 //    each, so every consumer works on every stage and the CTA's warps finish
@@ -25,9 +27,15 @@
 //  * A consumer serves all G query heads of its kv head from one K/V read,
 //    on the warp-level tensor cores: S^T = Q K^T and O^T += V^T P^T as
 //    m16n8k16 MMAs with fp32 accumulators, K and V fed by ldmatrix from the
-//    swizzled stage, P kept in registers (see attend_tile); the online
+//    swizzled stage, P kept in registers (see attend_tile); up to 16 virtual
+//    heads (queries x heads) fill the tile's two 8-row halves; the online
 //    softmax rescales only when a score passes the running max by a slack,
-//    and exponentials are ex2 of log2e-prescaled scores.
+//    and exponentials are ex2 of log2e-prescaled scores.  Query-split CTAs
+//    (QS) instead give every warp all tokens of one kv head and its own
+//    queries: long runs of new tokens share K/V passes.
+//  * The decode step's store can run in the same launch: the tile holding a
+//    sequence's new token takes its K/V row from the step's inputs and writes
+//    it to the cache (see DecodeParams::k_new).
 //  * The batch's unit list is cut into one slice per SM id, each slice's size
 //    following the finishing times the previous call on the workspace saw.
 //    A CTA whose slice covers a whole (sequence, head group) writes bf16
@@ -37,8 +45,9 @@
 //    flash-decoding without a second kernel).
 //
 // This header holds the kernel and its launch templates; pkv_decode.cu
-// instantiates the bf16-cache kernels and defines the C entry points,
-// pkv_decode_fp8.cu instantiates the E4M3-cache kernels.
+// instantiates the bf16-cache kernels for up to 8 virtual heads and defines
+// the C entry points, pkv_decode_wide.cu the bf16 ones for 9 to 16,
+// pkv_decode_qs.cu the query-split ones, pkv_decode_fp8.cu the E4M3 ones.
 #pragma once
 #include <cuda_fp16.h>
 
