@@ -408,6 +408,15 @@ PKV_API pkv_status pkv_paged_decode_store_fp8(const uint16_t *q, const uint16_t 
                                               int32_t num_workers, int32_t *err_word, pkv_stream_t stream);
 
 /*
+ * pkv_selftest_wait_timeout -- a diagnostic: one warp waits on a barrier that
+ * nothing completes.  Every wait on an asynchronous copy in the library is
+ * bounded (about 2 s); this one runs out, sets PKV_ERR_WAIT_TIMEOUT in
+ * *err_word (device) and returns, leaving the context usable.  It takes the
+ * wait's time limit to complete.  err_word NULL: PKV_EINVAL.
+ */
+PKV_API pkv_status pkv_selftest_wait_timeout(int32_t *err_word, pkv_stream_t stream);
+
+/*
  * pkv_copy_blocks -- batched copy-on-write block copies.
  *
  * Defined by the nano-vllm KV-cache post (§2.2: sequences that share a

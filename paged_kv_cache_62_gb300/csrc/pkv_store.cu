@@ -252,6 +252,29 @@ extern "C" pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, const i
     return launch_status("kv_store_kernel launch");
 }
 
+// A wait on an mbarrier that nothing completes: the bounded wait gives up at
+// its time limit, the kernel flags PKV_ERR_WAIT_TIMEOUT and returns (the
+// timeout path of every wait in the library, exercised without a fault).
+__global__ void wait_timeout_selftest_kernel(int32_t *err)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    if (!mbar_wait_bounded(&bar, 0u) && threadIdx.x == 0) flag_error(err, PKV_ERR_WAIT_TIMEOUT);
+}
+
+extern "C" pkv_status pkv_selftest_wait_timeout(int32_t *err_word, pkv_stream_t stream)
+{
+    if (!err_word) return PKV_EINVAL;
+    wait_timeout_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err_word);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail("wait_timeout_selftest_kernel launch", e);
+    return launch_status("wait_timeout_selftest_kernel launch");
+}
+
 extern "C" pkv_status pkv_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, const int32_t *pairs,
                                       int32_t num_pairs, int32_t num_blocks, int32_t block_size,
                                       int32_t num_kv_heads, int32_t head_dim, int32_t *err_word,

@@ -155,6 +155,7 @@ def test_newer_entry_points_validate_on_the_host(lib):
     tail8 = [FAKE, 4, FAKE, 2, 16, 8, 128, 16, 10, 64, 0.1, FAKE, NULL, FAKE, 1 << 30, 0, NULL, NULL]
     assert pf(FAKE, NULL, FAKE, FAKE, FAKE, FAKE, FAKE, *tail8) == pkv.EINVAL     # no k_new
     assert pf(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, *tail8) == pkv.EINVAL     # no k_scale
+    assert lib.pkv_selftest_wait_timeout(NULL, NULL) == pkv.EINVAL
     # pkv_kv_store_fp8(k, v, slots, T, kc8, vc8, NB, bs, Hkv, D, ks, vs, err, stream)
     kf = lib.pkv_kv_store_fp8
     assert kf(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 10, 16, 8, 128, NULL, FAKE, NULL, NULL) == pkv.EINVAL     # no k_scale

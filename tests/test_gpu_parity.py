@@ -379,6 +379,22 @@ def test_workers_do_not_change_results_much():
 
 
 # --------------------------------------------------------------------------- closed forms on the GPU
+def test_bounded_wait_runs_out_and_the_context_stays_usable():
+    """A wait that nothing completes gives up at its time limit with PKV_ERR_WAIT_TIMEOUT (no hang, no
+    fault), and the next calls on the device work as before."""
+    err = err_word()
+    pkv.selftest_wait_timeout(err)
+    torch.cuda.synchronize()
+    assert err.item() == pkv.ERR_WAIT_TIMEOUT
+    lens = [1, 40, 300]
+    q, kc, vc, bt, lens_t = synth(len(lens), 0, 8, 2, 64, 16, seed=9, lens=lens)
+    err.zero_()
+    out = run_decode(q, kc, vc, bt, lens_t, 0.125, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    check_close(out, oracle_of(q, kc, vc, bt, lens_t, 0.125), "after the timed-out wait")
+
+
 def test_worked_example_on_gpu():
     """Lab manual appendix B.1.2 example, zero-padded to D=64, scattered through a shuffled table."""
     D = 64
