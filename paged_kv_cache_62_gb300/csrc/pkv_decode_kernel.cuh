@@ -303,11 +303,18 @@ __device__ __forceinline__ Walker walker_locate(const int32_t *scan, int32_t B, 
     return w;
 }
 
+// Barrier of the CTA's nt set-up threads (its consumer warps, threads 0 .. nt - 1): the
+// producer warp runs its own part of the set-up meanwhile and meets them at __syncthreads.
+__device__ __forceinline__ void setup_sync(int nt)
+{
+    asm volatile("bar.sync 1, %0;" ::"r"(nt) : "memory");
+}
+
 // Units per sequence -> exclusive prefix in scan[0..B].
 // `tmp` needs 32 ints of shared memory that is free during the call.
-static __device__ void unit_prefix_scan(const DecodeParams &p, int32_t *scan, int32_t *tmp)
+static __device__ void unit_prefix_scan(const DecodeParams &p, int32_t *scan, int32_t *tmp, int nt)
 {
-    const int tid = threadIdx.x, nt = blockDim.x;
+    const int tid = threadIdx.x;
     const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
     const int per = (p.B + nt - 1) / nt;
     const int lo = min(p.B, tid * per), hi = min(p.B, lo + per);
@@ -332,7 +339,7 @@ static __device__ void unit_prefix_scan(const DecodeParams &p, int32_t *scan, in
         if (lane >= o) incl += v;
     }
     if (lane == 31) tmp[wid] = incl;
-    __syncthreads();
+    setup_sync(nt);
     if (wid == 0) {
         const int32_t v = lane < nw ? tmp[lane] : 0;
         int32_t inc = v;
@@ -343,7 +350,7 @@ static __device__ void unit_prefix_scan(const DecodeParams &p, int32_t *scan, in
         }
         if (lane < nw) tmp[lane] = inc - v;
     }
-    __syncthreads();
+    setup_sync(nt);
     int32_t run = tmp[wid] + incl - sum;
     for (int i = lo; i < hi; ++i) {
         const int32_t n = scan[i];
@@ -351,7 +358,7 @@ static __device__ void unit_prefix_scan(const DecodeParams &p, int32_t *scan, in
         run += n;
     }
     if (lo < hi && hi == p.B) scan[p.B] = run;
-    __syncthreads();
+    setup_sync(nt);
 }
 
 // ------------------------------------------------------------------ one tile
@@ -643,19 +650,19 @@ __device__ __forceinline__ unsigned nsmid()
     return v;
 }
 
-// Sums of two floats per thread over the CTA (fixed order: identical in every
-// CTA).  `red` holds 2 * 32 floats.
-__device__ __forceinline__ float2 block_sum2(float2 v, float *red)
+// Sums of two floats per thread over the nt set-up threads (fixed order:
+// identical in every CTA).  `red` holds 2 * 32 floats.
+__device__ __forceinline__ float2 block_sum2(float2 v, float *red, int nt)
 {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = nt >> 5;
     v.x = warp_sum(v.x);
     v.y = warp_sum(v.y);
-    __syncthreads();
+    setup_sync(nt);
     if (lane == 0) {
         red[2 * wid] = v.x;
         red[2 * wid + 1] = v.y;
     }
-    __syncthreads();
+    setup_sync(nt);
     float2 t = make_float2(0.f, 0.f);
     for (int i = 0; i < nw; ++i) {
         t.x += red[2 * i];
@@ -664,25 +671,27 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float *red)
     return t;
 }
 
-// The balance entries this thread reads in build_partition (slices tid and
-// tid + blockDim.x), loaded up front so that their memory round trip overlaps
-// the context-length loads of unit_prefix_scan.  Both table halves are
-// loaded, before this call's number is known; build_partition keeps the
-// entry whose tag names the previous call.
+// The balance entries this thread reads in build_partition (slices tid + k nt
+// for k < kBalE, nt set-up threads), loaded up front so that their memory
+// round trip overlaps the context-length loads of unit_prefix_scan.  Both
+// table halves are loaded, before this call's number is known;
+// build_partition keeps the entry whose tag names the previous call.
+constexpr int kBalE = 4;
 struct BalanceIn {
-    float w[2][2], t[2][2];  // [table half][entry k]
-    uint32_t tag[2][2];
+    float w[2][kBalE], t[2][kBalE];  // [table half][entry k]
+    uint32_t tag[2][kBalE];
 };
-static_assert(2 * (8 + 1) * 32 >= kMaxSlots, "two balance entries per thread must cover every slice");
+// the fewest set-up threads a CTA has: 5 consumer warps (a head group of 5)
+static_assert(kBalE * 5 * 32 >= kMaxSlots, "the balance entries of the set-up threads must cover every slice");
 
-__device__ __forceinline__ BalanceIn load_balance(const DecodeParams &p, bool adaptive, int nslots)
+__device__ __forceinline__ BalanceIn load_balance(const DecodeParams &p, bool adaptive, int nslots, int nt)
 {
     BalanceIn in;
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int i = threadIdx.x + k * blockDim.x;
+        for (int k = 0; k < kBalE; ++k) {
+            const int i = threadIdx.x + k * nt;
             in.w[h][k] = 1.0f;
             in.t[h][k] = 0.f;
             in.tag[h][k] = 0u;
@@ -703,17 +712,18 @@ __device__ __forceinline__ BalanceIn load_balance(const DecodeParams &p, bool ad
 // varies with the data it held, and the full step overcorrects (consecutive
 // calls' finishing times then anti-correlate); entries from any other call
 // count as unknown (weight 1).  Fixed mode: equal weights.  Every CTA computes the same bounds from the
-// same inputs in the same order; leaves the weights in w[].
+// same inputs in the same order; leaves the weights in w[].  Run by the nt
+// set-up threads.
 static __device__ void build_partition(const DecodeParams &p, uint32_t gen, bool adaptive, int nslots, long long T,
-                                long long *bound, float *w, float *red, const BalanceIn &in)
+                                long long *bound, float *w, float *red, const BalanceIn &in, int nt)
 {
-    const int tid = threadIdx.x, nt = blockDim.x;
+    const int tid = threadIdx.x;
     const uint32_t want = (gen - 1u) ^ kTableMagic;
     // pass 1: raw weights (kept in w) and elapsed times (kept in bound[] as float bits)
     float tsum = 0.f, tcnt = 0.f;
     float *el = reinterpret_cast<float *>(bound);
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < kBalE; ++k) {
         const int i = tid + k * nt;
         if (i >= nslots) break;
         float x = 1.0f, t = 0.f;
@@ -731,7 +741,7 @@ static __device__ void build_partition(const DecodeParams &p, uint32_t gen, bool
         w[i] = x;
         el[i] = t;
     }
-    const float2 tt = block_sum2(make_float2(tsum, tcnt), red);
+    const float2 tt = block_sum2(make_float2(tsum, tcnt), red, nt);
     tsum = tt.x;
     tcnt = tt.y;
     const float tmean = tcnt > 0.f ? tsum / tcnt : 0.f;
@@ -747,7 +757,7 @@ static __device__ void build_partition(const DecodeParams &p, uint32_t gen, bool
             wcnt += 1.f;
         }
     }
-    const float2 ww = block_sum2(make_float2(wsum, wcnt), red);
+    const float2 ww = block_sum2(make_float2(wsum, wcnt), red, nt);
     wsum = ww.x;
     wcnt = ww.y;
     const float wmean = wcnt > 0.f ? wsum / wcnt : 1.0f;
@@ -756,7 +766,7 @@ static __device__ void build_partition(const DecodeParams &p, uint32_t gen, bool
         if (x > 0.f) x = fminf(fmaxf(x, 0.25f), 4.0f);
         w[i] = x;
     }
-    __syncthreads();
+    setup_sync(nt);
     // bounds: float prefix of the weights -> 2^20 tickets -> tiles (a shift, no division)
     if (tid < 32) {
         const int per = (nslots + 31) / 32;
@@ -770,10 +780,13 @@ static __device__ void build_partition(const DecodeParams &p, uint32_t gen, bool
             if (tid >= o) incl += v;
         }
         const float total = __shfl_sync(kFull, incl, 31);
+        // tickets of a prefix: acc * (2^20 / total), one reciprocal for all; a positive factor keeps
+        // the nondecreasing prefix nondecreasing.  No weights: equal slices (i < 512: 32-bit).
+        const float tickets = total > 0.f ? 1048576.0f / total : 0.f;
         float acc = incl - run;
         for (int i = lo; i < hi; ++i) {
-            long long pre = total > 0.f ? (long long)(acc / total * 1048576.0f) : (long long)i * 1048576 / nslots;
-            pre = pre < 0 ? 0 : (pre > 1048576 ? 1048576 : pre);
+            int pre = total > 0.f ? int(fminf(acc * tickets, 1048576.0f)) : (i << 20) / nslots;
+            pre = pre < 0 ? 0 : pre;
             bound[i] = (T * pre) >> 20;
             acc += w[i];
         }
@@ -781,7 +794,7 @@ static __device__ void build_partition(const DecodeParams &p, uint32_t gen, bool
         if (tid == 0) bound[nslots] = T;
     }
     // bounds are monotone: the float prefix only grows and pre is clamped to [0, 2^20]
-    __syncthreads();
+    setup_sync(nt);
 }
 
 __device__ __forceinline__ bool try_claim(unsigned long long *word, uint32_t gen)
@@ -984,70 +997,9 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     int *sh = reinterpret_cast<int *>(smem + lay.off_sh);  // [0] own slice, [2..3] its start time
     int32_t *scan = reinterpret_cast<int32_t *>(smem + lay.off_scan);
 
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 32 * p.cons) {  // none of this reads what the previous kernel writes
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
-    }
-    griddep_launch_dependents();  // lets the next kernel in the stream get scheduled; it waits for this grid
-    griddep_wait();               // inputs may come from the previous kernel in the stream
-    if (threadIdx.x == 32 * p.cons && p.num_workers == 0 && !p.row_seq) {
-        // Warm L2 with up to kHintUnits units from the first copy this SM id's slice made in the
-        // previous call on the workspace, while the set-up runs, if the sequence's table still maps
-        // that block (then these are rows this call reads).
-        const unsigned sm = smid();
-        if (sm < unsigned(kMaxSlots)) {
-            const int4 h0 = __ldcg(&p.ws_bal->hint[sm][0]), h1 = __ldcg(&p.ws_bal->hint[sm][1]);
-            const uint32_t ep = __ldcg(&p.ws_bal->epoch);
-            if (h0.z == (int32_t(ep) ^ kHintMagic) && h0.w >= 0 && h0.w < p.B && h1.x >= 0 && h1.x < p.max_blocks &&
-                h0.x >= 0 && h0.x < p.NB * p.bs && h0.y >= 0 && h0.y + p.hg <= p.Hkv &&
-                __ldg(p.block_tables + (long long)h0.w * p.max_blocks + h1.x) == (h0.x >> p.log2_bs)) {
-                const int32_t in_block = h0.x & (p.bs - 1);
-                // rows of the block the sequence holds now (one decode step later: one more)
-                const int32_t held = min(p.bs, h1.y + 1 - h1.x * p.bs);
-                for (int i = 0; i < kHintUnits && in_block + i * p.toks < held && in_block + (i + 1) * p.toks <= p.bs;
-                     ++i) {
-                    tma_prefetch_4d(&kmap, 0, h0.x + i * p.toks, 0, h0.y);
-                    tma_prefetch_4d(&vmap, 0, h0.x + i * p.toks, 0, h0.y);
-                }
-            }
-        }
-    }
-
-    // Slices: one per SM id, sized by measured finishing times (adaptive), or one per CTA (fixed).
-    const bool adaptive = p.num_workers == 0;
-    int nslots = int(gridDim.x);
-    if (adaptive) nslots = int(min(nsmid(), unsigned(kMaxSlots)));
-    // The set-up's global reads are all issued here, so together they cost about one memory
-    // round trip: the workspace's control block (this call's number), the balance entries,
-    // the context lengths (in unit_prefix_scan) and, once the call number is in, the claim on
-    // this SM id's slice (an exchange: the first CTA of this call to run on the SM id finds
-    // another call's tag there), whose answer is needed only after the partition.
-    const uint32_t epoch = __ldcg(&p.ws_bal->epoch), stamp = __ldcg(&p.ws_bal->stamp);
-    const BalanceIn bal_in = load_balance(p, adaptive, nslots);
-    const bool ctl_ok = stamp == (epoch ^ kEpochMagic) || (epoch == 0u && stamp == 0u);
-    const uint32_t gen = epoch + 1u;  // tags of this call; zero-filled words never match
-    const int wp = int(gen & 1u);     // this call writes one half of the balance table
-    const unsigned my_sm = smid();
-    unsigned long long home_word = static_cast<unsigned long long>(gen) << 32;
-    if (threadIdx.x == 0 && adaptive && int(my_sm) < nslots)
-        home_word = atomicExch(&p.ws_bal->claim[my_sm], (static_cast<unsigned long long>(gen) << 32) | 1ull);
-    if (!ctl_ok && blockIdx.x == 0 && threadIdx.x == 0) flag_error(p.err, PKV_ERR_WORKSPACE);
-    unit_prefix_scan(p, scan, reinterpret_cast<int32_t *>(smem));
-    const long long T = (long long)p.nhg * scan[p.B];
-
-    // Entries without units (L == 0, or a rejected length) get zeros in their query rows; CTAs
-    // share the job.
-    for (int b = blockIdx.x; b < p.B; b += gridDim.x)
-        if (scan[b + 1] == scan[b]) {
-            if (p.slot_out && threadIdx.x == 0) p.slot_out[b] = -1;  // fused store: nothing stored
-            const int rows = p.row_cnt ? __ldg(p.row_cnt + b) : p.qn;
-            uint4 *o = reinterpret_cast<uint4 *>(p.out + int64_t(b) * p.qstride * p.Hq * D);
-            for (int i = threadIdx.x; i < rows * p.Hq * D / 8; i += blockDim.x) o[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
-
-    build_partition(p, gen, adaptive, nslots, T, bound, wts, red, bal_in);
-
-    if (threadIdx.x == 0) {
         for (int i = 0; i < p.nst; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], uint32_t(p.cons));
@@ -1059,12 +1011,75 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         mbar_init(cfull, uint32_t(p.cons - p.hg));  // the non-leading warps' states
         mbar_init(cfree, uint32_t(p.hg));           // read again by the leaders
         fence_barrier_init();
-        int home = -1;
-        if (!adaptive)
-            home = int(blockIdx.x);
-        else if (uint32_t(home_word >> 32) != gen)
-            home = int(my_sm);
-        sh[0] = home;
+    }
+    griddep_launch_dependents();  // lets the next kernel in the stream get scheduled; it waits for this grid
+    griddep_wait();               // inputs may come from the previous kernel in the stream
+
+    // Slices: one per SM id, sized by measured finishing times (adaptive), or one per CTA (fixed).
+    const bool adaptive = p.num_workers == 0;
+    int nslots = int(gridDim.x);
+    if (adaptive) nslots = int(min(nsmid(), unsigned(kMaxSlots)));
+    const uint32_t epoch = __ldcg(&p.ws_bal->epoch);  // the workspace's control block: this call's number
+    const uint32_t gen = epoch + 1u;                   // tags of this call; zero-filled words never match
+    const int wp = int(gen & 1u);                      // this call writes one half of the balance table
+    const unsigned my_sm = smid();
+    // The set-up splits in two parts that run at the same time, each about two memory round trips
+    // long.  The consumer warps (threads 0 .. 32 cons - 1, their own barrier) issue the control
+    // block, balance entries and context lengths together, then scan and partition.  The producer
+    // warp's lane 0 claims this SM id's slice (an exchange: the first CTA of this call to run on the
+    // SM id finds another call's tag there) and warms L2 from the hint; both need the call number
+    // first, and the hint a block-table entry after it.
+    const int nset = 32 * p.cons;
+    if (warp == p.cons) {
+        if (lane == 0) {
+            const uint32_t stamp = __ldcg(&p.ws_bal->stamp);
+            const bool hint = p.num_workers == 0 && !p.row_seq && my_sm < unsigned(kMaxSlots);
+            int4 h0 = make_int4(-1, -1, -1, -1), h1 = make_int4(-1, -1, -1, -1);
+            if (hint) {
+                h0 = __ldcg(&p.ws_bal->hint[my_sm][0]);
+                h1 = __ldcg(&p.ws_bal->hint[my_sm][1]);
+            }
+            unsigned long long home_word = static_cast<unsigned long long>(gen) << 32;
+            if (adaptive && int(my_sm) < nslots)
+                home_word = atomicExch(&p.ws_bal->claim[my_sm], (static_cast<unsigned long long>(gen) << 32) | 1ull);
+            // Warm L2 with up to kHintUnits units from the first copy this SM id's slice made in the
+            // previous call on the workspace, if the sequence's table still maps that block (then
+            // these are rows this call reads).
+            if (hint && h0.z == (int32_t(epoch) ^ kHintMagic) && h0.w >= 0 && h0.w < p.B && h1.x >= 0 &&
+                h1.x < p.max_blocks && h0.x >= 0 && h0.x < p.NB * p.bs && h0.y >= 0 && h0.y + p.hg <= p.Hkv &&
+                __ldg(p.block_tables + (long long)h0.w * p.max_blocks + h1.x) == (h0.x >> p.log2_bs)) {
+                const int32_t in_block = h0.x & (p.bs - 1);
+                // rows of the block the sequence holds now (one decode step later: one more)
+                const int32_t held = min(p.bs, h1.y + 1 - h1.x * p.bs);
+                for (int i = 0; i < kHintUnits && in_block + i * p.toks < held && in_block + (i + 1) * p.toks <= p.bs;
+                     ++i) {
+                    tma_prefetch_4d(&kmap, 0, h0.x + i * p.toks, 0, h0.y);
+                    tma_prefetch_4d(&vmap, 0, h0.x + i * p.toks, 0, h0.y);
+                }
+            }
+            const bool ctl_ok = stamp == (epoch ^ kEpochMagic) || (epoch == 0u && stamp == 0u);
+            if (!ctl_ok && blockIdx.x == 0) flag_error(p.err, PKV_ERR_WORKSPACE);
+            int home = -1;
+            if (!adaptive)
+                home = int(blockIdx.x);
+            else if (uint32_t(home_word >> 32) != gen)
+                home = int(my_sm);
+            sh[0] = home;
+        }
+    } else {
+        const BalanceIn bal_in = load_balance(p, adaptive, nslots, nset);
+        unit_prefix_scan(p, scan, reinterpret_cast<int32_t *>(smem), nset);
+        const long long T = (long long)p.nhg * scan[p.B];
+        // Entries without units (L == 0, or a rejected length) get zeros in their query rows; CTAs
+        // share the job.
+        for (int b = blockIdx.x; b < p.B; b += gridDim.x)
+            if (scan[b + 1] == scan[b]) {
+                if (p.slot_out && threadIdx.x == 0) p.slot_out[b] = -1;  // fused store: nothing stored
+                const int rows = p.row_cnt ? __ldg(p.row_cnt + b) : p.qn;
+                uint4 *o = reinterpret_cast<uint4 *>(p.out + int64_t(b) * p.qstride * p.Hq * D);
+                for (int i = threadIdx.x; i < rows * p.Hq * D / 8; i += nset) o[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        build_partition(p, gen, adaptive, nslots, T, bound, wts, red, bal_in, nset);
     }
     __syncthreads();
 
