@@ -16,10 +16,7 @@
 //    group's cache rows, moved by one 4-D TMA tensor copy per physical-block
 //    span and cache into a shared-memory stage as 128-byte-swizzled rows (see
 //    Tc).  Each CTA warms L2 with its first units while it sets up (see
-//    BalanceState::hint).  The set-up runs in two parts at once: the
-//    consumer warps scan the context lengths and partition the unit list on
-//    a barrier of their own, while the producer warp's lane 0 claims the SM
-//    id's slice and issues the L2 warm-up.
+//    BalanceState::hint).
 //  * One CTA per SM: a producer warp streams units through a ring of 2-16
 //    stages (mbarrier transaction counts for "full", consumer arrivals for
 //    "empty"); HG * SUB consumer warps take one TW-token slice of one kv head
