@@ -131,6 +131,21 @@ def test_decode_fp8_every_group_size(G, D):
     assert torch.all(out[3].float() == 0)
 
 
+@pytest.mark.parametrize("Hkv", [3, 5, 7])
+def test_decode_fp8_head_groups_below_eight_warps(Hkv):
+    """Head groups of 3 (x 2 slices), 5 and 7 kv heads: 6, 5 and 7 consumer warps run the set-up."""
+    lens = [700, 1, 33, 250, 96]
+    q, kc, vc, ks, vs, bt, lens_t = synth_fp8(len(lens), 2 * Hkv, Hkv, 128, 16, seed=Hkv * 5, lens=lens)
+    want = oracle_fp8(q, kc, vc, ks, vs, bt, lens_t, 0.0884)
+    ws = pkv.alloc_workspace(len(lens), 2 * Hkv, Hkv, 128)
+    for call in range(2):  # the second call sizes its slices from the first one's timings
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = run_fp8(q, kc, vc, ks, vs, bt, lens_t, 0.0884, ws=ws, err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        check_close(out, want, f"Hkv{Hkv} call{call}")
+
+
 @pytest.mark.parametrize("workers", [1, 7, 333, 4096])
 def test_decode_fp8_forced_splits(workers):
     lens = [1, 15, 17, 40, 300, 0, 1024, 2, 513]

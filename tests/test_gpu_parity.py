@@ -257,6 +257,28 @@ def test_every_group_size(G, D):
     check_close(out, oracle_of(q, kc, vc, bt, lens_t, 0.1), f"G{G} D{D}")
 
 
+@pytest.mark.parametrize("workers", [0, 7])
+@pytest.mark.parametrize("G", [1, 2])
+@pytest.mark.parametrize("Hkv", [1, 3, 5, 6, 7, 12])
+def test_head_groups_of_any_size(Hkv, G, workers):
+    """Kv-head counts whose head group (the largest divisor of Hkv up to 8) leaves 5, 6 or 7 consumer
+    warps, or one head over 8 token slices: the decode set-up's scan and partition run on the consumer
+    warps alone, so their count sets that barrier's size.  Three calls on one workspace: the second and
+    third size their slices from the previous call's timings."""
+    lens = [1, 17, 300, 64, 1000, 5, 256, 129]
+    D = 128 if Hkv in (3, 5) else 64
+    q, kc, vc, bt, lens_t = synth(len(lens), 0, G * Hkv, Hkv, D, 16, seed=Hkv * 31 + G + workers, lens=lens)
+    want = oracle_of(q, kc, vc, bt, lens_t, 0.2)
+    ws = pkv.alloc_workspace(len(lens), G * Hkv, Hkv, D)
+    for call in range(3):
+        out = torch.full_like(q, float("nan"))
+        err = err_word()
+        pkv.paged_decode(q, kc, vc, bt, lens_t, 0.2, out, ws, num_workers=workers, err_word=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0, (call, hex(err.item()))
+        check_close(out, want, f"Hkv{Hkv} G{G} workers{workers} call{call}")
+
+
 @pytest.mark.parametrize("workers", [1, 2, 3, 7, 64, 333, 4096])
 def test_forced_splits(workers):
     """Spread the same batch over very different worker counts: exercises the split-K merge."""
