@@ -82,7 +82,9 @@ def hbm_peak():
 
 
 def step_bytes(wl) -> dict:
-    """Algorithmic bytes of one step (see the per-kernel formulas in the design doc)."""
+    """Algorithmic bytes of one step: every K and V row of every sequence's context read once, q read and
+    the output written (bf16), the context length and block-table entries read, and the new token's
+    k, v rows read and stored."""
     s = wl.spec
     lens = wl.lens_host().astype(np.int64)
     B, Hq, Hkv, D = s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim
