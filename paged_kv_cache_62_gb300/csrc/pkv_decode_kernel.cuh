@@ -767,33 +767,52 @@ static __device__ void build_partition(const DecodeParams &p, uint32_t gen, bool
         w[i] = x;
     }
     setup_sync(nt);
-    // bounds: float prefix of the weights -> 2^20 tickets -> tiles (a shift, no division)
-    if (tid < 32) {
-        const int per = (nslots + 31) / 32;
+    // bounds: the weights in fixed point (2^16 per unit weight, at most 2^18 a slice), their exact
+    // integer prefix over the slices, then 2^20 tickets for the whole list -> tiles (a shift, no
+    // division).  Exact integers keep the bounds nondecreasing however the sums associate (a float
+    // prefix split over threads could drop a bound by one unit after a zero-weight slice).  Thread
+    // tid takes slices [tid per, (tid + 1) per), per <= kBalE; its sum is scanned over the set-up
+    // threads (warp shuffles, then the warp totals in red[]).
+    {
+        const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
+        const int per = (nslots + nt - 1) / nt;
         const int lo = min(nslots, tid * per), hi = min(nslots, lo + per);
-        float run = 0.f;
-        for (int i = lo; i < hi; ++i) run += w[i];
-        float incl = run;
+        int32_t *ired = reinterpret_cast<int32_t *>(red);
+        int32_t run = 0;
+        for (int i = lo; i < hi; ++i) run += int32_t(w[i] * 65536.0f);
+        int32_t incl = run;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const float v = __shfl_up_sync(kFull, incl, o);
-            if (tid >= o) incl += v;
+            const int32_t v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += v;
         }
-        const float total = __shfl_sync(kFull, incl, 31);
-        // tickets of a prefix: acc * (2^20 / total), one reciprocal for all; a positive factor keeps
-        // the nondecreasing prefix nondecreasing.  No weights: equal slices (i < 512: 32-bit).
-        const float tickets = total > 0.f ? 1048576.0f / total : 0.f;
-        float acc = incl - run;
+        if (lane == 31) ired[wid] = incl;
+        setup_sync(nt);
+        if (wid == 0) {
+            const int32_t v = lane < nw ? ired[lane] : 0;
+            int32_t inc = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t u = __shfl_up_sync(kFull, inc, o);
+                if (lane >= o) inc += u;
+            }
+            if (lane < nw) ired[lane] = inc - v;  // warp offsets
+            if (lane == 31) ired[32] = inc;       // total
+        }
+        setup_sync(nt);
+        const int32_t total = ired[32];
+        // an exact, nondecreasing prefix times one positive factor, rounded down: nondecreasing
+        // tickets.  No weights: equal slices (i < 512: 32-bit).
+        const float tickets = total > 0 ? 1048576.0f / float(total) : 0.f;
+        int32_t acc = ired[wid] + incl - run;
         for (int i = lo; i < hi; ++i) {
-            int pre = total > 0.f ? int(fminf(acc * tickets, 1048576.0f)) : (i << 20) / nslots;
-            pre = pre < 0 ? 0 : pre;
+            const int pre = total > 0 ? int(fminf(float(acc) * tickets, 1048576.0f)) : (i << 20) / nslots;
             bound[i] = (T * pre) >> 20;
-            acc += w[i];
+            acc += int32_t(w[i] * 65536.0f);
         }
-        __syncwarp();
         if (tid == 0) bound[nslots] = T;
     }
-    // bounds are monotone: the float prefix only grows and pre is clamped to [0, 2^20]
+    // bounds are monotone: the integer prefix only grows and pre is clamped to [0, 2^20]
     setup_sync(nt);
 }
 
