@@ -177,6 +177,151 @@ def traffic_from_profile():
         return None
 
 
+def warm_up(step, min_steps: int, min_seconds: float) -> int:
+    """Untimed steps right before a timed region: at least min_steps, and at least min_seconds of them (a GB300
+    idles at a low clock and takes a moment to ramp up; the per-SM split settles over the first calls on a
+    workspace).  Returns the number of steps run."""
+    n, t0 = 0, time.perf_counter()
+    while n < min_steps or time.perf_counter() - t0 < min_seconds:
+        for _ in range(max(1, min_steps)):
+            step()
+        n += max(1, min_steps)
+        torch.cuda.synchronize()
+    return n
+
+
+def launch_distribution(us):
+    """Summary of per-launch times (us, in launch order): mean, median, extremes, and the first and last five
+    (a settling or clock-ramp effect shows up as first5 above last5)."""
+    a = np.asarray(us, dtype=np.float64)
+    return {"launches": int(a.size), "mean_us": round(float(a.mean()), 2), "median_us": round(float(np.median(a)), 2),
+            "min_us": round(float(a.min()), 2), "max_us": round(float(a.max()), 2),
+            "first5_mean_us": round(float(a[:5].mean()), 2), "last5_mean_us": round(float(a[-5:].mean()), 2)}
+
+
+def source_sha() -> str:
+    """SHA-256 over every library source and the public header (the product as built), in sorted order."""
+    csrc = os.path.join(ROOT, "paged_kv_cache_62_gb300", "csrc")
+    h = hashlib.sha256()
+    for p in sorted(os.path.join(csrc, n) for n in os.listdir(csrc)) + [os.path.join(ROOT, "include", "pkv.h")]:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def run_metadata(dev) -> dict:
+    """GPU name, git commit (when the checkout has its .git), source hash and host CPU model."""
+    git = None
+    try:
+        r = subprocess.run(["git", "-C", ROOT, "rev-parse", "HEAD"], capture_output=True, text=True, timeout=10)
+        if r.returncode == 0:
+            git = r.stdout.strip()
+    except Exception:
+        pass
+    cpu = None
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.startswith("Model name:"):
+                cpu = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if cpu is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        cpu = line.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    import platform
+    return {"gpu_name": torch.cuda.get_device_name(dev), "git_commit": git, "source_sha256": source_sha(),
+            "host_cpu_model": cpu or platform.machine(), "host_cores": os.cpu_count(),
+            "torch": torch.__version__, "cuda": torch.version.cuda}
+
+
+def config_block(name, dev, rank, peak, warmup):
+    """One workload's decode step (pkv_paged_decode_store per layer), timed per launch with CUDA events after
+    `warmup` steps, and as one captured CUDA graph replayed back to back."""
+    from paged_kv_cache_62_gb300 import pkv, workloads
+    wl = workloads.make(name, dev, seed=rank_seed(name, rank))
+    s = wl.spec
+    B, Hq, Hkv, D = s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim
+    max_ctx = int(wl.lens_host().max())
+    outs = [torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev) for _ in wl.layers]
+    ws = pkv.alloc_workspace(B, Hq, Hkv, D, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    k_step = [lay.k_new[:B].contiguous() for lay in wl.layers]
+    v_step = [lay.v_new[:B].contiguous() for lay in wl.layers]
+
+    def step(evs=None, st=None):
+        st = stream if st is None else st
+        for li, lay in enumerate(wl.layers):
+            if evs is not None:
+                evs[li][0].record(st)
+            pkv.paged_decode_store(lay.q, k_step[li], v_step[li], lay.k_cache, lay.v_cache, wl.block_tables,
+                                   wl.context_lens, wl.scale, outs[li], ws, max_context_len=max_ctx, err_word=err,
+                                   stream=st)
+            if evs is not None:
+                evs[li][1].record(st)
+
+    nl = len(wl.layers)
+    n_steps = 300 if nl == 1 else 12
+    warm_up(step, max(warmup, 3), 0.1)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nl)]
+           for _ in range(n_steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(n_steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    step_ms = t0.elapsed_time(t1) / n_steps
+    per = [a.elapsed_time(b) * 1e3 for row in evs for (a, b) in row]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(st=torch.cuda.current_stream(dev))  # the capture stream
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    g_steps = 300 if nl == 1 else 20
+    t0.record(stream)
+    for _ in range(g_steps):
+        graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    g_ms = t0.elapsed_time(t1) / g_steps
+    assert err.item() == 0, f"{name}: device error word {err.item():#x}"
+    nb = step_bytes(wl)
+    dist = launch_distribution(per)
+    res = {"workload": s.description, "layers": nl, "batch": B, "launches_per_step": nl,
+           "algorithmic_bytes_per_launch": nb["fused"], "algorithmic_bytes_per_step": nb["step"],
+           "launch_us": dist,
+           "launch_gbs_median": round(nb["fused"] / (dist["median_us"] * 1e-6) / 1e9, 1),
+           "launch_frac_median": round(nb["fused"] / (dist["median_us"] * 1e-6) / 1e9 / peak, 4),
+           "step_ms": round(step_ms, 5), "step_gbs": round(nb["step"] / (step_ms * 1e-3) / 1e9, 1),
+           "step_frac": round(nb["step"] / (step_ms * 1e-3) / 1e9 / peak, 4),
+           "seq_steps_per_sec": round(B / (step_ms * 1e-3), 1),
+           "graph_step_ms": round(g_ms, 5), "graph_gbs": round(nb["step"] / (g_ms * 1e-3) / 1e9, 1),
+           "graph_seq_steps_per_sec": round(B / (g_ms * 1e-3), 1)}
+    if name == "long_mixed":
+        uniq, logical = wl.kv_bytes_unique(), wl.kv_bytes_logical()
+        ub = nb["fused"] - logical + uniq
+        res["logical_kv_bytes_per_launch"] = logical
+        res["unique_kv_bytes_per_launch"] = uniq
+        res["unique_bytes_per_launch"] = ub
+        res["unique_gbs_median"] = round(ub / (dist["median_us"] * 1e-6) / 1e9, 1)
+        res["unique_frac_median"] = round(ub / (dist["median_us"] * 1e-6) / 1e9 / peak, 4)
+        res["note"] = ("groups of 8 sequences share up to 64 leading blocks, which later readers find in L2: the "
+                       "logical figure can pass the copy peak, the unique one counts each cached row once")
+    del wl, outs, ws, graph
+    torch.cuda.empty_cache()
+    return res
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def run_pkv(args):
     ws, rank, local = dist_env()
@@ -221,11 +366,10 @@ def run_pkv(args):
         if ws > 1:
             torch.distributed.barrier()
 
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
-    assert err.item() == 0, f"device error word {err.item():#x}"
     if args.steps is None:
+        # size the run to about 2 s of GPU work (untimed calls, before the warm-up below)
+        step()
+        torch.cuda.synchronize()
         tw = time.perf_counter()
         for _ in range(10):
             step()
@@ -241,7 +385,11 @@ def run_pkv(args):
     gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] \
         if os.environ.get("CUDA_VISIBLE_DEVICES") else str(local)
     with ClockSampler(gpu_index) as clocks:
-        time.sleep(0.3)
+        time.sleep(0.3)  # nvidia-smi's first sample
+        # The warm-up runs here, right before the timed steps: an idle GB300 drops to its idle clock within
+        # a fraction of a second, and the first call after an idle gap then runs ~1.5x slower.
+        n_warm = warm_up(step, max(args.warmup, 3), 0.2)
+        assert err.item() == 0, f"device error word {err.item():#x}"
         barrier()
         torch.cuda.synchronize()
         t0.record(stream)
@@ -254,6 +402,7 @@ def run_pkv(args):
     ms = t0.elapsed_time(t1) / args.steps
     dec_ms = [a.elapsed_time(b) for row in dec_ev for (a, b) in row]
     dec_mean_ms = float(np.mean(dec_ms))
+    launch_stats = launch_distribution([x * 1e3 for x in dec_ms])
     ms = reduce_over_ranks(ms, "max", dev)
 
     # ---- the same step captured once as a CUDA graph and replayed (how a serving engine runs its
@@ -479,7 +628,7 @@ def run_pkv(args):
         "unit": "GB/s",
         "n_gpus": ws,
         "steps": args.steps,
-        "warmup": max(args.warmup, 3),
+        "warmup": n_warm,
         "ms_per_step": round(ms, 5),
         "higher_is_better": True,
         "scaling": "weak",
@@ -502,6 +651,8 @@ def run_pkv(args):
                      "achieved": round(dec_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(dec_gbs / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": nb["fused"], "mean_launch_us": round(dec_mean_ms * 1e3, 2),
+                     "median_launch_us": launch_stats["median_us"],
+                     "frac_median": round(nb["fused"] / (launch_stats["median_us"] * 1e-6) / 1e9 / peak, 4),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": round(job_bandwidth(nb["step"], ws, e2e_ms), 1), "unit": "GB/s",
@@ -515,6 +666,8 @@ def run_pkv(args):
                   "note": "the step captured once as a CUDA graph and replayed back to back (CUDA events around "
                           "all replays); the headline value above is plain stream launches"},
         "clocks": clocks.summary(),
+        "launches": launch_stats,
+        "meta": run_metadata(dev),
     }
     if mixed is not None:
         line["mixed"] = mixed
@@ -529,6 +682,9 @@ def run_pkv(args):
     if args.workload == "long_mixed":
         line["config"]["unique_kv_bytes_per_launch"] = wl.kv_bytes_unique()
         line["config"]["logical_kv_bytes_per_launch"] = wl.kv_bytes_logical()
+    if ws == 1 and not args.no_configs:
+        # every workload of the suite, one after the other (the headline one included, measured afresh)
+        line["configs"] = {name: config_block(name, dev, rank, peak, args.warmup) for name in workloads.ORDER}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
     if rank == 0:
@@ -661,6 +817,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the E4M3-cache decode measurement")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload block of all five workloads")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -53,7 +53,9 @@ typedef enum {
     PKV_EUNSUPPORTED = -2, /* valid request outside the compiled variants      */
     PKV_ECUDA = -3,        /* a CUDA runtime/driver call or launch failed      */
     PKV_EWORKSPACE = -4,   /* workspace missing or smaller than required       */
-    PKV_EBOUNDS = -5,      /* reserved for host-visible range errors           */
+    PKV_EBOUNDS = -5,      /* a size beyond a limit of the library: PKV_MAX_SEQS,
+                              PKV_MAX_WORKERS, num_blocks * block_size < 2^31,
+                              or a block table row too short for a sequence     */
     PKV_EFULL = -6         /* block allocator: not enough free blocks          */
 } pkv_status;
 
@@ -160,9 +162,16 @@ PKV_API pkv_status pkv_decode_store(const uint16_t *k, const uint16_t *v, const 
  * Bytes of device workspace that pkv_paged_decode needs for these sizes
  * (split-K partial states, one arrival counter per (sequence, kv head), and a
  * small load-balance record).  Depends only on the arguments; 0 means the
- * sizes are invalid.  The workspace must be zero-filled (cudaMemset) once
+ * sizes are invalid.  Context lengths and the block size do not enter: the
+ * kernel runs one persistent CTA per SM (at most 512 slices of the work
+ * list), and a slice leaves at most two partial states per kv head, so the
+ * partial states are bounded by the slice count and the batch, whatever the
+ * lengths.  The workspace must be zero-filled (cudaMemset) once
  * before its first use; from then on the library keeps it consistent, for
- * any sizes of later calls.  Its control block carries a call epoch that the
+ * any sizes of later calls.  Calls with up to 16384 arrival counters
+ * (num_seqs * num_kv_heads) keep them in a region no other data ever uses;
+ * larger calls clear theirs with a cudaMemsetAsync on the stream before the
+ * launch.  Its control block carries a call epoch that the
  * last CTA of every call advances on the device, so nothing per call is
  * baked into the launch and a captured CUDA graph may replay a call any
  * number of times; the per-(sequence, kv head) arrival counters return to
@@ -176,7 +185,7 @@ PKV_API pkv_status pkv_decode_store(const uint16_t *k, const uint16_t *v, const 
 PKV_API size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                        int32_t num_kv_heads, int32_t head_dim);
 
-/* Upper limits of pkv_paged_decode. */
+/* Upper limits of pkv_paged_decode (beyond them: PKV_EBOUNDS). */
 #define PKV_MAX_SEQS 16384
 #define PKV_MAX_WORKERS 4096
 
@@ -214,7 +223,13 @@ PKV_API size_t pkv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_h
  *                 has fewer units (bounded with max_context_len) than the
  *                 GPU has SMs, one CTA per unit.  Otherwise a fixed, even
  *                 split over about num_workers consumer warps (CTAs of 8
- *                 warps), 1..PKV_MAX_WORKERS (testing and tuning).
+ *                 warps), 1..PKV_MAX_WORKERS.  A tuning control, and the
+ *                 way to reproducible results: with a fixed split the
+ *                 partial states and their merge order depend only on the
+ *                 inputs, so two calls on the same inputs give bit-identical
+ *                 outputs.  The default split moves with the measured SM
+ *                 speeds, and with it the rounding of the split-K merge
+ *                 (outputs may differ in their last bits from call to call).
  * Supported: head_dim in {64, 128}; num_q_heads / num_kv_heads in 1..16
  * (bf16 caches; 1..8 for E4M3 caches);
  * block_size a power of two in [8, 1024]; num_seqs <= PKV_MAX_SEQS;
@@ -278,13 +293,20 @@ PKV_API pkv_status pkv_paged_decode_store(const uint16_t *q, const uint16_t *k_n
  *   - Sizes whose workspace (pkv_paged_decode_workspace_size) exceeds
  *     PKV_NOALLOC_SCRATCH_BYTES are rejected with PKV_EWORKSPACE before any
  *     device work; everything else is validated as in pkv_paged_decode.
- *   - The first call on a device looks up the array's device address (once,
- *     with that device current); make that first call before any stream
- *     capture.
+ *   - The array is loaded on a device, and its device memory taken, by the
+ *     first call of this entry point on that device, which also looks up its
+ *     device address (once, with that device current).  A call with
+ *     num_seqs == 0 does just that and launches nothing: make it, on each
+ *     device, before the caller hands the device's free memory to its KV
+ *     pool, and before any stream capture.  Callers of the other entry points
+ *     never load the array.
  *   - Every call on a device shares the one array, and the array keeps
- *     whatever the last call left in it (nothing in it needs to start at
- *     zero).  Calls that overlap on the GPU -- on different streams, or from
- *     different threads -- race on it: serialise them.
+ *     whatever the last call left in it.  Nothing in it needs to start at
+ *     zero: its call epoch and balance record stay valid from call to call,
+ *     and the arrival counters sit in a region no other data uses (or, for
+ *     calls with more than 16384 of them, are cleared on the stream before
+ *     the launch).  Calls that overlap on the GPU -- on different streams,
+ *     or from different threads -- race on it: serialise them.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
@@ -408,15 +430,6 @@ PKV_API pkv_status pkv_paged_decode_store_fp8(const uint16_t *q, const uint16_t 
                                               int32_t num_workers, int32_t *err_word, pkv_stream_t stream);
 
 /*
- * pkv_selftest_wait_timeout -- a diagnostic: one warp waits on a barrier that
- * nothing completes.  Every wait on an asynchronous copy in the library is
- * bounded (about 2 s); this one runs out, sets PKV_ERR_WAIT_TIMEOUT in
- * *err_word (device) and returns, leaving the context usable.  It takes the
- * wait's time limit to complete.  err_word NULL: PKV_EINVAL.
- */
-PKV_API pkv_status pkv_selftest_wait_timeout(int32_t *err_word, pkv_stream_t stream);
-
-/*
  * pkv_copy_blocks -- batched copy-on-write block copies.
  *
  * Defined by the nano-vllm KV-cache post (§2.2: sequences that share a
@@ -496,10 +509,25 @@ PKV_API int32_t pkv_allocator_num_tokens(const pkv_block_allocator *a, int32_t s
 
 /* Decode inputs for a batch, in host memory: row i of block_tables
  * [n][max_blocks] is the table of seq_ids[i], -1 padded; context_lens[i]
- * (may be NULL) its token count.  PKV_EINVAL if a sequence is unknown or
- * holds more than max_blocks blocks (nothing is written then). */
+ * (may be NULL) its token count.  PKV_EINVAL if a sequence is unknown,
+ * PKV_EBOUNDS if one holds more than max_blocks blocks (nothing is written
+ * then). */
 PKV_API pkv_status pkv_allocator_tables(const pkv_block_allocator *a, const int32_t *seq_ids, int32_t n,
                                         int32_t *block_tables, int32_t max_blocks, int32_t *context_lens);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics.  Not part of the paged-KV operations; they exercise the
+ * library's failure paths without a GPU fault.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * pkv_diag_wait_timeout -- one warp waits on a barrier that nothing completes.
+ * Every wait on an asynchronous copy in the library is bounded (about 2 s);
+ * this one runs out, sets PKV_ERR_WAIT_TIMEOUT in *err_word (device) and
+ * returns, leaving the context usable.  It takes the wait's time limit to
+ * complete.  err_word NULL: PKV_EINVAL.
+ */
+PKV_API pkv_status pkv_diag_wait_timeout(int32_t *err_word, pkv_stream_t stream);
 
 #ifdef __cplusplus
 }

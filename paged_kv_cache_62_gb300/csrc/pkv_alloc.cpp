@@ -183,7 +183,8 @@ extern "C" pkv_status pkv_allocator_tables(const pkv_block_allocator *a, const i
     if (bad(a) || n < 0 || max_blocks <= 0 || (n > 0 && (!seq_ids || !block_tables))) return PKV_EINVAL;
     for (int32_t i = 0; i < n; ++i) {
         auto it = a->seqs.find(seq_ids[i]);
-        if (it == a->seqs.end() || int64_t(it->second.table.size()) > max_blocks) return PKV_EINVAL;
+        if (it == a->seqs.end()) return PKV_EINVAL;
+        if (int64_t(it->second.table.size()) > max_blocks) return PKV_EBOUNDS;
     }
     for (int32_t i = 0; i < n; ++i) {
         const pkv_block_allocator::Seq &s = a->seqs.find(seq_ids[i])->second;

@@ -61,7 +61,7 @@ EncodeTiledFn encode_tiled_fn()
 
 }  // namespace pkv
 
-extern "C" int pkv_abi_version(void) { return 1; }
+extern "C" int pkv_abi_version(void) { return 2; }
 
 extern "C" const char *pkv_last_cuda_error(void) { return pkv::g_last_cuda_error; }
 
@@ -73,7 +73,7 @@ extern "C" const char *pkv_status_string(int status)
     case PKV_EUNSUPPORTED: return "unsupported configuration";
     case PKV_ECUDA: return "CUDA call or kernel launch failed";
     case PKV_EWORKSPACE: return "workspace missing or too small";
-    case PKV_EBOUNDS: return "index out of range";
+    case PKV_EBOUNDS: return "size beyond a limit of the library";
     case PKV_EFULL: return "not enough free blocks";
     default: return "unknown pkv status";
     }

@@ -1,6 +1,6 @@
 // Decode-phase PagedAttention entry points (include/pkv.h): argument checks,
 // the launch of the bf16-cache kernels (the kernel itself is in
-// pkv_decode_kernel.cuh), the workspace size and the allocation-free variant.
+// pkv_decode_kernel.cuh) and the workspace size.
 #include "pkv_decode_kernel.cuh"
 
 using namespace pkv;
@@ -33,16 +33,16 @@ static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, 
 {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
         head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 ||
-        num_workers < 0 || num_workers > PKV_MAX_WORKERS || !std::isfinite(scale))
+        num_workers < 0 || !std::isfinite(scale))
         return PKV_EINVAL;
-    if (num_seqs > PKV_MAX_SEQS) return PKV_EUNSUPPORTED;
+    if (num_seqs > PKV_MAX_SEQS || num_workers > PKV_MAX_WORKERS) return PKV_EBOUNDS;
     if (head_dim != 64 && head_dim != 128) return PKV_EUNSUPPORTED;
     if (qn < 1) return PKV_EINVAL;
     const int gq = num_q_heads / num_kv_heads;  // query heads per kv head
     const int G = gq * qn;                      // virtual heads per kv head sharing one K/V stream
     if (G > (fp8 ? 8 : 16)) return PKV_EUNSUPPORTED;  // virtual heads per warp: the MMA tile's rows
     if (!is_pow2(block_size) || block_size < 8 || block_size > 1024) return PKV_EUNSUPPORTED;
-    if (int64_t(num_blocks) * block_size > INT32_MAX) return PKV_EUNSUPPORTED;
+    if (int64_t(num_blocks) * block_size > INT32_MAX) return PKV_EBOUNDS;
     if (num_seqs == 0) return PKV_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_EINVAL;
     if (fp8 && (!k_scale || !v_scale)) return PKV_EINVAL;
@@ -50,7 +50,7 @@ static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, 
     const int64_t len_limit = std::min<int64_t>(max_context_len, int64_t(max_blocks_per_seq) * block_size);
     // unit counts (and positions in the unit list) are kept in 32 bits
     const int64_t max_units = int64_t(num_kv_heads) * num_seqs * ((len_limit + 7) / 8);
-    if (max_units > INT32_MAX) return PKV_EUNSUPPORTED;
+    if (max_units > INT32_MAX) return PKV_EBOUNDS;
     if (qs && (fp8 || !row_cnt)) return PKV_EINVAL;  // query-split entries are chunks of bf16 calls
     if ((k_new || v_new) && (qs || qn != 1 || row_seq || !k_new || !v_new || !aligned16(k_new) ||
                              !aligned16(v_new)))
@@ -124,6 +124,13 @@ static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, 
                   : G > 8 ? pick_decode_wide(head_dim, G)
                          : (head_dim == 64 ? pick_group<64, false, false>(G) : pick_group<128, false, false>(G));
     if (!fn) return PKV_EUNSUPPORTED;
+    if (ws.count_clear) {  // counters outside the fixed region start at zero (see WsLayout)
+        const cudaError_t ce = cudaMemsetAsync(p.ws_count, 0, ws.count_bytes, a.stream);
+        if (ce != cudaSuccess) {
+            cudaGetLastError();
+            return cuda_fail("cudaMemsetAsync (arrival counters)", ce);
+        }
+    }
     return fn(a);
 }
 
@@ -187,75 +194,6 @@ extern "C" pkv_status pkv_paged_decode_fp8(const uint16_t *q, const uint8_t *k_c
                        max_blocks_per_seq, context_lens,
                        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale,
                        out, workspace, workspace_bytes, num_workers, err_word, stream);
-}
-
-// ------------------------------------------------------------------ allocation-free variant
-// Some callers cannot hand the library a workspace: an engine that gave
-// (nearly) all free device memory to its KV block pool at start-up, or a host
-// framework whose plugin interface passes only inputs and outputs and forbids
-// device allocations while it runs.  For them the decode scratch lives in a
-// fixed array owned by this library: kStaticScratchBytes on every device that
-// loads it, held until the process exits.
-#include <mutex>
-
-namespace pkv {
-
-constexpr size_t kStaticScratchBytes = size_t(PKV_NOALLOC_SCRATCH_BYTES);
-static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
-
-// Device address of g_decode_scratch on the current device.  The name of the
-// array in host code is only a host-side stand-in, so the address is asked of
-// the runtime once per device (with that device current) and cached.
-static void *static_scratch_address(pkv_status *status)
-{
-    static std::mutex mu;
-    static void *addr[64] = {};
-    int dev = -1;
-    const cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64) {
-        cudaGetLastError();
-        record_cuda_error("cudaGetDevice", e != cudaSuccess ? cudaGetErrorString(e) : "device index out of range");
-        *status = PKV_ECUDA;
-        return nullptr;
-    }
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        const cudaError_t se = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (se != cudaSuccess || !p) {
-            cudaGetLastError();
-            record_cuda_error("cudaGetSymbolAddress", se != cudaSuccess ? cudaGetErrorString(se) : "null address");
-            *status = PKV_ECUDA;
-            return nullptr;
-        }
-        addr[dev] = p;
-    }
-    return addr[dev];
-}
-
-}  // namespace pkv
-
-extern "C" pkv_status pkv_paged_decode_noalloc(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
-                                               const int32_t *block_tables, int32_t max_blocks_per_seq,
-                                               const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
-                                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                                               int32_t num_blocks, int32_t max_context_len, float scale,
-                                               uint16_t *out, int32_t num_workers, int32_t *err_word,
-                                               pkv_stream_t stream)
-{
-    // Size check first, on the host only: reject what does not fit the fixed scratch.
-    const size_t need = pkv_paged_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim);
-    if (need > kStaticScratchBytes) return PKV_EWORKSPACE;
-    if (num_seqs == 0 || need == 0)  // nothing to do, or invalid sizes: the regular checks answer
-        return pkv_paged_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                                num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale,
-                                out, nullptr, 0, num_workers, err_word, stream);
-    pkv_status st = PKV_OK;
-    void *scratch = static_scratch_address(&st);
-    if (!scratch) return st;
-    return pkv_paged_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                            num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, out,
-                            scratch, kStaticScratchBytes, num_workers, err_word, stream);
 }
 
 // ------------------------------------------------------------------ several query rows per sequence
@@ -370,7 +308,7 @@ extern "C" pkv_status pkv_paged_attention(const uint16_t *q, const uint16_t *k_c
     if (new_per_seq > 0 && int64_t(num_seqs) * new_per_seq != num_rows) return PKV_EINVAL;
     if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0) return PKV_EINVAL;
     const size_t need = pkv_paged_attention_workspace_size(num_rows, num_q_heads, num_kv_heads, head_dim);
-    if (need == 0) return num_rows > PKV_MAX_SEQS ? PKV_EUNSUPPORTED : PKV_EINVAL;
+    if (need == 0) return num_rows > PKV_MAX_SEQS ? PKV_EBOUNDS : PKV_EINVAL;
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PKV_EWORKSPACE;
     // Up to qg queries of a sequence fit one regular CTA warp's MMA tile (qg * G <= 16 virtual heads):
     // the CTA's warps split the K/V tokens, as in decode.  Longer runs of new tokens go to query-split

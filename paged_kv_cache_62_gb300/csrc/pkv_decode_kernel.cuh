@@ -227,8 +227,18 @@ inline int warp_slices(int G, int hg)
     return s;
 }
 
+// Workspace regions.  The arrival counters of a call must read as zero (or as
+// another call's tag) when it starts.  A completed call leaves its counters at
+// zero, but a call of other sizes on the same workspace may have used the same
+// words for partial states, whose bits can be anything.  So calls with up to
+// kFixedCounters counters keep them in a region at a fixed offset that nothing
+// else ever uses; a larger call keeps them after that region, and the host
+// clears them on the stream before its launch (count_clear).
+constexpr size_t kFixedCounters = 16384;
+
 struct WsLayout {
-    size_t bal_off, count_off, ml_off, acc_off, total;
+    size_t bal_off, count_off, count_bytes, ml_off, acc_off, total;
+    bool count_clear;  // counters outside the fixed region: cleared by the host before the launch
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -257,8 +267,12 @@ inline WsLayout ws_layout(int32_t B, int32_t G, int32_t Hkv, int32_t D, bool qs 
                          size_t(hg) * subq;
     WsLayout w;
     w.bal_off = 0;
-    w.count_off = align256(sizeof(BalanceState));
-    w.ml_off = w.count_off + align256(size_t(B) * size_t(Hkv) * subq * 8);
+    const size_t fixed_off = align256(sizeof(BalanceState)), fixed_end = fixed_off + kFixedCounters * 8;
+    const size_t counters = size_t(B) * size_t(Hkv) * subq;
+    w.count_clear = counters > kFixedCounters;
+    w.count_off = w.count_clear ? fixed_end : fixed_off;
+    w.count_bytes = counters * 8;
+    w.ml_off = w.count_clear ? align256(fixed_end + w.count_bytes) : fixed_end;
     w.acc_off = w.ml_off + align256(slots * size_t(G) * 2 * 4);
     w.total = w.acc_off + slots * size_t(G) * size_t(D) * 4;
     return w;
@@ -574,7 +588,12 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
             }
         }
     }
-    uint32_t pb[HR][NT][2];
+    // The weights as the output product's operand.  bf16 caches: two parts, hi = bf16(p) and lo =
+    // bf16(p - hi); hi + lo carries p to 2^-17 of itself and both products are exact in the fp32
+    // accumulators, so the output is the fp32 weights' sum to about fp32 precision.  E4M3 caches: one
+    // f16 part (2^-12 of p; the products run in f16 there, and the consumers are the bound, so a
+    // second product would cost time).
+    uint32_t pb[HR][NT][2], pl[HR][NT][2];
 #pragma unroll
     for (int hr = 0; hr < HR; ++hr) {
         float pr[NT * 4];
@@ -585,11 +604,19 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
         for (int k = 0; k < NT * 4; ++k) ps += pr[k];
         l[hr] += ps;
 #pragma unroll
-        for (int st = 0; st < NT; ++st) {
-            pb[hr][st][0] = FP8 ? f16x2_of(pr[4 * st], pr[4 * st + 1]) : pack_bf16x2(pr[4 * st], pr[4 * st + 1]);
-            pb[hr][st][1] =
-                FP8 ? f16x2_of(pr[4 * st + 2], pr[4 * st + 3]) : pack_bf16x2(pr[4 * st + 2], pr[4 * st + 3]);
-        }
+        for (int st = 0; st < NT; ++st)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const float p0 = pr[4 * st + 2 * c], p1 = pr[4 * st + 2 * c + 1];
+                if constexpr (FP8) {
+                    pb[hr][st][c] = f16x2_of(p0, p1);
+                    pl[hr][st][c] = 0u;
+                } else {
+                    pb[hr][st][c] = pack_bf16x2(p0, p1);
+                    pl[hr][st][c] = pack_bf16x2(p0 - __uint_as_float(pb[hr][st][c] << 16),
+                                                p1 - __uint_as_float(pb[hr][st][c] & 0xffff0000u));
+                }
+            }
     }
 
 #pragma unroll
@@ -615,7 +642,10 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
             if constexpr (!FP8) {
                 // m-tile i: dims 16i + g (r0: tokens 0-7, r2: tokens 8-15) and 16i + 8 + g (r1, r3)
 #pragma unroll
-                for (int hr = 0; hr < HR; ++hr) mma_bf16_16816(o[i][hr], r0, r1, r2, r3, pb[hr][st][0], pb[hr][st][1]);
+                for (int hr = 0; hr < HR; ++hr) {
+                    mma_bf16_16816(o[i][hr], r0, r1, r2, r3, pb[hr][st][0], pb[hr][st][1]);
+                    mma_bf16_16816(o[i][hr], r0, r1, r2, r3, pl[hr][st][0], pl[hr][st][1]);
+                }
             } else {
                 // a register holds (token 2r4: dims 2g, 2g+1 | token 2r4+1: dims 2g, 2g+1) of a 16-dim
                 // chunk; the byte permute pairs the two tokens per dim: low half dim 2g, high half dim 2g+1

@@ -210,7 +210,8 @@ extern "C" pkv_status pkv_decode_slot_mapping(const int32_t *block_tables, int32
                                               int32_t *err_word, pkv_stream_t stream)
 {
     if (num_seqs < 0 || num_tokens < num_seqs || max_blocks_per_seq <= 0 || num_blocks <= 0) return PKV_EINVAL;
-    if (!is_pow2(block_size) || static_cast<int64_t>(num_blocks) * block_size > INT32_MAX) return PKV_EINVAL;
+    if (!is_pow2(block_size)) return PKV_EINVAL;
+    if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX) return PKV_EBOUNDS;
     if (num_tokens == 0) return PKV_OK;
     if (!slot_mapping || (num_seqs > 0 && (!block_tables || !context_lens))) return PKV_EINVAL;
     const int threads = 128;
@@ -255,7 +256,7 @@ extern "C" pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, const i
 // A wait on an mbarrier that nothing completes: the bounded wait gives up at
 // its time limit, the kernel flags PKV_ERR_WAIT_TIMEOUT and returns (the
 // timeout path of every wait in the library, exercised without a fault).
-__global__ void wait_timeout_selftest_kernel(int32_t *err)
+__global__ void diag_wait_timeout_kernel(int32_t *err)
 {
     __shared__ __align__(8) uint64_t bar;
     if (threadIdx.x == 0) {
@@ -266,13 +267,13 @@ __global__ void wait_timeout_selftest_kernel(int32_t *err)
     if (!mbar_wait_bounded(&bar, 0u) && threadIdx.x == 0) flag_error(err, PKV_ERR_WAIT_TIMEOUT);
 }
 
-extern "C" pkv_status pkv_selftest_wait_timeout(int32_t *err_word, pkv_stream_t stream)
+extern "C" pkv_status pkv_diag_wait_timeout(int32_t *err_word, pkv_stream_t stream)
 {
     if (!err_word) return PKV_EINVAL;
-    wait_timeout_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err_word);
+    diag_wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err_word);
     const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail("wait_timeout_selftest_kernel launch", e);
-    return launch_status("wait_timeout_selftest_kernel launch");
+    if (e != cudaSuccess) return cuda_fail("diag_wait_timeout_kernel launch", e);
+    return launch_status("diag_wait_timeout_kernel launch");
 }
 
 extern "C" pkv_status pkv_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, const int32_t *pairs,
@@ -339,7 +340,8 @@ extern "C" pkv_status pkv_decode_store(const uint16_t *k, const uint16_t *v, con
 {
     if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0)
         return PKV_EINVAL;
-    if (!is_pow2(block_size) || static_cast<int64_t>(num_blocks) * block_size > INT32_MAX) return PKV_EINVAL;
+    if (!is_pow2(block_size)) return PKV_EINVAL;
+    if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX) return PKV_EBOUNDS;
     const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * 2;
     if (row_bytes % 16 != 0 || row_bytes / 16 > INT32_MAX) return PKV_EINVAL;
     if (num_seqs == 0) return PKV_OK;

@@ -37,7 +37,7 @@ SIGNATURES = {
                                                   _I32, _I32, _I32, _I32, _F32, _P, _P, _P, _SZ, _I32, _P, _P]),
     "pkv_paged_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                                 _I32, _F32, _P, _I32, _P, _P]),
-    "pkv_selftest_wait_timeout": (ctypes.c_int, [_P, _P]),
+    "pkv_diag_wait_timeout": (ctypes.c_int, [_P, _P]),
     "pkv_copy_blocks": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P]),
     "pkv_paged_attention_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "pkv_paged_attention": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
@@ -238,10 +238,11 @@ def paged_decode_store_fp8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Te
         "pkv_paged_decode_store_fp8")
 
 
-def selftest_wait_timeout(err_word: torch.Tensor, stream=None) -> None:
-    """A bounded wait that runs out on purpose: sets ERR_WAIT_TIMEOUT in err_word after the wait's limit."""
-    _check(load().pkv_selftest_wait_timeout(_dev(err_word, torch.int32, "err_word"), _stream(stream)),
-           "pkv_selftest_wait_timeout")
+def diag_wait_timeout(err_word: torch.Tensor, stream=None) -> None:
+    """Diagnostic: a bounded wait that runs out on purpose; sets ERR_WAIT_TIMEOUT in err_word after the wait's
+    limit."""
+    _check(load().pkv_diag_wait_timeout(_dev(err_word, torch.int32, "err_word"), _stream(stream)),
+           "pkv_diag_wait_timeout")
 
 
 def paged_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,

@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.pkv_abi_version() == 1
+    assert lib.pkv_abi_version() == 2
     for st in (0, -1, -2, -3, -4, -5, 42):
         assert lib.pkv_status_string(st)
 
@@ -84,15 +84,15 @@ def decode_args(**kw):
     (dict(bs=4), pkv.EUNSUPPORTED),
     (dict(bs=2048), pkv.EUNSUPPORTED),
     (dict(B=-1), pkv.EINVAL),
-    (dict(B=pkv.MAX_SEQS + 1), pkv.EUNSUPPORTED),
+    (dict(B=pkv.MAX_SEQS + 1), pkv.EBOUNDS),
     (dict(maxctx=-1), pkv.EINVAL),
     (dict(workers=-1), pkv.EINVAL),
-    (dict(workers=pkv.MAX_WORKERS + 1), pkv.EINVAL),
+    (dict(workers=pkv.MAX_WORKERS + 1), pkv.EBOUNDS),
     (dict(scale=float("nan")), pkv.EINVAL),
     (dict(q=FAKE + 8), pkv.EINVAL),            # misaligned
     (dict(ws=NULL), pkv.EWORKSPACE),
     (dict(wsb=16), pkv.EWORKSPACE),
-    (dict(NB=1 << 27, bs=256), pkv.EUNSUPPORTED),  # rows beyond int32
+    (dict(NB=1 << 27, bs=256), pkv.EBOUNDS),       # rows beyond int32
 ])
 def test_paged_decode_host_validation(lib, kw, status):
     assert lib.pkv_paged_decode(*decode_args(**kw)) == status
@@ -155,7 +155,7 @@ def test_newer_entry_points_validate_on_the_host(lib):
     tail8 = [FAKE, 4, FAKE, 2, 16, 8, 128, 16, 10, 64, 0.1, FAKE, NULL, FAKE, 1 << 30, 0, NULL, NULL]
     assert pf(FAKE, NULL, FAKE, FAKE, FAKE, FAKE, FAKE, *tail8) == pkv.EINVAL     # no k_new
     assert pf(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, *tail8) == pkv.EINVAL     # no k_scale
-    assert lib.pkv_selftest_wait_timeout(NULL, NULL) == pkv.EINVAL
+    assert lib.pkv_diag_wait_timeout(NULL, NULL) == pkv.EINVAL
     # pkv_kv_store_fp8(k, v, slots, T, kc8, vc8, NB, bs, Hkv, D, ks, vs, err, stream)
     kf = lib.pkv_kv_store_fp8
     assert kf(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 10, 16, 8, 128, NULL, FAKE, NULL, NULL) == pkv.EINVAL     # no k_scale
@@ -187,7 +187,7 @@ def test_newer_entry_points_validate_on_the_host(lib):
     bad = list(att); bad[17] = 3                                                                        # 2 * 3 != 5 rows
     assert pa(*bad) == pkv.EINVAL
     bad = list(att); bad[8] = pkv.MAX_SEQS + 1
-    assert pa(*bad) == pkv.EUNSUPPORTED
+    assert pa(*bad) == pkv.EBOUNDS
     bad = list(att); bad[8] = 0
     assert pa(*bad) == pkv.OK                                                                           # no rows
 

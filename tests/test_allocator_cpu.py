@@ -124,6 +124,12 @@ def test_tables_are_padded_and_carry_lengths():
     bt, lens = a.tables([3, 7], 4)
     assert bt.tolist() == [[3, -1, -1, -1], [0, 1, 2, -1]]
     assert lens.tolist() == [1, 17]
+    with pytest.raises(pkv.PkvError) as e:      # sequence 7 holds 3 blocks: a row of 2 is too short
+        a.tables([3, 7], 2)
+    assert e.value.status == pkv.EBOUNDS
+    with pytest.raises(pkv.PkvError) as e:      # unknown sequence
+        a.tables([5], 4)
+    assert e.value.status == pkv.EINVAL
 
 
 class Model:
