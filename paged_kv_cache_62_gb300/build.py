@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(HERE, "libpkv.so")
 SOURCES = ["pkv_api.cu", "pkv_store.cu", "pkv_decode.cu", "pkv_decode_fp8.cu", "pkv_decode_qs.cu", "pkv_decode_wide.cu",
-           "pkv_noalloc.cu", "pkv_alloc.cpp"]
+           "pkv_decode_tc5.cu", "pkv_noalloc.cu", "pkv_alloc.cpp"]
 HEADERS = ["pkv_device.cuh", "pkv_host.h", "pkv_decode_kernel.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # Hidden visibility: only the PKV_API (extern "C") entry points are exported, so

@@ -81,14 +81,16 @@ static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, 
     p.NB = num_blocks;
     p.max_blocks = max_blocks_per_seq;
     p.len_limit = int32_t(len_limit);
+    // query-split entries of 128 rows run on the tensor-memory CTAs where they can
+    const bool tc5 = qs && !fp8 && tc5_eligible(head_dim, G, gq, block_size, num_seqs, dev.max_smem_optin);
     p.hg = qs ? 1 : head_group(num_kv_heads, G);
     p.nhg = num_kv_heads / p.hg;
     p.sub = qs ? team_warps(G) : warp_slices(G, p.hg);
-    p.toks = warp_tokens(G, fp8, qs) * (qs ? 1 : p.sub);
+    p.toks = warp_tokens(G, fp8, qs, tc5) * (qs ? 1 : p.sub);
     p.boxtok = std::min(p.toks, block_size);
     p.nbox = p.toks / p.boxtok;
     p.lg_nbox = ilog2(p.nbox);
-    p.cons = p.hg * p.sub;
+    p.cons = tc5 ? kTc5Consumers : p.hg * p.sub;
     p.nst = 2;
     p.num_workers = 0;
     p.scale_log2 = float(double(scale) * 1.4426950408889634);
@@ -120,6 +122,7 @@ static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, 
     a.stream = reinterpret_cast<cudaStream_t>(stream);
 
     LaunchFn fn = fp8    ? pick_decode_fp8(head_dim, G)
+                  : tc5  ? pick_decode_tc5(head_dim)
                   : qs   ? pick_decode_qs(head_dim, G)
                   : G > 8 ? pick_decode_wide(head_dim, G)
                          : (head_dim == 64 ? pick_group<64, false, false>(G) : pick_group<128, false, false>(G));

@@ -87,8 +87,21 @@ constexpr int kHintUnits = 16;
 __host__ __device__ constexpr int team_warps(int) { return 8; }
 // Query-split CTAs (qs; long runs of new tokens, see paged_decode_kernel)
 // take 32-token tiles too: one kv head's stage is small, and every warp
-// works on every token.
-__host__ __device__ constexpr int warp_tokens(int, bool fp8, bool qs = false) { return fp8 || qs ? 32 : 16; }
+// works on every token.  Their tensor-memory variant (tc5) takes 64 keys a
+// tile: the N extent of one score product.
+__host__ __device__ constexpr int warp_tokens(int, bool fp8, bool qs = false, bool tc5 = false)
+{
+    return tc5 ? 64 : (fp8 || qs ? 32 : 16);
+}
+
+// Tensor-memory (tcgen05) query-split CTAs: 4 warps that own the 128 rows of
+// the tile (the softmax and the epilogue), one warp that issues the tensor-core
+// products, then the producer warp.
+constexpr int kTc5SoftmaxWarps = 4;
+constexpr int kTc5Consumers = kTc5SoftmaxWarps + 1;
+constexpr int kTc5Keys = 64;           // keys per tile (one unit)
+constexpr uint32_t kTc5Cols = 256;     // TMEM columns: two 64-column score buffers, then the output (<= 128)
+constexpr uint32_t kTc5SlabBytes = 128u * 128u;  // one 64-dim slab of the 128-row Q tile, or of P
 
 // ------------------------------------------------------------------ load balance state
 // In the adaptive mode a slice's size follows what the previous call on this
@@ -163,8 +176,8 @@ constexpr int kSliceEnd = 4;  // last unit of the slice
 
 // Shared-memory layout, computed the same way on the host (size) and device (offsets).
 struct CtaLayout {
-    uint32_t kv_bytes, stage_bytes, q_bytes, comb_bytes;
-    uint32_t off_q, off_comb, off_meta, off_bar, off_bound, off_wts, off_red, off_sh, off_scan, total;
+    uint32_t kv_bytes, stage_bytes, q_bytes, comb_bytes, p_bytes;
+    uint32_t off_q, off_p, off_comb, off_meta, off_bar, off_bound, off_wts, off_red, off_sh, off_scan, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -175,26 +188,32 @@ __host__ __device__ inline int comb_stride(int D, int G) { return int(align_up(u
 
 // es: bytes per cached element (2 for bf16, 1 for E4M3); qs: query-split
 // CTA (all sub warps of a kv head on the same tokens, each with its own G
-// virtual heads).
+// virtual heads); tc5: its tensor-memory variant (the Q tile and the weights
+// P as 128-byte-swizzled 128-row operands of 64-dim slabs, P in two parts).
 __host__ __device__ inline CtaLayout cta_layout(int D, int G, int es, int hg, int sub, int nst, int B,
-                                                bool qs = false)
+                                                bool qs = false, bool tc5 = false)
 {
     CtaLayout l;
-    const int toks = warp_tokens(G, es == 1, qs) * (qs ? 1 : sub);
+    const int toks = warp_tokens(G, es == 1, qs, tc5) * (qs ? 1 : sub);
     l.kv_bytes = uint32_t(toks * hg * D * es);
     l.stage_bytes = align_up(2 * l.kv_bytes, 1024);  // stages start on the 1024-byte swizzle period
-    l.q_bytes = align_up(uint32_t(hg * (qs ? sub : 1) * G * D * 2), 128);
+    l.q_bytes = tc5 ? uint32_t(D / 64) * kTc5SlabBytes : align_up(uint32_t(hg * (qs ? sub : 1) * G * D * 2), 128);
+    l.p_bytes = tc5 ? 2 * kTc5SlabBytes : 0u;
     // states of the non-leading warps of every head (the leader keeps its own in registers)
     l.comb_bytes = sub > 1 && !qs ? align_up(uint32_t(hg * (sub - 1) * comb_stride(D, G) * 4), 128) : 0u;
     uint32_t o = uint32_t(nst) * l.stage_bytes;
     l.off_q = o;
     o += 2 * l.q_bytes;
+    l.off_p = o;
+    o += l.p_bytes;
     l.off_comb = o;
     o += l.comb_bytes;
     l.off_meta = o;
     o += uint32_t(nst) * uint32_t(sizeof(UnitMeta));
     l.off_bar = o;
-    o += uint32_t(2 * nst + 6) * 8;  // full / empty per stage, q full / empty x2, combine full / free
+    // full / empty per stage, q full / empty x2, combine full / free; tc5: scores full x2, weights
+    // full, output product done, drain
+    o += uint32_t(2 * nst + 6 + (tc5 ? 5 : 0)) * 8;
     l.off_bound = align_up(o, 16);
     o = l.off_bound + (kMaxSlots + 1) * 8;
     l.off_wts = o;
@@ -1013,21 +1032,341 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
     }
 }
 
+// ------------------------------------------------------------------ tensor-memory query-split CTA (tc5)
+// A query-split entry of 128 rows -- 128 / gq queries x gq query heads of one kv head, row r = query
+// r / gq, head r % gq, in blocks of G = 16 rows that play the part of the query-split CTA's warps (jq) --
+// against 64-key tiles of that kv head, on the 5th-generation tensor cores:
+//   S = Q K^T      128 x 64 fp32 in tensor memory (two buffers), Q and K 128-byte-swizzled K-major in
+//                  shared memory (the Q tile loaded by one TMA copy per entry, K by the stage's copy);
+//   P = 2^(S - m)  by 4 warps, thread r owning row r (its TMEM lane): masks, running max m and sum l,
+//                  P written to shared memory as two bf16 parts (hi, lo = P - hi);
+//   O += P V       128 x D fp32 in tensor memory, V the stage's rows as an MN-major operand; O is
+//                  rescaled in place (read, scaled, written back by its row's thread) only when a row's
+//                  max passes m by the slack, which after a segment's first tiles is rare.
+// One thread of the MMA warp issues the products in the order S(0), S(1), P(0)V, S(2), P(1)V, ..., so
+// the scores of the next tile are computed while the softmax warps work on the current one.  Ordering:
+// scores -> sfull[j % 2] (tcgen05.commit), weights written -> pfull (4 warps), output product done ->
+// odone and the stage's empty barrier (commits), a segment's last scores -> its Q slot's qempty.  The
+// softmax warps write P(j) only after the product of unit j - 1 is done, so one P buffer serves.
+struct Tc5Smem {
+    const UnitMeta *metas;
+    uint64_t *full, *empty, *qfull, *qempty, *sfull, *pfull, *odone, *drain;
+    uint8_t *stage0, *pbuf;
+    uint32_t stage_addr, q_addr, p_addr;  // shared addresses of stage 0, Q slot 0, P (hi; lo follows)
+};
+
+template <int D>
+__device__ __forceinline__ void tc5_output_product(const DecodeParams &p, const CtaLayout &lay, const Tc5Smem &m,
+                                                   uint32_t tmem, int slot, bool first, int lane)
+{
+    constexpr uint32_t IP = idesc_bf16_f32(128, D, true);
+    if (lane == 0) {
+        tc_fence_after();
+        const uint32_t va = m.stage_addr + uint32_t(slot) * lay.stage_bytes + lay.kv_bytes;
+        // V: keys along K (8-key groups 1024 bytes apart), dims along N (64-dim blocks 64 * 128 bytes apart)
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int ks = 0; ks < kTc5Keys / 16; ++ks)
+                tc_mma_bf16(tmem + 128u, smem_desc_sw128(m.p_addr + uint32_t(part) * kTc5SlabBytes + ks * 32, 16, 1024),
+                            smem_desc_sw128(va + ks * 2048, kTc5Keys * 128, 1024), IP, !(first && part == 0 && ks == 0));
+        tc_commit(m.odone);
+        tc_commit(&m.empty[slot]);
+    }
+    __syncwarp();
+}
+
+// The MMA warp: waits on the ring like the consumers, issues every tensor-core product of the CTA from
+// lane 0, and before it returns waits for all of them to complete (also when a wait gave up).
+template <int D>
+__device__ void tc5_mma_warp(const DecodeParams &p, const CtaLayout &lay, const Tc5Smem &m, uint32_t tmem)
+{
+    constexpr uint32_t IS = idesc_bf16_f32(128, kTc5Keys, false);
+    const int lane = threadIdx.x & 31;
+    int s = 0;
+    uint32_t ph = 0, j = 0, segs = 0;
+    int cur = -1;  // ring slot of unit j - 1, whose output product is pending
+    bool cur_first = false;
+    bool dead = false;
+    int qs = 0;
+    for (;;) {
+        if (!mbar_wait_bounded(&m.full[s], ph)) {
+            dead = true;
+            break;
+        }
+        const int b = m.metas[s].b, flags = m.metas[s].flags;
+        if (b < 0) break;
+        if (flags & kFirst) {
+            qs = int(segs & 1u);
+            if (!mbar_wait_bounded(&m.qfull[qs], (segs >> 1) & 1u)) {
+                dead = true;
+                break;
+            }
+            ++segs;
+        }
+        if (lane == 0) {  // S(j) = Q K^T into score buffer j % 2 (its previous scores were read: P(j - 2) came)
+            tc_fence_after();
+            const uint32_t qa = m.q_addr + uint32_t(qs) * lay.q_bytes;
+            const uint32_t ka = m.stage_addr + uint32_t(s) * lay.stage_bytes;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t within = uint32_t(ks & 3) * 32, slab = uint32_t(ks >> 2);
+                tc_mma_bf16(tmem + (j & 1u) * kTc5Keys, smem_desc_sw128(qa + slab * kTc5SlabBytes + within, 16, 1024),
+                            smem_desc_sw128(ka + slab * (kTc5Keys * 128) + within, 16, 1024), IS, ks > 0);
+            }
+            tc_commit(&m.sfull[j & 1u]);
+            if (flags & kLast) tc_commit(&m.qempty[qs]);  // the segment's Q tile is read for the last time
+        }
+        __syncwarp();
+        if (cur >= 0) {  // O += P(j - 1) V(j - 1) once its weights are written
+            if (!mbar_wait_bounded(m.pfull, (j - 1) & 1u)) {
+                dead = true;
+                break;
+            }
+            tc5_output_product<D>(p, lay, m, tmem, cur, cur_first, lane);
+        }
+        cur = s;
+        cur_first = (flags & kFirst) != 0;
+        ++j;
+        if (++s == p.nst) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+    if (!dead && cur >= 0) {
+        if (mbar_wait_bounded(m.pfull, (j - 1) & 1u))
+            tc5_output_product<D>(p, lay, m, tmem, cur, cur_first, lane);
+        else
+            dead = true;
+    }
+    if (dead && lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
+    // every product issued has completed before the tensor memory is freed
+    if (lane == 0) tc_commit(m.drain);
+    __syncwarp();
+    if (!mbar_wait_bounded(m.drain, 0u) && lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
+}
+
+// The softmax warps (threads 0..127, thread r = row r = TMEM lane r).
+template <int D, int G>
+__device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, const Tc5Smem &m, uint32_t tmem,
+                                  const long long *bound, const int32_t *scan, const int *sh, const float *wts,
+                                  int nslots, uint32_t gen, int wp, bool adaptive)
+{
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);  // this warp's lane quarter
+    const int qi = t / p.gq;                                    // query of the row within its entry
+    const int jq = t / G, hh = t - jq * G;                      // block of G rows and the row in it
+    const int home = sh[0];
+    int s = 0;
+    uint32_t ph = 0, j = 0;
+    float mrun = -INFINITY, lrun = 0.f;
+    bool row_ok = false;
+    int shift = 0, u_first = 0;
+    for (;;) {
+        if (!mbar_wait_bounded(&m.full[s], ph)) {
+            if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
+            break;
+        }
+        const UnitMeta mt = m.metas[s];
+        if (mt.b < 0) break;
+        const bool first = (mt.flags & kFirst) != 0;
+        if (first) {
+            row_ok = qi < mt.cnt;
+            shift = (mt.cnt - 1) - qi;  // the row's query sees this many fewer of the entry's last keys
+            mrun = -INFINITY;
+            lrun = 0.f;
+            u_first = mt.u;
+        }
+        const int tok0 = mt.u * kTc5Keys;
+        const int valid = min(kTc5Keys, mt.L - tok0);
+        const int lim = row_ok ? min(valid, mt.L - tok0 - shift) : 0;
+        if (valid < kTc5Keys) {
+            // V rows past the sequence's end hold anything (NaN included) and 0 * NaN is NaN: zero them
+            uint8_t *vrows = m.stage0 + size_t(s) * lay.stage_bytes + lay.kv_bytes;
+            const int per_part = (kTc5Keys - valid) * 8, n = per_part * (D / 64);
+            for (int i = t; i < n; i += 32 * kTc5SoftmaxWarps) {
+                const int part = i / per_part, r = i - part * per_part;
+                *reinterpret_cast<uint4 *>(vrows + part * (kTc5Keys * 128) + valid * 128 + r * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        if (!mbar_wait_bounded(&m.sfull[j & 1u], (j >> 1) & 1u)) {
+            if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
+            break;
+        }
+        tc_fence_after();
+        float x[kTc5Keys];
+        {
+            uint32_t r[32];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                tmem_ld32(trow + (j & 1u) * kTc5Keys + h2 * 32, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    x[h2 * 32 + i] = h2 * 32 + i < lim ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+            }
+        }
+        float mx = x[0];
+#pragma unroll
+        for (int i = 1; i < kTc5Keys; ++i) mx = fmaxf(mx, x[i]);
+        // the previous output product is done: P's buffer is free and O may be read
+        if (j > 0 && !mbar_wait_bounded(m.odone, (j - 1) & 1u)) {
+            if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
+            break;
+        }
+        tc_fence_after();
+        float alpha = 1.0f;
+        bool resc = false;
+        if (mx > mrun + kRescaleSlack) {  // also the row's first tile with a key (mrun = -inf)
+            if (!first && mrun != -INFINITY) {
+                alpha = ex2(mrun - mx);
+                lrun *= alpha;
+                resc = true;
+            }
+            mrun = mx;
+        }
+        if (__any_sync(kFull, resc)) {  // O rows of this warp scaled in place (alpha = 1 for the others)
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(trow + 128u + c * 32, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                tmem_st32(trow + 128u + c * 32, r);
+            }
+            tmem_wait_st();
+        }
+        // weights, as two bf16 parts: hi = bf16(p), lo = bf16(p - hi), row t of the two P slabs
+        {
+            float ps = 0.f;
+            const uint32_t rowoff = uint32_t(t) * 128u;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // keys 8c .. 8c + 7: 16-byte chunk c of the row, swizzled
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float p0 = x[8 * c + 2 * k] == -INFINITY ? 0.f : ex2(x[8 * c + 2 * k] - mrun);
+                    const float p1 = x[8 * c + 2 * k + 1] == -INFINITY ? 0.f : ex2(x[8 * c + 2 * k + 1] - mrun);
+                    ps += p0 + p1;
+                    hi[k] = pack_bf16x2(p0, p1);
+                    lo[k] = pack_bf16x2(p0 - __uint_as_float(hi[k] << 16), p1 - __uint_as_float(hi[k] & 0xffff0000u));
+                }
+                const uint32_t a = m.p_addr + rowoff + ((uint32_t(c) ^ uint32_t(t & 7)) << 4);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
+                             "r"(hi[3]) : "memory");
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a + kTc5SlabBytes), "r"(lo[0]),
+                             "r"(lo[1]), "r"(lo[2]), "r"(lo[3]) : "memory");
+            }
+            lrun += ps;
+        }
+        fence_proxy_async_smem();  // P and the zeroed V rows, for the tensor core
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(m.pfull);
+
+        if (mt.flags & kLast) {  // the segment's part in this slice ends: O once its last product is done
+            if (!mbar_wait_bounded(m.odone, j & 1u)) {
+                if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const int kvh = mt.g;  // hg = 1
+            const int piece = mt.u - u_first + 1;
+            if (piece == mt.n) {  // the whole segment ran here: bf16 output
+                const float inv = lrun > 0.f ? 1.0f / lrun : 0.f;
+                uint16_t *orow = p.out + ((long long)(mt.b + qi) * p.Hq + (long long)kvh * p.gq + (t % p.gq)) * D;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(trow + 128u + c * 32, r);
+                    if (row_ok) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(r[8 * k]) * inv, __uint_as_float(r[8 * k + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv);
+                            *reinterpret_cast<uint4 *>(orow + c * 32 + 8 * k) = w;
+                        }
+                    }
+                }
+            } else {
+                // a piece: (m, l, acc) of every row into the piece slot of its block jq (see ws_layout); the
+                // CTA that completes a block's count merges the block's pieces
+                const long long x0 = (long long)p.nhg * scan[mt.b] + (long long)mt.g * mt.n;
+                const bool firstseg = u_first > 0 || x0 == bound[mt.slice];
+                const long long slot = (slots_by_slice(p.B, p.nhg) ? 2LL * mt.slice + (firstseg ? 0 : 1)
+                                                                   : mt.slice + (long long)mt.b * p.nhg + mt.g) *
+                                           p.sub + jq;
+                float *dst = p.ws_acc + (slot * G + hh) * D;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(trow + 128u + c * 32, r);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<float4 *>(dst + c * 32 + 4 * k) =
+                            make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                        __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+                }
+                reinterpret_cast<float2 *>(p.ws_ml)[slot * G + hh] = make_float2(mrun, lrun);
+                __threadfence();
+                __syncwarp();
+                // lanes 0-15 hold block 2 warp, lanes 16-31 block 2 warp + 1 (G = 16 rows a block)
+                const int nvh = max(0, min(p.qn, mt.cnt - jq * p.qn)) * p.gq;
+                int last = 0;
+                if ((lane & 15) == 0 && nvh > 0)
+                    last = arrive_last(p.ws_count + ((long long)mt.b * p.Hkv + kvh) * p.sub + jq, gen,
+                                       uint32_t(piece), uint32_t(mt.n), p.err);
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    const int bq = 2 * warp + half;
+                    if (__shfl_sync(kFull, last, 16 * half)) {
+                        __threadfence();
+                        const int nv = max(0, min(p.qn, mt.cnt - bq * p.qn)) * p.gq;
+                        merge_pieces<D, G, false, true>(p, bound, slice_of(bound, nslots, x0),
+                                                        slice_of(bound, nslots, x0 + mt.n - 1), x0, mt.g, 0, bq,
+                                                        mt.b, kvh, nv, lane);
+                    }
+                }
+            }
+            tc_fence_before();  // the reads of O come before the next segment's first product overwrites it
+        }
+        if ((mt.flags & kSliceEnd) && adaptive && t == 0) {
+            // balance record for the next call (as the regular consumers leave it)
+            const bool own = mt.slice == home;
+            const float us = float(global_ns() - *reinterpret_cast<const volatile unsigned long long *>(sh + 2)) * 1e-3f;
+            p.ws_bal->weight[wp][mt.slice] = own ? wts[mt.slice] : 0.f;
+            p.ws_bal->elapsed[wp][mt.slice] = own ? fmaxf(us, 1e-3f) : 0.f;
+            p.ws_bal->tag[wp][mt.slice] = gen ^ kTableMagic;
+        }
+        ++j;
+        if (++s == p.nst) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+    tc_fence_before();
+}
+
 // ------------------------------------------------------------------ main kernel
 // Block: p.cons consumer warps and one producer warp (warp p.cons).  Consumer
 // warp w takes kv head w / sub of the group and, per unit, either the TW-token
 // slice w % sub (QS false: a unit is TW * sub tokens) or all TW tokens for
 // its own qn queries w % sub of the entry's (QS true, hg = 1: the query-split
 // CTA for long runs of new tokens, where the entry's up to sub * qn queries
-// share every K/V tile).
-template <int D, int G, bool FP8, bool QS>
+// share every K/V tile).  TC5 (with QS): the same entries on the tensor-memory
+// consumers (see tc5_softmax_warps), the entry's Q tile loaded through qmap.
+template <int D, int G, bool FP8, bool QS, bool TC5 = false>
 __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                        const DecodeParams p)
+                        const __grid_constant__ CUtensorMap qmap, const DecodeParams p)
 {
+    static_assert(!TC5 || (QS && !FP8 && G == 16 && (D == 64 || D == 128)), "tensor-memory CTAs: bf16 query-split");
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int ES = FP8 ? 1 : 2;  // bytes per cached element
-    const CtaLayout lay = cta_layout(D, G, ES, p.hg, p.sub, p.nst, p.B, QS);
+    const CtaLayout lay = cta_layout(D, G, ES, p.hg, p.sub, p.nst, p.B, QS, TC5);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     uint8_t *stage0 = smem;
@@ -1043,24 +1382,38 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     long long *bound = reinterpret_cast<long long *>(smem + lay.off_bound);
     float *wts = reinterpret_cast<float *>(smem + lay.off_wts);
     float *red = reinterpret_cast<float *>(smem + lay.off_red);
-    int *sh = reinterpret_cast<int *>(smem + lay.off_sh);  // [0] own slice, [2..3] its start time
+    // [0] own slice, [2..3] its start time, [4] tensor-memory address (TC5)
+    int *sh = reinterpret_cast<int *>(smem + lay.off_sh);
     int32_t *scan = reinterpret_cast<int32_t *>(smem + lay.off_scan);
+    uint64_t *tc5_bar = cfree + 1;  // TC5: sfull[2], pfull, odone, drain
 
     if (threadIdx.x == 32 * p.cons) {  // none of this reads what the previous kernel writes
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
+        if constexpr (TC5) prefetch_tensormap(&qmap);
+        // TC5: a stage and a Q slot are released by one tcgen05.commit of the MMA warp
+        const uint32_t releases = TC5 ? 1u : uint32_t(p.cons);
         for (int i = 0; i < p.nst; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], uint32_t(p.cons));
+            mbar_init(&empty[i], releases);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&qfull[i], 1);
-            mbar_init(&qempty[i], uint32_t(p.cons));
+            mbar_init(&qempty[i], releases);
         }
         mbar_init(cfull, uint32_t(p.cons - p.hg));  // the non-leading warps' states
         mbar_init(cfree, uint32_t(p.hg));           // read again by the leaders
+        if constexpr (TC5) {
+            mbar_init(&tc5_bar[0], 1);                  // scores of an even unit computed
+            mbar_init(&tc5_bar[1], 1);                  // ... of an odd unit
+            mbar_init(&tc5_bar[2], kTc5SoftmaxWarps);   // weights written
+            mbar_init(&tc5_bar[3], 1);                  // output product done
+            mbar_init(&tc5_bar[4], 1);                  // every product done (before TMEM is freed)
+        }
         fence_barrier_init();
     }
+    if constexpr (TC5)
+        if (warp == kTc5SoftmaxWarps) tmem_alloc(reinterpret_cast<uint32_t *>(sh + 4), kTc5Cols);
     griddep_launch_dependents();  // lets the next kernel in the stream get scheduled; it waits for this grid
     griddep_wait();               // inputs may come from the previous kernel in the stream
 
@@ -1130,7 +1483,9 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
             }
         build_partition(p, gen, adaptive, nslots, T, bound, wts, red, bal_in, nset);
     }
+    if constexpr (TC5) tc_fence_before();
     __syncthreads();
+    if constexpr (TC5) tc_fence_after();
 
     if (warp == p.cons) {
         // ============================== producer warp ==============================
@@ -1200,7 +1555,13 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                         dead = true;
                         break;
                     }
-                    if (p.qn == 1 && !QS) {  // the group's G * hg query rows are contiguous
+                    if constexpr (TC5) {
+                        // the entry's 128 rows (queries x heads of kv head g) as one 128-byte-swizzled tile
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(&qfull[qs], lay.q_bytes);
+                            tma_load_4d(qbuf + qs * lay.q_bytes, &qmap, 0, iw.g * p.gq, iw.b, 0, &qfull[qs], policy);
+                        }
+                    } else if (p.qn == 1 && !QS) {  // the group's G * hg query rows are contiguous
                         const uint32_t qb = uint32_t(p.hg * G * D * 2);
                         if (lane == 0) {
                             mbar_arrive_expect_tx(&qfull[qs], qb);
@@ -1312,6 +1673,34 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     }
 
     // ============================== consumer warps ==============================
+    if constexpr (TC5) {
+        const uint32_t tmem = uint32_t(sh[4]);
+        Tc5Smem tm;
+        tm.metas = metas;
+        tm.full = full;
+        tm.empty = empty;
+        tm.qfull = qfull;
+        tm.qempty = qempty;
+        tm.sfull = tc5_bar;
+        tm.pfull = tc5_bar + 2;
+        tm.odone = tc5_bar + 3;
+        tm.drain = tc5_bar + 4;
+        tm.stage0 = stage0;
+        tm.pbuf = smem + lay.off_p;
+        tm.stage_addr = smem_u32(stage0);
+        tm.q_addr = smem_u32(qbuf);
+        tm.p_addr = smem_u32(smem + lay.off_p);
+        if (warp == kTc5SoftmaxWarps)
+            tc5_mma_warp<D>(p, lay, tm, tmem);
+        else
+            tc5_softmax_warps<D, G>(p, lay, tm, tmem, bound, scan, sh, wts, nslots, gen, wp, adaptive);
+        named_barrier(2, 32 * kTc5Consumers);  // every tensor-memory access of the CTA is done
+        if (warp == kTc5SoftmaxWarps) {
+            tc_fence_after();
+            tmem_dealloc(tmem, kTc5Cols);
+        }
+        return;
+    } else {
     using TC = Tc<D, FP8, QS, (G > 8 ? 2 : 1)>;
     const int h = warp / p.sub, j = warp - h * p.sub;  // kv head in the group, slice of the unit or queries
     const int jt = QS ? 0 : j;                         // token slice of the unit
@@ -1643,6 +2032,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
             p.ws_bal->tag[wp][mt.slice] = gen ^ kTableMagic;
         }
     }
+    }  // not TC5
 }
 
 // ------------------------------------------------------------------ host side
@@ -1721,11 +2111,66 @@ inline bool cached_cache_map(CUtensorMap *map, int dev, const void *base, bool f
     return true;
 }
 
+// Tensor map over the query rows q [rows, Hq, D] for the tensor-memory CTAs:
+// dims (64 elements, Hq heads, rows, D / 64 parts) with byte strides
+// (D * 2, Hq * D * 2, 128); a box of gq heads x nq rows x all parts lands as
+// [part][row][head][128 bytes], 128-byte swizzled: the 64-dim slabs of a
+// 128-row K-major operand whose row r is (query r / gq, head r % gq).  Rows
+// past the tensor's end read as zeros.
+inline bool encode_q_map(CUtensorMap *map, const void *q, int Hq, int64_t rows, int D, int gq, int nq)
+{
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) {
+        record_cuda_error("cuTensorMapEncodeTiled", "driver entry point unavailable");
+        return false;
+    }
+    const cuuint64_t dims[4] = {64u, cuuint64_t(Hq), cuuint64_t(rows), cuuint64_t(D / 64)};
+    const cuuint64_t strides[3] = {cuuint64_t(D) * 2, cuuint64_t(Hq) * D * 2, 128u};
+    const cuuint32_t box[4] = {64u, cuuint32_t(gq), cuuint32_t(nq), cuuint32_t(D / 64)};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[64];
+        std::snprintf(msg, sizeof msg, "CUresult %d (query map)", int(r));
+        record_cuda_error("cuTensorMapEncodeTiled", msg);
+        return false;
+    }
+    return true;
+}
+
+// The most recent query maps (a serving loop reuses its query buffers).
+inline bool cached_q_map(CUtensorMap *map, int dev, const void *q, int Hq, int64_t rows, int D, int gq, int nq)
+{
+    struct Entry {
+        int dev;
+        const void *q;
+        int Hq;
+        int64_t rows;
+        int D, gq, nq;
+        CUtensorMap map;
+    };
+    constexpr size_t kMaxEntries = 64;
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry &e : cache)
+        if (e.dev == dev && e.q == q && e.Hq == Hq && e.rows == rows && e.D == D && e.gq == gq && e.nq == nq) {
+            *map = e.map;
+            return true;
+        }
+    if (!encode_q_map(map, q, Hq, rows, D, gq, nq)) return false;
+    if (cache.size() >= kMaxEntries) cache.erase(cache.begin());
+    cache.push_back(Entry{dev, q, Hq, rows, D, gq, nq, *map});
+    return true;
+}
+
 // cudaFuncSetAttribute once per device and kernel variant (it is a host-side
 // driver call; repeating it on every launch costs microseconds).  Keyed on
-// <D, G, FP8>: every variant has the same function-pointer type, so the memo
-// must be per instantiation.
-template <int D, int G, bool FP8, bool QS, typename Kernel>
+// <D, G, FP8, QS, TC5>: every variant has the same function-pointer type, so
+// the memo must be per instantiation.
+template <int D, int G, bool FP8, bool QS, bool TC5, typename Kernel>
 inline bool ensure_smem_attribute(Kernel kern, int dev, size_t smem)
 {
     static std::mutex mu;
@@ -1743,15 +2188,15 @@ inline bool ensure_smem_attribute(Kernel kern, int dev, size_t smem)
     return true;
 }
 
-template <int D, int G, bool FP8, bool QS>
+template <int D, int G, bool FP8, bool QS, bool TC5 = false>
 pkv_status launch_decode(LaunchArgs &a)
 {
     DecodeParams &p = a.p;
     // ring depth: as many stages (up to kMaxStages) as the shared memory holds
     int nst = kMaxStages;
     constexpr int ES = FP8 ? 1 : 2;
-    while (nst > 2 && cta_layout(D, G, ES, p.hg, p.sub, nst, p.B, QS).total > uint32_t(a.max_smem)) --nst;
-    const CtaLayout lay = cta_layout(D, G, ES, p.hg, p.sub, nst, p.B, QS);
+    while (nst > 2 && cta_layout(D, G, ES, p.hg, p.sub, nst, p.B, QS, TC5).total > uint32_t(a.max_smem)) --nst;
+    const CtaLayout lay = cta_layout(D, G, ES, p.hg, p.sub, nst, p.B, QS, TC5);
     if (lay.total > uint32_t(a.max_smem)) return PKV_EUNSUPPORTED;
     p.nst = nst;
 
@@ -1766,15 +2211,21 @@ pkv_status launch_decode(LaunchArgs &a)
     }
     if (grid > kMaxSlots) grid = kMaxSlots;
 
-    CUtensorMap kmap, vmap;
+    CUtensorMap kmap, vmap, qmap;
     const int64_t rows = int64_t(p.NB) * p.bs;
     if (!cached_cache_map(&kmap, a.device, a.k_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok) ||
         !cached_cache_map(&vmap, a.device, a.v_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok))
         return PKV_ECUDA;
+    if constexpr (TC5) {
+        if (!cached_q_map(&qmap, a.device, p.q, p.Hq, p.B, D, p.gq, team_warps(G) * p.qn)) return PKV_ECUDA;
+    } else {
+        qmap = kmap;  // not read
+    }
 
-    auto kern = paged_decode_kernel<D, G, FP8, QS>;
-    if (!ensure_smem_attribute<D, G, FP8, QS>(kern, a.device, lay.total)) return PKV_ECUDA;
-    const cudaError_t e = launch_pdl(kern, dim3(grid), dim3((p.cons + 1) * 32), lay.total, a.stream, kmap, vmap, p);
+    auto kern = paged_decode_kernel<D, G, FP8, QS, TC5>;
+    if (!ensure_smem_attribute<D, G, FP8, QS, TC5>(kern, a.device, lay.total)) return PKV_ECUDA;
+    const cudaError_t e =
+        launch_pdl(kern, dim3(grid), dim3((p.cons + 1) * 32), lay.total, a.stream, kmap, vmap, qmap, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return cuda_fail("paged_decode_kernel launch", e);
@@ -1807,5 +2258,15 @@ LaunchFn pick_group(int G)
 LaunchFn pick_decode_fp8(int D, int G);
 LaunchFn pick_decode_qs(int D, int G);
 LaunchFn pick_decode_wide(int D, int G);  // regular bf16 CTAs, 9 to 16 virtual heads (pkv_decode_wide.cu)
+LaunchFn pick_decode_tc5(int D);          // tensor-memory query-split CTAs, 16 virtual heads (pkv_decode_tc5.cu)
+
+// Whether a query-split call can run on the tensor-memory CTAs: bf16 caches, entries of 128 rows
+// (16 virtual heads per block: the query heads of a kv head a power of two), 64-key tiles within one
+// block (block_size >= 64), and a ring of at least two stages in shared memory.
+inline bool tc5_eligible(int D, int G, int gq, int block_size, int B, int max_smem)
+{
+    if (G != 16 || (D != 64 && D != 128) || block_size < kTc5Keys || (gq & (gq - 1)) != 0) return false;
+    return cta_layout(D, G, 2, 1, team_warps(G), 2, B, true, true).total <= uint32_t(max_smem);
+}
 
 }  // namespace pkv

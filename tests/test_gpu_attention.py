@@ -211,3 +211,40 @@ def test_uniform_new_tokens_share_one_pass(n, Hq, Hkv, D, bs, workers):
         torch.cuda.synchronize()
         assert err.item() == 0
         check_close(out, want, f"n {n} call {call}")
+
+
+# --------------------------------------------------------------------------- tensor-memory query-split CTAs
+# Long runs of new tokens with gq = Hq / Hkv a power of two and block_size >= 64 run on the tcgen05 CTAs:
+# 128-row entries (128 / gq queries x gq heads) against 64-key tiles, scores and outputs in tensor memory.
+@pytest.mark.parametrize("Hq,Hkv,D,bs,workers", [
+    (16, 8, 128, 256, 0), (16, 8, 128, 64, 0), (8, 8, 128, 64, 0), (32, 8, 64, 128, 0), (64, 8, 128, 256, 0),
+    (16, 1, 64, 64, 0), (16, 8, 128, 256, 7), (16, 8, 128, 256, 333), (16, 8, 128, 64, 2000)])
+def test_tensor_memory_prefill_chunks(Hq, Hkv, D, bs, workers):
+    """Whole prefills, 64-query chunks and partial chunks after cached prefixes (up to 5000 keys: split over
+    several CTAs and merged), decodes; every query with its own causal bound; repeated calls on one
+    workspace."""
+    lens = [5000, 700, 129, 1, 333, 64, 1200, 2100]
+    news = [64, 250, 129, 1, 100, 33, 2, 190]
+    q, kc, vc, bt, cu, lens_t = mixed_batch(lens, news, Hq, Hkv, D, bs, seed=Hq * 13 + Hkv + D + bs + workers)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    want = oracle_of(q, kc, vc, bt, cu, lens_t, 0.0884)
+    ws = pkv.alloc_attention_workspace(q.shape[0], Hq, Hkv, D)
+    for call in range(3):
+        out = run(q, kc, vc, bt, cu, lens_t, 0.0884, workers=workers, ws=ws, err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        check_close(out, want, f"{Hq}/{Hkv} D{D} bs{bs} workers {workers} call {call}")
+
+
+def test_tensor_memory_prefill_chunk_of_the_qwen3_shape():
+    """The Qwen3-0.6B-shaped layer (16 q / 8 kv heads, head_dim 128, block_size 256): the last 64 tokens of
+    each sequence as one prefill chunk over its cached prefix, context lengths U[512, 4096]."""
+    rng = np.random.default_rng(64)
+    lens = [int(x) for x in rng.integers(512, 4097, 12)]
+    news = [64] * len(lens)
+    q, kc, vc, bt, cu, lens_t = mixed_batch(lens, news, 16, 8, 128, 256, seed=65)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run(q, kc, vc, bt, cu, lens_t, 0.0884, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    check_close(out, oracle_of(q, kc, vc, bt, cu, lens_t, 0.0884), "64-token chunks")
