@@ -85,23 +85,32 @@ constexpr int kHintUnits = 16;
 // registers do not grow with the group size (G query heads are rows of one
 // MMA tile), so every group size runs 8 consumers.
 __host__ __device__ constexpr int team_warps(int) { return 8; }
+// Tensor-memory (tcgen05) query-split CTAs: 8 warps that own the 128 rows of
+// the tile, two per row (the softmax and the epilogue: warp w takes rows
+// 32 (w % 4) .. + 31 and keys 64 (w / 4) .. + 63 of every tile), one warp that
+// issues the tensor-core products, then the producer warp.
+constexpr int kTc5SoftmaxWarps = 8;
+constexpr int kTc5Consumers = kTc5SoftmaxWarps + 1;
+constexpr int kTc5Keys = 128;          // keys per tile (one unit): the N extent of one score product
+// TMEM columns (512): the score buffer (128 columns), the outputs of the two key halves (D <= 128 columns
+// each, from columns 128 and 384), and two weight buffers of 64 columns from column 256 (bf16 pairs of
+// keys 2c, 2c + 1 in column c; half h in columns 32 h .. 32 h + 31).
+constexpr uint32_t kTc5Cols = 512, kTc5PCol = 256;
+__host__ __device__ constexpr uint32_t tc5_ocol(int half) { return half ? 384u : 128u; }
+constexpr uint32_t kTc5SlabBytes = 128u * 128u;  // one 64-dim slab of 128 rows: the Q tile, or a stage's K or V
+// The K tiles stream through a ring of nst slots (a slot is free again once its scores are read); the V
+// tiles through a ring of kTc5VSlots (free again once their output product is done); one Q slot.
+constexpr int kTc5VSlots = 2;
+static_assert(kTc5Keys * 128 == int(kTc5SlabBytes), "a stage's K or V slab holds one tile of 128-byte rows");
+
 // Query-split CTAs (qs; long runs of new tokens, see paged_decode_kernel)
 // take 32-token tiles too: one kv head's stage is small, and every warp
-// works on every token.  Their tensor-memory variant (tc5) takes 64 keys a
-// tile: the N extent of one score product.
+// works on every token.  Their tensor-memory variant (tc5) takes kTc5Keys keys
+// a tile: the N extent of one score product.
 __host__ __device__ constexpr int warp_tokens(int, bool fp8, bool qs = false, bool tc5 = false)
 {
-    return tc5 ? 64 : (fp8 || qs ? 32 : 16);
+    return tc5 ? kTc5Keys : (fp8 || qs ? 32 : 16);
 }
-
-// Tensor-memory (tcgen05) query-split CTAs: 4 warps that own the 128 rows of
-// the tile (the softmax and the epilogue), one warp that issues the tensor-core
-// products, then the producer warp.
-constexpr int kTc5SoftmaxWarps = 4;
-constexpr int kTc5Consumers = kTc5SoftmaxWarps + 1;
-constexpr int kTc5Keys = 64;           // keys per tile (one unit)
-constexpr uint32_t kTc5Cols = 256;     // TMEM columns: two 64-column score buffers, then the output (<= 128)
-constexpr uint32_t kTc5SlabBytes = 128u * 128u;  // one 64-dim slab of the 128-row Q tile, or of P
 
 // ------------------------------------------------------------------ load balance state
 // In the adaptive mode a slice's size follows what the previous call on this
@@ -176,8 +185,8 @@ constexpr int kSliceEnd = 4;  // last unit of the slice
 
 // Shared-memory layout, computed the same way on the host (size) and device (offsets).
 struct CtaLayout {
-    uint32_t kv_bytes, stage_bytes, q_bytes, comb_bytes, p_bytes;
-    uint32_t off_q, off_p, off_comb, off_meta, off_bar, off_bound, off_wts, off_red, off_sh, off_scan, total;
+    uint32_t kv_bytes, stage_bytes, q_bytes, comb_bytes;
+    uint32_t off_v, off_q, off_comb, off_meta, off_bar, off_bound, off_wts, off_red, off_sh, off_scan, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -188,32 +197,35 @@ __host__ __device__ inline int comb_stride(int D, int G) { return int(align_up(u
 
 // es: bytes per cached element (2 for bf16, 1 for E4M3); qs: query-split
 // CTA (all sub warps of a kv head on the same tokens, each with its own G
-// virtual heads); tc5: its tensor-memory variant (the Q tile and the weights
-// P as 128-byte-swizzled 128-row operands of 64-dim slabs, P in two parts).
+// virtual heads); tc5: its tensor-memory variant (Q slots hold the 128-row
+// tile as 128-byte-swizzled 64-dim slabs).
 __host__ __device__ inline CtaLayout cta_layout(int D, int G, int es, int hg, int sub, int nst, int B,
                                                 bool qs = false, bool tc5 = false)
 {
     CtaLayout l;
     const int toks = warp_tokens(G, es == 1, qs, tc5) * (qs ? 1 : sub);
     l.kv_bytes = uint32_t(toks * hg * D * es);
-    l.stage_bytes = align_up(2 * l.kv_bytes, 1024);  // stages start on the 1024-byte swizzle period
+    // stages start on the 1024-byte swizzle period; tc5: a stage is a K slot, the V slots follow the ring
+    l.stage_bytes = align_up((tc5 ? 1 : 2) * l.kv_bytes, 1024);
     l.q_bytes = tc5 ? uint32_t(D / 64) * kTc5SlabBytes : align_up(uint32_t(hg * (qs ? sub : 1) * G * D * 2), 128);
-    l.p_bytes = tc5 ? 2 * kTc5SlabBytes : 0u;
-    // states of the non-leading warps of every head (the leader keeps its own in registers)
-    l.comb_bytes = sub > 1 && !qs ? align_up(uint32_t(hg * (sub - 1) * comb_stride(D, G) * 4), 128) : 0u;
+    // states of the non-leading warps of every head (the leader keeps its own in registers); tc5: the
+    // values each row's two key halves exchange ([2 tile parities][2 halves][128 rows] floats)
+    l.comb_bytes = tc5 ? 2u * 2u * 128u * 4u
+                       : (sub > 1 && !qs ? align_up(uint32_t(hg * (sub - 1) * comb_stride(D, G) * 4), 128) : 0u);
     uint32_t o = uint32_t(nst) * l.stage_bytes;
+    l.off_v = o;
+    if (tc5) o += uint32_t(kTc5VSlots) * align_up(l.kv_bytes, 1024);
     l.off_q = o;
-    o += 2 * l.q_bytes;
-    l.off_p = o;
-    o += l.p_bytes;
+    o += (tc5 ? 1 : 2) * l.q_bytes;
     l.off_comb = o;
     o += l.comb_bytes;
     l.off_meta = o;
     o += uint32_t(nst) * uint32_t(sizeof(UnitMeta));
     l.off_bar = o;
-    // full / empty per stage, q full / empty x2, combine full / free; tc5: scores full x2, weights
-    // full, output product done, drain
-    o += uint32_t(2 * nst + 6 + (tc5 ? 5 : 0)) * 8;
+    // full / empty per stage, q full / empty x2, combine full / free; tc5: scores full, scores read,
+    // weights full x2, output product done x2, drain, a row's two halves met (one per lane quarter) x4,
+    // all softmax warps met, and full / empty per V slot (the stages' pair then covers the K slots)
+    o += uint32_t(2 * nst + 6 + (tc5 ? 12 + 2 * kTc5VSlots : 0)) * 8;
     l.off_bound = align_up(o, 16);
     o = l.off_bound + (kMaxSlots + 1) * 8;
     l.off_wts = o;
@@ -1035,138 +1047,240 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
 // ------------------------------------------------------------------ tensor-memory query-split CTA (tc5)
 // A query-split entry of 128 rows -- 128 / gq queries x gq query heads of one kv head, row r = query
 // r / gq, head r % gq, in blocks of G = 16 rows that play the part of the query-split CTA's warps (jq) --
-// against 64-key tiles of that kv head, on the 5th-generation tensor cores:
-//   S = Q K^T      128 x 64 fp32 in tensor memory (two buffers), Q and K 128-byte-swizzled K-major in
-//                  shared memory (the Q tile loaded by one TMA copy per entry, K by the stage's copy);
-//   P = 2^(S - m)  by 4 warps, thread r owning row r (its TMEM lane): masks, running max m and sum l,
-//                  P written to shared memory as two bf16 parts (hi, lo = P - hi);
-//   O += P V       128 x D fp32 in tensor memory, V the stage's rows as an MN-major operand; O is
-//                  rescaled in place (read, scaled, written back by its row's thread) only when a row's
-//                  max passes m by the slack, which after a segment's first tiles is rare.
-// One thread of the MMA warp issues the products in the order S(0), S(1), P(0)V, S(2), P(1)V, ..., so
-// the scores of the next tile are computed while the softmax warps work on the current one.  Ordering:
-// scores -> sfull[j % 2] (tcgen05.commit), weights written -> pfull (4 warps), output product done ->
-// odone and the stage's empty barrier (commits), a segment's last scores -> its Q slot's qempty.  The
-// softmax warps write P(j) only after the product of unit j - 1 is done, so one P buffer serves.
+// against 128-key tiles of that kv head, on the 5th-generation tensor cores:
+//   S = Q K^T      128 x 128 fp32 in tensor memory, Q and K 128-byte-swizzled K-major in shared memory
+//                  (the Q tile loaded by one TMA copy per entry, K by the stage's copy);
+//   P = 2^(S - m)  by 8 warps, two threads per row (TMEM lane r; each takes 64 of the keys): masks, the
+//                  row's running max m (the two halves exchange their tile max) and sum l (fp32 weights),
+//                  P written back to tensor memory (two buffers) rounded to bf16, the product's operand
+//                  type (as flash-attention kernels do: a second product for the rounding error, as the
+//                  decode path carries, would double the output product, which bounds this path);
+//   O += P V       128 x D fp32 in tensor memory, P the A operand from tensor memory, V the stage's rows as
+//                  an MN-major operand from shared memory; O is rescaled in place (read, scaled, written
+//                  back) only when a row's max passes m by the slack, which after a segment's first tiles
+//                  is rare.
+// One thread of the MMA warp issues the products in the order S(0), S(1), P(0)V, S(2), P(1)V, ...: S(j + 1)
+// as soon as the softmax warps have read S(j) into registers, so the tensor core computes the next scores
+// and the current output product while they work on a tile.  Ordering: scores -> sfull (tcgen05.commit);
+// scores read -> sfree (8 warps); weights written -> pfull[j % 2] (8 warps); output product done ->
+// odone[j % 2] and the stage's empty barrier (commits); a segment's last scores -> its Q slot's qempty.
+// No barrier can run two phases ahead of its waiter: each one's next phase needs the waiter's own next step.
 struct Tc5Smem {
     const UnitMeta *metas;
-    uint64_t *full, *empty, *qfull, *qempty, *sfull, *pfull, *odone, *drain;
-    uint8_t *stage0, *pbuf;
-    uint32_t stage_addr, q_addr, p_addr;  // shared addresses of stage 0, Q slot 0, P (hi; lo follows)
+    // full / empty: a stage's K half (and its unit's meta); vfull / vempty: its V half
+    uint64_t *full, *empty, *vfull, *vempty, *qfull, *qempty, *sfull, *sfree, *pfull, *odone, *drain, *pair, *team;
+    uint8_t *stage0, *vbase;                // K slot 0, V slot 0
+    uint32_t stage_addr, v_addr, q_addr;   // their shared addresses, and the Q slot's
 };
 
+// O_h += P_h(u) V_h(u) for the two key halves h: the weights of unit u (buffer u % 2) times the V rows of
+// those keys in its ring slot.
 template <int D>
-__device__ __forceinline__ void tc5_output_product(const DecodeParams &p, const CtaLayout &lay, const Tc5Smem &m,
-                                                   uint32_t tmem, int slot, bool first, int lane)
+__device__ __forceinline__ void tc5_output_product(const CtaLayout &lay, const Tc5Smem &m, uint32_t tmem,
+                                                   uint32_t u, bool first, int lane)
 {
     constexpr uint32_t IP = idesc_bf16_f32(128, D, true);
     if (lane == 0) {
         tc_fence_after();
-        const uint32_t va = m.stage_addr + uint32_t(slot) * lay.stage_bytes + lay.kv_bytes;
-        // V: keys along K (8-key groups 1024 bytes apart), dims along N (64-dim blocks 64 * 128 bytes apart)
+        const uint32_t va = m.v_addr + (u % kTc5VSlots) * align_up(lay.kv_bytes, 1024);
+        const uint32_t pa = tmem + kTc5PCol + (u & 1u) * 64u;
+        // V: keys along K (8-key groups 1024 bytes apart: 16 keys = 2048 bytes), dims along N (64-dim
+        // blocks one slab apart)
 #pragma unroll
-        for (int part = 0; part < 2; ++part)
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int ks = 0; ks < kTc5Keys / 16; ++ks)
-                tc_mma_bf16(tmem + 128u, smem_desc_sw128(m.p_addr + uint32_t(part) * kTc5SlabBytes + ks * 32, 16, 1024),
-                            smem_desc_sw128(va + ks * 2048, kTc5Keys * 128, 1024), IP, !(first && part == 0 && ks == 0));
-        tc_commit(m.odone);
-        tc_commit(&m.empty[slot]);
+            for (int ks = 0; ks < kTc5Keys / 32; ++ks)
+                tc_mma_bf16_ta(tmem + tc5_ocol(h), pa + uint32_t(32 * h + 8 * ks),
+                               smem_desc_sw128(va + uint32_t(4 * h + ks) * 2048u, kTc5SlabBytes, 1024), IP,
+                               !(first && ks == 0));
+        tc_commit(&m.odone[u & 1u]);
+        tc_commit(&m.vempty[u % kTc5VSlots]);  // the V slot may take the next copy
     }
-    __syncwarp();
 }
 
-// The MMA warp: waits on the ring like the consumers, issues every tensor-core product of the CTA from
-// lane 0, and before it returns waits for all of them to complete (also when a wait gave up).
+// The MMA warp: lane 0 issues every tensor-core product of the CTA, each as soon as its inputs are
+// ready -- S(k) once unit k's K half has landed (and its Q tile, and S(k - 1) was read), P(k)V once the
+// weights of unit k are written and its V half has landed -- polling both without blocking on either,
+// so a late copy never holds back an output product whose weights are ready.  A stage's K half (and its
+// unit's meta) is released when the softmax warps have read that unit's scores, its V half when the
+// unit's output product is done.  Before it returns it waits for all products to complete (also when
+// it gave up: no progress for the wait limit).
 template <int D>
 __device__ void tc5_mma_warp(const DecodeParams &p, const CtaLayout &lay, const Tc5Smem &m, uint32_t tmem)
 {
     constexpr uint32_t IS = idesc_bf16_f32(128, kTc5Keys, false);
     const int lane = threadIdx.x & 31;
-    int s = 0;
-    uint32_t ph = 0, j = 0, segs = 0;
-    int cur = -1;  // ring slot of unit j - 1, whose output product is pending
-    bool cur_first = false;
     bool dead = false;
-    int qs = 0;
-    for (;;) {
-        if (!mbar_wait_bounded(&m.full[s], ph)) {
-            dead = true;
-            break;
-        }
-        const int b = m.metas[s].b, flags = m.metas[s].flags;
-        if (b < 0) break;
-        if (flags & kFirst) {
-            qs = int(segs & 1u);
-            if (!mbar_wait_bounded(&m.qfull[qs], (segs >> 1) & 1u)) {
-                dead = true;
-                break;
-            }
-            ++segs;
-        }
-        if (lane == 0) {  // S(j) = Q K^T into score buffer j % 2 (its previous scores were read: P(j - 2) came)
-            tc_fence_after();
-            const uint32_t qa = m.q_addr + uint32_t(qs) * lay.q_bytes;
-            const uint32_t ka = m.stage_addr + uint32_t(s) * lay.stage_bytes;
+    if (lane == 0) {
+        int s = 0;                       // ring slot of unit ns
+        uint32_t ph = 0;                 // its parity
+        uint32_t ns = 0, npv = 0;        // next unit to score, next unit to multiply by V
+        uint32_t segs = 0;
+        bool have_meta = false, ended = false;
+        int flags = 0;
+        int slot_of[2] = {0, 0};         // K slots of units npv, npv + 1 (at most two scored, not multiplied)
+        bool first_of[2] = {false, false};
+        uint64_t t0 = global_ns();
+        for (uint32_t it = 0;; ++it) {
+            bool progress = false;
+            // the next scores: unit ns's stage (and meta), its Q tile on a segment's first unit, and the
+            // score buffer free (S(ns - 1) read); at most two units ahead of the output products
+            if (!ended && ns < npv + 2) {
+                if (!have_meta && mbar_try_wait(smem_u32(&m.full[s]), ph)) {
+                    have_meta = true;
+                    flags = m.metas[s].flags;
+                    if (m.metas[s].b < 0) ended = true;
+                }
+                if (have_meta && !ended) {
+                    const bool qready = !(flags & kFirst) || mbar_try_wait(smem_u32(&m.qfull[0]), segs & 1u);
+                    const bool sready = ns == 0 || mbar_try_wait(smem_u32(m.sfree), (ns - 1) & 1u);
+                    if (qready && sready) {
+                        // S(ns - 1) was read, and with it the meta of unit ns - 1: its stage's K half is free
+                        if (ns > 0) mbar_arrive(&m.empty[slot_of[(ns - 1) & 1u]]);
+                        if (flags & kFirst) ++segs;
+                        tc_fence_after();
+                        const uint32_t qa = m.q_addr;
+                        const uint32_t ka = m.stage_addr + uint32_t(s) * lay.stage_bytes;
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t within = uint32_t(ks & 3) * 32, slab = uint32_t(ks >> 2);
-                tc_mma_bf16(tmem + (j & 1u) * kTc5Keys, smem_desc_sw128(qa + slab * kTc5SlabBytes + within, 16, 1024),
-                            smem_desc_sw128(ka + slab * (kTc5Keys * 128) + within, 16, 1024), IS, ks > 0);
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint32_t within = uint32_t(ks & 3) * 32, slab = uint32_t(ks >> 2);
+                            tc_mma_bf16(tmem, smem_desc_sw128(qa + slab * kTc5SlabBytes + within, 16, 1024),
+                                        smem_desc_sw128(ka + slab * kTc5SlabBytes + within, 16, 1024), IS, ks > 0);
+                        }
+                        tc_commit(m.sfull);
+                        if (flags & kLast) tc_commit(&m.qempty[0]);  // the segment's Q tile is read for the last time
+                        slot_of[ns & 1u] = s;
+                        first_of[ns & 1u] = (flags & kFirst) != 0;
+                        ++ns;
+                        have_meta = false;
+                        if (++s == p.nst) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                        progress = true;
+                    }
+                }
             }
-            tc_commit(&m.sfull[j & 1u]);
-            if (flags & kLast) tc_commit(&m.qempty[qs]);  // the segment's Q tile is read for the last time
-        }
-        __syncwarp();
-        if (cur >= 0) {  // O += P(j - 1) V(j - 1) once its weights are written
-            if (!mbar_wait_bounded(m.pfull, (j - 1) & 1u)) {
+            // the next output product, once its weights are written and its V tile has landed
+            if (npv < ns && mbar_try_wait(smem_u32(&m.pfull[npv & 1u]), (npv >> 1) & 1u) &&
+                mbar_try_wait(smem_u32(&m.vfull[npv % kTc5VSlots]), (npv / kTc5VSlots) & 1u)) {
+                tc5_output_product<D>(lay, m, tmem, npv, first_of[npv & 1u], 0);
+                ++npv;
+                progress = true;
+            }
+            if (ended && npv == ns) break;
+            if (progress) {
+                t0 = global_ns();
+            } else if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
                 dead = true;
                 break;
             }
-            tc5_output_product<D>(p, lay, m, tmem, cur, cur_first, lane);
         }
-        cur = s;
-        cur_first = (flags & kFirst) != 0;
-        ++j;
-        if (++s == p.nst) {
-            s = 0;
-            ph ^= 1u;
-        }
+        if (dead) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
+        // every product issued has completed before the tensor memory is freed
+        tc_commit(m.drain);
     }
-    if (!dead && cur >= 0) {
-        if (mbar_wait_bounded(m.pfull, (j - 1) & 1u))
-            tc5_output_product<D>(p, lay, m, tmem, cur, cur_first, lane);
-        else
-            dead = true;
-    }
-    if (dead && lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
-    // every product issued has completed before the tensor memory is freed
-    if (lane == 0) tc_commit(m.drain);
     __syncwarp();
     if (!mbar_wait_bounded(m.drain, 0u) && lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
 }
 
-// The softmax warps (threads 0..127, thread r = row r = TMEM lane r).
+// The pieces of one (entry, kv head) segment, merged by the CTA whose piece completed its unit count:
+// thread (row, half) folds columns [half D / 2, (half + 1) D / 2) of the row over the pieces left by the
+// non-empty slices sf..sl (slot numbering as in ws_layout: jq = row / G, hh = row % G), all of a piece's
+// loads in flight at once, then writes the row's bf16 output if the row is one of the entry's queries:
+//   M = max m_i,  l = sum 2^(m_i - M) l_i,  out = sum 2^(m_i - M) acc_i / l.
+template <int D, int G>
+__device__ void tc5_merge(const DecodeParams &p, const long long *bound, int sf, int sl, long long x0, int g,
+                          int b, int row, int half, bool row_ok, int qi)
+{
+    constexpr int C = D / 2;  // columns of this thread
+    const int jq = row / G, hh = row - jq * G;
+    const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);
+    float M = -INFINITY, lsum = 0.f, a[C];
+#pragma unroll
+    for (int e = 0; e < C; ++e) a[e] = 0.f;
+    for (int sk = sf; sk <= sl; ++sk) {
+        if (bound[sk + 1] <= bound[sk]) continue;  // an empty slice left nothing
+        const long long slot = (slots_by_slice(p.B, p.nhg) ? 2LL * sk + ((sk == sf && x0 != bound[sf]) ? 1 : 0)
+                                                           : sk + (long long)b * p.nhg + g) *
+                                   p.sub + jq;
+        const float2 st = __ldcg(ml + slot * G + hh);
+        const float4 *src = reinterpret_cast<const float4 *>(p.ws_acc + (slot * G + hh) * D + half * C);
+        float4 v[C / 4];
+#pragma unroll
+        for (int k = 0; k < C / 4; ++k) v[k] = __ldcg(src + k);
+        if (st.x == -INFINITY) continue;  // a piece in which the row saw no key
+        const float mb = fmaxf(M, st.x);
+        const float r = M == -INFINITY ? 0.f : ex2(M - mb), f = ex2(st.x - mb);
+        lsum = fmaf(f, st.y, lsum * r);
+#pragma unroll
+        for (int k = 0; k < C / 4; ++k) {
+            a[4 * k] = fmaf(f, v[k].x, a[4 * k] * r);
+            a[4 * k + 1] = fmaf(f, v[k].y, a[4 * k + 1] * r);
+            a[4 * k + 2] = fmaf(f, v[k].z, a[4 * k + 2] * r);
+            a[4 * k + 3] = fmaf(f, v[k].w, a[4 * k + 3] * r);
+        }
+        M = mb;
+    }
+    if (!row_ok) return;
+    const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+    uint16_t *o = p.out + ((long long)(b + qi) * p.Hq + (long long)g * p.gq + (row % p.gq)) * D + half * C;
+#pragma unroll
+    for (int k = 0; k < C / 8; ++k)
+        *reinterpret_cast<uint4 *>(o + 8 * k) =
+            make_uint4(pack_bf16x2(a[8 * k] * inv, a[8 * k + 1] * inv), pack_bf16x2(a[8 * k + 2] * inv, a[8 * k + 3] * inv),
+                       pack_bf16x2(a[8 * k + 4] * inv, a[8 * k + 5] * inv), pack_bf16x2(a[8 * k + 6] * inv, a[8 * k + 7] * inv));
+}
+
+// The softmax warps: thread t of the 256 takes row r = 32 (w % 4) + lane (TMEM lane r; w = t / 32) and
+// keys 64 h .. 64 h + 63 of every tile, h = w / 4, with its own running max and sum and its own output
+// O_h: the two threads of a row (warps w and w + 4) combine their states when a segment's part in the
+// slice ends.
 template <int D, int G>
 __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, const Tc5Smem &m, uint32_t tmem,
-                                  const long long *bound, const int32_t *scan, const int *sh, const float *wts,
-                                  int nslots, uint32_t gen, int wp, bool adaptive)
+                                  float *xch, const long long *bound, const int32_t *scan, int *sh,
+                                  const float *wts, int nslots, uint32_t gen, int wp, bool adaptive)
 {
+    constexpr int KH = kTc5Keys / 2;  // keys of a half
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);  // this warp's lane quarter
-    const int qi = t / p.gq;                                    // query of the row within its entry
-    const int jq = t / G, hh = t - jq * G;                      // block of G rows and the row in it
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = 32 * quarter + lane;
+    const uint32_t tlane = tmem + (uint32_t(32 * quarter) << 16);  // this warp's lane quarter
+    const int qi = row / p.gq;                                      // query of the row within its entry
+    const int jq = row / G, hh = row - jq * G;                      // block of G rows and the row in it
     const int home = sh[0];
+    const float c = p.scale_log2;
     int s = 0;
     uint32_t ph = 0, j = 0;
     float mrun = -INFINITY, lrun = 0.f;
     bool row_ok = false;
     int shift = 0, u_first = 0;
+    uint32_t meets = 0;  // exchanges with the row's other half so far (the same in both warps)
+    // a wait that may give up: the kernel's error word, and out of the loop
+    auto wait = [&](uint64_t *bar, uint32_t parity) {
+        if (mbar_wait_bounded(bar, parity)) return true;
+        if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
+        return false;
+    };
+    uint32_t teams = 0;  // meetings of all softmax warps so far (the same in every one)
+    auto meet_all = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(m.team);
+        return wait(m.team, teams++ & 1u);
+    };
+    // give v to the row's other half and take its value (slots alternate by exchange, so a warp one
+    // exchange ahead does not overwrite a value its partner has yet to read); false if the wait gave up
+    auto exchange = [&](float v, float &other) {
+        float *slot = xch + (meets & 1u) * 256u;
+        slot[half * 128 + row] = v;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m.pair[quarter]);
+        if (!wait(&m.pair[quarter], meets++ & 1u)) return false;
+        other = slot[(1 - half) * 128 + row];
+        return true;
+    };
     for (;;) {
-        if (!mbar_wait_bounded(&m.full[s], ph)) {
-            if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
-            break;
-        }
+        if (!wait(&m.full[s], ph)) break;
         const UnitMeta mt = m.metas[s];
         if (mt.b < 0) break;
         const bool first = (mt.flags & kFirst) != 0;
@@ -1179,42 +1293,43 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
         }
         const int tok0 = mt.u * kTc5Keys;
         const int valid = min(kTc5Keys, mt.L - tok0);
-        const int lim = row_ok ? min(valid, mt.L - tok0 - shift) : 0;
+        const int lim = row_ok ? min(valid, mt.L - tok0 - shift) - KH * half : 0;  // keys of this half
         if (valid < kTc5Keys) {
-            // V rows past the sequence's end hold anything (NaN included) and 0 * NaN is NaN: zero them
-            uint8_t *vrows = m.stage0 + size_t(s) * lay.stage_bytes + lay.kv_bytes;
+            // V rows past the sequence's end hold anything (NaN included) and 0 * NaN is NaN: zero them,
+            // once the V copy has landed
+            if (!wait(&m.vfull[j % kTc5VSlots], (j / kTc5VSlots) & 1u)) break;
+            uint8_t *vrows = m.vbase + size_t(j % kTc5VSlots) * align_up(lay.kv_bytes, 1024);
             const int per_part = (kTc5Keys - valid) * 8, n = per_part * (D / 64);
             for (int i = t; i < n; i += 32 * kTc5SoftmaxWarps) {
                 const int part = i / per_part, r = i - part * per_part;
-                *reinterpret_cast<uint4 *>(vrows + part * (kTc5Keys * 128) + valid * 128 + r * 16) =
+                *reinterpret_cast<uint4 *>(vrows + part * kTc5SlabBytes + valid * 128 + r * 16) =
                     make_uint4(0u, 0u, 0u, 0u);
             }
+            fence_proxy_async_smem();  // for the tensor core
         }
-        if (!mbar_wait_bounded(&m.sfull[j & 1u], (j >> 1) & 1u)) {
-            if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
-            break;
-        }
+        if (!wait(m.sfull, j & 1u)) break;
         tc_fence_after();
-        float x[kTc5Keys];
-        {
+        // raw scores s of the half's keys (at or past the row's bound: -inf); weights 2^(s c - m)
+        float x[KH];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
             uint32_t r[32];
+            tmem_ld32(tlane + uint32_t(KH * half + 32 * h2), r);
+            if (lim >= 32 * (h2 + 1)) {
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                tmem_ld32(trow + (j & 1u) * kTc5Keys + h2 * 32, r);
+                for (int i = 0; i < 32; ++i) x[32 * h2 + i] = __uint_as_float(r[i]);
+            } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    x[h2 * 32 + i] = h2 * 32 + i < lim ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+                for (int i = 0; i < 32; ++i) x[32 * h2 + i] = 32 * h2 + i < lim ? __uint_as_float(r[i]) : -INFINITY;
             }
         }
-        float mx = x[0];
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(m.sfree);  // the score buffer may take the next tile's scores
+        float mx4[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-        for (int i = 1; i < kTc5Keys; ++i) mx = fmaxf(mx, x[i]);
-        // the previous output product is done: P's buffer is free and O may be read
-        if (j > 0 && !mbar_wait_bounded(m.odone, (j - 1) & 1u)) {
-            if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
-            break;
-        }
-        tc_fence_after();
+        for (int i = 4; i < KH; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], x[i]);
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;  // c > 0
         float alpha = 1.0f;
         bool resc = false;
         if (mx > mrun + kRescaleSlack) {  // also the row's first tile with a key (mrun = -inf)
@@ -1225,70 +1340,76 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
             }
             mrun = mx;
         }
-        if (__any_sync(kFull, resc)) {  // O rows of this warp scaled in place (alpha = 1 for the others)
+        // this warp's rows of O_half scaled in place (alpha = 1 for rows that keep their max), once
+        // P(j - 1) V is in
+        if (__any_sync(kFull, resc)) {
+            if (!wait(&m.odone[(j - 1) & 1u], ((j - 1) >> 1) & 1u)) break;
+            tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t r[32];
-                tmem_ld32(trow + 128u + c * 32, r);
+                tmem_ld32(tlane + tc5_ocol(half) + cc * 32, r);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                tmem_st32(trow + 128u + c * 32, r);
+                tmem_st32(tlane + tc5_ocol(half) + cc * 32, r);
             }
-            tmem_wait_st();
         }
-        // weights, as two bf16 parts: hi = bf16(p), lo = bf16(p - hi), row t of the two P slabs
+        // P(j)'s buffer was last read by the product of unit j - 2
+        if (j >= 2 && !wait(&m.odone[j & 1u], ((j >> 1) - 1) & 1u)) break;
+        tc_fence_after();
+        // weights rounded to bf16 (the output product's operand), into this half's 32 columns of buffer
+        // j % 2; the row sum adds the fp32 weights (2^-inf = 0 for the masked keys; a row without any key
+        // so far takes m = 0 and gets zeros)
         {
-            float ps = 0.f;
-            const uint32_t rowoff = uint32_t(t) * 128u;
+            const float mneg = mrun == -INFINITY ? 0.f : -mrun;
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t w[32];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {  // keys 8c .. 8c + 7: 16-byte chunk c of the row, swizzled
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float p0 = x[8 * c + 2 * k] == -INFINITY ? 0.f : ex2(x[8 * c + 2 * k] - mrun);
-                    const float p1 = x[8 * c + 2 * k + 1] == -INFINITY ? 0.f : ex2(x[8 * c + 2 * k + 1] - mrun);
-                    ps += p0 + p1;
-                    hi[k] = pack_bf16x2(p0, p1);
-                    lo[k] = pack_bf16x2(p0 - __uint_as_float(hi[k] << 16), p1 - __uint_as_float(hi[k] & 0xffff0000u));
-                }
-                const uint32_t a = m.p_addr + rowoff + ((uint32_t(c) ^ uint32_t(t & 7)) << 4);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
-                             "r"(hi[3]) : "memory");
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a + kTc5SlabBytes), "r"(lo[0]),
-                             "r"(lo[1]), "r"(lo[2]), "r"(lo[3]) : "memory");
+            for (int k = 0; k < KH / 2; ++k) {
+                const float p0 = ex2(fmaf(x[2 * k], c, mneg)), p1 = ex2(fmaf(x[2 * k + 1], c, mneg));
+                ps[k & 3] += p0 + p1;
+                w[k] = pack_bf16x2(p0, p1);
             }
-            lrun += ps;
+            lrun += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+            tmem_st32(tlane + kTc5PCol + (j & 1u) * 64u + 32u * half, w);
         }
-        fence_proxy_async_smem();  // P and the zeroed V rows, for the tensor core
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(m.pfull);
+        if (lane == 0) mbar_arrive(&m.pfull[j & 1u]);
 
         if (mt.flags & kLast) {  // the segment's part in this slice ends: O once its last product is done
-            if (!mbar_wait_bounded(m.odone, j & 1u)) {
-                if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
-                break;
-            }
+            if (!wait(&m.odone[j & 1u], (j >> 1) & 1u)) break;
             tc_fence_after();
-            const int kvh = mt.g;  // hg = 1
+            // the row's two halves: M = max, weights fa, fb of O_0, O_1 (0 for a half without keys)
+            float mo, lo;
+            if (!exchange(mrun, mo) || !exchange(lrun, lo)) break;
+            const float m0 = half ? mo : mrun, m1 = half ? mrun : mo, l0 = half ? lo : lrun, l1 = half ? lrun : lo;
+            const float M = fmaxf(m0, m1);
+            const float fa = m0 == -INFINITY ? 0.f : ex2(m0 - M), fb = m1 == -INFINITY ? 0.f : ex2(m1 - M);
+            const float L = fa * l0 + fb * l1;
+            const int kvh = mt.g;           // hg = 1
             const int piece = mt.u - u_first + 1;
+            // this thread's columns of the row: [half * D / 2, (half + 1) * D / 2)
             if (piece == mt.n) {  // the whole segment ran here: bf16 output
-                const float inv = lrun > 0.f ? 1.0f / lrun : 0.f;
-                uint16_t *orow = p.out + ((long long)(mt.b + qi) * p.Hq + (long long)kvh * p.gq + (t % p.gq)) * D;
+                const float inv = L > 0.f ? 1.0f / L : 0.f;
+                uint16_t *orow = p.out + ((long long)(mt.b + qi) * p.Hq + (long long)kvh * p.gq + (row % p.gq)) * D;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(trow + 128u + c * 32, r);
+                for (int cc = half * (D / 64); cc < (half + 1) * (D / 64); ++cc) {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32(tlane + tc5_ocol(0) + cc * 32, ra);
+                    tmem_ld32(tlane + tc5_ocol(1) + cc * 32, rb);
                     if (row_ok) {
+                        float v[32];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(r[8 * k]) * inv, __uint_as_float(r[8 * k + 1]) * inv);
-                            w.y = pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv);
-                            w.z = pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv);
-                            w.w = pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv);
-                            *reinterpret_cast<uint4 *>(orow + c * 32 + 8 * k) = w;
-                        }
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = (fa * __uint_as_float(ra[i]) + fb * __uint_as_float(rb[i])) * inv;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            *reinterpret_cast<uint4 *>(orow + cc * 32 + 8 * k) =
+                                make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                                           pack_bf16x2(v[8 * k + 4], v[8 * k + 5]),
+                                           pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
                     }
                 }
             } else {
@@ -1301,34 +1422,31 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
                                            p.sub + jq;
                 float *dst = p.ws_acc + (slot * G + hh) * D;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(trow + 128u + c * 32, r);
+                for (int cc = half * (D / 64); cc < (half + 1) * (D / 64); ++cc) {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32(tlane + tc5_ocol(0) + cc * 32, ra);
+                    tmem_ld32(tlane + tc5_ocol(1) + cc * 32, rb);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        *reinterpret_cast<float4 *>(dst + c * 32 + 4 * k) =
-                            make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                        __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+                        *reinterpret_cast<float4 *>(dst + cc * 32 + 4 * k) =
+                            make_float4(fa * __uint_as_float(ra[4 * k]) + fb * __uint_as_float(rb[4 * k]),
+                                        fa * __uint_as_float(ra[4 * k + 1]) + fb * __uint_as_float(rb[4 * k + 1]),
+                                        fa * __uint_as_float(ra[4 * k + 2]) + fb * __uint_as_float(rb[4 * k + 2]),
+                                        fa * __uint_as_float(ra[4 * k + 3]) + fb * __uint_as_float(rb[4 * k + 3]));
                 }
-                reinterpret_cast<float2 *>(p.ws_ml)[slot * G + hh] = make_float2(mrun, lrun);
+                if (half == 0) reinterpret_cast<float2 *>(p.ws_ml)[slot * G + hh] = make_float2(M, L);
                 __threadfence();
-                __syncwarp();
-                // lanes 0-15 hold block 2 warp, lanes 16-31 block 2 warp + 1 (G = 16 rows a block)
-                const int nvh = max(0, min(p.qn, mt.cnt - jq * p.qn)) * p.gq;
-                int last = 0;
-                if ((lane & 15) == 0 && nvh > 0)
-                    last = arrive_last(p.ws_count + ((long long)mt.b * p.Hkv + kvh) * p.sub + jq, gen,
-                                       uint32_t(piece), uint32_t(mt.n), p.err);
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    const int bq = 2 * warp + half;
-                    if (__shfl_sync(kFull, last, 16 * half)) {
-                        __threadfence();
-                        const int nv = max(0, min(p.qn, mt.cnt - bq * p.qn)) * p.gq;
-                        merge_pieces<D, G, false, true>(p, bound, slice_of(bound, nslots, x0),
-                                                        slice_of(bound, nslots, x0 + mt.n - 1), x0, mt.g, 0, bq,
-                                                        mt.b, kvh, nv, lane);
-                    }
+                // the whole piece is written before it is counted in; one count per (entry, kv head), and
+                // the CTA whose piece completes it merges all 128 rows
+                if (!meet_all()) break;
+                if (t == 0)
+                    sh[5] = arrive_last(p.ws_count + ((long long)mt.b * p.Hkv + kvh) * p.sub, gen, uint32_t(piece),
+                                        uint32_t(mt.n), p.err);
+                if (!meet_all()) break;
+                if (sh[5]) {
+                    __threadfence();
+                    tc5_merge<D, G>(p, bound, slice_of(bound, nslots, x0), slice_of(bound, nslots, x0 + mt.n - 1),
+                                    x0, mt.g, mt.b, row, half, row_ok, qi);
                 }
             }
             tc_fence_before();  // the reads of O come before the next segment's first product overwrites it
@@ -1359,7 +1477,7 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
 // share every K/V tile).  TC5 (with QS): the same entries on the tensor-memory
 // consumers (see tc5_softmax_warps), the entry's Q tile loaded through qmap.
 template <int D, int G, bool FP8, bool QS, bool TC5 = false>
-__global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
+__global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G) + 1) * 32, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const __grid_constant__ CUtensorMap qmap, const DecodeParams p)
 {
@@ -1382,10 +1500,13 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
     long long *bound = reinterpret_cast<long long *>(smem + lay.off_bound);
     float *wts = reinterpret_cast<float *>(smem + lay.off_wts);
     float *red = reinterpret_cast<float *>(smem + lay.off_red);
-    // [0] own slice, [2..3] its start time, [4] tensor-memory address (TC5)
+    // [0] own slice, [2..3] its start time, [4] tensor-memory address (TC5), [5] a piece completed its
+    // segment (TC5)
     int *sh = reinterpret_cast<int *>(smem + lay.off_sh);
     int32_t *scan = reinterpret_cast<int32_t *>(smem + lay.off_scan);
-    uint64_t *tc5_bar = cfree + 1;  // TC5: sfull[2], pfull, odone, drain
+    uint64_t *tc5_bar = cfree + 1;  // TC5: sfull, sfree, pfull[2], odone[2], drain, pair[4]
+    uint64_t *vfull = tc5_bar + 12;        // TC5: [kTc5VSlots] a V slot loaded
+    uint64_t *vempty = vfull + kTc5VSlots;  // TC5: [kTc5VSlots] a V slot released
 
     if (threadIdx.x == 32 * p.cons) {  // none of this reads what the previous kernel writes
         prefetch_tensormap(&kmap);
@@ -1404,11 +1525,19 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         mbar_init(cfull, uint32_t(p.cons - p.hg));  // the non-leading warps' states
         mbar_init(cfree, uint32_t(p.hg));           // read again by the leaders
         if constexpr (TC5) {
-            mbar_init(&tc5_bar[0], 1);                  // scores of an even unit computed
-            mbar_init(&tc5_bar[1], 1);                  // ... of an odd unit
-            mbar_init(&tc5_bar[2], kTc5SoftmaxWarps);   // weights written
-            mbar_init(&tc5_bar[3], 1);                  // output product done
-            mbar_init(&tc5_bar[4], 1);                  // every product done (before TMEM is freed)
+            mbar_init(&tc5_bar[0], 1);                      // scores computed
+            mbar_init(&tc5_bar[1], kTc5SoftmaxWarps);       // scores read
+            for (int i = 0; i < 2; ++i) {                   // [i]: of a unit j with j % 2 == i
+                mbar_init(&tc5_bar[2 + i], kTc5SoftmaxWarps);  // weights written
+                mbar_init(&tc5_bar[4 + i], 1);              // output product done
+            }
+            mbar_init(&tc5_bar[6], 1);                      // every product done (before TMEM is freed)
+            for (int i = 0; i < 4; ++i) mbar_init(&tc5_bar[7 + i], 2);  // the two warps of lane quarter i met
+            mbar_init(&tc5_bar[11], kTc5SoftmaxWarps);                 // all softmax warps met
+            for (int i = 0; i < kTc5VSlots; ++i) {
+                mbar_init(&vfull[i], 1);
+                mbar_init(&vempty[i], 1);
+            }
         }
         fence_barrier_init();
     }
@@ -1492,6 +1621,7 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         const uint64_t policy = policy_evict_first();
         const uint32_t box_bytes = uint32_t(p.boxtok * p.hg * D * ES);
         uint32_t kk = 0, segs = 0;  // units issued, q-ring uses
+        uint32_t vunits = 0;        // TC5: V halves issued
         int rs = 0;                 // ring slot of unit kk (kk % nst, kept without a division)
         uint32_t rph = 0;           // parity of that slot's use (kk / nst) & 1
         bool dead = false;
@@ -1548,9 +1678,9 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                 const int flags = ((k == 0 || iw.u == 0) ? kFirst : 0) |
                                   ((k == nunits - 1 || iw.u == iw.n - 1) ? kLast : 0) |
                                   (k == nunits - 1 ? kSliceEnd : 0);
-                if (flags & kFirst) {  // q rows of this (b, group) for the consumers
-                    const int qs = int(segs & 1u);
-                    const uint32_t quse = segs >> 1;
+                if (flags & kFirst) {  // q rows of this (b, group) for the consumers (TC5: one slot)
+                    const int qs = TC5 ? 0 : int(segs & 1u);
+                    const uint32_t quse = TC5 ? segs : segs >> 1;
                     if (quse > 0 && !mbar_wait_bounded(&qempty[qs], (quse - 1) & 1u)) {
                         dead = true;
                         break;
@@ -1619,7 +1749,8 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                     mt.slice = slice;
                     mt.cnt = cnt;
                     mt.newrow = newrow;
-                    mbar_arrive_expect_tx(&full[s], 2 * nrows * box_bytes);
+                    // TC5: full[s] counts the K half only; the V half has barriers of its own
+                    mbar_arrive_expect_tx(&full[s], (TC5 ? 1u : 2u) * nrows * box_bytes);
                 }
                 __syncwarp();
                 if (k == 0 && lane == 0 && adaptive && !p.row_seq && slice == sh[0] && row >= 0 &&
@@ -1627,7 +1758,23 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
                     p.ws_bal->hint[my_sm][0] = make_int4(row, iw.g * p.hg, int32_t(gen) ^ kHintMagic, iw.b);
                     p.ws_bal->hint[my_sm][1] = make_int4((iw.u * p.toks) >> p.log2_bs, len, 0, 0);
                 }
-                if (row >= 0) {  // box j: lane j, one copy per cache
+                if constexpr (TC5) {
+                    // K now (its half of the stage is free once the previous scores of the slot are done);
+                    // V once the slot's previous output product is done
+                    if (row >= 0) tma_load_4d(st + lane * box_bytes, &kmap, 0, row, 0, iw.g, &full[s], policy);
+                    const uint32_t vs = vunits % kTc5VSlots;
+                    if (vunits >= kTc5VSlots && !mbar_wait_bounded(&vempty[vs], ((vunits / kTc5VSlots) - 1) & 1u)) {
+                        ++kk;  // its K copy is on the way
+                        dead = true;
+                        break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(&vfull[vs], nrows * box_bytes);
+                    __syncwarp();
+                    if (row >= 0)
+                        tma_load_4d(smem + lay.off_v + vs * align_up(lay.kv_bytes, 1024) + lane * box_bytes, &vmap, 0,
+                                    row, 0, iw.g, &vfull[vs], policy);
+                    ++vunits;
+                } else if (row >= 0) {  // box j: lane j, one copy per cache
                     tma_load_4d(st + lane * box_bytes, &kmap, 0, row, 0, iw.g * p.hg, &full[s], policy);
                     tma_load_4d(st + lay.kv_bytes + lane * box_bytes, &vmap, 0, row, 0, iw.g * p.hg, &full[s],
                                 policy);
@@ -1657,6 +1804,9 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         // let every copy this warp started land before the CTA can retire
         for (uint32_t i = kk > uint32_t(p.nst) ? kk - uint32_t(p.nst) : 0u; i < kk; ++i)
             mbar_wait_bounded(&full[i % uint32_t(p.nst)], (i / uint32_t(p.nst)) & 1u);
+        if constexpr (TC5)
+            for (uint32_t i = vunits > uint32_t(kTc5VSlots) ? vunits - uint32_t(kTc5VSlots) : 0u; i < vunits; ++i)
+                mbar_wait_bounded(&vfull[i % kTc5VSlots], (i / kTc5VSlots) & 1u);
         // Count this CTA in: every thread of it read the control block long ago (the fence orders
         // those reads before the count).  The CTA that completes the count leaves the block ready
         // for the next call.  This is the producer's last act, while the consumers still work
@@ -1682,18 +1832,23 @@ __global__ void __launch_bounds__((team_warps(G) + 1) * 32, 1)
         tm.qfull = qfull;
         tm.qempty = qempty;
         tm.sfull = tc5_bar;
+        tm.sfree = tc5_bar + 1;
         tm.pfull = tc5_bar + 2;
-        tm.odone = tc5_bar + 3;
-        tm.drain = tc5_bar + 4;
+        tm.odone = tc5_bar + 4;
+        tm.drain = tc5_bar + 6;
+        tm.pair = tc5_bar + 7;
+        tm.team = tc5_bar + 11;
+        tm.vfull = vfull;
+        tm.vempty = vempty;
         tm.stage0 = stage0;
-        tm.pbuf = smem + lay.off_p;
+        tm.vbase = smem + lay.off_v;
         tm.stage_addr = smem_u32(stage0);
+        tm.v_addr = smem_u32(smem + lay.off_v);
         tm.q_addr = smem_u32(qbuf);
-        tm.p_addr = smem_u32(smem + lay.off_p);
         if (warp == kTc5SoftmaxWarps)
             tc5_mma_warp<D>(p, lay, tm, tmem);
         else
-            tc5_softmax_warps<D, G>(p, lay, tm, tmem, bound, scan, sh, wts, nslots, gen, wp, adaptive);
+            tc5_softmax_warps<D, G>(p, lay, tm, tmem, comb, bound, scan, sh, wts, nslots, gen, wp, adaptive);
         named_barrier(2, 32 * kTc5Consumers);  // every tensor-memory access of the CTA is done
         if (warp == kTc5SoftmaxWarps) {
             tc_fence_after();
@@ -2261,11 +2416,11 @@ LaunchFn pick_decode_wide(int D, int G);  // regular bf16 CTAs, 9 to 16 virtual 
 LaunchFn pick_decode_tc5(int D);          // tensor-memory query-split CTAs, 16 virtual heads (pkv_decode_tc5.cu)
 
 // Whether a query-split call can run on the tensor-memory CTAs: bf16 caches, entries of 128 rows
-// (16 virtual heads per block: the query heads of a kv head a power of two), 64-key tiles within one
-// block (block_size >= 64), and a ring of at least two stages in shared memory.
+// (16 virtual heads per block: the query heads of a kv head a power of two), 128-key tiles within one
+// block (block_size >= 128), and a ring of at least two stages in shared memory.
 inline bool tc5_eligible(int D, int G, int gq, int block_size, int B, int max_smem)
 {
-    if (G != 16 || (D != 64 && D != 128) || block_size < kTc5Keys || (gq & (gq - 1)) != 0) return false;
+    if (G != 16 || (D != 64 && D != 128) || block_size < kTc5Keys || (gq & (gq - 1)) != 0) return false;  // one box a tile
     return cta_layout(D, G, 2, 1, team_warps(G), 2, B, true, true).total <= uint32_t(max_smem);
 }
 

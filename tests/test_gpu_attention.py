@@ -214,11 +214,12 @@ def test_uniform_new_tokens_share_one_pass(n, Hq, Hkv, D, bs, workers):
 
 
 # --------------------------------------------------------------------------- tensor-memory query-split CTAs
-# Long runs of new tokens with gq = Hq / Hkv a power of two and block_size >= 64 run on the tcgen05 CTAs:
-# 128-row entries (128 / gq queries x gq heads) against 64-key tiles, scores and outputs in tensor memory.
+# Long runs of new tokens with gq = Hq / Hkv a power of two and block_size >= 128 run on the tcgen05 CTAs:
+# 128-row entries (128 / gq queries x gq heads) against 128-key tiles, scores and outputs in tensor memory.
 @pytest.mark.parametrize("Hq,Hkv,D,bs,workers", [
-    (16, 8, 128, 256, 0), (16, 8, 128, 64, 0), (8, 8, 128, 64, 0), (32, 8, 64, 128, 0), (64, 8, 128, 256, 0),
-    (16, 1, 64, 64, 0), (16, 8, 128, 256, 7), (16, 8, 128, 256, 333), (16, 8, 128, 64, 2000)])
+    (16, 8, 128, 256, 0), (16, 8, 128, 128, 0), (8, 8, 128, 128, 0), (32, 8, 64, 128, 0), (64, 8, 128, 256, 0),
+    (16, 1, 64, 512, 0), (16, 8, 128, 256, 7), (16, 8, 128, 256, 333), (16, 8, 128, 128, 2000),
+    (16, 8, 128, 1024, 0)])
 def test_tensor_memory_prefill_chunks(Hq, Hkv, D, bs, workers):
     """Whole prefills, 64-query chunks and partial chunks after cached prefixes (up to 5000 keys: split over
     several CTAs and merged), decodes; every query with its own causal bound; repeated calls on one
