@@ -92,15 +92,15 @@ __host__ __device__ constexpr int team_warps(int) { return 8; }
 constexpr int kTc5SoftmaxWarps = 8;
 constexpr int kTc5Consumers = kTc5SoftmaxWarps + 1;
 constexpr int kTc5Keys = 128;          // keys per tile (one unit): the N extent of one score product
-// TMEM columns (512): the score buffer (128 columns), the outputs of the two key halves (D <= 128 columns
-// each, from columns 128 and 384), and two weight buffers of 64 columns from column 256 (bf16 pairs of
-// keys 2c, 2c + 1 in column c; half h in columns 32 h .. 32 h + 31).
-constexpr uint32_t kTc5Cols = 512, kTc5PCol = 256;
-__host__ __device__ constexpr uint32_t tc5_ocol(int half) { return half ? 384u : 128u; }
+// TMEM columns (512): two score buffers of 128 columns, each later holding its tile's weights P in its
+// first 64 columns (bf16 pairs of keys 2c, 2c + 1 in column c; key half h in columns 32 h .. 32 h + 31);
+// the output (D <= 128 columns, from column 256); and two Q tiles of 64 columns from column 384 (row r of
+// the tile in lane r, dims 2c, 2c + 1 in column c).
+constexpr uint32_t kTc5Cols = 512, kTc5OCol = 256, kTc5QCol = 384;
 constexpr uint32_t kTc5SlabBytes = 128u * 128u;  // one 64-dim slab of 128 rows: the Q tile, or a stage's K or V
 // The K tiles stream through a ring of nst slots (a slot is free again once its scores are read); the V
-// tiles through a ring of kTc5VSlots (free again once their output product is done); one Q slot.
-constexpr int kTc5VSlots = 2;
+// tiles through a ring of kTc5VSlots (free again once their output product is done).
+constexpr int kTc5VSlots = 3;
 static_assert(kTc5Keys * 128 == int(kTc5SlabBytes), "a stage's K or V slab holds one tile of 128-byte rows");
 
 // Query-split CTAs (qs; long runs of new tokens, see paged_decode_kernel)
@@ -207,7 +207,7 @@ __host__ __device__ inline CtaLayout cta_layout(int D, int G, int es, int hg, in
     l.kv_bytes = uint32_t(toks * hg * D * es);
     // stages start on the 1024-byte swizzle period; tc5: a stage is a K slot, the V slots follow the ring
     l.stage_bytes = align_up((tc5 ? 1 : 2) * l.kv_bytes, 1024);
-    l.q_bytes = tc5 ? uint32_t(D / 64) * kTc5SlabBytes : align_up(uint32_t(hg * (qs ? sub : 1) * G * D * 2), 128);
+    l.q_bytes = tc5 ? 0u : align_up(uint32_t(hg * (qs ? sub : 1) * G * D * 2), 128);  // tc5: Q in tensor memory
     // states of the non-leading warps of every head (the leader keeps its own in registers); tc5: the
     // values each row's two key halves exchange ([2 tile parities][2 halves][128 rows] floats)
     l.comb_bytes = tc5 ? 2u * 2u * 128u * 4u
@@ -216,16 +216,17 @@ __host__ __device__ inline CtaLayout cta_layout(int D, int G, int es, int hg, in
     l.off_v = o;
     if (tc5) o += uint32_t(kTc5VSlots) * align_up(l.kv_bytes, 1024);
     l.off_q = o;
-    o += (tc5 ? 1 : 2) * l.q_bytes;
+    o += 2 * l.q_bytes;
     l.off_comb = o;
     o += l.comb_bytes;
     l.off_meta = o;
     o += uint32_t(nst) * uint32_t(sizeof(UnitMeta));
     l.off_bar = o;
-    // full / empty per stage, q full / empty x2, combine full / free; tc5: scores full, scores read,
+    // full / empty per stage, q full / empty x2, combine full / free; tc5: scores full x2, scores read x2,
     // weights full x2, output product done x2, drain, a row's two halves met (one per lane quarter) x4,
-    // all softmax warps met, and full / empty per V slot (the stages' pair then covers the K slots)
-    o += uint32_t(2 * nst + 6 + (tc5 ? 12 + 2 * kTc5VSlots : 0)) * 8;
+    // all softmax warps met, a Q tile written, and full / empty per V slot (the stages' pair then covers
+    // the K slots)
+    o += uint32_t(2 * nst + 6 + (tc5 ? 15 + 2 * kTc5VSlots : 0)) * 8;
     l.off_bound = align_up(o, 16);
     o = l.off_bound + (kMaxSlots + 1) * 8;
     l.off_wts = o;
@@ -1048,63 +1049,63 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
 // A query-split entry of 128 rows -- 128 / gq queries x gq query heads of one kv head, row r = query
 // r / gq, head r % gq, in blocks of G = 16 rows that play the part of the query-split CTA's warps (jq) --
 // against 128-key tiles of that kv head, on the 5th-generation tensor cores:
-//   S = Q K^T      128 x 128 fp32 in tensor memory, Q and K 128-byte-swizzled K-major in shared memory
-//                  (the Q tile loaded by one TMA copy per entry, K by the stage's copy);
+//   S = Q K^T      128 x 128 fp32 in tensor memory (two buffers); Q in tensor memory (written there by the
+//                  softmax threads from the query rows when a segment starts, two tiles), K
+//                  128-byte-swizzled K-major in shared memory (a K slot of the ring);
 //   P = 2^(S - m)  by 8 warps, two threads per row (TMEM lane r; each takes 64 of the keys): masks, the
 //                  row's running max m (the two halves exchange their tile max) and sum l (fp32 weights),
-//                  P written back to tensor memory (two buffers) rounded to bf16, the product's operand
+//                  P written over its own scores in tensor memory (once both halves read theirs: the
+//                  exchange of the tile max orders it) rounded to bf16, the product's operand
 //                  type (as flash-attention kernels do: a second product for the rounding error, as the
 //                  decode path carries, would double the output product, which bounds this path);
-//   O += P V       128 x D fp32 in tensor memory, P the A operand from tensor memory, V the stage's rows as
-//                  an MN-major operand from shared memory; O is rescaled in place (read, scaled, written
-//                  back) only when a row's max passes m by the slack, which after a segment's first tiles
-//                  is rare.
-// One thread of the MMA warp issues the products in the order S(0), S(1), P(0)V, S(2), P(1)V, ...: S(j + 1)
-// as soon as the softmax warps have read S(j) into registers, so the tensor core computes the next scores
-// and the current output product while they work on a tile.  Ordering: scores -> sfull (tcgen05.commit);
-// scores read -> sfree (8 warps); weights written -> pfull[j % 2] (8 warps); output product done ->
-// odone[j % 2] and the stage's empty barrier (commits); a segment's last scores -> its Q slot's qempty.
-// No barrier can run two phases ahead of its waiter: each one's next phase needs the waiter's own next step.
+//   O += P V       128 x D fp32 in tensor memory, P the A operand from tensor memory, V a V slot's rows
+//                  as an MN-major operand from shared memory; O is rescaled in place (read, scaled, written
+//                  back) only when a row's max passes m by the slack, which after a segment's first tiles is
+//                  rare.
+// The MMA warp issues each product as soon as its inputs are ready (see tc5_mma_warp), so the tensor core
+// computes the next scores and the current output product while the softmax warps work on a tile.
+// Ordering: scores -> sfull[j % 2] (tcgen05.commit); scores read -> sfree[j % 2] (8 warps; it frees the
+// unit's K slot and meta); weights written -> pfull[j % 2] (8 warps); output product done -> odone[j % 2] and the
+// V slot's vempty (commits); a segment's Q tile written -> qready (8 warps).  A score buffer takes S(k)
+// once the output product of unit k - 2, which read its weights there, is done.  No barrier can run two
+// phases ahead of its waiter: each one's next phase needs the waiter's own next step.
 struct Tc5Smem {
     const UnitMeta *metas;
-    // full / empty: a stage's K half (and its unit's meta); vfull / vempty: its V half
-    uint64_t *full, *empty, *vfull, *vempty, *qfull, *qempty, *sfull, *sfree, *pfull, *odone, *drain, *pair, *team;
-    uint8_t *stage0, *vbase;                // K slot 0, V slot 0
-    uint32_t stage_addr, v_addr, q_addr;   // their shared addresses, and the Q slot's
+    // full / empty: a K slot (and its unit's meta); vfull / vempty: a V slot
+    uint64_t *full, *empty, *vfull, *vempty, *qready, *sfull, *sfree, *pfull, *odone, *drain, *pair, *team;
+    uint8_t *vbase;                  // V slot 0
+    uint32_t stage_addr, v_addr;     // shared addresses of K slot 0 and V slot 0
 };
 
-// O_h += P_h(u) V_h(u) for the two key halves h: the weights of unit u (buffer u % 2) times the V rows of
-// those keys in its ring slot.
+__host__ __device__ inline uint32_t tc5_vslot_bytes(const CtaLayout &lay) { return align_up(lay.kv_bytes, 1024); }
+
+// O += P(u) V(u): the weights of unit u (buffer u % 2) times the V rows of its V slot.
 template <int D>
 __device__ __forceinline__ void tc5_output_product(const CtaLayout &lay, const Tc5Smem &m, uint32_t tmem,
-                                                   uint32_t u, bool first, int lane)
+                                                   uint32_t u, bool first)
 {
     constexpr uint32_t IP = idesc_bf16_f32(128, D, true);
-    if (lane == 0) {
-        tc_fence_after();
-        const uint32_t va = m.v_addr + (u % kTc5VSlots) * align_up(lay.kv_bytes, 1024);
-        const uint32_t pa = tmem + kTc5PCol + (u & 1u) * 64u;
-        // V: keys along K (8-key groups 1024 bytes apart: 16 keys = 2048 bytes), dims along N (64-dim
-        // blocks one slab apart)
+    tc_fence_after();
+    const uint32_t va = m.v_addr + (u % kTc5VSlots) * tc5_vslot_bytes(lay);
+    const uint32_t pa = tmem + (u & 1u) * 128u;  // the weights, over the unit's scores
+    // V: keys along K (8-key groups 1024 bytes apart: 16 keys = 2048 bytes), dims along N (64-dim blocks
+    // one slab apart)
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int ks = 0; ks < kTc5Keys / 32; ++ks)
-                tc_mma_bf16_ta(tmem + tc5_ocol(h), pa + uint32_t(32 * h + 8 * ks),
-                               smem_desc_sw128(va + uint32_t(4 * h + ks) * 2048u, kTc5SlabBytes, 1024), IP,
-                               !(first && ks == 0));
-        tc_commit(&m.odone[u & 1u]);
-        tc_commit(&m.vempty[u % kTc5VSlots]);  // the V slot may take the next copy
-    }
+    for (int ks = 0; ks < kTc5Keys / 16; ++ks)
+        tc_mma_bf16_ta(tmem + kTc5OCol, pa + uint32_t(8 * ks),
+                       smem_desc_sw128(va + uint32_t(ks) * 2048u, kTc5SlabBytes, 1024), IP, !(first && ks == 0));
+    tc_commit(&m.odone[u & 1u]);
+    tc_commit(&m.vempty[u % kTc5VSlots]);  // the V slot may take the next copy
 }
 
 // The MMA warp: lane 0 issues every tensor-core product of the CTA, each as soon as its inputs are
-// ready -- S(k) once unit k's K half has landed (and its Q tile, and S(k - 1) was read), P(k)V once the
-// weights of unit k are written and its V half has landed -- polling both without blocking on either,
-// so a late copy never holds back an output product whose weights are ready.  A stage's K half (and its
-// unit's meta) is released when the softmax warps have read that unit's scores, its V half when the
-// unit's output product is done.  Before it returns it waits for all products to complete (also when
-// it gave up: no progress for the wait limit).
+// ready -- S(k) once unit k's K slot has landed (and, on a segment's first unit, its Q tile is written,
+// and the output product of unit k - 2 is done), P(k)V once the weights of unit k are written and its V
+// slot has landed --
+// polling both without blocking on either, so a late copy never holds back an output product whose
+// weights are ready.  A K slot (and its unit's meta) is released when the softmax warps have read that
+// unit's scores, a V slot when the unit's output product is done.  Before it returns it waits for all
+// products to complete (also when it gave up: no progress for the wait limit).
 template <int D>
 __device__ void tc5_mma_warp(const DecodeParams &p, const CtaLayout &lay, const Tc5Smem &m, uint32_t tmem)
 {
@@ -1112,44 +1113,49 @@ __device__ void tc5_mma_warp(const DecodeParams &p, const CtaLayout &lay, const 
     const int lane = threadIdx.x & 31;
     bool dead = false;
     if (lane == 0) {
-        int s = 0;                       // ring slot of unit ns
+        int s = 0;                       // K slot of unit ns
         uint32_t ph = 0;                 // its parity
         uint32_t ns = 0, npv = 0;        // next unit to score, next unit to multiply by V
-        uint32_t segs = 0;
+        uint32_t segs = 0;               // segments begun (Q tiles used)
         bool have_meta = false, ended = false;
         int flags = 0;
-        int slot_of[2] = {0, 0};         // K slots of units npv, npv + 1 (at most two scored, not multiplied)
+        uint32_t nrel = 0;               // units whose K slots were released (their scores read)
+        int slot_of[4] = {0, 0, 0, 0};   // K slots of units nrel .. ns - 1 (at most 3)
         bool first_of[2] = {false, false};
         uint64_t t0 = global_ns();
         for (uint32_t it = 0;; ++it) {
             bool progress = false;
-            // the next scores: unit ns's stage (and meta), its Q tile on a segment's first unit, and the
-            // score buffer free (S(ns - 1) read); at most two units ahead of the output products
-            if (!ended && ns < npv + 2) {
+            // K slots of units whose scores (and meta) the softmax warps have read
+            if (nrel < ns && mbar_try_wait(smem_u32(&m.sfree[nrel & 1u]), (nrel >> 1) & 1u)) {
+                mbar_arrive(&m.empty[slot_of[nrel & 3u]]);
+                ++nrel;
+                progress = true;
+            }
+            // the next scores: unit ns's K slot (and meta), its Q tile on a segment's first unit, and its
+            // score buffer free (the output product of unit ns - 2 done); at most two units ahead of the
+            // output products and one ahead of the K slot releases
+            if (!ended && ns < npv + 2 && nrel + 1 >= ns) {
                 if (!have_meta && mbar_try_wait(smem_u32(&m.full[s]), ph)) {
                     have_meta = true;
                     flags = m.metas[s].flags;
                     if (m.metas[s].b < 0) ended = true;
                 }
                 if (have_meta && !ended) {
-                    const bool qready = !(flags & kFirst) || mbar_try_wait(smem_u32(&m.qfull[0]), segs & 1u);
-                    const bool sready = ns == 0 || mbar_try_wait(smem_u32(m.sfree), (ns - 1) & 1u);
-                    if (qready && sready) {
-                        // S(ns - 1) was read, and with it the meta of unit ns - 1: its stage's K half is free
-                        if (ns > 0) mbar_arrive(&m.empty[slot_of[(ns - 1) & 1u]]);
+                    const bool qok = !(flags & kFirst) || mbar_try_wait(smem_u32(m.qready), segs & 1u);
+                    const bool bok = ns < 2 || mbar_try_wait(smem_u32(&m.odone[ns & 1u]), ((ns >> 1) - 1) & 1u);
+                    if (qok && bok) {
                         if (flags & kFirst) ++segs;
                         tc_fence_after();
-                        const uint32_t qa = m.q_addr;
+                        const uint32_t qa = tmem + kTc5QCol + ((segs - 1) & 1u) * 64u;
                         const uint32_t ka = m.stage_addr + uint32_t(s) * lay.stage_bytes;
 #pragma unroll
                         for (int ks = 0; ks < D / 16; ++ks) {
                             const uint32_t within = uint32_t(ks & 3) * 32, slab = uint32_t(ks >> 2);
-                            tc_mma_bf16(tmem, smem_desc_sw128(qa + slab * kTc5SlabBytes + within, 16, 1024),
-                                        smem_desc_sw128(ka + slab * kTc5SlabBytes + within, 16, 1024), IS, ks > 0);
+                            tc_mma_bf16_ta(tmem + (ns & 1u) * 128u, qa + uint32_t(8 * ks),
+                                           smem_desc_sw128(ka + slab * kTc5SlabBytes + within, 16, 1024), IS, ks > 0);
                         }
-                        tc_commit(m.sfull);
-                        if (flags & kLast) tc_commit(&m.qempty[0]);  // the segment's Q tile is read for the last time
-                        slot_of[ns & 1u] = s;
+                        tc_commit(&m.sfull[ns & 1u]);
+                        slot_of[ns & 3u] = s;
                         first_of[ns & 1u] = (flags & kFirst) != 0;
                         ++ns;
                         have_meta = false;
@@ -1161,10 +1167,10 @@ __device__ void tc5_mma_warp(const DecodeParams &p, const CtaLayout &lay, const 
                     }
                 }
             }
-            // the next output product, once its weights are written and its V tile has landed
+            // the next output product, once its weights are written and its V slot has landed
             if (npv < ns && mbar_try_wait(smem_u32(&m.pfull[npv & 1u]), (npv >> 1) & 1u) &&
                 mbar_try_wait(smem_u32(&m.vfull[npv % kTc5VSlots]), (npv / kTc5VSlots) & 1u)) {
-                tc5_output_product<D>(lay, m, tmem, npv, first_of[npv & 1u], 0);
+                tc5_output_product<D>(lay, m, tmem, npv, first_of[npv & 1u]);
                 ++npv;
                 progress = true;
             }
@@ -1184,43 +1190,73 @@ __device__ void tc5_mma_warp(const DecodeParams &p, const CtaLayout &lay, const 
     if (!mbar_wait_bounded(m.drain, 0u) && lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
 }
 
+// A tensor-memory CTA's piece of a segment: the 128 rows' (m, l) at ws_ml[tile * 128 + row] and their
+// unnormalised outputs at ws_acc[tile * 128 D ..], laid out as [D / 4][128 rows][4] so that a warp's
+// 32 rows move 512 contiguous bytes per access; tile numbers the 128-row blocks of the slot space of
+// ws_layout (slot = tile * 8 + row / 16).
+__device__ __forceinline__ long long tc5_piece_tile(const DecodeParams &p, int slice, bool slice_first, int b, int g)
+{
+    return slots_by_slice(p.B, p.nhg) ? 2LL * slice + (slice_first ? 0 : 1) : slice + (long long)b * p.nhg + g;
+}
+
 // The pieces of one (entry, kv head) segment, merged by the CTA whose piece completed its unit count:
 // thread (row, half) folds columns [half D / 2, (half + 1) D / 2) of the row over the pieces left by the
-// non-empty slices sf..sl (slot numbering as in ws_layout: jq = row / G, hh = row % G), all of a piece's
-// loads in flight at once, then writes the row's bf16 output if the row is one of the entry's queries:
+// non-empty slices sf..sl, in slice order (the CTA's own piece, that of slice own, read back from tensor
+// memory: the same values it stored), then writes the row's bf16 output if the row is one of the entry's
+// queries:
 //   M = max m_i,  l = sum 2^(m_i - M) l_i,  out = sum 2^(m_i - M) acc_i / l.
-template <int D, int G>
-__device__ void tc5_merge(const DecodeParams &p, const long long *bound, int sf, int sl, long long x0, int g,
-                          int b, int row, int half, bool row_ok, int qi)
+template <int D>
+__device__ void tc5_merge(const DecodeParams &p, const long long *bound, int sf, int sl, int own, float own_m,
+                          float own_l, uint32_t own_o, long long x0, int g, int b, int row, int half, bool row_ok,
+                          int qi)
 {
     constexpr int C = D / 2;  // columns of this thread
-    const int jq = row / G, hh = row - jq * G;
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);
     float M = -INFINITY, lsum = 0.f, a[C];
 #pragma unroll
     for (int e = 0; e < C; ++e) a[e] = 0.f;
+    // the running state takes piece (m, l) with weight f = 2^(m - M'), itself r = 2^(M - M')
+    auto rescale = [&](float2 st, float &r, float &f) {
+        const float mb = fmaxf(M, st.x);
+        r = M == -INFINITY ? 0.f : ex2(M - mb);
+        f = ex2(st.x - mb);
+        lsum = fmaf(f, st.y, lsum * r);
+        M = mb;
+    };
     for (int sk = sf; sk <= sl; ++sk) {
         if (bound[sk + 1] <= bound[sk]) continue;  // an empty slice left nothing
-        const long long slot = (slots_by_slice(p.B, p.nhg) ? 2LL * sk + ((sk == sf && x0 != bound[sf]) ? 1 : 0)
-                                                           : sk + (long long)b * p.nhg + g) *
-                                   p.sub + jq;
-        const float2 st = __ldcg(ml + slot * G + hh);
-        const float4 *src = reinterpret_cast<const float4 *>(p.ws_acc + (slot * G + hh) * D + half * C);
-        float4 v[C / 4];
+        float r, f;
+        if (sk == own) {
+            // (the load is warp-wide: every lane takes part, also for a row that saw no key here)
+            const bool has = own_m != -INFINITY;
+            if (has) rescale(make_float2(own_m, own_l), r, f);
+            __syncwarp();  // lanes that left an earlier piece early meet again
 #pragma unroll
-        for (int k = 0; k < C / 4; ++k) v[k] = __ldcg(src + k);
-        if (st.x == -INFINITY) continue;  // a piece in which the row saw no key
-        const float mb = fmaxf(M, st.x);
-        const float r = M == -INFINITY ? 0.f : ex2(M - mb), f = ex2(st.x - mb);
-        lsum = fmaf(f, st.y, lsum * r);
+            for (int cc = 0; cc < C / 32; ++cc) {
+                uint32_t w[32];
+                tmem_ld32(own_o + uint32_t(cc * 32), w);
+                if (has) {
 #pragma unroll
-        for (int k = 0; k < C / 4; ++k) {
-            a[4 * k] = fmaf(f, v[k].x, a[4 * k] * r);
-            a[4 * k + 1] = fmaf(f, v[k].y, a[4 * k + 1] * r);
-            a[4 * k + 2] = fmaf(f, v[k].z, a[4 * k + 2] * r);
-            a[4 * k + 3] = fmaf(f, v[k].w, a[4 * k + 3] * r);
+                    for (int i = 0; i < 32; ++i) a[32 * cc + i] = fmaf(f, __uint_as_float(w[i]), a[32 * cc + i] * r);
+                }
+            }
+        } else {
+            const long long tile = tc5_piece_tile(p, sk, !(sk == sf && x0 != bound[sf]), b, g);
+            const float2 st = __ldcg(ml + tile * 128 + row);
+            const float4 *src = reinterpret_cast<const float4 *>(p.ws_acc + tile * 128 * D) + half * (C / 4) * 128 + row;
+            float4 v[C / 4];
+#pragma unroll
+            for (int k = 0; k < C / 4; ++k) v[k] = __ldcg(src + k * 128);
+            if (st.x == -INFINITY) continue;
+            rescale(st, r, f);
+#pragma unroll
+            for (int k = 0; k < C / 4; ++k) {
+                a[4 * k] = fmaf(f, v[k].x, a[4 * k] * r);
+                a[4 * k + 1] = fmaf(f, v[k].y, a[4 * k + 1] * r);
+                a[4 * k + 2] = fmaf(f, v[k].z, a[4 * k + 2] * r);
+                a[4 * k + 3] = fmaf(f, v[k].w, a[4 * k + 3] * r);
+            }
         }
-        M = mb;
     }
     if (!row_ok) return;
     const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
@@ -1232,37 +1268,39 @@ __device__ void tc5_merge(const DecodeParams &p, const long long *bound, int sf,
                        pack_bf16x2(a[8 * k + 4] * inv, a[8 * k + 5] * inv), pack_bf16x2(a[8 * k + 6] * inv, a[8 * k + 7] * inv));
 }
 
+static_assert(team_warps(16) * 16 == 128, "a tensor-memory piece tile is 8 slots of 16 rows");
+
 // The softmax warps: thread t of the 256 takes row r = 32 (w % 4) + lane (TMEM lane r; w = t / 32) and
-// keys 64 h .. 64 h + 63 of every tile, h = w / 4, with its own running max and sum and its own output
-// O_h: the two threads of a row (warps w and w + 4) combine their states when a segment's part in the
-// slice ends.
+// keys 64 h .. 64 h + 63 of every tile, h = w / 4.  The two threads of a row (warps w and w + 4) hold the
+// same running max: they exchange their tile max each tile; each keeps the sum of its own keys' weights.
+// When a segment starts they write its Q tile (dims 64 h .. 64 h + 63 of row r) into tensor memory.
 template <int D, int G>
 __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, const Tc5Smem &m, uint32_t tmem,
                                   float *xch, const long long *bound, const int32_t *scan, int *sh,
                                   const float *wts, int nslots, uint32_t gen, int wp, bool adaptive)
 {
     constexpr int KH = kTc5Keys / 2;  // keys of a half
+    constexpr int DH = D / 2;         // dims of a half (of Q and of the output)
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int quarter = warp & 3, half = warp >> 2;
     const int row = 32 * quarter + lane;
     const uint32_t tlane = tmem + (uint32_t(32 * quarter) << 16);  // this warp's lane quarter
     const int qi = row / p.gq;                                      // query of the row within its entry
-    const int jq = row / G, hh = row - jq * G;                      // block of G rows and the row in it
     const int home = sh[0];
     const float c = p.scale_log2;
     int s = 0;
-    uint32_t ph = 0, j = 0;
+    uint32_t ph = 0, j = 0, segs = 0;
     float mrun = -INFINITY, lrun = 0.f;
     bool row_ok = false;
     int shift = 0, u_first = 0;
     uint32_t meets = 0;  // exchanges with the row's other half so far (the same in both warps)
+    uint32_t teams = 0;  // meetings of all softmax warps so far (the same in every one)
     // a wait that may give up: the kernel's error word, and out of the loop
     auto wait = [&](uint64_t *bar, uint32_t parity) {
         if (mbar_wait_bounded(bar, parity)) return true;
         if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
         return false;
     };
-    uint32_t teams = 0;  // meetings of all softmax warps so far (the same in every one)
     auto meet_all = [&]() {
         __syncwarp();
         if (lane == 0) mbar_arrive(m.team);
@@ -1284,12 +1322,46 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
         const UnitMeta mt = m.metas[s];
         if (mt.b < 0) break;
         const bool first = (mt.flags & kFirst) != 0;
+        const int kvh = mt.g;  // hg = 1
         if (first) {
             row_ok = qi < mt.cnt;
             shift = (mt.cnt - 1) - qi;  // the row's query sees this many fewer of the entry's last keys
             mrun = -INFINITY;
             lrun = 0.f;
             u_first = mt.u;
+            // the segment's Q tile into tensor memory (tile segs % 2: the tile before it was last read by
+            // the previous segment's scores, all of which were read back): this thread's 64 dims of its
+            // row, zeros for rows that are not queries of the entry
+            uint32_t w[32];
+            if (row_ok) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    p.q + ((long long)(mt.b + qi) * p.Hq + (long long)kvh * p.gq + (row % p.gq)) * D + half * DH);
+#pragma unroll
+                for (int k = 0; k < DH / 8; ++k) {
+                    const uint4 v = __ldg(src + k);
+                    w[4 * k] = v.x;
+                    w[4 * k + 1] = v.y;
+                    w[4 * k + 2] = v.z;
+                    w[4 * k + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < DH / 2; ++k) w[k] = 0u;
+            }
+            const uint32_t qa = tlane + kTc5QCol + (segs & 1u) * 64u + uint32_t(half * DH / 2);
+            if constexpr (DH / 2 == 32) {
+                tmem_st32(qa, w);
+            } else {
+                uint32_t w16[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) w16[k] = w[k];
+                tmem_st16(qa, w16);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(m.qready);
+            ++segs;
         }
         const int tok0 = mt.u * kTc5Keys;
         const int valid = min(kTc5Keys, mt.L - tok0);
@@ -1298,7 +1370,7 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
             // V rows past the sequence's end hold anything (NaN included) and 0 * NaN is NaN: zero them,
             // once the V copy has landed
             if (!wait(&m.vfull[j % kTc5VSlots], (j / kTc5VSlots) & 1u)) break;
-            uint8_t *vrows = m.vbase + size_t(j % kTc5VSlots) * align_up(lay.kv_bytes, 1024);
+            uint8_t *vrows = m.vbase + size_t(j % kTc5VSlots) * tc5_vslot_bytes(lay);
             const int per_part = (kTc5Keys - valid) * 8, n = per_part * (D / 64);
             for (int i = t; i < n; i += 32 * kTc5SoftmaxWarps) {
                 const int part = i / per_part, r = i - part * per_part;
@@ -1307,14 +1379,15 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
             }
             fence_proxy_async_smem();  // for the tensor core
         }
-        if (!wait(m.sfull, j & 1u)) break;
+        if (!wait(&m.sfull[j & 1u], (j >> 1) & 1u)) break;
         tc_fence_after();
+        const uint32_t sbuf = tlane + (j & 1u) * 128u;  // the unit's score buffer (and then its weights)
         // raw scores s of the half's keys (at or past the row's bound: -inf); weights 2^(s c - m)
         float x[KH];
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
             uint32_t r[32];
-            tmem_ld32(tlane + uint32_t(KH * half + 32 * h2), r);
+            tmem_ld32(sbuf + uint32_t(KH * half + 32 * h2), r);
             if (lim >= 32 * (h2 + 1)) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[32 * h2 + i] = __uint_as_float(r[i]);
@@ -1325,11 +1398,14 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(m.sfree);  // the score buffer may take the next tile's scores
+        if (lane == 0) mbar_arrive(&m.sfree[j & 1u]);  // the unit's K slot (and meta) may be reused
         float mx4[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
         for (int i = 4; i < KH; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], x[i]);
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;  // c > 0
+        float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;  // c > 0
+        float other;
+        if (!exchange(mx, other)) break;
+        mx = fmaxf(mx, other);  // the row's tile max: the same in both halves
         float alpha = 1.0f;
         bool resc = false;
         if (mx > mrun + kRescaleSlack) {  // also the row's first tile with a key (mrun = -inf)
@@ -1340,26 +1416,23 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
             }
             mrun = mx;
         }
-        // this warp's rows of O_half scaled in place (alpha = 1 for rows that keep their max), once
-        // P(j - 1) V is in
+        // O's rows scaled in place (alpha = 1 for rows that keep their max), this thread's half of the
+        // columns, once P(j - 1) V is in
         if (__any_sync(kFull, resc)) {
             if (!wait(&m.odone[(j - 1) & 1u], ((j - 1) >> 1) & 1u)) break;
             tc_fence_after();
 #pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = half * (D / 64); cc < (half + 1) * (D / 64); ++cc) {
                 uint32_t r[32];
-                tmem_ld32(tlane + tc5_ocol(half) + cc * 32, r);
+                tmem_ld32(tlane + kTc5OCol + cc * 32, r);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                tmem_st32(tlane + tc5_ocol(half) + cc * 32, r);
+                tmem_st32(tlane + kTc5OCol + cc * 32, r);
             }
         }
-        // P(j)'s buffer was last read by the product of unit j - 2
-        if (j >= 2 && !wait(&m.odone[j & 1u], ((j >> 1) - 1) & 1u)) break;
-        tc_fence_after();
-        // weights rounded to bf16 (the output product's operand), into this half's 32 columns of buffer
-        // j % 2; the row sum adds the fp32 weights (2^-inf = 0 for the masked keys; a row without any key
-        // so far takes m = 0 and gets zeros)
+        // weights rounded to bf16 (the output product's operand), over the scores in this half's 32 columns
+        // of the unit's buffer (both halves read their scores before the exchange); the row sum adds the fp32
+        // weights (2^-inf = 0 for the masked keys; a row without any key so far takes m = 0 and gets zeros)
         {
             const float mneg = mrun == -INFINITY ? 0.f : -mrun;
             float ps[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1371,7 +1444,7 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
                 w[k] = pack_bf16x2(p0, p1);
             }
             lrun += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-            tmem_st32(tlane + kTc5PCol + (j & 1u) * 64u + 32u * half, w);
+            tmem_st32(sbuf + 32u * half, w);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -1381,72 +1454,60 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
         if (mt.flags & kLast) {  // the segment's part in this slice ends: O once its last product is done
             if (!wait(&m.odone[j & 1u], (j >> 1) & 1u)) break;
             tc_fence_after();
-            // the row's two halves: M = max, weights fa, fb of O_0, O_1 (0 for a half without keys)
-            float mo, lo;
-            if (!exchange(mrun, mo) || !exchange(lrun, lo)) break;
-            const float m0 = half ? mo : mrun, m1 = half ? mrun : mo, l0 = half ? lo : lrun, l1 = half ? lrun : lo;
-            const float M = fmaxf(m0, m1);
-            const float fa = m0 == -INFINITY ? 0.f : ex2(m0 - M), fb = m1 == -INFINITY ? 0.f : ex2(m1 - M);
-            const float L = fa * l0 + fb * l1;
-            const int kvh = mt.g;           // hg = 1
+            float lother;
+            if (!exchange(lrun, lother)) break;
+            const float L = lrun + lother;  // the row's sum (both halves share the max)
             const int piece = mt.u - u_first + 1;
-            // this thread's columns of the row: [half * D / 2, (half + 1) * D / 2)
+            // this thread's columns of the row: [half D / 2, (half + 1) D / 2)
             if (piece == mt.n) {  // the whole segment ran here: bf16 output
                 const float inv = L > 0.f ? 1.0f / L : 0.f;
                 uint16_t *orow = p.out + ((long long)(mt.b + qi) * p.Hq + (long long)kvh * p.gq + (row % p.gq)) * D;
 #pragma unroll 1
                 for (int cc = half * (D / 64); cc < (half + 1) * (D / 64); ++cc) {
-                    uint32_t ra[32], rb[32];
-                    tmem_ld32(tlane + tc5_ocol(0) + cc * 32, ra);
-                    tmem_ld32(tlane + tc5_ocol(1) + cc * 32, rb);
+                    uint32_t r[32];
+                    tmem_ld32(tlane + kTc5OCol + cc * 32, r);
                     if (row_ok) {
-                        float v[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = (fa * __uint_as_float(ra[i]) + fb * __uint_as_float(rb[i])) * inv;
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            *reinterpret_cast<uint4 *>(orow + cc * 32 + 8 * k) =
-                                make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
-                                           pack_bf16x2(v[8 * k + 4], v[8 * k + 5]),
-                                           pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+                            *reinterpret_cast<uint4 *>(orow + cc * 32 + 8 * k) = make_uint4(
+                                pack_bf16x2(__uint_as_float(r[8 * k]) * inv, __uint_as_float(r[8 * k + 1]) * inv),
+                                pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv),
+                                pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv),
+                                pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv));
                     }
                 }
             } else {
-                // a piece: (m, l, acc) of every row into the piece slot of its block jq (see ws_layout); the
-                // CTA that completes a block's count merges the block's pieces
+                // a piece: (m, l, acc) of every row into the slice's piece tile (tc5_piece_tile); the CTA
+                // whose piece completes the (entry, kv head) count merges all 128 rows
                 const long long x0 = (long long)p.nhg * scan[mt.b] + (long long)mt.g * mt.n;
                 const bool firstseg = u_first > 0 || x0 == bound[mt.slice];
-                const long long slot = (slots_by_slice(p.B, p.nhg) ? 2LL * mt.slice + (firstseg ? 0 : 1)
-                                                                   : mt.slice + (long long)mt.b * p.nhg + mt.g) *
-                                           p.sub + jq;
-                float *dst = p.ws_acc + (slot * G + hh) * D;
+                const long long tile = tc5_piece_tile(p, mt.slice, firstseg, mt.b, mt.g);
+                float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + tile * 128 * D) + row;
 #pragma unroll 1
                 for (int cc = half * (D / 64); cc < (half + 1) * (D / 64); ++cc) {
-                    uint32_t ra[32], rb[32];
-                    tmem_ld32(tlane + tc5_ocol(0) + cc * 32, ra);
-                    tmem_ld32(tlane + tc5_ocol(1) + cc * 32, rb);
+                    uint32_t r[32];
+                    tmem_ld32(tlane + kTc5OCol + cc * 32, r);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        *reinterpret_cast<float4 *>(dst + cc * 32 + 4 * k) =
-                            make_float4(fa * __uint_as_float(ra[4 * k]) + fb * __uint_as_float(rb[4 * k]),
-                                        fa * __uint_as_float(ra[4 * k + 1]) + fb * __uint_as_float(rb[4 * k + 1]),
-                                        fa * __uint_as_float(ra[4 * k + 2]) + fb * __uint_as_float(rb[4 * k + 2]),
-                                        fa * __uint_as_float(ra[4 * k + 3]) + fb * __uint_as_float(rb[4 * k + 3]));
+                        dst[(cc * 8 + k) * 128] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                                              __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
                 }
-                if (half == 0) reinterpret_cast<float2 *>(p.ws_ml)[slot * G + hh] = make_float2(M, L);
-                __threadfence();
-                // the whole piece is written before it is counted in; one count per (entry, kv head), and
-                // the CTA whose piece completes it merges all 128 rows
+                if (half == 0) reinterpret_cast<float2 *>(p.ws_ml)[tile * 128 + row] = make_float2(mrun, L);
+                // the whole piece is written before it is counted in: every thread's stores precede the
+                // meeting (release / acquire at CTA scope), and the counting thread's fence at device scope
+                // carries them (fences are cumulative)
                 if (!meet_all()) break;
-                if (t == 0)
+                if (t == 0) {
+                    __threadfence();
                     sh[5] = arrive_last(p.ws_count + ((long long)mt.b * p.Hkv + kvh) * p.sub, gen, uint32_t(piece),
                                         uint32_t(mt.n), p.err);
+                }
                 if (!meet_all()) break;
                 if (sh[5]) {
                     __threadfence();
-                    tc5_merge<D, G>(p, bound, slice_of(bound, nslots, x0), slice_of(bound, nslots, x0 + mt.n - 1),
-                                    x0, mt.g, mt.b, row, half, row_ok, qi);
+                    tc5_merge<D>(p, bound, slice_of(bound, nslots, x0), slice_of(bound, nslots, x0 + mt.n - 1),
+                                 mt.slice, mrun, L, tlane + kTc5OCol + uint32_t(half * (D / 2)), x0, mt.g, mt.b, row,
+                                 half, row_ok, qi);
                 }
             }
             tc_fence_before();  // the reads of O come before the next segment's first product overwrites it
@@ -1475,11 +1536,11 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
 // its own qn queries w % sub of the entry's (QS true, hg = 1: the query-split
 // CTA for long runs of new tokens, where the entry's up to sub * qn queries
 // share every K/V tile).  TC5 (with QS): the same entries on the tensor-memory
-// consumers (see tc5_softmax_warps), the entry's Q tile loaded through qmap.
+// consumers (see tc5_softmax_warps).
 template <int D, int G, bool FP8, bool QS, bool TC5 = false>
 __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G) + 1) * 32, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                        const __grid_constant__ CUtensorMap qmap, const DecodeParams p)
+                        const DecodeParams p)
 {
     static_assert(!TC5 || (QS && !FP8 && G == 16 && (D == 64 || D == 128)), "tensor-memory CTAs: bf16 query-split");
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -1504,14 +1565,13 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
     // segment (TC5)
     int *sh = reinterpret_cast<int *>(smem + lay.off_sh);
     int32_t *scan = reinterpret_cast<int32_t *>(smem + lay.off_scan);
-    uint64_t *tc5_bar = cfree + 1;  // TC5: sfull, sfree, pfull[2], odone[2], drain, pair[4]
-    uint64_t *vfull = tc5_bar + 12;        // TC5: [kTc5VSlots] a V slot loaded
+    uint64_t *tc5_bar = cfree + 1;  // TC5: sfull[2], sfree[2], pfull[2], odone[2], drain, pair[4], team, qready
+    uint64_t *vfull = tc5_bar + 15;        // TC5: [kTc5VSlots] a V slot loaded
     uint64_t *vempty = vfull + kTc5VSlots;  // TC5: [kTc5VSlots] a V slot released
 
     if (threadIdx.x == 32 * p.cons) {  // none of this reads what the previous kernel writes
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
-        if constexpr (TC5) prefetch_tensormap(&qmap);
         // TC5: a stage and a Q slot are released by one tcgen05.commit of the MMA warp
         const uint32_t releases = TC5 ? 1u : uint32_t(p.cons);
         for (int i = 0; i < p.nst; ++i) {
@@ -1525,15 +1585,16 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
         mbar_init(cfull, uint32_t(p.cons - p.hg));  // the non-leading warps' states
         mbar_init(cfree, uint32_t(p.hg));           // read again by the leaders
         if constexpr (TC5) {
-            mbar_init(&tc5_bar[0], 1);                      // scores computed
-            mbar_init(&tc5_bar[1], kTc5SoftmaxWarps);       // scores read
             for (int i = 0; i < 2; ++i) {                   // [i]: of a unit j with j % 2 == i
-                mbar_init(&tc5_bar[2 + i], kTc5SoftmaxWarps);  // weights written
-                mbar_init(&tc5_bar[4 + i], 1);              // output product done
+                mbar_init(&tc5_bar[i], 1);                  // scores computed
+                mbar_init(&tc5_bar[2 + i], kTc5SoftmaxWarps);  // scores read
+                mbar_init(&tc5_bar[4 + i], kTc5SoftmaxWarps);  // weights written
+                mbar_init(&tc5_bar[6 + i], 1);              // output product done
             }
-            mbar_init(&tc5_bar[6], 1);                      // every product done (before TMEM is freed)
-            for (int i = 0; i < 4; ++i) mbar_init(&tc5_bar[7 + i], 2);  // the two warps of lane quarter i met
-            mbar_init(&tc5_bar[11], kTc5SoftmaxWarps);                 // all softmax warps met
+            mbar_init(&tc5_bar[8], 1);                      // every product done (before TMEM is freed)
+            for (int i = 0; i < 4; ++i) mbar_init(&tc5_bar[9 + i], 2);  // the two warps of lane quarter i met
+            mbar_init(&tc5_bar[13], kTc5SoftmaxWarps);      // all softmax warps met
+            mbar_init(&tc5_bar[14], kTc5SoftmaxWarps);      // a segment's Q tile written
             for (int i = 0; i < kTc5VSlots; ++i) {
                 mbar_init(&vfull[i], 1);
                 mbar_init(&vempty[i], 1);
@@ -1632,15 +1693,31 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
             if (lane == 0 && slice == sh[0])
                 *reinterpret_cast<unsigned long long *>(sh + 2) = global_ns();
             const long long nunits = hi - lo, nboxes = nunits * p.nbox;
+            // TC5: the slice's units from its last (entry, kv head) segment on, then from its start: the
+            // part of that segment which continues in the next slice (and the part of the first segment
+            // which continued from the previous one) finishes early, so the merge of a split segment
+            // happens amid the run, not at its end.  Segments stay whole and in order (and a merge folds
+            // its pieces in slice order), so the results are unchanged.
+            long long rot = 0;
+            if constexpr (TC5) {
+                if (nunits > 1) {
+                    const Walker last = walker_locate(scan, p.B, p.nhg, hi - 1);
+                    rot = max(0LL, hi - 1 - last.u - lo);
+                }
+            }
+            auto unit_at = [&](long long k) {  // unit processed k-th
+                const long long y = k + rot;
+                return lo + (y >= nunits ? y - nunits : y);
+            };
             // Block-table prefetch, 32 boxes per batch: lane j of `cur` holds the entry (and the
             // context length) of box kb + j; `nxt` is loaded one batch ahead.  Two register sets,
             // because the scoreboard tracks a register for the whole warp.
-            Walker iw = nunits > 0 ? walker_locate(scan, p.B, p.nhg, lo) : Walker{0, 0, 0, 1};
+            Walker iw = nunits > 0 ? walker_locate(scan, p.B, p.nhg, lo + rot) : Walker{0, 0, 0, 1};
             int32_t cur_e = -1, cur_L = 0, cur_c = 1, nxt_e = -1, nxt_L = 0, nxt_c = 1;
             auto prefetch_batch = [&](long long kb) {  // boxes [kb, kb + 32) -> nxt, one per lane
                 const long long x = kb + lane;
                 if (x < nboxes) {
-                    const Walker mine = walker_locate(scan, p.B, p.nhg, lo + (x >> p.lg_nbox));
+                    const Walker mine = walker_locate(scan, p.B, p.nhg, unit_at(x >> p.lg_nbox));
                     const int32_t pos = mine.u * p.toks + int32_t(x & (p.nbox - 1)) * p.boxtok;
                     // The entry is only used for pos < L, where pos / bs < max_blocks (lengths
                     // beyond the table were rejected by the scan); clamping keeps the load in
@@ -1675,22 +1752,25 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
                 const int32_t len = __shfl_sync(kFull, cur_L, src);
                 const int32_t cnt = __shfl_sync(kFull, cur_c, src);
                 const int32_t e = __shfl_sync(kFull, cur_e, (src + lane) & 31);  // lane j: box j's entry
-                const int flags = ((k == 0 || iw.u == 0) ? kFirst : 0) |
-                                  ((k == nunits - 1 || iw.u == iw.n - 1) ? kLast : 0) |
+                const long long x = unit_at(k);
+                const int flags = ((x == lo || iw.u == 0) ? kFirst : 0) |
+                                  ((x == hi - 1 || iw.u == iw.n - 1) ? kLast : 0) |
                                   (k == nunits - 1 ? kSliceEnd : 0);
-                if (flags & kFirst) {  // q rows of this (b, group) for the consumers (TC5: one slot)
-                    const int qs = TC5 ? 0 : int(segs & 1u);
-                    const uint32_t quse = TC5 ? segs : segs >> 1;
-                    if (quse > 0 && !mbar_wait_bounded(&qempty[qs], (quse - 1) & 1u)) {
+                if (flags & kFirst) {  // q rows of this (b, group) for the consumers
+                    const int qs = int(segs & 1u);
+                    const uint32_t quse = segs >> 1;
+                    if (!TC5 && quse > 0 && !mbar_wait_bounded(&qempty[qs], (quse - 1) & 1u)) {
                         dead = true;
                         break;
                     }
                     if constexpr (TC5) {
-                        // the entry's 128 rows (queries x heads of kv head g) as one 128-byte-swizzled tile
-                        if (lane == 0) {
-                            mbar_arrive_expect_tx(&qfull[qs], lay.q_bytes);
-                            tma_load_4d(qbuf + qs * lay.q_bytes, &qmap, 0, iw.g * p.gq, iw.b, 0, &qfull[qs], policy);
-                        }
+                        // the consumers load the entry's Q tile themselves (into tensor memory); warm L2 with
+                        // its rows: 8 qn queries x gq heads of kv head g, D values each
+                        const int nq = team_warps(G) * p.qn;
+                        for (int i = lane; i < nq; i += 32)
+                            if (iw.b + i < p.B)
+                                bulk_prefetch_l2(p.q + ((long long)(iw.b + i) * p.Hq + (long long)iw.g * p.gq) * D,
+                                                 uint32_t(p.gq * D * 2));
                     } else if (p.qn == 1 && !QS) {  // the group's G * hg query rows are contiguous
                         const uint32_t qb = uint32_t(p.hg * G * D * 2);
                         if (lane == 0) {
@@ -1784,7 +1864,12 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
                     rs = 0;
                     rph ^= 1u;
                 }
-                if (k + 1 < nunits) walker_advance(iw, scan, p.nhg, p.B);
+                if (k + 1 < nunits) {
+                    if (rot > 0 && k + 1 == nunits - rot)
+                        iw = walker_locate(scan, p.B, p.nhg, lo);  // from the slice's last unit to its first
+                    else
+                        walker_advance(iw, scan, p.nhg, p.B);
+                }
                 if (k == 0 && nboxes > 32) prefetch_batch(32);  // after the first copies are on their way
             }
             slice = (adaptive && !dead) ? claim_leftover(p, gen, bound, nslots, wp, true) : -1;
@@ -1829,22 +1914,19 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
         tm.metas = metas;
         tm.full = full;
         tm.empty = empty;
-        tm.qfull = qfull;
-        tm.qempty = qempty;
-        tm.sfull = tc5_bar;
-        tm.sfree = tc5_bar + 1;
-        tm.pfull = tc5_bar + 2;
-        tm.odone = tc5_bar + 4;
-        tm.drain = tc5_bar + 6;
-        tm.pair = tc5_bar + 7;
-        tm.team = tc5_bar + 11;
         tm.vfull = vfull;
         tm.vempty = vempty;
-        tm.stage0 = stage0;
+        tm.sfull = tc5_bar;
+        tm.sfree = tc5_bar + 2;
+        tm.pfull = tc5_bar + 4;
+        tm.odone = tc5_bar + 6;
+        tm.drain = tc5_bar + 8;
+        tm.pair = tc5_bar + 9;
+        tm.team = tc5_bar + 13;
+        tm.qready = tc5_bar + 14;
         tm.vbase = smem + lay.off_v;
         tm.stage_addr = smem_u32(stage0);
         tm.v_addr = smem_u32(smem + lay.off_v);
-        tm.q_addr = smem_u32(qbuf);
         if (warp == kTc5SoftmaxWarps)
             tc5_mma_warp<D>(p, lay, tm, tmem);
         else
@@ -2266,61 +2348,6 @@ inline bool cached_cache_map(CUtensorMap *map, int dev, const void *base, bool f
     return true;
 }
 
-// Tensor map over the query rows q [rows, Hq, D] for the tensor-memory CTAs:
-// dims (64 elements, Hq heads, rows, D / 64 parts) with byte strides
-// (D * 2, Hq * D * 2, 128); a box of gq heads x nq rows x all parts lands as
-// [part][row][head][128 bytes], 128-byte swizzled: the 64-dim slabs of a
-// 128-row K-major operand whose row r is (query r / gq, head r % gq).  Rows
-// past the tensor's end read as zeros.
-inline bool encode_q_map(CUtensorMap *map, const void *q, int Hq, int64_t rows, int D, int gq, int nq)
-{
-    EncodeTiledFn enc = encode_tiled_fn();
-    if (!enc) {
-        record_cuda_error("cuTensorMapEncodeTiled", "driver entry point unavailable");
-        return false;
-    }
-    const cuuint64_t dims[4] = {64u, cuuint64_t(Hq), cuuint64_t(rows), cuuint64_t(D / 64)};
-    const cuuint64_t strides[3] = {cuuint64_t(D) * 2, cuuint64_t(Hq) * D * 2, 128u};
-    const cuuint32_t box[4] = {64u, cuuint32_t(gq), cuuint32_t(nq), cuuint32_t(D / 64)};
-    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        char msg[64];
-        std::snprintf(msg, sizeof msg, "CUresult %d (query map)", int(r));
-        record_cuda_error("cuTensorMapEncodeTiled", msg);
-        return false;
-    }
-    return true;
-}
-
-// The most recent query maps (a serving loop reuses its query buffers).
-inline bool cached_q_map(CUtensorMap *map, int dev, const void *q, int Hq, int64_t rows, int D, int gq, int nq)
-{
-    struct Entry {
-        int dev;
-        const void *q;
-        int Hq;
-        int64_t rows;
-        int D, gq, nq;
-        CUtensorMap map;
-    };
-    constexpr size_t kMaxEntries = 64;
-    static std::mutex mu;
-    static std::vector<Entry> cache;
-    std::lock_guard<std::mutex> lock(mu);
-    for (const Entry &e : cache)
-        if (e.dev == dev && e.q == q && e.Hq == Hq && e.rows == rows && e.D == D && e.gq == gq && e.nq == nq) {
-            *map = e.map;
-            return true;
-        }
-    if (!encode_q_map(map, q, Hq, rows, D, gq, nq)) return false;
-    if (cache.size() >= kMaxEntries) cache.erase(cache.begin());
-    cache.push_back(Entry{dev, q, Hq, rows, D, gq, nq, *map});
-    return true;
-}
-
 // cudaFuncSetAttribute once per device and kernel variant (it is a host-side
 // driver call; repeating it on every launch costs microseconds).  Keyed on
 // <D, G, FP8, QS, TC5>: every variant has the same function-pointer type, so
@@ -2366,21 +2393,16 @@ pkv_status launch_decode(LaunchArgs &a)
     }
     if (grid > kMaxSlots) grid = kMaxSlots;
 
-    CUtensorMap kmap, vmap, qmap;
+    CUtensorMap kmap, vmap;
     const int64_t rows = int64_t(p.NB) * p.bs;
     if (!cached_cache_map(&kmap, a.device, a.k_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok) ||
         !cached_cache_map(&vmap, a.device, a.v_cache, FP8, D, p.Hkv, rows, p.hg, p.boxtok))
         return PKV_ECUDA;
-    if constexpr (TC5) {
-        if (!cached_q_map(&qmap, a.device, p.q, p.Hq, p.B, D, p.gq, team_warps(G) * p.qn)) return PKV_ECUDA;
-    } else {
-        qmap = kmap;  // not read
-    }
 
     auto kern = paged_decode_kernel<D, G, FP8, QS, TC5>;
     if (!ensure_smem_attribute<D, G, FP8, QS, TC5>(kern, a.device, lay.total)) return PKV_ECUDA;
     const cudaError_t e =
-        launch_pdl(kern, dim3(grid), dim3((p.cons + 1) * 32), lay.total, a.stream, kmap, vmap, qmap, p);
+        launch_pdl(kern, dim3(grid), dim3((p.cons + 1) * 32), lay.total, a.stream, kmap, vmap, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return cuda_fail("paged_decode_kernel launch", e);
