@@ -452,25 +452,37 @@ __device__ __forceinline__ uint32_t swizzled_chunk(uint32_t c, uint32_t R)
 // 2i + (lane / 8) % 2 of the row.  Matrix q of an .x4 load is then
 // (tokens 0-7 | 8-15 of the sub-tile) x (chunk 2i | 2i + 1) for q = 0 (0-7, 2i),
 // 1 (0-7, 2i+1), 2 (8-15, 2i), 3 (8-15, 2i+1).
+// Kept factored (a few registers instead of NT x NCP): chunk pair i lies in
+// row part i / (RB / 32) (part stride boxtok RB bytes), and since boxtok is a
+// multiple of 8 the swizzle key of its row is that of the token alone, so the
+// piece's chunk is ((i % (RB / 32)) << 5) ^ kx.
 template <int D, bool FP8, bool QS>
-__device__ __forceinline__ void lane_offsets(uint32_t (&off)[Tc<D, FP8, QS>::NT][Tc<D, FP8, QS>::NCP], int lane,
-                                             int j, int h, int hg, int boxtok)
+struct LaneOffsets {
+    using T = Tc<D, FP8, QS>;
+    uint32_t base[T::NT];  // row of the sub-tile's token, part 0, chunk 0
+    uint32_t part;         // bytes between a row's parts
+    uint32_t kx;           // the lane's chunk bit and the row's swizzle key, as a byte offset
+    __device__ __forceinline__ uint32_t at(int st, int i) const
+    {
+        constexpr int per = T::RB / 32;  // chunk pairs per part
+        return base[st] + uint32_t(i / per) * part + ((uint32_t(i % per) << 5) ^ kx);
+    }
+};
+
+template <int D, bool FP8, bool QS>
+__device__ __forceinline__ void lane_offsets(LaneOffsets<D, FP8, QS> &off, int lane, int j, int h, int hg, int boxtok)
 {
     using T = Tc<D, FP8, QS>;
     const int tl = ((lane >> 4) << 3) | (lane & 7), e = (lane >> 3) & 1;
     const int lg = __ffs(boxtok) - 1;
     const uint32_t box_bytes = uint32_t(boxtok * hg * T::ROWB);
+    off.part = uint32_t(boxtok * T::RB);
 #pragma unroll
     for (int st = 0; st < T::NT; ++st) {
         const int t = j * T::TW + 16 * st + tl;
         const int bi = t >> lg, r = t & (boxtok - 1);
-#pragma unroll
-        for (int i = 0; i < T::NCP; ++i) {
-            const int gc = 2 * i + e;
-            const int pp = gc / (T::RB / 16), cc = gc % (T::RB / 16);
-            const uint32_t R = uint32_t((h * T::NP + pp) * boxtok + r);
-            off[st][i] = uint32_t(bi) * box_bytes + R * T::RB + (swizzled_chunk<T::RB>(uint32_t(cc), R) << 4);
-        }
+        off.base[st] = uint32_t(bi) * box_bytes + uint32_t(h * T::NP * boxtok + r) * T::RB;
+        if (st == 0) off.kx = uint32_t(e ^ (T::RB == 128 ? (r & 7) : ((r >> 1) & 3))) << 4;  // the same for every st
     }
 }
 
@@ -522,7 +534,7 @@ __device__ __forceinline__ uint32_t f16x2_sat(float lo, float hi)
 // applied by the caller.
 template <int D, bool FP8, bool QS, int HR_, bool TAIL>
 __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
-                                            const uint32_t (&off)[Tc<D, FP8, QS, HR_>::NT][Tc<D, FP8, QS, HR_>::NCP],
+                                            const LaneOffsets<D, FP8, QS> &off,
                                             const uint32_t (&qa)[Tc<D, FP8, QS, HR_>::KS][2 * Tc<D, FP8, QS, HR_>::HR],
                                             float ksc, const int (&lim)[Tc<D, FP8, QS, HR_>::HR], int valid,
                                             float (&m)[Tc<D, FP8, QS, HR_>::HR], float (&l)[Tc<D, FP8, QS, HR_>::HR],
@@ -530,7 +542,9 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
 {
     using T = Tc<D, FP8, QS, HR_>;
     constexpr int NT = T::NT, HR = T::HR;
-    constexpr int CH = NT == 1 ? 2 : 1;  // accumulation chains per n-tile (bf16: halves the MMA dependency depth)
+    // accumulation chains per n-tile (bf16: halves the MMA dependency depth; not with 16 rows, whose
+    // registers would spill at D = 128)
+    constexpr int CH = NT == 1 && HR == 1 ? 2 : 1;
     const int r4 = lane & 3;
     // A operand of k-step ks: rows g (qa[ks][0], [1]) and g + 8 (qa[ks][2], [3], zero when HR = 1)
     auto a1 = [&](int ks) { return HR == 2 ? qa[ks][2 % (2 * HR)] : 0u; };
@@ -549,7 +563,7 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
 #pragma unroll
         for (int st = 0; st < NT; ++st) {
             uint32_t r0, r1, r2, r3;
-            ldsm_x4(kb + off[st][i], r0, r1, r2, r3);
+            ldsm_x4(kb + off.at(st, i), r0, r1, r2, r3);
             if constexpr (!FP8) {
                 // chunks 2i, 2i+1 = dims 16i..16i+15 = k-step i; r0/r1 tokens 0-7, r2/r3 tokens 8-15
                 mma_bf16_16816(sa[st][i % CH][0], qa[i][0], a1(i), qa[i][1], a3(i), r0, r1);
@@ -573,8 +587,7 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
     }
     // the thread's scores: row g (half 0, fragment elements c0, c1) and row g + 8 (half 1, c2, c3),
     // tokens 16 st + 8 nt + 2 r4 + e
-    float x[HR][NT * 4];
-    bool ok[HR][NT * 4];
+    float x[HR][NT * 4];  // -inf past the row's bound
 #pragma unroll
     for (int hr = 0; hr < HR; ++hr)
 #pragma unroll
@@ -586,8 +599,7 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
                     const int k = 4 * st + 2 * nt + e;
                     float sum = sa[st][0][nt][2 * hr + e];
                     if constexpr (CH == 2) sum += sa[st][1][nt][2 * hr + e];
-                    ok[hr][k] = 16 * st + 8 * nt + 2 * r4 + e < lim[hr];
-                    x[hr][k] = ok[hr][k] ? sum * ksc : -INFINITY;
+                    x[hr][k] = 16 * st + 8 * nt + 2 * r4 + e < lim[hr] ? sum * ksc : -INFINITY;
                 }
     float mx[HR];
     bool grow = false;
@@ -628,9 +640,11 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
     uint32_t pb[HR][NT][2], pl[HR][NT][2];
 #pragma unroll
     for (int hr = 0; hr < HR; ++hr) {
+        // 2^(-inf) = 0 for the masked tokens; a row without any valid token so far (m = -inf) takes 0
+        const float mr = m[hr] == -INFINITY ? 0.f : m[hr];
         float pr[NT * 4];
 #pragma unroll
-        for (int k = 0; k < NT * 4; ++k) pr[k] = ok[hr][k] ? ex2(x[hr][k] - m[hr]) : 0.f;
+        for (int k = 0; k < NT * 4; ++k) pr[k] = ex2(x[hr][k] - mr);
         float ps = 0.f;
 #pragma unroll
         for (int k = 0; k < NT * 4; ++k) ps += pr[k];
@@ -664,7 +678,7 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb,
 #pragma unroll
         for (int i = 0; i < T::NCP; ++i) {
             uint32_t r0, r1, r2, r3;
-            ldsm_x4_t(vb + off[st][i], r0, r1, r2, r3);
+            ldsm_x4_t(vb + off.at(st, i), r0, r1, r2, r3);
             if constexpr (TAIL) {
                 r0 &= keep0;
                 r1 &= keep0;
@@ -1126,7 +1140,7 @@ __device__ void tc5_mma_warp(const DecodeParams &p, const CtaLayout &lay, const 
         for (uint32_t it = 0;; ++it) {
             bool progress = false;
             // K slots of units whose scores (and meta) the softmax warps have read
-            if (nrel < ns && mbar_try_wait(smem_u32(&m.sfree[nrel & 1u]), (nrel >> 1) & 1u)) {
+            if (nrel < ns && mbar_test_wait(smem_u32(&m.sfree[nrel & 1u]), (nrel >> 1) & 1u)) {
                 mbar_arrive(&m.empty[slot_of[nrel & 3u]]);
                 ++nrel;
                 progress = true;
@@ -1135,14 +1149,14 @@ __device__ void tc5_mma_warp(const DecodeParams &p, const CtaLayout &lay, const 
             // score buffer free (the output product of unit ns - 2 done); at most two units ahead of the
             // output products and one ahead of the K slot releases
             if (!ended && ns < npv + 2 && nrel + 1 >= ns) {
-                if (!have_meta && mbar_try_wait(smem_u32(&m.full[s]), ph)) {
+                if (!have_meta && mbar_test_wait(smem_u32(&m.full[s]), ph)) {
                     have_meta = true;
                     flags = m.metas[s].flags;
                     if (m.metas[s].b < 0) ended = true;
                 }
                 if (have_meta && !ended) {
-                    const bool qok = !(flags & kFirst) || mbar_try_wait(smem_u32(m.qready), segs & 1u);
-                    const bool bok = ns < 2 || mbar_try_wait(smem_u32(&m.odone[ns & 1u]), ((ns >> 1) - 1) & 1u);
+                    const bool qok = !(flags & kFirst) || mbar_test_wait(smem_u32(m.qready), segs & 1u);
+                    const bool bok = ns < 2 || mbar_test_wait(smem_u32(&m.odone[ns & 1u]), ((ns >> 1) - 1) & 1u);
                     if (qok && bok) {
                         if (flags & kFirst) ++segs;
                         tc_fence_after();
@@ -1168,8 +1182,8 @@ __device__ void tc5_mma_warp(const DecodeParams &p, const CtaLayout &lay, const 
                 }
             }
             // the next output product, once its weights are written and its V slot has landed
-            if (npv < ns && mbar_try_wait(smem_u32(&m.pfull[npv & 1u]), (npv >> 1) & 1u) &&
-                mbar_try_wait(smem_u32(&m.vfull[npv % kTc5VSlots]), (npv / kTc5VSlots) & 1u)) {
+            if (npv < ns && mbar_test_wait(smem_u32(&m.pfull[npv & 1u]), (npv >> 1) & 1u) &&
+                mbar_test_wait(smem_u32(&m.vfull[npv % kTc5VSlots]), (npv / kTc5VSlots) & 1u)) {
                 tc5_output_product<D>(lay, m, tmem, npv, first_of[npv & 1u]);
                 ++npv;
                 progress = true;
@@ -1384,16 +1398,15 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
         const uint32_t sbuf = tlane + (j & 1u) * 128u;  // the unit's score buffer (and then its weights)
         // raw scores s of the half's keys (at or past the row's bound: -inf); weights 2^(s c - m)
         float x[KH];
+        {
+            uint32_t r[KH];
+            tmem_ld64(sbuf + uint32_t(KH * half), r);
+            if (lim >= KH) {
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            uint32_t r[32];
-            tmem_ld32(sbuf + uint32_t(KH * half + 32 * h2), r);
-            if (lim >= 32 * (h2 + 1)) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[32 * h2 + i] = __uint_as_float(r[i]);
+                for (int i = 0; i < KH; ++i) x[i] = __uint_as_float(r[i]);
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[32 * h2 + i] = 32 * h2 + i < lim ? __uint_as_float(r[i]) : -INFINITY;
+                for (int i = 0; i < KH; ++i) x[i] = i < lim ? __uint_as_float(r[i]) : -INFINITY;
             }
         }
         tc_fence_before();
@@ -1944,7 +1957,7 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
     const int jq = QS ? j : 0;                         // block of qn queries of the entry
     const int g8 = lane >> 2, r4 = lane & 3;           // fragment row group and column pair of the thread
     const int home = sh[0];
-    uint32_t off[TC::NT][TC::NCP];
+    LaneOffsets<D, FP8, QS> off;
     lane_offsets<D, FP8, QS>(off, lane, jt, h, p.hg, p.boxtok);
     const uint32_t stage_addr = smem_u32(stage0);
     constexpr int HR = TC::HR;  // halves of the MMA tile's rows that hold virtual heads
