@@ -492,8 +492,8 @@ def run_pkv(args):
             per_query = int(sum(L - npf + 1 + i for L in lens_h for i in range(npf))) * row
             mixed = dict(mixed or {})
             mixed["prefill_chunk"] = {
-                "kernel": "pkv_paged_attention (expand_rows_kernel + paged_decode_kernel query-split, %d queries "
-                          "share each K/V pass)" % qe,
+                "kernel": "pkv_paged_attention (expand_rows_kernel + paged_decode_kernel on tensor-memory "
+                          "query-split CTAs (tcgen05.mma, 128 rows per tile), %d queries share each K/V pass)" % qe,
                 "query_rows": B * npf, "new_tokens_per_sequence": npf, "mean_call_us": round(us_p, 2),
                 "chunk_streamed_kv_bytes": chunk_rows, "per_query_kv_bytes": per_query,
                 "chunk_streamed_gbs": round(chunk_rows / (us_p * 1e-6) / 1e9, 1),

@@ -27,12 +27,16 @@
 //  * A consumer serves all G query heads of its kv head from one K/V read,
 //    on the warp-level tensor cores: S^T = Q K^T and O^T += V^T P^T as
 //    m16n8k16 MMAs with fp32 accumulators, K and V fed by ldmatrix from the
-//    swizzled stage, P kept in registers (see attend_tile); up to 16 virtual
-//    heads (queries x heads) fill the tile's two 8-row halves; the online
-//    softmax rescales only when a score passes the running max by a slack,
-//    and exponentials are ex2 of log2e-prescaled scores.  Query-split CTAs
-//    (QS) instead give every warp all tokens of one kv head and its own
-//    queries: long runs of new tokens share K/V passes.
+//    swizzled stage, P kept in registers as two bf16 parts (see attend_tile);
+//    up to 16 virtual heads (queries x heads) fill the tile's two 8-row
+//    halves; the online softmax rescales only when a score passes the running
+//    max by a slack, and exponentials are ex2 of log2e-prescaled scores.
+//    Query-split CTAs (QS) instead give every warp all tokens of one kv head
+//    and its own queries: long runs of new tokens share K/V passes.  Their
+//    tensor-memory variant (TC5) runs a 128-row entry against 128-key tiles
+//    on the 5th-generation tensor cores: tcgen05.mma issued by one thread,
+//    scores, weights and output in tensor memory, 8 softmax warps (see
+//    tc5_softmax_warps).
 //  * The decode step's store can run in the same launch: the tile holding a
 //    sequence's new token takes its K/V row from the step's inputs and writes
 //    it to the cache (see DecodeParams::k_new).
@@ -47,7 +51,8 @@
 // This header holds the kernel and its launch templates; pkv_decode.cu
 // instantiates the bf16-cache kernels for up to 8 virtual heads and defines
 // the C entry points, pkv_decode_wide.cu the bf16 ones for 9 to 16,
-// pkv_decode_qs.cu the query-split ones, pkv_decode_fp8.cu the E4M3 ones.
+// pkv_decode_qs.cu the query-split ones, pkv_decode_tc5.cu their tensor-memory
+// variant, pkv_decode_fp8.cu the E4M3 ones.
 #pragma once
 #include <cuda_fp16.h>
 
