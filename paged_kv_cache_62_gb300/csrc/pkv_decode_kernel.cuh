@@ -949,7 +949,10 @@ static __device__ int claim_leftover(const DecodeParams &p, uint32_t gen, const 
 __device__ __forceinline__ int arrive_last(unsigned long long *ctr, uint32_t gen, uint32_t units, uint32_t total,
                                            int32_t *err)
 {
-    unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(ctr);
+    // first guess: the counter is at rest (0: the merge of the previous call reset it, or the workspace is
+    // new), so the first arrival of a segment takes one round trip; any other value comes back from the
+    // failed exchange and the loop goes on from it
+    unsigned long long cur = 0ull;
     for (int it = 0; it < (1 << 20); ++it) {
         const uint32_t n = ((uint32_t(cur >> 32) == gen) ? uint32_t(cur) : 0u) + units;
         const unsigned long long next = (static_cast<unsigned long long>(gen) << 32) | n;
