@@ -243,8 +243,10 @@ def run_metadata(dev) -> dict:
 
 
 def config_block(name, dev, rank, peak, warmup):
-    """One workload's decode step (pkv_paged_decode_store per layer), timed per launch with CUDA events after
-    `warmup` steps, and as one captured CUDA graph replayed back to back."""
+    """One workload's decode step (pkv_paged_decode_store per layer, issued through pkv.DecodeStoreStep, the
+    binding a serving loop keeps across steps), after `warmup` steps: back to back (CUDA events around all the
+    steps), per launch with CUDA events around each (the event pairs themselves add a few microseconds to a
+    short launch), and as one captured CUDA graph replayed back to back."""
     from paged_kv_cache_62_gb300 import pkv, workloads
     wl = workloads.make(name, dev, seed=rank_seed(name, rank))
     s = wl.spec
@@ -256,30 +258,34 @@ def config_block(name, dev, rank, peak, warmup):
     stream = torch.cuda.current_stream(dev)
     k_step = [lay.k_new[:B].contiguous() for lay in wl.layers]
     v_step = [lay.v_new[:B].contiguous() for lay in wl.layers]
+    bound = [pkv.DecodeStoreStep(lay.q, k_step[li], v_step[li], lay.k_cache, lay.v_cache, wl.block_tables,
+                                 wl.context_lens, wl.scale, outs[li], ws, max_context_len=max_ctx, err_word=err)
+             for li, lay in enumerate(wl.layers)]
 
     def step(evs=None, st=None):
-        st = stream if st is None else st
-        for li, lay in enumerate(wl.layers):
+        h = (stream if st is None else st).cuda_stream
+        for li in range(len(bound)):
             if evs is not None:
-                evs[li][0].record(st)
-            pkv.paged_decode_store(lay.q, k_step[li], v_step[li], lay.k_cache, lay.v_cache, wl.block_tables,
-                                   wl.context_lens, wl.scale, outs[li], ws, max_context_len=max_ctx, err_word=err,
-                                   stream=st)
+                evs[li][0].record(st if st is not None else stream)
+            bound[li].run(h)
             if evs is not None:
-                evs[li][1].record(st)
+                evs[li][1].record(st if st is not None else stream)
 
     nl = len(wl.layers)
     n_steps = 300 if nl == 1 else 12
     warm_up(step, max(warmup, 3), 0.1)
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nl)]
-           for _ in range(n_steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(n_steps):
-        step(evs[i])
+        step()
     t1.record(stream)
     torch.cuda.synchronize()
     step_ms = t0.elapsed_time(t1) / n_steps
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nl)]
+           for _ in range(n_steps)]
+    for i in range(n_steps):
+        step(evs[i])
+    torch.cuda.synchronize()
     per = [a.elapsed_time(b) * 1e3 for row in evs for (a, b) in row]
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
@@ -299,7 +305,7 @@ def config_block(name, dev, rank, peak, warmup):
     dist = launch_distribution(per)
     res = {"workload": s.description, "layers": nl, "batch": B, "launches_per_step": nl,
            "algorithmic_bytes_per_launch": nb["fused"], "algorithmic_bytes_per_step": nb["step"],
-           "launch_us": dist,
+           "launch_us": dist, "back_to_back_launch_us": round(step_ms * 1e3 / nl, 2),
            "launch_gbs_median": round(nb["fused"] / (dist["median_us"] * 1e-6) / 1e9, 1),
            "launch_frac_median": round(nb["fused"] / (dist["median_us"] * 1e-6) / 1e9 / peak, 4),
            "step_ms": round(step_ms, 5), "step_gbs": round(nb["step"] / (step_ms * 1e-3) / 1e9, 1),

@@ -72,6 +72,7 @@ namespace pkv {
 
 constexpr int kMaxStages = 16;    // ring depth (as many as fit: 3 of 64 KiB, 12 of 16 KiB)
 constexpr int kMaxSlots = 512;    // slices: SM ids (adaptive) or CTAs (fixed split)
+constexpr int kSegmentUnits = 8;  // small calls: one CTA per segment when no segment has more units
 constexpr uint32_t kTableMagic = 0x62616c31u;
 constexpr uint32_t kEpochMagic = 0x65706f63u;
 constexpr int32_t kHintMagic = 0x6869;
@@ -156,6 +157,7 @@ struct DecodeParams {
     int32_t boxtok, nbox;        // tokens per TMA box (min(toks, bs)) and boxes per unit
     int32_t nst, cons, lg_nbox;  // ring stages, consumer warps (hg * sub), log2(nbox)
     int32_t num_workers;         // > 0: fixed split over about num_workers / consumers CTAs; 0: adaptive
+    int32_t per_segment;         // fixed split with one slice per (entry, head group): no split-K pieces
     float scale_log2;            // scale * log2(e)
     const float *k_scale, *v_scale;  // E4M3 caches: per-kv-head scales (unused for bf16 caches)
     const int32_t *row_seq;          // several query rows per sequence: row -> the sequence whose table it
@@ -1692,7 +1694,20 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
                 uint4 *o = reinterpret_cast<uint4 *>(p.out + int64_t(b) * p.qstride * p.Hq * D);
                 for (int i = threadIdx.x; i < rows * p.Hq * D / 8; i += nset) o[i] = make_uint4(0u, 0u, 0u, 0u);
             }
-        build_partition(p, gen, adaptive, nslots, T, bound, wts, red, bal_in, nset);
+        if (p.per_segment) {
+            // slice i = segment (entry i / nhg, group i % nhg), whole: the grid has one CTA per segment
+            for (int i = threadIdx.x; i <= nslots; i += nset) {
+                long long x = T;
+                if (i < nslots && i < p.B * p.nhg) {
+                    const int b = i / p.nhg, g = i - b * p.nhg;
+                    x = (long long)p.nhg * scan[b] + (long long)g * (scan[b + 1] - scan[b]);
+                }
+                bound[i] = x;
+            }
+            setup_sync(nset);
+        } else {
+            build_partition(p, gen, adaptive, nslots, T, bound, wts, red, bal_in, nset);
+        }
     }
     if constexpr (TC5) tc_fence_before();
     __syncthreads();

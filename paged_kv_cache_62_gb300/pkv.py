@@ -206,6 +206,52 @@ def paged_decode_store(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor
         "pkv_paged_decode_store")
 
 
+class DecodeStoreStep:
+    """A decode step (paged_decode_store) bound to persistent buffers: the arguments are checked once, here,
+    and run() issues the C call with them, so a serving loop that reuses its buffers step after step (as a
+    CUDA-graph engine does) pays no per-call checks.  The buffers' contents may change between runs; their
+    shapes, dtypes and addresses may not (make a new step for new buffers).  max_context_len must bound every
+    run's context_lens (run() takes a new bound)."""
+
+    _MAXLEN = 14  # position of max_context_len in pkv_paged_decode_store's arguments
+
+    def __init__(self, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
+                 slot_mapping=None, max_context_len=None, num_workers=0, err_word=None):
+        B, Hq, D = q.shape
+        NB, bs, Hkv, D2 = k_cache.shape
+        if D2 != D or v_cache.shape != k_cache.shape or block_tables.shape[0] != B or context_lens.numel() != B \
+                or out.shape != q.shape or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) \
+                or (slot_mapping is not None and slot_mapping.numel() != B):
+            raise ValueError("DecodeStoreStep: shape mismatch")
+        mb = block_tables.shape[1]
+        if max_context_len is None:
+            max_context_len = mb * bs
+        if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+            raise ValueError("workspace must be a CUDA uint8 tensor")
+        self._fn = load().pkv_paged_decode_store
+        self._args = [
+            _dev(q, torch.bfloat16, "q", 3), _dev(k_new, torch.bfloat16, "k_new", 3),
+            _dev(v_new, torch.bfloat16, "v_new", 3), _dev(k_cache, torch.bfloat16, "k_cache", 4),
+            _dev(v_cache, torch.bfloat16, "v_cache", 4), _dev(block_tables, torch.int32, "block_tables", 2), mb,
+            _dev(context_lens, torch.int32, "context_lens", 1), B, Hq, Hkv, D, bs, NB, int(max_context_len),
+            float(scale), _dev(out, torch.bfloat16, "out", 3),
+            None if slot_mapping is None else _dev(slot_mapping, torch.int32, "slot_mapping", 1),
+            workspace.data_ptr(), workspace.numel(), int(num_workers), _opt(err_word)]
+        # the tensors stay referenced as long as the step exists
+        self._keep = (q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out, workspace, slot_mapping,
+                      err_word)
+
+    def run(self, stream=None, max_context_len: int | None = None) -> None:
+        """Issue the step on `stream` (a torch stream, a raw cudaStream_t handle as an int, or None for the
+        current stream)."""
+        if max_context_len is not None:
+            self._args[self._MAXLEN] = int(max_context_len)
+        st = stream if isinstance(stream, int) else _stream(stream)
+        status = self._fn(*self._args, st)
+        if status != OK:
+            raise PkvError(status, "pkv_paged_decode_store")
+
+
 def paged_decode_store_fp8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
                            v_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
                            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, out: torch.Tensor,

@@ -128,6 +128,16 @@ def test_binding_refuses_cpu_tensors(lib):
                          torch.zeros(2, dtype=torch.int32), 0.1, torch.empty_like(q), torch.empty(16, dtype=torch.uint8))
 
 
+def test_bound_step_refuses_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    t = torch.zeros(2, 4, 64, dtype=torch.bfloat16)
+    kv = torch.zeros(2, 2, 64, dtype=torch.bfloat16)
+    cache = torch.zeros(8, 16, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pkv.DecodeStoreStep(t, kv, kv, cache, cache, torch.zeros(2, 4, dtype=torch.int32),
+                            torch.zeros(2, dtype=torch.int32), 0.1, t.clone(), torch.zeros(64, dtype=torch.uint8))
+
+
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         pkv.load(str(tmp_path / "libpkv.so"))

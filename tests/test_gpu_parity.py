@@ -169,6 +169,46 @@ def test_decode_and_store_in_one_launch(name):
     assert torch.all(out[B // 2].float() == 0)
 
 
+@pytest.mark.parametrize("name", ["tiny", "qwen25_0p5b"])
+def test_bound_decode_step_matches_the_call(name):
+    """DecodeStoreStep (the step bound to its buffers once) issues the same pkv_paged_decode_store: over three
+    steps whose buffer contents change in place (new q and new K/V rows, lengths grown by one), its outputs and
+    caches equal those of paged_decode_store run on copies of the same buffers, bit for bit (fixed split)."""
+    wl = W.make(name, "cuda", layers=1)
+    s, lay = wl.spec, wl.layers[0]
+    B, Hq, Hkv, D = s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim
+    q = lay.q.clone()
+    k_new, v_new = lay.k_new[:B].contiguous(), lay.v_new[:B].contiguous()
+    lens = (wl.context_lens - 3).clamp(min=0)  # three steps bring them back to the workload's lengths
+    caches = [(lay.k_cache.clone(), lay.v_cache.clone()) for _ in range(2)]
+    outs = [torch.full_like(q, float("nan")) for _ in range(2)]
+    wss = [torch.zeros(pkv.paged_decode_workspace_size(B, Hq, Hkv, D), dtype=torch.uint8, device="cuda")
+           for _ in range(2)]
+    err = err_word()
+    cap = int(wl.context_lens.max())
+    step = pkv.DecodeStoreStep(q, k_new, v_new, caches[0][0], caches[0][1], wl.block_tables, lens, wl.scale,
+                               outs[0], wss[0], max_context_len=cap, num_workers=64, err_word=err)
+    g = torch.Generator(device="cuda").manual_seed(3)
+    for i in range(3):
+        lens += (lens > 0).int()
+        q.copy_(torch.randn(q.shape, generator=g, device="cuda").bfloat16())
+        k_new.copy_(torch.randn(k_new.shape, generator=g, device="cuda").bfloat16())
+        v_new.copy_(torch.randn(v_new.shape, generator=g, device="cuda").bfloat16())
+        step.run()
+        pkv.paged_decode_store(q, k_new, v_new, caches[1][0], caches[1][1], wl.block_tables, lens, wl.scale,
+                               outs[1], wss[1], max_context_len=cap, num_workers=64, err_word=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0, hex(err.item())
+        assert torch.equal(outs[0], outs[1]), f"{name} step {i}"
+        # (bit patterns: the pools hold NaN canaries, which torch.equal never calls equal)
+        assert np.array_equal(W.bits(caches[0][0]), W.bits(caches[1][0]))
+        assert np.array_equal(W.bits(caches[0][1]), W.bits(caches[1][1]))
+    lens_h = lens.cpu().numpy()
+    want = oracle.paged_decode(W.bits(q), W.bits(caches[1][0]), W.bits(caches[1][1]), wl.block_tables.cpu().numpy(),
+                               lens_h, wl.scale, nthreads=NTHREADS)
+    check_close(outs[0], want, name)
+
+
 @pytest.mark.parametrize("workers", [1, 7, 333])
 def test_decode_and_store_split_over_workers(workers):
     """The fused store where the new token's unit lands in a later slice than the sequence's first
