@@ -199,6 +199,28 @@ def launch_distribution(us):
             "first5_mean_us": round(float(a[:5].mean()), 2), "last5_mean_us": round(float(a[-5:].mean()), 2)}
 
 
+def time_calls(call, reps: int, stream) -> tuple[float, float]:
+    """Mean us per call of `call`, issued `reps` times back to back with CUDA events around the whole run
+    (as a loop issues it), then mean us with an event pair around every call (the pairs cut the overlap of
+    a launch's set-up with the previous launch's tail).  Five untimed calls come first."""
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(reps):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for c0, c1 in evs:
+        c0.record(stream)
+        call()
+        c1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) * 1e3 / reps, float(np.mean([c0.elapsed_time(c1) for c0, c1 in evs])) * 1e3
+
+
 def source_sha() -> str:
     """SHA-256 over every library source and the public header (the product as built), in sorted order."""
     csrc = os.path.join(ROOT, "paged_kv_cache_62_gb300", "csrc")
@@ -450,7 +472,7 @@ def run_pkv(args):
 
         def time_attention(nq, offsets, reps):
             """Mean us of a pkv_paged_attention call with nq new tokens per sequence (given by offsets, or
-            as new_per_seq = nq)."""
+            as new_per_seq = nq), back to back (and with an event pair around each call)."""
             cu = torch.arange(0, (B + 1) * nq, nq, dtype=torch.int32, device=dev) if offsets else None
             qa = torch.randn(B * nq, Hq, D, device=dev).bfloat16()
             oa = torch.empty_like(qa)
@@ -460,27 +482,20 @@ def run_pkv(args):
                 pkv.paged_attention(qa, lay0.k_cache, lay0.v_cache, wl.block_tables, cu, wl.context_lens, wl.scale,
                                     oa, wsa, max_context_len=max_ctx, err_word=err, stream=stream,
                                     new_per_seq=0 if offsets else nq)
-            for _ in range(5):
-                call()
-            torch.cuda.synchronize()
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-            for c0, c1 in evs:
-                c0.record(stream)
-                call()
-                c1.record(stream)
-            torch.cuda.synchronize()
+            us, us_ev = time_calls(call, reps, stream)
             assert err.item() == 0, f"device error word {err.item():#x}"
-            return float(np.mean([c0.elapsed_time(c1) for c0, c1 in evs])) * 1e3
+            return us, us_ev
 
         nq = 4
         if lens_h.min() >= nq:
             # a speculative-decoding verify step: the 4 queries of a sequence as 4 x G virtual heads
-            us_m = time_attention(nq, False, 50)
+            us_m, us_m_ev = time_attention(nq, False, 50)
             unique = int(lens_h.sum()) * row
             streamed = int(sum(L - nq + 1 + i for L in lens_h for i in range(nq))) * row
             mixed = {"kernel": "pkv_paged_attention (paged_decode_kernel, the 4 queries of a sequence as 4 x G "
                                "virtual heads over one pass of its keys)",
                      "query_rows": B * nq, "new_tokens_per_sequence": nq, "mean_call_us": round(us_m, 2),
+                     "event_pair_mean_call_us": round(us_m_ev, 2),
                      "unique_kv_bytes": unique, "streamed_kv_bytes": streamed,
                      "unique_gbs": round(unique / (us_m * 1e-6) / 1e9, 1),
                      "streamed_gbs": round(streamed / (us_m * 1e-6) / 1e9, 1),
@@ -489,19 +504,19 @@ def run_pkv(args):
         nv = 8
         if lens_h.min() >= nv:
             # a verify step with the offsets given: chunks of max(1, 16 // G) queries on regular CTAs
-            us_v = time_attention(nv, True, 50)
+            us_v, us_v_ev = time_attention(nv, True, 50)
             unique = int(lens_h.sum()) * row
             mixed = dict(mixed or {})
             mixed["verify_offsets"] = {
                 "kernel": "pkv_paged_attention (expand_rows_kernel + paged_decode_kernel, chunks of up to "
                           "16 / G queries)", "query_rows": B * nv, "new_tokens_per_sequence": nv,
-                "mean_call_us": round(us_v, 2), "unique_kv_bytes": unique,
+                "mean_call_us": round(us_v, 2), "event_pair_mean_call_us": round(us_v_ev, 2), "unique_kv_bytes": unique,
                 "unique_gbs": round(unique / (us_v * 1e-6) / 1e9, 1)}
         npf = 64
         if lens_h.min() >= npf and B * npf <= 16384:
             # the last npf tokens of every sequence as one prefill chunk over its cached prefix (offsets
             # given): query-split CTAs, 8 x max(1, 16 // G) queries per K/V pass
-            us_p = time_attention(npf, True, 30)
+            us_p, us_p_ev = time_attention(npf, True, 30)
             qe = max(1, 16 // (Hq // Hkv)) * 8
             chunk_rows = int(sum(L - npf + min(c + qe, npf) for L in lens_h for c in range(0, npf, qe))) * row
             per_query = int(sum(L - npf + 1 + i for L in lens_h for i in range(npf))) * row
@@ -510,6 +525,7 @@ def run_pkv(args):
                 "kernel": "pkv_paged_attention (expand_rows_kernel + paged_decode_kernel on tensor-memory "
                           "query-split CTAs (tcgen05.mma, 128 rows per tile), %d queries share each K/V pass)" % qe,
                 "query_rows": B * npf, "new_tokens_per_sequence": npf, "mean_call_us": round(us_p, 2),
+                "event_pair_mean_call_us": round(us_p_ev, 2),
                 "chunk_streamed_kv_bytes": chunk_rows, "per_query_kv_bytes": per_query,
                 "chunk_streamed_gbs": round(chunk_rows / (us_p * 1e-6) / 1e9, 1),
                 "note": "the last %d tokens of every sequence as a prefill chunk over its cached prefix; "
@@ -526,21 +542,14 @@ def run_pkv(args):
     if n_cow >= 8:
         lay0 = wl.layers[0]
         cow_pairs = torch.from_numpy(np.stack([owned[:n_cow], free_ids[:n_cow]], 1).astype(np.int32)).to(dev)
-        for _ in range(3):
-            pkv.copy_blocks(lay0.k_cache, lay0.v_cache, cow_pairs, err, stream)
-        torch.cuda.synchronize()
-        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
-        for c0, c1 in cev:
-            c0.record(stream)
-            pkv.copy_blocks(lay0.k_cache, lay0.v_cache, cow_pairs, err, stream)
-            c1.record(stream)
-        torch.cuda.synchronize()
+        cow_us, cow_us_ev = time_calls(lambda: pkv.copy_blocks(lay0.k_cache, lay0.v_cache, cow_pairs, err, stream),
+                                       50, stream)
         assert err.item() == 0, f"device error word {err.item():#x}"
-        cow_us = float(np.mean([c0.elapsed_time(c1) for c0, c1 in cev])) * 1e3
         block_bytes = s.block_size * Hkv * D * 2
         cow_bytes = n_cow * 2 * block_bytes * 2  # K and V blocks, each read once and written once
         cow = {"kernel": "pkv_copy_blocks (copy_blocks_kernel)", "pairs": n_cow, "block_bytes": block_bytes,
                "bytes_per_launch": cow_bytes, "mean_launch_us": round(cow_us, 2),
+               "event_pair_mean_launch_us": round(cow_us_ev, 2),
                "achieved": round(cow_bytes / (cow_us * 1e-6) / 1e9, 1), "unit": "GB/s",
                "note": "bytes read + written; peak is the measured copy bandwidth (read + write)"}
 
@@ -560,22 +569,14 @@ def run_pkv(args):
         def dec8():
             pkv.paged_decode_fp8(lay0.q, kc8, vc8, ks8, vs8, wl.block_tables, wl.context_lens, wl.scale, out8,
                                  wsbuf, max_context_len=max_ctx, err_word=err, stream=stream)
-        for _ in range(5):
-            dec8()
-        torch.cuda.synchronize()
         n8 = max(20, min(args.steps, 500))
-        fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n8)]
-        for c0, c1 in fev:
-            c0.record(stream)
-            dec8()
-            c1.record(stream)
-        torch.cuda.synchronize()
+        us8, us8_ev = time_calls(dec8, n8, stream)
         assert err.item() == 0, f"device error word {err.item():#x}"
-        us8 = float(np.mean([c0.elapsed_time(c1) for c0, c1 in fev])) * 1e3
         nb0 = step_bytes(wl)
         bytes8 = nb0["decode"] - nb0["decode_kv_only"] // 2  # K/V at one byte an element
         fp8 = {"kernel": "pkv_paged_decode_fp8 (paged_decode_kernel, E4M3 caches)", "bytes_per_launch": bytes8,
-               "mean_launch_us": round(us8, 2), "achieved": round(bytes8 / (us8 * 1e-6) / 1e9, 1), "unit": "GB/s",
+               "mean_launch_us": round(us8, 2), "event_pair_mean_launch_us": round(us8_ev, 2),
+               "achieved": round(bytes8 / (us8 * 1e-6) / 1e9, 1), "unit": "GB/s",
                "seq_steps_per_sec_decode_only": round(B / (us8 * 1e-6), 1),
                "speedup_vs_bf16_decode": round(dec_mean_ms * 1e3 / us8, 3),
                "note": "layer 0 of the workload, caches quantised per kv head (scale = max|x| / 448)"}
