@@ -2004,6 +2004,23 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
     float vsc = 1.0f;  // E4M3 caches: the kv head's V scale, applied in the final division
     // fused store: this lane's 8 bytes of the new K / V row (4 bf16 elements, or 8 E4M3 codes)
     uint2 kn = make_uint2(0u, 0u), vn = make_uint2(0u, 0u);
+    // 16-row tiles hold twice the accumulators: their registers are short, so they load the new row only
+    // when its tile comes (one load's latency, once per segment of a decode with more than 8 query heads
+    // per kv head), instead of holding it from the segment's start
+    constexpr bool kLateNewRow = TC::HR == 2;
+    auto load_new_row = [&](const UnitMeta &m_, uint2 &k2, uint2 &v2) {
+        const long long row0 = ((long long)m_.b * p.Hkv + m_.g * p.hg + h) * D;
+        if constexpr (!FP8) {
+            k2 = __ldg(reinterpret_cast<const uint2 *>(p.k_new + row0 + lane * 4));
+            v2 = __ldg(reinterpret_cast<const uint2 *>(p.v_new + row0 + lane * 4));
+        } else {  // quantised as pkv_kv_store_fp8 does
+            const int kvh = m_.g * p.hg + h;
+            k2 = quantise8_e4m3(__ldg(reinterpret_cast<const uint4 *>(p.k_new + row0 + lane * 8)),
+                                __ldg(p.k_scale + kvh));
+            v2 = quantise8_e4m3(__ldg(reinterpret_cast<const uint4 *>(p.v_new + row0 + lane * 8)),
+                                __ldg(p.v_scale + kvh));
+        }
+    };
     int u_first = 0;
     for (;;) {
         if (!mbar_wait_bounded(&full[s], sph)) {
@@ -2023,20 +2040,9 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
                 if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
                 break;
             }
-            if constexpr (!QS) {
-                if (p.k_new && lane < TC::ROWB / 8) {  // the segment's new K/V row, used at its last tile
-                    const long long row0 = ((long long)mt.b * p.Hkv + mt.g * p.hg + h) * D;
-                    if constexpr (!FP8) {
-                        kn = __ldg(reinterpret_cast<const uint2 *>(p.k_new + row0 + lane * 4));
-                        vn = __ldg(reinterpret_cast<const uint2 *>(p.v_new + row0 + lane * 4));
-                    } else {  // quantised as pkv_kv_store_fp8 does
-                        const int kvh = mt.g * p.hg + h;
-                        kn = quantise8_e4m3(__ldg(reinterpret_cast<const uint4 *>(p.k_new + row0 + lane * 8)),
-                                            __ldg(p.k_scale + kvh));
-                        vn = quantise8_e4m3(__ldg(reinterpret_cast<const uint4 *>(p.v_new + row0 + lane * 8)),
-                                            __ldg(p.v_scale + kvh));
-                    }
-                }
+            if constexpr (!QS && !kLateNewRow) {
+                // the segment's new K/V row, used at its last tile (its load's latency hides until then)
+                if (p.k_new && lane < TC::ROWB / 8) load_new_row(mt, kn, vn);
             }
             nvh = max(0, min(p.qn, mt.cnt - jq * p.qn)) * p.gq;
             // Q operand fragments of rows g8 (qa[ks][0], [1]) and g8 + 8 (qa[ks][2], [3]; HR = 2), zero
@@ -2087,6 +2093,7 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
                 const int tl = mt.L - 1 - tok0;
                 if (p.k_new && mt.newrow >= 0 && tl >= 0 && tl < TC::TW) {
                     if (lane < TC::ROWB / 8) {
+                        if constexpr (kLateNewRow) load_new_row(mt, kn, vn);
                         const int t = jt * TC::TW + tl, lg = __ffs(p.boxtok) - 1;
                         const int bi = t >> lg, r = t & (p.boxtok - 1);
                         const int byte = lane * 8, pp = byte / TC::RB, within = byte % TC::RB;

@@ -209,18 +209,21 @@ def test_bound_decode_step_matches_the_call(name):
     check_close(outs[0], want, name)
 
 
-@pytest.mark.parametrize("workers", [1, 7, 333])
-def test_decode_and_store_split_over_workers(workers):
+@pytest.mark.parametrize("heads", [(16, 8), (32, 2), (24, 2)])
+@pytest.mark.parametrize("workers", [0, 1, 7, 333])
+def test_decode_and_store_split_over_workers(workers, heads):
     """The fused store where the new token's unit lands in a later slice than the sequence's first
-    units (forced splits), over block sizes 8 and 16 (several boxes per unit)."""
+    units (forced splits), over block sizes 8 and 16 (several boxes per unit); also with 16 and 12 query
+    heads per kv head (the 16-row tiles, which load the new row when its tile comes)."""
+    Hq, Hkv = heads
     for bs in (8, 16):
         lens = [1, 15, 16, 17, 300, 1024, 2, 513]
-        q, kc, vc, bt, lens_t = synth(len(lens), 0, 16, 8, 128, bs, seed=workers * 10 + bs, lens=lens)
-        g = torch.Generator(device="cuda").manual_seed(workers + bs)
-        k_new = torch.randn(len(lens), 8, 128, generator=g, device="cuda").bfloat16()
-        v_new = torch.randn(len(lens), 8, 128, generator=g, device="cuda").bfloat16()
+        q, kc, vc, bt, lens_t = synth(len(lens), 0, Hq, Hkv, 128, bs, seed=workers * 10 + bs + Hq, lens=lens)
+        g = torch.Generator(device="cuda").manual_seed(workers + bs + Hq)
+        k_new = torch.randn(len(lens), Hkv, 128, generator=g, device="cuda").bfloat16()
+        v_new = torch.randn(len(lens), Hkv, 128, generator=g, device="cuda").bfloat16()
         kc_h, vc_h = W.bits(kc), W.bits(vc)
-        ws = shared_workspace(len(lens), 16, 8, 128)
+        ws = shared_workspace(len(lens), Hq, Hkv, 128)
         out = torch.empty_like(q)
         err = err_word()
         pkv.paged_decode_store(q, k_new, v_new, kc, vc, bt, lens_t, 0.0884, out, ws, num_workers=workers, err_word=err)
@@ -231,7 +234,7 @@ def test_decode_and_store_split_over_workers(workers):
         assert np.array_equal(W.bits(kc), kc_h) and np.array_equal(W.bits(vc), vc_h)
         want = oracle.paged_decode(W.bits(q), kc_h, vc_h, bt.cpu().numpy(), np.asarray(lens, np.int32), 0.0884,
                                    nthreads=NTHREADS)
-        check_close(out, want, f"workers {workers} bs {bs}")
+        check_close(out, want, f"workers {workers} bs {bs} heads {heads}")
 
 
 # --------------------------------------------------------------------------- mini-vLLM-style matrix
