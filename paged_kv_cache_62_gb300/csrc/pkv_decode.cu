@@ -61,7 +61,7 @@ static pkv_status decode_call(bool fp8, bool qs, int32_t qn, const uint16_t *q, 
     DeviceInfo dev;
     if (!current_device_info(&dev)) return PKV_ECUDA;
 
-    LaunchArgs a;
+    LaunchArgs a{};  // every field starts at zero; those a call uses are set below
     DecodeParams &p = a.p;
     uint8_t *wsb = static_cast<uint8_t *>(workspace);
     p.q = q;
