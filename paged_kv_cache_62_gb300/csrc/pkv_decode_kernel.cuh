@@ -103,7 +103,7 @@ constexpr int kTc5Keys = 128;          // keys per tile (one unit): the N extent
 // the output (D <= 128 columns, from column 256); and two Q tiles of 64 columns from column 384 (row r of
 // the tile in lane r, dims 2c, 2c + 1 in column c).
 constexpr uint32_t kTc5Cols = 512, kTc5OCol = 256, kTc5QCol = 384;
-constexpr uint32_t kTc5SlabBytes = 128u * 128u;  // one 64-dim slab of 128 rows: the Q tile, or a stage's K or V
+constexpr uint32_t kTc5SlabBytes = 128u * 128u;  // one 64-dim slab of 128 rows of a K or V slot
 // The K tiles stream through a ring of nst slots (a slot is free again once its scores are read); the V
 // tiles through a ring of kTc5VSlots (free again once their output product is done).
 constexpr int kTc5VSlots = 3;
@@ -1718,7 +1718,7 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
         const uint64_t policy = policy_evict_first();
         const uint32_t box_bytes = uint32_t(p.boxtok * p.hg * D * ES);
         uint32_t kk = 0, segs = 0;  // units issued, q-ring uses
-        uint32_t vunits = 0;        // TC5: V halves issued
+        uint32_t vunits = 0;        // TC5: V tiles issued
         int rs = 0;                 // ring slot of unit kk (kk % nst, kept without a division)
         uint32_t rph = 0;           // parity of that slot's use (kk / nst) & 1
         bool dead = false;
