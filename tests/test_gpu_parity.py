@@ -209,6 +209,25 @@ def test_bound_decode_step_matches_the_call(name):
     check_close(outs[0], want, name)
 
 
+@pytest.mark.parametrize("lens", [[1, 15, 40, 96, 0, 128], [1, 15, 600, 700, 5, 0]])
+@pytest.mark.parametrize("heads", [(4, 2), (14, 2), (16, 8)])
+def test_small_calls_one_cta_per_segment_or_split(lens, heads):
+    """Calls with fewer units than SMs: when no (sequence, head group) segment has more than 8 units they
+    run one CTA per segment (no split-K pieces); a longer segment sends the call back to one CTA per unit
+    (pieces and merges).  Both against the oracle, with zero-length rows, on a workspace other calls used."""
+    Hq, Hkv = heads
+    for D, bs in ((64, 16), (128, 16)):
+        q, kc, vc, bt, lens_t = synth(len(lens), 0, Hq, Hkv, D, bs, seed=sum(lens) + Hq + D, lens=lens)
+        err = err_word()
+        out = run_decode(q, kc, vc, bt, lens_t, 0.1, max_ctx=max(lens), err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        check_close(out, oracle_of(q, kc, vc, bt, lens_t, 0.1), f"lens {lens} heads {heads} D {D}")
+        for b, L in enumerate(lens):
+            if L == 0:
+                assert torch.all(out[b].float() == 0)
+
+
 @pytest.mark.parametrize("heads", [(16, 8), (32, 2), (24, 2)])
 @pytest.mark.parametrize("workers", [0, 1, 7, 333])
 def test_decode_and_store_split_over_workers(workers, heads):
