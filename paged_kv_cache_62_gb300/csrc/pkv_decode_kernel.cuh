@@ -1080,8 +1080,8 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
 //                  row's running max m (the two halves exchange their tile max) and sum l (fp32 weights),
 //                  P written over its own scores in tensor memory (once both halves read theirs: the
 //                  exchange of the tile max orders it) rounded to bf16, the product's operand
-//                  type (as flash-attention kernels do: a second product for the rounding error, as the
-//                  decode path carries, would double the output product, which bounds this path);
+//                  type (as flash-attention kernels do; a second product for the rounding error, as the
+//                  decode path carries, would double the output product's tensor-core time);
 //   O += P V       128 x D fp32 in tensor memory, P the A operand from tensor memory, V a V slot's rows
 //                  as an MN-major operand from shared memory; O is rescaled in place (read, scaled, written
 //                  back) only when a row's max passes m by the slack, which after a segment's first tiles is
@@ -1089,8 +1089,8 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
 // The MMA warp issues each product as soon as its inputs are ready (see tc5_mma_warp), so the tensor core
 // computes the next scores and the current output product while the softmax warps work on a tile.
 // Ordering: scores -> sfull[j % 2] (tcgen05.commit); scores read -> sfree[j % 2] (8 warps; it frees the
-// unit's K slot and meta); weights written -> pfull[j % 2] (8 warps); output product done -> odone[j % 2] and the
-// V slot's vempty (commits); a segment's Q tile written -> qready (8 warps).  A score buffer takes S(k)
+// unit's K slot and meta); weights written -> pfull[j % 2] (8 warps); output product done -> odone[j % 2]
+// and the V slot's vempty (commits); a segment's Q tile written -> qready (8 warps).  A score buffer takes S(k)
 // once the output product of unit k - 2, which read its weights there, is done.  No barrier can run two
 // phases ahead of its waiter: each one's next phase needs the waiter's own next step.
 struct Tc5Smem {
@@ -1288,8 +1288,10 @@ __device__ void tc5_merge(const DecodeParams &p, const long long *bound, int sf,
 #pragma unroll
     for (int k = 0; k < C / 8; ++k)
         *reinterpret_cast<uint4 *>(o + 8 * k) =
-            make_uint4(pack_bf16x2(a[8 * k] * inv, a[8 * k + 1] * inv), pack_bf16x2(a[8 * k + 2] * inv, a[8 * k + 3] * inv),
-                       pack_bf16x2(a[8 * k + 4] * inv, a[8 * k + 5] * inv), pack_bf16x2(a[8 * k + 6] * inv, a[8 * k + 7] * inv));
+            make_uint4(pack_bf16x2(a[8 * k] * inv, a[8 * k + 1] * inv),
+                       pack_bf16x2(a[8 * k + 2] * inv, a[8 * k + 3] * inv),
+                       pack_bf16x2(a[8 * k + 4] * inv, a[8 * k + 5] * inv),
+                       pack_bf16x2(a[8 * k + 6] * inv, a[8 * k + 7] * inv));
 }
 
 static_assert(team_warps(16) * 16 == 128, "a tensor-memory piece tile is 8 slots of 16 rows");
@@ -1512,8 +1514,9 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
                     tmem_ld32(tlane + kTc5OCol + cc * 32, r);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        dst[(cc * 8 + k) * 128] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                                              __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+                        dst[(cc * 8 + k) * 128] =
+                            make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                        __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
                 }
                 if (half == 0) reinterpret_cast<float2 *>(p.ws_ml)[tile * 128 + row] = make_float2(mrun, L);
                 // the whole piece is written before it is counted in: every thread's stores precede the
