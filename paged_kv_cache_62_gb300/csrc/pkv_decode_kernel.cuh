@@ -80,6 +80,8 @@ constexpr int32_t kHintMagic = 0x6869;
 // batch, 64 KiB units: 3 -> 94.6 us, 6 -> 93.1, 8 -> 92.6, 12 -> 92.0 per call; none: 96.5; 16, the whole
 // 256-token block, about 0.3 us less than 12 graph-replayed).
 constexpr int kHintUnits = 16;
+// Context lengths a set-up thread loads at once in the unit scan.
+constexpr int kScanBatch = 16;
 
 // Consumer warps per CTA and tokens each takes from a stage (a stage holds
 // team_warps * warp_tokens token rows of head_dim: 64 KiB for head_dim 128).
@@ -369,22 +371,38 @@ static __device__ void unit_prefix_scan(const DecodeParams &p, int32_t *scan, in
 {
     const int tid = threadIdx.x;
     const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
+    // every entry's unit count into scan[]: the lengths kScanBatch at a time a thread, all in flight
+    // together (one memory round trip a batch, where a loop over a thread's own entries would wait for
+    // each in turn), consecutive threads on consecutive entries
+    for (int i0 = 0; i0 < p.B; i0 += kScanBatch * nt) {
+        int32_t len[kScanBatch];
+#pragma unroll
+        for (int k = 0; k < kScanBatch; ++k) {
+            const int i = i0 + k * nt + tid;
+            len[k] = i < p.B ? __ldg(p.context_lens + i) : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < kScanBatch; ++k) {
+            const int i = i0 + k * nt + tid;
+            if (i >= p.B) break;
+            int32_t n = 0;
+            // several queries of a sequence sharing a stream need at least one key each (the row
+            // arrays of a chunked call are built that way; a same-n call can break it)
+            if (len[k] < 0 || len[k] > p.len_limit || (!p.row_cnt && p.qn > 1 && len[k] < p.qn)) {
+                if (blockIdx.x == 0) flag_error(p.err, PKV_ERR_CONTEXT_RANGE);
+            } else {
+                n = (len[k] + p.toks - 1) / p.toks;
+            }
+            scan[i] = n;
+        }
+    }
+    setup_sync(nt);
+    // the exclusive prefix: thread tid sums its run of entries [lo, hi), the runs are scanned over the
+    // set-up threads, and each thread writes its run's offsets
     const int per = (p.B + nt - 1) / nt;
     const int lo = min(p.B, tid * per), hi = min(p.B, lo + per);
     int32_t sum = 0;
-    for (int i = lo; i < hi; ++i) {
-        const int32_t len = __ldg(p.context_lens + i);
-        int32_t n = 0;
-        // several queries of a sequence sharing a stream need at least one key each (the row
-        // arrays of a chunked call are built that way; a same-n call can break it)
-        if (len < 0 || len > p.len_limit || (!p.row_cnt && p.qn > 1 && len < p.qn)) {
-            if (blockIdx.x == 0) flag_error(p.err, PKV_ERR_CONTEXT_RANGE);
-        } else {
-            n = (len + p.toks - 1) / p.toks;
-        }
-        scan[i] = n;
-        sum += n;
-    }
+    for (int i = lo; i < hi; ++i) sum += scan[i];
     int32_t incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1343,6 +1361,51 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
         other = slot[(1 - half) * 128 + row];
         return true;
     };
+    // A segment's Q tile into tensor memory (tile segs % 2: the tile before it was last read by the
+    // segment before the previous one's scores, all of which were read back): this thread's 64 dims of
+    // its row, zeros for rows that are not queries of the entry.
+    auto write_q = [&](const UnitMeta &sg) {
+        uint32_t w[32];
+        if (qi < sg.cnt) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                p.q + ((long long)(sg.b + qi) * p.Hq + (long long)sg.g * p.gq + (row % p.gq)) * D + half * DH);
+#pragma unroll
+            for (int k = 0; k < DH / 8; ++k) {
+                const uint4 v = __ldg(src + k);
+                w[4 * k] = v.x;
+                w[4 * k + 1] = v.y;
+                w[4 * k + 2] = v.z;
+                w[4 * k + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < DH / 2; ++k) w[k] = 0u;
+        }
+        const uint32_t qa = tlane + kTc5QCol + (segs & 1u) * 64u + uint32_t(half * DH / 2);
+        if constexpr (DH / 2 == 32) {
+            tmem_st32(qa, w);
+        } else {
+            uint32_t w16[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) w16[k] = w[k];
+            tmem_st16(qa, w16);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(m.qready);
+        ++segs;
+    };
+    // the next segment's Q tile is already written: the first one before the loop, each later one at the
+    // end of the segment before it
+    bool q_early = false;
+    if (wait(&m.full[0], 0u)) {
+        const UnitMeta f0 = m.metas[0];
+        if (f0.b >= 0 && (f0.flags & kFirst)) {
+            write_q(f0);
+            q_early = true;
+        }
+    }
     for (;;) {
         if (!wait(&m.full[s], ph)) break;
         const UnitMeta mt = m.metas[s];
@@ -1355,39 +1418,8 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
             mrun = -INFINITY;
             lrun = 0.f;
             u_first = mt.u;
-            // the segment's Q tile into tensor memory (tile segs % 2: the tile before it was last read by
-            // the previous segment's scores, all of which were read back): this thread's 64 dims of its
-            // row, zeros for rows that are not queries of the entry
-            uint32_t w[32];
-            if (row_ok) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    p.q + ((long long)(mt.b + qi) * p.Hq + (long long)kvh * p.gq + (row % p.gq)) * D + half * DH);
-#pragma unroll
-                for (int k = 0; k < DH / 8; ++k) {
-                    const uint4 v = __ldg(src + k);
-                    w[4 * k] = v.x;
-                    w[4 * k + 1] = v.y;
-                    w[4 * k + 2] = v.z;
-                    w[4 * k + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < DH / 2; ++k) w[k] = 0u;
-            }
-            const uint32_t qa = tlane + kTc5QCol + (segs & 1u) * 64u + uint32_t(half * DH / 2);
-            if constexpr (DH / 2 == 32) {
-                tmem_st32(qa, w);
-            } else {
-                uint32_t w16[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) w16[k] = w[k];
-                tmem_st16(qa, w16);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(m.qready);
-            ++segs;
+            if (!q_early) write_q(mt);
+            q_early = false;
         }
         const int tok0 = mt.u * kTc5Keys;
         const int valid = min(kTc5Keys, mt.L - tok0);
@@ -1477,6 +1509,18 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
         if (lane == 0) mbar_arrive(&m.pfull[j & 1u]);
 
         if (mt.flags & kLast) {  // the segment's part in this slice ends: O once its last product is done
+            // First the next segment's Q tile, so that its first scores run during this epilogue: the
+            // next unit's meta once its K copy has landed (the producer issues it without waiting for
+            // anything past this unit's weights)
+            {
+                const int sn = s + 1 == p.nst ? 0 : s + 1;
+                if (!wait(&m.full[sn], s + 1 == p.nst ? ph ^ 1u : ph)) break;
+                const UnitMeta nx = m.metas[sn];
+                if (nx.b >= 0 && (nx.flags & kFirst)) {
+                    write_q(nx);
+                    q_early = true;
+                }
+            }
             if (!wait(&m.odone[j & 1u], (j >> 1) & 1u)) break;
             tc_fence_after();
             float lother;
@@ -1689,14 +1733,24 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
         unit_prefix_scan(p, scan, reinterpret_cast<int32_t *>(smem), nset);
         const long long T = (long long)p.nhg * scan[p.B];
         // Entries without units (L == 0, or a rejected length) get zeros in their query rows; CTAs
-        // share the job.
-        for (int b = blockIdx.x; b < p.B; b += gridDim.x)
-            if (scan[b + 1] == scan[b]) {
-                if (p.slot_out && threadIdx.x == 0) p.slot_out[b] = -1;  // fused store: nothing stored
-                const int rows = p.row_cnt ? __ldg(p.row_cnt + b) : p.qn;
-                uint4 *o = reinterpret_cast<uint4 *>(p.out + int64_t(b) * p.qstride * p.Hq * D);
-                for (int i = threadIdx.x; i < rows * p.Hq * D / 8; i += nset) o[i] = make_uint4(0u, 0u, 0u, 0u);
+        // share the job (CTA c takes entries c, c + grid, ...), a set-up thread checks one of them at a
+        // time (the row counts of a batch of them are loaded together), and a warp zeroes the rows of
+        // its threads' entries together.
+        for (long long k0 = 0; blockIdx.x + k0 * gridDim.x < p.B; k0 += nset) {
+            const long long b = blockIdx.x + (k0 + threadIdx.x) * gridDim.x;
+            int rows = 0;
+            if (b < p.B && scan[b + 1] == scan[b]) {
+                if (p.slot_out) p.slot_out[b] = -1;  // fused store: nothing stored
+                rows = p.row_cnt ? __ldg(p.row_cnt + b) : p.qn;
             }
+            for (unsigned zm = __ballot_sync(kFull, rows > 0); zm; zm &= zm - 1) {
+                const int l = __ffs(zm) - 1;
+                const long long bz = __shfl_sync(kFull, b, l);
+                const int nz = __shfl_sync(kFull, rows, l) * p.Hq * D / 8;
+                uint4 *o = reinterpret_cast<uint4 *>(p.out + bz * p.qstride * p.Hq * D);
+                for (int i = lane; i < nz; i += 32) o[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
         if (p.per_segment) {
             // slice i = segment (entry i / nhg, group i % nhg), whole: the grid has one CTA per segment
             for (int i = threadIdx.x; i <= nslots; i += nset) {
@@ -1768,6 +1822,19 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
                     nxt_e = __ldg(p.block_tables + (long long)trow * p.max_blocks + blk);
                 }
             };
+            // TC5: the query rows of segment w into L2 (the softmax warps load them into tensor memory at
+            // the end of the segment before): 8 qn queries x gq heads of kv head g, D values each, as
+            // 128-byte lines, lane-strided (plain prefetches: they do not queue behind the copies)
+            auto prefetch_q = [&](const Walker &w) {
+                const int nq = min(team_warps(G) * p.qn, p.B - w.b);
+                const int lines = p.gq * D * 2 / 128;
+                for (int i = lane; i < nq * lines; i += 32) {
+                    const int r = i / lines, c = i - r * lines;
+                    prefetch_l2(reinterpret_cast<const uint8_t *>(
+                                    p.q + ((long long)(w.b + r) * p.Hq + (long long)w.g * p.gq) * D) +
+                                c * 128);
+                }
+            };
             if (nunits > 0) {
                 prefetch_batch(0);
                 cur_e = nxt_e;
@@ -1803,13 +1870,9 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
                         break;
                     }
                     if constexpr (TC5) {
-                        // the consumers load the entry's Q tile themselves (into tensor memory); warm L2 with
-                        // its rows: 8 qn queries x gq heads of kv head g, D values each
-                        const int nq = team_warps(G) * p.qn;
-                        for (int i = lane; i < nq; i += 32)
-                            if (iw.b + i < p.B)
-                                bulk_prefetch_l2(p.q + ((long long)(iw.b + i) * p.Hq + (long long)iw.g * p.gq) * D,
-                                                 uint32_t(p.gq * D * 2));
+                        // the consumers load the entry's Q tile themselves (into tensor memory); its rows
+                        // were warmed in L2 when the segment before it was issued (here: a slice's first)
+                        if (k == 0) prefetch_q(iw);
                     } else if (p.qn == 1 && !QS) {  // the group's G * hg query rows are contiguous
                         const uint32_t qb = uint32_t(p.hg * G * D * 2);
                         if (lane == 0) {
@@ -1908,6 +1971,8 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
                         iw = walker_locate(scan, p.B, p.nhg, lo);  // from the slice's last unit to its first
                     else
                         walker_advance(iw, scan, p.nhg, p.B);
+                    if constexpr (TC5)
+                        if (flags & kLast) prefetch_q(iw);  // the next segment's query rows
                 }
                 if (k == 0 && nboxes > 32) prefetch_batch(32);  // after the first copies are on their way
             }

@@ -149,11 +149,10 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
-// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned global address.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+// L2 prefetch of the 128-byte line holding a global address (a plain memory instruction, not a copy).
+__device__ __forceinline__ void prefetch_l2(const void *src)
 {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
-                 : "memory");
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(src)));
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
