@@ -233,9 +233,9 @@ __host__ __device__ inline CtaLayout cta_layout(int D, int G, int es, int hg, in
     l.off_bar = o;
     // full / empty per stage, q full / empty x2, combine full / free; tc5: scores full x2, scores read x2,
     // weights full x2, output product done x2, drain, a row's two halves met (one per lane quarter) x4,
-    // all softmax warps met, a Q tile written, and full / empty per V slot (the stages' pair then covers
-    // the K slots)
-    o += uint32_t(2 * nst + 6 + (tc5 ? 15 + 2 * kTc5VSlots : 0)) * 8;
+    // all softmax warps met, a Q tile written, full / empty per V slot (the stages' pair then covers the
+    // K slots), and per K slot its meta written
+    o += uint32_t(2 * nst + 6 + (tc5 ? 15 + 2 * kTc5VSlots + nst : 0)) * 8;
     l.off_bound = align_up(o, 16);
     o = l.off_bound + (kMaxSlots + 1) * 8;
     l.off_wts = o;
@@ -1115,6 +1115,7 @@ struct Tc5Smem {
     const UnitMeta *metas;
     // full / empty: a K slot (and its unit's meta); vfull / vempty: a V slot
     uint64_t *full, *empty, *vfull, *vempty, *qready, *sfull, *sfree, *pfull, *odone, *drain, *pair, *team;
+    uint64_t *mready;  // [nst] a K slot's meta written (its copy may still be on the way)
     uint8_t *vbase;                  // V slot 0
     uint32_t stage_addr, v_addr;     // shared addresses of K slot 0 and V slot 0
 };
@@ -1399,7 +1400,7 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
     // the next segment's Q tile is already written: the first one before the loop, each later one at the
     // end of the segment before it
     bool q_early = false;
-    if (wait(&m.full[0], 0u)) {
+    if (wait(&m.mready[0], 0u)) {
         const UnitMeta f0 = m.metas[0];
         if (f0.b >= 0 && (f0.flags & kFirst)) {
             write_q(f0);
@@ -1510,11 +1511,11 @@ __device__ void tc5_softmax_warps(const DecodeParams &p, const CtaLayout &lay, c
 
         if (mt.flags & kLast) {  // the segment's part in this slice ends: O once its last product is done
             // First the next segment's Q tile, so that its first scores run during this epilogue: the
-            // next unit's meta once its K copy has landed (the producer issues it without waiting for
-            // anything past this unit's weights)
+            // next unit's meta, written before its K copy is issued (the producer issues it without
+            // waiting for anything past this unit's weights)
             {
                 const int sn = s + 1 == p.nst ? 0 : s + 1;
-                if (!wait(&m.full[sn], s + 1 == p.nst ? ph ^ 1u : ph)) break;
+                if (!wait(&m.mready[sn], s + 1 == p.nst ? ph ^ 1u : ph)) break;
                 const UnitMeta nx = m.metas[sn];
                 if (nx.b >= 0 && (nx.flags & kFirst)) {
                     write_q(nx);
@@ -1638,6 +1639,7 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
     uint64_t *tc5_bar = cfree + 1;  // TC5: sfull[2], sfree[2], pfull[2], odone[2], drain, pair[4], team, qready
     uint64_t *vfull = tc5_bar + 15;        // TC5: [kTc5VSlots] a V slot loaded
     uint64_t *vempty = vfull + kTc5VSlots;  // TC5: [kTc5VSlots] a V slot released
+    uint64_t *mready = vempty + kTc5VSlots;  // TC5: [nst] a K slot's meta written (before its copy lands)
 
     if (threadIdx.x == 32 * p.cons) {  // none of this reads what the previous kernel writes
         prefetch_tensormap(&kmap);
@@ -1669,6 +1671,7 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
                 mbar_init(&vfull[i], 1);
                 mbar_init(&vempty[i], 1);
             }
+            for (int i = 0; i < p.nst; ++i) mbar_init(&mready[i], 1);
         }
         fence_barrier_init();
     }
@@ -1931,6 +1934,7 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
                     mt.slice = slice;
                     mt.cnt = cnt;
                     mt.newrow = newrow;
+                    if constexpr (TC5) mbar_arrive(&mready[s]);  // the meta, for a look ahead
                     // TC5: full[s] counts the K half only; the V half has barriers of its own
                     mbar_arrive_expect_tx(&full[s], (TC5 ? 1u : 2u) * nrows * box_bytes);
                 }
@@ -1982,6 +1986,7 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
             if (kk < uint32_t(p.nst) || mbar_wait_bounded(&empty[rs], rph ^ 1u)) {
                 if (lane == 0) {
                     metas[rs].b = -1;
+                    if constexpr (TC5) mbar_arrive(&mready[rs]);
                     mbar_arrive(&full[rs]);
                 }
                 ++kk;
@@ -2020,6 +2025,7 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
         tm.empty = empty;
         tm.vfull = vfull;
         tm.vempty = vempty;
+        tm.mready = mready;
         tm.sfull = tc5_bar;
         tm.sfree = tc5_bar + 2;
         tm.pfull = tc5_bar + 4;
