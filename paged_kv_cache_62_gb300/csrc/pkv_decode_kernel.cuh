@@ -371,20 +371,18 @@ static __device__ void unit_prefix_scan(const DecodeParams &p, int32_t *scan, in
 {
     const int tid = threadIdx.x;
     const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
-    // every entry's unit count into scan[]: the lengths kScanBatch at a time a thread, all in flight
-    // together (one memory round trip a batch, where a loop over a thread's own entries would wait for
-    // each in turn), consecutive threads on consecutive entries
-    for (int i0 = 0; i0 < p.B; i0 += kScanBatch * nt) {
+    // thread tid counts the units of its run of entries [lo, hi), the lengths loaded kScanBatch at a
+    // time (all in flight together: one memory round trip a batch, not one an entry)
+    const int per = (p.B + nt - 1) / nt;
+    const int lo = min(p.B, tid * per), hi = min(p.B, lo + per);
+    int32_t sum = 0;
+    for (int i0 = lo; i0 < hi; i0 += kScanBatch) {
         int32_t len[kScanBatch];
 #pragma unroll
-        for (int k = 0; k < kScanBatch; ++k) {
-            const int i = i0 + k * nt + tid;
-            len[k] = i < p.B ? __ldg(p.context_lens + i) : 0;
-        }
+        for (int k = 0; k < kScanBatch; ++k) len[k] = i0 + k < hi ? __ldg(p.context_lens + i0 + k) : 0;
 #pragma unroll
         for (int k = 0; k < kScanBatch; ++k) {
-            const int i = i0 + k * nt + tid;
-            if (i >= p.B) break;
+            if (i0 + k >= hi) break;
             int32_t n = 0;
             // several queries of a sequence sharing a stream need at least one key each (the row
             // arrays of a chunked call are built that way; a same-n call can break it)
@@ -393,16 +391,10 @@ static __device__ void unit_prefix_scan(const DecodeParams &p, int32_t *scan, in
             } else {
                 n = (len[k] + p.toks - 1) / p.toks;
             }
-            scan[i] = n;
+            scan[i0 + k] = n;
+            sum += n;
         }
     }
-    setup_sync(nt);
-    // the exclusive prefix: thread tid sums its run of entries [lo, hi), the runs are scanned over the
-    // set-up threads, and each thread writes its run's offsets
-    const int per = (p.B + nt - 1) / nt;
-    const int lo = min(p.B, tid * per), hi = min(p.B, lo + per);
-    int32_t sum = 0;
-    for (int i = lo; i < hi; ++i) sum += scan[i];
     int32_t incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1733,18 +1725,20 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
         }
     } else {
         const BalanceIn bal_in = load_balance(p, adaptive, nslots, nset);
+        // the query count of this thread's first entry to check for zeros below, loaded with the rest
+        const long long b_first = blockIdx.x + (long long)threadIdx.x * gridDim.x;
+        const int rows_first = p.row_cnt && b_first < p.B ? __ldg(p.row_cnt + b_first) : p.qn;
         unit_prefix_scan(p, scan, reinterpret_cast<int32_t *>(smem), nset);
         const long long T = (long long)p.nhg * scan[p.B];
         // Entries without units (L == 0, or a rejected length) get zeros in their query rows; CTAs
         // share the job (CTA c takes entries c, c + grid, ...), a set-up thread checks one of them at a
-        // time (the row counts of a batch of them are loaded together), and a warp zeroes the rows of
-        // its threads' entries together.
+        // time, and a warp zeroes the rows of its threads' entries together.
         for (long long k0 = 0; blockIdx.x + k0 * gridDim.x < p.B; k0 += nset) {
             const long long b = blockIdx.x + (k0 + threadIdx.x) * gridDim.x;
             int rows = 0;
             if (b < p.B && scan[b + 1] == scan[b]) {
                 if (p.slot_out) p.slot_out[b] = -1;  // fused store: nothing stored
-                rows = p.row_cnt ? __ldg(p.row_cnt + b) : p.qn;
+                rows = k0 == 0 ? rows_first : (p.row_cnt ? __ldg(p.row_cnt + b) : p.qn);
             }
             for (unsigned zm = __ballot_sync(kFull, rows > 0); zm; zm &= zm - 1) {
                 const int l = __ffs(zm) - 1;
