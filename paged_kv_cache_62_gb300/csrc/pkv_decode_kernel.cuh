@@ -1100,9 +1100,13 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, const long l
 // computes the next scores and the current output product while the softmax warps work on a tile.
 // Ordering: scores -> sfull[j % 2] (tcgen05.commit); scores read -> sfree[j % 2] (8 warps; it frees the
 // unit's K slot and meta); weights written -> pfull[j % 2] (8 warps); output product done -> odone[j % 2]
-// and the V slot's vempty (commits); a segment's Q tile written -> qready (8 warps).  A score buffer takes S(k)
-// once the output product of unit k - 2, which read its weights there, is done.  No barrier can run two
-// phases ahead of its waiter: each one's next phase needs the waiter's own next step.
+// and the V slot's vempty (commits); a segment's Q tile written -> qready (8 warps); a unit's meta written
+// -> mready[slot] (the producer, before the unit's copy is issued).  A score buffer takes S(k) once the
+// output product of unit k - 2, which read its weights there, is done.  A segment's last unit writes the
+// next segment's Q tile (into the other Q tile, from the next unit's meta) right after its weights and
+// before its epilogue, so the next segment's first scores run while the epilogue waits for the last output
+// product and writes O out.  No barrier can run two phases ahead of its waiter: each one's next phase
+// needs the waiter's own next step.
 struct Tc5Smem {
     const UnitMeta *metas;
     // full / empty: a K slot (and its unit's meta); vfull / vempty: a V slot
