@@ -160,6 +160,8 @@ struct DecodeParams {
     int32_t nst, cons, lg_nbox;  // ring stages, consumer warps (hg * sub), log2(nbox)
     int32_t num_workers;         // > 0: fixed split over about num_workers / consumers CTAs; 0: adaptive
     int32_t per_segment;         // fixed split with one slice per (entry, head group): no split-K pieces
+    int32_t qslots;              // Q row buffers: 2 (the next segment's rows load during this one), or 1
+                                 // where that buys the ring another stage
     float scale_log2;            // scale * log2(e)
     const float *k_scale, *v_scale;  // E4M3 caches: per-kv-head scales (unused for bf16 caches)
     const int32_t *row_seq;          // several query rows per sequence: row -> the sequence whose table it
@@ -204,12 +206,21 @@ __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x
 // multiple of 4, so every block (and its float4 rows) is 16-byte aligned.
 __host__ __device__ inline int comb_stride(int D, int G) { return int(align_up(uint32_t(G * (D + 2)), 4)); }
 
+// Whether a kernel variant may run with one Q row buffer: regular bf16 CTAs of 8 virtual heads, where
+// at head_dim 128 and 8 kv heads a CTA the second buffer (32 KiB) costs the ring its third stage.  The
+// other variants keep two, a fixed count that keeps their code as it was (fewer heads fit three stages
+// beside two buffers; the 16-row tiles miss a third stage either way).
+__host__ __device__ constexpr bool one_q_buffer_ok(int G, bool fp8, bool qs, bool tc5)
+{
+    return G == 8 && !fp8 && !qs && !tc5;
+}
+
 // es: bytes per cached element (2 for bf16, 1 for E4M3); qs: query-split
 // CTA (all sub warps of a kv head on the same tokens, each with its own G
 // virtual heads); tc5: its tensor-memory variant (Q slots hold the 128-row
 // tile as 128-byte-swizzled 64-dim slabs).
 __host__ __device__ inline CtaLayout cta_layout(int D, int G, int es, int hg, int sub, int nst, int B,
-                                                bool qs = false, bool tc5 = false)
+                                                bool qs = false, bool tc5 = false, int qslots = 2)
 {
     CtaLayout l;
     const int toks = warp_tokens(G, es == 1, qs, tc5) * (qs ? 1 : sub);
@@ -225,7 +236,7 @@ __host__ __device__ inline CtaLayout cta_layout(int D, int G, int es, int hg, in
     l.off_v = o;
     if (tc5) o += uint32_t(kTc5VSlots) * align_up(l.kv_bytes, 1024);
     l.off_q = o;
-    o += 2 * l.q_bytes;
+    o += uint32_t(qslots) * l.q_bytes;
     l.off_comb = o;
     o += l.comb_bytes;
     l.off_meta = o;
@@ -1612,7 +1623,8 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
     static_assert(!TC5 || (QS && !FP8 && G == 16 && (D == 64 || D == 128)), "tensor-memory CTAs: bf16 query-split");
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int ES = FP8 ? 1 : 2;  // bytes per cached element
-    const CtaLayout lay = cta_layout(D, G, ES, p.hg, p.sub, p.nst, p.B, QS, TC5);
+    const int qslots = one_q_buffer_ok(G, FP8, QS, TC5) ? p.qslots : 2;
+    const CtaLayout lay = cta_layout(D, G, ES, p.hg, p.sub, p.nst, p.B, QS, TC5, qslots);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     uint8_t *stage0 = smem;
@@ -1864,8 +1876,8 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
                                   ((x == hi - 1 || iw.u == iw.n - 1) ? kLast : 0) |
                                   (k == nunits - 1 ? kSliceEnd : 0);
                 if (flags & kFirst) {  // q rows of this (b, group) for the consumers
-                    const int qs = int(segs & 1u);
-                    const uint32_t quse = segs >> 1;
+                    const int qs = int(segs & uint32_t(qslots - 1));
+                    const uint32_t quse = segs >> (qslots - 1);  // earlier uses of the buffer
                     if (!TC5 && quse > 0 && !mbar_wait_bounded(&qempty[qs], (quse - 1) & 1u)) {
                         dead = true;
                         break;
@@ -2102,13 +2114,14 @@ __global__ void __launch_bounds__(TC5 ? (kTc5Consumers + 1) * 32 : (team_warps(G
         const UnitMeta mt = metas[s];
         if (mt.b < 0) break;
         if (mt.flags & kFirst) {
-            const int qs = int(segs & 1u);
+            const int qs = int(segs & uint32_t(qslots - 1));
+            const uint32_t quse = segs >> (qslots - 1);
             ksc = p.scale_log2;  // E4M3 caches: the kv head's K scale joins the score scale
             if constexpr (FP8) {
                 ksc *= __ldg(p.k_scale + mt.g * p.hg + h);
                 vsc = __ldg(p.v_scale + mt.g * p.hg + h);
             }
-            if (!mbar_wait_bounded(&qfull[qs], (segs >> 1) & 1u)) {
+            if (!mbar_wait_bounded(&qfull[qs], quse & 1u)) {
                 if (lane == 0) flag_error(p.err, PKV_ERR_WAIT_TIMEOUT);
                 break;
             }
@@ -2489,11 +2502,22 @@ template <int D, int G, bool FP8, bool QS, bool TC5 = false>
 pkv_status launch_decode(LaunchArgs &a)
 {
     DecodeParams &p = a.p;
-    // ring depth: as many stages (up to kMaxStages) as the shared memory holds
-    int nst = kMaxStages;
+    // ring depth: as many stages (up to kMaxStages) as the shared memory holds, beside two Q row
+    // buffers, or beside one where that fits more stages (a segment's Q rows go into registers at its
+    // first tile, so one buffer is free again long before the next segment needs it)
     constexpr int ES = FP8 ? 1 : 2;
-    while (nst > 2 && cta_layout(D, G, ES, p.hg, p.sub, nst, p.B, QS, TC5).total > uint32_t(a.max_smem)) --nst;
-    const CtaLayout lay = cta_layout(D, G, ES, p.hg, p.sub, nst, p.B, QS, TC5);
+    auto depth = [&](int qslots) {
+        int n = kMaxStages;
+        while (n > 2 && cta_layout(D, G, ES, p.hg, p.sub, n, p.B, QS, TC5, qslots).total > uint32_t(a.max_smem)) --n;
+        return n;
+    };
+    int nst = depth(2);
+    p.qslots = 2;
+    if (one_q_buffer_ok(G, FP8, QS, TC5) && depth(1) > nst) {
+        nst = depth(1);
+        p.qslots = 1;
+    }
+    const CtaLayout lay = cta_layout(D, G, ES, p.hg, p.sub, nst, p.B, QS, TC5, p.qslots);
     if (lay.total > uint32_t(a.max_smem)) return PKV_EUNSUPPORTED;
     p.nst = nst;
 
